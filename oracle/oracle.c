@@ -1,0 +1,396 @@
+/*
+ * Oracle for exact scaled dot-product attention, forward and backward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously correct
+ * CPU definition that the CUDA path is checked against.  Only the test suite,
+ * the package smoke check and the benchmark's CPU-baseline leg may load it.
+ * It shares no code, header, table or helper with the CUDA library, and the
+ * library never calls it.
+ *
+ * Everything is IEEE double.  Inputs of narrower types are widened exactly by
+ * the caller before they reach this file.
+ *
+ * What is computed, and where it is defined:
+ *
+ *  - Scores and output.  TIGA-lang, "注意力与稠密关系" (attention examples),
+ *    section "全量注意力，无掩码" (full attention, no mask), its display
+ *    equation:  s_hij = <k_hj, q_hi> * scale,  out_hi = sum_j softmax_j(s) v_hj.
+ *    The pages use scale = D^-1/2; here the scale is an argument.
+ *
+ *  - Relations.  Same page, section "因果稠密关系" (causal dense relation):
+ *    query i admits key j iff j <= i.  Section "用图组合表达 varlen 因果注意力"
+ *    (varlen causal attention by graph composition): a key is admitted only
+ *    inside the query's own sequence, seq(i) = b <=> cu_b <= i < cu_{b+1}.
+ *    Positions i, j below are offsets inside the sequence.
+ *
+ *  - Composed two-pass softmax.  OCANNL "Module Ir.Online_softmax", opening
+ *    paragraph: a max-reduction, then a sum of exponentials shifted by that
+ *    max, then the reduction against v.  The oracle is exactly that composed
+ *    form (probabilities normalised first, then summed against v); it is NOT
+ *    the online / block recurrence the GPU path uses.
+ *
+ *  - Row log-sum-exp.  The final (m, l) of a row, persisted for the backward
+ *    (OCANNL page, fourth bullet: "the final (m, l) land in their nodes"),
+ *    reported as lse = m + ln l, natural log of the sum over admitted keys of
+ *    exp(scaled score).
+ *
+ *  - Backward.  The textbook softmax Jacobian, written out:
+ *        P_ij  = exp(s_ij - m_i) / l_i
+ *        dP_ij = <dO_i, v_j>
+ *        c_i   = sum_j P_ij dP_ij
+ *        dS_ij = P_ij (dP_ij - c_i)
+ *        dq_i = scale sum_j dS_ij k_j,  dk_j = scale sum_i dS_ij q_i,
+ *        dv_j = sum_i P_ij dO_i.
+ *    c_i is computed from P and dP, deliberately not from the shortcut
+ *    D_i = <dO_i, O_i> that the OCANNL page's third bullet uses; the tests
+ *    check that identity separately.
+ *
+ * Readings where the pages are silent (also listed in the design notes):
+ *  - A row that admits no key (only possible for an empty key segment under
+ *    the full relation) gets O = 0 and lse = -inf.
+ *  - Causal is defined only for a sequence whose query and key lengths are
+ *    equal; other inputs return -1.
+ *
+ * Layout: q, o, dq, dO are (T_q, H, D) row-major; k, v, dk, dv are (T_k, H, D);
+ * lse is (H, T_q).  cu_q / cu_k hold n_seq + 1 cumulative offsets starting at 0.
+ * All arrays are host memory owned by the caller.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_ABI_VERSION 1
+
+int oracle_abi_version(void) { return ORACLE_ABI_VERSION; }
+
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Segment holding global token index t, by linear scan over the offsets. */
+static int segment_of(int n_seq, const int32_t *cu, int64_t t)
+{
+    for (int b = 0; b < n_seq; ++b)
+        if (t >= cu[b] && t < cu[b + 1]) return b;
+    return -1;
+}
+
+static int check_segments(int n_seq, const int32_t *cu_q, const int32_t *cu_k, int causal)
+{
+    if (n_seq < 1 || !cu_q || !cu_k) return -1;
+    if (cu_q[0] != 0 || cu_k[0] != 0) return -1;
+    for (int b = 0; b < n_seq; ++b) {
+        if (cu_q[b + 1] < cu_q[b] || cu_k[b + 1] < cu_k[b]) return -1;
+        if (causal && (cu_q[b + 1] - cu_q[b]) != (cu_k[b + 1] - cu_k[b])) return -1;
+    }
+    return 0;
+}
+
+/* Number of keys that query offset i of a segment with Lk keys admits. */
+static int admitted(int i, int Lk, int causal)
+{
+    if (!causal) return Lk;
+    return i + 1 < Lk ? i + 1 : Lk;
+}
+
+static double dot(const double *a, const double *b, int D)
+{
+    double acc = 0.0;
+    for (int d = 0; d < D; ++d) acc += a[d] * b[d];
+    return acc;
+}
+
+/*
+ * Row statistics of one query row: scores s_j for its nj admitted keys
+ * (written to s[]), their max m and the shifted sum l = sum_j exp(s_j - m).
+ */
+static void row_scores(const double *qi, const double *k0, int64_t ldk, int nj, int D,
+                       double scale, double *s, double *m_out, double *l_out)
+{
+    double m = -INFINITY;
+    for (int j = 0; j < nj; ++j) {
+        s[j] = scale * dot(qi, k0 + (int64_t)j * ldk, D);
+        if (s[j] > m) m = s[j];
+    }
+    double l = 0.0;
+    for (int j = 0; j < nj; ++j) l += exp(s[j] - m);
+    *m_out = m;
+    *l_out = l;
+}
+
+/* Forward for one (query token, head): O row and lse, by the composed form. */
+static void fwd_one(int n_seq, const int32_t *cu_q, const int32_t *cu_k, int H, int D,
+                    const double *q, const double *k, const double *v, double scale,
+                    int causal, int64_t t, int h, double *o_row, double *lse_out, double *s)
+{
+    const int b = segment_of(n_seq, cu_q, t);
+    const int i = (int)(t - cu_q[b]);
+    const int Lk = cu_k[b + 1] - cu_k[b];
+    const int nj = admitted(i, Lk, causal);
+    const int64_t ld = (int64_t)H * D;
+    const double *qi = q + t * ld + (int64_t)h * D;
+    const double *k0 = k + (int64_t)cu_k[b] * ld + (int64_t)h * D;
+    const double *v0 = v + (int64_t)cu_k[b] * ld + (int64_t)h * D;
+
+    for (int d = 0; d < D; ++d) o_row[d] = 0.0;
+    if (nj == 0) {
+        *lse_out = -INFINITY;
+        return;
+    }
+    double m, l;
+    row_scores(qi, k0, ld, nj, D, scale, s, &m, &l);
+    for (int j = 0; j < nj; ++j) {
+        const double p = exp(s[j] - m) / l; /* normalised probability first */
+        const double *vj = v0 + (int64_t)j * ld;
+        for (int d = 0; d < D; ++d) o_row[d] += p * vj[d];
+    }
+    *lse_out = m + log(l);
+}
+
+static int max_len(int n_seq, const int32_t *cu)
+{
+    int mx = 0;
+    for (int b = 0; b < n_seq; ++b)
+        if (cu[b + 1] - cu[b] > mx) mx = cu[b + 1] - cu[b];
+    return mx;
+}
+
+static void set_threads(int n_threads)
+{
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+}
+
+/*
+ * Full forward: every (query token, head).  o is (T_q, H, D), lse is (H, T_q).
+ * Returns 0, or -1 on inconsistent segments.
+ */
+int oracle_attn_fwd(int n_seq, const int32_t *cu_q, const int32_t *cu_k, int H, int D,
+                    const double *q, const double *k, const double *v, double scale,
+                    int causal, double *o, double *lse, int n_threads)
+{
+    if (check_segments(n_seq, cu_q, cu_k, causal) || H < 1 || D < 1) return -1;
+    set_threads(n_threads);
+    const int64_t Tq = cu_q[n_seq];
+    const int Lk_max = max_len(n_seq, cu_k);
+    const int64_t n_rows = Tq * H;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(Lk_max > 0 ? Lk_max : 1));
+#pragma omp for schedule(dynamic, 8)
+        for (int64_t r = 0; r < n_rows; ++r) {
+            const int64_t t = r / H;
+            const int h = (int)(r % H);
+            fwd_one(n_seq, cu_q, cu_k, H, D, q, k, v, scale, causal, t, h,
+                    o + r * D, lse + (int64_t)h * Tq + t, s);
+        }
+        free(s);
+    }
+    return 0;
+}
+
+/*
+ * Sampled forward: only the listed (token, head) query rows.  o_rows is
+ * (n, D), lse_rows is (n).  Used to check full-size runs row by row.
+ */
+int oracle_attn_fwd_rows(int n_seq, const int32_t *cu_q, const int32_t *cu_k, int H, int D,
+                         const double *q, const double *k, const double *v, double scale,
+                         int causal, int n, const int64_t *tokens, const int32_t *heads,
+                         double *o_rows, double *lse_rows, int n_threads)
+{
+    if (check_segments(n_seq, cu_q, cu_k, causal) || H < 1 || D < 1) return -1;
+    for (int r = 0; r < n; ++r)
+        if (tokens[r] < 0 || tokens[r] >= cu_q[n_seq] || heads[r] < 0 || heads[r] >= H) return -1;
+    set_threads(n_threads);
+    const int Lk_max = max_len(n_seq, cu_k);
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(Lk_max > 0 ? Lk_max : 1));
+#pragma omp for schedule(dynamic, 1)
+        for (int r = 0; r < n; ++r)
+            fwd_one(n_seq, cu_q, cu_k, H, D, q, k, v, scale, causal, tokens[r], heads[r],
+                    o_rows + (int64_t)r * D, lse_rows + r, s);
+        free(s);
+    }
+    return 0;
+}
+
+/*
+ * Per-row backward statistics of one (query token, head): m, l and
+ * c = sum_j P_j dP_j, and optionally that row's dq.
+ */
+static void bwd_row(int n_seq, const int32_t *cu_q, const int32_t *cu_k, int H, int D,
+                    const double *q, const double *k, const double *v, const double *dO,
+                    double scale, int causal, int64_t t, int h, double *m_out, double *l_out,
+                    double *c_out, double *dq_row, double *s)
+{
+    const int b = segment_of(n_seq, cu_q, t);
+    const int i = (int)(t - cu_q[b]);
+    const int Lk = cu_k[b + 1] - cu_k[b];
+    const int nj = admitted(i, Lk, causal);
+    const int64_t ld = (int64_t)H * D;
+    const double *qi = q + t * ld + (int64_t)h * D;
+    const double *dOi = dO + t * ld + (int64_t)h * D;
+    const double *k0 = k + (int64_t)cu_k[b] * ld + (int64_t)h * D;
+    const double *v0 = v + (int64_t)cu_k[b] * ld + (int64_t)h * D;
+
+    if (dq_row)
+        for (int d = 0; d < D; ++d) dq_row[d] = 0.0;
+    if (nj == 0) {
+        *m_out = -INFINITY;
+        *l_out = 0.0;
+        *c_out = 0.0;
+        return;
+    }
+    double m, l;
+    row_scores(qi, k0, ld, nj, D, scale, s, &m, &l);
+    double c = 0.0;
+    for (int j = 0; j < nj; ++j) {
+        const double p = exp(s[j] - m) / l;
+        c += p * dot(dOi, v0 + (int64_t)j * ld, D);
+    }
+    if (dq_row) {
+        for (int j = 0; j < nj; ++j) {
+            const double p = exp(s[j] - m) / l;
+            const double *kj = k0 + (int64_t)j * ld;
+            const double ds = p * (dot(dOi, v0 + (int64_t)j * ld, D) - c);
+            for (int d = 0; d < D; ++d) dq_row[d] += scale * ds * kj[d];
+        }
+    }
+    *m_out = m;
+    *l_out = l;
+    *c_out = c;
+}
+
+/*
+ * dk and dv of one (key token, head), given the statistics (m, l, c) of every
+ * query row of that head (arrays indexed (H, T_q)).
+ */
+static void bwd_key(int n_seq, const int32_t *cu_q, const int32_t *cu_k, int H, int D,
+                    const double *q, const double *k, const double *v, const double *dO,
+                    double scale, int causal, int64_t u, int h, const double *m_st,
+                    const double *l_st, const double *c_st, double *dk_row, double *dv_row)
+{
+    const int b = segment_of(n_seq, cu_k, u);
+    const int j = (int)(u - cu_k[b]);
+    const int Lq = cu_q[b + 1] - cu_q[b];
+    const int64_t Tq = cu_q[n_seq];
+    const int64_t ld = (int64_t)H * D;
+    const double *kj = k + u * ld + (int64_t)h * D;
+    const double *vj = v + u * ld + (int64_t)h * D;
+
+    for (int d = 0; d < D; ++d) {
+        dk_row[d] = 0.0;
+        dv_row[d] = 0.0;
+    }
+    for (int i = 0; i < Lq; ++i) {
+        if (causal && j > i) continue; /* (i, j) not in the relation */
+        const int64_t t = cu_q[b] + i;
+        const double *qi = q + t * ld + (int64_t)h * D;
+        const double *dOi = dO + t * ld + (int64_t)h * D;
+        const int64_t st = (int64_t)h * Tq + t;
+        const double p = exp(scale * dot(qi, kj, D) - m_st[st]) / l_st[st];
+        const double ds = p * (dot(dOi, vj, D) - c_st[st]);
+        for (int d = 0; d < D; ++d) {
+            dk_row[d] += scale * ds * qi[d];
+            dv_row[d] += p * dOi[d];
+        }
+    }
+}
+
+/*
+ * Backward.  Computes dq for the listed query rows and dk, dv for the listed
+ * key rows.  A NULL token list means "every row" and then the output arrays
+ * are full (T, H, D) tensors; otherwise they are (n, D).
+ */
+int oracle_attn_bwd(int n_seq, const int32_t *cu_q, const int32_t *cu_k, int H, int D,
+                    const double *q, const double *k, const double *v, const double *dO,
+                    double scale, int causal,
+                    int n_q_sel, const int64_t *q_tokens, const int32_t *q_heads, double *dq,
+                    int n_k_sel, const int64_t *k_tokens, const int32_t *k_heads, double *dk,
+                    double *dv, int n_threads)
+{
+    if (check_segments(n_seq, cu_q, cu_k, causal) || H < 1 || D < 1) return -1;
+    set_threads(n_threads);
+    const int64_t Tq = cu_q[n_seq];
+    const int64_t Tk = cu_k[n_seq];
+    const int Lk_max = max_len(n_seq, cu_k);
+    const int64_t nq = q_tokens ? n_q_sel : Tq * H;
+    const int64_t nk = k_tokens ? n_k_sel : Tk * H;
+    if (q_tokens)
+        for (int64_t r = 0; r < nq; ++r)
+            if (q_tokens[r] < 0 || q_tokens[r] >= Tq || q_heads[r] < 0 || q_heads[r] >= H) return -1;
+    if (k_tokens)
+        for (int64_t r = 0; r < nk; ++r)
+            if (k_tokens[r] < 0 || k_tokens[r] >= Tk || k_heads[r] < 0 || k_heads[r] >= H) return -1;
+
+    /* Which (segment, head) pairs need the statistics of all their rows. */
+    const int64_t n_pairs = (int64_t)n_seq * H;
+    unsigned char *need = (unsigned char *)calloc((size_t)n_pairs, 1);
+    double *m_st = (double *)malloc(sizeof(double) * (size_t)(Tq * H + 1));
+    double *l_st = (double *)malloc(sizeof(double) * (size_t)(Tq * H + 1));
+    double *c_st = (double *)malloc(sizeof(double) * (size_t)(Tq * H + 1));
+    if (!need || !m_st || !l_st || !c_st) {
+        free(need); free(m_st); free(l_st); free(c_st);
+        return -2;
+    }
+    for (int64_t r = 0; r < nk; ++r) {
+        const int64_t u = k_tokens ? k_tokens[r] : r / H;
+        const int h = k_tokens ? k_heads[r] : (int)(r % H);
+        need[(int64_t)segment_of(n_seq, cu_k, u) * H + h] = 1;
+    }
+
+    /* Pass 1: statistics of every query row of the needed pairs, and dq. */
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(Lk_max > 0 ? Lk_max : 1));
+        double m, l, c;
+#pragma omp for schedule(dynamic, 8)
+        for (int64_t r = 0; r < Tq * H; ++r) {
+            const int64_t t = r / H;
+            const int h = (int)(r % H);
+            if (!need[(int64_t)segment_of(n_seq, cu_q, t) * H + h]) continue;
+            bwd_row(n_seq, cu_q, cu_k, H, D, q, k, v, dO, scale, causal, t, h, &m, &l, &c,
+                    NULL, s);
+            m_st[(int64_t)h * Tq + t] = m;
+            l_st[(int64_t)h * Tq + t] = l;
+            c_st[(int64_t)h * Tq + t] = c;
+        }
+#pragma omp for schedule(dynamic, 8)
+        for (int64_t r = 0; r < nq; ++r) {
+            const int64_t t = q_tokens ? q_tokens[r] : r / H;
+            const int h = q_tokens ? q_heads[r] : (int)(r % H);
+            bwd_row(n_seq, cu_q, cu_k, H, D, q, k, v, dO, scale, causal, t, h, &m, &l, &c,
+                    dq + r * D, s);
+        }
+        free(s);
+    }
+
+    /* Pass 2: dk and dv of the requested keys, one key row at a time. */
+#pragma omp parallel for schedule(dynamic, 8)
+    for (int64_t r = 0; r < nk; ++r) {
+        const int64_t u = k_tokens ? k_tokens[r] : r / H;
+        const int h = k_tokens ? k_heads[r] : (int)(r % H);
+        bwd_key(n_seq, cu_q, cu_k, H, D, q, k, v, dO, scale, causal, u, h, m_st, l_st, c_st,
+                dk + r * D, dv + r * D);
+    }
+
+    free(need);
+    free(m_st);
+    free(l_st);
+    free(c_st);
+    return 0;
+}

@@ -1,0 +1,311 @@
+"""Pins for the f64 oracle, independent of the oracle itself (CPU only).
+
+Each test checks the oracle against something the pages or the mathematics
+fix: hand-derived closed forms (tests/golden/hand_cases.json), invariants of
+softmax attention, special cases that reduce to a library routine (torch's
+scaled_dot_product_attention and autograd, scipy's logsumexp), and central
+finite differences.  Together they fail on a dropped scale, a wrong sign, a
+transposed operand, an off-by-one in the causal relation, a wrong log base or a
+segment leak.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _ev(x):
+    if isinstance(x, str):
+        return eval(x, {"__builtins__": {}}, {"log": math.log, "exp": math.exp})  # noqa: S307
+    if isinstance(x, list):
+        return [_ev(y) for y in x]
+    return x
+
+
+def _rand(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+def _sdpa(q, k, v, causal, scale):
+    """torch's own attention in f64 on (T, H, D) numpy arrays, one sequence."""
+    Q, K, V = (torch.from_numpy(np.ascontiguousarray(x)).permute(1, 0, 2)[None] for x in (q, k, v))
+    out = torch.nn.functional.scaled_dot_product_attention(Q, K, V, is_causal=causal, scale=scale)
+    return out[0].permute(1, 0, 2).numpy()
+
+
+# --- hand-derived closed forms -------------------------------------------------
+
+def _hand():
+    with open(os.path.join(GOLDEN, "hand_cases.json")) as f:
+        return json.load(f)
+
+
+@pytest.mark.parametrize("case", _hand()["cases"], ids=lambda c: c["name"])
+def test_hand_cases_forward(case):
+    q, k, v = (np.array(_ev(case[n]), dtype=np.float64) for n in ("q", "k", "v"))
+    o, lse = oracle.fwd(q, k, v, causal=case["causal"], scale=case["scale"],
+                        cu_seqlens_q=case["cu_seqlens"])
+    np.testing.assert_allclose(o, np.array(_ev(case["o"])), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, np.array(_ev(case["lse"])), rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("case", _hand()["backward_cases"], ids=lambda c: c["name"])
+def test_hand_cases_backward(case):
+    q, k, v, dO = (np.array(_ev(case[n]), dtype=np.float64) for n in ("q", "k", "v", "dO"))
+    dq, dk, dv = oracle.bwd(q, k, v, dO, causal=case["causal"], scale=case["scale"])
+    np.testing.assert_allclose(dq, np.array(_ev(case["dq"])), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(dk, np.array(_ev(case["dk"])), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(dv, np.array(_ev(case["dv"])), rtol=0, atol=1e-13)
+
+
+# --- closed forms and invariants -----------------------------------------------
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_identical_keys_give_mean_of_admitted_values(causal):
+    T, H, D = 37, 3, 8
+    q = _rand((T, H, D), 1)
+    k = np.broadcast_to(_rand((1, H, D), 2), (T, H, D)).copy()
+    v = _rand((T, H, D), 3)
+    scale = 0.3
+    o, lse = oracle.fwd(q, k, v, causal=causal, scale=scale)
+    for i in range(T):
+        n = i + 1 if causal else T
+        np.testing.assert_allclose(o[i], v[:n].mean(axis=0), rtol=0, atol=1e-13)
+        s = scale * np.einsum("hd,hd->h", q[i], k[0])
+        np.testing.assert_allclose(lse[:, i], s + math.log(n), rtol=0, atol=1e-12)
+
+
+def test_one_hot_dominant_score_selects_one_value():
+    T, H, D = 12, 2, 16
+    rng = np.random.default_rng(4)
+    k = np.zeros((T, H, D))
+    for j in range(T):
+        k[j, :, j] = 1.0  # orthonormal keys
+    target = rng.integers(0, T, size=(T, H))
+    c = 40.0
+    q = np.zeros((T, H, D))
+    for i in range(T):
+        for h in range(H):
+            q[i, h, target[i, h]] = c
+    v = rng.standard_normal((T, H, D))
+    o, lse = oracle.fwd(q, k, v, causal=False, scale=1.0)
+    # all other weights are exp(-c) relative to the selected one
+    bound = (T - 1) * math.exp(-c) * 2 * np.abs(v).max()
+    for i in range(T):
+        for h in range(H):
+            np.testing.assert_allclose(o[i, h], v[target[i, h], h], rtol=0, atol=bound + 1e-15)
+            np.testing.assert_allclose(lse[h, i], c + math.log1p((T - 1) * math.exp(-c)),
+                                       rtol=0, atol=1e-12)
+
+
+def test_per_row_constant_shift():
+    """Adding c_i to every score of row i leaves O unchanged and shifts lse by c_i.
+
+    The shift is made with one extra dimension: k[:, D] = 1, q[i, D] = c_i / scale.
+    """
+    T, H, D = 29, 2, 6
+    q, k, v = _rand((T, H, D), 5), _rand((T, H, D), 6), _rand((T, H, D), 7)
+    scale = D ** -0.5
+    c = 50.0 * _rand((T, H), 8)
+    q2 = np.concatenate([q, (c / scale)[..., None]], axis=2)
+    k2 = np.concatenate([k, np.ones((T, H, 1))], axis=2)
+    v2 = np.concatenate([v, np.zeros((T, H, 1))], axis=2)
+    for causal in (False, True):
+        o, lse = oracle.fwd(q, k, v, causal=causal, scale=scale)
+        o2, lse2 = oracle.fwd(q2, k2, v2, causal=causal, scale=scale)
+        np.testing.assert_allclose(o2[..., :D], o, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse2, lse + c.T, rtol=0, atol=1e-11)
+
+
+def test_joint_key_value_permutation_full_relation():
+    T, H, D = 41, 3, 5
+    q, k, v = _rand((T, H, D), 9), _rand((T, H, D), 10), _rand((T, H, D), 11)
+    perm = np.random.default_rng(12).permutation(T)
+    o, lse = oracle.fwd(q, k, v, causal=False)
+    o2, lse2 = oracle.fwd(q, k[perm], v[perm], causal=False)
+    np.testing.assert_allclose(o2, o, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse2, lse, rtol=0, atol=1e-13)
+
+
+def test_causal_first_row_is_first_value_exactly():
+    T, H, D = 17, 2, 4
+    q, k, v = _rand((T, H, D), 13), _rand((T, H, D), 14), _rand((T, H, D), 15)
+    o, lse = oracle.fwd(q, k, v, causal=True, scale=0.7)
+    np.testing.assert_array_equal(o[0], v[0])
+    for h in range(H):
+        acc = 0.0
+        for d in range(D):  # in index order, as a plain loop sums
+            acc += float(q[0, h, d]) * float(k[0, h, d])
+        assert lse[h, 0] == 0.7 * acc  # m + ln(1) with the single admitted score
+
+
+def test_varlen_equals_concatenation_of_independent_sequences():
+    lengths = [5, 1, 9, 1, 13]  # includes length-1 sequences
+    T, H, D = sum(lengths), 2, 4
+    q, k, v = _rand((T, H, D), 16), _rand((T, H, D), 17), _rand((T, H, D), 18)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    o, lse = oracle.fwd(q, k, v, causal=True, cu_seqlens_q=cu)
+    for b in range(len(lengths)):
+        a, e = cu[b], cu[b + 1]
+        ob, lb = oracle.fwd(q[a:e], k[a:e], v[a:e], causal=True)
+        np.testing.assert_array_equal(o[a:e], ob)
+        np.testing.assert_array_equal(lse[:, a:e], lb)
+    # and length-1 sequences return their own value row
+    np.testing.assert_array_equal(o[5], v[5])
+
+
+def test_large_scores_are_stable_and_match_library_logsumexp():
+    from scipy.special import logsumexp, softmax
+    T, H, D = 23, 2, 8
+    q, k, v = _rand((T, H, D), 19), _rand((T, H, D), 20), _rand((T, H, D), 21)
+    scale = 100.0 * D ** -0.5
+    o, lse = oracle.fwd(q, k, v, causal=False, scale=scale)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    for h in range(H):
+        s = scale * q[:, h] @ k[:, h].T
+        np.testing.assert_allclose(lse[h], logsumexp(s, axis=1), rtol=1e-14, atol=1e-11)
+        np.testing.assert_allclose(o[:, h], softmax(s, axis=1) @ v[:, h], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("T,D", [(1, 4), (7, 3), (64, 16), (130, 32)])
+def test_matches_torch_sdpa_f64(causal, T, D):
+    H = 3
+    q, k, v = _rand((T, H, D), 22), _rand((T, H, D), 23), _rand((T, H, D), 24)
+    o, lse = oracle.fwd(q, k, v, causal=causal)
+    np.testing.assert_allclose(o, _sdpa(q, k, v, causal, D ** -0.5), rtol=0, atol=1e-12)
+
+
+def test_cross_attention_matches_torch_sdpa_f64():
+    Tq, Tk, H, D = 19, 7, 2, 8
+    q, k, v = _rand((Tq, H, D), 25), _rand((Tk, H, D), 26), _rand((Tk, H, D), 27)
+    o, _ = oracle.fwd(q, k, v, causal=False)
+    np.testing.assert_allclose(o, _sdpa(q, k, v, False, D ** -0.5), rtol=0, atol=1e-12)
+
+
+def test_causal_rejects_unequal_lengths():
+    q, k = _rand((5, 1, 2), 0), _rand((4, 1, 2), 1)
+    with pytest.raises(ValueError):
+        oracle.fwd(q, k, k, causal=True)
+
+
+def test_sampled_rows_equal_full_forward():
+    lengths = [37, 1, 140]
+    T, H, D = sum(lengths), 3, 8
+    q, k, v = _rand((T, H, D), 28), _rand((T, H, D), 29), _rand((T, H, D), 30)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    o, lse = oracle.fwd(q, k, v, causal=True, cu_seqlens_q=cu)
+    tokens = np.array([0, 36, 37, 38, 177, 100])
+    heads = np.array([0, 2, 1, 0, 2, 1])
+    orow, lrow = oracle.fwd_rows(q, k, v, tokens, heads, causal=True, cu_seqlens_q=cu)
+    np.testing.assert_array_equal(orow, o[tokens, heads])
+    np.testing.assert_array_equal(lrow, lse[heads, tokens])
+
+
+# --- backward ------------------------------------------------------------------
+
+def _loss(q, k, v, dO, causal, scale, cu=None):
+    o, _ = oracle.fwd(q, k, v, causal=causal, scale=scale, cu_seqlens_q=cu)
+    return float(np.sum(o * dO))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_central_finite_differences(causal):
+    T, H, D = 6, 1, 4
+    q, k, v, dO = (_rand((T, H, D), s) for s in (31, 32, 33, 34))
+    scale = 0.6
+    dq, dk, dv = oracle.bwd(q, k, v, dO, causal=causal, scale=scale)
+    h = 1e-6
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args = {"q": q, "k": k, "v": v}
+            args[name] = xp
+            lp = _loss(args["q"], args["k"], args["v"], dO, causal, scale)
+            args[name] = xm
+            lm = _loss(args["q"], args["k"], args["v"], dO, causal, scale)
+            num[idx] = (lp - lm) / (2 * h)
+        rel = np.linalg.norm(num - g) / np.linalg.norm(g)
+        assert rel <= 1e-7, (name, rel)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_matches_torch_autograd_f64(causal):
+    T, H, D = 45, 2, 8
+    q, k, v, dO = (_rand((T, H, D), s) for s in (35, 36, 37, 38))
+    dq, dk, dv = oracle.bwd(q, k, v, dO, causal=causal)
+    Q, K, V = (torch.from_numpy(x).permute(1, 0, 2)[None].clone().requires_grad_() for x in (q, k, v))
+    out = torch.nn.functional.scaled_dot_product_attention(Q, K, V, is_causal=causal)
+    out.backward(torch.from_numpy(dO).permute(1, 0, 2)[None])
+    for g, t in ((dq, Q), (dk, K), (dv, V)):
+        np.testing.assert_allclose(g, t.grad[0].permute(1, 0, 2).numpy(), rtol=0, atol=1e-12)
+
+
+def test_backward_varlen_equals_per_sequence():
+    lengths = [4, 1, 11]
+    T, H, D = sum(lengths), 2, 4
+    q, k, v, dO = (_rand((T, H, D), s) for s in (39, 40, 41, 42))
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    dq, dk, dv = oracle.bwd(q, k, v, dO, causal=True, cu_seqlens_q=cu)
+    for b in range(len(lengths)):
+        a, e = cu[b], cu[b + 1]
+        gq, gk, gv = oracle.bwd(q[a:e], k[a:e], v[a:e], dO[a:e], causal=True)
+        np.testing.assert_allclose(dq[a:e], gq, rtol=0, atol=1e-14)
+        np.testing.assert_allclose(dk[a:e], gk, rtol=0, atol=1e-14)
+        np.testing.assert_allclose(dv[a:e], gv, rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_row_dot_identity(causal):
+    """sum_j P_ij dP_ij equals <dO_i, O_i> (the per-row D of the OCANNL page's
+    fused backward): dq rebuilt from that shortcut equals the oracle's dq."""
+    from scipy.special import softmax
+    T, H, D = 21, 2, 6
+    q, k, v, dO = (_rand((T, H, D), s) for s in (43, 44, 45, 46))
+    scale = D ** -0.5
+    o, _ = oracle.fwd(q, k, v, causal=causal)
+    dq, _, _ = oracle.bwd(q, k, v, dO, causal=causal)
+    for h in range(H):
+        s = scale * q[:, h] @ k[:, h].T
+        if causal:
+            s = np.where(np.tril(np.ones((T, T), dtype=bool)), s, -np.inf)
+        p = softmax(s, axis=1)
+        dp = dO[:, h] @ v[:, h].T
+        Drow = np.einsum("id,id->i", dO[:, h], o[:, h])
+        ds = p * (dp - Drow[:, None])
+        np.testing.assert_allclose(dq[:, h], scale * ds @ k[:, h], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_sum_invariants(causal):
+    """Softmax is invariant to a common shift of all keys, so sum_j dk_j = 0;
+    the probabilities of a row sum to 1, so sum_j dv_j = sum_i dO_i."""
+    T, H, D = 33, 3, 5
+    q, k, v, dO = (_rand((T, H, D), s) for s in (47, 48, 49, 50))
+    dq, dk, dv = oracle.bwd(q, k, v, dO, causal=causal)
+    np.testing.assert_allclose(dk.sum(axis=0), 0.0, atol=1e-12)
+    np.testing.assert_allclose(dv.sum(axis=0), dO.sum(axis=0), atol=1e-12)
+
+
+def test_backward_sampled_rows_equal_full():
+    lengths = [19, 1, 30]
+    T, H, D = sum(lengths), 2, 4
+    q, k, v, dO = (_rand((T, H, D), s) for s in (51, 52, 53, 54))
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    dq, dk, dv = oracle.bwd(q, k, v, dO, causal=True, cu_seqlens_q=cu)
+    rows = (np.array([0, 18, 19, 49, 25]), np.array([1, 0, 1, 1, 0]))
+    keys = (np.array([0, 19, 20, 49, 3]), np.array([0, 1, 0, 1, 1]))
+    sq, sk, sv = oracle.bwd(q, k, v, dO, causal=True, cu_seqlens_q=cu, q_rows=rows, k_rows=keys)
+    np.testing.assert_array_equal(sq, dq[rows[0], rows[1]])
+    np.testing.assert_array_equal(sk, dk[keys[0], keys[1]])
+    np.testing.assert_array_equal(sv, dv[keys[0], keys[1]])
