@@ -1,0 +1,388 @@
+#!/usr/bin/env python3
+"""Attention training-step benchmark on GB300.
+
+Workload: causal attention forward + backward, batch 4 x N=8192, H=32, D=128,
+bf16 Q/K/V/dO ~ N(0,1) (seed 5), scale D^-1/2; the batch is packed as four
+sequences with cu_seqlens [0, 8192, 16384, 24576, 32768].  One step = one
+forward (O stored in f32, lse) and one backward (Dr preprocess, dK/dV, dQ)
+through the library's C ABI.
+
+Metric: attention fwd+bwd TFLOP/s, with fwd = 4 N^2 D H / 2 per causal
+sequence and bwd = 2.5 x fwd, summed over the batch; `value` is the whole-job
+rate over all ranks (each rank runs the full batch: weak scaling, no
+collective on the data path).
+
+Prints one JSON line.  `--impl reference` times the f64 CPU oracle instead,
+on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "causal_train_bf16_b4_n8192"
+METRIC = "attention fwd+bwd TFLOP/s (causal, B=4, N=8192, H=32, D=128, bf16)"
+UNIT = "TFLOP/s"
+
+
+def attention_flops(lengths_q, lengths_k, H, D, causal):
+    """Algorithmic forward FLOPs: 4 Lq Lk D H per sequence, halved for causal."""
+    f = 0.0
+    for lq, lk in zip(lengths_q, lengths_k):
+        f += 4.0 * lq * lk * D * H * (0.5 if causal else 1.0)
+    return f
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p.get("hbm_gbs"), "bf16_tflops": p.get("bf16_tflops"),
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"),
+                "sm_max_mhz": p.get("sm_max_mhz", 2070.0), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+def source_hash(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key, src_hash):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel
+    source has not changed since the counters were taken (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel_key)
+    if not rec or rec.get("source_hash") != src_hash:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        if not self.proc or not self.file:
+            return None
+        self.file.flush()
+        with open(self.file.name) as f:
+            rows = [r.strip().split(", ") for r in f if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def time_oracle_sample(x, w, max_seconds=20.0):
+    """Time the oracle's forward + backward on whole (sequence, head) pairs of
+    the workload, adding pairs until about `max_seconds` of CPU work."""
+    import numpy as np
+
+    import oracle
+    L = x["lengths_q"][0]
+    pair_flops = attention_flops([L], [L], 1, w.D, w.causal) * 3.5
+    done, spent, pairs = 0, 0.0, []
+    rng = np.random.default_rng(0)
+    while spent < max_seconds * 0.5 and done < 8:
+        b, h = int(rng.integers(0, w.batch)), int(rng.integers(0, w.H))
+        s0, s1 = b * L, (b + 1) * L
+        q, k, v, dO = (x[n][s0:s1, h:h + 1] for n in ("q", "k", "v", "dO"))
+        t0 = time.perf_counter()
+        oracle.fwd(q, k, v, causal=True)
+        oracle.bwd(q, k, v, dO, causal=True)
+        spent += time.perf_counter() - t0
+        done += 1
+        pairs.append((b, h))
+    return {"value": pair_flops * done / spent / 1e12, "unit": UNIT, "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"{done} whole (sequence, head) pairs of the workload, fwd+bwd, "
+                      f"N={L}, D={w.D}, causal: {spent:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the f64 CPU oracle on the host cores, bounded samples."""
+    if rank != 0:
+        return
+    import attn_inputs
+    w = attn_inputs.WORKLOADS[WORKLOAD]
+    x = attn_inputs.make_workload(w)
+    vals = []
+    for _ in range(args.warmup):
+        time_oracle_sample(x, w, max_seconds=4.0)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(time_oracle_sample(x, w, max_seconds=6.0))
+    elapsed = time.perf_counter() - t0
+    value = statistics.median(v["value"] for v in vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": elapsed * 1e3 / max(1, args.steps),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "batch": 4, "seq_len": 8192,
+                                            "heads": 32, "head_dim": 128, "relation": "causal"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": vals[0]["cores"],
+                             "kind": "oracle", "sample": vals[0]["sample"]},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import attn_inputs
+    import online_softmax_attention_gb300 as attn
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    w = attn_inputs.WORKLOADS[WORKLOAD]
+    x = attn_inputs.make_workload(w)
+    lq, lk = x["lengths_q"], x["lengths_k"]
+    fwd_flops = attention_flops(lq, lk, w.H, w.D, w.causal)
+    bwd_flops = 2.5 * fwd_flops
+    step_flops = fwd_flops + bwd_flops
+
+    q, k, v, dO = (x[n].to(dev) for n in ("q", "k", "v", "dO"))
+    cu = x["cu_seqlens_q"].to(dev)
+    fcall = attn.FwdCall(q, k, v, causal=True, cu_seqlens_q=cu, out_dtype=torch.float32,
+                         kernel=args.kernel)
+    bcall = attn.BwdCall(q, k, v, fcall.o, fcall.lse, dO, causal=True, cu_seqlens_q=cu,
+                         kernel=args.kernel)
+    stream = torch.cuda.current_stream()
+    stages = ["fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq"]
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        fcall.run(stream)
+        if ev is not None:
+            ev[1].record(stream)
+        bcall.preprocess(stream)
+        if ev is not None:
+            ev[2].record(stream)
+        bcall.dkdv(stream)
+        if ev is not None:
+            ev[3].record(stream)
+        bcall.dq_stage(stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if attn.device_status() != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    n0 = attn.launch_count()
+    with ClockSampler(local) as clk:
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    launches = attn.launch_count() - n0
+    ms = start.elapsed_time(end) / args.steps
+    stage_ms = {s: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j, s in enumerate(stages)}
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    status = attn.device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+
+    # end-to-end through the public API with host buffers
+    pin = {n: x[n].contiguous().pin_memory() for n in ("q", "k", "v", "dO")}
+    outs_host = {"o": torch.empty(fcall.o.shape, dtype=fcall.o.dtype).pin_memory(),
+                 "lse": torch.empty(fcall.lse.shape, dtype=torch.float32).pin_memory(),
+                 "dq": torch.empty(bcall.dq.shape, dtype=bcall.dq.dtype).pin_memory(),
+                 "dk": torch.empty(bcall.dk.shape, dtype=bcall.dk.dtype).pin_memory(),
+                 "dv": torch.empty(bcall.dv.shape, dtype=bcall.dv.dtype).pin_memory()}
+    dev_in = {"q": q, "k": k, "v": v, "dO": dO}
+    dev_out = {"o": fcall.o, "lse": fcall.lse, "dq": bcall.dq, "dk": bcall.dk, "dv": bcall.dv}
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs_host.values())
+
+    def e2e_step():
+        for n, t in pin.items():
+            dev_in[n].copy_(t, non_blocking=True)
+        fcall.run(stream)
+        bcall.run(stream)
+        for n, t in outs_host.items():
+            t.copy_(dev_out[n], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e_steps = max(2, min(args.steps, 5))
+    barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = t0.elapsed_time(t1) / e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    peaks = load_peaks()
+    # algorithmic FLOPs per launch of each stage: fwd = S and PV contractions;
+    # dkdv = S (recompute), dP, dV, dK; dq = dQ only (its S / dP recomputes are
+    # not algorithmic work); preprocess is HBM-bound (reads O f32 and dO bf16).
+    stage_flops = {"fwd": fwd_flops, "bwd_dkdv": 2.0 * fwd_flops, "bwd_dq": 0.5 * fwd_flops}
+    dominant = max(("fwd", "bwd_dkdv", "bwd_dq"), key=lambda s: stage_ms[s])
+    kernel_files = {"fwd": ["online_softmax_attention_gb300/csrc/fwd_simt.cu"],
+                    "bwd_dkdv": ["online_softmax_attention_gb300/csrc/bwd_simt.cu"],
+                    "bwd_dq": ["online_softmax_attention_gb300/csrc/bwd_simt.cu"]}
+    using_tc = fcall.selected_kernel() == "tc" and bcall.selected_kernel() == "tc"
+    if using_tc:
+        kernel_files = {"fwd": ["online_softmax_attention_gb300/csrc/fwd_tc.cu"],
+                        "bwd_dkdv": ["online_softmax_attention_gb300/csrc/bwd_tc.cu"],
+                        "bwd_dq": ["online_softmax_attention_gb300/csrc/bwd_tc.cu"]}
+    achieved = stage_flops[dominant] / (stage_ms[dominant] * 1e-3) / 1e12
+    if using_tc:
+        peak, bound, punit = peaks["bf16_tflops_sustained"], "tensor", "TFLOP/s"
+        peak_note = f"bf16 dense, sustained ({peaks['source']})"
+    else:
+        # FP32 FFMA: 152 SMs x 128 lanes x 2 FLOP x max SM clock
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        peak = sms * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+        bound, punit = "alu", "TFLOP/s"
+        peak_note = f"FP32 FFMA: {sms} SMs x 128 lanes x 2 FLOP x {peaks['sm_max_mhz']:.0f} MHz"
+    src = [p for p in kernel_files[dominant] if os.path.exists(os.path.join(ROOT, p))]
+    traffic = recorded_traffic(dominant, source_hash(src)) if src else None
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": punit,
+                "frac": achieved / peak, "traffic": traffic, "kernel": dominant,
+                "peak_source": peak_note}
+
+    fwd_tflops = fwd_flops / (stage_ms["fwd"] * 1e-3) / 1e12
+    bwd_ms = stage_ms["bwd_preprocess"] + stage_ms["bwd_dkdv"] + stage_ms["bwd_dq"]
+    bwd_tflops = bwd_flops / (bwd_ms * 1e-3) / 1e12
+    value = step_flops * world / (ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": 4, "seq_len": 8192, "heads": 32, "head_dim": 128,
+                   "relation": "causal", "o_dtype": "f32", "grad_dtype": "bf16",
+                   "kernel": "tc" if using_tc else "simt",
+                   "l2": "no flush: each input tensor is 268 MB, larger than the 129 MB L2",
+                   "parallelism": f"replicas x{world}"},
+        "breakdown": {"fwd_ms": stage_ms["fwd"], "bwd_ms": bwd_ms,
+                      "stage_ms": stage_ms, "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
+                      "fwd_frac_of_bf16_peak": fwd_tflops / peaks["bf16_tflops"],
+                      "bf16_peak_tflops": peaks["bf16_tflops"]},
+        "roofline": roofline,
+        "e2e": {"value": step_flops * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = time_oracle_sample(x, w)
+    else:
+        line["cpu_baseline"] = None
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

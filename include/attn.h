@@ -1,0 +1,197 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) online-softmax attention library.
+ *
+ * Exact scaled dot-product attention, forward and fused backward, computed by
+ * the online-softmax block recurrence on one GPU.
+ *
+ * Definition (TIGA-lang, "注意力与稠密关系" attention examples page, section
+ * "全量注意力，无掩码", display equation):
+ *     s_hij  = <k_hj, q_hi> * scale
+ *     out_hi = sum_j softmax_j(s_hi.) v_hj
+ * over a relation that decides which (i, j) pairs exist:
+ *   ATTN_FULL    every key of the query's sequence (dense relation);
+ *   ATTN_CAUSAL  keys j <= i of the query's sequence (same page, section
+ *                "因果稠密关系", triangular relation).
+ * With cu_seqlens the tokens form independent sequences back to back and no
+ * pair crosses a sequence boundary (same page, section
+ * "用图组合表达 varlen 因果注意力": block-diagonal relation, flash-attn's
+ * cu_seqlens convention [0, L1, L1+L2, ...]).
+ *
+ * Algorithm (OCANNL "Module Ir.Online_softmax", fourth bullet): for each
+ * query tile a scan over key blocks carries the running row max m and the
+ * rescaled row sum l, accumulates the numerator U = sum p*v, and the last
+ * block writes O = U / l.  A key block that runs past the end of a sequence
+ * is a guarded tail padded with -inf scores.  The row log-sum-exp
+ * lse = m + ln l (natural log, of the scaled scores) is written for the
+ * backward.
+ *
+ * Backward (same page, third bullet): Dr_i = sum_d dO_id * O_id per row;
+ * per pair recompute p and dp = <dO_i, v_j>; ds = p * (dp - Dr_i);
+ * dq = scale * ds . k, dk = scale * ds^T . q, dv = p^T . dO.  Each output is
+ * written by exactly one kernel that owns it (no atomics), so results are
+ * run-to-run deterministic.
+ *
+ * Conventions for every entry point:
+ *  - Every tensor pointer is a DEVICE pointer on the current CUDA device,
+ *    owned by the caller.  The library allocates no memory visible to the
+ *    caller; scratch comes from the caller's workspace.
+ *  - Tensors are (tokens, heads, D) with element strides given per tensor for
+ *    the token and head axes; the D axis must be contiguous (stride 1).
+ *    Token and head strides must be multiples of 8 elements for 16-bit types
+ *    and of 4 elements for f32 (16-byte rows), and base pointers must be
+ *    16-byte aligned.
+ *  - lse / Dr are f32 (H, n_q) contiguous.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream).  No call synchronises the host, except
+ *    attn_device_status().
+ *  - Return value: ATTN_OK (0) or a negative attn_status.  Invalid arguments
+ *    are rejected before any launch.  Errors found by kernels (inconsistent
+ *    cu_seqlens, a watchdog timeout) are reported by attn_device_status().
+ *  - Outputs are fully overwritten; no zero-initialisation is needed.
+ *  - A query row that admits no key (only an empty key sequence under
+ *    ATTN_FULL) gets O = 0 and lse = -inf.
+ *  - Inputs must be finite.
+ */
+#ifndef ATTN_GB300_ATTN_H
+#define ATTN_GB300_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ATTN_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+typedef enum attn_status {
+    ATTN_OK = 0,
+    ATTN_EINVAL = -1,        /* bad pointer, stride, size or cu_seqlens */
+    ATTN_EUNSUPPORTED = -2,  /* valid but not implemented (dtype, D, relation mix, GPU) */
+    ATTN_ECUDA = -3,         /* a CUDA runtime call failed; see attn_last_error_string() */
+    ATTN_ETIMEOUT = -4,      /* a kernel's bounded wait expired (device watchdog) */
+    ATTN_EWORKSPACE = -5     /* workspace missing or smaller than *_workspace_bytes() */
+} attn_status;
+
+typedef enum attn_dtype { ATTN_F16 = 0, ATTN_BF16 = 1, ATTN_F32 = 2 } attn_dtype;
+
+typedef enum attn_relation { ATTN_FULL = 0, ATTN_CAUSAL = 1 } attn_relation;
+
+/* Kernel choice.  AUTO picks the tcgen05 tensor-core kernels for f16/bf16 and
+ * the FP32 SIMT kernels for f32.  SIMT forces the CUDA-core kernels (any
+ * dtype); TC forces the tensor-core kernels (f16/bf16 only). */
+typedef enum attn_kernel { ATTN_KERNEL_AUTO = 0, ATTN_KERNEL_SIMT = 1, ATTN_KERNEL_TC = 2 } attn_kernel;
+
+/* A (tokens, heads, D) tensor view: element strides of the token and head axes. */
+typedef struct attn_tensor {
+    void *ptr;
+    int64_t stride_tok;
+    int64_t stride_head;
+} attn_tensor;
+
+typedef struct attn_fwd_args {
+    attn_tensor q;        /* in:  (n_q, H, D), dtype */
+    attn_tensor k;        /* in:  (n_k, H, D), dtype */
+    attn_tensor v;        /* in:  (n_k, H, D), dtype */
+    attn_tensor o;        /* out: (n_q, H, D), o_dtype */
+    float *lse;           /* out: (H, n_q) f32, natural-log row log-sum-exp; may be NULL */
+    int32_t n_q, n_k;     /* total query / key tokens */
+    int32_t H, D;         /* heads; head dim (64 or 128) */
+    float scale;          /* score scale, usually D^-1/2 */
+    int32_t relation;     /* attn_relation */
+    int32_t dtype;        /* attn_dtype of q, k, v */
+    int32_t o_dtype;      /* attn_dtype of o: dtype or ATTN_F32 */
+    int32_t n_seq;        /* sequences; 1 when cu_seqlens_* are NULL */
+    const int32_t *cu_seqlens_q; /* device, n_seq+1 offsets from 0, or NULL (one sequence of n_q) */
+    const int32_t *cu_seqlens_k; /* device, n_seq+1 offsets from 0, or NULL (one sequence of n_k) */
+    void *workspace;      /* device scratch, attn_fwd_workspace_bytes() bytes, 256-byte aligned */
+    size_t workspace_bytes;
+    int32_t kernel;       /* attn_kernel */
+    int32_t num_ctas;     /* persistent grid size; 0 = one per SM */
+} attn_fwd_args;
+
+typedef struct attn_bwd_args {
+    attn_tensor q, k, v;  /* in: as in the forward */
+    attn_tensor o;        /* in: forward output, o_dtype */
+    attn_tensor dout;     /* in: dL/dO, (n_q, H, D), dtype */
+    const float *lse;     /* in: (H, n_q) f32 from attn_fwd */
+    attn_tensor dq;       /* out: (n_q, H, D), grad_dtype */
+    attn_tensor dk;       /* out: (n_k, H, D), grad_dtype */
+    attn_tensor dv;       /* out: (n_k, H, D), grad_dtype */
+    int32_t n_q, n_k, H, D;
+    float scale;
+    int32_t relation, dtype, o_dtype;
+    int32_t grad_dtype;   /* attn_dtype of dq, dk, dv: dtype or ATTN_F32 */
+    int32_t n_seq;
+    const int32_t *cu_seqlens_q, *cu_seqlens_k;
+    void *workspace;      /* attn_bwd_workspace_bytes() bytes, 256-byte aligned */
+    size_t workspace_bytes;
+    int32_t kernel;
+    int32_t num_ctas;
+} attn_bwd_args;
+
+/* Library ABI version (ATTN_ABI_VERSION) and struct sizes, for bindings to
+ * check their mirrors of the structs above. */
+ATTN_API int attn_abi_version(void);
+ATTN_API size_t attn_fwd_args_size(void);
+ATTN_API size_t attn_bwd_args_size(void);
+
+/* Bytes of device workspace the call needs (depends on n_seq, H, n_q). */
+ATTN_API size_t attn_fwd_workspace_bytes(const attn_fwd_args *a);
+ATTN_API size_t attn_bwd_workspace_bytes(const attn_bwd_args *a);
+
+/* Forward: writes o and lse.  Launches a schedule-preparation kernel and one
+ * persistent attention kernel on `stream`. */
+ATTN_API int attn_fwd(const attn_fwd_args *a, void *stream);
+
+/* Backward: writes dq, dk, dv.  Equivalent to attn_bwd_preprocess, then
+ * attn_bwd_dkdv, then attn_bwd_dq on the same stream and workspace. */
+ATTN_API int attn_bwd(const attn_bwd_args *a, void *stream);
+
+/* The three stages of attn_bwd, callable one by one (e.g. to time each):
+ *  preprocess: Dr = rowsum(dO * O) into the workspace, and the schedules;
+ *  dkdv:       per key block, loop over query blocks, write dk and dv;
+ *  dq:         per query block, loop over key blocks, write dq.
+ * dkdv and dq read what preprocess wrote into the same workspace. */
+ATTN_API int attn_bwd_preprocess(const attn_bwd_args *a, void *stream);
+ATTN_API int attn_bwd_dkdv(const attn_bwd_args *a, void *stream);
+ATTN_API int attn_bwd_dq(const attn_bwd_args *a, void *stream);
+
+/* Flat form for contiguous (N, H, D) self-attention tensors (token stride
+ * H*D, head stride D), o in the input dtype, AUTO kernel choice.
+ * cu_seqlens: device, n_seq+1 entries, or NULL for one sequence. */
+ATTN_API int attn_fwd_simple(const void *q, const void *k, const void *v, void *out, float *lse,
+                    int32_t N, int32_t H, int32_t D, float scale, int32_t relation,
+                    const int32_t *cu_seqlens, int32_t n_seq, int32_t dtype,
+                    void *workspace, size_t workspace_bytes, void *stream);
+
+/* The kernel family a call with these arguments runs (ATTN_KERNEL_SIMT or
+ * ATTN_KERNEL_TC, resolving AUTO), or a negative attn_status if the call
+ * would be rejected.  Host-only; launches nothing. */
+ATTN_API int attn_fwd_selected_kernel(const attn_fwd_args *a);
+ATTN_API int attn_bwd_selected_kernel(const attn_bwd_args *a);
+
+/* Synchronises `stream`, then returns and clears the device-side status word
+ * of the current device: ATTN_OK, ATTN_EINVAL (a kernel found inconsistent
+ * cu_seqlens and skipped the work) or ATTN_ETIMEOUT (a bounded wait expired
+ * and the kernel exited early; outputs are then incomplete). */
+ATTN_API int attn_device_status(void *stream);
+
+/* Number of kernels the library has launched in this process (all devices). */
+ATTN_API uint64_t attn_launch_count(void);
+
+/* Static text for a status code, and the last CUDA error text of this thread. */
+ATTN_API const char *attn_strerror(int code);
+ATTN_API const char *attn_last_error_string(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_ATTN_H */

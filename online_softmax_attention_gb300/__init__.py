@@ -1,0 +1,218 @@
+"""Exact online-softmax attention on one GB300 (sm_103a), forward and backward.
+
+PyTorch is used for device memory and streams only; every step of the
+computation runs in the CUDA library ``_lib/libattn_gb300.so`` through its C
+ABI (``include/attn.h``).  This module marshals tensors into the ABI's
+argument structs:
+
+* ``fwd(q, k, v, causal=..., cu_seqlens_q=...)`` -> ``(o, lse)``
+* ``bwd(q, k, v, o, lse, dout, causal=...)`` -> ``(dq, dk, dv)``
+* ``FwdCall`` / ``BwdCall`` hold prepared argument structs for repeated
+  launches (the benchmark and CUDA-graph capture use them).
+
+Tensors are (tokens, heads, D) with the D axis contiguous; any token / head
+strides whose rows stay 16-byte aligned are accepted (for example an (H, N, D)
+tensor viewed as (N, H, D)).  ``cu_seqlens`` follow flash-attn's varlen
+convention ``[0, L1, L1+L2, ...]`` as int32.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _abi
+from ._abi import (ATTN_BF16, ATTN_CAUSAL, ATTN_F16, ATTN_F32, ATTN_FULL, ATTN_KERNEL_AUTO,
+                   ATTN_KERNEL_SIMT, ATTN_KERNEL_TC, AttnError, check)
+
+__all__ = ["fwd", "bwd", "FwdCall", "BwdCall", "device_status", "launch_count", "AttnError",
+           "library_path"]
+
+_DT = {torch.float16: ATTN_F16, torch.bfloat16: ATTN_BF16, torch.float32: ATTN_F32}
+_KERNELS = {"auto": ATTN_KERNEL_AUTO, "simt": ATTN_KERNEL_SIMT, "tc": ATTN_KERNEL_TC}
+
+
+def library_path() -> str:
+    return _abi.LIB_PATH
+
+
+def launch_count() -> int:
+    """Kernels launched by the library so far in this process."""
+    return int(_abi.load().attn_launch_count())
+
+
+def device_status(stream: torch.cuda.Stream | None = None) -> int:
+    """Synchronise the stream and return / clear the device status word."""
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(_abi.load().attn_device_status(ctypes.c_void_p(s.cuda_stream)))
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt not in _DT:
+        raise TypeError(f"unsupported dtype {dt}; use float16, bfloat16 or float32")
+    return _DT[dt]
+
+
+def _view(t: torch.Tensor | None, name: str) -> _abi.AttnTensor:
+    if t is None:
+        return _abi.AttnTensor(None, 0, 0)
+    if t.dim() != 3:
+        raise ValueError(f"{name} must be (tokens, heads, D), got {tuple(t.shape)}")
+    if t.stride(2) != 1 and t.shape[2] > 1:
+        raise ValueError(f"{name}: the D axis must be contiguous")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    # a size-1 axis is never stepped along, so any aligned stride describes it
+    st = t.stride(0) if t.shape[0] > 1 else t.shape[1] * t.shape[2]
+    sh = t.stride(1) if t.shape[1] > 1 else t.shape[2]
+    return _abi.AttnTensor(t.data_ptr() if t.numel() else None, st, sh)
+
+
+def _cu(cu, device) -> torch.Tensor | None:
+    if cu is None:
+        return None
+    cu = torch.as_tensor(cu)
+    if cu.dtype != torch.int32:
+        cu = cu.to(torch.int32)
+    return cu.to(device).contiguous()
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor:
+    # torch's caching allocator returns 512-byte aligned blocks
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def _selected(code: int, where: str) -> str:
+    if code < 0:
+        check(code, where)
+    return "tc" if code == ATTN_KERNEL_TC else "simt"
+
+
+class FwdCall:
+    """Prepared forward: holds the argument struct, outputs and workspace."""
+
+    def __init__(self, q, k, v, *, causal: bool = False, scale: float | None = None,
+                 cu_seqlens_q=None, cu_seqlens_k=None, out_dtype: torch.dtype | None = None,
+                 kernel: str = "auto", num_ctas: int = 0, out: torch.Tensor | None = None,
+                 lse: torch.Tensor | None = None, workspace: torch.Tensor | None = None):
+        if q.dtype != k.dtype or q.dtype != v.dtype:
+            raise TypeError("q, k, v must share one dtype")
+        dev = q.device
+        Tq, H, D = q.shape
+        Tk = k.shape[0]
+        out_dtype = out_dtype or q.dtype
+        self.cu_q = _cu(cu_seqlens_q, dev)
+        self.cu_k = _cu(cu_seqlens_k if cu_seqlens_k is not None else cu_seqlens_q, dev)
+        self.o = out if out is not None else torch.empty((Tq, H, D), dtype=out_dtype, device=dev)
+        self.lse = lse if lse is not None else torch.empty((H, Tq), dtype=torch.float32, device=dev)
+        self.inputs = (q, k, v)
+        a = _abi.FwdArgs()
+        a.q, a.k, a.v, a.o = _view(q, "q"), _view(k, "k"), _view(v, "v"), _view(self.o, "out")
+        a.lse = self.lse.data_ptr() if self.lse.numel() else None
+        a.n_q, a.n_k, a.H, a.D = Tq, Tk, H, D
+        a.scale = float(scale) if scale is not None else D ** -0.5
+        a.relation = ATTN_CAUSAL if causal else ATTN_FULL
+        a.dtype, a.o_dtype = _dtype_code(q.dtype), _dtype_code(self.o.dtype)
+        a.n_seq = (self.cu_q.numel() - 1) if self.cu_q is not None else 1
+        a.cu_seqlens_q = self.cu_q.data_ptr() if self.cu_q is not None else None
+        a.cu_seqlens_k = self.cu_k.data_ptr() if self.cu_k is not None else None
+        a.kernel = _KERNELS[kernel]
+        a.num_ctas = int(num_ctas)
+        lib = _abi.load()
+        need = lib.attn_fwd_workspace_bytes(ctypes.byref(a))
+        self.workspace = workspace if workspace is not None else _workspace(need, dev)
+        a.workspace = self.workspace.data_ptr()
+        a.workspace_bytes = self.workspace.numel() * self.workspace.element_size()
+        self.args = a
+        self._fn = lib.attn_fwd
+
+    def run(self, stream: torch.cuda.Stream | None = None):
+        s = stream if stream is not None else torch.cuda.current_stream()
+        check(self._fn(ctypes.byref(self.args), ctypes.c_void_p(s.cuda_stream)), "attn_fwd")
+        return self.o, self.lse
+
+    def selected_kernel(self) -> str:
+        """"tc" or "simt": the kernel family these arguments run."""
+        return _selected(_abi.load().attn_fwd_selected_kernel(ctypes.byref(self.args)),
+                         "attn_fwd_selected_kernel")
+
+
+class BwdCall:
+    """Prepared backward: holds the argument struct, gradients and workspace."""
+
+    def __init__(self, q, k, v, o, lse, dout, *, causal: bool = False, scale: float | None = None,
+                 cu_seqlens_q=None, cu_seqlens_k=None, grad_dtype: torch.dtype | None = None,
+                 kernel: str = "auto", num_ctas: int = 0, dq=None, dk=None, dv=None,
+                 workspace: torch.Tensor | None = None):
+        dev = q.device
+        Tq, H, D = q.shape
+        Tk = k.shape[0]
+        gdt = grad_dtype or q.dtype
+        self.cu_q = _cu(cu_seqlens_q, dev)
+        self.cu_k = _cu(cu_seqlens_k if cu_seqlens_k is not None else cu_seqlens_q, dev)
+        self.dq = dq if dq is not None else torch.empty((Tq, H, D), dtype=gdt, device=dev)
+        self.dk = dk if dk is not None else torch.empty((Tk, H, D), dtype=gdt, device=dev)
+        self.dv = dv if dv is not None else torch.empty((Tk, H, D), dtype=gdt, device=dev)
+        self.inputs = (q, k, v, o, lse, dout)
+        a = _abi.BwdArgs()
+        a.q, a.k, a.v = _view(q, "q"), _view(k, "k"), _view(v, "v")
+        a.o, a.dout = _view(o, "o"), _view(dout, "dout")
+        a.lse = lse.data_ptr() if lse.numel() else None
+        a.dq, a.dk, a.dv = _view(self.dq, "dq"), _view(self.dk, "dk"), _view(self.dv, "dv")
+        a.n_q, a.n_k, a.H, a.D = Tq, Tk, H, D
+        a.scale = float(scale) if scale is not None else D ** -0.5
+        a.relation = ATTN_CAUSAL if causal else ATTN_FULL
+        a.dtype, a.o_dtype = _dtype_code(q.dtype), _dtype_code(o.dtype)
+        a.grad_dtype = _dtype_code(gdt)
+        a.n_seq = (self.cu_q.numel() - 1) if self.cu_q is not None else 1
+        a.cu_seqlens_q = self.cu_q.data_ptr() if self.cu_q is not None else None
+        a.cu_seqlens_k = self.cu_k.data_ptr() if self.cu_k is not None else None
+        a.kernel = _KERNELS[kernel]
+        a.num_ctas = int(num_ctas)
+        lib = _abi.load()
+        need = lib.attn_bwd_workspace_bytes(ctypes.byref(a))
+        self.workspace = workspace if workspace is not None else _workspace(need, dev)
+        a.workspace = self.workspace.data_ptr()
+        a.workspace_bytes = self.workspace.numel() * self.workspace.element_size()
+        self.args = a
+        self._lib = lib
+
+    def _call(self, fn, name, stream):
+        s = stream if stream is not None else torch.cuda.current_stream()
+        check(fn(ctypes.byref(self.args), ctypes.c_void_p(s.cuda_stream)), name)
+
+    def preprocess(self, stream=None):
+        self._call(self._lib.attn_bwd_preprocess, "attn_bwd_preprocess", stream)
+
+    def dkdv(self, stream=None):
+        self._call(self._lib.attn_bwd_dkdv, "attn_bwd_dkdv", stream)
+
+    def dq_stage(self, stream=None):
+        self._call(self._lib.attn_bwd_dq, "attn_bwd_dq", stream)
+
+    def run(self, stream=None):
+        self._call(self._lib.attn_bwd, "attn_bwd", stream)
+        return self.dq, self.dk, self.dv
+
+    def selected_kernel(self) -> str:
+        """"tc" or "simt": the kernel family these arguments run."""
+        return _selected(self._lib.attn_bwd_selected_kernel(ctypes.byref(self.args)),
+                         "attn_bwd_selected_kernel")
+
+
+def fwd(q, k, v, *, causal: bool = False, scale: float | None = None, cu_seqlens_q=None,
+        cu_seqlens_k=None, out_dtype: torch.dtype | None = None, kernel: str = "auto",
+        num_ctas: int = 0):
+    """Attention forward.  Returns ``(o, lse)``; lse is (H, T_q) f32, natural log."""
+    return FwdCall(q, k, v, causal=causal, scale=scale, cu_seqlens_q=cu_seqlens_q,
+                   cu_seqlens_k=cu_seqlens_k, out_dtype=out_dtype, kernel=kernel,
+                   num_ctas=num_ctas).run()
+
+
+def bwd(q, k, v, o, lse, dout, *, causal: bool = False, scale: float | None = None,
+        cu_seqlens_q=None, cu_seqlens_k=None, grad_dtype: torch.dtype | None = None,
+        kernel: str = "auto", num_ctas: int = 0):
+    """Attention backward from the forward's o and lse.  Returns ``(dq, dk, dv)``."""
+    return BwdCall(q, k, v, o, lse, dout, causal=causal, scale=scale, cu_seqlens_q=cu_seqlens_q,
+                   cu_seqlens_k=cu_seqlens_k, grad_dtype=grad_dtype, kernel=kernel,
+                   num_ctas=num_ctas).run()

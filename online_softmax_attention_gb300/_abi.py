@@ -1,0 +1,125 @@
+"""ctypes mirror of include/attn.h and the loader of the in-tree library.
+
+Argument marshalling only: every step of the attention computation runs in
+the CUDA library.  Importing this module fails loudly when the library has
+not been built; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_lib", "libattn_gb300.so")
+
+ABI_VERSION = 1
+
+ATTN_OK, ATTN_EINVAL, ATTN_EUNSUPPORTED, ATTN_ECUDA, ATTN_ETIMEOUT, ATTN_EWORKSPACE = 0, -1, -2, -3, -4, -5
+ATTN_F16, ATTN_BF16, ATTN_F32 = 0, 1, 2
+ATTN_FULL, ATTN_CAUSAL = 0, 1
+ATTN_KERNEL_AUTO, ATTN_KERNEL_SIMT, ATTN_KERNEL_TC = 0, 1, 2
+
+# every symbol include/attn.h declares
+EXPORTS = (
+    "attn_abi_version", "attn_fwd_args_size", "attn_bwd_args_size",
+    "attn_fwd_workspace_bytes", "attn_bwd_workspace_bytes", "attn_fwd", "attn_bwd",
+    "attn_bwd_preprocess", "attn_bwd_dkdv", "attn_bwd_dq", "attn_fwd_simple",
+    "attn_device_status", "attn_launch_count", "attn_strerror", "attn_last_error_string",
+    "attn_fwd_selected_kernel", "attn_bwd_selected_kernel",
+)
+
+
+class AttnTensor(ctypes.Structure):
+    _fields_ = [("ptr", ctypes.c_void_p), ("stride_tok", ctypes.c_int64),
+                ("stride_head", ctypes.c_int64)]
+
+
+class FwdArgs(ctypes.Structure):
+    _fields_ = [
+        ("q", AttnTensor), ("k", AttnTensor), ("v", AttnTensor), ("o", AttnTensor),
+        ("lse", ctypes.c_void_p),
+        ("n_q", ctypes.c_int32), ("n_k", ctypes.c_int32), ("H", ctypes.c_int32), ("D", ctypes.c_int32),
+        ("scale", ctypes.c_float), ("relation", ctypes.c_int32), ("dtype", ctypes.c_int32),
+        ("o_dtype", ctypes.c_int32), ("n_seq", ctypes.c_int32),
+        ("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_k", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("kernel", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
+    ]
+
+
+class BwdArgs(ctypes.Structure):
+    _fields_ = [
+        ("q", AttnTensor), ("k", AttnTensor), ("v", AttnTensor), ("o", AttnTensor),
+        ("dout", AttnTensor), ("lse", ctypes.c_void_p),
+        ("dq", AttnTensor), ("dk", AttnTensor), ("dv", AttnTensor),
+        ("n_q", ctypes.c_int32), ("n_k", ctypes.c_int32), ("H", ctypes.c_int32), ("D", ctypes.c_int32),
+        ("scale", ctypes.c_float), ("relation", ctypes.c_int32), ("dtype", ctypes.c_int32),
+        ("o_dtype", ctypes.c_int32), ("grad_dtype", ctypes.c_int32), ("n_seq", ctypes.c_int32),
+        ("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_k", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("kernel", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
+    ]
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load the library (once).  Raises if it is missing or mismatched."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"CUDA attention library not built ({LIB_PATH} missing); run "
+            "`python -c 'import __graft_entry__ as g; g.build()'` or "
+            "`python online_softmax_attention_gb300/build.py`")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    fa, ba = ctypes.POINTER(FwdArgs), ctypes.POINTER(BwdArgs)
+    sigs = {
+        "attn_abi_version": (ctypes.c_int, []),
+        "attn_fwd_args_size": (sz, []),
+        "attn_bwd_args_size": (sz, []),
+        "attn_fwd_workspace_bytes": (sz, [fa]),
+        "attn_bwd_workspace_bytes": (sz, [ba]),
+        "attn_fwd": (ctypes.c_int, [fa, vp]),
+        "attn_bwd": (ctypes.c_int, [ba, vp]),
+        "attn_bwd_preprocess": (ctypes.c_int, [ba, vp]),
+        "attn_bwd_dkdv": (ctypes.c_int, [ba, vp]),
+        "attn_bwd_dq": (ctypes.c_int, [ba, vp]),
+        "attn_fwd_simple": (ctypes.c_int, [vp, vp, vp, vp, vp, i32, i32, i32, ctypes.c_float, i32,
+                                           vp, i32, i32, vp, sz, vp]),
+        "attn_device_status": (ctypes.c_int, [vp]),
+        "attn_fwd_selected_kernel": (ctypes.c_int, [fa]),
+        "attn_bwd_selected_kernel": (ctypes.c_int, [ba]),
+        "attn_launch_count": (ctypes.c_uint64, []),
+        "attn_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+        "attn_last_error_string": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if lib.attn_abi_version() != ABI_VERSION:
+        raise ImportError(f"libattn_gb300 ABI {lib.attn_abi_version()} != binding ABI {ABI_VERSION}")
+    if lib.attn_fwd_args_size() != ctypes.sizeof(FwdArgs) or \
+            lib.attn_bwd_args_size() != ctypes.sizeof(BwdArgs):
+        raise ImportError("libattn_gb300 struct layout does not match the binding")
+    _lib = lib
+    return lib
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        lib = load()
+        msg = lib.attn_strerror(code).decode()
+        if code == ATTN_ECUDA:
+            msg += ": " + lib.attn_last_error_string().decode()
+        super().__init__(f"{where} failed ({code}): {msg}")
+        self.code = code
+
+
+def check(code: int, where: str) -> None:
+    if code != ATTN_OK:
+        raise AttnError(code, where)

@@ -1,0 +1,385 @@
+// C ABI of the attention library: argument validation, workspace layout,
+// schedule preparation and kernel dispatch.  See include/attn.h for the
+// contract of each entry point.
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/attn.h"
+#include "internal.h"
+#include "tc.h"
+
+namespace attn {
+
+namespace {
+
+__device__ int g_status;  // first error reported by a kernel on this device
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int *g_status_ptr[kMaxDevices];
+int g_sm_count[kMaxDevices];
+std::atomic<uint64_t> g_launches{0};
+thread_local std::string g_last_error;
+
+int set_cuda_error(cudaError_t e) {
+    g_last_error = cudaGetErrorString(e);
+    return ATTN_ECUDA;
+}
+
+int current_device() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    return dev;
+}
+
+int *status_ptr() {
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<int *>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+long long watchdog_cycles() {
+    static long long v = [] {
+        const char *e = std::getenv("ATTN_WATCHDOG_CYCLES");
+        long long x = e ? std::atoll(e) : 0;
+        return x > 0 ? x : 4000000000LL;  // about 2 s at 2 GHz per bounded wait
+    }();
+    return v;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+size_t elem_size(int dt) { return dt == ATTN_F32 ? 4 : 2; }
+
+bool valid_dtype(int dt) { return dt == ATTN_F16 || dt == ATTN_BF16 || dt == ATTN_F32; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// A tensor view is usable when its pointer and row strides keep every
+// D-element row 16-byte aligned.
+bool valid_view(const attn_tensor &t, int dt, bool required) {
+    if (!t.ptr) return !required;
+    const int64_t es = (int64_t)elem_size(dt);
+    if (!aligned16(t.ptr)) return false;
+    if (t.stride_tok <= 0 || t.stride_head <= 0) return false;
+    return (t.stride_tok * es) % 16 == 0 && (t.stride_head * es) % 16 == 0;
+}
+
+// Which implementation runs: true = tcgen05 kernels.  `tc_ok` says whether
+// the tensor-core kernels cover the arguments.
+int choose_tc(int kernel, bool tc_ok, bool &use_tc) {
+    if (kernel == ATTN_KERNEL_SIMT) {
+        use_tc = false;
+        return ATTN_OK;
+    }
+    if (kernel == ATTN_KERNEL_TC) {
+        if (!tc_ok) return ATTN_EUNSUPPORTED;
+        use_tc = true;
+        return ATTN_OK;
+    }
+    if (kernel != ATTN_KERNEL_AUTO) return ATTN_EINVAL;
+    use_tc = tc_ok;
+    return ATTN_OK;
+}
+
+int check_common(int n_q, int n_k, int H, int D, int relation, int dtype, int n_seq,
+                 const int32_t *cu_q, const int32_t *cu_k, float scale) {
+    if (n_q < 0 || n_k < 0 || H < 1 || n_seq < 1) return ATTN_EINVAL;
+    if (!valid_dtype(dtype)) return ATTN_EINVAL;
+    if (relation != ATTN_FULL && relation != ATTN_CAUSAL) return ATTN_EINVAL;
+    if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return ATTN_EINVAL;
+    if ((cu_q == nullptr) != (cu_k == nullptr)) return ATTN_EINVAL;
+    if (!cu_q && n_seq != 1) return ATTN_EINVAL;
+    if (!cu_q && relation == ATTN_CAUSAL && n_q != n_k) return ATTN_EUNSUPPORTED;
+    if (D != 64 && D != 128) return ATTN_EUNSUPPORTED;
+    // work-item numbering is int32: H * (tiles + sequences) must fit
+    const int64_t items = (int64_t)H * ((int64_t)(n_q > n_k ? n_q : n_k) / kSimtBlock + n_seq + 1);
+    if (items >= (int64_t)1 << 31 || (int64_t)n_q * H >= (int64_t)1 << 31) return ATTN_EUNSUPPORTED;
+    return ATTN_OK;
+}
+
+size_t sched_bytes(int n_seq) { return align256(sizeof(int) * (size_t)(kSchedHeaderInts + n_seq + 1)); }
+
+Sched sched_at(void *base) {
+    int *p = static_cast<int *>(base);
+    return Sched{p, p + kSchedHeaderInts};
+}
+
+// ---- forward ---------------------------------------------------------------
+
+int build_fwd(const attn_fwd_args *a, FwdParams &p, bool &use_tc) {
+    if (!a) return ATTN_EINVAL;
+    int rc = check_common(a->n_q, a->n_k, a->H, a->D, a->relation, a->dtype, a->n_seq,
+                          a->cu_seqlens_q, a->cu_seqlens_k, a->scale);
+    if (rc) return rc;
+    if (a->o_dtype != a->dtype && a->o_dtype != ATTN_F32) return ATTN_EINVAL;
+    const bool any_q = a->n_q > 0, any_k = a->n_k > 0;
+    if (!valid_view(a->q, a->dtype, any_q) || !valid_view(a->o, a->o_dtype, any_q) ||
+        !valid_view(a->k, a->dtype, any_k) || !valid_view(a->v, a->dtype, any_k))
+        return ATTN_EINVAL;
+    if (!a->workspace || a->workspace_bytes < attn_fwd_workspace_bytes(a) ||
+        (reinterpret_cast<uintptr_t>(a->workspace) & 255))
+        return ATTN_EWORKSPACE;
+    std::memset(&p, 0, sizeof(p));
+    p.q = a->q.ptr; p.k = a->k.ptr; p.v = a->v.ptr; p.o = a->o.ptr; p.lse = a->lse;
+    p.q_st = a->q.stride_tok; p.q_sh = a->q.stride_head;
+    p.k_st = a->k.stride_tok; p.k_sh = a->k.stride_head;
+    p.v_st = a->v.stride_tok; p.v_sh = a->v.stride_head;
+    p.o_st = a->o.stride_tok; p.o_sh = a->o.stride_head;
+    p.n_q = a->n_q; p.n_k = a->n_k; p.H = a->H; p.D = a->D;
+    p.scale = a->scale;
+    p.scale_log2 = a->scale * 1.4426950408889634f;
+    p.causal = a->relation == ATTN_CAUSAL;
+    p.dtype = a->dtype; p.o_dtype = a->o_dtype;
+    p.n_seq = a->n_seq;
+    p.cu_q = a->cu_seqlens_q; p.cu_k = a->cu_seqlens_k;
+    p.sched = sched_at(a->workspace);
+    p.status = status_ptr();
+    p.watchdog_cycles = watchdog_cycles();
+    if (!p.status) return ATTN_ECUDA;
+    return choose_tc(a->kernel, tc_fwd_supported(p), use_tc);
+}
+
+// ---- backward --------------------------------------------------------------
+
+struct BwdLayout {
+    size_t kv, q, dr, total;
+};
+
+BwdLayout bwd_layout(int n_seq, int H, int n_q) {
+    BwdLayout L;
+    L.kv = 0;
+    L.q = sched_bytes(n_seq);
+    L.dr = L.q + sched_bytes(n_seq);
+    L.total = L.dr + align256(sizeof(float) * (size_t)H * (size_t)(n_q > 0 ? n_q : 1));
+    return L;
+}
+
+int build_bwd(const attn_bwd_args *a, BwdParams &p, bool &use_tc) {
+    if (!a) return ATTN_EINVAL;
+    int rc = check_common(a->n_q, a->n_k, a->H, a->D, a->relation, a->dtype, a->n_seq,
+                          a->cu_seqlens_q, a->cu_seqlens_k, a->scale);
+    if (rc) return rc;
+    if (a->o_dtype != a->dtype && a->o_dtype != ATTN_F32) return ATTN_EINVAL;
+    if (a->grad_dtype != a->dtype && a->grad_dtype != ATTN_F32) return ATTN_EINVAL;
+    const bool any_q = a->n_q > 0, any_k = a->n_k > 0;
+    if (!valid_view(a->q, a->dtype, any_q) || !valid_view(a->o, a->o_dtype, any_q) ||
+        !valid_view(a->dout, a->dtype, any_q) || !valid_view(a->dq, a->grad_dtype, any_q) ||
+        !valid_view(a->k, a->dtype, any_k) || !valid_view(a->v, a->dtype, any_k) ||
+        !valid_view(a->dk, a->grad_dtype, any_k) || !valid_view(a->dv, a->grad_dtype, any_k))
+        return ATTN_EINVAL;
+    if (any_q && !a->lse) return ATTN_EINVAL;
+    if (!a->workspace || a->workspace_bytes < attn_bwd_workspace_bytes(a) ||
+        (reinterpret_cast<uintptr_t>(a->workspace) & 255))
+        return ATTN_EWORKSPACE;
+    std::memset(&p, 0, sizeof(p));
+    p.q = a->q.ptr; p.k = a->k.ptr; p.v = a->v.ptr; p.o = a->o.ptr; p.dout = a->dout.ptr;
+    p.lse = a->lse; p.dq = a->dq.ptr; p.dk = a->dk.ptr; p.dv = a->dv.ptr;
+    p.q_st = a->q.stride_tok; p.q_sh = a->q.stride_head;
+    p.k_st = a->k.stride_tok; p.k_sh = a->k.stride_head;
+    p.v_st = a->v.stride_tok; p.v_sh = a->v.stride_head;
+    p.o_st = a->o.stride_tok; p.o_sh = a->o.stride_head;
+    p.do_st = a->dout.stride_tok; p.do_sh = a->dout.stride_head;
+    p.dq_st = a->dq.stride_tok; p.dq_sh = a->dq.stride_head;
+    p.dk_st = a->dk.stride_tok; p.dk_sh = a->dk.stride_head;
+    p.dv_st = a->dv.stride_tok; p.dv_sh = a->dv.stride_head;
+    p.n_q = a->n_q; p.n_k = a->n_k; p.H = a->H; p.D = a->D;
+    p.scale = a->scale;
+    p.scale_log2 = a->scale * 1.4426950408889634f;
+    p.causal = a->relation == ATTN_CAUSAL;
+    p.dtype = a->dtype; p.o_dtype = a->o_dtype; p.grad_dtype = a->grad_dtype;
+    p.n_seq = a->n_seq;
+    p.cu_q = a->cu_seqlens_q; p.cu_k = a->cu_seqlens_k;
+    const BwdLayout L = bwd_layout(a->n_seq, a->H, a->n_q);
+    char *ws = static_cast<char *>(a->workspace);
+    p.sched_kv = sched_at(ws + L.kv);
+    p.sched_q = sched_at(ws + L.q);
+    p.dr = reinterpret_cast<float *>(ws + L.dr);
+    p.status = status_ptr();
+    p.watchdog_cycles = watchdog_cycles();
+    if (!p.status) return ATTN_ECUDA;
+    return choose_tc(a->kernel, tc_bwd_supported(p), use_tc);
+}
+
+}  // namespace
+
+int sm_count() {
+    const int dev = current_device();
+    if (dev >= 0 && dev < kMaxDevices && g_sm_count[dev] > 0) return g_sm_count[dev];
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+    if (dev >= 0 && dev < kMaxDevices) g_sm_count[dev] = n;
+    return n;
+}
+
+void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+int attn_abi_version(void) { return ATTN_ABI_VERSION; }
+size_t attn_fwd_args_size(void) { return sizeof(attn_fwd_args); }
+size_t attn_bwd_args_size(void) { return sizeof(attn_bwd_args); }
+uint64_t attn_launch_count(void) { return g_launches.load(); }
+
+size_t attn_fwd_workspace_bytes(const attn_fwd_args *a) {
+    if (!a || a->n_seq < 1) return 0;
+    return sched_bytes(a->n_seq);
+}
+
+size_t attn_bwd_workspace_bytes(const attn_bwd_args *a) {
+    if (!a || a->n_seq < 1 || a->H < 1 || a->n_q < 0) return 0;
+    return bwd_layout(a->n_seq, a->H, a->n_q).total;
+}
+
+int attn_fwd(const attn_fwd_args *a, void *stream) {
+    FwdParams p;
+    bool use_tc = false;
+    int rc = build_fwd(a, p, use_tc);
+    if (rc) return rc;
+    if (a->n_q == 0) return ATTN_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int block = use_tc ? tc_fwd_block_rows(p) : kSimtBlock;
+    cudaError_t e = launch_prep(p.cu_q, p.cu_k, p.n_seq, p.n_q, p.n_k, p.H, block, p.causal, 0,
+                                p.sched, p.status, s);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    e = use_tc ? launch_fwd_tc(p, a->num_ctas, s) : launch_fwd_simt(p, a->num_ctas, s);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    return ATTN_OK;
+}
+
+int attn_bwd_preprocess(const attn_bwd_args *a, void *stream) {
+    BwdParams p;
+    bool use_tc = false;
+    int rc = build_bwd(a, p, use_tc);
+    if (rc) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int kv_block = use_tc ? tc_bwd_kv_block(p) : kSimtBlock;
+    const int q_block = use_tc ? tc_bwd_q_block(p) : kSimtBlock;
+    cudaError_t e = launch_prep(p.cu_q, p.cu_k, p.n_seq, p.n_q, p.n_k, p.H, kv_block, p.causal, 1,
+                                p.sched_kv, p.status, s);
+    if (e == cudaSuccess)
+        e = launch_prep(p.cu_q, p.cu_k, p.n_seq, p.n_q, p.n_k, p.H, q_block, p.causal, 0,
+                        p.sched_q, p.status, s);
+    if (e == cudaSuccess) e = launch_bwd_preprocess(p, s);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    return ATTN_OK;
+}
+
+int attn_bwd_dkdv(const attn_bwd_args *a, void *stream) {
+    BwdParams p;
+    bool use_tc = false;
+    int rc = build_bwd(a, p, use_tc);
+    if (rc) return rc;
+    if (a->n_k == 0) return ATTN_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = use_tc ? launch_bwd_dkdv_tc(p, a->num_ctas, s)
+                           : launch_bwd_dkdv_simt(p, a->num_ctas, s);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    return ATTN_OK;
+}
+
+int attn_bwd_dq(const attn_bwd_args *a, void *stream) {
+    BwdParams p;
+    bool use_tc = false;
+    int rc = build_bwd(a, p, use_tc);
+    if (rc) return rc;
+    if (a->n_q == 0) return ATTN_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = use_tc ? launch_bwd_dq_tc(p, a->num_ctas, s) : launch_bwd_dq_simt(p, a->num_ctas, s);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    return ATTN_OK;
+}
+
+int attn_bwd(const attn_bwd_args *a, void *stream) {
+    int rc = attn_bwd_preprocess(a, stream);
+    if (rc) return rc;
+    rc = attn_bwd_dkdv(a, stream);
+    if (rc) return rc;
+    return attn_bwd_dq(a, stream);
+}
+
+int attn_fwd_simple(const void *q, const void *k, const void *v, void *out, float *lse,
+                    int32_t N, int32_t H, int32_t D, float scale, int32_t relation,
+                    const int32_t *cu_seqlens, int32_t n_seq, int32_t dtype, void *workspace,
+                    size_t workspace_bytes, void *stream) {
+    attn_fwd_args a;
+    std::memset(&a, 0, sizeof(a));
+    const int64_t st = (int64_t)H * D;
+    a.q = attn_tensor{const_cast<void *>(q), st, D};
+    a.k = attn_tensor{const_cast<void *>(k), st, D};
+    a.v = attn_tensor{const_cast<void *>(v), st, D};
+    a.o = attn_tensor{out, st, D};
+    a.lse = lse;
+    a.n_q = a.n_k = N;
+    a.H = H;
+    a.D = D;
+    a.scale = scale;
+    a.relation = relation;
+    a.dtype = a.o_dtype = dtype;
+    a.n_seq = cu_seqlens ? n_seq : 1;
+    a.cu_seqlens_q = a.cu_seqlens_k = cu_seqlens;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    a.kernel = ATTN_KERNEL_AUTO;
+    return attn_fwd(&a, stream);
+}
+
+int attn_fwd_selected_kernel(const attn_fwd_args *a) {
+    FwdParams p;
+    bool use_tc = false;
+    const int rc = build_fwd(a, p, use_tc);
+    return rc ? rc : (use_tc ? ATTN_KERNEL_TC : ATTN_KERNEL_SIMT);
+}
+
+int attn_bwd_selected_kernel(const attn_bwd_args *a) {
+    BwdParams p;
+    bool use_tc = false;
+    const int rc = build_bwd(a, p, use_tc);
+    return rc ? rc : (use_tc ? ATTN_KERNEL_TC : ATTN_KERNEL_SIMT);
+}
+
+int attn_device_status(void *stream) {
+    int *sp = status_ptr();
+    if (!sp) return ATTN_ECUDA;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return set_cuda_error(e);
+    int v = 0;
+    e = cudaMemcpy(&v, sp, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    if (v != 0) {
+        const int zero = 0;
+        e = cudaMemcpy(sp, &zero, sizeof(int), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return set_cuda_error(e);
+    }
+    return v;
+}
+
+const char *attn_strerror(int code) {
+    switch (code) {
+    case ATTN_OK: return "success";
+    case ATTN_EINVAL: return "invalid argument";
+    case ATTN_EUNSUPPORTED: return "unsupported argument combination";
+    case ATTN_ECUDA: return "CUDA runtime error";
+    case ATTN_ETIMEOUT: return "device watchdog timeout";
+    case ATTN_EWORKSPACE: return "workspace missing, too small or misaligned";
+    default: return "unknown status";
+    }
+}
+
+const char *attn_last_error_string(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,240 @@
+// Forward attention on CUDA cores (FP32 FFMA), any input dtype.
+//
+// This is the f32-accurate path (f32 inputs are never rounded to a narrower
+// type) and the portable path for f16/bf16.  It runs the online-softmax block
+// recurrence of the OCANNL "Module Ir.Online_softmax" page (fourth bullet):
+// per query tile of 64 rows, a scan over key tiles of 64 keys keeps the row
+// max m and the rescaled sum l, accumulates U = sum p * v, and writes
+// O = U / l and lse = m + ln l after the last tile.  Keys past the end of the
+// sequence, and keys j > i under the causal relation, score -inf (the guarded
+// tail).  Scores are kept in the base-2 domain (s * scale * log2 e).
+//
+// Layout: 256 threads; thread (ty, tx) = (tid / 16, tid % 16) owns query rows
+// ty + 16 r and keys tx + 16 c (r, c < 4) of the score tile, and output
+// columns 64 g + 4 tx + e of its four rows.  Tiles are staged in shared memory
+// as f32 rows padded to D + 4 floats, which makes the 16-byte reads of a
+// quarter warp fall on distinct banks.
+#include "../../include/attn.h"
+#include "common.cuh"
+
+namespace attn {
+
+namespace {
+
+constexpr int BQ = kSimtBlock;  // query rows per work item
+constexpr int BK = 64;          // keys per tile
+constexpr int NT = 256;
+constexpr int LDP = BK + 4;
+
+template <int D>
+constexpr size_t fwd_smem_bytes() {
+    return sizeof(float) * (size_t)(BQ * (D + 4) + 2 * BK * (D + 4) + BQ * LDP);
+}
+
+// Stage rows [row0, row0 + 64) of a (tokens, heads, D) tensor into shared
+// memory as f32; rows at or beyond `nrows` are zero.
+template <typename T, int D>
+__device__ __forceinline__ void stage_tile(float *dst, const T *src, int64_t st, int row0,
+                                           int nrows) {
+    constexpr int LD = D + 4;
+    constexpr int CPR = D / 4;  // 4-element chunks per row
+    for (int c = threadIdx.x; c < 64 * CPR; c += NT) {
+        const int r = c / CPR, cc = c - r * CPR;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (row0 + r < nrows) x = load4(src + (int64_t)(row0 + r) * st + cc * 4);
+        *reinterpret_cast<float4 *>(dst + r * LD + cc * 4) = x;
+    }
+}
+
+template <typename Tin, typename Tout, int D>
+__global__ void __launch_bounds__(NT) fwd_simt_kernel(const FwdParams p) {
+    constexpr int LD = D + 4;
+    constexpr int NG = D / 64;  // column groups of 64 per thread row
+    extern __shared__ float4 smem4[];
+    float *sQ = reinterpret_cast<float *>(smem4);
+    float *sK = sQ + BQ * LD;
+    float *sV = sK + BK * LD;
+    float *sP = sV + BK * LD;
+    __shared__ int s_w;
+
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    const int total = p.sched.hdr[1];
+    const Tin *gq = static_cast<const Tin *>(p.q);
+    const Tin *gk = static_cast<const Tin *>(p.k);
+    const Tin *gv = static_cast<const Tin *>(p.v);
+    Tout *go = static_cast<Tout *>(p.o);
+
+    for (;;) {
+        if (tid == 0) s_w = atomicAdd(p.sched.hdr, 1);
+        __syncthreads();
+        const int w = s_w;
+        __syncthreads();
+        if (w >= total) break;
+        const WorkItem it = map_item(w, p.sched.prefix, p.n_seq, p.H, true);
+        int q_start, Lq, k_start, Lk;
+        seq_bounds(p.cu_q, p.n_q, it.b, q_start, Lq);
+        seq_bounds(p.cu_k, p.n_k, it.b, k_start, Lk);
+        const int row0 = it.t * BQ;
+        const int h = it.h;
+
+        stage_tile<Tin, D>(sQ, gq + (int64_t)q_start * p.q_st + (int64_t)h * p.q_sh, p.q_st, row0, Lq);
+
+        float m[4], l[4], acc[4][NG * 4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            m[r] = -INFINITY;
+            l[r] = 0.f;
+#pragma unroll
+            for (int e = 0; e < NG * 4; ++e) acc[r][e] = 0.f;
+        }
+        const int n_keys = p.causal ? min(Lk, row0 + BQ) : Lk;
+        const int n_tiles = (n_keys + BK - 1) / BK;
+        const Tin *kbase = gk + (int64_t)k_start * p.k_st + (int64_t)h * p.k_sh;
+        const Tin *vbase = gv + (int64_t)k_start * p.v_st + (int64_t)h * p.v_sh;
+
+        for (int kt = 0; kt < n_tiles; ++kt) {
+            const int key0 = kt * BK;
+            __syncthreads();  // previous tile's sK / sV / sP no longer read
+            stage_tile<Tin, D>(sK, kbase, p.k_st, key0, Lk);
+            stage_tile<Tin, D>(sV, vbase, p.v_st, key0, Lk);
+            __syncthreads();
+
+            // score micro-tile: rows ty + 16 r, keys tx + 16 c
+            float s[4][4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) s[r][c] = 0.f;
+#pragma unroll 4
+            for (int d = 0; d < D; d += 4) {
+                float4 a[4], b[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) a[r] = *reinterpret_cast<const float4 *>(sQ + (ty + 16 * r) * LD + d);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) b[c] = *reinterpret_cast<const float4 *>(sK + (tx + 16 * c) * LD + d);
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        s[r][c] = fmaf(a[r].x, b[c].x, s[r][c]);
+                        s[r][c] = fmaf(a[r].y, b[c].y, s[r][c]);
+                        s[r][c] = fmaf(a[r].z, b[c].z, s[r][c]);
+                        s[r][c] = fmaf(a[r].w, b[c].w, s[r][c]);
+                    }
+            }
+
+            // scale into the base-2 domain, mask, online softmax update
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int row = row0 + ty + 16 * r;
+                float mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int key = key0 + tx + 16 * c;
+                    const bool ok = key < Lk && (!p.causal || key <= row);
+                    s[r][c] = ok ? s[r][c] * p.scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, s[r][c]);
+                }
+#pragma unroll
+                for (int o = 1; o < 16; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                const float m_new = fmaxf(m[r], mx);
+                const float m_use = (m_new == -INFINITY) ? 0.f : m_new;  // row with nothing admitted yet
+                const float alpha = exp2_approx(m[r] - m_use);
+                float rs = 0.f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float pv = exp2_approx(s[r][c] - m_use);
+                    rs += pv;
+                    sP[(ty + 16 * r) * LDP + tx + 16 * c] = pv;
+                }
+#pragma unroll
+                for (int o = 1; o < 16; o <<= 1) rs += __shfl_xor_sync(0xffffffffu, rs, o);
+                l[r] = alpha * l[r] + rs;
+                m[r] = m_new;
+#pragma unroll
+                for (int e = 0; e < NG * 4; ++e) acc[r][e] *= alpha;
+            }
+            __syncthreads();
+
+            // U += P V
+#pragma unroll 2
+            for (int j = 0; j < BK; j += 4) {
+                float4 pr[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) pr[r] = *reinterpret_cast<const float4 *>(sP + (ty + 16 * r) * LDP + j);
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+#pragma unroll
+                    for (int g = 0; g < NG; ++g) {
+                        const float4 vv = *reinterpret_cast<const float4 *>(sV + (j + jj) * LD + 64 * g + 4 * tx);
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            const float pj = jj == 0 ? pr[r].x : jj == 1 ? pr[r].y : jj == 2 ? pr[r].z : pr[r].w;
+                            acc[r][4 * g + 0] = fmaf(pj, vv.x, acc[r][4 * g + 0]);
+                            acc[r][4 * g + 1] = fmaf(pj, vv.y, acc[r][4 * g + 1]);
+                            acc[r][4 * g + 2] = fmaf(pj, vv.z, acc[r][4 * g + 2]);
+                            acc[r][4 * g + 3] = fmaf(pj, vv.w, acc[r][4 * g + 3]);
+                        }
+                    }
+                }
+            }
+        }
+
+        // epilogue: O = U / l, lse = m ln 2 + ln l
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int row = row0 + ty + 16 * r;
+            if (row >= Lq) continue;
+            const float inv = l[r] > 0.f ? 1.f / l[r] : 0.f;
+            Tout *orow = go + (int64_t)(q_start + row) * p.o_st + (int64_t)h * p.o_sh;
+#pragma unroll
+            for (int g = 0; g < NG; ++g)
+                store4(orow + 64 * g + 4 * tx,
+                       make_float4(acc[r][4 * g] * inv, acc[r][4 * g + 1] * inv,
+                                   acc[r][4 * g + 2] * inv, acc[r][4 * g + 3] * inv));
+            if (tx == 0 && p.lse)
+                p.lse[(int64_t)h * p.n_q + q_start + row] =
+                    l[r] > 0.f ? m[r] * kLn2 + logf(l[r]) : -INFINITY;
+        }
+    }
+}
+
+template <typename Tin, typename Tout, int D>
+cudaError_t launch_typed(const FwdParams &p, int num_ctas, cudaStream_t s) {
+    auto kern = fwd_simt_kernel<Tin, Tout, D>;
+    const size_t smem = fwd_smem_bytes<D>();
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (num_ctas <= 0) {
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NT, smem);
+        if (e != cudaSuccess) return e;
+        num_ctas = sm_count() * (per_sm > 0 ? per_sm : 1);
+    }
+    kern<<<num_ctas, NT, smem, s>>>(p);
+    count_launch();
+    return cudaGetLastError();
+}
+
+template <typename Tin, int D>
+cudaError_t launch_out(const FwdParams &p, int num_ctas, cudaStream_t s) {
+    if (p.o_dtype == ATTN_F32) return launch_typed<Tin, float, D>(p, num_ctas, s);
+    return launch_typed<Tin, Tin, D>(p, num_ctas, s);
+}
+
+template <int D>
+cudaError_t launch_d(const FwdParams &p, int num_ctas, cudaStream_t s) {
+    switch (p.dtype) {
+    case ATTN_F16: return launch_out<__half, D>(p, num_ctas, s);
+    case ATTN_BF16: return launch_out<__nv_bfloat16, D>(p, num_ctas, s);
+    default: return launch_typed<float, float, D>(p, num_ctas, s);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_simt(const FwdParams &p, int num_ctas, cudaStream_t s) {
+    return p.D == 64 ? launch_d<64>(p, num_ctas, s) : launch_d<128>(p, num_ctas, s);
+}
+
+}  // namespace attn

@@ -1,0 +1,132 @@
+"""The C-ABI library loads, exports what include/attn.h declares, and rejects
+bad arguments before touching the GPU (CPU only: no kernel is launched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import online_softmax_attention_gb300 as attn
+from online_softmax_attention_gb300 import _abi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "attn.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"ATTN_API\s+[\w\s\*]+?\b(attn_\w+)\s*\(", text)))
+
+
+def test_library_loads_and_abi_matches():
+    lib = _abi.load()
+    assert lib.attn_abi_version() == _abi.ABI_VERSION
+    assert lib.attn_fwd_args_size() == ctypes.sizeof(_abi.FwdArgs)
+    assert lib.attn_bwd_args_size() == ctypes.sizeof(_abi.BwdArgs)
+
+
+def test_every_declared_symbol_is_exported():
+    names = _declared()
+    assert len(names) >= 15
+    lib = _abi.load()
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/attn.h but not exported"
+    assert set(names) == set(_abi.EXPORTS)
+
+
+def test_strerror_texts():
+    lib = _abi.load()
+    for code in (0, -1, -2, -3, -4, -5):
+        assert lib.attn_strerror(code)
+    assert lib.attn_strerror(-99) == b"unknown status"
+
+
+FAKE = 1 << 20  # 256-byte aligned host integer; never dereferenced by these calls
+
+
+def _fwd_args(**kw):
+    a = _abi.FwdArgs()
+    H, D, N = kw.get("H", 2), kw.get("D", 64), kw.get("N", 256)
+    es = 4 if kw.get("dtype", _abi.ATTN_F16) == _abi.ATTN_F32 else 2
+    for name in ("q", "k", "v", "o"):
+        setattr(a, name, _abi.AttnTensor(FAKE, H * D, D))
+    a.lse = FAKE
+    a.n_q = kw.get("n_q", N)
+    a.n_k = kw.get("n_k", N)
+    a.H, a.D = H, D
+    a.scale = D ** -0.5
+    a.relation = kw.get("relation", _abi.ATTN_CAUSAL)
+    a.dtype = kw.get("dtype", _abi.ATTN_F16)
+    a.o_dtype = kw.get("o_dtype", a.dtype)
+    a.n_seq = 1
+    a.kernel = kw.get("kernel", _abi.ATTN_KERNEL_AUTO)
+    lib = _abi.load()
+    a.workspace = FAKE
+    a.workspace_bytes = kw.get("ws", lib.attn_fwd_workspace_bytes(ctypes.byref(a)))
+    del es
+    return a
+
+
+@pytest.mark.parametrize("kw,code", [
+    ({"D": 96}, _abi.ATTN_EUNSUPPORTED),
+    ({"D": 256}, _abi.ATTN_EUNSUPPORTED),
+    ({"n_q": 256, "n_k": 128}, _abi.ATTN_EUNSUPPORTED),      # causal needs equal lengths
+    ({"relation": 7}, _abi.ATTN_EINVAL),
+    ({"dtype": 9}, _abi.ATTN_EINVAL),
+    ({"o_dtype": _abi.ATTN_BF16}, _abi.ATTN_EINVAL),         # fp16 in, bf16 out
+    ({"ws": 16}, _abi.ATTN_EWORKSPACE),
+    ({"kernel": 42}, None),
+    ({"dtype": _abi.ATTN_F32, "kernel": _abi.ATTN_KERNEL_TC}, None),
+])
+def test_forward_argument_validation(kw, code):
+    lib = _abi.load()
+    a = _fwd_args(**kw)
+    rc = lib.attn_fwd(ctypes.byref(a), None)
+    if code is None:
+        assert rc in (_abi.ATTN_EINVAL, _abi.ATTN_EUNSUPPORTED, _abi.ATTN_ECUDA)
+    else:
+        assert rc == code
+
+
+def test_forward_rejects_misaligned_strides_and_null_pointers():
+    lib = _abi.load()
+    a = _fwd_args()
+    a.q = _abi.AttnTensor(FAKE, 2 * 64 + 1, 64)
+    assert lib.attn_fwd(ctypes.byref(a), None) == _abi.ATTN_EINVAL
+    a = _fwd_args()
+    a.k = _abi.AttnTensor(FAKE + 2, 128, 64)
+    assert lib.attn_fwd(ctypes.byref(a), None) == _abi.ATTN_EINVAL
+    a = _fwd_args()
+    a.v = _abi.AttnTensor(None, 128, 64)
+    assert lib.attn_fwd(ctypes.byref(a), None) == _abi.ATTN_EINVAL
+    assert lib.attn_fwd(None, None) == _abi.ATTN_EINVAL
+
+
+def test_cu_seqlens_must_come_in_pairs():
+    lib = _abi.load()
+    a = _fwd_args()
+    a.cu_seqlens_q = FAKE
+    assert lib.attn_fwd(ctypes.byref(a), None) == _abi.ATTN_EINVAL
+    a = _fwd_args()
+    a.n_seq = 3  # several sequences need offsets
+    assert lib.attn_fwd(ctypes.byref(a), None) == _abi.ATTN_EINVAL
+
+
+def test_workspace_sizes_grow_with_sequences_and_rows():
+    lib = _abi.load()
+    a = _fwd_args()
+    small = lib.attn_fwd_workspace_bytes(ctypes.byref(a))
+    a.n_seq = 10000
+    assert lib.attn_fwd_workspace_bytes(ctypes.byref(a)) > small
+    b = _abi.BwdArgs()
+    b.n_seq, b.H, b.n_q = 1, 32, 32768
+    need = lib.attn_bwd_workspace_bytes(ctypes.byref(b))
+    assert need >= 32 * 32768 * 4  # Dr is (H, n_q) f32
+    assert need % 256 == 0
+
+
+def test_binding_fails_loudly_without_cuda_tensors():
+    import torch
+    q = torch.zeros(8, 1, 64, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        attn.fwd(q, q, q)
