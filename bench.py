@@ -194,6 +194,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=4,
+                    help="sequences of N=8192 (4 = the benchmark workload; fewer for profiling)")
+    ap.add_argument("--skip-e2e", action="store_true", help="profiling runs: no host-buffer leg")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -221,6 +224,9 @@ def main():
             dist.barrier()
 
     w = attn_inputs.WORKLOADS[WORKLOAD]
+    if args.batch != w.batch:
+        import dataclasses
+        w = dataclasses.replace(w, batch=args.batch)
     x = attn_inputs.make_workload(w)
     lq, lk = x["lengths_q"], x["lengths_k"]
     fwd_flops = attention_flops(lq, lk, w.H, w.D, w.causal)
@@ -228,7 +234,7 @@ def main():
     step_flops = fwd_flops + bwd_flops
 
     q, k, v, dO = (x[n].to(dev) for n in ("q", "k", "v", "dO"))
-    cu = x["cu_seqlens_q"].to(dev)
+    cu = x["cu_seqlens_q"].to(dev) if x["cu_seqlens_q"] is not None else None
     fcall = attn.FwdCall(q, k, v, causal=True, cu_seqlens_q=cu, out_dtype=torch.float32,
                          kernel=args.kernel)
     bcall = attn.BwdCall(q, k, v, fcall.o, fcall.lse, dO, causal=True, cu_seqlens_q=cu,
@@ -295,6 +301,8 @@ def main():
     d2h = sum(t.numel() * t.element_size() for t in outs_host.values())
 
     def e2e_step():
+        if args.skip_e2e:
+            return
         for n, t in pin.items():
             dev_in[n].copy_(t, non_blocking=True)
         fcall.run(stream)
@@ -327,14 +335,15 @@ def main():
     # not algorithmic work); preprocess is HBM-bound (reads O f32 and dO bf16).
     stage_flops = {"fwd": fwd_flops, "bwd_dkdv": 2.0 * fwd_flops, "bwd_dq": 0.5 * fwd_flops}
     dominant = max(("fwd", "bwd_dkdv", "bwd_dq"), key=lambda s: stage_ms[s])
-    kernel_files = {"fwd": ["online_softmax_attention_gb300/csrc/fwd_simt.cu"],
-                    "bwd_dkdv": ["online_softmax_attention_gb300/csrc/bwd_simt.cu"],
-                    "bwd_dq": ["online_softmax_attention_gb300/csrc/bwd_simt.cu"]}
-    using_tc = fcall.selected_kernel() == "tc" and bcall.selected_kernel() == "tc"
-    if using_tc:
-        kernel_files = {"fwd": ["online_softmax_attention_gb300/csrc/fwd_tc.cu"],
-                        "bwd_dkdv": ["online_softmax_attention_gb300/csrc/bwd_tc.cu"],
-                        "bwd_dq": ["online_softmax_attention_gb300/csrc/bwd_tc.cu"]}
+    family = {"fwd": fcall.selected_kernel(), "bwd_dkdv": bcall.selected_kernel(),
+              "bwd_dq": bcall.selected_kernel()}
+    kernel_files = {("fwd", "simt"): ["online_softmax_attention_gb300/csrc/fwd_simt.cu"],
+                    ("fwd", "tc"): ["online_softmax_attention_gb300/csrc/fwd_tc.cu"],
+                    ("bwd_dkdv", "simt"): ["online_softmax_attention_gb300/csrc/bwd_simt.cu"],
+                    ("bwd_dq", "simt"): ["online_softmax_attention_gb300/csrc/bwd_simt.cu"],
+                    ("bwd_dkdv", "tc"): ["online_softmax_attention_gb300/csrc/bwd_tc.cu"],
+                    ("bwd_dq", "tc"): ["online_softmax_attention_gb300/csrc/bwd_tc.cu"]}
+    using_tc = family[dominant] == "tc"
     achieved = stage_flops[dominant] / (stage_ms[dominant] * 1e-3) / 1e12
     if using_tc:
         peak, bound, punit = peaks["bf16_tflops_sustained"], "tensor", "TFLOP/s"
@@ -345,7 +354,7 @@ def main():
         peak = sms * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
         bound, punit = "alu", "TFLOP/s"
         peak_note = f"FP32 FFMA: {sms} SMs x 128 lanes x 2 FLOP x {peaks['sm_max_mhz']:.0f} MHz"
-    src = [p for p in kernel_files[dominant] if os.path.exists(os.path.join(ROOT, p))]
+    src = [p for p in kernel_files[(dominant, family[dominant])] if os.path.exists(os.path.join(ROOT, p))]
     traffic = recorded_traffic(dominant, source_hash(src)) if src else None
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": punit,
                 "frac": achieved / peak, "traffic": traffic, "kernel": dominant,
@@ -359,9 +368,9 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "batch": 4, "seq_len": 8192, "heads": 32, "head_dim": 128,
+        "config": {"workload": WORKLOAD if w.batch == 4 else f"{WORKLOAD} (batch {w.batch})", "batch": w.batch, "seq_len": 8192, "heads": 32, "head_dim": 128,
                    "relation": "causal", "o_dtype": "f32", "grad_dtype": "bf16",
-                   "kernel": "tc" if using_tc else "simt",
+                   "kernels": family,
                    "l2": "no flush: each input tensor is 268 MB, larger than the 129 MB L2",
                    "parallelism": f"replicas x{world}"},
         "breakdown": {"fwd_ms": stage_ms["fwd"], "bwd_ms": bwd_ms,
@@ -374,6 +383,8 @@ def main():
         "gpu_launches": launches,
         "clocks": clk.summary(),
     }
+    if args.skip_e2e:
+        line["e2e"] = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = time_oracle_sample(x, w)
     else:

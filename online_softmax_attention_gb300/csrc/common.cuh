@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/attn.h"
 #include "internal.h"
 
 namespace attn {

@@ -1,0 +1,579 @@
+// Forward attention on the sm_103a tensor cores (tcgen05 + TMEM + TMA), for
+// f16 / bf16 inputs, D in {64, 128}.
+//
+// The online-softmax block recurrence of the OCANNL "Module Ir.Online_softmax"
+// page (fourth bullet) -- per query row a scan over key blocks carrying the
+// running max m and rescaled sum l, the numerator U accumulated with p * v,
+// O = U / l after the last block, -inf padding past the sequence end -- mapped
+// onto one GB300 SM as follows.
+//
+// Work item: 256 query rows of one (sequence, head), split in two 128-row
+// tiles (t = 0, 1) that ping-pong between the tensor core and the softmax
+// warps.  Items are taken from a global counter (persistent grid, one CTA per
+// SM) and broadcast to the warp roles through a two-slot shared ring.
+//
+// Warp roles (12 warps):
+//   warp 0      TMA producer: Q tiles, then K_j, V_j tiles into a ring of
+//               shared-memory slots (128-byte swizzle, 64-column boxes).
+//   warp 1      MMA issuer (one thread): S_t = Q_t K_j^T into TMEM, and
+//               U_t += P_t V_j with P_t read from TMEM (it overwrites S_t).
+//               Issue order PV_j(0), S_{j+1}(0), PV_j(1), S_{j+1}(1) keeps the
+//               tensor core busy while the other tile's softmax runs.
+//   warps 4-7   softmax of tile 0, warps 8-11 softmax of tile 1: thread =
+//               query row = TMEM lane.  Loads S (f32) from TMEM, masks the
+//               causal diagonal / sequence tail with -inf, updates m and l in
+//               the base-2 domain, writes P = 2^(s*scale*log2e - m) as packed
+//               16-bit pairs into TMEM, and after the last block normalises
+//               U and stores O and lse.
+// The row max is refreshed (and U, l rescaled) only when it grows by more than
+// 2^8; otherwise the stale max is kept, which leaves O = U / l exact.
+//
+// TMEM (512 columns): S_0 / P_0 at [0, 128), S_1 / P_1 at [128, 256),
+// U_0 at [256, 256 + D), U_1 at [256 + D, 256 + 2D).
+//
+// Every mbarrier wait is bounded (sm100::mbar_wait); on expiry the CTA stops
+// issuing work, drains its outstanding TMA loads, frees TMEM and exits, and
+// the status word reads ATTN_ETIMEOUT.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "sm100.cuh"
+#include "tc.h"
+
+namespace attn {
+
+namespace {
+
+using namespace sm100;
+
+constexpr int BM = 128;        // query rows per tile (tcgen05 M)
+constexpr int BN = 128;        // keys per KV tile
+constexpr int NQT = 2;         // query tiles per work item
+constexpr int kItemRows = NQT * BM;
+constexpr int kThreads = 384;
+constexpr int kSchedConsumers = 1 + 8;  // MMA thread + one lane per softmax warp
+// Register split: the block is launched at 168 registers per thread (384
+// threads); warpgroup 0 (TMA, MMA, two idle warps) gives registers to the two
+// softmax warpgroups.  Chosen per D from ptxas spill reports.
+constexpr float kRescaleThreshold = 8.f;  // log2 units
+
+template <int D>
+struct Cfg {
+    static constexpr int kBoxes = D / 64;
+    static constexpr int kBoxBytes = 128 * 64 * 2;
+    static constexpr int kTileBytes = 128 * D * 2;
+    static constexpr int kStages = D == 128 ? 4 : 8;
+    static constexpr int kSmemBytes = (NQT + kStages) * kTileBytes + 1024;
+    static constexpr int kRegsProducer = D == 128 ? 88 : 72;
+    static constexpr int kRegsSoftmax = D == 128 ? 208 : 216;
+    static_assert(128 * kRegsProducer + 256 * kRegsSoftmax <= kThreads * 168, "register split");
+};
+
+struct TcFwdArgs {
+    CUtensorMap tq, tk, tv;
+    FwdParams p;
+};
+
+struct __align__(8) FwdBars {
+    uint64_t q_full[NQT], q_empty[NQT];
+    uint64_t kv_full[8], kv_empty[8];
+    uint64_t s_full[NQT], p_full[NQT], o_done[NQT], o_free[NQT];
+    uint64_t sched_full[2], sched_empty[2];
+};
+
+struct ItemInfo {
+    int q_start, Lq, k_start, Lk, h, row0;
+    int n[NQT];  // key tiles each query tile scans
+    int nkv;     // max over the tiles
+};
+
+__device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+__device__ __forceinline__ ItemInfo item_info(const FwdParams &p, int w) {
+    const WorkItem it = map_item(w, p.sched.prefix, p.n_seq, p.H, true);
+    ItemInfo f;
+    seq_bounds(p.cu_q, p.n_q, it.b, f.q_start, f.Lq);
+    seq_bounds(p.cu_k, p.n_k, it.b, f.k_start, f.Lk);
+    f.h = it.h;
+    f.row0 = it.t * kItemRows;
+    f.nkv = 0;
+#pragma unroll
+    for (int t = 0; t < NQT; ++t) {
+        const int r0 = f.row0 + BM * t;
+        int n = 0;
+        if (r0 < f.Lq) n = p.causal ? cdiv(min(f.Lk, r0 + BM), BN) : cdiv(f.Lk, BN);
+        f.n[t] = n;
+        f.nkv = max(f.nkv, n);
+    }
+    return f;
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
+    uint32_t u;
+    if (bf16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        u = *reinterpret_cast<uint32_t *>(&v);
+    } else {
+        __half2 v = __floats2half2_rn(lo, hi);
+        u = *reinterpret_cast<uint32_t *>(&v);
+    }
+    return u;
+}
+
+// Bounded wait for outstanding TMA writes before the CTA exits after an abort.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long long budget) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > budget) return;
+    }
+}
+
+// ---- warp 0: TMA producer ------------------------------------------------------
+
+template <int D>
+__device__ void producer(const TcFwdArgs &a, FwdBars &bars, int *sched_item, uint32_t sQ, uint32_t sKV,
+                         const Watchdog &wd) {
+    using C = Cfg<D>;
+    const FwdParams &p = a.p;
+    const int total = p.sched.hdr[1];
+    uint32_t kv_i = 0;
+    uint32_t q_uses[NQT] = {0, 0};
+    bool q_pending[NQT] = {false, false};
+    for (int i = 0;; ++i) {
+        const int slot = i & 1;
+        if (!mbar_wait(smem_u32(&bars.sched_empty[slot]), ((i >> 1) & 1) ^ 1, wd)) break;
+        const int w = atomicAdd(p.sched.hdr, 1);
+        sched_item[slot] = w;
+        mbar_arrive(smem_u32(&bars.sched_full[slot]));
+        if (w >= total) break;
+        const ItemInfo f = item_info(p, w);
+        bool ok = true;
+#pragma unroll
+        for (int t = 0; t < NQT; ++t) {
+            if (!ok) break;
+            if (f.n[t] == 0) continue;
+            ok = mbar_wait(smem_u32(&bars.q_empty[t]), (q_uses[t] & 1) ^ 1, wd);
+            if (!ok) break;
+            const uint32_t bar = smem_u32(&bars.q_full[t]);
+            mbar_expect_tx(bar, C::kTileBytes);
+#pragma unroll
+            for (int g = 0; g < C::kBoxes; ++g)
+                tma_load_3d(sQ + t * C::kTileBytes + g * C::kBoxBytes, &a.tq, 64 * g,
+                            f.q_start + f.row0 + BM * t, f.h, bar);
+            ++q_uses[t];
+            q_pending[t] = true;
+        }
+        if (!ok) break;
+        for (int j = 0; j < f.nkv && ok; ++j) {
+#pragma unroll
+            for (int kv = 0; kv < 2; ++kv) {
+                const uint32_t s = kv_i % C::kStages;
+                ok = mbar_wait(smem_u32(&bars.kv_empty[s]), ((kv_i / C::kStages) & 1) ^ 1, wd);
+                if (!ok) break;
+                const uint32_t bar = smem_u32(&bars.kv_full[s]);
+                mbar_expect_tx(bar, C::kTileBytes);
+#pragma unroll
+                for (int g = 0; g < C::kBoxes; ++g)
+                    tma_load_3d(sKV + s * C::kTileBytes + g * C::kBoxBytes, kv ? &a.tv : &a.tk, 64 * g,
+                                f.k_start + BN * j, f.h, bar);
+                ++kv_i;
+            }
+        }
+        if (!ok) break;
+    }
+    if (aborting(wd)) {
+        // the newest load of every slot may still be landing in shared memory
+        const long long budget = wd.budget;
+        for (uint32_t k = kv_i > (uint32_t)C::kStages ? kv_i - C::kStages : 0; k < kv_i; ++k)
+            drain_wait(smem_u32(&bars.kv_full[k % C::kStages]), (k / C::kStages) & 1, budget);
+#pragma unroll
+        for (int t = 0; t < NQT; ++t)
+            if (q_pending[t]) drain_wait(smem_u32(&bars.q_full[t]), (q_uses[t] - 1) & 1, budget);
+    }
+}
+
+// ---- warp 1: MMA issuer ----------------------------------------------------------
+
+template <int D, bool kBF16>
+__device__ void mma_issuer(const TcFwdArgs &a, FwdBars &bars, const int *sched_item, uint32_t sQ,
+                           uint32_t sKV, uint32_t tmem, const Watchdog &wd) {
+    using C = Cfg<D>;
+    const FwdParams &p = a.p;
+    const int total = p.sched.hdr[1];
+    constexpr uint32_t idS = idesc_f16(kBF16, BM, BN, 0);
+    constexpr uint32_t idO = idesc_f16(kBF16, BM, D, 1);
+    uint32_t kv_i = 0, q_cnt[NQT] = {0, 0}, p_cnt[NQT] = {0, 0}, of_cnt[NQT] = {0, 0};
+
+    // S_t = Q_t K^T over D in steps of 16 (32 bytes inside a 128-byte swizzle row)
+    auto issue_s = [&](int t, uint32_t kslot) {
+        const uint32_t qa = sQ + t * C::kTileBytes, ka = sKV + kslot * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+            mma_ss(tmem + BN * t, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idS,
+                   kk > 0);
+        }
+        tc_commit(smem_u32(&bars.s_full[t]));
+    };
+    // U_t (+)= P_t V over the 128 keys in steps of 16 (8 TMEM columns of P)
+    auto issue_pv = [&](int t, uint32_t vslot, bool acc) {
+        const uint32_t va = sKV + vslot * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(tmem + 256 + D * t, tmem + BN * t + 8 * kk, sdesc_sw128(va + kk * 2048, C::kBoxBytes, 1024),
+                   idO, acc || kk > 0);
+    };
+
+    for (int i = 0;; ++i) {
+        const int slot = i & 1;
+        if (!mbar_wait(smem_u32(&bars.sched_full[slot]), (i >> 1) & 1, wd)) return;
+        const int w = sched_item[slot];
+        mbar_arrive(smem_u32(&bars.sched_empty[slot]));
+        if (w >= total) return;
+        const ItemInfo f = item_info(p, w);
+        if (f.nkv == 0) continue;
+#pragma unroll
+        for (int t = 0; t < NQT; ++t) {
+            if (f.n[t] == 0) continue;
+            if (!mbar_wait(smem_u32(&bars.q_full[t]), q_cnt[t] & 1, wd)) return;
+            ++q_cnt[t];
+        }
+        // K_0
+        uint32_t ks = kv_i % C::kStages;
+        if (!mbar_wait(smem_u32(&bars.kv_full[ks]), (kv_i / C::kStages) & 1, wd)) return;
+        ++kv_i;
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < NQT; ++t) {
+            if (f.n[t] == 0) continue;
+            issue_s(t, ks);
+            if (f.n[t] == 1) tc_commit(smem_u32(&bars.q_empty[t]));
+        }
+        tc_commit(smem_u32(&bars.kv_empty[ks]));
+
+        for (int j = 0; j < f.nkv; ++j) {
+            const uint32_t vs = kv_i % C::kStages;
+            if (!mbar_wait(smem_u32(&bars.kv_full[vs]), (kv_i / C::kStages) & 1, wd)) return;
+            ++kv_i;
+            bool have_next_k = false;
+            uint32_t nks = 0;
+#pragma unroll
+            for (int t = 0; t < NQT; ++t) {
+                if (j >= f.n[t]) continue;
+                if (!mbar_wait(smem_u32(&bars.p_full[t]), p_cnt[t] & 1, wd)) return;
+                ++p_cnt[t];
+                if (j == 0) {
+                    // the previous item's epilogue of this tile has read U_t
+                    if (!mbar_wait(smem_u32(&bars.o_free[t]), (of_cnt[t] & 1) ^ 1, wd)) return;
+                    ++of_cnt[t];
+                }
+                tc_fence_after();
+                issue_pv(t, vs, j > 0);
+                if (j == f.n[t] - 1) tc_commit(smem_u32(&bars.o_done[t]));
+                if (j + 1 < f.n[t]) {
+                    if (!have_next_k) {
+                        nks = kv_i % C::kStages;
+                        if (!mbar_wait(smem_u32(&bars.kv_full[nks]), (kv_i / C::kStages) & 1, wd)) return;
+                        ++kv_i;
+                        have_next_k = true;
+                        tc_fence_after();
+                    }
+                    issue_s(t, nks);
+                    if (j + 1 == f.n[t] - 1) tc_commit(smem_u32(&bars.q_empty[t]));
+                }
+            }
+            tc_commit(smem_u32(&bars.kv_empty[vs]));
+            if (have_next_k) tc_commit(smem_u32(&bars.kv_empty[nks]));
+        }
+    }
+}
+
+// ---- warps 4-11: softmax and epilogue ------------------------------------------
+
+template <int D, bool kBF16, typename Tout>
+__device__ void softmax_wg(const TcFwdArgs &a, FwdBars &bars, const int *sched_item, uint32_t tmem,
+                           const Watchdog &wd) {
+    const FwdParams &p = a.p;
+    const int total = p.sched.hdr[1];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = (warp - 4) >> 2;    // query tile of this warpgroup
+    const int quarter = warp & 3;     // TMEM lane quarter this warp may access
+    const int lrow = 32 * quarter + lane;
+    const uint32_t s_addr = tmem_addr(tmem, 32 * quarter, BN * t);
+    const uint32_t o_addr = tmem_addr(tmem, 32 * quarter, 256 + D * t);
+    // a negative scale is applied as |scale| to negated scores
+    const float sl2 = fabsf(p.scale_log2);
+    const bool neg = p.scale_log2 < 0.f;
+    uint32_t s_cnt = 0, o_cnt = 0;
+    Tout *go = static_cast<Tout *>(p.o);
+
+    for (int i = 0;; ++i) {
+        const int slot = i & 1;
+        bool ok = mbar_wait(smem_u32(&bars.sched_full[slot]), (i >> 1) & 1, wd);
+        if (!__all_sync(0xffffffffu, ok)) return;
+        const int w = sched_item[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars.sched_empty[slot]));
+        if (w >= total) return;
+        const ItemInfo f = item_info(p, w);
+        const int n = t == 0 ? f.n[0] : f.n[1];
+        const int r0 = f.row0 + BM * t;
+        const int row = r0 + lrow;  // query offset inside the sequence
+        Tout *orow = go + (int64_t)(f.q_start + row) * p.o_st + (int64_t)f.h * p.o_sh;
+        float *lse_at = p.lse ? p.lse + (int64_t)f.h * p.n_q + f.q_start + row : nullptr;
+        if (n == 0) {
+            // rows of this tile exist but admit no key (empty key sequence)
+            if (r0 < f.Lq && row < f.Lq) {
+#pragma unroll 4
+                for (int c = 0; c < D; c += 4) store4(orow + c, make_float4(0.f, 0.f, 0.f, 0.f));
+                if (lse_at) *lse_at = -INFINITY;
+            }
+            continue;
+        }
+
+        float m = -INFINITY, l = 0.f;
+        for (int j = 0; j < n; ++j) {
+            ok = mbar_wait(smem_u32(&bars.s_full[t]), s_cnt & 1, wd);
+            ++s_cnt;
+            if (!__all_sync(0xffffffffu, ok)) return;
+            tc_fence_after();
+            uint32_t r[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld_x32(s_addr + 32 * c, r[c]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld_wait(r[c]);
+            float s[BN];
+#pragma unroll
+            for (int c = 0; c < BN; ++c) s[c] = neg ? -__uint_as_float(r[c >> 5][c & 31]) : __uint_as_float(r[c >> 5][c & 31]);
+
+            const int key0 = BN * j;
+            if ((p.causal && key0 + BN - 1 > r0) || key0 + BN > f.Lk) {
+                const int lim = min(f.Lk - key0, p.causal ? row - key0 + 1 : BN);  // keys [0, lim) admitted
+#pragma unroll
+                for (int c = 0; c < BN; ++c)
+                    if (c >= lim) s[c] = -INFINITY;
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < BN; ++c) mx = fmaxf(mx, s[c]);
+            mx *= sl2;
+            const float m_new = fmaxf(m, mx);
+            // refresh the max only when it grew by more than 2^8 somewhere in the warp
+            const bool rescale = j > 0 && __any_sync(0xffffffffu, m_new > m + kRescaleThreshold);
+            float alpha = 1.f;
+            if (j == 0) {
+                m = m_new;
+            } else if (rescale) {
+                alpha = exp2_approx(m - m_new);
+                m = m_new;
+            }
+            const float m_use = m == -INFINITY ? 0.f : m;
+            float sum = 0.f;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float p0 = exp2_approx(fmaf(s[64 * hh + 2 * e], sl2, -m_use));
+                    const float p1 = exp2_approx(fmaf(s[64 * hh + 2 * e + 1], sl2, -m_use));
+                    sum += p0 + p1;
+                    pk[e] = pack2(p0, p1, kBF16);
+                }
+                tmem_st_x32(s_addr + 32 * hh, pk);
+            }
+            l = l * alpha + sum;
+            if (rescale) {
+                // U_t is stable here: S_j(t) completed after PV_{j-1}(t)
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t u[32];
+                    tmem_ld_x32(o_addr + 32 * c, u);
+                    tmem_ld_wait(u);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
+                    tmem_st_x32(o_addr + 32 * c, u);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars.p_full[t]));
+        }
+
+        // epilogue: O = U / l, lse = (m + log2 l) ln 2
+        ok = mbar_wait(smem_u32(&bars.o_done[t]), o_cnt & 1, wd);
+        ++o_cnt;
+        if (!__all_sync(0xffffffffu, ok)) return;
+        tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const bool live = row < f.Lq;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t u[32];
+            tmem_ld_x32(o_addr + 32 * c, u);
+            tmem_ld_wait(u);
+            if (live) {
+#pragma unroll
+                for (int e = 0; e < 32; e += 4)
+                    store4(orow + 32 * c + e,
+                           make_float4(__uint_as_float(u[e]) * inv, __uint_as_float(u[e + 1]) * inv,
+                                       __uint_as_float(u[e + 2]) * inv, __uint_as_float(u[e + 3]) * inv));
+            }
+        }
+        if (live && lse_at) *lse_at = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars.o_free[t]));
+    }
+}
+
+template <int D, bool kBF16, typename Tout>
+__global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ TcFwdArgs a) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ FwdBars bars;
+    __shared__ int sched_item[2];
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sQ = (raw + 1023u) & ~1023u;
+    const uint32_t sKV = sQ + NQT * C::kTileBytes;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Watchdog wd{a.p.watchdog_cycles, &abort_flag, a.p.status};
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int t = 0; t < NQT; ++t) {
+            mbar_init(smem_u32(&bars.q_full[t]), 1);
+            mbar_init(smem_u32(&bars.q_empty[t]), 1);
+            mbar_init(smem_u32(&bars.s_full[t]), 1);
+            mbar_init(smem_u32(&bars.p_full[t]), 128);
+            mbar_init(smem_u32(&bars.o_done[t]), 1);
+            mbar_init(smem_u32(&bars.o_free[t]), 128);
+        }
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(smem_u32(&bars.kv_full[s]), 1);
+            mbar_init(smem_u32(&bars.kv_empty[s]), 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_u32(&bars.sched_full[s]), 1);
+            mbar_init(smem_u32(&bars.sched_empty[s]), kSchedConsumers);
+        }
+        fence_mbar_init();
+        prefetch_tmap(&a.tq);
+        prefetch_tmap(&a.tk);
+        prefetch_tmap(&a.tv);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&tmem_base), 512);
+        tmem_relinquish();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+
+    if (warp < 4) {
+        regs_dec<C::kRegsProducer>();
+        if (warp == 0) {
+            if (lane == 0) producer<D>(a, bars, sched_item, sQ, sKV, wd);
+        } else if (warp == 1) {
+            if (lane == 0) mma_issuer<D, kBF16>(a, bars, sched_item, sQ, sKV, tmem, wd);
+        }
+    } else {
+        regs_inc<C::kRegsSoftmax>();
+        softmax_wg<D, kBF16, Tout>(a, bars, sched_item, tmem, wd);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ---- host side ------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    return fn;
+}
+
+// (tokens, heads, D) 16-bit tensor -> 3-D map {D, tokens, heads}, box {64, 128, 1}.
+bool make_tile_map(CUtensorMap *m, const void *ptr, int dtype, int D, int tokens, int H, int64_t st,
+                   int64_t sh) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)tokens, (cuuint64_t)H};
+    cuuint64_t strides[2] = {(cuuint64_t)st * 2, (cuuint64_t)sh * 2};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    const CUtensorMapDataType dt =
+        dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    return enc(m, dt, 3, const_cast<void *>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool device_is_sm103() {
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return false;
+    return major == 10 && minor == 3;
+}
+
+template <int D, bool kBF16, typename Tout>
+cudaError_t launch_typed(const TcFwdArgs &args, int num_ctas, cudaStream_t s) {
+    auto kern = fwd_tc_kernel<D, kBF16, Tout>;
+    const int smem = Cfg<D>::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (num_ctas <= 0) num_ctas = sm_count();
+    kern<<<num_ctas, kThreads, smem, s>>>(args);
+    count_launch();
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const TcFwdArgs &args, int num_ctas, cudaStream_t s) {
+    const FwdParams &p = args.p;
+    if (p.dtype == ATTN_BF16) {
+        if (p.o_dtype == ATTN_F32) return launch_typed<D, true, float>(args, num_ctas, s);
+        return launch_typed<D, true, __nv_bfloat16>(args, num_ctas, s);
+    }
+    if (p.o_dtype == ATTN_F32) return launch_typed<D, false, float>(args, num_ctas, s);
+    return launch_typed<D, false, __half>(args, num_ctas, s);
+}
+
+}  // namespace
+
+bool tc_fwd_supported(const FwdParams &p) {
+    if (p.dtype != ATTN_F16 && p.dtype != ATTN_BF16) return false;
+    if (p.D != 64 && p.D != 128) return false;
+    if (p.n_q <= 0 || p.n_k <= 0) return false;
+    static const bool sm103 = device_is_sm103();
+    return sm103 && encode_fn() != nullptr;
+}
+
+int tc_fwd_block_rows(const FwdParams &) { return kItemRows; }
+
+cudaError_t launch_fwd_tc(const FwdParams &p, int num_ctas, cudaStream_t s) {
+    TcFwdArgs args;
+    args.p = p;
+    if (!make_tile_map(&args.tq, p.q, p.dtype, p.D, p.n_q, p.H, p.q_st, p.q_sh) ||
+        !make_tile_map(&args.tk, p.k, p.dtype, p.D, p.n_k, p.H, p.k_st, p.k_sh) ||
+        !make_tile_map(&args.tv, p.v, p.dtype, p.D, p.n_k, p.H, p.v_st, p.v_sh))
+        return cudaErrorInvalidValue;
+    return p.D == 64 ? launch_d<64>(args, num_ctas, s) : launch_d<128>(args, num_ctas, s);
+}
+
+}  // namespace attn

@@ -1,14 +1,11 @@
-// Placeholder until the tcgen05 kernels land: reports "not covered".
+// Placeholder until the tcgen05 backward kernels land: reports "not covered".
 #include "tc.h"
 
 namespace attn {
 
-bool tc_fwd_supported(const FwdParams &) { return false; }
 bool tc_bwd_supported(const BwdParams &) { return false; }
-int tc_fwd_block_rows(const FwdParams &) { return 128; }
 int tc_bwd_kv_block(const BwdParams &) { return 128; }
 int tc_bwd_q_block(const BwdParams &) { return 128; }
-cudaError_t launch_fwd_tc(const FwdParams &, int, cudaStream_t) { return cudaErrorNotSupported; }
 cudaError_t launch_bwd_dkdv_tc(const BwdParams &, int, cudaStream_t) { return cudaErrorNotSupported; }
 cudaError_t launch_bwd_dq_tc(const BwdParams &, int, cudaStream_t) { return cudaErrorNotSupported; }
 

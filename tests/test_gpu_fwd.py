@@ -11,8 +11,13 @@ from parity_util import check_lse, check_o, f64
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = ["auto", "simt"]
+KERNELS = ["auto", "simt", "tc"]
 DEV = "cuda"
+
+
+def _skip_unsupported(kernel, dtype):
+    if kernel == "tc" and dtype in ("f32", torch.float32):
+        pytest.skip("the tensor-core kernels take f16 / bf16 only")
 
 
 def _run(x, *, causal, kernel, out_dtype=None, scale=None, num_ctas=0):
@@ -42,6 +47,7 @@ def _out_dtype(dtype):
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N", [1, 127, 129, 300])
 def test_single_sequence(kernel, dtype, D, causal, N):
+    _skip_unsupported(kernel, dtype)
     x = attn_inputs.make(dtype=dtype, H=3, D=D, seed=100 + N, n_q=N)
     o, lse = _run(x, causal=causal, kernel=kernel, out_dtype=_out_dtype(dtype))
     o_ref, lse_ref = _ref(x, causal=causal)
@@ -53,6 +59,7 @@ def test_single_sequence(kernel, dtype, D, causal, N):
 @pytest.mark.parametrize("dtype,D", [("fp16", 64), ("bf16", 128), ("f32", 64)])
 def test_varlen_pages_lengths(kernel, dtype, D):
     """The varlen example's lengths [384, 1, 96, 640, 57], block-diagonal causal."""
+    _skip_unsupported(kernel, dtype)
     x = attn_inputs.make(dtype=dtype, H=4, D=D, seed=11, lengths=[384, 1, 96, 640, 57])
     o, lse = _run(x, causal=True, kernel=kernel, out_dtype=_out_dtype(dtype))
     o_ref, lse_ref = _ref(x, causal=True)
@@ -73,6 +80,7 @@ def test_varlen_with_empty_and_tiny_sequences(kernel):
 @pytest.mark.parametrize("dtype", ["fp16", "f32"])
 def test_cross_attention_varlen_full(kernel, dtype):
     """Full relation with different query / key lengths per sequence."""
+    _skip_unsupported(kernel, dtype)
     x = attn_inputs.make(dtype=dtype, H=2, D=64, seed=13, lengths=[100, 3, 257],
                          lengths_k=[31, 300, 128])
     o, lse = _run(x, causal=False, kernel=kernel)
@@ -122,17 +130,18 @@ def test_grid_size_independent_and_deterministic(kernel):
         assert torch.equal(o, outs[0][0]) and torch.equal(lse, outs[0][1])
 
 
-def test_invalid_cu_seqlens_reported_by_device_status():
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_invalid_cu_seqlens_reported_by_device_status(kernel):
     """Offsets past the tensor end are caught on the device: no work is done
     and the status word reads ATTN_EINVAL."""
     x = attn_inputs.make(dtype="fp16", H=2, D=64, seed=18, n_q=64)
     q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
     bad = torch.tensor([0, 32, 96], dtype=torch.int32, device=DEV)  # 96 > 64 tokens
-    attn.fwd(q, k, v, causal=True, cu_seqlens_q=bad, cu_seqlens_k=bad)
+    attn.fwd(q, k, v, causal=True, cu_seqlens_q=bad, cu_seqlens_k=bad, kernel=kernel)
     assert attn.device_status() == attn._abi.ATTN_EINVAL
     assert attn.device_status() == 0  # cleared by the read
     bad2 = torch.tensor([0, 40, 20], dtype=torch.int32, device=DEV)  # decreasing
-    attn.fwd(q, k, v, causal=False, cu_seqlens_q=bad2, cu_seqlens_k=bad2)
+    attn.fwd(q, k, v, causal=False, cu_seqlens_q=bad2, cu_seqlens_k=bad2, kernel=kernel)
     assert attn.device_status() == attn._abi.ATTN_EINVAL
 
 
@@ -141,3 +150,30 @@ def test_zero_queries_is_a_no_op():
     k = torch.randn(10, 2, 64, dtype=torch.float16, device=DEV)
     o, lse = attn.fwd(q, k, k)
     assert o.shape == (0, 2, 64) and lse.shape == (2, 0)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_negative_scale(kernel):
+    x = attn_inputs.make(dtype="fp16", H=2, D=128, seed=19, n_q=300)
+    o, lse = _run(x, causal=True, kernel=kernel, scale=-0.09)
+    o_ref, lse_ref = _ref(x, causal=True, scale=-0.09)
+    check_o(o, o_ref, x["q"].dtype, o.dtype)
+    check_lse(lse, lse_ref)
+
+
+def test_auto_selects_tensor_cores_for_16_bit():
+    x = attn_inputs.make(dtype="bf16", H=2, D=128, seed=20, n_q=256)
+    q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
+    assert attn.FwdCall(q, k, v, causal=True).selected_kernel() == "tc"
+    q32 = q.float()
+    assert attn.FwdCall(q32, q32, q32, causal=True).selected_kernel() == "simt"
+
+
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("fp16", 64)])
+def test_tc_matches_simt_closely(dtype, D):
+    """The two kernel families agree to well within the oracle tolerance."""
+    x = attn_inputs.make(dtype=dtype, H=4, D=D, seed=21, lengths=[1000, 3, 517])
+    o1, l1 = _run(x, causal=True, kernel="tc", out_dtype=torch.float32)
+    o2, l2 = _run(x, causal=True, kernel="simt", out_dtype=torch.float32)
+    assert (o1 - o2).abs().max().item() < 1e-2
+    assert (l1 - l2).abs().max().item() < 1e-4
