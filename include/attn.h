@@ -177,6 +177,22 @@ ATTN_API int attn_fwd_simple(const void *q, const void *k, const void *v, void *
 ATTN_API int attn_fwd_selected_kernel(const attn_fwd_args *a);
 ATTN_API int attn_bwd_selected_kernel(const attn_bwd_args *a);
 
+/* Forward for callers that cannot allocate device memory (no counterpart on
+ * the pages; a deployment convenience).  Same arguments and results as
+ * attn_fwd, except that `workspace` / `workspace_bytes` are ignored: the
+ * scheduler's scratch lives in a fixed 64 KiB array inside this library's
+ * device memory, which every GPU that loads the library keeps until the
+ * process exits.  No call allocates anything.
+ *  - n_seq must be at most ATTN_NOALLOC_MAX_SEQ; larger inputs return
+ *    ATTN_EUNSUPPORTED before any launch.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - All calls share the one array and each call rewrites the part it reads,
+ *    so calls whose kernels overlap on the GPU (concurrent streams, or
+ *    threads on one device) race: serialise them on one stream. */
+#define ATTN_NOALLOC_MAX_SEQ 16367
+ATTN_API int attn_fwd_noalloc(const attn_fwd_args *a, void *stream);
+
 /* Synchronises `stream`, then returns and clears the device-side status word
  * of the current device: ATTN_OK, ATTN_EINVAL (a kernel found inconsistent
  * cu_seqlens and skipped the work) or ATTN_ETIMEOUT (a bounded wait expired

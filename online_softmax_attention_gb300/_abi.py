@@ -18,6 +18,7 @@ ATTN_OK, ATTN_EINVAL, ATTN_EUNSUPPORTED, ATTN_ECUDA, ATTN_ETIMEOUT, ATTN_EWORKSP
 ATTN_F16, ATTN_BF16, ATTN_F32 = 0, 1, 2
 ATTN_FULL, ATTN_CAUSAL = 0, 1
 ATTN_KERNEL_AUTO, ATTN_KERNEL_SIMT, ATTN_KERNEL_TC = 0, 1, 2
+ATTN_NOALLOC_MAX_SEQ = 16367
 
 # every symbol include/attn.h declares
 EXPORTS = (
@@ -25,7 +26,7 @@ EXPORTS = (
     "attn_fwd_workspace_bytes", "attn_bwd_workspace_bytes", "attn_fwd", "attn_bwd",
     "attn_bwd_preprocess", "attn_bwd_dkdv", "attn_bwd_dq", "attn_fwd_simple",
     "attn_device_status", "attn_launch_count", "attn_strerror", "attn_last_error_string",
-    "attn_fwd_selected_kernel", "attn_bwd_selected_kernel",
+    "attn_fwd_selected_kernel", "attn_bwd_selected_kernel", "attn_fwd_noalloc",
 )
 
 
@@ -92,6 +93,7 @@ def load() -> ctypes.CDLL:
                                            vp, i32, i32, vp, sz, vp]),
         "attn_device_status": (ctypes.c_int, [vp]),
         "attn_fwd_selected_kernel": (ctypes.c_int, [fa]),
+        "attn_fwd_noalloc": (ctypes.c_int, [fa, vp]),
         "attn_bwd_selected_kernel": (ctypes.c_int, [ba]),
         "attn_launch_count": (ctypes.c_uint64, []),
         "attn_strerror": (ctypes.c_char_p, [ctypes.c_int]),
