@@ -152,15 +152,17 @@ int build_fwd(const attn_fwd_args *a, FwdParams &p, bool &use_tc) {
 // ---- backward --------------------------------------------------------------
 
 struct BwdLayout {
-    size_t kv, q, dr, total;
+    size_t kv, q, dr, lse2, total;
 };
 
 BwdLayout bwd_layout(int n_seq, int H, int n_q) {
     BwdLayout L;
+    const size_t rows = align256(sizeof(float) * (size_t)H * (size_t)(n_q > 0 ? n_q : 1));
     L.kv = 0;
     L.q = sched_bytes(n_seq);
     L.dr = L.q + sched_bytes(n_seq);
-    L.total = L.dr + align256(sizeof(float) * (size_t)H * (size_t)(n_q > 0 ? n_q : 1));
+    L.lse2 = L.dr + rows;
+    L.total = L.lse2 + rows;
     return L;
 }
 
@@ -204,6 +206,7 @@ int build_bwd(const attn_bwd_args *a, BwdParams &p, bool &use_tc) {
     p.sched_kv = sched_at(ws + L.kv);
     p.sched_q = sched_at(ws + L.q);
     p.dr = reinterpret_cast<float *>(ws + L.dr);
+    p.lse2 = reinterpret_cast<float *>(ws + L.lse2);
     p.status = status_ptr();
     p.watchdog_cycles = watchdog_cycles();
     if (!p.status) return ATTN_ECUDA;

@@ -6,7 +6,8 @@
 // Dr = sum(dO * O) and nests that recompute each pair's p, dp and
 // ds = p * (dp - Dr): one over the keys accumulating dk and dv, one over the
 // query rows accumulating dq, each owning what it writes.  Here:
-//   preprocess  Dr_i = <dO_i, O_i> (f32), one warp per (row, head);
+//   preprocess  Dr_i = <dO_i, O_i> (f32) and lse2_i = lse_i * log2(e), one warp
+//               per (row, head);
 //   dkdv        one work item per (sequence, head, 64-key block): loop over the
 //               64-row query blocks that can see the block, recompute
 //               P = 2^(s*scale*log2e - lse*log2e), dV += P^T dO, dP = dO V^T,
@@ -84,7 +85,7 @@ __device__ __forceinline__ void tile_nt(float (&acc)[4][4], const float *A, cons
     }
 }
 
-// ---- preprocess: Dr = rowsum(dO * O) ---------------------------------------
+// ---- preprocess: Dr = rowsum(dO * O), and lse in the base-2 domain ----------
 
 template <typename Tin, typename To, int D>
 __global__ void __launch_bounds__(256) row_dot_kernel(const BwdParams p) {
@@ -101,7 +102,12 @@ __global__ void __launch_bounds__(256) row_dot_kernel(const BwdParams p) {
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) p.dr[(int64_t)h * p.n_q + t] = acc;
+    if (lane == 0) {
+        const int64_t at = (int64_t)h * p.n_q + t;
+        p.dr[at] = acc;
+        const float x = p.lse[at];
+        p.lse2[at] = x == -INFINITY ? INFINITY : x * kLog2e;
+    }
 }
 
 // ---- dK, dV ----------------------------------------------------------------

@@ -1,0 +1,830 @@
+// Backward attention on the sm_103a tensor cores (tcgen05 + TMEM + TMA), for
+// f16 / bf16 inputs, D in {64, 128}.
+//
+// The fused backward of the OCANNL "Module Ir.Online_softmax" page (third
+// bullet): a per-row Dr = sum(dO * O) (the preprocess kernel), then nests that
+// recompute each pair's p, dp and ds = p * (dp - Dr) -- one over the keys
+// accumulating dk and dv, one over the query rows accumulating dq, each owning
+// what it writes (no atomics; results are run-to-run deterministic).
+//
+// dkdv kernel -- work item = 128 keys of one (sequence, head); loop over the
+// 128-row query blocks that can see them.  Per block, with the key tile as the
+// MMA's M dimension (TMEM lane = key):
+//   S^T  = K Q^T          (smem x smem)            -> TMEM [0, 128)
+//   dP^T = V dO^T         (smem x smem)            -> TMEM [128, 256)
+//   P^T  = 2^(S^T * scale * log2e - lse2[q])       elementwise warps, 16-bit into TMEM over S^T
+//   dV  += P^T dO         (TMEM x smem, dO N-major) -> TMEM [256, 256 + D)
+//   dS^T = P^T (dP^T - Dr[q])                      elementwise, 16-bit into TMEM over dP^T
+//   dK  += dS^T Q         (TMEM x smem, Q N-major)  -> TMEM [256 + D, 256 + 2D)
+// MMA issue order dV_i, S_{i+1}, dK_i, dP_{i+1} overlaps the elementwise work
+// of one block with the contractions of the next.
+//
+// dq kernel -- work item = 128 query rows; loop over key blocks:
+//   S = Q K^T, dP = dO V^T into TMEM; the elementwise warps read both into
+//   registers at once (freeing the buffers for the next block's MMAs), form
+//   dS = P (dP - Dr) and write it, 16-bit, into one of two TMEM buffers;
+//   dQ += dS K (TMEM x smem, K N-major).
+//
+// Warp roles (12 warps): 0 TMA producer, 1 MMA issuer (one thread), 4-11 two
+// elementwise warpgroups that split each row's 128 columns in halves.  lse2 =
+// lse * log2(e) and Dr come from the preprocess kernel.  All waits bounded.
+#include "sm100.cuh"
+#include "tc.h"
+
+namespace attn {
+
+namespace {
+
+using namespace sm100;
+
+constexpr int BT = 128;           // rows of a query tile = keys of a key tile
+constexpr int kThreads = 384;
+constexpr int kEw = 256;          // elementwise threads (warps 4-11)
+constexpr int kSchedConsumers = 1 + 8;
+
+template <int D>
+struct BCfg {
+    static constexpr int kBoxes = D / 64;
+    static constexpr int kBoxBytes = 128 * 64 * 2;
+    static constexpr int kTileBytes = 128 * D * 2;
+    static constexpr int kQdStages = D == 128 ? 2 : 4;   // dkdv: (Q, dO) ring slots
+    static constexpr int kKvStages = D == 128 ? 4 : 8;   // dq: K / V ring slots
+    static constexpr int kDkdvSmem = (2 + 2 * kQdStages) * kTileBytes + 1024;
+    static constexpr int kDqSmem = (2 + kKvStages) * kTileBytes + 1024;
+    static constexpr int kRegsProducer = 88;
+    static constexpr int kRegsEw = 208;
+    static_assert(128 * kRegsProducer + 256 * kRegsEw <= kThreads * 168, "register split");
+};
+
+struct TcBwdArgs {
+    CUtensorMap tq, tk, tv, tdo;
+    BwdParams p;
+};
+
+__device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
+    uint32_t u;
+    if (bf16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        u = *reinterpret_cast<uint32_t *>(&v);
+    } else {
+        __half2 v = __floats2half2_rn(lo, hi);
+        u = *reinterpret_cast<uint32_t *>(&v);
+    }
+    return u;
+}
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long long budget) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > budget) return;
+    }
+}
+
+// The scheduler ring shared by both kernels: the producer fetches item
+// indices from the global counter, the MMA thread and 8 elementwise warps read them.
+struct SchedRing {
+    uint64_t full[2], empty[2];
+    int item[2];
+};
+
+__device__ __forceinline__ bool sched_publish(SchedRing &r, int i, int *counter, int &w, const Watchdog &wd) {
+    const int slot = i & 1;
+    if (!mbar_wait(smem_u32(&r.empty[slot]), ((i >> 1) & 1) ^ 1, wd)) return false;
+    w = atomicAdd(counter, 1);
+    r.item[slot] = w;
+    mbar_arrive(smem_u32(&r.full[slot]));
+    return true;
+}
+
+__device__ __forceinline__ bool sched_take(SchedRing &r, int i, int &w, const Watchdog &wd) {
+    const int slot = i & 1;
+    if (!mbar_wait(smem_u32(&r.full[slot]), (i >> 1) & 1, wd)) return false;
+    w = r.item[slot];
+    mbar_arrive(smem_u32(&r.empty[slot]));
+    return true;
+}
+
+// warp-wide version for the elementwise warps (lane 0 arrives)
+__device__ __forceinline__ bool sched_take_warp(SchedRing &r, int i, int &w, const Watchdog &wd) {
+    const int slot = i & 1;
+    const bool ok = mbar_wait(smem_u32(&r.full[slot]), (i >> 1) & 1, wd);
+    if (!__all_sync(0xffffffffu, ok)) return false;
+    w = r.item[slot];
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&r.empty[slot]));
+    return true;
+}
+
+template <typename T>
+__device__ __forceinline__ void store_row32(T *dst, const uint32_t (&u)[32], float mul) {
+#pragma unroll
+    for (int e = 0; e < 32; e += 4)
+        store4(dst + e, make_float4(__uint_as_float(u[e]) * mul, __uint_as_float(u[e + 1]) * mul,
+                                    __uint_as_float(u[e + 2]) * mul, __uint_as_float(u[e + 3]) * mul));
+}
+
+template <typename T>
+__device__ __forceinline__ void zero_cols(T *dst, int n) {
+    for (int c = 0; c < n; c += 4) store4(dst + c, make_float4(0.f, 0.f, 0.f, 0.f));
+}
+
+// =============================== dK, dV =======================================
+
+struct DkdvInfo {
+    int q_start, Lq, k_start, Lk, h, key0, qb0, nq, t;
+};
+
+__device__ __forceinline__ DkdvInfo dkdv_info(const BwdParams &p, int w) {
+    const WorkItem it = map_item(w, p.sched_kv.prefix, p.n_seq, p.H, false);
+    DkdvInfo f;
+    seq_bounds(p.cu_q, p.n_q, it.b, f.q_start, f.Lq);
+    seq_bounds(p.cu_k, p.n_k, it.b, f.k_start, f.Lk);
+    f.h = it.h;
+    f.t = it.t;
+    f.key0 = it.t * BT;
+    f.qb0 = p.causal ? it.t : 0;
+    f.nq = max(0, cdiv(f.Lq, BT) - f.qb0);
+    return f;
+}
+
+struct __align__(8) DkdvBars {
+    uint64_t kv_full, kv_empty;
+    uint64_t qd_full[4], qd_empty[4];
+    uint64_t st_full, dp_full, p_ready, ds_ready, acc_done, acc_free;
+    uint64_t stats_ready[2];  // all elementwise threads staged a query block's lse2 / Dr
+    SchedRing sched;
+};
+
+template <int D>
+__device__ void dkdv_producer(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, uint32_t sV, uint32_t sQD,
+                              const Watchdog &wd) {
+    using C = BCfg<D>;
+    const BwdParams &p = a.p;
+    const int total = p.sched_kv.hdr[1];
+    uint32_t kv_uses = 0, qd_i = 0;
+    bool kv_pending = false;
+    for (int i = 0;; ++i) {
+        int w;
+        if (!sched_publish(bars.sched, i, p.sched_kv.hdr, w, wd)) break;
+        if (w >= total) break;
+        const DkdvInfo f = dkdv_info(p, w);
+        if (f.nq == 0) continue;
+        if (!mbar_wait(smem_u32(&bars.kv_empty), (kv_uses & 1) ^ 1, wd)) break;
+        {
+            const uint32_t bar = smem_u32(&bars.kv_full);
+            mbar_expect_tx(bar, 2 * C::kTileBytes);
+#pragma unroll
+            for (int g = 0; g < C::kBoxes; ++g) {
+                tma_load_3d(sK + g * C::kBoxBytes, &a.tk, 64 * g, f.k_start + f.key0, f.h, bar);
+                tma_load_3d(sV + g * C::kBoxBytes, &a.tv, 64 * g, f.k_start + f.key0, f.h, bar);
+            }
+            ++kv_uses;
+            kv_pending = true;
+        }
+        bool ok = true;
+        for (int qb = 0; qb < f.nq; ++qb) {
+            const uint32_t s = qd_i % C::kQdStages;
+            ok = mbar_wait(smem_u32(&bars.qd_empty[s]), ((qd_i / C::kQdStages) & 1) ^ 1, wd);
+            if (!ok) break;
+            const uint32_t bar = smem_u32(&bars.qd_full[s]);
+            const uint32_t dq = sQD + s * 2 * C::kTileBytes, ddo = dq + C::kTileBytes;
+            const int row = f.q_start + BT * (f.qb0 + qb);
+            mbar_expect_tx(bar, 2 * C::kTileBytes);
+#pragma unroll
+            for (int g = 0; g < C::kBoxes; ++g) {
+                tma_load_3d(dq + g * C::kBoxBytes, &a.tq, 64 * g, row, f.h, bar);
+                tma_load_3d(ddo + g * C::kBoxBytes, &a.tdo, 64 * g, row, f.h, bar);
+            }
+            ++qd_i;
+        }
+        if (!ok) break;
+    }
+    if (aborting(wd)) {
+        const long long budget = wd.budget;
+        for (uint32_t k = qd_i > (uint32_t)C::kQdStages ? qd_i - C::kQdStages : 0; k < qd_i; ++k)
+            drain_wait(smem_u32(&bars.qd_full[k % C::kQdStages]), (k / C::kQdStages) & 1, budget);
+        if (kv_pending) drain_wait(smem_u32(&bars.kv_full), (kv_uses - 1) & 1, budget);
+    }
+}
+
+template <int D, bool kBF16>
+__device__ void dkdv_mma(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, uint32_t sV, uint32_t sQD,
+                         uint32_t tmem, const Watchdog &wd) {
+    using C = BCfg<D>;
+    const BwdParams &p = a.p;
+    const int total = p.sched_kv.hdr[1];
+    constexpr uint32_t idSS = idesc_f16(kBF16, BT, BT, 0);
+    constexpr uint32_t idTS = idesc_f16(kBF16, BT, D, 1);
+    uint32_t kv_cnt = 0, qd_i = 0, p_cnt = 0, ds_cnt = 0, af_cnt = 0;
+
+    // X^T = A B^T with A, B (128 x D) K-major tiles -> TMEM columns [col, col + 128)
+    auto issue_ss = [&](uint32_t col, uint32_t A, uint32_t B) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+            mma_ss(tmem + col, sdesc_sw128(A + off, 16, 1024), sdesc_sw128(B + off, 16, 1024), idSS, kk > 0);
+        }
+    };
+    // acc (+)= X^T Y with X^T 16-bit in TMEM (two 32-column halves at +0 and +64)
+    // and Y (128 rows x D) N-major in shared memory
+    auto issue_ts = [&](uint32_t acc_col, uint32_t a_col, uint32_t Y, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < BT / 16; ++kk)
+            mma_ts(tmem + acc_col, tmem + a_col + 8 * kk + (kk >= 4 ? 32 : 0),
+                   sdesc_sw128(Y + kk * 2048, C::kBoxBytes, 1024), idTS, acc || kk > 0);
+    };
+
+    for (int i = 0;; ++i) {
+        int w;
+        if (!sched_take(bars.sched, i, w, wd)) return;
+        if (w >= total) return;
+        const DkdvInfo f = dkdv_info(p, w);
+        if (f.nq == 0) continue;
+        if (!mbar_wait(smem_u32(&bars.kv_full), kv_cnt & 1, wd)) return;
+        ++kv_cnt;
+        uint32_t s = qd_i % C::kQdStages;
+        if (!mbar_wait(smem_u32(&bars.qd_full[s]), (qd_i / C::kQdStages) & 1, wd)) return;
+        tc_fence_after();
+        {
+            const uint32_t q = sQD + s * 2 * C::kTileBytes, d_o = q + C::kTileBytes;
+            issue_ss(0, sK, q);
+            tc_commit(smem_u32(&bars.st_full));
+            issue_ss(BT, sV, d_o);
+            tc_commit(smem_u32(&bars.dp_full));
+        }
+        for (int qb = 0; qb < f.nq; ++qb) {
+            const uint32_t q = sQD + s * 2 * C::kTileBytes, d_o = q + C::kTileBytes;
+            if (!mbar_wait(smem_u32(&bars.p_ready), p_cnt & 1, wd)) return;
+            ++p_cnt;
+            if (qb == 0) {
+                if (!mbar_wait(smem_u32(&bars.acc_free), (af_cnt & 1) ^ 1, wd)) return;
+                ++af_cnt;
+            }
+            tc_fence_after();
+            issue_ts(256, 0, d_o, qb > 0);  // dV += P^T dO
+            const bool next = qb + 1 < f.nq;
+            uint32_t sn = 0;
+            if (next) {
+                sn = (qd_i + 1) % C::kQdStages;
+                if (!mbar_wait(smem_u32(&bars.qd_full[sn]), ((qd_i + 1) / C::kQdStages) & 1, wd)) return;
+                tc_fence_after();
+                issue_ss(0, sK, sQD + sn * 2 * C::kTileBytes);  // S^T of the next block
+                tc_commit(smem_u32(&bars.st_full));
+            }
+            if (!mbar_wait(smem_u32(&bars.ds_ready), ds_cnt & 1, wd)) return;
+            ++ds_cnt;
+            tc_fence_after();
+            issue_ts(256 + D, BT, q, qb > 0);  // dK += dS^T Q
+            tc_commit(smem_u32(&bars.qd_empty[s]));
+            ++qd_i;
+            if (next) {
+                issue_ss(BT, sV, sQD + sn * 2 * C::kTileBytes + C::kTileBytes);  // dP^T of the next block
+                tc_commit(smem_u32(&bars.dp_full));
+                s = sn;
+            }
+        }
+        tc_commit(smem_u32(&bars.acc_done));
+        tc_commit(smem_u32(&bars.kv_empty));
+    }
+}
+
+template <int D, bool kBF16, typename Tg>
+__device__ void dkdv_elementwise(const TcBwdArgs &a, DkdvBars &bars, float *stats, uint32_t tmem,
+                                 const Watchdog &wd) {
+    const BwdParams &p = a.p;
+    const int total = p.sched_kv.hdr[1];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = threadIdx.x - 128;       // 0..255
+    const int wg = (warp - 4) >> 2;        // column half
+    const int quarter = warp & 3;
+    const int kl = 32 * quarter + lane;    // key row inside the tile = TMEM lane
+    const uint32_t lane_base = tmem_addr(tmem, 32 * quarter, 0);
+    const float sl2 = fabsf(p.scale_log2);
+    const bool neg = p.scale_log2 < 0.f;
+    uint32_t st_cnt = 0, dp_cnt = 0, ad_cnt = 0, stat_i = 0;
+
+    for (int i = 0;; ++i) {
+        int w;
+        if (!sched_take_warp(bars.sched, i, w, wd)) return;
+        if (w >= total) return;
+        const DkdvInfo f = dkdv_info(p, w);
+        const int key = f.key0 + kl;
+        const bool live = key < f.Lk;
+        Tg *dst = static_cast<Tg *>(wg == 0 ? p.dv : p.dk) +
+                  (int64_t)(f.k_start + key) * (wg == 0 ? p.dv_st : p.dk_st) +
+                  (int64_t)f.h * (wg == 0 ? p.dv_sh : p.dk_sh);
+        if (f.nq == 0) {
+            if (live) zero_cols(dst, D);
+            continue;
+        }
+        for (int qb = 0; qb < f.nq; ++qb) {
+            // stage lse2 / Dr of this query block (rows past the sequence: P = 0, Dr = 0)
+            float *sb = stats + (stat_i & 1) * 2 * BT;
+            {
+                const int qr = BT * (f.qb0 + qb) + (e & (BT - 1));
+                const int64_t at = (int64_t)f.h * p.n_q + f.q_start + qr;
+                if (e < BT) sb[e] = qr < f.Lq ? p.lse2[at] : INFINITY;
+                else sb[e] = qr < f.Lq ? p.dr[at] : 0.f;
+            }
+            mbar_arrive(smem_u32(&bars.stats_ready[stat_i & 1]));
+            bool ok = mbar_wait(smem_u32(&bars.stats_ready[stat_i & 1]), (stat_i >> 1) & 1, wd);
+            if (!__all_sync(0xffffffffu, ok)) return;
+            ++stat_i;
+            const float *lse2 = sb + 64 * wg;
+            const float *drv = sb + BT + 64 * wg;
+
+            ok = mbar_wait(smem_u32(&bars.st_full), st_cnt & 1, wd);
+            ++st_cnt;
+            if (!__all_sync(0xffffffffu, ok)) return;
+            tc_fence_after();
+            uint32_t r[2][32];
+            tmem_ld_x32(lane_base + 64 * wg, r[0]);
+            tmem_ld_x32(lane_base + 64 * wg + 32, r[1]);
+            tmem_ld_wait(r[0]);
+            tmem_ld_wait(r[1]);
+            float pr[64];
+            const bool diag = p.causal && (f.qb0 + qb == f.t);  // query block == key block
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                float sv = __uint_as_float(r[c >> 5][c & 31]);
+                sv = neg ? -sv : sv;
+                float pv = exp2_approx(fmaf(sv, sl2, -lse2[c]));
+                if (diag && kl > 64 * wg + c) pv = 0.f;  // key after query
+                pr[c] = pv;
+            }
+            {
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) pk[c] = pack2(pr[2 * c], pr[2 * c + 1], kBF16);
+                tmem_st_x32(lane_base + 64 * wg, pk);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars.p_ready));
+
+            ok = mbar_wait(smem_u32(&bars.dp_full), dp_cnt & 1, wd);
+            ++dp_cnt;
+            if (!__all_sync(0xffffffffu, ok)) return;
+            tc_fence_after();
+            tmem_ld_x32(lane_base + BT + 64 * wg, r[0]);
+            tmem_ld_x32(lane_base + BT + 64 * wg + 32, r[1]);
+            tmem_ld_wait(r[0]);
+            tmem_ld_wait(r[1]);
+            {
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const float d0 = pr[2 * c] * (__uint_as_float(r[(2 * c) >> 5][(2 * c) & 31]) - drv[2 * c]);
+                    const float d1 =
+                        pr[2 * c + 1] * (__uint_as_float(r[(2 * c + 1) >> 5][(2 * c + 1) & 31]) - drv[2 * c + 1]);
+                    pk[c] = pack2(d0, d1, kBF16);
+                }
+                tmem_st_x32(lane_base + BT + 64 * wg, pk);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars.ds_ready));
+        }
+        // epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK * scale
+        bool ok = mbar_wait(smem_u32(&bars.acc_done), ad_cnt & 1, wd);
+        ++ad_cnt;
+        if (!__all_sync(0xffffffffu, ok)) return;
+        tc_fence_after();
+        const float mul = wg == 0 ? 1.f : p.scale;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t u[32];
+            tmem_ld_x32(lane_base + 256 + D * wg + 32 * c, u);
+            tmem_ld_wait(u);
+            if (live) store_row32(dst + 32 * c, u, mul);
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars.acc_free));
+    }
+}
+
+template <int D, bool kBF16, typename Tg>
+__global__ void __launch_bounds__(kThreads, 1) dkdv_tc_kernel(const __grid_constant__ TcBwdArgs a) {
+    using C = BCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ DkdvBars bars;
+    __shared__ __align__(16) float stats[2 * 2 * BT];
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t sK = base, sV = base + C::kTileBytes, sQD = base + 2 * C::kTileBytes;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Watchdog wd{a.p.watchdog_cycles, &abort_flag, a.p.status};
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(smem_u32(&bars.kv_full), 1);
+        mbar_init(smem_u32(&bars.kv_empty), 1);
+        for (int s = 0; s < C::kQdStages; ++s) {
+            mbar_init(smem_u32(&bars.qd_full[s]), 1);
+            mbar_init(smem_u32(&bars.qd_empty[s]), 1);
+        }
+        mbar_init(smem_u32(&bars.st_full), 1);
+        mbar_init(smem_u32(&bars.dp_full), 1);
+        mbar_init(smem_u32(&bars.p_ready), kEw);
+        mbar_init(smem_u32(&bars.ds_ready), kEw);
+        mbar_init(smem_u32(&bars.acc_done), 1);
+        mbar_init(smem_u32(&bars.acc_free), kEw);
+        mbar_init(smem_u32(&bars.stats_ready[0]), kEw);
+        mbar_init(smem_u32(&bars.stats_ready[1]), kEw);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_u32(&bars.sched.full[s]), 1);
+            mbar_init(smem_u32(&bars.sched.empty[s]), kSchedConsumers);
+        }
+        fence_mbar_init();
+        prefetch_tmap(&a.tq);
+        prefetch_tmap(&a.tk);
+        prefetch_tmap(&a.tv);
+        prefetch_tmap(&a.tdo);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&tmem_base), 512);
+        tmem_relinquish();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    if (warp < 4) {
+        regs_dec<C::kRegsProducer>();
+        if (warp == 0 && lane == 0) dkdv_producer<D>(a, bars, sK, sV, sQD, wd);
+        else if (warp == 1 && lane == 0) dkdv_mma<D, kBF16>(a, bars, sK, sV, sQD, tmem, wd);
+    } else {
+        regs_inc<C::kRegsEw>();
+        dkdv_elementwise<D, kBF16, Tg>(a, bars, stats, tmem, wd);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ================================= dQ =========================================
+
+struct DqInfo {
+    int q_start, Lq, k_start, Lk, h, row0, nk;
+};
+
+__device__ __forceinline__ DqInfo dq_info(const BwdParams &p, int w) {
+    const WorkItem it = map_item(w, p.sched_q.prefix, p.n_seq, p.H, true);
+    DqInfo f;
+    seq_bounds(p.cu_q, p.n_q, it.b, f.q_start, f.Lq);
+    seq_bounds(p.cu_k, p.n_k, it.b, f.k_start, f.Lk);
+    f.h = it.h;
+    f.row0 = it.t * BT;
+    f.nk = p.causal ? cdiv(min(f.Lk, f.row0 + BT), BT) : cdiv(f.Lk, BT);
+    return f;
+}
+
+struct __align__(8) DqBars {
+    uint64_t q_full, q_empty;
+    uint64_t kv_full[8], kv_empty[8];
+    uint64_t sp_full, sp_free, ds_ready, acc_done, acc_free;
+    SchedRing sched;
+};
+
+template <int D>
+__device__ void dq_producer(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint32_t sDO, uint32_t sKV,
+                            const Watchdog &wd) {
+    using C = BCfg<D>;
+    const BwdParams &p = a.p;
+    const int total = p.sched_q.hdr[1];
+    uint32_t q_uses = 0, kv_i = 0;
+    bool q_pending = false;
+    for (int i = 0;; ++i) {
+        int w;
+        if (!sched_publish(bars.sched, i, p.sched_q.hdr, w, wd)) break;
+        if (w >= total) break;
+        const DqInfo f = dq_info(p, w);
+        if (f.nk == 0) continue;
+        if (!mbar_wait(smem_u32(&bars.q_empty), (q_uses & 1) ^ 1, wd)) break;
+        {
+            const uint32_t bar = smem_u32(&bars.q_full);
+            mbar_expect_tx(bar, 2 * C::kTileBytes);
+#pragma unroll
+            for (int g = 0; g < C::kBoxes; ++g) {
+                tma_load_3d(sQ + g * C::kBoxBytes, &a.tq, 64 * g, f.q_start + f.row0, f.h, bar);
+                tma_load_3d(sDO + g * C::kBoxBytes, &a.tdo, 64 * g, f.q_start + f.row0, f.h, bar);
+            }
+            ++q_uses;
+            q_pending = true;
+        }
+        bool ok = true;
+        for (int j = 0; j < f.nk && ok; ++j) {
+#pragma unroll
+            for (int kv = 0; kv < 2; ++kv) {
+                const uint32_t s = kv_i % C::kKvStages;
+                ok = mbar_wait(smem_u32(&bars.kv_empty[s]), ((kv_i / C::kKvStages) & 1) ^ 1, wd);
+                if (!ok) break;
+                const uint32_t bar = smem_u32(&bars.kv_full[s]);
+                mbar_expect_tx(bar, C::kTileBytes);
+#pragma unroll
+                for (int g = 0; g < C::kBoxes; ++g)
+                    tma_load_3d(sKV + s * C::kTileBytes + g * C::kBoxBytes, kv ? &a.tv : &a.tk, 64 * g,
+                                f.k_start + BT * j, f.h, bar);
+                ++kv_i;
+            }
+        }
+        if (!ok) break;
+    }
+    if (aborting(wd)) {
+        const long long budget = wd.budget;
+        for (uint32_t k = kv_i > (uint32_t)C::kKvStages ? kv_i - C::kKvStages : 0; k < kv_i; ++k)
+            drain_wait(smem_u32(&bars.kv_full[k % C::kKvStages]), (k / C::kKvStages) & 1, budget);
+        if (q_pending) drain_wait(smem_u32(&bars.q_full), (q_uses - 1) & 1, budget);
+    }
+}
+
+template <int D, bool kBF16>
+__device__ void dq_mma(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint32_t sDO, uint32_t sKV, uint32_t tmem,
+                       const Watchdog &wd) {
+    using C = BCfg<D>;
+    const BwdParams &p = a.p;
+    const int total = p.sched_q.hdr[1];
+    constexpr uint32_t idSS = idesc_f16(kBF16, BT, BT, 0);
+    constexpr uint32_t idTS = idesc_f16(kBF16, BT, D, 1);
+    uint32_t q_cnt = 0, kv_i = 0, spf_cnt = 0, ds_cnt = 0, af_cnt = 0;
+
+    auto issue_ss = [&](uint32_t col, uint32_t A, uint32_t B) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+            mma_ss(tmem + col, sdesc_sw128(A + off, 16, 1024), sdesc_sw128(B + off, 16, 1024), idSS, kk > 0);
+        }
+    };
+    auto take_slot = [&](uint32_t &slot) -> bool {
+        slot = kv_i % C::kKvStages;
+        if (!mbar_wait(smem_u32(&bars.kv_full[slot]), (kv_i / C::kKvStages) & 1, wd)) return false;
+        ++kv_i;
+        return true;
+    };
+
+    for (int i = 0;; ++i) {
+        int w;
+        if (!sched_take(bars.sched, i, w, wd)) return;
+        if (w >= total) return;
+        const DqInfo f = dq_info(p, w);
+        if (f.nk == 0) continue;
+        if (!mbar_wait(smem_u32(&bars.q_full), q_cnt & 1, wd)) return;
+        ++q_cnt;
+        uint32_t ks, vs;
+        if (!take_slot(ks) || !take_slot(vs)) return;
+        tc_fence_after();
+        issue_ss(0, sQ, sKV + ks * C::kTileBytes);    // S = Q K^T
+        issue_ss(BT, sDO, sKV + vs * C::kTileBytes);  // dP = dO V^T
+        tc_commit(smem_u32(&bars.sp_full));
+        tc_commit(smem_u32(&bars.kv_empty[vs]));
+        for (int j = 0; j < f.nk; ++j) {
+            if (!mbar_wait(smem_u32(&bars.sp_free), spf_cnt & 1, wd)) return;
+            ++spf_cnt;
+            uint32_t ksn = 0;
+            if (j + 1 < f.nk) {
+                uint32_t vsn;
+                if (!take_slot(ksn) || !take_slot(vsn)) return;
+                tc_fence_after();
+                issue_ss(0, sQ, sKV + ksn * C::kTileBytes);
+                issue_ss(BT, sDO, sKV + vsn * C::kTileBytes);
+                tc_commit(smem_u32(&bars.sp_full));
+                tc_commit(smem_u32(&bars.kv_empty[vsn]));
+            }
+            if (!mbar_wait(smem_u32(&bars.ds_ready), ds_cnt & 1, wd)) return;
+            ++ds_cnt;
+            if (j == 0) {
+                if (!mbar_wait(smem_u32(&bars.acc_free), (af_cnt & 1) ^ 1, wd)) return;
+                ++af_cnt;
+            }
+            tc_fence_after();
+            {
+                const uint32_t kt = sKV + ks * C::kTileBytes;
+                const uint32_t ds_col = 256 + 64 * (j & 1);
+#pragma unroll
+                for (int kk = 0; kk < BT / 16; ++kk)  // dQ += dS K
+                    mma_ts(tmem + 384, tmem + ds_col + 8 * kk, sdesc_sw128(kt + kk * 2048, C::kBoxBytes, 1024),
+                           idTS, j > 0 || kk > 0);
+            }
+            tc_commit(smem_u32(&bars.kv_empty[ks]));
+            ks = ksn;
+        }
+        tc_commit(smem_u32(&bars.acc_done));
+        tc_commit(smem_u32(&bars.q_empty));
+    }
+}
+
+template <int D, bool kBF16, typename Tg>
+__device__ void dq_elementwise(const TcBwdArgs &a, DqBars &bars, uint32_t tmem, const Watchdog &wd) {
+    const BwdParams &p = a.p;
+    const int total = p.sched_q.hdr[1];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wg = (warp - 4) >> 2;
+    const int quarter = warp & 3;
+    const int rl = 32 * quarter + lane;
+    const uint32_t lane_base = tmem_addr(tmem, 32 * quarter, 0);
+    const float sl2 = fabsf(p.scale_log2);
+    const bool neg = p.scale_log2 < 0.f;
+    uint32_t sp_cnt = 0, ad_cnt = 0, step = 0;
+
+    for (int i = 0;; ++i) {
+        int w;
+        if (!sched_take_warp(bars.sched, i, w, wd)) return;
+        if (w >= total) return;
+        const DqInfo f = dq_info(p, w);
+        const int row = f.row0 + rl;
+        const bool live = row < f.Lq;
+        const int64_t at = (int64_t)f.h * p.n_q + f.q_start + row;
+        const float lse2 = live ? p.lse2[at] : INFINITY;
+        const float drr = live ? p.dr[at] : 0.f;
+        Tg *dst = static_cast<Tg *>(p.dq) + (int64_t)(f.q_start + row) * p.dq_st + (int64_t)f.h * p.dq_sh +
+                  (D / 2) * wg;
+        if (f.nk == 0) {
+            if (live) zero_cols(dst, D / 2);
+            continue;
+        }
+        for (int j = 0; j < f.nk; ++j, ++step) {
+            bool ok = mbar_wait(smem_u32(&bars.sp_full), sp_cnt & 1, wd);
+            ++sp_cnt;
+            if (!__all_sync(0xffffffffu, ok)) return;
+            tc_fence_after();
+            uint32_t rs[2][32], rp[2][32];
+            tmem_ld_x32(lane_base + 64 * wg, rs[0]);
+            tmem_ld_x32(lane_base + 64 * wg + 32, rs[1]);
+            tmem_ld_x32(lane_base + BT + 64 * wg, rp[0]);
+            tmem_ld_x32(lane_base + BT + 64 * wg + 32, rp[1]);
+            tmem_ld_wait(rs[0]);
+            tmem_ld_wait(rs[1]);
+            tmem_ld_wait(rp[0]);
+            tmem_ld_wait(rp[1]);
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars.sp_free));  // S and dP buffers may be overwritten
+
+            const int key0 = BT * j;
+            int lim = BT;  // keys [0, lim) of the tile are admitted for this row
+            if ((p.causal && key0 + BT - 1 > f.row0) || key0 + BT > f.Lk)
+                lim = min(f.Lk - key0, p.causal ? row - key0 + 1 : BT);
+            const int c0 = 64 * wg;
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                float d[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int cc = 2 * c + u;
+                    float sv = __uint_as_float(rs[cc >> 5][cc & 31]);
+                    sv = neg ? -sv : sv;
+                    float pv = exp2_approx(fmaf(sv, sl2, -lse2));
+                    if (c0 + cc >= lim) pv = 0.f;
+                    d[u] = pv * (__uint_as_float(rp[cc >> 5][cc & 31]) - drr);
+                }
+                pk[c] = pack2(d[0], d[1], kBF16);
+            }
+            tmem_st_x32(lane_base + 256 + 64 * (j & 1) + 32 * wg, pk);
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars.ds_ready));
+        }
+        bool ok = mbar_wait(smem_u32(&bars.acc_done), ad_cnt & 1, wd);
+        ++ad_cnt;
+        if (!__all_sync(0xffffffffu, ok)) return;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < D / 64; ++c) {
+            uint32_t u[32];
+            tmem_ld_x32(lane_base + 384 + (D / 2) * wg + 32 * c, u);
+            tmem_ld_wait(u);
+            if (live) store_row32(dst + 32 * c, u, p.scale);
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars.acc_free));
+    }
+    (void)step;
+}
+
+template <int D, bool kBF16, typename Tg>
+__global__ void __launch_bounds__(kThreads, 1) dq_tc_kernel(const __grid_constant__ TcBwdArgs a) {
+    using C = BCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ DqBars bars;
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t sQ = base, sDO = base + C::kTileBytes, sKV = base + 2 * C::kTileBytes;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Watchdog wd{a.p.watchdog_cycles, &abort_flag, a.p.status};
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(smem_u32(&bars.q_full), 1);
+        mbar_init(smem_u32(&bars.q_empty), 1);
+        for (int s = 0; s < C::kKvStages; ++s) {
+            mbar_init(smem_u32(&bars.kv_full[s]), 1);
+            mbar_init(smem_u32(&bars.kv_empty[s]), 1);
+        }
+        mbar_init(smem_u32(&bars.sp_full), 1);
+        mbar_init(smem_u32(&bars.sp_free), kEw);
+        mbar_init(smem_u32(&bars.ds_ready), kEw);
+        mbar_init(smem_u32(&bars.acc_done), 1);
+        mbar_init(smem_u32(&bars.acc_free), kEw);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_u32(&bars.sched.full[s]), 1);
+            mbar_init(smem_u32(&bars.sched.empty[s]), kSchedConsumers);
+        }
+        fence_mbar_init();
+        prefetch_tmap(&a.tq);
+        prefetch_tmap(&a.tk);
+        prefetch_tmap(&a.tv);
+        prefetch_tmap(&a.tdo);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&tmem_base), 512);
+        tmem_relinquish();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    if (warp < 4) {
+        regs_dec<C::kRegsProducer>();
+        if (warp == 0 && lane == 0) dq_producer<D>(a, bars, sQ, sDO, sKV, wd);
+        else if (warp == 1 && lane == 0) dq_mma<D, kBF16>(a, bars, sQ, sDO, sKV, tmem, wd);
+    } else {
+        regs_inc<C::kRegsEw>();
+        dq_elementwise<D, kBF16, Tg>(a, bars, tmem, wd);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ================================ host ========================================
+
+bool make_maps(const BwdParams &p, TcBwdArgs &a) {
+    a.p = p;
+    return make_tile_map(&a.tq, p.q, p.dtype, p.D, p.n_q, p.H, p.q_st, p.q_sh) &&
+           make_tile_map(&a.tk, p.k, p.dtype, p.D, p.n_k, p.H, p.k_st, p.k_sh) &&
+           make_tile_map(&a.tv, p.v, p.dtype, p.D, p.n_k, p.H, p.v_st, p.v_sh) &&
+           make_tile_map(&a.tdo, p.dout, p.dtype, p.D, p.n_q, p.H, p.do_st, p.do_sh);
+}
+
+template <typename K>
+cudaError_t launch(K kern, int smem, const TcBwdArgs &a, int num_ctas, cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (num_ctas <= 0) num_ctas = sm_count();
+    kern<<<num_ctas, kThreads, smem, s>>>(a);
+    count_launch();
+    return cudaGetLastError();
+}
+
+template <int D, bool kBF16, typename Tg>
+cudaError_t launch_typed(const TcBwdArgs &a, int num_ctas, cudaStream_t s, bool dkdv) {
+    if (dkdv) return launch(dkdv_tc_kernel<D, kBF16, Tg>, BCfg<D>::kDkdvSmem, a, num_ctas, s);
+    return launch(dq_tc_kernel<D, kBF16, Tg>, BCfg<D>::kDqSmem, a, num_ctas, s);
+}
+
+template <int D>
+cudaError_t launch_d(const TcBwdArgs &a, int num_ctas, cudaStream_t s, bool dkdv) {
+    const BwdParams &p = a.p;
+    if (p.dtype == ATTN_BF16) {
+        if (p.grad_dtype == ATTN_F32) return launch_typed<D, true, float>(a, num_ctas, s, dkdv);
+        return launch_typed<D, true, __nv_bfloat16>(a, num_ctas, s, dkdv);
+    }
+    if (p.grad_dtype == ATTN_F32) return launch_typed<D, false, float>(a, num_ctas, s, dkdv);
+    return launch_typed<D, false, __half>(a, num_ctas, s, dkdv);
+}
+
+cudaError_t launch_bwd(const BwdParams &p, int num_ctas, cudaStream_t s, bool dkdv) {
+    TcBwdArgs a;
+    if (!make_maps(p, a)) return cudaErrorInvalidValue;
+    return p.D == 64 ? launch_d<64>(a, num_ctas, s, dkdv) : launch_d<128>(a, num_ctas, s, dkdv);
+}
+
+}  // namespace
+
+bool tc_bwd_supported(const BwdParams &p) {
+    if (p.dtype != ATTN_F16 && p.dtype != ATTN_BF16) return false;
+    if (p.D != 64 && p.D != 128) return false;
+    if (p.n_q <= 0 || p.n_k <= 0) return false;
+    return tc_device_ok();
+}
+
+int tc_bwd_kv_block(const BwdParams &) { return BT; }
+int tc_bwd_q_block(const BwdParams &) { return BT; }
+
+cudaError_t launch_bwd_dkdv_tc(const BwdParams &p, int num_ctas, cudaStream_t s) {
+    return launch_bwd(p, num_ctas, s, true);
+}
+
+cudaError_t launch_bwd_dq_tc(const BwdParams &p, int num_ctas, cudaStream_t s) {
+    return launch_bwd(p, num_ctas, s, false);
+}
+
+}  // namespace attn

@@ -34,10 +34,6 @@
 // Every mbarrier wait is bounded (sm100::mbar_wait); on expiry the CTA stops
 // issuing work, drains its outstanding TMA loads, frees TMEM and exits, and
 // the status word reads ATTN_ETIMEOUT.
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
 #include "sm100.cuh"
 #include "tc.h"
 
@@ -494,43 +490,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 
 // ---- host side ------------------------------------------------------------------
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            f = nullptr;
-        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    }();
-    return fn;
-}
-
-// (tokens, heads, D) 16-bit tensor -> 3-D map {D, tokens, heads}, box {64, 128, 1}.
-bool make_tile_map(CUtensorMap *m, const void *ptr, int dtype, int D, int tokens, int H, int64_t st,
-                   int64_t sh) {
-    auto enc = encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)tokens, (cuuint64_t)H};
-    cuuint64_t strides[2] = {(cuuint64_t)st * 2, (cuuint64_t)sh * 2};
-    cuuint32_t box[3] = {64, 128, 1};
-    cuuint32_t es[3] = {1, 1, 1};
-    const CUtensorMapDataType dt =
-        dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    return enc(m, dt, 3, const_cast<void *>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-bool device_is_sm103() {
-    int dev = 0, major = 0, minor = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return false;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return false;
-    if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return false;
-    return major == 10 && minor == 3;
-}
-
 template <int D, bool kBF16, typename Tout>
 cudaError_t launch_typed(const TcFwdArgs &args, int num_ctas, cudaStream_t s) {
     auto kern = fwd_tc_kernel<D, kBF16, Tout>;
@@ -560,8 +519,7 @@ bool tc_fwd_supported(const FwdParams &p) {
     if (p.dtype != ATTN_F16 && p.dtype != ATTN_BF16) return false;
     if (p.D != 64 && p.D != 128) return false;
     if (p.n_q <= 0 || p.n_k <= 0) return false;
-    static const bool sm103 = device_is_sm103();
-    return sm103 && encode_fn() != nullptr;
+    return tc_device_ok();
 }
 
 int tc_fwd_block_rows(const FwdParams &) { return kItemRows; }

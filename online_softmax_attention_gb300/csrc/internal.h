@@ -48,6 +48,7 @@ struct BwdParams {
     int n_seq;
     const int32_t *cu_q, *cu_k;
     float *dr;          // (H, n_q) rowsum(dO * O), in the workspace
+    float *lse2;        // (H, n_q) lse * log2(e), +inf where lse = -inf, in the workspace
     Sched sched_kv;     // items over key blocks (dk, dv)
     Sched sched_q;      // items over query blocks (dq)
     int *status;

@@ -1,9 +1,19 @@
 // Tensor-core (tcgen05 / TMEM / TMA) attention kernels for sm_103a.
 #pragma once
 
+#include <cuda.h>
+
 #include "internal.h"
 
 namespace attn {
+
+// True on an sm_103 device with the driver's tensor-map encoder available.
+bool tc_device_ok();
+
+// (tokens, heads, D) 16-bit tensor -> 3-D TMA map {D, tokens, heads} with a
+// {64, 128, 1} box and 128-byte swizzle.  False if the encoder rejects it.
+bool make_tile_map(CUtensorMap *m, const void *ptr, int dtype, int D, int tokens, int H,
+                   int64_t stride_tok, int64_t stride_head);
 
 // Whether the tensor-core kernels cover these arguments (dtype, D, strides).
 bool tc_fwd_supported(const FwdParams &p);

@@ -10,8 +10,13 @@ from parity_util import check_grad
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = ["auto", "simt"]
+KERNELS = ["auto", "simt", "tc"]
 DEV = "cuda"
+
+
+def _skip_unsupported(kernel, dtype):
+    if kernel == "tc" and dtype == "f32":
+        pytest.skip("the tensor-core kernels take f16 / bf16 only")
 
 
 def _fwd_bwd(x, *, causal, kernel, out_dtype=None, grad_dtype=None, num_ctas=0, scale=None):
@@ -42,6 +47,7 @@ def _check(got, ref):
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N", [1, 129, 300])
 def test_single_sequence(kernel, dtype, D, causal, N):
+    _skip_unsupported(kernel, dtype)
     x = attn_inputs.make(dtype=dtype, H=2, D=D, seed=200 + N, n_q=N, backward=True)
     _check(_fwd_bwd(x, causal=causal, kernel=kernel), _ref(x, causal=causal))
 
@@ -75,3 +81,23 @@ def test_deterministic_and_grid_independent(kernel):
     for r in runs[1:]:
         for a, b in zip(r, runs[0]):
             assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_empty_sequences_and_empty_keys(kernel):
+    """Zero-length query / key sequences: their gradients are zero, others unaffected."""
+    x = attn_inputs.make(dtype="fp16", H=2, D=64, seed=25, lengths=[0, 70, 9, 130],
+                         lengths_k=[40, 0, 33, 129], backward=True)
+    got = _fwd_bwd(x, causal=False, kernel=kernel)
+    ref = _ref(x, causal=False)
+    _check(got, ref)
+    assert float(got[1][:40].abs().max()) == 0.0 and float(got[2][:40].abs().max()) == 0.0
+
+
+def test_tc_backward_matches_simt_closely():
+    x = attn_inputs.make(dtype="bf16", H=2, D=128, seed=26, lengths=[700, 129], backward=True)
+    a = _fwd_bwd(x, causal=True, kernel="tc", out_dtype=torch.float32, grad_dtype=torch.float32)
+    b = _fwd_bwd(x, causal=True, kernel="simt", out_dtype=torch.float32, grad_dtype=torch.float32)
+    for u, v in zip(a, b):
+        rel = float((u - v).norm() / v.norm())
+        assert rel < 5e-3, rel
