@@ -199,6 +199,12 @@ ATTN_API int attn_fwd_noalloc(const attn_fwd_args *a, void *stream);
  * and the kernel exited early; outputs are then incomplete). */
 ATTN_API int attn_device_status(void *stream);
 
+/* Diagnostic: y[i] = 2^x[i] computed by the polynomial exp2 that the
+ * tensor-core kernels run on the FMA pipe for part of the softmax (Cody-Waite
+ * range reduction, degree-4 polynomial; max relative error 2.9e-6 for
+ * -126 <= x <= 127).  x, y: device arrays of n floats. */
+ATTN_API int attn_selftest_exp2(const float *x, float *y, int32_t n, void *stream);
+
 /* Number of kernels the library has launched in this process (all devices). */
 ATTN_API uint64_t attn_launch_count(void);
 

@@ -27,6 +27,7 @@ EXPORTS = (
     "attn_bwd_preprocess", "attn_bwd_dkdv", "attn_bwd_dq", "attn_fwd_simple",
     "attn_device_status", "attn_launch_count", "attn_strerror", "attn_last_error_string",
     "attn_fwd_selected_kernel", "attn_bwd_selected_kernel", "attn_fwd_noalloc",
+    "attn_selftest_exp2",
 )
 
 
@@ -94,6 +95,7 @@ def load() -> ctypes.CDLL:
         "attn_device_status": (ctypes.c_int, [vp]),
         "attn_fwd_selected_kernel": (ctypes.c_int, [fa]),
         "attn_fwd_noalloc": (ctypes.c_int, [fa, vp]),
+        "attn_selftest_exp2": (ctypes.c_int, [vp, vp, i32, vp]),
         "attn_bwd_selected_kernel": (ctypes.c_int, [ba]),
         "attn_launch_count": (ctypes.c_uint64, []),
         "attn_strerror": (ctypes.c_char_p, [ctypes.c_int]),

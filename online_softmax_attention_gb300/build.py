@@ -44,10 +44,15 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
+def _env_flags():
+    """Extra nvcc flags from ATTN_NVCC_FLAGS (tuning builds, e.g. -DATTN_FWD_STAGES_D128=4)."""
+    return os.environ.get("ATTN_NVCC_FLAGS", "").split()
+
+
 def _compile(src: str, extra) -> str:
     obj = os.path.join(OBJ_DIR, os.path.basename(src) + ".o")
     if _stale(obj, [src] + _headers()):
-        cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj + ".tmp"]
+        cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *_env_flags(), *extra, "-c", src, "-o", obj + ".tmp"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")

@@ -216,24 +216,31 @@ __device__ void dkdv_mma(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, uint32
     const BwdParams &p = a.p;
     const int total = p.sched_kv.hdr[1];
     constexpr uint32_t idSS = idesc_f16(kBF16, BT, BT, 0);
+    // S^T with a negative scale: negate K (the A operand) so P uses |scale|
+    const uint32_t idST = idSS | (p.scale_log2 < 0.f ? (1u << 13) : 0u);
     constexpr uint32_t idTS = idesc_f16(kBF16, BT, D, 1);
     uint32_t kv_cnt = 0, qd_i = 0, p_cnt = 0, ds_cnt = 0, af_cnt = 0;
 
+    // Descriptors built once; per MMA a constant is added to the start address.
+    const uint64_t kmaj = sdesc_sw128(0, 16, 1024);            // K-major, base address 0
+    const uint64_t nmaj = sdesc_sw128(0, C::kBoxBytes, 1024);  // N-major, base address 0
     // X^T = A B^T with A, B (128 x D) K-major tiles -> TMEM columns [col, col + 128)
-    auto issue_ss = [&](uint32_t col, uint32_t A, uint32_t B) {
+    auto issue_ss = [&](uint32_t col, uint32_t A, uint32_t B, uint32_t id) {
+        const uint64_t ad = kmaj + sdesc_step(A), bd = kmaj + sdesc_step(B);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-            mma_ss(tmem + col, sdesc_sw128(A + off, 16, 1024), sdesc_sw128(B + off, 16, 1024), idSS, kk > 0);
+            const uint64_t off = sdesc_step((kk >> 2) * C::kBoxBytes + (kk & 3) * 32);
+            mma_ss(tmem + col, ad + off, bd + off, id, kk > 0);
         }
     };
     // acc (+)= X^T Y with X^T 16-bit in TMEM (two 32-column halves at +0 and +64)
     // and Y (128 rows x D) N-major in shared memory
     auto issue_ts = [&](uint32_t acc_col, uint32_t a_col, uint32_t Y, bool acc) {
+        const uint64_t yd = nmaj + sdesc_step(Y);
 #pragma unroll
         for (int kk = 0; kk < BT / 16; ++kk)
-            mma_ts(tmem + acc_col, tmem + a_col + 8 * kk + (kk >= 4 ? 32 : 0),
-                   sdesc_sw128(Y + kk * 2048, C::kBoxBytes, 1024), idTS, acc || kk > 0);
+            mma_ts(tmem + acc_col, tmem + a_col + 8 * kk + (kk >= 4 ? 32 : 0), yd + sdesc_step(kk * 2048), idTS,
+                   acc || kk > 0);
     };
 
     for (int i = 0;; ++i) {
@@ -249,9 +256,9 @@ __device__ void dkdv_mma(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, uint32
         tc_fence_after();
         {
             const uint32_t q = sQD + s * 2 * C::kTileBytes, d_o = q + C::kTileBytes;
-            issue_ss(0, sK, q);
+            issue_ss(0, sK, q, idST);
             tc_commit(smem_u32(&bars.st_full));
-            issue_ss(BT, sV, d_o);
+            issue_ss(BT, sV, d_o, idSS);
             tc_commit(smem_u32(&bars.dp_full));
         }
         for (int qb = 0; qb < f.nq; ++qb) {
@@ -270,7 +277,7 @@ __device__ void dkdv_mma(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, uint32
                 sn = (qd_i + 1) % C::kQdStages;
                 if (!mbar_wait(smem_u32(&bars.qd_full[sn]), ((qd_i + 1) / C::kQdStages) & 1, wd)) return;
                 tc_fence_after();
-                issue_ss(0, sK, sQD + sn * 2 * C::kTileBytes);  // S^T of the next block
+                issue_ss(0, sK, sQD + sn * 2 * C::kTileBytes, idST);  // S^T of the next block
                 tc_commit(smem_u32(&bars.st_full));
             }
             if (!mbar_wait(smem_u32(&bars.ds_ready), ds_cnt & 1, wd)) return;
@@ -280,7 +287,7 @@ __device__ void dkdv_mma(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, uint32
             tc_commit(smem_u32(&bars.qd_empty[s]));
             ++qd_i;
             if (next) {
-                issue_ss(BT, sV, sQD + sn * 2 * C::kTileBytes + C::kTileBytes);  // dP^T of the next block
+                issue_ss(BT, sV, sQD + sn * 2 * C::kTileBytes + C::kTileBytes, idSS);  // dP^T of the next block
                 tc_commit(smem_u32(&bars.dp_full));
                 s = sn;
             }
@@ -301,8 +308,7 @@ __device__ void dkdv_elementwise(const TcBwdArgs &a, DkdvBars &bars, float *stat
     const int quarter = warp & 3;
     const int kl = 32 * quarter + lane;    // key row inside the tile = TMEM lane
     const uint32_t lane_base = tmem_addr(tmem, 32 * quarter, 0);
-    const float sl2 = fabsf(p.scale_log2);
-    const bool neg = p.scale_log2 < 0.f;
+    const float sl2 = fabsf(p.scale_log2);  // the score MMA negated S for a negative scale
     uint32_t st_cnt = 0, dp_cnt = 0, ad_cnt = 0, stat_i = 0;
 
     for (int i = 0;; ++i) {
@@ -325,15 +331,16 @@ __device__ void dkdv_elementwise(const TcBwdArgs &a, DkdvBars &bars, float *stat
             {
                 const int qr = BT * (f.qb0 + qb) + (e & (BT - 1));
                 const int64_t at = (int64_t)f.h * p.n_q + f.q_start + qr;
-                if (e < BT) sb[e] = qr < f.Lq ? p.lse2[at] : INFINITY;
-                else sb[e] = qr < f.Lq ? p.dr[at] : 0.f;
+                // stored negated: the elementwise math adds them
+                if (e < BT) sb[e] = qr < f.Lq ? -p.lse2[at] : -INFINITY;
+                else sb[e] = qr < f.Lq ? -p.dr[at] : 0.f;
             }
             mbar_arrive(smem_u32(&bars.stats_ready[stat_i & 1]));
             bool ok = mbar_wait(smem_u32(&bars.stats_ready[stat_i & 1]), (stat_i >> 1) & 1, wd);
             if (!__all_sync(0xffffffffu, ok)) return;
             ++stat_i;
-            const float *lse2 = sb + 64 * wg;
-            const float *drv = sb + BT + 64 * wg;
+            const float2 *nlse2 = reinterpret_cast<const float2 *>(sb + 64 * wg);
+            const float2 *ndr = reinterpret_cast<const float2 *>(sb + BT + 64 * wg);
 
             ok = mbar_wait(smem_u32(&bars.st_full), st_cnt & 1, wd);
             ++st_cnt;
@@ -344,22 +351,24 @@ __device__ void dkdv_elementwise(const TcBwdArgs &a, DkdvBars &bars, float *stat
             tmem_ld_x32(lane_base + 64 * wg + 32, r[1]);
             tmem_ld_wait(r[0]);
             tmem_ld_wait(r[1]);
-            float pr[64];
+            float2 pr[32];
             const bool diag = p.causal && (f.qb0 + qb == f.t);  // query block == key block
+            const float2 sc2 = make_float2(sl2, sl2);
+            uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                float sv = __uint_as_float(r[c >> 5][c & 31]);
-                sv = neg ? -sv : sv;
-                float pv = exp2_approx(fmaf(sv, sl2, -lse2[c]));
-                if (diag && kl > 64 * wg + c) pv = 0.f;  // key after query
+            for (int c = 0; c < 32; ++c) {
+                const float2 sv = make_float2(__uint_as_float(r[(2 * c) >> 5][(2 * c) & 31]),
+                                              __uint_as_float(r[(2 * c + 1) >> 5][(2 * c + 1) & 31]));
+                const float2 x = __ffma2_rn(sv, sc2, nlse2[c]);
+                float2 pv = make_float2(exp2_approx(x.x), exp2_approx(x.y));
+                if (diag) {  // key after query
+                    if (kl > 64 * wg + 2 * c) pv.x = 0.f;
+                    if (kl > 64 * wg + 2 * c + 1) pv.y = 0.f;
+                }
                 pr[c] = pv;
+                pk[c] = pack2(pv.x, pv.y, kBF16);
             }
-            {
-                uint32_t pk[32];
-#pragma unroll
-                for (int c = 0; c < 32; ++c) pk[c] = pack2(pr[2 * c], pr[2 * c + 1], kBF16);
-                tmem_st_x32(lane_base + 64 * wg, pk);
-            }
+            tmem_st_x32(lane_base + 64 * wg, pk);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(smem_u32(&bars.p_ready));
@@ -372,17 +381,14 @@ __device__ void dkdv_elementwise(const TcBwdArgs &a, DkdvBars &bars, float *stat
             tmem_ld_x32(lane_base + BT + 64 * wg + 32, r[1]);
             tmem_ld_wait(r[0]);
             tmem_ld_wait(r[1]);
-            {
-                uint32_t pk[32];
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const float d0 = pr[2 * c] * (__uint_as_float(r[(2 * c) >> 5][(2 * c) & 31]) - drv[2 * c]);
-                    const float d1 =
-                        pr[2 * c + 1] * (__uint_as_float(r[(2 * c + 1) >> 5][(2 * c + 1) & 31]) - drv[2 * c + 1]);
-                    pk[c] = pack2(d0, d1, kBF16);
-                }
-                tmem_st_x32(lane_base + BT + 64 * wg, pk);
+            for (int c = 0; c < 32; ++c) {
+                const float2 dp = make_float2(__uint_as_float(r[(2 * c) >> 5][(2 * c) & 31]),
+                                              __uint_as_float(r[(2 * c + 1) >> 5][(2 * c + 1) & 31]));
+                const float2 d = __fmul2_rn(pr[c], __fadd2_rn(dp, ndr[c]));
+                pk[c] = pack2(d.x, d.y, kBF16);
             }
+            tmem_st_x32(lane_base + BT + 64 * wg, pk);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(smem_u32(&bars.ds_ready));
@@ -550,14 +556,19 @@ __device__ void dq_mma(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint32_t s
     const BwdParams &p = a.p;
     const int total = p.sched_q.hdr[1];
     constexpr uint32_t idSS = idesc_f16(kBF16, BT, BT, 0);
+    // S with a negative scale: negate Q (the A operand) so P uses |scale|
+    const uint32_t idS = idSS | (p.scale_log2 < 0.f ? (1u << 13) : 0u);
     constexpr uint32_t idTS = idesc_f16(kBF16, BT, D, 1);
     uint32_t q_cnt = 0, kv_i = 0, spf_cnt = 0, ds_cnt = 0, af_cnt = 0;
 
-    auto issue_ss = [&](uint32_t col, uint32_t A, uint32_t B) {
+    const uint64_t kmaj = sdesc_sw128(0, 16, 1024);
+    const uint64_t nmaj = sdesc_sw128(0, C::kBoxBytes, 1024);
+    auto issue_ss = [&](uint32_t col, uint32_t A, uint32_t B, uint32_t id) {
+        const uint64_t ad = kmaj + sdesc_step(A), bd = kmaj + sdesc_step(B);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-            mma_ss(tmem + col, sdesc_sw128(A + off, 16, 1024), sdesc_sw128(B + off, 16, 1024), idSS, kk > 0);
+            const uint64_t off = sdesc_step((kk >> 2) * C::kBoxBytes + (kk & 3) * 32);
+            mma_ss(tmem + col, ad + off, bd + off, id, kk > 0);
         }
     };
     auto take_slot = [&](uint32_t &slot) -> bool {
@@ -578,8 +589,8 @@ __device__ void dq_mma(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint32_t s
         uint32_t ks, vs;
         if (!take_slot(ks) || !take_slot(vs)) return;
         tc_fence_after();
-        issue_ss(0, sQ, sKV + ks * C::kTileBytes);    // S = Q K^T
-        issue_ss(BT, sDO, sKV + vs * C::kTileBytes);  // dP = dO V^T
+        issue_ss(0, sQ, sKV + ks * C::kTileBytes, idS);     // S = Q K^T
+        issue_ss(BT, sDO, sKV + vs * C::kTileBytes, idSS);  // dP = dO V^T
         tc_commit(smem_u32(&bars.sp_full));
         tc_commit(smem_u32(&bars.kv_empty[vs]));
         for (int j = 0; j < f.nk; ++j) {
@@ -590,8 +601,8 @@ __device__ void dq_mma(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint32_t s
                 uint32_t vsn;
                 if (!take_slot(ksn) || !take_slot(vsn)) return;
                 tc_fence_after();
-                issue_ss(0, sQ, sKV + ksn * C::kTileBytes);
-                issue_ss(BT, sDO, sKV + vsn * C::kTileBytes);
+                issue_ss(0, sQ, sKV + ksn * C::kTileBytes, idS);
+                issue_ss(BT, sDO, sKV + vsn * C::kTileBytes, idSS);
                 tc_commit(smem_u32(&bars.sp_full));
                 tc_commit(smem_u32(&bars.kv_empty[vsn]));
             }
@@ -603,12 +614,11 @@ __device__ void dq_mma(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint32_t s
             }
             tc_fence_after();
             {
-                const uint32_t kt = sKV + ks * C::kTileBytes;
-                const uint32_t ds_col = 256 + 64 * (j & 1);
+                const uint64_t kd = nmaj + sdesc_step(sKV + ks * C::kTileBytes);
+                const uint32_t ds_col = tmem + 256 + 64 * (j & 1);
 #pragma unroll
                 for (int kk = 0; kk < BT / 16; ++kk)  // dQ += dS K
-                    mma_ts(tmem + 384, tmem + ds_col + 8 * kk, sdesc_sw128(kt + kk * 2048, C::kBoxBytes, 1024),
-                           idTS, j > 0 || kk > 0);
+                    mma_ts(tmem + 384, ds_col + 8 * kk, kd + sdesc_step(kk * 2048), idTS, j > 0 || kk > 0);
             }
             tc_commit(smem_u32(&bars.kv_empty[ks]));
             ks = ksn;
@@ -627,8 +637,7 @@ __device__ void dq_elementwise(const TcBwdArgs &a, DqBars &bars, uint32_t tmem, 
     const int quarter = warp & 3;
     const int rl = 32 * quarter + lane;
     const uint32_t lane_base = tmem_addr(tmem, 32 * quarter, 0);
-    const float sl2 = fabsf(p.scale_log2);
-    const bool neg = p.scale_log2 < 0.f;
+    const float sl2 = fabsf(p.scale_log2);  // the score MMA negated S for a negative scale
     uint32_t sp_cnt = 0, ad_cnt = 0, step = 0;
 
     for (int i = 0;; ++i) {
@@ -669,20 +678,24 @@ __device__ void dq_elementwise(const TcBwdArgs &a, DqBars &bars, uint32_t tmem, 
             if ((p.causal && key0 + BT - 1 > f.row0) || key0 + BT > f.Lk)
                 lim = min(f.Lk - key0, p.causal ? row - key0 + 1 : BT);
             const int c0 = 64 * wg;
+            const float2 sc2 = make_float2(sl2, sl2), nl2 = make_float2(-lse2, -lse2);
+            const float2 ndr2 = make_float2(-drr, -drr);
+            const bool masked = lim < BT;
             uint32_t pk[32];
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
-                float d[2];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int cc = 2 * c + u;
-                    float sv = __uint_as_float(rs[cc >> 5][cc & 31]);
-                    sv = neg ? -sv : sv;
-                    float pv = exp2_approx(fmaf(sv, sl2, -lse2));
-                    if (c0 + cc >= lim) pv = 0.f;
-                    d[u] = pv * (__uint_as_float(rp[cc >> 5][cc & 31]) - drr);
+                const float2 sv = make_float2(__uint_as_float(rs[(2 * c) >> 5][(2 * c) & 31]),
+                                              __uint_as_float(rs[(2 * c + 1) >> 5][(2 * c + 1) & 31]));
+                const float2 x = __ffma2_rn(sv, sc2, nl2);
+                float2 pv = make_float2(exp2_approx(x.x), exp2_approx(x.y));
+                if (masked) {
+                    if (c0 + 2 * c >= lim) pv.x = 0.f;
+                    if (c0 + 2 * c + 1 >= lim) pv.y = 0.f;
                 }
-                pk[c] = pack2(d[0], d[1], kBF16);
+                const float2 dp = make_float2(__uint_as_float(rp[(2 * c) >> 5][(2 * c) & 31]),
+                                              __uint_as_float(rp[(2 * c + 1) >> 5][(2 * c + 1) & 31]));
+                const float2 d = __fmul2_rn(pv, __fadd2_rn(dp, ndr2));
+                pk[c] = pack2(d.x, d.y, kBF16);
             }
             tmem_st_x32(lane_base + 256 + 64 * (j & 1) + 32 * wg, pk);
             tmem_st_wait();

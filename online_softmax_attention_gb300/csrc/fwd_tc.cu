@@ -54,12 +54,24 @@ constexpr int kSchedConsumers = 1 + 8;  // MMA thread + one lane per softmax war
 // softmax warpgroups.  Chosen per D from ptxas spill reports.
 constexpr float kRescaleThreshold = 8.f;  // log2 units
 
+// Tunables (compile-time): K/V ring slots at D = 128, and how many exp2 pairs
+// of every ATTN_FWD_EXP_GROUP go to the FMA pipe instead of the SFU (0 = none).
+#ifndef ATTN_FWD_STAGES_D128
+#define ATTN_FWD_STAGES_D128 4
+#endif
+#ifndef ATTN_FWD_EXP_GROUP
+#define ATTN_FWD_EXP_GROUP 3
+#endif
+#ifndef ATTN_FWD_EXP_FMA
+#define ATTN_FWD_EXP_FMA 0
+#endif
+
 template <int D>
 struct Cfg {
     static constexpr int kBoxes = D / 64;
     static constexpr int kBoxBytes = 128 * 64 * 2;
     static constexpr int kTileBytes = 128 * D * 2;
-    static constexpr int kStages = D == 128 ? 4 : 8;
+    static constexpr int kStages = D == 128 ? ATTN_FWD_STAGES_D128 : 8;
     static constexpr int kSmemBytes = (NQT + kStages) * kTileBytes + 1024;
     static constexpr int kRegsProducer = D == 128 ? 88 : 72;
     static constexpr int kRegsSoftmax = D == 128 ? 208 : 216;
@@ -197,28 +209,36 @@ __device__ void mma_issuer(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
     using C = Cfg<D>;
     const FwdParams &p = a.p;
     const int total = p.sched.hdr[1];
-    constexpr uint32_t idS = idesc_f16(kBF16, BM, BN, 0);
+    // a negative scale negates Q in the score MMA (A-negate bit), so the softmax
+    // always scales by |scale|
+    const uint32_t idS = idesc_f16(kBF16, BM, BN, 0) | (p.scale_log2 < 0.f ? (1u << 13) : 0u);
     constexpr uint32_t idO = idesc_f16(kBF16, BM, D, 1);
     uint32_t kv_i = 0, q_cnt[NQT] = {0, 0}, p_cnt[NQT] = {0, 0}, of_cnt[NQT] = {0, 0};
 
+    // Descriptors are built once; per MMA only a constant is added to the start
+    // address (issuing must stay faster than the 64-cycle 128x128x16 MMA).
+    const uint64_t q_desc = sdesc_sw128(sQ, 16, 1024);
+    const uint64_t k_desc = sdesc_sw128(sKV, 16, 1024);
+    const uint64_t v_desc = sdesc_sw128(sKV, C::kBoxBytes, 1024);
     // S_t = Q_t K^T over D in steps of 16 (32 bytes inside a 128-byte swizzle row)
     auto issue_s = [&](int t, uint32_t kslot) {
-        const uint32_t qa = sQ + t * C::kTileBytes, ka = sKV + kslot * C::kTileBytes;
+        const uint64_t qa = q_desc + sdesc_step(t * C::kTileBytes);
+        const uint64_t ka = k_desc + sdesc_step(kslot * C::kTileBytes);
+        const uint32_t d = tmem + BN * t;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-            mma_ss(tmem + BN * t, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idS,
-                   kk > 0);
+            const uint64_t off = sdesc_step((kk >> 2) * C::kBoxBytes + (kk & 3) * 32);
+            mma_ss(d, qa + off, ka + off, idS, kk > 0);
         }
         tc_commit(smem_u32(&bars.s_full[t]));
     };
     // U_t (+)= P_t V over the 128 keys in steps of 16 (8 TMEM columns of P)
     auto issue_pv = [&](int t, uint32_t vslot, bool acc) {
-        const uint32_t va = sKV + vslot * C::kTileBytes;
+        const uint64_t va = v_desc + sdesc_step(vslot * C::kTileBytes);
+        const uint32_t d = tmem + 256 + D * t, pa = tmem + BN * t;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts(tmem + 256 + D * t, tmem + BN * t + 8 * kk, sdesc_sw128(va + kk * 2048, C::kBoxBytes, 1024),
-                   idO, acc || kk > 0);
+            mma_ts(d, pa + 8 * kk, va + sdesc_step(kk * 2048), idO, acc || kk > 0);
     };
 
     for (int i = 0;; ++i) {
@@ -298,9 +318,8 @@ __device__ void softmax_wg(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
     const int lrow = 32 * quarter + lane;
     const uint32_t s_addr = tmem_addr(tmem, 32 * quarter, BN * t);
     const uint32_t o_addr = tmem_addr(tmem, 32 * quarter, 256 + D * t);
-    // a negative scale is applied as |scale| to negated scores
+    // the score MMA negated S when the scale is negative
     const float sl2 = fabsf(p.scale_log2);
-    const bool neg = p.scale_log2 < 0.f;
     uint32_t s_cnt = 0, o_cnt = 0;
     Tout *go = static_cast<Tout *>(p.o);
 
@@ -341,19 +360,17 @@ __device__ void softmax_wg(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
             for (int c = 0; c < 4; ++c) tmem_ld_wait(r[c]);
             float s[BN];
 #pragma unroll
-            for (int c = 0; c < BN; ++c) s[c] = neg ? -__uint_as_float(r[c >> 5][c & 31]) : __uint_as_float(r[c >> 5][c & 31]);
+            for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(r[c >> 5][c & 31]);
 
             const int key0 = BN * j;
-            if ((p.causal && key0 + BN - 1 > r0) || key0 + BN > f.Lk) {
+            const bool masked = (p.causal && key0 + BN - 1 > r0) || key0 + BN > f.Lk;
+            if (masked) {
                 const int lim = min(f.Lk - key0, p.causal ? row - key0 + 1 : BN);  // keys [0, lim) admitted
 #pragma unroll
                 for (int c = 0; c < BN; ++c)
                     if (c >= lim) s[c] = -INFINITY;
             }
-            float mx = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < BN; ++c) mx = fmaxf(mx, s[c]);
-            mx *= sl2;
+            const float mx = row_max<BN>(s) * sl2;
             const float m_new = fmaxf(m, mx);
             // refresh the max only when it grew by more than 2^8 somewhere in the warp
             const bool rescale = j > 0 && __any_sync(0xffffffffu, m_new > m + kRescaleThreshold);
@@ -365,19 +382,28 @@ __device__ void softmax_wg(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
                 m = m_new;
             }
             const float m_use = m == -INFINITY ? 0.f : m;
-            float sum = 0.f;
+            // p = 2^(s * scale * log2e - m): packed FMA pairs, four packed partial sums
+            const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-m_use, -m_use);
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 uint32_t pk[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const float p0 = exp2_approx(fmaf(s[64 * hh + 2 * e], sl2, -m_use));
-                    const float p1 = exp2_approx(fmaf(s[64 * hh + 2 * e + 1], sl2, -m_use));
-                    sum += p0 + p1;
-                    pk[e] = pack2(p0, p1, kBF16);
+                    const float2 x = __ffma2_rn(make_float2(s[64 * hh + 2 * e], s[64 * hh + 2 * e + 1]), sc2, nm2);
+                    // optionally some pairs on the FMA pipe (unmasked tiles), the rest on the SFU
+                    const bool on_fma = ATTN_FWD_EXP_FMA > 0 && !masked &&
+                                        (e % ATTN_FWD_EXP_GROUP) < ATTN_FWD_EXP_FMA;
+                    const float2 pv = on_fma ? exp2_fma2(x) : make_float2(exp2_approx(x.x), exp2_approx(x.y));
+                    acc[e & 3] = __fadd2_rn(acc[e & 3], pv);
+                    pk[e] = pack2(pv.x, pv.y, kBF16);
                 }
                 tmem_st_x32(s_addr + 32 * hh, pk);
             }
+            const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
+            const float2 a03 = __fadd2_rn(a01, a23);
+            const float sum = a03.x + a03.y;
             l = l * alpha + sum;
             if (rescale) {
                 // U_t is stable here: S_j(t) completed after PV_{j-1}(t)

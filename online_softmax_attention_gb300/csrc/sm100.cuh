@@ -78,6 +78,55 @@ __device__ __forceinline__ bool aborting(const Watchdog &wd) {
     return *reinterpret_cast<volatile int *>(wd.abort_flag) != 0;
 }
 
+// ---- packed / 3-input FP32 arithmetic (sm_100 family) ------------------------------
+
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Maximum of n (a multiple of 16) values with eight independent chains.
+template <int N>
+__device__ __forceinline__ float row_max(const float *v) {
+    static_assert(N % 16 == 0, "row_max: N must be a multiple of 16");
+    constexpr int L = N / 8;  // values per chain
+    float m[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        m[k] = v[k * L];
+#pragma unroll
+        for (int c = 1; c + 1 < L; c += 2) m[k] = max3f(m[k], v[k * L + c], v[k * L + c + 1]);
+        if (L % 2 == 0) m[k] = fmaxf(m[k], v[k * L + L - 1]);
+    }
+    return max3f(max3f(m[0], m[1], m[2]), max3f(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
+}
+
+// 2^x for a pair, on the FMA and integer pipes instead of the SFU.
+// Range reduction (Cody and Waite): n = rint(x) via the 1.5 * 2^23 rounding
+// constant, f = x - n in [-1/2, 1/2]; 2^f by a degree-4 polynomial fitted for
+// this library (relative minimax on [-1/2, 1/2] with p(0) = 1; max relative
+// error 2.9e-6 evaluated in f32); the result's exponent field gets n added.
+// x is clamped to >= -126, so the result is >= ~2^-126 (never 0): callers use
+// it only where no -inf mask applies.
+__device__ __forceinline__ float2 exp2_fma2(float2 x) {
+    constexpr float kRound = 12582912.f;  // 1.5 * 2^23
+    x.x = fmaxf(x.x, -126.f);
+    x.y = fmaxf(x.y, -126.f);
+    const float2 t = __fadd2_rn(x, make_float2(kRound, kRound));
+    const float2 n = __fadd2_rn(t, make_float2(-kRound, -kRound));
+    const float2 f = __ffma2_rn(n, make_float2(-1.f, -1.f), x);
+    float2 p = __ffma2_rn(make_float2(0.00958278402686119f, 0.00958278402686119f), f,
+                          make_float2(0.055906277149915695f, 0.055906277149915695f));
+    p = __ffma2_rn(p, f, make_float2(0.24024099111557007f, 0.24024099111557007f));
+    p = __ffma2_rn(p, f, make_float2(0.6931242346763611f, 0.6931242346763611f));
+    p = __ffma2_rn(p, f, make_float2(1.f, 1.f));
+    // the low mantissa bits of t hold n; shifting them into the exponent field
+    // adds n to it (the rounding constant's own bits shift out entirely)
+    return make_float2(__int_as_float(__float_as_int(p.x) + (__float_as_int(t.x) << 23)),
+                       __int_as_float(__float_as_int(p.y) + (__float_as_int(t.y) << 23)));
+}
+
 // ---- register reallocation between warpgroups ------------------------------------
 // All threads of a warpgroup execute the same call.  The counts must add up to
 // at most the registers the block was launched with.
@@ -178,6 +227,10 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
            (1ull << 46) |   // descriptor version for tcgen05
            (2ull << 61);    // 128-byte swizzle
 }
+
+// Advancing a descriptor by `bytes` (a multiple of 16, staying inside the
+// 256 KiB shared window) only adds to its start-address field.
+__host__ __device__ constexpr uint64_t sdesc_step(uint32_t bytes) { return static_cast<uint64_t>(bytes >> 4); }
 
 // Instruction descriptor of tcgen05.mma kind::f16 with an f32 accumulator.
 // is_bf16: A and B are bf16 (else f16); b_mn_major: B is N-contiguous.
