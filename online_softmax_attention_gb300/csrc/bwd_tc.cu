@@ -47,10 +47,17 @@ struct BCfg {
     static constexpr int kBoxes = D / 64;
     static constexpr int kBoxBytes = 128 * 64 * 2;
     static constexpr int kTileBytes = 128 * D * 2;
-    static constexpr int kQdStages = D == 128 ? 2 : 4;   // dkdv: (Q, dO) ring slots
-    static constexpr int kKvStages = D == 128 ? 4 : 8;   // dq: K / V ring slots
-    static constexpr int kDkdvSmem = (2 + 2 * kQdStages) * kTileBytes + 1024;
-    static constexpr int kDqSmem = (2 + kKvStages) * kTileBytes + 1024;
+    // dkdv: Q tiles stay until dK of their block, dO tiles only until dV
+    static constexpr int kDkdvQStages = D == 128 ? 2 : 4;
+    static constexpr int kDkdvDoStages = D == 128 ? 2 : 4;
+    // dq: K tiles stay until dQ of their block, V tiles only until its dP, so
+    // the K ring is deeper; both prefetch far enough ahead to hide L2 latency
+    static constexpr int kDqKStages = D == 128 ? 3 : 5;
+    static constexpr int kDqVStages = D == 128 ? 2 : 3;
+    static constexpr int kDkdvSmem = (2 + kDkdvQStages + kDkdvDoStages) * kTileBytes + 1024;
+    static constexpr int kDqSmem = (2 + kDqKStages + kDqVStages) * kTileBytes + 1024;
+    // dynamic + static (barriers, stats) shared memory within the 227 KiB per block
+    static_assert(kDkdvSmem + 3 * 1024 <= 232448 && kDqSmem + 1024 <= 232448, "shared memory budget");
     static constexpr int kRegsProducer = 88;
     static constexpr int kRegsEw = 208;
     static_assert(128 * kRegsProducer + 256 * kRegsEw <= kThreads * 168, "register split");
@@ -151,20 +158,33 @@ __device__ __forceinline__ DkdvInfo dkdv_info(const BwdParams &p, int w) {
 
 struct __align__(8) DkdvBars {
     uint64_t kv_full, kv_empty;
-    uint64_t qd_full[4], qd_empty[4];
+    uint64_t q_full[4], q_empty[4], do_full[4], do_empty[4];
     uint64_t st_full, dp_full, p_ready, ds_ready, acc_done, acc_free;
     uint64_t stats_ready[2];  // all elementwise threads staged a query block's lse2 / Dr
     SchedRing sched;
 };
 
 template <int D>
-__device__ void dkdv_producer(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, uint32_t sV, uint32_t sQD,
-                              const Watchdog &wd) {
+__device__ void dkdv_producer(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, uint32_t sV, uint32_t sQ,
+                              uint32_t sDO, const Watchdog &wd) {
     using C = BCfg<D>;
     const BwdParams &p = a.p;
     const int total = p.sched_kv.hdr[1];
-    uint32_t kv_uses = 0, qd_i = 0;
+    uint32_t kv_uses = 0;
+    RingPos<C::kDkdvQStages> qr;
+    RingPos<C::kDkdvDoStages> dr;
     bool kv_pending = false;
+    // load the Q or dO tile of query block `row` into its ring
+    auto load_row = [&](uint64_t *full, uint64_t *empty, uint32_t slot, uint32_t phase, uint32_t base,
+                        const CUtensorMap *tm, int row, int h) -> bool {
+        if (!mbar_wait(smem_u32(&empty[slot]), phase ^ 1, wd)) return false;
+        const uint32_t bar = smem_u32(&full[slot]);
+        mbar_expect_tx(bar, C::kTileBytes);
+#pragma unroll
+        for (int g = 0; g < C::kBoxes; ++g)
+            tma_load_3d(base + slot * C::kTileBytes + g * C::kBoxBytes, tm, 64 * g, row, h, bar);
+        return true;
+    };
     for (int i = 0;; ++i) {
         int w;
         if (!sched_publish(bars.sched, i, p.sched_kv.hdr, w, wd)) break;
@@ -185,32 +205,28 @@ __device__ void dkdv_producer(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, u
         }
         bool ok = true;
         for (int qb = 0; qb < f.nq; ++qb) {
-            const uint32_t s = qd_i % C::kQdStages;
-            ok = mbar_wait(smem_u32(&bars.qd_empty[s]), ((qd_i / C::kQdStages) & 1) ^ 1, wd);
-            if (!ok) break;
-            const uint32_t bar = smem_u32(&bars.qd_full[s]);
-            const uint32_t dq = sQD + s * 2 * C::kTileBytes, ddo = dq + C::kTileBytes;
             const int row = f.q_start + BT * (f.qb0 + qb);
-            mbar_expect_tx(bar, 2 * C::kTileBytes);
-#pragma unroll
-            for (int g = 0; g < C::kBoxes; ++g) {
-                tma_load_3d(dq + g * C::kBoxBytes, &a.tq, 64 * g, row, f.h, bar);
-                tma_load_3d(ddo + g * C::kBoxBytes, &a.tdo, 64 * g, row, f.h, bar);
-            }
-            ++qd_i;
+            ok = load_row(bars.q_full, bars.q_empty, qr.slot(), qr.phase(), sQ, &a.tq, row, f.h);
+            if (!ok) break;
+            ++qr.i;
+            ok = load_row(bars.do_full, bars.do_empty, dr.slot(), dr.phase(), sDO, &a.tdo, row, f.h);
+            if (!ok) break;
+            ++dr.i;
         }
         if (!ok) break;
     }
     if (aborting(wd)) {
         const long long budget = wd.budget;
-        for (uint32_t k = qd_i > (uint32_t)C::kQdStages ? qd_i - C::kQdStages : 0; k < qd_i; ++k)
-            drain_wait(smem_u32(&bars.qd_full[k % C::kQdStages]), (k / C::kQdStages) & 1, budget);
+        for (uint32_t k = qr.i > (uint32_t)C::kDkdvQStages ? qr.i - C::kDkdvQStages : 0; k < qr.i; ++k)
+            drain_wait(smem_u32(&bars.q_full[k % C::kDkdvQStages]), (k / C::kDkdvQStages) & 1, budget);
+        for (uint32_t k = dr.i > (uint32_t)C::kDkdvDoStages ? dr.i - C::kDkdvDoStages : 0; k < dr.i; ++k)
+            drain_wait(smem_u32(&bars.do_full[k % C::kDkdvDoStages]), (k / C::kDkdvDoStages) & 1, budget);
         if (kv_pending) drain_wait(smem_u32(&bars.kv_full), (kv_uses - 1) & 1, budget);
     }
 }
 
 template <int D, bool kBF16>
-__device__ void dkdv_mma(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, uint32_t sV, uint32_t sQD,
+__device__ void dkdv_mma(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, uint32_t sV, uint32_t sQ, uint32_t sDO,
                          uint32_t tmem, const Watchdog &wd) {
     using C = BCfg<D>;
     const BwdParams &p = a.p;
@@ -219,7 +235,9 @@ __device__ void dkdv_mma(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, uint32
     // S^T with a negative scale: negate K (the A operand) so P uses |scale|
     const uint32_t idST = idSS | (p.scale_log2 < 0.f ? (1u << 13) : 0u);
     constexpr uint32_t idTS = idesc_f16(kBF16, BT, D, 1);
-    uint32_t kv_cnt = 0, qd_i = 0, p_cnt = 0, ds_cnt = 0, af_cnt = 0;
+    uint32_t kv_cnt = 0, p_cnt = 0, ds_cnt = 0, af_cnt = 0;
+    RingPos<C::kDkdvQStages> qr;
+    RingPos<C::kDkdvDoStages> dr;
 
     // Descriptors built once; per MMA a constant is added to the start address.
     const uint64_t kmaj = sdesc_sw128(0, 16, 1024);            // K-major, base address 0
@@ -242,6 +260,9 @@ __device__ void dkdv_mma(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, uint32
             mma_ts(tmem + acc_col, tmem + a_col + 8 * kk + (kk >= 4 ? 32 : 0), yd + sdesc_step(kk * 2048), idTS,
                    acc || kk > 0);
     };
+    auto take = [&](uint64_t *full, uint32_t slot, uint32_t phase) -> bool {
+        return mbar_wait(smem_u32(&full[slot]), phase, wd);
+    };
 
     for (int i = 0;; ++i) {
         int w;
@@ -251,18 +272,16 @@ __device__ void dkdv_mma(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, uint32
         if (f.nq == 0) continue;
         if (!mbar_wait(smem_u32(&bars.kv_full), kv_cnt & 1, wd)) return;
         ++kv_cnt;
-        uint32_t s = qd_i % C::kQdStages;
-        if (!mbar_wait(smem_u32(&bars.qd_full[s]), (qd_i / C::kQdStages) & 1, wd)) return;
+        uint32_t qs = qr.slot(), os = dr.slot();
+        if (!take(bars.q_full, qs, qr.phase()) || !take(bars.do_full, os, dr.phase())) return;
+        ++qr.i;
+        ++dr.i;
         tc_fence_after();
-        {
-            const uint32_t q = sQD + s * 2 * C::kTileBytes, d_o = q + C::kTileBytes;
-            issue_ss(0, sK, q, idST);
-            tc_commit(smem_u32(&bars.st_full));
-            issue_ss(BT, sV, d_o, idSS);
-            tc_commit(smem_u32(&bars.dp_full));
-        }
+        issue_ss(0, sK, sQ + qs * C::kTileBytes, idST);  // S^T = K Q^T
+        tc_commit(smem_u32(&bars.st_full));
+        issue_ss(BT, sV, sDO + os * C::kTileBytes, idSS);  // dP^T = V dO^T
+        tc_commit(smem_u32(&bars.dp_full));
         for (int qb = 0; qb < f.nq; ++qb) {
-            const uint32_t q = sQD + s * 2 * C::kTileBytes, d_o = q + C::kTileBytes;
             if (!mbar_wait(smem_u32(&bars.p_ready), p_cnt & 1, wd)) return;
             ++p_cnt;
             if (qb == 0) {
@@ -270,26 +289,32 @@ __device__ void dkdv_mma(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, uint32
                 ++af_cnt;
             }
             tc_fence_after();
-            issue_ts(256, 0, d_o, qb > 0);  // dV += P^T dO
+            issue_ts(256, 0, sDO + os * C::kTileBytes, qb > 0);  // dV += P^T dO
+            tc_commit(smem_u32(&bars.do_empty[os]));
             const bool next = qb + 1 < f.nq;
-            uint32_t sn = 0;
+            uint32_t qsn = 0, osn = 0;
             if (next) {
-                sn = (qd_i + 1) % C::kQdStages;
-                if (!mbar_wait(smem_u32(&bars.qd_full[sn]), ((qd_i + 1) / C::kQdStages) & 1, wd)) return;
+                qsn = qr.slot();
+                if (!take(bars.q_full, qsn, qr.phase())) return;
+                ++qr.i;
                 tc_fence_after();
-                issue_ss(0, sK, sQD + sn * 2 * C::kTileBytes, idST);  // S^T of the next block
+                issue_ss(0, sK, sQ + qsn * C::kTileBytes, idST);  // S^T of the next block
                 tc_commit(smem_u32(&bars.st_full));
             }
             if (!mbar_wait(smem_u32(&bars.ds_ready), ds_cnt & 1, wd)) return;
             ++ds_cnt;
             tc_fence_after();
-            issue_ts(256 + D, BT, q, qb > 0);  // dK += dS^T Q
-            tc_commit(smem_u32(&bars.qd_empty[s]));
-            ++qd_i;
+            issue_ts(256 + D, BT, sQ + qs * C::kTileBytes, qb > 0);  // dK += dS^T Q
+            tc_commit(smem_u32(&bars.q_empty[qs]));
             if (next) {
-                issue_ss(BT, sV, sQD + sn * 2 * C::kTileBytes + C::kTileBytes, idSS);  // dP^T of the next block
+                osn = dr.slot();
+                if (!take(bars.do_full, osn, dr.phase())) return;
+                ++dr.i;
+                tc_fence_after();
+                issue_ss(BT, sV, sDO + osn * C::kTileBytes, idSS);  // dP^T of the next block
                 tc_commit(smem_u32(&bars.dp_full));
-                s = sn;
+                qs = qsn;
+                os = osn;
             }
         }
         tc_commit(smem_u32(&bars.acc_done));
@@ -325,20 +350,24 @@ __device__ void dkdv_elementwise(const TcBwdArgs &a, DkdvBars &bars, float *stat
             if (live) zero_cols(dst, D);
             continue;
         }
+        // lse2 / Dr of a query block, stored negated (the elementwise math adds
+        // them); rows past the sequence give P = 0 and Dr = 0.  Each of the 256
+        // threads fetches one value, one block ahead of its use.
+        auto fetch_stat = [&](int qb) -> float {
+            const int qr = BT * (f.qb0 + qb) + (e & (BT - 1));
+            const int64_t at = (int64_t)f.h * p.n_q + f.q_start + qr;
+            if (e < BT) return qr < f.Lq ? -p.lse2[at] : -INFINITY;
+            return qr < f.Lq ? -p.dr[at] : 0.f;
+        };
+        float stat_next = fetch_stat(0);
         for (int qb = 0; qb < f.nq; ++qb) {
-            // stage lse2 / Dr of this query block (rows past the sequence: P = 0, Dr = 0)
             float *sb = stats + (stat_i & 1) * 2 * BT;
-            {
-                const int qr = BT * (f.qb0 + qb) + (e & (BT - 1));
-                const int64_t at = (int64_t)f.h * p.n_q + f.q_start + qr;
-                // stored negated: the elementwise math adds them
-                if (e < BT) sb[e] = qr < f.Lq ? -p.lse2[at] : -INFINITY;
-                else sb[e] = qr < f.Lq ? -p.dr[at] : 0.f;
-            }
+            sb[e] = stat_next;
             mbar_arrive(smem_u32(&bars.stats_ready[stat_i & 1]));
             bool ok = mbar_wait(smem_u32(&bars.stats_ready[stat_i & 1]), (stat_i >> 1) & 1, wd);
             if (!__all_sync(0xffffffffu, ok)) return;
             ++stat_i;
+            if (qb + 1 < f.nq) stat_next = fetch_stat(qb + 1);  // in flight during this block
             const float2 *nlse2 = reinterpret_cast<const float2 *>(sb + 64 * wg);
             const float2 *ndr = reinterpret_cast<const float2 *>(sb + BT + 64 * wg);
 
@@ -420,7 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_tc_kernel(const __grid_const
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-    const uint32_t sK = base, sV = base + C::kTileBytes, sQD = base + 2 * C::kTileBytes;
+    const uint32_t sK = base, sV = base + C::kTileBytes, sQ = base + 2 * C::kTileBytes;
+    const uint32_t sDO = sQ + C::kDkdvQStages * C::kTileBytes;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const Watchdog wd{a.p.watchdog_cycles, &abort_flag, a.p.status};
 
@@ -428,9 +458,13 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_tc_kernel(const __grid_const
         abort_flag = 0;
         mbar_init(smem_u32(&bars.kv_full), 1);
         mbar_init(smem_u32(&bars.kv_empty), 1);
-        for (int s = 0; s < C::kQdStages; ++s) {
-            mbar_init(smem_u32(&bars.qd_full[s]), 1);
-            mbar_init(smem_u32(&bars.qd_empty[s]), 1);
+        for (int s = 0; s < C::kDkdvQStages; ++s) {
+            mbar_init(smem_u32(&bars.q_full[s]), 1);
+            mbar_init(smem_u32(&bars.q_empty[s]), 1);
+        }
+        for (int s = 0; s < C::kDkdvDoStages; ++s) {
+            mbar_init(smem_u32(&bars.do_full[s]), 1);
+            mbar_init(smem_u32(&bars.do_empty[s]), 1);
         }
         mbar_init(smem_u32(&bars.st_full), 1);
         mbar_init(smem_u32(&bars.dp_full), 1);
@@ -459,8 +493,8 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_tc_kernel(const __grid_const
     const uint32_t tmem = tmem_base;
     if (warp < 4) {
         regs_dec<C::kRegsProducer>();
-        if (warp == 0 && lane == 0) dkdv_producer<D>(a, bars, sK, sV, sQD, wd);
-        else if (warp == 1 && lane == 0) dkdv_mma<D, kBF16>(a, bars, sK, sV, sQD, tmem, wd);
+        if (warp == 0 && lane == 0) dkdv_producer<D>(a, bars, sK, sV, sQ, sDO, wd);
+        else if (warp == 1 && lane == 0) dkdv_mma<D, kBF16>(a, bars, sK, sV, sQ, sDO, tmem, wd);
     } else {
         regs_inc<C::kRegsEw>();
         dkdv_elementwise<D, kBF16, Tg>(a, bars, stats, tmem, wd);
@@ -492,19 +526,32 @@ __device__ __forceinline__ DqInfo dq_info(const BwdParams &p, int w) {
 
 struct __align__(8) DqBars {
     uint64_t q_full, q_empty;
-    uint64_t kv_full[8], kv_empty[8];
+    uint64_t k_full[8], k_empty[8], v_full[8], v_empty[8];
     uint64_t sp_full, sp_free, ds_ready, acc_done, acc_free;
     SchedRing sched;
 };
 
 template <int D>
-__device__ void dq_producer(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint32_t sDO, uint32_t sKV,
+__device__ void dq_producer(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint32_t sDO, uint32_t sK, uint32_t sV,
                             const Watchdog &wd) {
     using C = BCfg<D>;
     const BwdParams &p = a.p;
     const int total = p.sched_q.hdr[1];
-    uint32_t q_uses = 0, kv_i = 0;
+    uint32_t q_uses = 0;
+    RingPos<C::kDqKStages> kr;
+    RingPos<C::kDqVStages> vr;
     bool q_pending = false;
+    // load one K or V tile of key block j into its ring
+    auto load_kv = [&](uint64_t *full, uint64_t *empty, uint32_t slot, uint32_t phase, uint32_t base,
+                       const CUtensorMap *tm, const DqInfo &f, int j) -> bool {
+        if (!mbar_wait(smem_u32(&empty[slot]), phase ^ 1, wd)) return false;
+        const uint32_t bar = smem_u32(&full[slot]);
+        mbar_expect_tx(bar, C::kTileBytes);
+#pragma unroll
+        for (int g = 0; g < C::kBoxes; ++g)
+            tma_load_3d(base + slot * C::kTileBytes + g * C::kBoxBytes, tm, 64 * g, f.k_start + BT * j, f.h, bar);
+        return true;
+    };
     for (int i = 0;; ++i) {
         int w;
         if (!sched_publish(bars.sched, i, p.sched_q.hdr, w, wd)) break;
@@ -525,33 +572,28 @@ __device__ void dq_producer(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint3
         }
         bool ok = true;
         for (int j = 0; j < f.nk && ok; ++j) {
-#pragma unroll
-            for (int kv = 0; kv < 2; ++kv) {
-                const uint32_t s = kv_i % C::kKvStages;
-                ok = mbar_wait(smem_u32(&bars.kv_empty[s]), ((kv_i / C::kKvStages) & 1) ^ 1, wd);
-                if (!ok) break;
-                const uint32_t bar = smem_u32(&bars.kv_full[s]);
-                mbar_expect_tx(bar, C::kTileBytes);
-#pragma unroll
-                for (int g = 0; g < C::kBoxes; ++g)
-                    tma_load_3d(sKV + s * C::kTileBytes + g * C::kBoxBytes, kv ? &a.tv : &a.tk, 64 * g,
-                                f.k_start + BT * j, f.h, bar);
-                ++kv_i;
-            }
+            ok = load_kv(bars.k_full, bars.k_empty, kr.slot(), kr.phase(), sK, &a.tk, f, j);
+            if (!ok) break;
+            ++kr.i;
+            ok = load_kv(bars.v_full, bars.v_empty, vr.slot(), vr.phase(), sV, &a.tv, f, j);
+            if (!ok) break;
+            ++vr.i;
         }
         if (!ok) break;
     }
     if (aborting(wd)) {
         const long long budget = wd.budget;
-        for (uint32_t k = kv_i > (uint32_t)C::kKvStages ? kv_i - C::kKvStages : 0; k < kv_i; ++k)
-            drain_wait(smem_u32(&bars.kv_full[k % C::kKvStages]), (k / C::kKvStages) & 1, budget);
+        for (uint32_t k = kr.i > (uint32_t)C::kDqKStages ? kr.i - C::kDqKStages : 0; k < kr.i; ++k)
+            drain_wait(smem_u32(&bars.k_full[k % C::kDqKStages]), (k / C::kDqKStages) & 1, budget);
+        for (uint32_t k = vr.i > (uint32_t)C::kDqVStages ? vr.i - C::kDqVStages : 0; k < vr.i; ++k)
+            drain_wait(smem_u32(&bars.v_full[k % C::kDqVStages]), (k / C::kDqVStages) & 1, budget);
         if (q_pending) drain_wait(smem_u32(&bars.q_full), (q_uses - 1) & 1, budget);
     }
 }
 
 template <int D, bool kBF16>
-__device__ void dq_mma(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint32_t sDO, uint32_t sKV, uint32_t tmem,
-                       const Watchdog &wd) {
+__device__ void dq_mma(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint32_t sDO, uint32_t sK, uint32_t sV,
+                       uint32_t tmem, const Watchdog &wd) {
     using C = BCfg<D>;
     const BwdParams &p = a.p;
     const int total = p.sched_q.hdr[1];
@@ -559,7 +601,9 @@ __device__ void dq_mma(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint32_t s
     // S with a negative scale: negate Q (the A operand) so P uses |scale|
     const uint32_t idS = idSS | (p.scale_log2 < 0.f ? (1u << 13) : 0u);
     constexpr uint32_t idTS = idesc_f16(kBF16, BT, D, 1);
-    uint32_t q_cnt = 0, kv_i = 0, spf_cnt = 0, ds_cnt = 0, af_cnt = 0;
+    uint32_t q_cnt = 0, spf_cnt = 0, ds_cnt = 0, af_cnt = 0;
+    RingPos<C::kDqKStages> kr;
+    RingPos<C::kDqVStages> vr;
 
     const uint64_t kmaj = sdesc_sw128(0, 16, 1024);
     const uint64_t nmaj = sdesc_sw128(0, C::kBoxBytes, 1024);
@@ -571,10 +615,14 @@ __device__ void dq_mma(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint32_t s
             mma_ss(tmem + col, ad + off, bd + off, id, kk > 0);
         }
     };
-    auto take_slot = [&](uint32_t &slot) -> bool {
-        slot = kv_i % C::kKvStages;
-        if (!mbar_wait(smem_u32(&bars.kv_full[slot]), (kv_i / C::kKvStages) & 1, wd)) return false;
-        ++kv_i;
+    // wait for the next K and V tiles; returns their slots
+    auto take_kv = [&](uint32_t &ks, uint32_t &vs) -> bool {
+        ks = kr.slot();
+        if (!mbar_wait(smem_u32(&bars.k_full[ks]), kr.phase(), wd)) return false;
+        ++kr.i;
+        vs = vr.slot();
+        if (!mbar_wait(smem_u32(&bars.v_full[vs]), vr.phase(), wd)) return false;
+        ++vr.i;
         return true;
     };
 
@@ -587,24 +635,24 @@ __device__ void dq_mma(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint32_t s
         if (!mbar_wait(smem_u32(&bars.q_full), q_cnt & 1, wd)) return;
         ++q_cnt;
         uint32_t ks, vs;
-        if (!take_slot(ks) || !take_slot(vs)) return;
+        if (!take_kv(ks, vs)) return;
         tc_fence_after();
-        issue_ss(0, sQ, sKV + ks * C::kTileBytes, idS);     // S = Q K^T
-        issue_ss(BT, sDO, sKV + vs * C::kTileBytes, idSS);  // dP = dO V^T
+        issue_ss(0, sQ, sK + ks * C::kTileBytes, idS);     // S = Q K^T
+        issue_ss(BT, sDO, sV + vs * C::kTileBytes, idSS);  // dP = dO V^T
         tc_commit(smem_u32(&bars.sp_full));
-        tc_commit(smem_u32(&bars.kv_empty[vs]));
+        tc_commit(smem_u32(&bars.v_empty[vs]));
         for (int j = 0; j < f.nk; ++j) {
             if (!mbar_wait(smem_u32(&bars.sp_free), spf_cnt & 1, wd)) return;
             ++spf_cnt;
             uint32_t ksn = 0;
             if (j + 1 < f.nk) {
                 uint32_t vsn;
-                if (!take_slot(ksn) || !take_slot(vsn)) return;
+                if (!take_kv(ksn, vsn)) return;
                 tc_fence_after();
-                issue_ss(0, sQ, sKV + ksn * C::kTileBytes, idS);
-                issue_ss(BT, sDO, sKV + vsn * C::kTileBytes, idSS);
+                issue_ss(0, sQ, sK + ksn * C::kTileBytes, idS);
+                issue_ss(BT, sDO, sV + vsn * C::kTileBytes, idSS);
                 tc_commit(smem_u32(&bars.sp_full));
-                tc_commit(smem_u32(&bars.kv_empty[vsn]));
+                tc_commit(smem_u32(&bars.v_empty[vsn]));
             }
             if (!mbar_wait(smem_u32(&bars.ds_ready), ds_cnt & 1, wd)) return;
             ++ds_cnt;
@@ -614,13 +662,13 @@ __device__ void dq_mma(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint32_t s
             }
             tc_fence_after();
             {
-                const uint64_t kd = nmaj + sdesc_step(sKV + ks * C::kTileBytes);
+                const uint64_t kd = nmaj + sdesc_step(sK + ks * C::kTileBytes);
                 const uint32_t ds_col = tmem + 256 + 64 * (j & 1);
 #pragma unroll
                 for (int kk = 0; kk < BT / 16; ++kk)  // dQ += dS K
                     mma_ts(tmem + 384, ds_col + 8 * kk, kd + sdesc_step(kk * 2048), idTS, j > 0 || kk > 0);
             }
-            tc_commit(smem_u32(&bars.kv_empty[ks]));
+            tc_commit(smem_u32(&bars.k_empty[ks]));
             ks = ksn;
         }
         tc_commit(smem_u32(&bars.acc_done));
@@ -727,7 +775,8 @@ __global__ void __launch_bounds__(kThreads, 1) dq_tc_kernel(const __grid_constan
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-    const uint32_t sQ = base, sDO = base + C::kTileBytes, sKV = base + 2 * C::kTileBytes;
+    const uint32_t sQ = base, sDO = base + C::kTileBytes, sK = base + 2 * C::kTileBytes;
+    const uint32_t sV = sK + C::kDqKStages * C::kTileBytes;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const Watchdog wd{a.p.watchdog_cycles, &abort_flag, a.p.status};
 
@@ -735,9 +784,13 @@ __global__ void __launch_bounds__(kThreads, 1) dq_tc_kernel(const __grid_constan
         abort_flag = 0;
         mbar_init(smem_u32(&bars.q_full), 1);
         mbar_init(smem_u32(&bars.q_empty), 1);
-        for (int s = 0; s < C::kKvStages; ++s) {
-            mbar_init(smem_u32(&bars.kv_full[s]), 1);
-            mbar_init(smem_u32(&bars.kv_empty[s]), 1);
+        for (int s = 0; s < C::kDqKStages; ++s) {
+            mbar_init(smem_u32(&bars.k_full[s]), 1);
+            mbar_init(smem_u32(&bars.k_empty[s]), 1);
+        }
+        for (int s = 0; s < C::kDqVStages; ++s) {
+            mbar_init(smem_u32(&bars.v_full[s]), 1);
+            mbar_init(smem_u32(&bars.v_empty[s]), 1);
         }
         mbar_init(smem_u32(&bars.sp_full), 1);
         mbar_init(smem_u32(&bars.sp_free), kEw);
@@ -763,8 +816,8 @@ __global__ void __launch_bounds__(kThreads, 1) dq_tc_kernel(const __grid_constan
     const uint32_t tmem = tmem_base;
     if (warp < 4) {
         regs_dec<C::kRegsProducer>();
-        if (warp == 0 && lane == 0) dq_producer<D>(a, bars, sQ, sDO, sKV, wd);
-        else if (warp == 1 && lane == 0) dq_mma<D, kBF16>(a, bars, sQ, sDO, sKV, tmem, wd);
+        if (warp == 0 && lane == 0) dq_producer<D>(a, bars, sQ, sDO, sK, sV, wd);
+        else if (warp == 1 && lane == 0) dq_mma<D, kBF16>(a, bars, sQ, sDO, sK, sV, tmem, wd);
     } else {
         regs_inc<C::kRegsEw>();
         dq_elementwise<D, kBF16, Tg>(a, bars, tmem, wd);

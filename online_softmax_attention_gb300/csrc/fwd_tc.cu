@@ -54,10 +54,15 @@ constexpr int kSchedConsumers = 1 + 8;  // MMA thread + one lane per softmax war
 // softmax warpgroups.  Chosen per D from ptxas spill reports.
 constexpr float kRescaleThreshold = 8.f;  // log2 units
 
-// Tunables (compile-time): K/V ring slots at D = 128, and how many exp2 pairs
-// of every ATTN_FWD_EXP_GROUP go to the FMA pipe instead of the SFU (0 = none).
-#ifndef ATTN_FWD_STAGES_D128
-#define ATTN_FWD_STAGES_D128 4
+// Tunables (compile-time): K and V ring slots at D = 128 (K tiles are released
+// after the two score MMAs, V tiles only after the two value MMAs, so V gets the
+// deeper ring), and how many exp2 pairs of every ATTN_FWD_EXP_GROUP go to the
+// FMA pipe instead of the SFU (0 = none).
+#ifndef ATTN_FWD_KSTAGES_D128
+#define ATTN_FWD_KSTAGES_D128 2
+#endif
+#ifndef ATTN_FWD_VSTAGES_D128
+#define ATTN_FWD_VSTAGES_D128 3
 #endif
 #ifndef ATTN_FWD_EXP_GROUP
 #define ATTN_FWD_EXP_GROUP 3
@@ -71,8 +76,10 @@ struct Cfg {
     static constexpr int kBoxes = D / 64;
     static constexpr int kBoxBytes = 128 * 64 * 2;
     static constexpr int kTileBytes = 128 * D * 2;
-    static constexpr int kStages = D == 128 ? ATTN_FWD_STAGES_D128 : 8;
-    static constexpr int kSmemBytes = (NQT + kStages) * kTileBytes + 1024;
+    static constexpr int kKStages = D == 128 ? ATTN_FWD_KSTAGES_D128 : 4;
+    static constexpr int kVStages = D == 128 ? ATTN_FWD_VSTAGES_D128 : 4;
+    static constexpr int kSmemBytes = (NQT + kKStages + kVStages) * kTileBytes + 1024;
+    static_assert(kSmemBytes + 1024 <= 232448, "shared memory budget (dynamic + static)");
     static constexpr int kRegsProducer = D == 128 ? 88 : 72;
     static constexpr int kRegsSoftmax = D == 128 ? 208 : 216;
     static_assert(128 * kRegsProducer + 256 * kRegsSoftmax <= kThreads * 168, "register split");
@@ -85,7 +92,7 @@ struct TcFwdArgs {
 
 struct __align__(8) FwdBars {
     uint64_t q_full[NQT], q_empty[NQT];
-    uint64_t kv_full[8], kv_empty[8];
+    uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
     uint64_t s_full[NQT], p_full[NQT], o_done[NQT], o_free[NQT];
     uint64_t sched_full[2], sched_empty[2];
 };
@@ -140,14 +147,25 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long l
 // ---- warp 0: TMA producer ------------------------------------------------------
 
 template <int D>
-__device__ void producer(const TcFwdArgs &a, FwdBars &bars, int *sched_item, uint32_t sQ, uint32_t sKV,
-                         const Watchdog &wd) {
+__device__ void producer(const TcFwdArgs &a, FwdBars &bars, int *sched_item, uint32_t sQ, uint32_t sK,
+                         uint32_t sV, const Watchdog &wd) {
     using C = Cfg<D>;
     const FwdParams &p = a.p;
     const int total = p.sched.hdr[1];
-    uint32_t kv_i = 0;
+    RingPos<C::kKStages> kr;
+    RingPos<C::kVStages> vr;
     uint32_t q_uses[NQT] = {0, 0};
     bool q_pending[NQT] = {false, false};
+    auto load_kv = [&](uint64_t *full, uint64_t *empty, uint32_t slot, uint32_t phase, uint32_t base,
+                       const CUtensorMap *tm, int row, int h) -> bool {
+        if (!mbar_wait(smem_u32(&empty[slot]), phase ^ 1, wd)) return false;
+        const uint32_t bar = smem_u32(&full[slot]);
+        mbar_expect_tx(bar, C::kTileBytes);
+#pragma unroll
+        for (int g = 0; g < C::kBoxes; ++g)
+            tma_load_3d(base + slot * C::kTileBytes + g * C::kBoxBytes, tm, 64 * g, row, h, bar);
+        return true;
+    };
     for (int i = 0;; ++i) {
         const int slot = i & 1;
         if (!mbar_wait(smem_u32(&bars.sched_empty[slot]), ((i >> 1) & 1) ^ 1, wd)) break;
@@ -174,27 +192,22 @@ __device__ void producer(const TcFwdArgs &a, FwdBars &bars, int *sched_item, uin
         }
         if (!ok) break;
         for (int j = 0; j < f.nkv && ok; ++j) {
-#pragma unroll
-            for (int kv = 0; kv < 2; ++kv) {
-                const uint32_t s = kv_i % C::kStages;
-                ok = mbar_wait(smem_u32(&bars.kv_empty[s]), ((kv_i / C::kStages) & 1) ^ 1, wd);
-                if (!ok) break;
-                const uint32_t bar = smem_u32(&bars.kv_full[s]);
-                mbar_expect_tx(bar, C::kTileBytes);
-#pragma unroll
-                for (int g = 0; g < C::kBoxes; ++g)
-                    tma_load_3d(sKV + s * C::kTileBytes + g * C::kBoxBytes, kv ? &a.tv : &a.tk, 64 * g,
-                                f.k_start + BN * j, f.h, bar);
-                ++kv_i;
-            }
+            ok = load_kv(bars.k_full, bars.k_empty, kr.slot(), kr.phase(), sK, &a.tk, f.k_start + BN * j, f.h);
+            if (!ok) break;
+            ++kr.i;
+            ok = load_kv(bars.v_full, bars.v_empty, vr.slot(), vr.phase(), sV, &a.tv, f.k_start + BN * j, f.h);
+            if (!ok) break;
+            ++vr.i;
         }
         if (!ok) break;
     }
     if (aborting(wd)) {
         // the newest load of every slot may still be landing in shared memory
         const long long budget = wd.budget;
-        for (uint32_t k = kv_i > (uint32_t)C::kStages ? kv_i - C::kStages : 0; k < kv_i; ++k)
-            drain_wait(smem_u32(&bars.kv_full[k % C::kStages]), (k / C::kStages) & 1, budget);
+        for (uint32_t k = kr.i > (uint32_t)C::kKStages ? kr.i - C::kKStages : 0; k < kr.i; ++k)
+            drain_wait(smem_u32(&bars.k_full[k % C::kKStages]), (k / C::kKStages) & 1, budget);
+        for (uint32_t k = vr.i > (uint32_t)C::kVStages ? vr.i - C::kVStages : 0; k < vr.i; ++k)
+            drain_wait(smem_u32(&bars.v_full[k % C::kVStages]), (k / C::kVStages) & 1, budget);
 #pragma unroll
         for (int t = 0; t < NQT; ++t)
             if (q_pending[t]) drain_wait(smem_u32(&bars.q_full[t]), (q_uses[t] - 1) & 1, budget);
@@ -205,7 +218,7 @@ __device__ void producer(const TcFwdArgs &a, FwdBars &bars, int *sched_item, uin
 
 template <int D, bool kBF16>
 __device__ void mma_issuer(const TcFwdArgs &a, FwdBars &bars, const int *sched_item, uint32_t sQ,
-                           uint32_t sKV, uint32_t tmem, const Watchdog &wd) {
+                           uint32_t sK, uint32_t sV, uint32_t tmem, const Watchdog &wd) {
     using C = Cfg<D>;
     const FwdParams &p = a.p;
     const int total = p.sched.hdr[1];
@@ -213,15 +226,17 @@ __device__ void mma_issuer(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
     // always scales by |scale|
     const uint32_t idS = idesc_f16(kBF16, BM, BN, 0) | (p.scale_log2 < 0.f ? (1u << 13) : 0u);
     constexpr uint32_t idO = idesc_f16(kBF16, BM, D, 1);
-    uint32_t kv_i = 0, q_cnt[NQT] = {0, 0}, p_cnt[NQT] = {0, 0}, of_cnt[NQT] = {0, 0};
+    uint32_t q_cnt[NQT] = {0, 0}, p_cnt[NQT] = {0, 0}, of_cnt[NQT] = {0, 0};
+    RingPos<C::kKStages> kr;
+    RingPos<C::kVStages> vr;
 
     // Descriptors are built once; per MMA only a constant is added to the start
     // address (issuing must stay faster than the 64-cycle 128x128x16 MMA).
     const uint64_t q_desc = sdesc_sw128(sQ, 16, 1024);
-    const uint64_t k_desc = sdesc_sw128(sKV, 16, 1024);
-    const uint64_t v_desc = sdesc_sw128(sKV, C::kBoxBytes, 1024);
+    const uint64_t k_desc = sdesc_sw128(sK, 16, 1024);
+    const uint64_t v_desc = sdesc_sw128(sV, C::kBoxBytes, 1024);
     // S_t = Q_t K^T over D in steps of 16 (32 bytes inside a 128-byte swizzle row)
-    auto issue_s = [&](int t, uint32_t kslot) {
+    auto issue_s = [&](int t, uint32_t kslot) {  // K tile in slot `kslot` of the K ring
         const uint64_t qa = q_desc + sdesc_step(t * C::kTileBytes);
         const uint64_t ka = k_desc + sdesc_step(kslot * C::kTileBytes);
         const uint32_t d = tmem + BN * t;
@@ -233,7 +248,7 @@ __device__ void mma_issuer(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
         tc_commit(smem_u32(&bars.s_full[t]));
     };
     // U_t (+)= P_t V over the 128 keys in steps of 16 (8 TMEM columns of P)
-    auto issue_pv = [&](int t, uint32_t vslot, bool acc) {
+    auto issue_pv = [&](int t, uint32_t vslot, bool acc) {  // V tile in slot `vslot` of the V ring
         const uint64_t va = v_desc + sdesc_step(vslot * C::kTileBytes);
         const uint32_t d = tmem + 256 + D * t, pa = tmem + BN * t;
 #pragma unroll
@@ -256,9 +271,9 @@ __device__ void mma_issuer(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
             ++q_cnt[t];
         }
         // K_0
-        uint32_t ks = kv_i % C::kStages;
-        if (!mbar_wait(smem_u32(&bars.kv_full[ks]), (kv_i / C::kStages) & 1, wd)) return;
-        ++kv_i;
+        const uint32_t ks = kr.slot();
+        if (!mbar_wait(smem_u32(&bars.k_full[ks]), kr.phase(), wd)) return;
+        ++kr.i;
         tc_fence_after();
 #pragma unroll
         for (int t = 0; t < NQT; ++t) {
@@ -266,12 +281,12 @@ __device__ void mma_issuer(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
             issue_s(t, ks);
             if (f.n[t] == 1) tc_commit(smem_u32(&bars.q_empty[t]));
         }
-        tc_commit(smem_u32(&bars.kv_empty[ks]));
+        tc_commit(smem_u32(&bars.k_empty[ks]));
 
         for (int j = 0; j < f.nkv; ++j) {
-            const uint32_t vs = kv_i % C::kStages;
-            if (!mbar_wait(smem_u32(&bars.kv_full[vs]), (kv_i / C::kStages) & 1, wd)) return;
-            ++kv_i;
+            const uint32_t vs = vr.slot();
+            if (!mbar_wait(smem_u32(&bars.v_full[vs]), vr.phase(), wd)) return;
+            ++vr.i;
             bool have_next_k = false;
             uint32_t nks = 0;
 #pragma unroll
@@ -289,9 +304,9 @@ __device__ void mma_issuer(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
                 if (j == f.n[t] - 1) tc_commit(smem_u32(&bars.o_done[t]));
                 if (j + 1 < f.n[t]) {
                     if (!have_next_k) {
-                        nks = kv_i % C::kStages;
-                        if (!mbar_wait(smem_u32(&bars.kv_full[nks]), (kv_i / C::kStages) & 1, wd)) return;
-                        ++kv_i;
+                        nks = kr.slot();
+                        if (!mbar_wait(smem_u32(&bars.k_full[nks]), kr.phase(), wd)) return;
+                        ++kr.i;
                         have_next_k = true;
                         tc_fence_after();
                     }
@@ -299,8 +314,8 @@ __device__ void mma_issuer(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
                     if (j + 1 == f.n[t] - 1) tc_commit(smem_u32(&bars.q_empty[t]));
                 }
             }
-            tc_commit(smem_u32(&bars.kv_empty[vs]));
-            if (have_next_k) tc_commit(smem_u32(&bars.kv_empty[nks]));
+            tc_commit(smem_u32(&bars.v_empty[vs]));
+            if (have_next_k) tc_commit(smem_u32(&bars.k_empty[nks]));
         }
     }
 }
@@ -459,7 +474,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sQ = (raw + 1023u) & ~1023u;
-    const uint32_t sKV = sQ + NQT * C::kTileBytes;
+    const uint32_t sK = sQ + NQT * C::kTileBytes;
+    const uint32_t sV = sK + C::kKStages * C::kTileBytes;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const Watchdog wd{a.p.watchdog_cycles, &abort_flag, a.p.status};
 
@@ -473,9 +489,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             mbar_init(smem_u32(&bars.o_done[t]), 1);
             mbar_init(smem_u32(&bars.o_free[t]), 128);
         }
-        for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(smem_u32(&bars.kv_full[s]), 1);
-            mbar_init(smem_u32(&bars.kv_empty[s]), 1);
+        for (int s = 0; s < C::kKStages; ++s) {
+            mbar_init(smem_u32(&bars.k_full[s]), 1);
+            mbar_init(smem_u32(&bars.k_empty[s]), 1);
+        }
+        for (int s = 0; s < C::kVStages; ++s) {
+            mbar_init(smem_u32(&bars.v_full[s]), 1);
+            mbar_init(smem_u32(&bars.v_empty[s]), 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&bars.sched_full[s]), 1);
@@ -497,9 +517,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     if (warp < 4) {
         regs_dec<C::kRegsProducer>();
         if (warp == 0) {
-            if (lane == 0) producer<D>(a, bars, sched_item, sQ, sKV, wd);
+            if (lane == 0) producer<D>(a, bars, sched_item, sQ, sK, sV, wd);
         } else if (warp == 1) {
-            if (lane == 0) mma_issuer<D, kBF16>(a, bars, sched_item, sQ, sKV, tmem, wd);
+            if (lane == 0) mma_issuer<D, kBF16>(a, bars, sched_item, sQ, sK, sV, tmem, wd);
         }
     } else {
         regs_inc<C::kRegsSoftmax>();

@@ -74,6 +74,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
     }
 }
 
+// Position in a ring of N shared-memory slots guarded by full / empty
+// mbarriers; `i` counts the uses of the ring.
+template <int N>
+struct RingPos {
+    uint32_t i = 0;
+    __device__ __forceinline__ uint32_t slot() const { return i % N; }
+    __device__ __forceinline__ uint32_t phase() const { return (i / N) & 1; }
+};
+
 __device__ __forceinline__ bool aborting(const Watchdog &wd) {
     return *reinterpret_cast<volatile int *>(wd.abort_flag) != 0;
 }
