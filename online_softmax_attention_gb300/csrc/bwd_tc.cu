@@ -164,9 +164,12 @@ struct __align__(8) DkdvBars {
     SchedRing sched;
 };
 
+// Two producer warps: warp 0 publishes the work items and loads K, V and the Q
+// ring; warp 2 loads the dO ring.  Splitting them keeps a dO load from waiting
+// behind a Q slot (Q tiles are released only after dK, dO tiles after dV).
 template <int D>
 __device__ void dkdv_producer(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, uint32_t sV, uint32_t sQ,
-                              uint32_t sDO, const Watchdog &wd) {
+                              uint32_t sDO, bool dout_role, const Watchdog &wd) {
     using C = BCfg<D>;
     const BwdParams &p = a.p;
     const int total = p.sched_kv.hdr[1];
@@ -187,10 +190,25 @@ __device__ void dkdv_producer(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, u
     };
     for (int i = 0;; ++i) {
         int w;
-        if (!sched_publish(bars.sched, i, p.sched_kv.hdr, w, wd)) break;
+        if (dout_role) {
+            if (!sched_take(bars.sched, i, w, wd)) break;
+        } else {
+            if (!sched_publish(bars.sched, i, p.sched_kv.hdr, w, wd)) break;
+        }
         if (w >= total) break;
         const DkdvInfo f = dkdv_info(p, w);
         if (f.nq == 0) continue;
+        bool ok = true;
+        if (dout_role) {
+            for (int qb = 0; qb < f.nq; ++qb) {
+                ok = load_row(bars.do_full, bars.do_empty, dr.slot(), dr.phase(), sDO, &a.tdo,
+                              f.q_start + BT * (f.qb0 + qb), f.h);
+                if (!ok) break;
+                ++dr.i;
+            }
+            if (!ok) break;
+            continue;
+        }
         if (!mbar_wait(smem_u32(&bars.kv_empty), (kv_uses & 1) ^ 1, wd)) break;
         {
             const uint32_t bar = smem_u32(&bars.kv_full);
@@ -203,15 +221,11 @@ __device__ void dkdv_producer(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, u
             ++kv_uses;
             kv_pending = true;
         }
-        bool ok = true;
         for (int qb = 0; qb < f.nq; ++qb) {
-            const int row = f.q_start + BT * (f.qb0 + qb);
-            ok = load_row(bars.q_full, bars.q_empty, qr.slot(), qr.phase(), sQ, &a.tq, row, f.h);
+            ok = load_row(bars.q_full, bars.q_empty, qr.slot(), qr.phase(), sQ, &a.tq,
+                          f.q_start + BT * (f.qb0 + qb), f.h);
             if (!ok) break;
             ++qr.i;
-            ok = load_row(bars.do_full, bars.do_empty, dr.slot(), dr.phase(), sDO, &a.tdo, row, f.h);
-            if (!ok) break;
-            ++dr.i;
         }
         if (!ok) break;
     }
@@ -352,22 +366,25 @@ __device__ void dkdv_elementwise(const TcBwdArgs &a, DkdvBars &bars, float *stat
         }
         // lse2 / Dr of a query block, stored negated (the elementwise math adds
         // them); rows past the sequence give P = 0 and Dr = 0.  Each of the 256
-        // threads fetches one value, one block ahead of its use.
-        auto fetch_stat = [&](int qb) -> float {
+        // threads fetches one value one block ahead of its use, from an address
+        // clamped into the sequence so that the load needs no predicate and no
+        // arithmetic waits on it before the value is staged.
+        const float *stat_src = (e < BT ? p.lse2 : p.dr) + (int64_t)f.h * p.n_q + f.q_start;
+        auto fetch_stat = [&](int qb, bool &valid) -> float {
             const int qr = BT * (f.qb0 + qb) + (e & (BT - 1));
-            const int64_t at = (int64_t)f.h * p.n_q + f.q_start + qr;
-            if (e < BT) return qr < f.Lq ? -p.lse2[at] : -INFINITY;
-            return qr < f.Lq ? -p.dr[at] : 0.f;
+            valid = qr < f.Lq;
+            return __ldg(stat_src + min(qr, f.Lq - 1));
         };
-        float stat_next = fetch_stat(0);
+        bool stat_valid;
+        float stat_next = fetch_stat(0, stat_valid);
         for (int qb = 0; qb < f.nq; ++qb) {
             float *sb = stats + (stat_i & 1) * 2 * BT;
-            sb[e] = stat_next;
+            sb[e] = stat_valid ? -stat_next : (e < BT ? -INFINITY : 0.f);
             mbar_arrive(smem_u32(&bars.stats_ready[stat_i & 1]));
             bool ok = mbar_wait(smem_u32(&bars.stats_ready[stat_i & 1]), (stat_i >> 1) & 1, wd);
             if (!__all_sync(0xffffffffu, ok)) return;
             ++stat_i;
-            if (qb + 1 < f.nq) stat_next = fetch_stat(qb + 1);  // in flight during this block
+            if (qb + 1 < f.nq) stat_next = fetch_stat(qb + 1, stat_valid);  // in flight during this block
             const float2 *nlse2 = reinterpret_cast<const float2 *>(sb + 64 * wg);
             const float2 *ndr = reinterpret_cast<const float2 *>(sb + BT + 64 * wg);
 
@@ -476,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_tc_kernel(const __grid_const
         mbar_init(smem_u32(&bars.stats_ready[1]), kEw);
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&bars.sched.full[s]), 1);
-            mbar_init(smem_u32(&bars.sched.empty[s]), kSchedConsumers);
+            mbar_init(smem_u32(&bars.sched.empty[s]), kSchedConsumers + 1);  // + the dO producer
         }
         fence_mbar_init();
         prefetch_tmap(&a.tq);
@@ -493,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_tc_kernel(const __grid_const
     const uint32_t tmem = tmem_base;
     if (warp < 4) {
         regs_dec<C::kRegsProducer>();
-        if (warp == 0 && lane == 0) dkdv_producer<D>(a, bars, sK, sV, sQ, sDO, wd);
+        if ((warp == 0 || warp == 2) && lane == 0) dkdv_producer<D>(a, bars, sK, sV, sQ, sDO, warp == 2, wd);
         else if (warp == 1 && lane == 0) dkdv_mma<D, kBF16>(a, bars, sK, sV, sQ, sDO, tmem, wd);
     } else {
         regs_inc<C::kRegsEw>();
