@@ -43,6 +43,23 @@ def attention_flops(lengths_q, lengths_k, H, D, causal):
     return f
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """Maximum of a per-rank number over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: float, world: int, ms_max: float) -> float:
+    """Whole-job throughput: every rank processes `units_per_rank` (weak
+    scaling); the job takes as long as its slowest rank."""
+    return units_per_rank * world / (ms_max * 1e-3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -280,10 +297,7 @@ def main():
     launches = attn.launch_count() - n0
     ms = start.elapsed_time(end) / args.steps
     stage_ms = {s: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j, s in enumerate(stages)}
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
     status = attn.device_status()
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
@@ -323,11 +337,7 @@ def main():
     t1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    e2e_ms = t0.elapsed_time(t1) / e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(t0.elapsed_time(t1) / e_steps, dev)
 
     peaks = load_peaks()
     # algorithmic FLOPs per launch of each stage: fwd = S and PV contractions;
@@ -363,7 +373,7 @@ def main():
     fwd_tflops = fwd_flops / (stage_ms["fwd"] * 1e-3) / 1e12
     bwd_ms = stage_ms["bwd_preprocess"] + stage_ms["bwd_dkdv"] + stage_ms["bwd_dq"]
     bwd_tflops = bwd_flops / (bwd_ms * 1e-3) / 1e12
-    value = step_flops * world / (ms * 1e-3) / 1e12
+    value = job_rate(step_flops, world, ms) / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -378,7 +388,7 @@ def main():
                       "fwd_frac_of_bf16_peak": fwd_tflops / peaks["bf16_tflops"],
                       "bf16_peak_tflops": peaks["bf16_tflops"]},
         "roofline": roofline,
-        "e2e": {"value": step_flops * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+        "e2e": {"value": job_rate(step_flops, world, e2e_ms) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches,
         "clocks": clk.summary(),

@@ -193,6 +193,14 @@ ATTN_API int attn_bwd_selected_kernel(const attn_bwd_args *a);
 #define ATTN_NOALLOC_MAX_SEQ 16367
 ATTN_API int attn_fwd_noalloc(const attn_fwd_args *a, void *stream);
 
+/* Bounded-wait budget, in SM clock cycles, of every mbarrier wait in the
+ * tensor-core kernels launched after this call (default 4e9, or the
+ * ATTN_WATCHDOG_CYCLES environment variable; cycles <= 0 restores that).  When
+ * a wait runs out the kernel stops, drains its loads in flight, frees its
+ * tensor memory and exits; attn_device_status() then returns ATTN_ETIMEOUT.
+ * Returns the previous budget. */
+ATTN_API long long attn_set_watchdog_cycles(long long cycles);
+
 /* Synchronises `stream`, then returns and clears the device-side status word
  * of the current device: ATTN_OK, ATTN_EINVAL (a kernel found inconsistent
  * cu_seqlens and skipped the work) or ATTN_ETIMEOUT (a bounded wait expired

@@ -27,7 +27,7 @@ EXPORTS = (
     "attn_bwd_preprocess", "attn_bwd_dkdv", "attn_bwd_dq", "attn_fwd_simple",
     "attn_device_status", "attn_launch_count", "attn_strerror", "attn_last_error_string",
     "attn_fwd_selected_kernel", "attn_bwd_selected_kernel", "attn_fwd_noalloc",
-    "attn_selftest_exp2",
+    "attn_selftest_exp2", "attn_set_watchdog_cycles",
 )
 
 
@@ -96,6 +96,7 @@ def load() -> ctypes.CDLL:
         "attn_fwd_selected_kernel": (ctypes.c_int, [fa]),
         "attn_fwd_noalloc": (ctypes.c_int, [fa, vp]),
         "attn_selftest_exp2": (ctypes.c_int, [vp, vp, i32, vp]),
+        "attn_set_watchdog_cycles": (ctypes.c_longlong, [ctypes.c_longlong]),
         "attn_bwd_selected_kernel": (ctypes.c_int, [ba]),
         "attn_launch_count": (ctypes.c_uint64, []),
         "attn_strerror": (ctypes.c_char_p, [ctypes.c_int]),

@@ -47,13 +47,15 @@ int *status_ptr() {
     return g_status_ptr[dev];
 }
 
+constexpr long long kDefaultWatchdog = 4000000000LL;  // about 2 s at 2 GHz per bounded wait
+std::atomic<long long> g_watchdog{0};
+
 long long watchdog_cycles() {
-    static long long v = [] {
-        const char *e = std::getenv("ATTN_WATCHDOG_CYCLES");
-        long long x = e ? std::atoll(e) : 0;
-        return x > 0 ? x : 4000000000LL;  // about 2 s at 2 GHz per bounded wait
-    }();
-    return v;
+    long long v = g_watchdog.load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    const char *e = std::getenv("ATTN_WATCHDOG_CYCLES");
+    const long long x = e ? std::atoll(e) : 0;
+    return x > 0 ? x : kDefaultWatchdog;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -353,6 +355,12 @@ int attn_bwd_selected_kernel(const attn_bwd_args *a) {
     bool use_tc = false;
     const int rc = build_bwd(a, p, use_tc);
     return rc ? rc : (use_tc ? ATTN_KERNEL_TC : ATTN_KERNEL_SIMT);
+}
+
+long long attn_set_watchdog_cycles(long long cycles) {
+    const long long prev = watchdog_cycles();
+    g_watchdog.store(cycles > 0 ? cycles : 0, std::memory_order_relaxed);
+    return prev;
 }
 
 int attn_device_status(void *stream) {

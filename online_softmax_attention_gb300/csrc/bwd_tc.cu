@@ -82,6 +82,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
     return u;
 }
 
+constexpr long long kDrainCycles = 1ll << 31;  // post-abort wait for TMA loads in flight
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long long budget) {
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
@@ -161,6 +162,7 @@ struct __align__(8) DkdvBars {
     uint64_t q_full[4], q_empty[4], do_full[4], do_empty[4];
     uint64_t st_full, dp_full, p_ready, ds_ready, acc_done, acc_free;
     uint64_t stats_ready[2];  // all elementwise threads staged a query block's lse2 / Dr
+    uint64_t mma_drain;       // abort path: completion of the MMAs already issued
     SchedRing sched;
 };
 
@@ -230,7 +232,7 @@ __device__ void dkdv_producer(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, u
         if (!ok) break;
     }
     if (aborting(wd)) {
-        const long long budget = wd.budget;
+        const long long budget = kDrainCycles;  // loads in flight land within microseconds
         for (uint32_t k = qr.i > (uint32_t)C::kDkdvQStages ? qr.i - C::kDkdvQStages : 0; k < qr.i; ++k)
             drain_wait(smem_u32(&bars.q_full[k % C::kDkdvQStages]), (k / C::kDkdvQStages) & 1, budget);
         for (uint32_t k = dr.i > (uint32_t)C::kDkdvDoStages ? dr.i - C::kDkdvDoStages : 0; k < dr.i; ++k)
@@ -491,6 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_tc_kernel(const __grid_const
         mbar_init(smem_u32(&bars.acc_free), kEw);
         mbar_init(smem_u32(&bars.stats_ready[0]), kEw);
         mbar_init(smem_u32(&bars.stats_ready[1]), kEw);
+        mbar_init(smem_u32(&bars.mma_drain), 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&bars.sched.full[s]), 1);
             mbar_init(smem_u32(&bars.sched.empty[s]), kSchedConsumers + 1);  // + the dO producer
@@ -511,7 +514,13 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_tc_kernel(const __grid_const
     if (warp < 4) {
         regs_dec<C::kRegsProducer>();
         if ((warp == 0 || warp == 2) && lane == 0) dkdv_producer<D>(a, bars, sK, sV, sQ, sDO, warp == 2, wd);
-        else if (warp == 1 && lane == 0) dkdv_mma<D, kBF16>(a, bars, sK, sV, sQ, sDO, tmem, wd);
+        else if (warp == 1 && lane == 0) {
+            dkdv_mma<D, kBF16>(a, bars, sK, sV, sQ, sDO, tmem, wd);
+            if (aborting(wd)) {  // let issued MMAs finish before TMEM is freed
+                tc_commit(smem_u32(&bars.mma_drain));
+                drain_wait(smem_u32(&bars.mma_drain), 0, kDrainCycles);
+            }
+        }
     } else {
         regs_inc<C::kRegsEw>();
         dkdv_elementwise<D, kBF16, Tg>(a, bars, stats, tmem, wd);
@@ -545,6 +554,7 @@ struct __align__(8) DqBars {
     uint64_t q_full, q_empty;
     uint64_t k_full[8], k_empty[8], v_full[8], v_empty[8];
     uint64_t sp_full, sp_free, ds_ready, acc_done, acc_free;
+    uint64_t mma_drain;  // abort path: completion of the MMAs already issued
     SchedRing sched;
 };
 
@@ -599,7 +609,7 @@ __device__ void dq_producer(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint3
         if (!ok) break;
     }
     if (aborting(wd)) {
-        const long long budget = wd.budget;
+        const long long budget = kDrainCycles;  // loads in flight land within microseconds
         for (uint32_t k = kr.i > (uint32_t)C::kDqKStages ? kr.i - C::kDqKStages : 0; k < kr.i; ++k)
             drain_wait(smem_u32(&bars.k_full[k % C::kDqKStages]), (k / C::kDqKStages) & 1, budget);
         for (uint32_t k = vr.i > (uint32_t)C::kDqVStages ? vr.i - C::kDqVStages : 0; k < vr.i; ++k)
@@ -810,6 +820,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_tc_kernel(const __grid_constan
             mbar_init(smem_u32(&bars.v_empty[s]), 1);
         }
         mbar_init(smem_u32(&bars.sp_full), 1);
+        mbar_init(smem_u32(&bars.mma_drain), 1);
         mbar_init(smem_u32(&bars.sp_free), kEw);
         mbar_init(smem_u32(&bars.ds_ready), kEw);
         mbar_init(smem_u32(&bars.acc_done), 1);
@@ -834,7 +845,13 @@ __global__ void __launch_bounds__(kThreads, 1) dq_tc_kernel(const __grid_constan
     if (warp < 4) {
         regs_dec<C::kRegsProducer>();
         if (warp == 0 && lane == 0) dq_producer<D>(a, bars, sQ, sDO, sK, sV, wd);
-        else if (warp == 1 && lane == 0) dq_mma<D, kBF16>(a, bars, sQ, sDO, sK, sV, tmem, wd);
+        else if (warp == 1 && lane == 0) {
+            dq_mma<D, kBF16>(a, bars, sQ, sDO, sK, sV, tmem, wd);
+            if (aborting(wd)) {  // let issued MMAs finish before TMEM is freed
+                tc_commit(smem_u32(&bars.mma_drain));
+                drain_wait(smem_u32(&bars.mma_drain), 0, kDrainCycles);
+            }
+        }
     } else {
         regs_inc<C::kRegsEw>();
         dq_elementwise<D, kBF16, Tg>(a, bars, tmem, wd);

@@ -95,6 +95,7 @@ struct __align__(8) FwdBars {
     uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
     uint64_t s_full[NQT], p_full[NQT], o_done[NQT], o_free[NQT];
     uint64_t sched_full[2], sched_empty[2];
+    uint64_t mma_drain;  // abort path: completion of the MMAs already issued
 };
 
 struct ItemInfo {
@@ -137,6 +138,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
 }
 
 // Bounded wait for outstanding TMA writes before the CTA exits after an abort.
+constexpr long long kDrainCycles = 1ll << 31;
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long long budget) {
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
@@ -203,7 +205,7 @@ __device__ void producer(const TcFwdArgs &a, FwdBars &bars, int *sched_item, uin
     }
     if (aborting(wd)) {
         // the newest load of every slot may still be landing in shared memory
-        const long long budget = wd.budget;
+        const long long budget = kDrainCycles;  // loads in flight land within microseconds
         for (uint32_t k = kr.i > (uint32_t)C::kKStages ? kr.i - C::kKStages : 0; k < kr.i; ++k)
             drain_wait(smem_u32(&bars.k_full[k % C::kKStages]), (k / C::kKStages) & 1, budget);
         for (uint32_t k = vr.i > (uint32_t)C::kVStages ? vr.i - C::kVStages : 0; k < vr.i; ++k)
@@ -501,6 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             mbar_init(smem_u32(&bars.sched_full[s]), 1);
             mbar_init(smem_u32(&bars.sched_empty[s]), kSchedConsumers);
         }
+        mbar_init(smem_u32(&bars.mma_drain), 1);
         fence_mbar_init();
         prefetch_tmap(&a.tq);
         prefetch_tmap(&a.tk);
@@ -519,7 +522,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         if (warp == 0) {
             if (lane == 0) producer<D>(a, bars, sched_item, sQ, sK, sV, wd);
         } else if (warp == 1) {
-            if (lane == 0) mma_issuer<D, kBF16>(a, bars, sched_item, sQ, sK, sV, tmem, wd);
+            if (lane == 0) {
+                mma_issuer<D, kBF16>(a, bars, sched_item, sQ, sK, sV, tmem, wd);
+                if (aborting(wd)) {  // let issued MMAs finish before TMEM is freed
+                    tc_commit(smem_u32(&bars.mma_drain));
+                    drain_wait(smem_u32(&bars.mma_drain), 0, kDrainCycles);
+                }
+            }
         }
     } else {
         regs_inc<C::kRegsSoftmax>();
