@@ -347,12 +347,15 @@ def main():
     dominant = max(("fwd", "bwd_dkdv", "bwd_dq"), key=lambda s: stage_ms[s])
     family = {"fwd": fcall.selected_kernel(), "bwd_dkdv": bcall.selected_kernel(),
               "bwd_dq": bcall.selected_kernel()}
-    kernel_files = {("fwd", "simt"): ["online_softmax_attention_gb300/csrc/fwd_simt.cu"],
-                    ("fwd", "tc"): ["online_softmax_attention_gb300/csrc/fwd_tc.cu"],
-                    ("bwd_dkdv", "simt"): ["online_softmax_attention_gb300/csrc/bwd_simt.cu"],
-                    ("bwd_dq", "simt"): ["online_softmax_attention_gb300/csrc/bwd_simt.cu"],
-                    ("bwd_dkdv", "tc"): ["online_softmax_attention_gb300/csrc/bwd_tc.cu"],
-                    ("bwd_dq", "tc"): ["online_softmax_attention_gb300/csrc/bwd_tc.cu"]}
+    csrc = "online_softmax_attention_gb300/csrc/"
+    shared = [csrc + "common.cuh", csrc + "internal.h"]
+    tc_shared = shared + [csrc + "sm100.cuh"]
+    kernel_files = {("fwd", "simt"): [csrc + "fwd_simt.cu"] + shared,
+                    ("fwd", "tc"): [csrc + "fwd_tc.cu"] + tc_shared,
+                    ("bwd_dkdv", "simt"): [csrc + "bwd_simt.cu"] + shared,
+                    ("bwd_dq", "simt"): [csrc + "bwd_simt.cu"] + shared,
+                    ("bwd_dkdv", "tc"): [csrc + "bwd_tc.cu"] + tc_shared,
+                    ("bwd_dq", "tc"): [csrc + "bwd_tc.cu"] + tc_shared}
     using_tc = family[dominant] == "tc"
     achieved = stage_flops[dominant] / (stage_ms[dominant] * 1e-3) / 1e12
     if using_tc:
