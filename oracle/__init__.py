@@ -59,6 +59,10 @@ def _load():
             ctypes.c_double, ctypes.c_int,
             ctypes.c_int, _i64p, _i32p, _dp,
             ctypes.c_int, _i64p, _i32p, _dp, _dp, ctypes.c_int]
+        lib.oracle_attn_merge.restype = ctypes.c_int
+        lib.oracle_attn_merge.argtypes = [
+            ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _dp, _dp, _dp, _dp,
+            ctypes.c_int]
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -187,6 +191,29 @@ def bwd(q, k, v, dO, *, causal: bool, scale: float | None = None, cu_seqlens_q=N
     if rc != 0:
         raise ValueError(f"oracle_attn_bwd rejected its arguments (rc={rc})")
     return dq, dk, dv
+
+
+def merge(o_parts, lse_parts, *, threads: int = 0):
+    """Attention over the union of C disjoint key sets from each set's result.
+
+    ``o_parts`` is (C, T, H, D), ``lse_parts`` is (C, H, T); returns float64
+    ``(o (T, H, D), lse (H, T))`` with lse = ln sum_c exp(lse_c) and
+    o = sum_c exp(lse_c - lse) o_c (rows whose partials are all -inf: o = 0,
+    lse = -inf).
+    """
+    op, lp = _f64(o_parts), _f64(lse_parts)
+    if op.ndim != 4:
+        raise ValueError(f"o_parts must be (C, T, H, D), got shape {op.shape}")
+    C, T, H, D = op.shape
+    if lp.shape != (C, H, T):
+        raise ValueError(f"lse_parts must be (C, H, T) = {(C, H, T)}, got {lp.shape}")
+    o = np.zeros((T, H, D), dtype=np.float64)
+    lse = np.zeros((H, T), dtype=np.float64)
+    rc = _load().oracle_attn_merge(C, T, H, D, _ptr(op, _dp), _ptr(lp, _dp), _ptr(o, _dp),
+                                   _ptr(lse, _dp), int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle_attn_merge rejected its arguments (rc={rc})")
+    return o, lse
 
 
 if __name__ == "__main__":  # pragma: no cover - manual build hook

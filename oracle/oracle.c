@@ -51,6 +51,19 @@
  *  - Causal is defined only for a sequence whose query and key lengths are
  *    equal; other inputs return -1.
  *
+ *  - Merge of partial results over disjoint key sets (the split-K forward of
+ *    the Vx issue "Chunked-dot Reduce lowering: shorten the reduction
+ *    dependency chain", measurement section: split-K with C = 8 key chunks).
+ *    Attention over the union of C disjoint key sets, from each set's own
+ *    result (O_c, lse_c): softmax over the union weighs set c by
+ *    exp(lse_c) / sum_c' exp(lse_c'), so
+ *        lse = ln sum_c exp(lse_c),   O = sum_c exp(lse_c - lse) O_c.
+ *    This is the (m, l, U) state merge of the OCANNL page's block recurrence
+ *    (fourth bullet) with each partial's state written as m_c = lse_c,
+ *    l_c = 1, U_c = O_c.  The exponentials are taken relative to
+ *    M = max_c lse_c.  A partial with lse_c = -inf admits no key and has
+ *    weight 0; if every partial is -inf the row gets O = 0, lse = -inf.
+ *
  * Layout: q, o, dq, dO are (T_q, H, D) row-major; k, v, dk, dv are (T_k, H, D);
  * lse is (H, T_q).  cu_q / cu_k hold n_seq + 1 cumulative offsets starting at 0.
  * All arrays are host memory owned by the caller.
@@ -392,5 +405,43 @@ int oracle_attn_bwd(int n_seq, const int32_t *cu_q, const int32_t *cu_k, int H, 
     free(m_st);
     free(l_st);
     free(c_st);
+    return 0;
+}
+
+/*
+ * Merge of C partial results (see the header comment): o_parts is (C, T, H, D),
+ * lse_parts is (C, H, T), o is (T, H, D), lse is (H, T).  Returns 0, or -1 on
+ * bad sizes.
+ */
+int oracle_attn_merge(int C, int64_t T, int H, int D, const double *o_parts,
+                      const double *lse_parts, double *o, double *lse, int n_threads)
+{
+    if (C < 1 || T < 0 || H < 1 || D < 1) return -1;
+    set_threads(n_threads);
+    const int64_t n_rows = T * H;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < n_rows; ++r) {
+        const int64_t t = r / H;
+        const int h = (int)(r % H);
+        double M = -INFINITY;
+        for (int c = 0; c < C; ++c) {
+            const double x = lse_parts[((int64_t)c * H + h) * T + t];
+            if (x > M) M = x;
+        }
+        double *orow = o + r * D;
+        for (int d = 0; d < D; ++d) orow[d] = 0.0;
+        if (M == -INFINITY) {
+            lse[(int64_t)h * T + t] = -INFINITY;
+            continue;
+        }
+        double l = 0.0;
+        for (int c = 0; c < C; ++c) l += exp(lse_parts[((int64_t)c * H + h) * T + t] - M);
+        for (int c = 0; c < C; ++c) {
+            const double w = exp(lse_parts[((int64_t)c * H + h) * T + t] - M) / l;
+            const double *prow = o_parts + ((int64_t)c * T * H + r) * D;
+            for (int d = 0; d < D; ++d) orow[d] += w * prow[d];
+        }
+        lse[(int64_t)h * T + t] = M + log(l);
+    }
     return 0;
 }

@@ -309,3 +309,75 @@ def test_backward_sampled_rows_equal_full():
     np.testing.assert_array_equal(sq, dq[rows[0], rows[1]])
     np.testing.assert_array_equal(sk, dk[keys[0], keys[1]])
     np.testing.assert_array_equal(sv, dv[keys[0], keys[1]])
+
+
+# --- merge of partial results over disjoint key sets (split-K) -------------------
+
+def _ev_inf(x):
+    if x == "-inf":
+        return -math.inf
+    if isinstance(x, list):
+        return [_ev_inf(y) for y in x]
+    return _ev(x)
+
+
+def _merge_cases():
+    with open(os.path.join(GOLDEN, "merge_cases.json")) as f:
+        return json.load(f)["cases"]
+
+
+@pytest.mark.parametrize("case", _merge_cases(), ids=lambda c: c["name"])
+def test_merge_hand_cases(case):
+    op, lp = (np.array(_ev_inf(case[n]), dtype=np.float64) for n in ("o_parts", "lse_parts"))
+    o, lse = oracle.merge(op, lp)
+    np.testing.assert_allclose(o, np.array(_ev_inf(case["o"])), rtol=0, atol=1e-13)
+    np.testing.assert_array_equal(np.isneginf(lse), np.isneginf(np.array(_ev_inf(case["lse"]))))
+    fin = np.isfinite(lse)
+    np.testing.assert_allclose(lse[fin], np.array(_ev_inf(case["lse"]))[fin], rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("bounds", [(0, 40, 41, 97), (0, 1, 97), (0, 13, 26, 50, 77, 90, 97), (0, 97)])
+def test_merge_of_key_chunks_equals_attention_over_all_keys(bounds):
+    """Attention over keys split into disjoint chunks, each chunk attended on
+    its own and then merged, is attention over all keys (full relation)."""
+    q, k, v = _rand((23, 3, 16), 71), _rand((97, 3, 16), 72), _rand((97, 3, 16), 73)
+    parts = [oracle.fwd(q, k[a:b], v[a:b], causal=False, scale=0.3)
+             for a, b in zip(bounds[:-1], bounds[1:])]
+    o, lse = oracle.merge(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+    o_ref, lse_ref = oracle.fwd(q, k, v, causal=False, scale=0.3)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-13)
+
+
+def test_merge_with_an_empty_key_chunk():
+    """A chunk with no key (lse = -inf, O = 0 from the forward) changes nothing."""
+    q, k, v = _rand((9, 2, 8), 74), _rand((30, 2, 8), 75), _rand((30, 2, 8), 76)
+    a = oracle.fwd(q, k[:0], v[:0], causal=False)
+    b = oracle.fwd(q, k, v, causal=False)
+    assert np.all(np.isneginf(a[1])) and not np.any(a[0])
+    o, lse = oracle.merge(np.stack([a[0], b[0]]), np.stack([a[1], b[1]]))
+    np.testing.assert_array_equal(o, b[0])
+    np.testing.assert_array_equal(lse, b[1])
+
+
+def test_merge_is_invariant_to_part_order():
+    rng = np.random.default_rng(77)
+    op, lp = rng.standard_normal((5, 11, 2, 8)), 3 * rng.standard_normal((5, 2, 11))
+    perm = [3, 0, 4, 2, 1]
+    o1, l1 = oracle.merge(op, lp)
+    o2, l2 = oracle.merge(op[perm], lp[perm])
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-13)
+
+
+def test_merge_large_lse_is_stable_and_matches_library_logsumexp():
+    from scipy.special import logsumexp, softmax
+    rng = np.random.default_rng(78)
+    op = rng.standard_normal((4, 6, 1, 8))
+    lp = 2000.0 * rng.standard_normal((4, 1, 6))
+    o, lse = oracle.merge(op, lp)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+    np.testing.assert_allclose(lse, logsumexp(lp, axis=0), rtol=1e-15, atol=1e-12)
+    w = softmax(lp[:, 0, :], axis=0)  # (C, T)
+    np.testing.assert_allclose(o[:, 0, :], np.einsum("ct,ctd->td", w, op[:, :, 0, :]), rtol=0,
+                               atol=1e-12)
