@@ -62,7 +62,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 1
+#define ATTN_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define ATTN_API __attribute__((visibility("default")))
@@ -114,7 +114,12 @@ typedef struct attn_fwd_args {
     size_t workspace_bytes;
     int32_t kernel;       /* attn_kernel */
     int32_t num_ctas;     /* persistent grid size; 0 = one per SM */
+    int32_t num_splits;   /* key splits per query tile (split-K): 0 = chosen by the
+                             library (see attn_fwd_num_splits), 1 = none, 2..ATTN_MAX_SPLITS */
 } attn_fwd_args;
+
+/* Upper bound of attn_fwd_args.num_splits and of attn_merge_args.n_parts. */
+#define ATTN_MAX_SPLITS 64
 
 typedef struct attn_bwd_args {
     attn_tensor q, k, v;  /* in: as in the forward */
@@ -136,19 +141,59 @@ typedef struct attn_bwd_args {
     int32_t num_ctas;
 } attn_bwd_args;
 
+/* Partial attention results over disjoint key sets, to be merged
+ * (attn_merge).  Partial c is attention of the same query rows over its own
+ * key set: its output O_c (normalised by its own row sum) and its row
+ * log-sum-exp lse_c (-inf when it admits no key; O_c is then ignored). */
+typedef struct attn_merge_args {
+    const float *o_parts;   /* in:  (n_parts, n_q, H, D) f32, contiguous */
+    const float *lse_parts; /* in:  (n_parts, H, n_q) f32, contiguous */
+    attn_tensor o;          /* out: (n_q, H, D), o_dtype; may not overlap the inputs */
+    float *lse;             /* out: (H, n_q) f32, or NULL */
+    int32_t n_parts;        /* 1..ATTN_MAX_SPLITS */
+    int32_t n_q, H, D;      /* D: a multiple of 4, at most 256 */
+    int32_t o_dtype;        /* attn_dtype */
+} attn_merge_args;
+
 /* Library ABI version (ATTN_ABI_VERSION) and struct sizes, for bindings to
  * check their mirrors of the structs above. */
 ATTN_API int attn_abi_version(void);
 ATTN_API size_t attn_fwd_args_size(void);
 ATTN_API size_t attn_bwd_args_size(void);
+ATTN_API size_t attn_merge_args_size(void);
 
-/* Bytes of device workspace the call needs (depends on n_seq, H, n_q). */
+/* Bytes of device workspace the call needs (depends on n_seq, H, n_q, and
+ * for the forward on the number of key splits: n_splits > 1 adds the partial
+ * results, n_splits * n_q * H * (D + 1) * 4 bytes). */
 ATTN_API size_t attn_fwd_workspace_bytes(const attn_fwd_args *a);
 ATTN_API size_t attn_bwd_workspace_bytes(const attn_bwd_args *a);
 
 /* Forward: writes o and lse.  Launches a schedule-preparation kernel and one
- * persistent attention kernel on `stream`. */
+ * persistent attention kernel on `stream`; with key splits (split-K) the
+ * attention kernel writes one partial result per split into the workspace
+ * and a merge kernel (as attn_merge) combines them into o and lse. */
 ATTN_API int attn_fwd(const attn_fwd_args *a, void *stream);
+
+/* Key splits a forward with these arguments runs (>= 1), resolving
+ * num_splits = 0, or a negative attn_status.  Host-only; launches nothing.
+ *
+ * Split-K (Vx issue "Chunked-dot Reduce lowering: shorten the reduction
+ * dependency chain", measurement section: the record FP32 kernel splits the
+ * keys in C = 8 chunks): each query tile's key tiles are cut into n_splits
+ * contiguous chunks that run as separate work items, so shapes with few
+ * query tiles still fill the GPU.  The automatic choice splits only when the
+ * query tiles alone leave most SMs idle and every chunk keeps at least two
+ * key tiles. */
+ATTN_API int attn_fwd_num_splits(const attn_fwd_args *a);
+
+/* Merge of partial results over disjoint key sets into attention over their
+ * union (the split-K merge; with each partial's online-softmax state written
+ * as m_c = lse_c, l_c = 1, U_c = O_c, this is the (m, l, U) combination of the
+ * OCANNL "Module Ir.Online_softmax" page, fourth bullet):
+ *     lse = ln sum_c exp(lse_c),   O = sum_c exp(lse_c - lse) O_c.
+ * A row whose partials are all -inf gets O = 0, lse = -inf.  One kernel on
+ * `stream`; no workspace. */
+ATTN_API int attn_merge(const attn_merge_args *a, void *stream);
 
 /* Backward: writes dq, dk, dv.  Equivalent to attn_bwd_preprocess, then
  * attn_bwd_dkdv, then attn_bwd_dq on the same stream and workspace. */
@@ -179,7 +224,8 @@ ATTN_API int attn_bwd_selected_kernel(const attn_bwd_args *a);
 
 /* Forward for callers that cannot allocate device memory (no counterpart on
  * the pages; a deployment convenience).  Same arguments and results as
- * attn_fwd, except that `workspace` / `workspace_bytes` are ignored: the
+ * attn_fwd, except that `num_splits` is taken as 1 (no key splits) and
+ * `workspace` / `workspace_bytes` are ignored: the
  * scheduler's scratch lives in a fixed 64 KiB array inside this library's
  * device memory, which every GPU that loads the library keeps until the
  * process exits.  No call allocates anything.

@@ -7,6 +7,8 @@ argument structs:
 
 * ``fwd(q, k, v, causal=..., cu_seqlens_q=...)`` -> ``(o, lse)``
 * ``bwd(q, k, v, o, lse, dout, causal=...)`` -> ``(dq, dk, dv)``
+* ``merge(o_parts, lse_parts)`` -> ``(o, lse)``: attention over the union of
+  disjoint key sets from each set's result (the split-K merge)
 * ``FwdCall`` / ``BwdCall`` hold prepared argument structs for repeated
   launches (the benchmark and CUDA-graph capture use them).
 
@@ -25,8 +27,8 @@ from . import _abi
 from ._abi import (ATTN_BF16, ATTN_CAUSAL, ATTN_F16, ATTN_F32, ATTN_FULL, ATTN_KERNEL_AUTO,
                    ATTN_KERNEL_SIMT, ATTN_KERNEL_TC, AttnError, check)
 
-__all__ = ["fwd", "bwd", "FwdCall", "BwdCall", "device_status", "launch_count", "AttnError",
-           "library_path"]
+__all__ = ["fwd", "bwd", "merge", "FwdCall", "BwdCall", "MergeCall", "device_status",
+           "launch_count", "AttnError", "library_path"]
 
 _DT = {torch.float16: ATTN_F16, torch.bfloat16: ATTN_BF16, torch.float32: ATTN_F32}
 _KERNELS = {"auto": ATTN_KERNEL_AUTO, "simt": ATTN_KERNEL_SIMT, "tc": ATTN_KERNEL_TC}
@@ -93,8 +95,9 @@ class FwdCall:
 
     def __init__(self, q, k, v, *, causal: bool = False, scale: float | None = None,
                  cu_seqlens_q=None, cu_seqlens_k=None, out_dtype: torch.dtype | None = None,
-                 kernel: str = "auto", num_ctas: int = 0, out: torch.Tensor | None = None,
-                 lse: torch.Tensor | None = None, workspace: torch.Tensor | None = None):
+                 kernel: str = "auto", num_ctas: int = 0, num_splits: int = 0,
+                 out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                 workspace: torch.Tensor | None = None):
         if q.dtype != k.dtype or q.dtype != v.dtype:
             raise TypeError("q, k, v must share one dtype")
         dev = q.device
@@ -118,6 +121,7 @@ class FwdCall:
         a.cu_seqlens_k = self.cu_k.data_ptr() if self.cu_k is not None else None
         a.kernel = _KERNELS[kernel]
         a.num_ctas = int(num_ctas)
+        a.num_splits = int(num_splits)
         lib = _abi.load()
         need = lib.attn_fwd_workspace_bytes(ctypes.byref(a))
         self.workspace = workspace if workspace is not None else _workspace(need, dev)
@@ -135,6 +139,50 @@ class FwdCall:
         """"tc" or "simt": the kernel family these arguments run."""
         return _selected(_abi.load().attn_fwd_selected_kernel(ctypes.byref(self.args)),
                          "attn_fwd_selected_kernel")
+
+    def num_splits(self) -> int:
+        """Key splits (split-K chunks) these arguments run, 1 = none."""
+        n = int(_abi.load().attn_fwd_num_splits(ctypes.byref(self.args)))
+        if n < 0:
+            check(n, "attn_fwd_num_splits")
+        return n
+
+
+class MergeCall:
+    """Prepared merge of partial results over disjoint key sets.
+
+    ``o_parts`` is (C, T, H, D) float32 contiguous, ``lse_parts`` (C, H, T)
+    float32 contiguous (-inf marks a partial that admits no key).
+    """
+
+    def __init__(self, o_parts: torch.Tensor, lse_parts: torch.Tensor, *,
+                 out_dtype: torch.dtype = torch.float32, out: torch.Tensor | None = None,
+                 lse: torch.Tensor | None = None):
+        if o_parts.dtype != torch.float32 or lse_parts.dtype != torch.float32:
+            raise TypeError("o_parts and lse_parts must be float32")
+        if o_parts.dim() != 4 or not o_parts.is_contiguous() or not lse_parts.is_contiguous():
+            raise ValueError("o_parts must be contiguous (C, T, H, D), lse_parts contiguous (C, H, T)")
+        C, T, H, D = o_parts.shape
+        if tuple(lse_parts.shape) != (C, H, T):
+            raise ValueError(f"lse_parts must be {(C, H, T)}, got {tuple(lse_parts.shape)}")
+        dev = o_parts.device
+        self.o = out if out is not None else torch.empty((T, H, D), dtype=out_dtype, device=dev)
+        self.lse = lse if lse is not None else torch.empty((H, T), dtype=torch.float32, device=dev)
+        self.inputs = (o_parts, lse_parts)
+        a = _abi.MergeArgs()
+        a.o_parts = o_parts.data_ptr() if o_parts.numel() else None
+        a.lse_parts = lse_parts.data_ptr() if lse_parts.numel() else None
+        a.o = _view(self.o, "out")
+        a.lse = self.lse.data_ptr() if self.lse.numel() else None
+        a.n_parts, a.n_q, a.H, a.D = C, T, H, D
+        a.o_dtype = _dtype_code(self.o.dtype)
+        self.args = a
+        self._fn = _abi.load().attn_merge
+
+    def run(self, stream: torch.cuda.Stream | None = None):
+        s = stream if stream is not None else torch.cuda.current_stream()
+        check(self._fn(ctypes.byref(self.args), ctypes.c_void_p(s.cuda_stream)), "attn_merge")
+        return self.o, self.lse
 
 
 class BwdCall:
@@ -202,11 +250,20 @@ class BwdCall:
 
 def fwd(q, k, v, *, causal: bool = False, scale: float | None = None, cu_seqlens_q=None,
         cu_seqlens_k=None, out_dtype: torch.dtype | None = None, kernel: str = "auto",
-        num_ctas: int = 0):
-    """Attention forward.  Returns ``(o, lse)``; lse is (H, T_q) f32, natural log."""
+        num_ctas: int = 0, num_splits: int = 0):
+    """Attention forward.  Returns ``(o, lse)``; lse is (H, T_q) f32, natural log.
+
+    ``num_splits``: key splits per query tile (split-K); 0 lets the library
+    choose, 1 disables splitting."""
     return FwdCall(q, k, v, causal=causal, scale=scale, cu_seqlens_q=cu_seqlens_q,
                    cu_seqlens_k=cu_seqlens_k, out_dtype=out_dtype, kernel=kernel,
-                   num_ctas=num_ctas).run()
+                   num_ctas=num_ctas, num_splits=num_splits).run()
+
+
+def merge(o_parts, lse_parts, *, out_dtype: torch.dtype = torch.float32):
+    """Attention over the union of C disjoint key sets from each set's result:
+    lse = ln sum_c exp(lse_c), o = sum_c exp(lse_c - lse) o_c.  Returns ``(o, lse)``."""
+    return MergeCall(o_parts, lse_parts, out_dtype=out_dtype).run()
 
 
 def bwd(q, k, v, o, lse, dout, *, causal: bool = False, scale: float | None = None,

@@ -12,13 +12,14 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_lib", "libattn_gb300.so")
 
-ABI_VERSION = 1
+ABI_VERSION = 2
 
 ATTN_OK, ATTN_EINVAL, ATTN_EUNSUPPORTED, ATTN_ECUDA, ATTN_ETIMEOUT, ATTN_EWORKSPACE = 0, -1, -2, -3, -4, -5
 ATTN_F16, ATTN_BF16, ATTN_F32 = 0, 1, 2
 ATTN_FULL, ATTN_CAUSAL = 0, 1
 ATTN_KERNEL_AUTO, ATTN_KERNEL_SIMT, ATTN_KERNEL_TC = 0, 1, 2
 ATTN_NOALLOC_MAX_SEQ = 16367
+ATTN_MAX_SPLITS = 64
 
 # every symbol include/attn.h declares
 EXPORTS = (
@@ -27,7 +28,8 @@ EXPORTS = (
     "attn_bwd_preprocess", "attn_bwd_dkdv", "attn_bwd_dq", "attn_fwd_simple",
     "attn_device_status", "attn_launch_count", "attn_strerror", "attn_last_error_string",
     "attn_fwd_selected_kernel", "attn_bwd_selected_kernel", "attn_fwd_noalloc",
-    "attn_selftest_exp2", "attn_set_watchdog_cycles",
+    "attn_selftest_exp2", "attn_set_watchdog_cycles", "attn_merge_args_size",
+    "attn_fwd_num_splits", "attn_merge",
 )
 
 
@@ -45,7 +47,15 @@ class FwdArgs(ctypes.Structure):
         ("o_dtype", ctypes.c_int32), ("n_seq", ctypes.c_int32),
         ("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_k", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
-        ("kernel", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
+        ("kernel", ctypes.c_int32), ("num_ctas", ctypes.c_int32), ("num_splits", ctypes.c_int32),
+    ]
+
+
+class MergeArgs(ctypes.Structure):
+    _fields_ = [
+        ("o_parts", ctypes.c_void_p), ("lse_parts", ctypes.c_void_p), ("o", AttnTensor),
+        ("lse", ctypes.c_void_p), ("n_parts", ctypes.c_int32), ("n_q", ctypes.c_int32),
+        ("H", ctypes.c_int32), ("D", ctypes.c_int32), ("o_dtype", ctypes.c_int32),
     ]
 
 
@@ -78,11 +88,14 @@ def load() -> ctypes.CDLL:
             "`python online_softmax_attention_gb300/build.py`")
     lib = ctypes.CDLL(LIB_PATH)
     vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
-    fa, ba = ctypes.POINTER(FwdArgs), ctypes.POINTER(BwdArgs)
+    fa, ba, ma = ctypes.POINTER(FwdArgs), ctypes.POINTER(BwdArgs), ctypes.POINTER(MergeArgs)
     sigs = {
         "attn_abi_version": (ctypes.c_int, []),
         "attn_fwd_args_size": (sz, []),
         "attn_bwd_args_size": (sz, []),
+        "attn_merge_args_size": (sz, []),
+        "attn_fwd_num_splits": (ctypes.c_int, [fa]),
+        "attn_merge": (ctypes.c_int, [ma, vp]),
         "attn_fwd_workspace_bytes": (sz, [fa]),
         "attn_bwd_workspace_bytes": (sz, [ba]),
         "attn_fwd": (ctypes.c_int, [fa, vp]),
@@ -109,7 +122,8 @@ def load() -> ctypes.CDLL:
     if lib.attn_abi_version() != ABI_VERSION:
         raise ImportError(f"libattn_gb300 ABI {lib.attn_abi_version()} != binding ABI {ABI_VERSION}")
     if lib.attn_fwd_args_size() != ctypes.sizeof(FwdArgs) or \
-            lib.attn_bwd_args_size() != ctypes.sizeof(BwdArgs):
+            lib.attn_bwd_args_size() != ctypes.sizeof(BwdArgs) or \
+            lib.attn_merge_args_size() != ctypes.sizeof(MergeArgs):
         raise ImportError("libattn_gb300 struct layout does not match the binding")
     _lib = lib
     return lib

@@ -118,19 +118,57 @@ Sched sched_at(void *base) {
 
 // ---- forward ---------------------------------------------------------------
 
-int build_fwd(const attn_fwd_args *a, FwdParams &p, bool &use_tc) {
+// Split-K choice when the caller leaves it to the library: split only when the
+// query tiles alone fill less than half of the resident CTA slots, into as
+// many chunks as fill the slots once, keeping at least two key tiles per chunk
+// (of the average sequence; the causal relation halves the keys a tile scans
+// on average).
+int auto_splits(const FwdParams &p, bool use_tc) {
+    const int64_t q_block = use_tc ? tc_fwd_block_rows(p) : kSimtBlock;
+    const int64_t k_block = use_tc ? 128 : 64;
+    const int64_t per_seq_q = p.n_q / p.n_seq, per_seq_k = p.n_k / p.n_seq;
+    const int64_t q_tiles = (int64_t)p.n_seq * ((per_seq_q + q_block - 1) / q_block);
+    const int64_t items = (q_tiles > 0 ? q_tiles : 1) * p.H;
+    const int64_t slots = (int64_t)sm_count() * (use_tc ? 1 : fwd_simt_ctas_per_sm(p));
+    if (2 * items > slots) return 1;
+    int64_t k_tiles = (per_seq_k + k_block - 1) / k_block;
+    if (p.causal) k_tiles /= 2;
+    int64_t c = slots / items;
+    if (c > k_tiles / 2) c = k_tiles / 2;
+    if (c > ATTN_MAX_SPLITS) c = ATTN_MAX_SPLITS;
+    return c >= 2 ? (int)c : 1;
+}
+
+struct FwdLayout {
+    size_t o_parts, lse_parts, total;
+};
+
+FwdLayout fwd_layout(int n_seq, int n_q, int H, int D, int splits) {
+    FwdLayout L;
+    L.o_parts = sched_bytes(n_seq);
+    L.lse_parts = L.o_parts;
+    L.total = L.o_parts;
+    if (splits > 1) {
+        const size_t rows = (size_t)splits * (size_t)n_q * (size_t)H;
+        L.lse_parts = L.o_parts + align256(sizeof(float) * rows * (size_t)D);
+        L.total = L.lse_parts + align256(sizeof(float) * rows);
+    }
+    return L;
+}
+
+// Validates everything but the workspace and fills the kernel parameters that
+// do not depend on it; resolves the kernel family and the key splits.
+int plan_fwd(const attn_fwd_args *a, FwdParams &p, bool &use_tc) {
     if (!a) return ATTN_EINVAL;
     int rc = check_common(a->n_q, a->n_k, a->H, a->D, a->relation, a->dtype, a->n_seq,
                           a->cu_seqlens_q, a->cu_seqlens_k, a->scale);
     if (rc) return rc;
     if (a->o_dtype != a->dtype && a->o_dtype != ATTN_F32) return ATTN_EINVAL;
+    if (a->num_splits < 0 || a->num_splits > ATTN_MAX_SPLITS) return ATTN_EINVAL;
     const bool any_q = a->n_q > 0, any_k = a->n_k > 0;
     if (!valid_view(a->q, a->dtype, any_q) || !valid_view(a->o, a->o_dtype, any_q) ||
         !valid_view(a->k, a->dtype, any_k) || !valid_view(a->v, a->dtype, any_k))
         return ATTN_EINVAL;
-    if (!a->workspace || a->workspace_bytes < attn_fwd_workspace_bytes(a) ||
-        (reinterpret_cast<uintptr_t>(a->workspace) & 255))
-        return ATTN_EWORKSPACE;
     std::memset(&p, 0, sizeof(p));
     p.q = a->q.ptr; p.k = a->k.ptr; p.v = a->v.ptr; p.o = a->o.ptr; p.lse = a->lse;
     p.q_st = a->q.stride_tok; p.q_sh = a->q.stride_head;
@@ -144,11 +182,58 @@ int build_fwd(const attn_fwd_args *a, FwdParams &p, bool &use_tc) {
     p.dtype = a->dtype; p.o_dtype = a->o_dtype;
     p.n_seq = a->n_seq;
     p.cu_q = a->cu_seqlens_q; p.cu_k = a->cu_seqlens_k;
+    p.watchdog_cycles = watchdog_cycles();
+    rc = choose_tc(a->kernel, tc_fwd_supported(p), use_tc);
+    if (rc) return rc;
+    p.n_splits = a->num_splits > 0 ? a->num_splits : auto_splits(p, use_tc);
+    // work items (tiles x heads x splits) are numbered in int32
+    const int64_t tiles = (int64_t)a->H * ((int64_t)a->n_q / kSimtBlock + a->n_seq + 1);
+    if (tiles * p.n_splits >= (int64_t)1 << 31) return ATTN_EUNSUPPORTED;
+    return ATTN_OK;
+}
+
+int build_fwd(const attn_fwd_args *a, FwdParams &p, bool &use_tc) {
+    int rc = plan_fwd(a, p, use_tc);
+    if (rc) return rc;
+    const FwdLayout L = fwd_layout(a->n_seq, a->n_q, a->H, a->D, p.n_splits);
+    if (!a->workspace || a->workspace_bytes < L.total ||
+        (reinterpret_cast<uintptr_t>(a->workspace) & 255))
+        return ATTN_EWORKSPACE;
     p.sched = sched_at(a->workspace);
     p.status = status_ptr();
-    p.watchdog_cycles = watchdog_cycles();
     if (!p.status) return ATTN_ECUDA;
-    return choose_tc(a->kernel, tc_fwd_supported(p), use_tc);
+    return ATTN_OK;
+}
+
+// Kernel parameters of the split-K partial pass and of its merge: the
+// attention kernel writes chunk c's O_c (f32, token stride H*D, head stride D)
+// and lse_c into the workspace; the merge writes the caller's o and lse.
+void split_params(const attn_fwd_args *a, const FwdParams &p, FwdParams &part, MergeParams &m) {
+    const FwdLayout L = fwd_layout(a->n_seq, a->n_q, a->H, a->D, p.n_splits);
+    char *ws = static_cast<char *>(a->workspace);
+    float *o_parts = reinterpret_cast<float *>(ws + L.o_parts);
+    float *lse_parts = reinterpret_cast<float *>(ws + L.lse_parts);
+    part = p;
+    part.o = o_parts;
+    part.o_dtype = ATTN_F32;
+    part.o_st = (int64_t)a->H * a->D;
+    part.o_sh = a->D;
+    part.o_split_st = (int64_t)a->n_q * a->H * a->D;
+    part.lse = lse_parts;
+    part.lse_split_st = (int64_t)a->H * a->n_q;
+    std::memset(&m, 0, sizeof(m));
+    m.o_parts = o_parts;
+    m.lse_parts = lse_parts;
+    m.o = a->o.ptr;
+    m.lse = a->lse;
+    m.o_st = a->o.stride_tok;
+    m.o_sh = a->o.stride_head;
+    m.part_st = part.o_split_st;
+    m.n_parts = p.n_splits;
+    m.n_q = a->n_q;
+    m.H = a->H;
+    m.D = a->D;
+    m.o_dtype = a->o_dtype;
 }
 
 // ---- backward --------------------------------------------------------------
@@ -242,8 +327,15 @@ uint64_t attn_launch_count(void) { return g_launches.load(); }
 
 size_t attn_fwd_workspace_bytes(const attn_fwd_args *a) {
     if (!a || a->n_seq < 1) return 0;
-    return sched_bytes(a->n_seq);
+    FwdParams p;
+    bool use_tc = false;
+    // arguments the forward would reject need no split buffers
+    const int splits = plan_fwd(a, p, use_tc) == ATTN_OK ? p.n_splits : 1;
+    return fwd_layout(a->n_seq, a->n_q > 0 ? a->n_q : 0, a->H > 0 ? a->H : 0,
+                      a->D > 0 ? a->D : 0, splits).total;
 }
+
+size_t attn_merge_args_size(void) { return sizeof(attn_merge_args); }
 
 size_t attn_bwd_workspace_bytes(const attn_bwd_args *a) {
     if (!a || a->n_seq < 1 || a->H < 1 || a->n_q < 0) return 0;
@@ -259,9 +351,53 @@ int attn_fwd(const attn_fwd_args *a, void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int block = use_tc ? tc_fwd_block_rows(p) : kSimtBlock;
     cudaError_t e = launch_prep(p.cu_q, p.cu_k, p.n_seq, p.n_q, p.n_k, p.H, block, p.causal, 0,
-                                p.sched, p.status, s);
+                                p.n_splits, p.sched, p.status, s);
     if (e != cudaSuccess) return set_cuda_error(e);
-    e = use_tc ? launch_fwd_tc(p, a->num_ctas, s) : launch_fwd_simt(p, a->num_ctas, s);
+    if (p.n_splits == 1) {
+        e = use_tc ? launch_fwd_tc(p, a->num_ctas, s) : launch_fwd_simt(p, a->num_ctas, s);
+    } else {
+        FwdParams part;
+        MergeParams m;
+        split_params(a, p, part, m);
+        e = use_tc ? launch_fwd_tc(part, a->num_ctas, s) : launch_fwd_simt(part, a->num_ctas, s);
+        if (e == cudaSuccess) e = launch_merge(m, s);
+    }
+    if (e != cudaSuccess) return set_cuda_error(e);
+    return ATTN_OK;
+}
+
+int attn_fwd_num_splits(const attn_fwd_args *a) {
+    FwdParams p;
+    bool use_tc = false;
+    const int rc = plan_fwd(a, p, use_tc);
+    return rc ? rc : p.n_splits;
+}
+
+int attn_merge(const attn_merge_args *a, void *stream) {
+    if (!a) return ATTN_EINVAL;
+    if (a->n_parts < 1 || a->n_parts > ATTN_MAX_SPLITS || a->n_q < 0 || a->H < 1 || a->D < 4 ||
+        a->D > 256 || (a->D & 3) || !valid_dtype(a->o_dtype))
+        return ATTN_EINVAL;
+    if ((int64_t)a->n_q * a->H * a->n_parts >= (int64_t)1 << 31) return ATTN_EUNSUPPORTED;
+    if (a->n_q == 0) return ATTN_OK;
+    if (!a->o_parts || !aligned16(a->o_parts) || !a->lse_parts ||
+        (reinterpret_cast<uintptr_t>(a->lse_parts) & 3) || !valid_view(a->o, a->o_dtype, true))
+        return ATTN_EINVAL;
+    MergeParams m;
+    std::memset(&m, 0, sizeof(m));
+    m.o_parts = a->o_parts;
+    m.lse_parts = a->lse_parts;
+    m.o = a->o.ptr;
+    m.lse = a->lse;
+    m.o_st = a->o.stride_tok;
+    m.o_sh = a->o.stride_head;
+    m.part_st = (int64_t)a->n_q * a->H * a->D;
+    m.n_parts = a->n_parts;
+    m.n_q = a->n_q;
+    m.H = a->H;
+    m.D = a->D;
+    m.o_dtype = a->o_dtype;
+    cudaError_t e = launch_merge(m, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return set_cuda_error(e);
     return ATTN_OK;
 }
@@ -275,10 +411,10 @@ int attn_bwd_preprocess(const attn_bwd_args *a, void *stream) {
     const int kv_block = use_tc ? tc_bwd_kv_block(p) : kSimtBlock;
     const int q_block = use_tc ? tc_bwd_q_block(p) : kSimtBlock;
     cudaError_t e = launch_prep(p.cu_q, p.cu_k, p.n_seq, p.n_q, p.n_k, p.H, kv_block, p.causal, 1,
-                                p.sched_kv, p.status, s);
+                                1, p.sched_kv, p.status, s);
     if (e == cudaSuccess)
         e = launch_prep(p.cu_q, p.cu_k, p.n_seq, p.n_q, p.n_k, p.H, q_block, p.causal, 0,
-                        p.sched_q, p.status, s);
+                        1, p.sched_q, p.status, s);
     if (e == cudaSuccess) e = launch_bwd_preprocess(p, s);
     if (e != cudaSuccess) return set_cuda_error(e);
     return ATTN_OK;

@@ -68,19 +68,20 @@ __device__ __forceinline__ float exp2_approx(float x) {
 
 // ---- persistent scheduler -------------------------------------------------
 //
-// Work items are (sequence b, head h, tile t) triples, numbered
-// sequence-major, then head, then tile.  prefix[b] = H * (tiles of sequences
-// before b), written by the preparation kernel; item w belongs to the last
-// sequence whose prefix is <= w.  Tiles of one (b, h) are consecutive so that
-// the CTAs running at the same time share K/V in L2; `descending` orders them
+// Work items are (sequence b, head h, tile t, key split c) tuples, numbered
+// sequence-major, then head, then tile, then split (c < splits; splits = 1
+// without split-K).  prefix[b] = H * splits * (tiles of sequences before b),
+// written by the preparation kernel; item w belongs to the last sequence
+// whose prefix is <= w.  Tiles of one (b, h) are consecutive so that the CTAs
+// running at the same time share K/V in L2; `descending` orders them
 // longest-first for the causal relation.
 
 struct WorkItem {
-    int b, h, t, ntiles;
+    int b, h, t, ntiles, c;
 };
 
 __device__ __forceinline__ WorkItem map_item(int w, const int *prefix, int n_seq, int H,
-                                             bool descending) {
+                                             bool descending, int splits = 1) {
     int lo = 0, hi = n_seq - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -88,12 +89,15 @@ __device__ __forceinline__ WorkItem map_item(int w, const int *prefix, int n_seq
         else hi = mid - 1;
     }
     const int base = __ldg(prefix + lo);
-    const int ntiles = (__ldg(prefix + lo + 1) - base) / H;
+    const int per_head = (__ldg(prefix + lo + 1) - base) / H;  // tiles * splits
     const int r = w - base;
-    const int h = r / ntiles;
-    int t = r - h * ntiles;
+    const int h = r / per_head;
+    const int rem = r - h * per_head;
+    int t = splits == 1 ? rem : rem / splits;
+    const int c = rem - t * splits;
+    const int ntiles = per_head / splits;
     if (descending) t = ntiles - 1 - t;
-    return {lo, h, t, ntiles};
+    return {lo, h, t, ntiles, c};
 }
 
 // Offsets of sequence b (one sequence when cu is null).

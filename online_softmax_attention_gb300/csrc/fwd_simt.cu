@@ -9,6 +9,10 @@
 // sequence, and keys j > i under the causal relation, score -inf (the guarded
 // tail).  Scores are kept in the base-2 domain (s * scale * log2 e).
 //
+// Split-K: with n_splits > 1 every query tile is n_splits work items, each
+// scanning one contiguous chunk of the tile's key tiles and writing its own
+// partial O (f32, normalised by its own l) and lse; a merge kernel combines them.
+//
 // Layout: 256 threads; thread (ty, tx) = (tid / 16, tid % 16) owns query rows
 // ty + 16 r and keys tx + 16 c (r, c < 4) of the score tile, and output
 // columns 64 g + 4 tx + e of its four rows.  Tiles are staged in shared memory
@@ -70,7 +74,7 @@ __global__ void __launch_bounds__(NT) fwd_simt_kernel(const FwdParams p) {
         const int w = s_w;
         __syncthreads();
         if (w >= total) break;
-        const WorkItem it = map_item(w, p.sched.prefix, p.n_seq, p.H, true);
+        const WorkItem it = map_item(w, p.sched.prefix, p.n_seq, p.H, true, p.n_splits);
         int q_start, Lq, k_start, Lk;
         seq_bounds(p.cu_q, p.n_q, it.b, q_start, Lq);
         seq_bounds(p.cu_k, p.n_k, it.b, k_start, Lk);
@@ -88,11 +92,12 @@ __global__ void __launch_bounds__(NT) fwd_simt_kernel(const FwdParams p) {
             for (int e = 0; e < NG * 4; ++e) acc[r][e] = 0.f;
         }
         const int n_keys = p.causal ? min(Lk, row0 + BQ) : Lk;
-        const int n_tiles = (n_keys + BK - 1) / BK;
+        // split-K: this item scans chunk it.c of the row's key tiles
+        const KeyChunk chunk = key_chunk((n_keys + BK - 1) / BK, p.n_splits, it.c);
         const Tin *kbase = gk + (int64_t)k_start * p.k_st + (int64_t)h * p.k_sh;
         const Tin *vbase = gv + (int64_t)k_start * p.v_st + (int64_t)h * p.v_sh;
 
-        for (int kt = 0; kt < n_tiles; ++kt) {
+        for (int kt = chunk.begin; kt < chunk.end; ++kt) {
             const int key0 = kt * BK;
             __syncthreads();  // previous tile's sK / sV / sP no longer read
             stage_tile<Tin, D>(sK, kbase, p.k_st, key0, Lk);
@@ -186,21 +191,23 @@ __global__ void __launch_bounds__(NT) fwd_simt_kernel(const FwdParams p) {
             const int row = row0 + ty + 16 * r;
             if (row >= Lq) continue;
             const float inv = l[r] > 0.f ? 1.f / l[r] : 0.f;
-            Tout *orow = go + (int64_t)(q_start + row) * p.o_st + (int64_t)h * p.o_sh;
+            Tout *orow = go + it.c * p.o_split_st + (int64_t)(q_start + row) * p.o_st + (int64_t)h * p.o_sh;
 #pragma unroll
             for (int g = 0; g < NG; ++g)
                 store4(orow + 64 * g + 4 * tx,
                        make_float4(acc[r][4 * g] * inv, acc[r][4 * g + 1] * inv,
                                    acc[r][4 * g + 2] * inv, acc[r][4 * g + 3] * inv));
             if (tx == 0 && p.lse)
-                p.lse[(int64_t)h * p.n_q + q_start + row] =
+                p.lse[it.c * p.lse_split_st + (int64_t)h * p.n_q + q_start + row] =
                     l[r] > 0.f ? m[r] * kLn2 + logf(l[r]) : -INFINITY;
         }
     }
 }
 
+// Launches the kernel (num_ctas >= 0), or with num_ctas < 0 only reports its
+// resident CTAs per SM through *per_sm_out.
 template <typename Tin, typename Tout, int D>
-cudaError_t launch_typed(const FwdParams &p, int num_ctas, cudaStream_t s) {
+cudaError_t launch_typed(const FwdParams &p, int num_ctas, cudaStream_t s, int *per_sm_out) {
     auto kern = fwd_simt_kernel<Tin, Tout, D>;
     const size_t smem = fwd_smem_bytes<D>();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -209,6 +216,10 @@ cudaError_t launch_typed(const FwdParams &p, int num_ctas, cudaStream_t s) {
         int per_sm = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NT, smem);
         if (e != cudaSuccess) return e;
+        if (num_ctas < 0) {
+            *per_sm_out = per_sm > 0 ? per_sm : 1;
+            return cudaSuccess;
+        }
         num_ctas = sm_count() * (per_sm > 0 ? per_sm : 1);
     }
     kern<<<num_ctas, NT, smem, s>>>(p);
@@ -217,24 +228,34 @@ cudaError_t launch_typed(const FwdParams &p, int num_ctas, cudaStream_t s) {
 }
 
 template <typename Tin, int D>
-cudaError_t launch_out(const FwdParams &p, int num_ctas, cudaStream_t s) {
-    if (p.o_dtype == ATTN_F32) return launch_typed<Tin, float, D>(p, num_ctas, s);
-    return launch_typed<Tin, Tin, D>(p, num_ctas, s);
+cudaError_t launch_out(const FwdParams &p, int num_ctas, cudaStream_t s, int *per_sm) {
+    if (p.o_dtype == ATTN_F32) return launch_typed<Tin, float, D>(p, num_ctas, s, per_sm);
+    return launch_typed<Tin, Tin, D>(p, num_ctas, s, per_sm);
 }
 
 template <int D>
-cudaError_t launch_d(const FwdParams &p, int num_ctas, cudaStream_t s) {
+cudaError_t launch_d(const FwdParams &p, int num_ctas, cudaStream_t s, int *per_sm) {
     switch (p.dtype) {
-    case ATTN_F16: return launch_out<__half, D>(p, num_ctas, s);
-    case ATTN_BF16: return launch_out<__nv_bfloat16, D>(p, num_ctas, s);
-    default: return launch_typed<float, float, D>(p, num_ctas, s);
+    case ATTN_F16: return launch_out<__half, D>(p, num_ctas, s, per_sm);
+    case ATTN_BF16: return launch_out<__nv_bfloat16, D>(p, num_ctas, s, per_sm);
+    default: return launch_typed<float, float, D>(p, num_ctas, s, per_sm);
     }
 }
 
 }  // namespace
 
 cudaError_t launch_fwd_simt(const FwdParams &p, int num_ctas, cudaStream_t s) {
-    return p.D == 64 ? launch_d<64>(p, num_ctas, s) : launch_d<128>(p, num_ctas, s);
+    if (num_ctas < 0) num_ctas = 0;
+    return p.D == 64 ? launch_d<64>(p, num_ctas, s, nullptr) : launch_d<128>(p, num_ctas, s, nullptr);
+}
+
+int fwd_simt_ctas_per_sm(const FwdParams &p) {
+    int per_sm = 1;
+    // the split-K pass stores f32 partials: ask about that kernel instance
+    FwdParams q = p;
+    q.o_dtype = ATTN_F32;
+    const cudaError_t e = q.D == 64 ? launch_d<64>(q, -1, nullptr, &per_sm) : launch_d<128>(q, -1, nullptr, &per_sm);
+    return e == cudaSuccess ? per_sm : 1;
 }
 
 }  // namespace attn

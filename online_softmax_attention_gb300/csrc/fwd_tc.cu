@@ -31,6 +31,10 @@
 // TMEM (512 columns): S_0 / P_0 at [0, 128), S_1 / P_1 at [128, 256),
 // U_0 at [256, 256 + D), U_1 at [256 + D, 256 + 2D).
 //
+// Split-K: with n_splits > 1 an item is (256 query rows, key chunk c); both
+// tiles scan chunk c of the item's key tiles and write a partial O (f32,
+// normalised by its own l) and lse, which a merge kernel combines.
+//
 // Every mbarrier wait is bounded (sm100::mbar_wait); on expiry the CTA stops
 // issuing work, drains its outstanding TMA loads, frees TMEM and exits, and
 // the status word reads ATTN_ETIMEOUT.
@@ -100,27 +104,39 @@ struct __align__(8) FwdBars {
 
 struct ItemInfo {
     int q_start, Lq, k_start, Lk, h, row0;
-    int n[NQT];  // key tiles each query tile scans
+    int c;       // key split (split-K chunk) of this item
+    int j0;      // first key tile of the chunk
+    int n[NQT];  // key tiles each query tile scans, from j0 on
     int nkv;     // max over the tiles
 };
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 __device__ __forceinline__ ItemInfo item_info(const FwdParams &p, int w) {
-    const WorkItem it = map_item(w, p.sched.prefix, p.n_seq, p.H, true);
+    const WorkItem it = map_item(w, p.sched.prefix, p.n_seq, p.H, true, p.n_splits);
     ItemInfo f;
     seq_bounds(p.cu_q, p.n_q, it.b, f.q_start, f.Lq);
     seq_bounds(p.cu_k, p.n_k, it.b, f.k_start, f.Lk);
     f.h = it.h;
+    f.c = it.c;
     f.row0 = it.t * kItemRows;
-    f.nkv = 0;
+    int full[NQT], most = 0;
 #pragma unroll
     for (int t = 0; t < NQT; ++t) {
         const int r0 = f.row0 + BM * t;
         int n = 0;
         if (r0 < f.Lq) n = p.causal ? cdiv(min(f.Lk, r0 + BM), BN) : cdiv(f.Lk, BN);
-        f.n[t] = n;
-        f.nkv = max(f.nkv, n);
+        full[t] = n;
+        most = max(most, n);
+    }
+    // split-K: both query tiles scan the same chunk of the item's key tiles
+    const KeyChunk ch = key_chunk(most, p.n_splits, it.c);
+    f.j0 = ch.begin;
+    f.nkv = 0;
+#pragma unroll
+    for (int t = 0; t < NQT; ++t) {
+        f.n[t] = max(0, min(full[t], ch.end) - ch.begin);
+        f.nkv = max(f.nkv, f.n[t]);
     }
     return f;
 }
@@ -194,10 +210,11 @@ __device__ void producer(const TcFwdArgs &a, FwdBars &bars, int *sched_item, uin
         }
         if (!ok) break;
         for (int j = 0; j < f.nkv && ok; ++j) {
-            ok = load_kv(bars.k_full, bars.k_empty, kr.slot(), kr.phase(), sK, &a.tk, f.k_start + BN * j, f.h);
+            const int krow = f.k_start + BN * (f.j0 + j);
+            ok = load_kv(bars.k_full, bars.k_empty, kr.slot(), kr.phase(), sK, &a.tk, krow, f.h);
             if (!ok) break;
             ++kr.i;
-            ok = load_kv(bars.v_full, bars.v_empty, vr.slot(), vr.phase(), sV, &a.tv, f.k_start + BN * j, f.h);
+            ok = load_kv(bars.v_full, bars.v_empty, vr.slot(), vr.phase(), sV, &a.tv, krow, f.h);
             if (!ok) break;
             ++vr.i;
         }
@@ -352,10 +369,11 @@ __device__ void softmax_wg(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
         const int n = t == 0 ? f.n[0] : f.n[1];
         const int r0 = f.row0 + BM * t;
         const int row = r0 + lrow;  // query offset inside the sequence
-        Tout *orow = go + (int64_t)(f.q_start + row) * p.o_st + (int64_t)f.h * p.o_sh;
-        float *lse_at = p.lse ? p.lse + (int64_t)f.h * p.n_q + f.q_start + row : nullptr;
+        Tout *orow = go + f.c * p.o_split_st + (int64_t)(f.q_start + row) * p.o_st + (int64_t)f.h * p.o_sh;
+        float *lse_at = p.lse ? p.lse + f.c * p.lse_split_st + (int64_t)f.h * p.n_q + f.q_start + row : nullptr;
         if (n == 0) {
-            // rows of this tile exist but admit no key (empty key sequence)
+            // rows of this tile exist but admit no key (empty key sequence, or
+            // a key split past the tile's last key tile)
             if (r0 < f.Lq && row < f.Lq) {
 #pragma unroll 4
                 for (int c = 0; c < D; c += 4) store4(orow + c, make_float4(0.f, 0.f, 0.f, 0.f));
@@ -379,7 +397,7 @@ __device__ void softmax_wg(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
 #pragma unroll
             for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(r[c >> 5][c & 31]);
 
-            const int key0 = BN * j;
+            const int key0 = BN * (f.j0 + j);
             const bool masked = (p.causal && key0 + BN - 1 > r0) || key0 + BN > f.Lk;
             if (masked) {
                 const int lim = min(f.Lk - key0, p.causal ? row - key0 + 1 : BN);  // keys [0, lim) admitted

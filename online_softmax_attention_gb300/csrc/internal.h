@@ -33,6 +33,36 @@ struct FwdParams {
     Sched sched;
     int *status;
     long long watchdog_cycles;
+    // split-K: key tiles of every query tile cut into n_splits chunks; chunk c
+    // writes its partial (O_c f32, lse_c) at o + c * o_split_st, lse + c * lse_split_st
+    int n_splits;
+    int64_t o_split_st, lse_split_st;
+};
+
+// Key-tile range [begin, end) of chunk c when n_tiles key tiles are cut into
+// n_splits contiguous chunks of ceil(n_tiles / n_splits) tiles (the last ones
+// may be shorter or empty).
+struct KeyChunk {
+    int begin, end;
+};
+#ifdef __CUDACC__
+__host__ __device__
+#endif
+inline KeyChunk key_chunk(int n_tiles, int n_splits, int c) {
+    const int per = (n_tiles + n_splits - 1) / n_splits;
+    int b = c * per, e = b + per;
+    if (b > n_tiles) b = n_tiles;
+    if (e > n_tiles) e = n_tiles;
+    return KeyChunk{b, e};
+}
+
+struct MergeParams {
+    const float *o_parts, *lse_parts;
+    void *o;
+    float *lse;
+    int64_t o_st, o_sh;        // output strides (elements)
+    int64_t part_st;           // elements between partials of o_parts (n_q * H * D)
+    int n_parts, n_q, H, D, o_dtype;
 };
 
 struct BwdParams {
@@ -57,13 +87,18 @@ struct BwdParams {
 
 // Schedule preparation: validates cu_seqlens on the device and writes the
 // prefix of item counts for tiles of `block` rows of the `cu_rows` side.
+// Each tile counts as `splits` work items (split-K), numbered tile-major.
 cudaError_t launch_prep(const int32_t *cu_q, const int32_t *cu_k, int n_seq, int n_q, int n_k,
-                        int H, int block, int causal, int rows_are_keys, Sched sched,
+                        int H, int block, int causal, int rows_are_keys, int splits, Sched sched,
                         int *status, cudaStream_t s);
+
+// Merge of partial results (split-K): one warp per (query row, head).
+cudaError_t launch_merge(const MergeParams &p, cudaStream_t s);
 
 // SIMT (CUDA-core) kernels: any dtype, D in {64, 128}.
 constexpr int kSimtBlock = 64;
 cudaError_t launch_fwd_simt(const FwdParams &p, int num_ctas, cudaStream_t s);
+int fwd_simt_ctas_per_sm(const FwdParams &p);  // resident CTAs per SM of the kernel p selects
 cudaError_t launch_bwd_preprocess(const BwdParams &p, cudaStream_t s);
 cudaError_t launch_bwd_dkdv_simt(const BwdParams &p, int num_ctas, cudaStream_t s);
 cudaError_t launch_bwd_dq_simt(const BwdParams &p, int num_ctas, cudaStream_t s);

@@ -51,6 +51,7 @@ extern "C" int attn_fwd_noalloc(const attn_fwd_args *a, void *stream) {
     std::memcpy(&b, a, sizeof(b));
     b.workspace = nullptr;
     b.workspace_bytes = 0;
+    b.num_splits = 1;  // split-K partials would need more scratch than the fixed array
     if (attn_fwd_workspace_bytes(&b) > kScratchBytes) return ATTN_EUNSUPPORTED;
     void *scratch = scratch_address();
     if (!scratch) return ATTN_ECUDA;

@@ -1,8 +1,8 @@
 // Schedule preparation for the persistent attention kernels.
 //
 // One block validates the cu_seqlens offsets on the device (no host copy of
-// them is needed) and writes, for tiles of `block` rows, the prefix of work
-// items per sequence into the workspace; it also resets the dynamic work
+// them is needed) and writes, for tiles of `block` rows (each counted `splits`
+// times under split-K), the prefix of work items per sequence into the workspace; it also resets the dynamic work
 // counter.  Inconsistent offsets make the schedule empty and set the device
 // status word to ATTN_EINVAL, so the attention kernel that follows does no
 // work and reads nothing out of bounds.
@@ -17,8 +17,8 @@ constexpr int kPrepThreads = 1024;
 
 __global__ void __launch_bounds__(kPrepThreads)
 prep_kernel(const int32_t *__restrict__ cu_q, const int32_t *__restrict__ cu_k, int n_seq,
-            int n_q, int n_k, int H, int block, int causal, int rows_are_keys, int *hdr,
-            int *prefix, int *status) {
+            int n_q, int n_k, int H, int block, int causal, int rows_are_keys, int splits,
+            int *hdr, int *prefix, int *status) {
     __shared__ int s_bad;
     __shared__ int s_warp[kPrepThreads / 32];
     __shared__ long long s_carry;
@@ -47,7 +47,7 @@ prep_kernel(const int32_t *__restrict__ cu_q, const int32_t *__restrict__ cu_k, 
         if (b < n_seq && !bad) {
             const int len = rows_are_keys ? ((cu_k ? cu_k[b + 1] - cu_k[b] : n_k))
                                           : ((cu_q ? cu_q[b + 1] - cu_q[b] : n_q));
-            cnt = (len + block - 1) / block * H;
+            cnt = (len + block - 1) / block * H * splits;
         }
         // inclusive scan across the block
         int x = cnt;
@@ -86,10 +86,10 @@ prep_kernel(const int32_t *__restrict__ cu_q, const int32_t *__restrict__ cu_k, 
 }  // namespace
 
 cudaError_t launch_prep(const int32_t *cu_q, const int32_t *cu_k, int n_seq, int n_q, int n_k,
-                        int H, int block, int causal, int rows_are_keys, Sched sched,
+                        int H, int block, int causal, int rows_are_keys, int splits, Sched sched,
                         int *status, cudaStream_t s) {
     prep_kernel<<<1, kPrepThreads, 0, s>>>(cu_q, cu_k, n_seq, n_q, n_k, H, block, causal,
-                                          rows_are_keys, sched.hdr,
+                                          rows_are_keys, splits, sched.hdr,
                                           const_cast<int *>(sched.prefix), status);
     count_launch();
     return cudaGetLastError();

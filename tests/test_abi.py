@@ -23,6 +23,7 @@ def test_library_loads_and_abi_matches():
     assert lib.attn_abi_version() == _abi.ABI_VERSION
     assert lib.attn_fwd_args_size() == ctypes.sizeof(_abi.FwdArgs)
     assert lib.attn_bwd_args_size() == ctypes.sizeof(_abi.BwdArgs)
+    assert lib.attn_merge_args_size() == ctypes.sizeof(_abi.MergeArgs)
 
 
 def test_every_declared_symbol_is_exported():
@@ -60,6 +61,7 @@ def _fwd_args(**kw):
     a.o_dtype = kw.get("o_dtype", a.dtype)
     a.n_seq = 1
     a.kernel = kw.get("kernel", _abi.ATTN_KERNEL_AUTO)
+    a.num_splits = kw.get("num_splits", 0)
     lib = _abi.load()
     a.workspace = FAKE
     a.workspace_bytes = kw.get("ws", lib.attn_fwd_workspace_bytes(ctypes.byref(a)))
@@ -75,6 +77,8 @@ def _fwd_args(**kw):
     ({"dtype": 9}, _abi.ATTN_EINVAL),
     ({"o_dtype": _abi.ATTN_BF16}, _abi.ATTN_EINVAL),         # fp16 in, bf16 out
     ({"ws": 16}, _abi.ATTN_EWORKSPACE),
+    ({"num_splits": -1}, _abi.ATTN_EINVAL),
+    ({"num_splits": _abi.ATTN_MAX_SPLITS + 1}, _abi.ATTN_EINVAL),
     ({"kernel": 42}, None),
     ({"dtype": _abi.ATTN_F32, "kernel": _abi.ATTN_KERNEL_TC}, None),
 ])
@@ -130,3 +134,59 @@ def test_binding_fails_loudly_without_cuda_tensors():
     q = torch.zeros(8, 1, 64, dtype=torch.float16)
     with pytest.raises(ValueError):
         attn.fwd(q, q, q)
+
+
+def _align256(x):
+    return (x + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("splits", [1, 2, 7, 64])
+def test_explicit_splits_are_reported_and_size_the_workspace(splits):
+    """num_splits > 1 adds the f32 partial outputs and partial lse of every
+    split to the forward workspace; attn_fwd_num_splits reports the choice."""
+    lib = _abi.load()
+    H, D, N = 3, 128, 1000
+    base = lib.attn_fwd_workspace_bytes(ctypes.byref(_fwd_args(H=H, D=D, N=N, num_splits=1)))
+    a = _fwd_args(H=H, D=D, N=N, num_splits=splits)
+    assert lib.attn_fwd_num_splits(ctypes.byref(a)) == splits
+    extra = 0 if splits == 1 else (_align256(splits * N * H * D * 4) + _align256(splits * H * N * 4))
+    assert lib.attn_fwd_workspace_bytes(ctypes.byref(a)) == base + extra
+
+
+def test_num_splits_query_rejects_what_the_forward_rejects():
+    lib = _abi.load()
+    assert lib.attn_fwd_num_splits(ctypes.byref(_fwd_args(D=96))) == _abi.ATTN_EUNSUPPORTED
+    assert lib.attn_fwd_num_splits(ctypes.byref(_fwd_args(num_splits=-3))) == _abi.ATTN_EINVAL
+    assert lib.attn_fwd_num_splits(None) == _abi.ATTN_EINVAL
+    # the automatic choice is a valid split count
+    assert 1 <= lib.attn_fwd_num_splits(ctypes.byref(_fwd_args())) <= _abi.ATTN_MAX_SPLITS
+
+
+def _merge_args(**kw):
+    a = _abi.MergeArgs()
+    H, D, n = kw.get("H", 2), kw.get("D", 64), kw.get("n_q", 16)
+    a.o_parts = kw.get("o_parts", FAKE)
+    a.lse_parts = kw.get("lse_parts", FAKE)
+    a.o = _abi.AttnTensor(kw.get("o", FAKE), H * D, D)
+    a.lse = FAKE
+    a.n_parts, a.n_q, a.H, a.D = kw.get("n_parts", 4), n, H, D
+    a.o_dtype = kw.get("o_dtype", _abi.ATTN_F32)
+    return a
+
+
+@pytest.mark.parametrize("kw", [
+    {"n_parts": 0}, {"n_parts": _abi.ATTN_MAX_SPLITS + 1}, {"D": 6}, {"D": 260}, {"H": 0},
+    {"n_q": -1}, {"o_dtype": 5}, {"o_parts": None}, {"o_parts": FAKE + 4}, {"lse_parts": None},
+    {"lse_parts": FAKE + 2}, {"o": None}, {"o": FAKE + 8},
+])
+def test_merge_argument_validation(kw):
+    lib = _abi.load()
+    assert lib.attn_merge(ctypes.byref(_merge_args(**kw)), None) == _abi.ATTN_EINVAL
+    assert lib.attn_merge(None, None) == _abi.ATTN_EINVAL
+
+
+def test_merge_of_no_rows_launches_nothing():
+    lib = _abi.load()
+    before = lib.attn_launch_count()
+    assert lib.attn_merge(ctypes.byref(_merge_args(n_q=0)), None) == _abi.ATTN_OK
+    assert lib.attn_launch_count() == before
