@@ -53,7 +53,7 @@ WORKLOADS = {
         layout="hnd", note="full fwd, N=1024, H=4, D=64, fp16, (H,N,D) storage"),
     "varlen_causal_bf16": Workload(
         "varlen_causal_bf16", "bf16", H=16, D=128, causal=True, seed=1, varlen=(32, 64, 4096),
-        note="varlen causal fwd, 32 sequences with lengths uniform in [64,4096], H=16, D=128"),
+        note="varlen causal fwd, 32 sequences with lengths uniform in [64,4096], H=16, D=128, bf16"),
     "cross_f32_8192x2048": Workload(
         "cross_f32_8192x2048", "f32", H=1, D=64, causal=False, seed=3, n_q=8192, n_k=2048,
         note="cross fwd in f32, SQ=8192, SK=2048, H=1, D=64"),

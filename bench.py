@@ -13,7 +13,9 @@ rate over all ranks (each rank runs the full batch: weak scaling, no
 collective on the data path).
 
 Prints one JSON line.  `--impl reference` times the f64 CPU oracle instead,
-on a bounded sample of the same workload.
+on a bounded sample of the same workload.  `--workload <name>` measures the
+forward alone on one of the smaller workloads (causal_fp16_n256,
+full_fp16_n1024, varlen_causal_bf16, cross_f32_8192x2048) with the same line.
 """
 from __future__ import annotations
 
@@ -176,6 +178,158 @@ def time_oracle_sample(x, w, max_seconds=20.0):
                       f"N={L}, D={w.D}, causal: {spent:.1f} s"}
 
 
+FWD_WORKLOADS = ("causal_fp16_n256", "full_fp16_n1024", "varlen_causal_bf16", "cross_f32_8192x2048")
+L2_BYTES = 129 * 1024 * 1024
+
+
+def time_oracle_fwd_rows(x, w, max_seconds=15.0):
+    """Time the oracle's forward on randomly drawn query rows of the workload,
+    adding rows until about `max_seconds` of CPU work; report the workload's
+    FLOP rate over those rows."""
+    import numpy as np
+
+    import oracle
+    lq, lk = x["lengths_q"], x["lengths_k"]
+    cu = np.concatenate([[0], np.cumsum(lq)])
+    rng = np.random.default_rng(0)
+    done_rows, spent, flops = 0, 0.0, 0.0
+    n = 64
+    while spent < max_seconds * 0.5:
+        toks = rng.integers(0, int(cu[-1]), n)
+        heads = rng.integers(0, w.H, n)
+        t0 = time.perf_counter()
+        oracle.fwd_rows(x["q"], x["k"], x["v"], toks, heads, causal=w.causal,
+                        cu_seqlens_q=x["cu_seqlens_q"], cu_seqlens_k=x["cu_seqlens_k"])
+        spent += time.perf_counter() - t0
+        seq = np.searchsorted(cu, toks, side="right") - 1
+        for t, b in zip(toks, seq):
+            keys = min(int(t - cu[b]) + 1, lk[b]) if w.causal else lk[b]
+            flops += 4.0 * keys * w.D
+        done_rows += n
+        n = min(4 * n, 1 << 16)
+    return {"value": flops / spent / 1e12, "unit": UNIT, "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"{done_rows} random (query row, head) pairs of the workload, forward: "
+                      f"{spent:.1f} s"}
+
+
+def run_forward_workload(args, rank, world):
+    """Forward-only measurement of one of the smaller workloads (a parity
+    workload, timed on request): TFLOP/s of the forward, L2 flushed between
+    launches when the inputs fit in L2."""
+    import torch
+    import torch.distributed as dist
+
+    import attn_inputs
+    import online_softmax_attention_gb300 as attn
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    w = attn_inputs.WORKLOADS[args.workload]
+    x = attn_inputs.make_workload(w)
+    flops = attention_flops(x["lengths_q"], x["lengths_k"], w.H, w.D, w.causal)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    cq = x["cu_seqlens_q"].to(dev) if x["cu_seqlens_q"] is not None else None
+    ck = x["cu_seqlens_k"].to(dev) if x["cu_seqlens_k"] is not None else None
+    out_dtype = torch.float32 if w.dtype == "bf16" else None
+    call = attn.FwdCall(q, k, v, causal=w.causal, cu_seqlens_q=cq, cu_seqlens_k=ck,
+                        out_dtype=out_dtype, kernel=args.kernel, num_splits=args.num_splits)
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v))
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if in_bytes < L2_BYTES else None
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        call.run(stream)
+    torch.cuda.synchronize()
+    if attn.device_status() != 0:
+        raise RuntimeError("device status set during warm-up")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    n0 = attn.launch_count()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for e0, e1 in evs:
+            if flush is not None:
+                flush.zero_()
+            e0.record(stream)
+            call.run(stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    launches = attn.launch_count() - n0
+    ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in evs), dev)
+    if attn.device_status() != 0:
+        raise RuntimeError("device status set in the timed region")
+
+    # end to end: host inputs in, o and lse out, through the same call
+    pin = {n: x[n].contiguous().pin_memory() for n in ("q", "k", "v")}
+    dev_in = {"q": q, "k": k, "v": v}
+    o_h = torch.empty(call.o.shape, dtype=call.o.dtype).pin_memory()
+    l_h = torch.empty(call.lse.shape, dtype=torch.float32).pin_memory()
+
+    def e2e():
+        for n, t in pin.items():
+            dev_in[n].copy_(t, non_blocking=True)
+        call.run(stream)
+        o_h.copy_(call.o, non_blocking=True)
+        l_h.copy_(call.lse, non_blocking=True)
+
+    e2e()
+    torch.cuda.synchronize()
+    e_steps = max(2, min(args.steps, 10))
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(e_steps):
+        e2e()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(t0.elapsed_time(t1) / e_steps, dev)
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = o_h.numel() * o_h.element_size() + l_h.numel() * 4
+
+    peaks = load_peaks()
+    family = call.selected_kernel()
+    achieved = flops / (ms * 1e-3) / 1e12
+    if family == "tc":
+        peak, bound = peaks["bf16_tflops"], "tensor"
+        note = f"bf16/f16 dense, burst ({peaks['source']})"
+    else:
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        peak, bound = sms * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12, "alu"
+        note = f"FP32 FFMA: {sms} SMs x 128 lanes x 2 FLOP x {peaks['sm_max_mhz']:.0f} MHz"
+    metric = f"attention fwd TFLOP/s ({w.note})"
+    line = {
+        "metric": metric, "value": job_rate(flops, world, ms) / 1e12, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": {"fp16": "f16", "bf16": "bf16", "f32": "f32"}[w.dtype], "data": "synthetic",
+        "config": {"workload": w.name, "kernel": family, "num_splits": call.num_splits(),
+                   "tokens_q": int(sum(x["lengths_q"])), "tokens_k": int(sum(x["lengths_k"])),
+                   "heads": w.H, "head_dim": w.D, "relation": "causal" if w.causal else "full",
+                   "l2": "flushed before every launch (inputs fit in L2)" if flush is not None
+                   else "no flush: inputs larger than L2",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": UNIT,
+                     "frac": achieved / peak, "traffic": None, "kernel": "fwd", "peak_source": note},
+        "e2e": {"value": job_rate(flops, world, e2e_ms) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "cpu_baseline": None,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = time_oracle_fwd_rows(x, w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def run_reference(args, rank, world):
     """Reference arm: the f64 CPU oracle on the host cores, bounded samples."""
     if rank != 0:
@@ -214,6 +368,10 @@ def main():
     ap.add_argument("--batch", type=int, default=4,
                     help="sequences of N=8192 (4 = the benchmark workload; fewer for profiling)")
     ap.add_argument("--skip-e2e", action="store_true", help="profiling runs: no host-buffer leg")
+    ap.add_argument("--workload", default=WORKLOAD, choices=(WORKLOAD,) + FWD_WORKLOADS,
+                    help="the training workload (default), or a forward-only workload")
+    ap.add_argument("--num-splits", type=int, default=0,
+                    help="forward-only workloads: key splits (0 = library's choice)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -223,6 +381,9 @@ def main():
 
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.workload != WORKLOAD:
+        run_forward_workload(args, rank, world)
         return
 
     import torch
