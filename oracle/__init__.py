@@ -63,6 +63,11 @@ def _load():
         lib.oracle_attn_merge.argtypes = [
             ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _dp, _dp, _dp, _dp,
             ctypes.c_int]
+        lib.oracle_attn_fwd_pruned.restype = ctypes.c_int
+        lib.oracle_attn_fwd_pruned.argtypes = [
+            ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _dp, _dp, _dp,
+            ctypes.c_double, ctypes.c_double, ctypes.c_int, ctypes.c_int, _dp, _dp, _i64p, _dp,
+            ctypes.c_int]
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -214,6 +219,35 @@ def merge(o_parts, lse_parts, *, threads: int = 0):
     if rc != 0:
         raise ValueError(f"oracle_attn_merge rejected its arguments (rc={rc})")
     return o, lse
+
+
+def fwd_pruned(q, k, v, *, rho: float, block_q: int, block_k: int, scale: float | None = None,
+               threads: int = 0):
+    """Tile-pruned approximate forward, one sequence, full relation.
+
+    Returns ``(o, lse, n_pruned, min_margin)``: o (T_q, H, D) and lse (H, T_q)
+    float64; n_pruned = pruned (query block, key tile) pairs over all heads;
+    min_margin = smallest |m_tile - (m_run + ln rho)| of the decisions taken
+    against a finite rolling max (inf when there were none).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    Tq, H, D = _shape3(q, "q")
+    Tk = _shape3(k, "k")[0]
+    if v.shape != k.shape:
+        raise ValueError("v must have k's shape")
+    if scale is None:
+        scale = D ** -0.5
+    o = np.zeros((Tq, H, D), dtype=np.float64)
+    lse = np.zeros((H, Tq), dtype=np.float64)
+    n_pruned = np.zeros(1, dtype=np.int64)
+    margin = np.zeros(1, dtype=np.float64)
+    rc = _load().oracle_attn_fwd_pruned(Tq, Tk, H, D, _ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp),
+                                        float(scale), float(rho), int(block_q), int(block_k),
+                                        _ptr(o, _dp), _ptr(lse, _dp), _ptr(n_pruned, _i64p),
+                                        _ptr(margin, _dp), int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle_attn_fwd_pruned rejected its arguments (rc={rc})")
+    return o, lse, int(n_pruned[0]), float(margin[0])
 
 
 if __name__ == "__main__":  # pragma: no cover - manual build hook

@@ -64,6 +64,23 @@
  *    M = max_c lse_c.  A partial with lse_c = -inf admits no key and has
  *    weight 0; if every partial is -inf the row gets O = 0, lse = -inf.
  *
+ *  - Tile-pruned approximate attention.  TIGA-lang attention examples page,
+ *    section "基于 tile 剪枝的稀疏注意力" (tile-pruned sparse attention),
+ *    display equations.  A tile pairs a block of block_q query rows with a
+ *    block of block_k keys.  For each query block the key tiles are visited
+ *    in order; every tile's scores are computed, and m_tile, the largest
+ *    score of the whole tile, is compared with m_run, the largest score of
+ *    the tiles admitted so far for this query block (the block's rolling
+ *    max).  The tile is admitted iff
+ *        m_tile >= m_run + ln(rho),   0 < rho <= 1
+ *    (the first tile always is: m_run starts at -inf).  An admitted tile
+ *    raises m_run to max(m_run, m_tile); a pruned tile contributes nothing.
+ *    Each query row's output is then softmax attention over the keys of its
+ *    block's admitted tiles only.  Only the dense (full) relation over one
+ *    sequence is defined (the page's other paths fail closed).  Rows past
+ *    the end of the queries and keys past the end of the keys are not part
+ *    of any tile.
+ *
  * Layout: q, o, dq, dO are (T_q, H, D) row-major; k, v, dk, dv are (T_k, H, D);
  * lse is (H, T_q).  cu_q / cu_k hold n_seq + 1 cumulative offsets starting at 0.
  * All arrays are host memory owned by the caller.
@@ -443,5 +460,103 @@ int oracle_attn_merge(int C, int64_t T, int H, int D, const double *o_parts,
         }
         lse[(int64_t)h * T + t] = M + log(l);
     }
+    return 0;
+}
+
+/*
+ * Tile-pruned approximate forward (see the header comment): one sequence,
+ * full relation.  o is (T_q, H, D), lse is (H, T_q).  n_pruned (optional)
+ * receives the number of pruned (query block, key tile) pairs over all heads;
+ * min_margin (optional) the smallest |m_tile - (m_run + ln rho)| over all
+ * decisions taken against a finite m_run, so that callers can tell whether
+ * rounding could flip a decision.  Returns 0, or -1 on bad sizes.
+ */
+int oracle_attn_fwd_pruned(int64_t Tq, int64_t Tk, int H, int D, const double *q,
+                           const double *k, const double *v, double scale, double rho,
+                           int block_q, int block_k, double *o, double *lse,
+                           int64_t *n_pruned, double *min_margin, int n_threads)
+{
+    if (Tq < 0 || Tk < 0 || H < 1 || D < 1 || block_q < 1 || block_k < 1) return -1;
+    if (!(rho > 0.0 && rho <= 1.0)) return -1;
+    set_threads(n_threads);
+    const int64_t ld = (int64_t)H * D;
+    const int64_t n_qb = (Tq + block_q - 1) / block_q, n_kt = (Tk + block_k - 1) / block_k;
+    const double log_rho = log(rho);
+    int64_t pruned_total = 0;
+    double margin_min = INFINITY;
+#pragma omp parallel reduction(+ : pruned_total) reduction(min : margin_min)
+    {
+        unsigned char *admit = (unsigned char *)malloc((size_t)(n_kt > 0 ? n_kt : 1));
+        double *s = (double *)malloc(sizeof(double) * (size_t)(Tk > 0 ? Tk : 1));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t blk = 0; blk < n_qb * H; ++blk) {
+            const int h = (int)(blk / n_qb);
+            const int64_t i0 = (blk % n_qb) * block_q;
+            const int64_t i1 = i0 + block_q < Tq ? i0 + block_q : Tq;
+            /* decisions: scan the key tiles in order with the block's rolling max */
+            double m_run = -INFINITY;
+            for (int64_t kt = 0; kt < n_kt; ++kt) {
+                const int64_t j0 = kt * block_k, j1 = j0 + block_k < Tk ? j0 + block_k : Tk;
+                double m_tile = -INFINITY;
+                for (int64_t i = i0; i < i1; ++i)
+                    for (int64_t j = j0; j < j1; ++j) {
+                        const double x = scale * dot(q + i * ld + (int64_t)h * D,
+                                                     k + j * ld + (int64_t)h * D, D);
+                        if (x > m_tile) m_tile = x;
+                    }
+                if (m_run == -INFINITY) {
+                    admit[kt] = 1;
+                } else {
+                    const double margin = m_tile - (m_run + log_rho);
+                    admit[kt] = margin >= 0.0;
+                    if (fabs(margin) < margin_min) margin_min = fabs(margin);
+                }
+                if (admit[kt]) {
+                    if (m_tile > m_run) m_run = m_tile;
+                } else {
+                    ++pruned_total;
+                }
+            }
+            /* each row: composed softmax over the keys of the admitted tiles */
+            for (int64_t i = i0; i < i1; ++i) {
+                const double *qi = q + i * ld + (int64_t)h * D;
+                double m = -INFINITY;
+                for (int64_t kt = 0; kt < n_kt; ++kt) {
+                    if (!admit[kt]) continue;
+                    const int64_t j0 = kt * block_k, j1 = j0 + block_k < Tk ? j0 + block_k : Tk;
+                    for (int64_t j = j0; j < j1; ++j) {
+                        s[j] = scale * dot(qi, k + j * ld + (int64_t)h * D, D);
+                        if (s[j] > m) m = s[j];
+                    }
+                }
+                double *orow = o + i * ld + (int64_t)h * D;
+                for (int d = 0; d < D; ++d) orow[d] = 0.0;
+                if (m == -INFINITY) {
+                    lse[(int64_t)h * Tq + i] = -INFINITY;
+                    continue;
+                }
+                double l = 0.0;
+                for (int64_t kt = 0; kt < n_kt; ++kt) {
+                    if (!admit[kt]) continue;
+                    const int64_t j0 = kt * block_k, j1 = j0 + block_k < Tk ? j0 + block_k : Tk;
+                    for (int64_t j = j0; j < j1; ++j) l += exp(s[j] - m);
+                }
+                for (int64_t kt = 0; kt < n_kt; ++kt) {
+                    if (!admit[kt]) continue;
+                    const int64_t j0 = kt * block_k, j1 = j0 + block_k < Tk ? j0 + block_k : Tk;
+                    for (int64_t j = j0; j < j1; ++j) {
+                        const double p = exp(s[j] - m) / l;
+                        const double *vj = v + j * ld + (int64_t)h * D;
+                        for (int d = 0; d < D; ++d) orow[d] += p * vj[d];
+                    }
+                }
+                lse[(int64_t)h * Tq + i] = m + log(l);
+            }
+        }
+        free(s);
+        free(admit);
+    }
+    if (n_pruned) *n_pruned = pruned_total;
+    if (min_margin) *min_margin = margin_min;
     return 0;
 }

@@ -381,3 +381,75 @@ def test_merge_large_lse_is_stable_and_matches_library_logsumexp():
     w = softmax(lp[:, 0, :], axis=0)  # (C, T)
     np.testing.assert_allclose(o[:, 0, :], np.einsum("ct,ctd->td", w, op[:, :, 0, :]), rtol=0,
                                atol=1e-12)
+
+
+# --- tile-pruned approximate forward ----------------------------------------------
+
+def _prune_cases():
+    with open(os.path.join(GOLDEN, "tile_prune_cases.json")) as f:
+        return json.load(f)["cases"]
+
+
+@pytest.mark.parametrize("case", _prune_cases(), ids=lambda c: c["name"])
+def test_pruned_hand_cases(case):
+    q, k, v = (np.array(_ev(case[n]), dtype=np.float64) for n in ("q", "k", "v"))
+    o, lse, n_pruned, _ = oracle.fwd_pruned(q, k, v, rho=case["rho"], block_q=case["block_q"],
+                                            block_k=case["block_k"], scale=1.0)
+    assert n_pruned == case["n_pruned"]
+    np.testing.assert_allclose(o, np.array(_ev(case["o"])), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, np.array(_ev(case["lse"])), rtol=0, atol=1e-13)
+
+
+def test_pruned_page_worked_value():
+    """The page prints exp(1 - 10) ~ 0.00012 for a block whose best score is 1
+    after a seen maximum of 10, skipped under threshold 0.01."""
+    with open(os.path.join(GOLDEN, "tile_prune_worked_example.json")) as f:
+        g = json.load(f)
+    ratio = math.exp(g["tile_max"] - g["seen_max"])
+    assert float(f"{ratio:.{g['printed_digits']}g}") == g["printed_ratio"]
+    # the rule in log form: skipped iff m_tile < m_run + ln(rho), i.e. ratio < rho
+    assert (ratio < g["threshold"]) == g["skipped"]
+    q = np.ones((1, 1, 1))
+    k = np.array([g["seen_max"], g["tile_max"]]).reshape(2, 1, 1)
+    _, _, n_pruned, margin = oracle.fwd_pruned(q, k, np.ones((2, 1, 1)), rho=g["threshold"],
+                                               block_q=1, block_k=1, scale=1.0)
+    assert n_pruned == int(g["skipped"])
+    assert margin == pytest.approx(abs(g["tile_max"] - g["seen_max"] - math.log(g["threshold"])))
+
+
+@pytest.mark.parametrize("bq,bk", [(16, 16), (64, 64), (128, 128), (7, 33)])
+def test_pruned_with_negligible_rho_is_exact_attention(bq, bk):
+    q, k, v = _rand((150, 2, 16), 81), _rand((230, 2, 16), 82), _rand((230, 2, 16), 83)
+    o, lse, n_pruned, _ = oracle.fwd_pruned(q, k, v, rho=1e-300, block_q=bq, block_k=bk)
+    o_ref, lse_ref = oracle.fwd(q, k, v, causal=False)
+    assert n_pruned == 0
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-13)
+
+
+def test_pruned_cold_tile_is_dropped_from_every_block():
+    """Keys of one tile set to zero (all its scores 0) among tiles of large
+    scores: every query block prunes exactly that tile, and the result is exact
+    attention over the remaining keys."""
+    bq, bk, Tq, Tk, H, D = 32, 16, 100, 80, 2, 8
+    q = _rand((Tq, H, D), 84)
+    q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    k = 10.0 * q[np.random.default_rng(85).integers(0, Tq, Tk)]  # scores up to 10
+    k[32:48] = 0.0                                               # the cold tile (tile 2)
+    v = _rand((Tk, H, D), 86)
+    scale = 1.0
+    o, lse, n_pruned, margin = oracle.fwd_pruned(q, k, v, rho=0.01, block_q=bq, block_k=bk,
+                                                 scale=scale)
+    keep = np.r_[0:32, 48:80]
+    o_ref, lse_ref = oracle.fwd(q, k[keep], v[keep], causal=False, scale=scale)
+    assert n_pruned == H * ((Tq + bq - 1) // bq)
+    assert margin > 0.5
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-12)
+
+
+def test_pruned_rejects_rho_outside_unit_interval():
+    q = np.zeros((2, 1, 4))
+    for rho in (0.0, -0.5, 1.5, float("nan")):
+        with pytest.raises(ValueError):
+            oracle.fwd_pruned(q, q, q, rho=rho, block_q=2, block_k=2)
