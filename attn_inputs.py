@@ -14,9 +14,16 @@ CPU oracle cannot replay, so every draw here uses a CPU generator instead):
 * ``layout="hnd"`` draws an (H, N, D) tensor and returns its (N, H, D) view,
   as the TIGA-lang full / causal examples do ("the streaming kernel reads
   lane-major storage"); ``layout="thd"`` draws (T, H, D) directly.
+* ``key_gain=(block, lo, hi)`` (structured keys for the tile-pruning tests):
+  after all other draws, one gain per (block of ``block`` keys, head) is
+  drawn uniformly in [lo, hi] (``torch.rand`` on the same generator) and the
+  keys of that block and head are multiplied by it in f32, then cast back.
+  Blocks of large gain hold the large scores, so whole key tiles differ in
+  their best score as on the tile-pruning page's picture.
 
-The named workloads are the five benchmark configurations; they carry their
-shapes, dtype, relation and seed.
+The named workloads are the five benchmark configurations, plus one with
+structured keys for the tile-pruning option; they carry their shapes, dtype,
+relation and seed.
 """
 from __future__ import annotations
 
@@ -41,6 +48,7 @@ class Workload:
     varlen: tuple = ()        # (n_seq, lo, hi): lengths drawn uniformly in [lo, hi]
     layout: str = "thd"
     backward: bool = False
+    key_gain: tuple = ()      # (block, lo, hi): structured keys, see the recipe
     note: str = field(default="", compare=False)
 
 
@@ -61,6 +69,12 @@ WORKLOADS = {
         "causal_train_bf16_b4_n8192", "bf16", H=32, D=128, causal=True, seed=5, n_q=8192,
         n_k=8192, batch=4, backward=True,
         note="causal fwd+bwd, batch 4 x N=8192, H=32, D=128, bf16"),
+    # tile pruning (approximate forward): keys with one gain in [0.2, 3] per
+    # 128-key tile and head, so that whole tiles differ in their best score
+    "pruned_full_bf16_n8192": Workload(
+        "pruned_full_bf16_n8192", "bf16", H=16, D=128, causal=False, seed=9, n_q=8192,
+        n_k=8192, key_gain=(128, 0.2, 3.0),
+        note="full fwd, N=8192, H=16, D=128, bf16, key gain per 128-key tile in [0.2, 3]"),
 }
 
 
@@ -70,7 +84,8 @@ def _randn(gen: torch.Generator, shape, dtype: torch.dtype) -> torch.Tensor:
 
 def make(*, dtype: str, H: int, D: int, seed: int, n_q: int | None = None,
          n_k: int | None = None, batch: int = 1, lengths=None, lengths_k=None,
-         varlen: tuple = (), layout: str = "thd", backward: bool = False) -> dict:
+         varlen: tuple = (), layout: str = "thd", backward: bool = False,
+         key_gain: tuple = ()) -> dict:
     """Draw one input set.  Returns CPU tensors and host cu_seqlens.
 
     Keys: q, k, v, (dO), cu_seqlens_q, cu_seqlens_k (int32, or None for a
@@ -98,6 +113,12 @@ def make(*, dtype: str, H: int, D: int, seed: int, n_q: int | None = None,
     out = {"q": draw(Tq), "k": draw(Tk), "v": draw(Tk)}
     if backward:
         out["dO"] = draw(Tq)
+    if key_gain:
+        block, lo, hi = key_gain
+        n_blocks = (Tk + block - 1) // block
+        g = lo + (hi - lo) * torch.rand((n_blocks, H), generator=gen, dtype=torch.float32)
+        gain = g.repeat_interleave(block, dim=0)[:Tk].unsqueeze(-1)  # (Tk, H, 1)
+        out["k"] = (out["k"].to(torch.float32) * gain).to(tdt)
     multi = len(lq) > 1 or varlen or lengths is not None
     if multi:
         out["cu_seqlens_q"] = torch.tensor([0] + lq, dtype=torch.int64).cumsum(0).to(torch.int32)
@@ -115,4 +136,4 @@ def make_workload(w: Workload | str) -> dict:
         w = WORKLOADS[w]
     return make(dtype=w.dtype, H=w.H, D=w.D, seed=w.seed, n_q=w.n_q or None,
                 n_k=w.n_k or None, batch=w.batch, varlen=w.varlen, layout=w.layout,
-                backward=w.backward)
+                backward=w.backward, key_gain=w.key_gain)

@@ -15,7 +15,8 @@ collective on the data path).
 Prints one JSON line.  `--impl reference` times the f64 CPU oracle instead,
 on a bounded sample of the same workload.  `--workload <name>` measures the
 forward alone on one of the smaller workloads (causal_fp16_n256,
-full_fp16_n1024, varlen_causal_bf16, cross_f32_8192x2048) with the same line.
+full_fp16_n1024, varlen_causal_bf16, cross_f32_8192x2048, and
+pruned_full_bf16_n8192 for `--prune-threshold`) with the same line.
 """
 from __future__ import annotations
 
@@ -178,7 +179,8 @@ def time_oracle_sample(x, w, max_seconds=20.0):
                       f"N={L}, D={w.D}, causal: {spent:.1f} s"}
 
 
-FWD_WORKLOADS = ("causal_fp16_n256", "full_fp16_n1024", "varlen_causal_bf16", "cross_f32_8192x2048")
+FWD_WORKLOADS = ("causal_fp16_n256", "full_fp16_n1024", "varlen_causal_bf16", "cross_f32_8192x2048",
+                 "pruned_full_bf16_n8192")
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -236,7 +238,8 @@ def run_forward_workload(args, rank, world):
     ck = x["cu_seqlens_k"].to(dev) if x["cu_seqlens_k"] is not None else None
     out_dtype = torch.float32 if w.dtype == "bf16" else None
     call = attn.FwdCall(q, k, v, causal=w.causal, cu_seqlens_q=cq, cu_seqlens_k=ck,
-                        out_dtype=out_dtype, kernel=args.kernel, num_splits=args.num_splits)
+                        out_dtype=out_dtype, kernel=args.kernel, num_splits=args.num_splits,
+                        prune_threshold=args.prune_threshold)
     in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v))
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if in_bytes < L2_BYTES else None
     stream = torch.cuda.current_stream()
@@ -262,6 +265,7 @@ def run_forward_workload(args, rank, world):
     if world > 1:
         dist.barrier()
     launches = attn.launch_count() - n0
+    pruned_per_run = call.pruned_count() / (args.warmup + args.steps)
     ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in evs), dev)
     if attn.device_status() != 0:
         raise RuntimeError("device status set in the timed region")
@@ -303,6 +307,17 @@ def run_forward_workload(args, rank, world):
         peak, bound = sms * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12, "alu"
         note = f"FP32 FFMA: {sms} SMs x 128 lanes x 2 FLOP x {peaks['sm_max_mhz']:.0f} MHz"
     metric = f"attention fwd TFLOP/s ({w.note})"
+    prune = {}
+    if args.prune_threshold:
+        # FLOPs stay those of the exact forward: the rate is exact-equivalent
+        tiles = 0
+        for lq_, lk_ in zip(x["lengths_q"], x["lengths_k"]):
+            b = 128 if call.selected_kernel() == "tc" else 64
+            tiles += -(-lq_ // b) * -(-lk_ // b) * w.H
+        prune = {"prune_threshold": args.prune_threshold,
+                 "pruned_fraction": pruned_per_run / tiles,
+                 "flops": "of the exact forward (exact-equivalent rate)"}
+        metric = f"attention fwd TFLOP/s, tile-pruned rho={args.prune_threshold} ({w.note})"
     line = {
         "metric": metric, "value": job_rate(flops, world, ms) / 1e12, "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -313,7 +328,7 @@ def run_forward_workload(args, rank, world):
                    "heads": w.H, "head_dim": w.D, "relation": "causal" if w.causal else "full",
                    "l2": "flushed before every launch (inputs fit in L2)" if flush is not None
                    else "no flush: inputs larger than L2",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}", **prune},
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak, "traffic": None, "kernel": "fwd", "peak_source": note},
         "e2e": {"value": job_rate(flops, world, e2e_ms) / 1e12, "unit": UNIT,
@@ -372,6 +387,8 @@ def main():
                     help="the training workload (default), or a forward-only workload")
     ap.add_argument("--num-splits", type=int, default=0,
                     help="forward-only workloads: key splits (0 = library's choice)")
+    ap.add_argument("--prune-threshold", type=float, default=0.0,
+                    help="forward-only workloads, full relation: tile pruning rho (0 = exact)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 

@@ -116,7 +116,24 @@ typedef struct attn_fwd_args {
     int32_t num_ctas;     /* persistent grid size; 0 = one per SM */
     int32_t num_splits;   /* key splits per query tile (split-K): 0 = chosen by the
                              library (see attn_fwd_num_splits), 1 = none, 2..ATTN_MAX_SPLITS */
+    float prune_threshold; /* tile pruning (approximate forward, see below): 0 = off,
+                              the exact forward; 0 < rho <= 1 enables it */
+    uint64_t *pruned_tiles; /* optional device counter, or NULL: with pruning on, the
+                               forward adds the number of pruned tiles to it */
 } attn_fwd_args;
+
+/* Tile pruning (TIGA-lang attention examples page, section
+ * "基于 tile 剪枝的稀疏注意力", tile-pruned sparse attention): an explicit,
+ * approximate option of the forward.  A tile pairs a query tile with a key
+ * tile of the kernel's own sizes (128 x 128 for the tensor-core kernel, 64 x 64
+ * for the SIMT kernel).  Per query tile the key tiles are scanned in order;
+ * every tile's scores are computed, and a tile whose largest score m_tile
+ * satisfies  m_tile < m_run + ln(rho)  -- m_run being the largest score of the
+ * tiles admitted so far for that query tile -- is pruned: it adds nothing to
+ * the softmax or to O (its value tile is still loaded).  The rule bounds no
+ * per-row error.  Only the full relation over one sequence (no cu_seqlens) and
+ * no key splits are supported; other combinations, and any backward call with
+ * a non-zero prune_threshold, return ATTN_EUNSUPPORTED (fail closed). */
 
 /* Upper bound of attn_fwd_args.num_splits and of attn_merge_args.n_parts. */
 #define ATTN_MAX_SPLITS 64
@@ -139,6 +156,8 @@ typedef struct attn_bwd_args {
     size_t workspace_bytes;
     int32_t kernel;
     int32_t num_ctas;
+    float prune_threshold; /* must be 0: the backward of a tile-pruned forward is not
+                              defined, and a non-zero value returns ATTN_EUNSUPPORTED */
 } attn_bwd_args;
 
 /* Partial attention results over disjoint key sets, to be merged

@@ -96,8 +96,8 @@ class FwdCall:
     def __init__(self, q, k, v, *, causal: bool = False, scale: float | None = None,
                  cu_seqlens_q=None, cu_seqlens_k=None, out_dtype: torch.dtype | None = None,
                  kernel: str = "auto", num_ctas: int = 0, num_splits: int = 0,
-                 out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
-                 workspace: torch.Tensor | None = None):
+                 prune_threshold: float = 0.0, out: torch.Tensor | None = None,
+                 lse: torch.Tensor | None = None, workspace: torch.Tensor | None = None):
         if q.dtype != k.dtype or q.dtype != v.dtype:
             raise TypeError("q, k, v must share one dtype")
         dev = q.device
@@ -122,6 +122,10 @@ class FwdCall:
         a.kernel = _KERNELS[kernel]
         a.num_ctas = int(num_ctas)
         a.num_splits = int(num_splits)
+        a.prune_threshold = float(prune_threshold)
+        # pruned-tile counter (device, int64 storage of the library's uint64)
+        self.pruned_tiles = torch.zeros(1, dtype=torch.int64, device=dev) if prune_threshold else None
+        a.pruned_tiles = self.pruned_tiles.data_ptr() if self.pruned_tiles is not None else None
         lib = _abi.load()
         need = lib.attn_fwd_workspace_bytes(ctypes.byref(a))
         self.workspace = workspace if workspace is not None else _workspace(need, dev)
@@ -139,6 +143,10 @@ class FwdCall:
         """"tc" or "simt": the kernel family these arguments run."""
         return _selected(_abi.load().attn_fwd_selected_kernel(ctypes.byref(self.args)),
                          "attn_fwd_selected_kernel")
+
+    def pruned_count(self) -> int:
+        """Tiles pruned by all runs of this call so far (0 without pruning)."""
+        return int(self.pruned_tiles.item()) if self.pruned_tiles is not None else 0
 
     def num_splits(self) -> int:
         """Key splits (split-K chunks) these arguments run, 1 = none."""
@@ -191,7 +199,7 @@ class BwdCall:
     def __init__(self, q, k, v, o, lse, dout, *, causal: bool = False, scale: float | None = None,
                  cu_seqlens_q=None, cu_seqlens_k=None, grad_dtype: torch.dtype | None = None,
                  kernel: str = "auto", num_ctas: int = 0, dq=None, dk=None, dv=None,
-                 workspace: torch.Tensor | None = None):
+                 workspace: torch.Tensor | None = None, prune_threshold: float = 0.0):
         dev = q.device
         Tq, H, D = q.shape
         Tk = k.shape[0]
@@ -217,6 +225,7 @@ class BwdCall:
         a.cu_seqlens_k = self.cu_k.data_ptr() if self.cu_k is not None else None
         a.kernel = _KERNELS[kernel]
         a.num_ctas = int(num_ctas)
+        a.prune_threshold = float(prune_threshold)  # non-zero: the library refuses (fails closed)
         lib = _abi.load()
         need = lib.attn_bwd_workspace_bytes(ctypes.byref(a))
         self.workspace = workspace if workspace is not None else _workspace(need, dev)
@@ -250,14 +259,16 @@ class BwdCall:
 
 def fwd(q, k, v, *, causal: bool = False, scale: float | None = None, cu_seqlens_q=None,
         cu_seqlens_k=None, out_dtype: torch.dtype | None = None, kernel: str = "auto",
-        num_ctas: int = 0, num_splits: int = 0):
+        num_ctas: int = 0, num_splits: int = 0, prune_threshold: float = 0.0):
     """Attention forward.  Returns ``(o, lse)``; lse is (H, T_q) f32, natural log.
 
     ``num_splits``: key splits per query tile (split-K); 0 lets the library
-    choose, 1 disables splitting."""
+    choose, 1 disables splitting.  ``prune_threshold``: 0 = exact; rho in
+    (0, 1] enables approximate tile pruning (full relation, one sequence)."""
     return FwdCall(q, k, v, causal=causal, scale=scale, cu_seqlens_q=cu_seqlens_q,
                    cu_seqlens_k=cu_seqlens_k, out_dtype=out_dtype, kernel=kernel,
-                   num_ctas=num_ctas, num_splits=num_splits).run()
+                   num_ctas=num_ctas, num_splits=num_splits,
+                   prune_threshold=prune_threshold).run()
 
 
 def merge(o_parts, lse_parts, *, out_dtype: torch.dtype = torch.float32):

@@ -48,6 +48,7 @@ class FwdArgs(ctypes.Structure):
         ("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_k", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("kernel", ctypes.c_int32), ("num_ctas", ctypes.c_int32), ("num_splits", ctypes.c_int32),
+        ("prune_threshold", ctypes.c_float), ("pruned_tiles", ctypes.c_void_p),
     ]
 
 
@@ -70,6 +71,7 @@ class BwdArgs(ctypes.Structure):
         ("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_k", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("kernel", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
+        ("prune_threshold", ctypes.c_float),
     ]
 
 

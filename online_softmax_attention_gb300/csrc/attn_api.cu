@@ -2,6 +2,7 @@
 // schedule preparation and kernel dispatch.  See include/attn.h for the
 // contract of each entry point.
 #include <atomic>
+#include <cmath>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -165,6 +166,11 @@ int plan_fwd(const attn_fwd_args *a, FwdParams &p, bool &use_tc) {
     if (rc) return rc;
     if (a->o_dtype != a->dtype && a->o_dtype != ATTN_F32) return ATTN_EINVAL;
     if (a->num_splits < 0 || a->num_splits > ATTN_MAX_SPLITS) return ATTN_EINVAL;
+    const float rho = a->prune_threshold;
+    if (!(rho >= 0.f && rho <= 1.f)) return ATTN_EINVAL;  // also rejects NaN
+    // tile pruning is defined for the dense relation over one sequence, unsplit
+    if (rho > 0.f && (a->relation != ATTN_FULL || a->cu_seqlens_q || a->num_splits > 1))
+        return ATTN_EUNSUPPORTED;
     const bool any_q = a->n_q > 0, any_k = a->n_k > 0;
     if (!valid_view(a->q, a->dtype, any_q) || !valid_view(a->o, a->o_dtype, any_q) ||
         !valid_view(a->k, a->dtype, any_k) || !valid_view(a->v, a->dtype, any_k))
@@ -185,7 +191,10 @@ int plan_fwd(const attn_fwd_args *a, FwdParams &p, bool &use_tc) {
     p.watchdog_cycles = watchdog_cycles();
     rc = choose_tc(a->kernel, tc_fwd_supported(p), use_tc);
     if (rc) return rc;
-    p.n_splits = a->num_splits > 0 ? a->num_splits : auto_splits(p, use_tc);
+    p.prune = rho > 0.f;
+    p.prune_log2 = p.prune ? std::log2(rho) : 0.f;
+    p.pruned_tiles = reinterpret_cast<unsigned long long *>(a->pruned_tiles);
+    p.n_splits = p.prune ? 1 : (a->num_splits > 0 ? a->num_splits : auto_splits(p, use_tc));
     // work items (tiles x heads x splits) are numbered in int32
     const int64_t tiles = (int64_t)a->H * ((int64_t)a->n_q / kSimtBlock + a->n_seq + 1);
     if (tiles * p.n_splits >= (int64_t)1 << 31) return ATTN_EUNSUPPORTED;
@@ -260,6 +269,7 @@ int build_bwd(const attn_bwd_args *a, BwdParams &p, bool &use_tc) {
     if (rc) return rc;
     if (a->o_dtype != a->dtype && a->o_dtype != ATTN_F32) return ATTN_EINVAL;
     if (a->grad_dtype != a->dtype && a->grad_dtype != ATTN_F32) return ATTN_EINVAL;
+    if (a->prune_threshold != 0.f) return ATTN_EUNSUPPORTED;  // fails closed
     const bool any_q = a->n_q > 0, any_k = a->n_k > 0;
     if (!valid_view(a->q, a->dtype, any_q) || !valid_view(a->o, a->o_dtype, any_q) ||
         !valid_view(a->dout, a->dtype, any_q) || !valid_view(a->dq, a->grad_dtype, any_q) ||

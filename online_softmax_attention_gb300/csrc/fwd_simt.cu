@@ -60,6 +60,7 @@ __global__ void __launch_bounds__(NT) fwd_simt_kernel(const FwdParams p) {
     float *sV = sK + BK * LD;
     float *sP = sV + BK * LD;
     __shared__ int s_w;
+    __shared__ float s_tile_max[NT / 32];  // tile pruning: per-warp largest score
 
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
     const int total = p.sched.hdr[1];
@@ -94,6 +95,7 @@ __global__ void __launch_bounds__(NT) fwd_simt_kernel(const FwdParams p) {
         const int n_keys = p.causal ? min(Lk, row0 + BQ) : Lk;
         // split-K: this item scans chunk it.c of the row's key tiles
         const KeyChunk chunk = key_chunk((n_keys + BK - 1) / BK, p.n_splits, it.c);
+        float m_run = -INFINITY;  // tile pruning: largest score of the admitted tiles (log2 units)
         const Tin *kbase = gk + (int64_t)k_start * p.k_st + (int64_t)h * p.k_sh;
         const Tin *vbase = gv + (int64_t)k_start * p.v_st + (int64_t)h * p.v_sh;
 
@@ -128,18 +130,46 @@ __global__ void __launch_bounds__(NT) fwd_simt_kernel(const FwdParams p) {
                     }
             }
 
-            // scale into the base-2 domain, mask, online softmax update
+            // scale into the base-2 domain, mask
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int row = row0 + ty + 16 * r;
-                float mx = -INFINITY;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int key = key0 + tx + 16 * c;
                     const bool ok = key < Lk && (!p.causal || key <= row);
                     s[r][c] = ok ? s[r][c] * p.scale_log2 : -INFINITY;
-                    mx = fmaxf(mx, s[r][c]);
                 }
+            }
+            if (p.prune) {
+                // tile pruning: the largest score of the 64 x 64 tile (rows past the
+                // queries excluded) against the query tile's rolling max
+                float tm = -INFINITY;
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    if (row0 + ty + 16 * r < Lq)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) tm = fmaxf(tm, s[r][c]);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
+                if ((tid & 31) == 0) s_tile_max[tid >> 5] = tm;
+                __syncthreads();
+                float m_tile = s_tile_max[0];
+#pragma unroll
+                for (int w8 = 1; w8 < NT / 32; ++w8) m_tile = fmaxf(m_tile, s_tile_max[w8]);
+                const bool admit = m_run == -INFINITY || m_tile >= m_run + p.prune_log2;
+                if (!admit) {  // uniform across the block: nothing of this tile is used
+                    if (tid == 0 && p.pruned_tiles) atomicAdd(p.pruned_tiles, 1ull);
+                    continue;   // the next tile's first barrier orders the s_tile_max reuse
+                }
+                m_run = fmaxf(m_run, m_tile);
+            }
+            // online softmax update
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                float mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) mx = fmaxf(mx, s[r][c]);
 #pragma unroll
                 for (int o = 1; o < 16; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
                 const float m_new = fmaxf(m[r], mx);

@@ -31,6 +31,11 @@
 // TMEM (512 columns): S_0 / P_0 at [0, 128), S_1 / P_1 at [128, 256),
 // U_0 at [256, 256 + D), U_1 at [256 + D, 256 + 2D).
 //
+// Tile pruning (approximate, on request): after S of a 128 x 128 tile is in
+// registers the four warps of the tile's softmax warpgroup combine their row
+// maxima into the tile's largest score; a tile below the query tile's rolling
+// max + log2(rho) is skipped (no exponentials, no value MMA).
+//
 // Split-K: with n_splits > 1 an item is (256 query rows, key chunk c); both
 // tiles scan chunk c of the item's key tiles and write a partial O (f32,
 // normalised by its own l) and lse, which a merge kernel combines.
@@ -100,6 +105,15 @@ struct __align__(8) FwdBars {
     uint64_t s_full[NQT], p_full[NQT], o_done[NQT], o_free[NQT];
     uint64_t sched_full[2], sched_empty[2];
     uint64_t mma_drain;  // abort path: completion of the MMAs already issued
+    uint64_t tile_max[NQT];  // tile pruning: the four warps' row maxima of the tile are in
+};
+
+// Tile pruning exchange: per query tile, each softmax warp's largest score of
+// the current key tile (double-buffered by use parity), and the decision the
+// softmax warps hand to the MMA issuer (1 = pruned: no value MMA).
+struct PruneShared {
+    float warp_max[NQT][2][4];
+    int skip[NQT];
 };
 
 struct ItemInfo {
@@ -236,8 +250,9 @@ __device__ void producer(const TcFwdArgs &a, FwdBars &bars, int *sched_item, uin
 // ---- warp 1: MMA issuer ----------------------------------------------------------
 
 template <int D, bool kBF16>
-__device__ void mma_issuer(const TcFwdArgs &a, FwdBars &bars, const int *sched_item, uint32_t sQ,
-                           uint32_t sK, uint32_t sV, uint32_t tmem, const Watchdog &wd) {
+__device__ void mma_issuer(const TcFwdArgs &a, FwdBars &bars, const int *sched_item,
+                           const PruneShared *ps, uint32_t sQ, uint32_t sK, uint32_t sV,
+                           uint32_t tmem, const Watchdog &wd) {
     using C = Cfg<D>;
     const FwdParams &p = a.p;
     const int total = p.sched.hdr[1];
@@ -319,7 +334,9 @@ __device__ void mma_issuer(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
                     ++of_cnt[t];
                 }
                 tc_fence_after();
-                issue_pv(t, vs, j > 0);
+                // a pruned tile adds nothing to U (the first tile is always admitted)
+                const bool pruned = p.prune && *reinterpret_cast<const volatile int *>(&ps->skip[t]);
+                if (!pruned) issue_pv(t, vs, j > 0);
                 if (j == f.n[t] - 1) tc_commit(smem_u32(&bars.o_done[t]));
                 if (j + 1 < f.n[t]) {
                     if (!have_next_k) {
@@ -342,8 +359,8 @@ __device__ void mma_issuer(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
 // ---- warps 4-11: softmax and epilogue ------------------------------------------
 
 template <int D, bool kBF16, typename Tout>
-__device__ void softmax_wg(const TcFwdArgs &a, FwdBars &bars, const int *sched_item, uint32_t tmem,
-                           const Watchdog &wd) {
+__device__ void softmax_wg(const TcFwdArgs &a, FwdBars &bars, const int *sched_item, PruneShared *ps,
+                           uint32_t tmem, const Watchdog &wd) {
     const FwdParams &p = a.p;
     const int total = p.sched.hdr[1];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -354,7 +371,7 @@ __device__ void softmax_wg(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
     const uint32_t o_addr = tmem_addr(tmem, 32 * quarter, 256 + D * t);
     // the score MMA negated S when the scale is negative
     const float sl2 = fabsf(p.scale_log2);
-    uint32_t s_cnt = 0, o_cnt = 0;
+    uint32_t s_cnt = 0, o_cnt = 0, tm_cnt = 0;
     Tout *go = static_cast<Tout *>(p.o);
 
     for (int i = 0;; ++i) {
@@ -383,6 +400,7 @@ __device__ void softmax_wg(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
         }
 
         float m = -INFINITY, l = 0.f;
+        float m_run = -INFINITY;  // tile pruning: largest score of the admitted tiles (log2 units)
         for (int j = 0; j < n; ++j) {
             ok = mbar_wait(smem_u32(&bars.s_full[t]), s_cnt & 1, wd);
             ++s_cnt;
@@ -406,6 +424,33 @@ __device__ void softmax_wg(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
                     if (c >= lim) s[c] = -INFINITY;
             }
             const float mx = row_max<BN>(s) * sl2;
+            if (p.prune) {
+                // largest score of the whole 128 x 128 tile (rows past the queries excluded),
+                // gathered from the four warps through shared memory and an mbarrier
+                float tm = row < f.Lq ? mx : -INFINITY;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
+                const int par = tm_cnt & 1;
+                if (lane == 0) {
+                    ps->warp_max[t][par][quarter] = tm;
+                    mbar_arrive(smem_u32(&bars.tile_max[t]));
+                }
+                ok = mbar_wait(smem_u32(&bars.tile_max[t]), par, wd);
+                ++tm_cnt;
+                if (!__all_sync(0xffffffffu, ok)) return;
+                const volatile float *wm = ps->warp_max[t][par];
+                const float m_tile = fmaxf(fmaxf(wm[0], wm[1]), fmaxf(wm[2], wm[3]));
+                const bool admit = m_run == -INFINITY || m_tile >= m_run + p.prune_log2;
+                if (lrow == 0) *reinterpret_cast<volatile int *>(&ps->skip[t]) = admit ? 0 : 1;
+                if (!admit) {
+                    // nothing of this tile enters m, l or U; S_t may be overwritten
+                    if (lrow == 0 && p.pruned_tiles) atomicAdd(p.pruned_tiles, 1ull);
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(&bars.p_full[t]));
+                    continue;
+                }
+                m_run = fmaxf(m_run, m_tile);
+            }
             const float m_new = fmaxf(m, mx);
             // refresh the max only when it grew by more than 2^8 somewhere in the warp
             const bool rescale = j > 0 && __any_sync(0xffffffffu, m_new > m + kRescaleThreshold);
@@ -488,6 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ FwdBars bars;
+    __shared__ PruneShared prune_shared;
     __shared__ int sched_item[2];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
@@ -508,6 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             mbar_init(smem_u32(&bars.p_full[t]), 128);
             mbar_init(smem_u32(&bars.o_done[t]), 1);
             mbar_init(smem_u32(&bars.o_free[t]), 128);
+            mbar_init(smem_u32(&bars.tile_max[t]), 4);
         }
         for (int s = 0; s < C::kKStages; ++s) {
             mbar_init(smem_u32(&bars.k_full[s]), 1);
@@ -541,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             if (lane == 0) producer<D>(a, bars, sched_item, sQ, sK, sV, wd);
         } else if (warp == 1) {
             if (lane == 0) {
-                mma_issuer<D, kBF16>(a, bars, sched_item, sQ, sK, sV, tmem, wd);
+                mma_issuer<D, kBF16>(a, bars, sched_item, &prune_shared, sQ, sK, sV, tmem, wd);
                 if (aborting(wd)) {  // let issued MMAs finish before TMEM is freed
                     tc_commit(smem_u32(&bars.mma_drain));
                     drain_wait(smem_u32(&bars.mma_drain), 0, kDrainCycles);
@@ -550,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         }
     } else {
         regs_inc<C::kRegsSoftmax>();
-        softmax_wg<D, kBF16, Tout>(a, bars, sched_item, tmem, wd);
+        softmax_wg<D, kBF16, Tout>(a, bars, sched_item, &prune_shared, tmem, wd);
     }
 
     tc_fence_before();

@@ -37,6 +37,11 @@ struct FwdParams {
     // writes its partial (O_c f32, lse_c) at o + c * o_split_st, lse + c * lse_split_st
     int n_splits;
     int64_t o_split_st, lse_split_st;
+    // tile pruning: prune a key tile when its largest score (log2 units) is
+    // below the query tile's rolling max + prune_log2; count pruned tiles
+    int prune;
+    float prune_log2;  // log2(rho)
+    unsigned long long *pruned_tiles;
 };
 
 // Key-tile range [begin, end) of chunk c when n_tiles key tiles are cut into

@@ -62,6 +62,7 @@ def _fwd_args(**kw):
     a.n_seq = 1
     a.kernel = kw.get("kernel", _abi.ATTN_KERNEL_AUTO)
     a.num_splits = kw.get("num_splits", 0)
+    a.prune_threshold = kw.get("prune", 0.0)
     lib = _abi.load()
     a.workspace = FAKE
     a.workspace_bytes = kw.get("ws", lib.attn_fwd_workspace_bytes(ctypes.byref(a)))
@@ -78,6 +79,11 @@ def _fwd_args(**kw):
     ({"o_dtype": _abi.ATTN_BF16}, _abi.ATTN_EINVAL),         # fp16 in, bf16 out
     ({"ws": 16}, _abi.ATTN_EWORKSPACE),
     ({"num_splits": -1}, _abi.ATTN_EINVAL),
+    ({"prune": -0.1}, _abi.ATTN_EINVAL),
+    ({"prune": 1.5}, _abi.ATTN_EINVAL),
+    ({"prune": float("nan")}, _abi.ATTN_EINVAL),
+    ({"prune": 0.5}, _abi.ATTN_EUNSUPPORTED),                  # causal: fails closed
+    ({"prune": 0.5, "relation": _abi.ATTN_FULL, "num_splits": 2}, _abi.ATTN_EUNSUPPORTED),
     ({"num_splits": _abi.ATTN_MAX_SPLITS + 1}, _abi.ATTN_EINVAL),
     ({"kernel": 42}, None),
     ({"dtype": _abi.ATTN_F32, "kernel": _abi.ATTN_KERNEL_TC}, None),
@@ -190,3 +196,24 @@ def test_merge_of_no_rows_launches_nothing():
     before = lib.attn_launch_count()
     assert lib.attn_merge(ctypes.byref(_merge_args(n_q=0)), None) == _abi.ATTN_OK
     assert lib.attn_launch_count() == before
+
+
+def test_pruning_fails_closed_on_varlen_and_backward():
+    lib = _abi.load()
+    a = _fwd_args(relation=_abi.ATTN_FULL, prune=0.5)
+    a.cu_seqlens_q = a.cu_seqlens_k = FAKE
+    assert lib.attn_fwd(ctypes.byref(a), None) == _abi.ATTN_EUNSUPPORTED
+    # a pruned forward never runs split: the query reports one split
+    a = _fwd_args(relation=_abi.ATTN_FULL, prune=0.5)
+    assert lib.attn_fwd_num_splits(ctypes.byref(a)) == 1
+    b = _abi.BwdArgs()
+    for name in ("q", "k", "v", "o", "dout", "dq", "dk", "dv"):
+        setattr(b, name, _abi.AttnTensor(FAKE, 128, 64))
+    b.lse = FAKE
+    b.n_q = b.n_k = 256
+    b.H, b.D, b.scale, b.n_seq = 2, 64, 0.125, 1
+    b.workspace = FAKE
+    b.workspace_bytes = lib.attn_bwd_workspace_bytes(ctypes.byref(b))
+    b.prune_threshold = 0.5
+    for fn in (lib.attn_bwd, lib.attn_bwd_preprocess, lib.attn_bwd_dkdv, lib.attn_bwd_dq):
+        assert fn(ctypes.byref(b), None) == _abi.ATTN_EUNSUPPORTED
