@@ -137,3 +137,89 @@ def make_workload(w: Workload | str) -> dict:
     return make(dtype=w.dtype, H=w.H, D=w.D, seed=w.seed, n_q=w.n_q or None,
                 n_k=w.n_k or None, batch=w.batch, varlen=w.varlen, layout=w.layout,
                 backward=w.backward, key_gain=w.key_gain)
+
+
+# ---- CSR relations (general sparse attention / segment softmax) ---------------------
+#
+# Structure only: which (destination, source) edges exist.  The GAT example of
+# the TIGA-lang attention page builds a radius graph over random points in the
+# unit cube (cutoff 0.15 over 512 points, average degree about 7); the block-
+# diagonal (causal) relation of the varlen section can also be written as CSR.
+
+
+def radius_graph(n: int, cutoff: float, seed: int):
+    """Points uniform in [0, 1)^3 (CPU generator `seed`); an edge j -> i for
+    every pair with |p_i - p_j| < cutoff, i != j.  Returns (positions (n, 3)
+    f32, row_ptr (n + 1) int64 over destinations i, col (E) int32 sources j,
+    sorted within each row).  Pairs are found through a grid of cells of side
+    >= cutoff (the 27 neighbouring cells of each point's cell)."""
+    import numpy as np
+    gen = torch.Generator().manual_seed(seed)
+    pos = torch.rand((n, 3), generator=gen, dtype=torch.float32)
+    p = pos.double().numpy()
+    cells = max(1, int(1.0 / cutoff))
+    cid = np.minimum((p * cells).astype(np.int64), cells - 1)
+    key = (cid[:, 0] * cells + cid[:, 1]) * cells + cid[:, 2]
+    order = np.argsort(key, kind="stable")
+    starts = np.searchsorted(key[order], np.arange(cells ** 3), side="left")
+    counts = np.searchsorted(key[order], np.arange(cells ** 3), side="right") - starts
+    dst_all, src_all = [], []
+    for a in (-1, 0, 1):
+        for b in (-1, 0, 1):
+            for c in (-1, 0, 1):
+                nc = cid + np.array([a, b, c])
+                ok = ((nc >= 0) & (nc < cells)).all(axis=1)
+                i_idx = np.nonzero(ok)[0]
+                kk = (nc[i_idx, 0] * cells + nc[i_idx, 1]) * cells + nc[i_idx, 2]
+                cnt = counts[kk]
+                i_rep = np.repeat(i_idx, cnt)
+                first = np.repeat(starts[kk] - np.concatenate([[0], np.cumsum(cnt)[:-1]]), cnt)
+                j = order[first + np.arange(len(i_rep))]
+                d2 = ((p[i_rep] - p[j]) ** 2).sum(axis=1)
+                keep = (d2 < cutoff * cutoff) & (i_rep != j)
+                dst_all.append(i_rep[keep])
+                src_all.append(j[keep])
+    dst = np.concatenate(dst_all)
+    src = np.concatenate(src_all)
+    srt = np.lexsort((src, dst))
+    dst, src = dst[srt], src[srt]
+    row_ptr = torch.tensor(np.concatenate([[0], np.cumsum(np.bincount(dst, minlength=n))]),
+                           dtype=torch.int64)
+    col = torch.tensor(src.astype(np.int32), dtype=torch.int32)
+    return pos, row_ptr, col
+
+
+def csr_of_segments(lengths_q, lengths_k, causal: bool):
+    """CSR of the block-diagonal relation of cu_seqlens-packed sequences:
+    query i of sequence b has edges to keys of sequence b (j <= i if causal)."""
+    rows, cols = [], []
+    q0 = k0 = 0
+    for lq, lk in zip(lengths_q, lengths_k):
+        for i in range(lq):
+            n = min(i + 1, lk) if causal else lk
+            rows.append(n)
+            cols.append(torch.arange(k0, k0 + n, dtype=torch.int32))
+        q0 += lq
+        k0 += lk
+    row_ptr = torch.tensor([0] + rows, dtype=torch.int64).cumsum(0)
+    col = torch.cat(cols) if cols else torch.zeros(0, dtype=torch.int32)
+    return row_ptr, col
+
+
+def make_csr(*, row_ptr, col, n_src: int, H: int, D: int, dtype: str, seed: int,
+             field_scores: bool, score_std: float = 1.0) -> dict:
+    """Tensors for a CSR attention: v (n_src, H, D) always; with field_scores,
+    scores (E, H) f32 ~ score_std * N(0, 1); else q (n_dst, H, D) and
+    k (n_src, H, D).  Draw order: v, then scores or q, k."""
+    gen = torch.Generator().manual_seed(seed)
+    tdt = DTYPES[dtype]
+    n_dst = len(row_ptr) - 1
+    out = {"row_ptr": row_ptr, "col": col, "v": _randn(gen, (n_src, H, D), tdt)}
+    if field_scores:
+        out["scores"] = score_std * torch.randn((len(col), H), generator=gen, dtype=torch.float32)
+        out["q"] = out["k"] = None
+    else:
+        out["scores"] = None
+        out["q"] = _randn(gen, (n_dst, H, D), tdt)
+        out["k"] = _randn(gen, (n_src, H, D), tdt)
+    return out

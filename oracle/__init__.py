@@ -68,6 +68,10 @@ def _load():
             ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _dp, _dp, _dp,
             ctypes.c_double, ctypes.c_double, ctypes.c_int, ctypes.c_int, _dp, _dp, _i64p, _dp,
             ctypes.c_int]
+        lib.oracle_csr_fwd.restype = ctypes.c_int
+        lib.oracle_csr_fwd.argtypes = [
+            ctypes.c_int64, ctypes.c_int64, _i64p, _i32p, ctypes.c_int, ctypes.c_int, _dp, _dp,
+            _dp, _dp, ctypes.c_double, _dp, _dp, ctypes.c_int]
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -248,6 +252,40 @@ def fwd_pruned(q, k, v, *, rho: float, block_q: int, block_k: int, scale: float 
     if rc != 0:
         raise ValueError(f"oracle_attn_fwd_pruned rejected its arguments (rc={rc})")
     return o, lse, int(n_pruned[0]), float(margin[0])
+
+
+def csr_fwd(row_ptr, col, v, *, scores=None, q=None, k=None, scale: float | None = None,
+            threads: int = 0):
+    """Attention over a CSR relation: softmax over each destination row's edges.
+
+    ``row_ptr`` (n_dst + 1) and ``col`` (E) define the relation; ``v`` is
+    (n_src, H, D).  Scores are ``scores`` (E, H) when given, else
+    scale * <q_i, k_j> with q (n_dst, H, D), k (n_src, H, D), scale default
+    D^-1/2.  Returns float64 ``(o (n_dst, H, D), lse (H, n_dst))``.
+    """
+    rp = np.ascontiguousarray(np.asarray(row_ptr.cpu() if hasattr(row_ptr, "cpu") else row_ptr,
+                                         dtype=np.int64))
+    cl = np.ascontiguousarray(np.asarray(col.cpu() if hasattr(col, "cpu") else col, dtype=np.int32))
+    v = _f64(v)
+    n_src, H, D = _shape3(v, "v")
+    n_dst = len(rp) - 1
+    sc = _f64(scores) if scores is not None else None
+    if sc is not None and sc.shape != (len(cl), H):
+        raise ValueError(f"scores must be (E, H) = {(len(cl), H)}, got {sc.shape}")
+    qq = _f64(q) if q is not None else None
+    kk = _f64(k) if k is not None else None
+    if scale is None:
+        scale = D ** -0.5
+    o = np.zeros((n_dst, H, D), dtype=np.float64)
+    lse = np.zeros((H, n_dst), dtype=np.float64)
+    rc = _load().oracle_csr_fwd(n_dst, n_src, _ptr(rp, _i64p), _ptr(cl, _i32p), H, D,
+                                None if sc is None else _ptr(sc, _dp),
+                                None if qq is None else _ptr(qq, _dp),
+                                None if kk is None else _ptr(kk, _dp), _ptr(v, _dp), float(scale),
+                                _ptr(o, _dp), _ptr(lse, _dp), int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle_csr_fwd rejected its arguments (rc={rc})")
+    return o, lse
 
 
 if __name__ == "__main__":  # pragma: no cover - manual build hook

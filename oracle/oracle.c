@@ -81,6 +81,18 @@
  *    the end of the queries and keys past the end of the keys are not part
  *    of any tile.
  *
+ *  - Attention over a general CSR relation.  TIGA-lang attention examples
+ *    page: section "用图组合表达 varlen 因果注意力" (the relation as an explicit
+ *    CSR graph holding exactly the admitted edges; a missing edge is simply
+ *    absent) and section "用 nn 打分的 GAT 边注意力", its display equation
+ *        out_i = sum_{e = (j -> i)} exp(s_e) / sum_{e' = (j' -> i)} exp(s_e') x_j,
+ *    a softmax over the incoming edges of each destination row.  Row i's
+ *    edges are col[row_ptr[i] .. row_ptr[i+1]); a repeated edge counts once
+ *    per occurrence.  The score of an edge is either given per edge and head
+ *    (a field score; the page's score network itself is not part of this) or
+ *    the dot-product score scale * <q_i, k_j>.  A row without edges gets
+ *    O = 0, lse = -inf.
+ *
  * Layout: q, o, dq, dO are (T_q, H, D) row-major; k, v, dk, dv are (T_k, H, D);
  * lse is (H, T_q).  cu_q / cu_k hold n_seq + 1 cumulative offsets starting at 0.
  * All arrays are host memory owned by the caller.
@@ -558,5 +570,63 @@ int oracle_attn_fwd_pruned(int64_t Tq, int64_t Tk, int H, int D, const double *q
     }
     if (n_pruned) *n_pruned = pruned_total;
     if (min_margin) *min_margin = margin_min;
+    return 0;
+}
+
+/*
+ * Attention over a CSR relation (see the header comment).  row_ptr has n_dst+1
+ * nondecreasing offsets from 0; col holds row_ptr[n_dst] source indices in
+ * [0, n_src).  scores is (E, H) or NULL (then scores are scale * <q_i, k_j>,
+ * q (n_dst, H, D), k (n_src, H, D)).  v is (n_src, H, D); o is (n_dst, H, D),
+ * lse (H, n_dst).  Returns 0, or -1 on a malformed relation.
+ */
+int oracle_csr_fwd(int64_t n_dst, int64_t n_src, const int64_t *row_ptr, const int32_t *col,
+                   int H, int D, const double *scores, const double *q, const double *k,
+                   const double *v, double scale, double *o, double *lse, int n_threads)
+{
+    if (n_dst < 0 || n_src < 0 || H < 1 || D < 1 || !row_ptr || row_ptr[0] != 0) return -1;
+    for (int64_t i = 0; i < n_dst; ++i)
+        if (row_ptr[i + 1] < row_ptr[i]) return -1;
+    const int64_t E = row_ptr[n_dst];
+    for (int64_t e = 0; e < E; ++e)
+        if (col[e] < 0 || col[e] >= n_src) return -1;
+    if (!scores && (!q || !k)) return -1;
+    set_threads(n_threads);
+    const int64_t ld = (int64_t)H * D;
+    int64_t max_deg = 0;
+    for (int64_t i = 0; i < n_dst; ++i)
+        if (row_ptr[i + 1] - row_ptr[i] > max_deg) max_deg = row_ptr[i + 1] - row_ptr[i];
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(max_deg > 0 ? max_deg : 1));
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t r = 0; r < n_dst * H; ++r) {
+            const int64_t i = r / H;
+            const int h = (int)(r % H);
+            const int64_t e0 = row_ptr[i], deg = row_ptr[i + 1] - e0;
+            double *orow = o + i * ld + (int64_t)h * D;
+            for (int d = 0; d < D; ++d) orow[d] = 0.0;
+            if (deg == 0) {
+                lse[(int64_t)h * n_dst + i] = -INFINITY;
+                continue;
+            }
+            double m = -INFINITY;
+            for (int64_t t = 0; t < deg; ++t) {
+                const int64_t j = col[e0 + t];
+                s[t] = scores ? scores[(e0 + t) * H + h]
+                              : scale * dot(q + i * ld + (int64_t)h * D, k + j * ld + (int64_t)h * D, D);
+                if (s[t] > m) m = s[t];
+            }
+            double l = 0.0;
+            for (int64_t t = 0; t < deg; ++t) l += exp(s[t] - m);
+            for (int64_t t = 0; t < deg; ++t) {
+                const double p = exp(s[t] - m) / l;
+                const double *vj = v + (int64_t)col[e0 + t] * ld + (int64_t)h * D;
+                for (int d = 0; d < D; ++d) orow[d] += p * vj[d];
+            }
+            lse[(int64_t)h * n_dst + i] = m + log(l);
+        }
+        free(s);
+    }
     return 0;
 }

@@ -453,3 +453,92 @@ def test_pruned_rejects_rho_outside_unit_interval():
     for rho in (0.0, -0.5, 1.5, float("nan")):
         with pytest.raises(ValueError):
             oracle.fwd_pruned(q, q, q, rho=rho, block_q=2, block_k=2)
+
+
+# --- attention over a general CSR relation -------------------------------------------
+
+def _csr_cases():
+    with open(os.path.join(GOLDEN, "csr_cases.json")) as f:
+        return json.load(f)["cases"]
+
+
+@pytest.mark.parametrize("case", _csr_cases(), ids=lambda c: c["name"])
+def test_csr_hand_cases(case):
+    v = np.array(_ev_inf(case["v"]), dtype=np.float64)
+    sc = np.array(_ev_inf(case["scores"]), dtype=np.float64)
+    o, lse = oracle.csr_fwd(case["row_ptr"], case["col"], v, scores=sc)
+    np.testing.assert_allclose(o, np.array(_ev_inf(case["o"])), rtol=0, atol=1e-13)
+    ref = np.array(_ev_inf(case["lse"]))
+    np.testing.assert_array_equal(np.isneginf(lse), np.isneginf(ref))
+    np.testing.assert_allclose(lse[np.isfinite(ref)], ref[np.isfinite(ref)], rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal,lengths_q,lengths_k", [
+    (True, [384, 1, 96, 640, 57], None),   # the varlen example's lengths
+    (False, [100, 3, 257], [31, 300, 128]),
+    (True, [0, 5, 0, 70], None),
+])
+def test_csr_of_segment_relations_equals_dense_attention(causal, lengths_q, lengths_k):
+    """The block-diagonal (causal) relation written as CSR gives the same
+    attention as the cu_seqlens form."""
+    import attn_inputs
+    lk = lengths_k or lengths_q
+    x = attn_inputs.make(dtype="f32", H=2, D=16, seed=90, lengths=lengths_q, lengths_k=lk)
+    row_ptr, col = attn_inputs.csr_of_segments(lengths_q, lk, causal)
+    o, lse = oracle.csr_fwd(row_ptr, col, x["v"], q=x["q"], k=x["k"], scale=0.3)
+    o_ref, lse_ref = oracle.fwd(x["q"], x["k"], x["v"], causal=causal, scale=0.3,
+                                cu_seqlens_q=x["cu_seqlens_q"], cu_seqlens_k=x["cu_seqlens_k"])
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-13)
+    np.testing.assert_array_equal(np.isneginf(lse), np.isneginf(lse_ref))
+    fin = np.isfinite(lse_ref)
+    np.testing.assert_allclose(lse[fin], lse_ref[fin], rtol=0, atol=1e-13)
+
+
+def test_csr_field_scores_equal_dot_scores_given_as_a_field():
+    import attn_inputs
+    _, row_ptr, col = attn_inputs.radius_graph(300, 0.2, seed=91)
+    x = attn_inputs.make_csr(row_ptr=row_ptr, col=col, n_src=300, H=3, D=8, dtype="f32", seed=92,
+                             field_scores=False)
+    q, k = x["q"].double().numpy(), x["k"].double().numpy()
+    dst = np.repeat(np.arange(300), np.diff(row_ptr.numpy()))
+    sc = 0.5 * np.einsum("ehd,ehd->eh", q[dst], k[col.numpy()])
+    a = oracle.csr_fwd(row_ptr, col, x["v"], scores=sc)
+    b = oracle.csr_fwd(row_ptr, col, x["v"], q=x["q"], k=x["k"], scale=0.5)
+    np.testing.assert_allclose(a[0], b[0], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(a[1], b[1], rtol=0, atol=1e-12)
+
+
+def test_csr_edge_order_within_a_row_does_not_matter():
+    import attn_inputs
+    _, row_ptr, col = attn_inputs.radius_graph(200, 0.25, seed=93)
+    x = attn_inputs.make_csr(row_ptr=row_ptr, col=col, n_src=200, H=2, D=4, dtype="f32", seed=94,
+                             field_scores=True)
+    rng = np.random.default_rng(95)
+    perm = np.concatenate([a + rng.permutation(b - a) for a, b in
+                           zip(row_ptr[:-1].tolist(), row_ptr[1:].tolist())]).astype(np.int64)
+    a = oracle.csr_fwd(row_ptr, col, x["v"], scores=x["scores"])
+    b = oracle.csr_fwd(row_ptr, col.numpy()[perm], x["v"], scores=x["scores"].numpy()[perm])
+    np.testing.assert_allclose(a[0], b[0], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(a[1], b[1], rtol=0, atol=1e-13)
+
+
+def test_csr_rejects_malformed_relations():
+    v = np.zeros((2, 1, 4))
+    sc = np.zeros((2, 1))
+    with pytest.raises(ValueError):
+        oracle.csr_fwd([0, 2], [0, 2], v, scores=sc)    # source out of range
+    with pytest.raises(ValueError):
+        oracle.csr_fwd([0, 2, 1], [0, 1], v, scores=sc)  # decreasing offsets
+    with pytest.raises(ValueError):
+        oracle.csr_fwd([1, 2], [0, 1], v, scores=sc)     # not starting at 0
+
+
+def test_radius_graph_matches_brute_force():
+    """The input generator's cell search finds exactly the pairs closer than the cutoff."""
+    import attn_inputs
+    pos, row_ptr, col = attn_inputs.radius_graph(512, 0.15, seed=0)
+    p = pos.double().numpy()
+    d2 = ((p[:, None, :] - p[None, :, :]) ** 2).sum(-1)
+    adj = (d2 < 0.15 ** 2) & ~np.eye(512, dtype=bool)
+    for i in range(512):
+        np.testing.assert_array_equal(col[row_ptr[i]:row_ptr[i + 1]].numpy(), np.nonzero(adj[i])[0])
