@@ -174,12 +174,42 @@ typedef struct attn_merge_args {
     int32_t o_dtype;        /* attn_dtype */
 } attn_merge_args;
 
+/* Attention over a general CSR relation (TIGA-lang attention examples page:
+ * the varlen section writes a relation as an explicit CSR graph of exactly
+ * the admitted edges; the GAT section's display equation is a softmax over
+ * each row's incoming edges):
+ *     out[i, h] = sum_{e in row i} exp(s[e, h]) / sum_{e' in row i} exp(s[e', h]) * v[col[e], h]
+ * Row i's edges are col_idx[row_ptr[i] .. row_ptr[i+1]); an edge listed twice
+ * counts twice.  The score is the field edge_scores[e, h] (segment softmax)
+ * or, with edge_scores NULL, scale * <q[i, h], k[col[e], h]>.  A row without
+ * edges gets O = 0, lse = -inf.  Malformed relations (offsets that decrease
+ * or leave [0, n_edges], sources outside [0, n_src)) are not read out of
+ * bounds: the row or edge is skipped and attn_device_status() reports
+ * ATTN_EINVAL.  One kernel on `stream`; no workspace. */
+typedef struct attn_csr_args {
+    const int64_t *row_ptr;   /* device, n_dst + 1 nondecreasing offsets in [0, n_edges] */
+    const int32_t *col_idx;   /* device, n_edges source indices */
+    int64_t n_edges;
+    int32_t n_dst, n_src;     /* destination rows; source rows */
+    int32_t H, D;             /* heads; D a multiple of 4, at most 256 */
+    const float *edge_scores; /* device (n_edges, H) f32 field scores, or NULL */
+    attn_tensor q;            /* (n_dst, H, D) dtype, dot-product scores only */
+    attn_tensor k;            /* (n_src, H, D) dtype, dot-product scores only */
+    attn_tensor v;            /* (n_src, H, D) dtype */
+    attn_tensor o;            /* out: (n_dst, H, D) o_dtype */
+    float *lse;               /* out: (H, n_dst) f32, or NULL */
+    float scale;              /* dot-product scores only */
+    int32_t dtype;            /* attn_dtype of q, k, v */
+    int32_t o_dtype;          /* dtype or ATTN_F32 */
+} attn_csr_args;
+
 /* Library ABI version (ATTN_ABI_VERSION) and struct sizes, for bindings to
  * check their mirrors of the structs above. */
 ATTN_API int attn_abi_version(void);
 ATTN_API size_t attn_fwd_args_size(void);
 ATTN_API size_t attn_bwd_args_size(void);
 ATTN_API size_t attn_merge_args_size(void);
+ATTN_API size_t attn_csr_args_size(void);
 
 /* Bytes of device workspace the call needs (depends on n_seq, H, n_q, and
  * for the forward on the number of key splits: n_splits > 1 adds the partial
@@ -240,6 +270,9 @@ ATTN_API int attn_fwd_simple(const void *q, const void *k, const void *v, void *
  * would be rejected.  Host-only; launches nothing. */
 ATTN_API int attn_fwd_selected_kernel(const attn_fwd_args *a);
 ATTN_API int attn_bwd_selected_kernel(const attn_bwd_args *a);
+
+/* Attention over the CSR relation of `a` (see attn_csr_args). */
+ATTN_API int attn_csr_fwd(const attn_csr_args *a, void *stream);
 
 /* Forward for callers that cannot allocate device memory (no counterpart on
  * the pages; a deployment convenience).  Same arguments and results as

@@ -9,6 +9,8 @@ argument structs:
 * ``bwd(q, k, v, o, lse, dout, causal=...)`` -> ``(dq, dk, dv)``
 * ``merge(o_parts, lse_parts)`` -> ``(o, lse)``: attention over the union of
   disjoint key sets from each set's result (the split-K merge)
+* ``csr_fwd(row_ptr, col, v, scores=... | q=..., k=...)`` -> ``(o, lse)``:
+  attention over a general CSR relation (softmax over each row's edges)
 * ``FwdCall`` / ``BwdCall`` hold prepared argument structs for repeated
   launches (the benchmark and CUDA-graph capture use them).
 
@@ -27,8 +29,8 @@ from . import _abi
 from ._abi import (ATTN_BF16, ATTN_CAUSAL, ATTN_F16, ATTN_F32, ATTN_FULL, ATTN_KERNEL_AUTO,
                    ATTN_KERNEL_SIMT, ATTN_KERNEL_TC, AttnError, check)
 
-__all__ = ["fwd", "bwd", "merge", "FwdCall", "BwdCall", "MergeCall", "device_status",
-           "launch_count", "AttnError", "library_path"]
+__all__ = ["fwd", "bwd", "merge", "csr_fwd", "FwdCall", "BwdCall", "MergeCall", "CsrCall",
+           "device_status", "launch_count", "AttnError", "library_path"]
 
 _DT = {torch.float16: ATTN_F16, torch.bfloat16: ATTN_BF16, torch.float32: ATTN_F32}
 _KERNELS = {"auto": ATTN_KERNEL_AUTO, "simt": ATTN_KERNEL_SIMT, "tc": ATTN_KERNEL_TC}
@@ -255,6 +257,65 @@ class BwdCall:
         """"tc" or "simt": the kernel family these arguments run."""
         return _selected(self._lib.attn_bwd_selected_kernel(ctypes.byref(self.args)),
                          "attn_bwd_selected_kernel")
+
+
+class CsrCall:
+    """Prepared attention over a CSR relation.
+
+    ``row_ptr`` (n_dst + 1) int64 and ``col`` (E) int32 on the device define
+    the relation (row i's edges are ``col[row_ptr[i]:row_ptr[i+1]]``); ``v``
+    is (n_src, H, D).  Scores: ``scores`` (E, H) float32 field scores, or
+    ``q`` (n_dst, H, D) and ``k`` (n_src, H, D) for scale * <q_i, k_j>.
+    """
+
+    def __init__(self, row_ptr, col, v, *, scores=None, q=None, k=None, n_dst: int | None = None,
+                 scale: float | None = None, out_dtype: torch.dtype | None = None,
+                 out: torch.Tensor | None = None, lse: torch.Tensor | None = None):
+        dev = v.device
+        if row_ptr.dtype != torch.int64 or col.dtype != torch.int32:
+            raise TypeError("row_ptr must be int64 and col int32")
+        if not (row_ptr.is_cuda and col.is_cuda):
+            raise ValueError("row_ptr and col must be CUDA tensors")
+        n_src, H, D = v.shape
+        n_dst = len(row_ptr) - 1 if n_dst is None else n_dst
+        if scores is None and (q is None or k is None):
+            raise ValueError("give either scores or both q and k")
+        out_dtype = out_dtype or v.dtype
+        self.o = out if out is not None else torch.empty((n_dst, H, D), dtype=out_dtype, device=dev)
+        self.lse = lse if lse is not None else torch.empty((H, n_dst), dtype=torch.float32, device=dev)
+        self.inputs = (row_ptr, col, v, scores, q, k)
+        a = _abi.CsrArgs()
+        a.row_ptr = row_ptr.data_ptr()
+        a.col_idx = col.data_ptr() if col.numel() else None
+        a.n_edges = col.numel()
+        a.n_dst, a.n_src, a.H, a.D = n_dst, n_src, H, D
+        if scores is not None:
+            if scores.dtype != torch.float32 or tuple(scores.shape) != (col.numel(), H) \
+                    or not scores.is_contiguous():
+                raise ValueError("scores must be contiguous float32 (E, H)")
+            a.edge_scores = scores.data_ptr() if scores.numel() else None
+            if not scores.numel():
+                a.edge_scores = row_ptr.data_ptr()  # no edge reads it; marks field scores
+        else:
+            a.q, a.k = _view(q, "q"), _view(k, "k")
+        a.v, a.o = _view(v, "v"), _view(self.o, "out")
+        a.lse = self.lse.data_ptr() if self.lse.numel() else None
+        a.scale = float(scale) if scale is not None else D ** -0.5
+        a.dtype, a.o_dtype = _dtype_code(v.dtype), _dtype_code(self.o.dtype)
+        self.args = a
+        self._fn = _abi.load().attn_csr_fwd
+
+    def run(self, stream: torch.cuda.Stream | None = None):
+        s = stream if stream is not None else torch.cuda.current_stream()
+        check(self._fn(ctypes.byref(self.args), ctypes.c_void_p(s.cuda_stream)), "attn_csr_fwd")
+        return self.o, self.lse
+
+
+def csr_fwd(row_ptr, col, v, *, scores=None, q=None, k=None, scale: float | None = None,
+            out_dtype: torch.dtype | None = None):
+    """Attention over a CSR relation.  Returns ``(o, lse)``."""
+    return CsrCall(row_ptr, col, v, scores=scores, q=q, k=k, scale=scale,
+                   out_dtype=out_dtype).run()
 
 
 def fwd(q, k, v, *, causal: bool = False, scale: float | None = None, cu_seqlens_q=None,

@@ -29,7 +29,7 @@ EXPORTS = (
     "attn_device_status", "attn_launch_count", "attn_strerror", "attn_last_error_string",
     "attn_fwd_selected_kernel", "attn_bwd_selected_kernel", "attn_fwd_noalloc",
     "attn_selftest_exp2", "attn_set_watchdog_cycles", "attn_merge_args_size",
-    "attn_fwd_num_splits", "attn_merge",
+    "attn_fwd_num_splits", "attn_merge", "attn_csr_args_size", "attn_csr_fwd",
 )
 
 
@@ -57,6 +57,17 @@ class MergeArgs(ctypes.Structure):
         ("o_parts", ctypes.c_void_p), ("lse_parts", ctypes.c_void_p), ("o", AttnTensor),
         ("lse", ctypes.c_void_p), ("n_parts", ctypes.c_int32), ("n_q", ctypes.c_int32),
         ("H", ctypes.c_int32), ("D", ctypes.c_int32), ("o_dtype", ctypes.c_int32),
+    ]
+
+
+class CsrArgs(ctypes.Structure):
+    _fields_ = [
+        ("row_ptr", ctypes.c_void_p), ("col_idx", ctypes.c_void_p), ("n_edges", ctypes.c_int64),
+        ("n_dst", ctypes.c_int32), ("n_src", ctypes.c_int32), ("H", ctypes.c_int32),
+        ("D", ctypes.c_int32), ("edge_scores", ctypes.c_void_p),
+        ("q", AttnTensor), ("k", AttnTensor), ("v", AttnTensor), ("o", AttnTensor),
+        ("lse", ctypes.c_void_p), ("scale", ctypes.c_float), ("dtype", ctypes.c_int32),
+        ("o_dtype", ctypes.c_int32),
     ]
 
 
@@ -91,6 +102,7 @@ def load() -> ctypes.CDLL:
     lib = ctypes.CDLL(LIB_PATH)
     vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
     fa, ba, ma = ctypes.POINTER(FwdArgs), ctypes.POINTER(BwdArgs), ctypes.POINTER(MergeArgs)
+    ca = ctypes.POINTER(CsrArgs)
     sigs = {
         "attn_abi_version": (ctypes.c_int, []),
         "attn_fwd_args_size": (sz, []),
@@ -98,6 +110,8 @@ def load() -> ctypes.CDLL:
         "attn_merge_args_size": (sz, []),
         "attn_fwd_num_splits": (ctypes.c_int, [fa]),
         "attn_merge": (ctypes.c_int, [ma, vp]),
+        "attn_csr_args_size": (sz, []),
+        "attn_csr_fwd": (ctypes.c_int, [ca, vp]),
         "attn_fwd_workspace_bytes": (sz, [fa]),
         "attn_bwd_workspace_bytes": (sz, [ba]),
         "attn_fwd": (ctypes.c_int, [fa, vp]),
@@ -125,7 +139,8 @@ def load() -> ctypes.CDLL:
         raise ImportError(f"libattn_gb300 ABI {lib.attn_abi_version()} != binding ABI {ABI_VERSION}")
     if lib.attn_fwd_args_size() != ctypes.sizeof(FwdArgs) or \
             lib.attn_bwd_args_size() != ctypes.sizeof(BwdArgs) or \
-            lib.attn_merge_args_size() != ctypes.sizeof(MergeArgs):
+            lib.attn_merge_args_size() != ctypes.sizeof(MergeArgs) or \
+            lib.attn_csr_args_size() != ctypes.sizeof(CsrArgs):
         raise ImportError("libattn_gb300 struct layout does not match the binding")
     _lib = lib
     return lib

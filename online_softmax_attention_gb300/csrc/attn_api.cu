@@ -525,6 +525,51 @@ int attn_device_status(void *stream) {
     return v;
 }
 
+size_t attn_csr_args_size(void) { return sizeof(attn_csr_args); }
+
+int attn_csr_fwd(const attn_csr_args *a, void *stream) {
+    if (!a) return ATTN_EINVAL;
+    if (a->n_dst < 0 || a->n_src < 0 || a->n_edges < 0 || a->H < 1 || a->D < 4 || a->D > 256 ||
+        (a->D & 3) || !valid_dtype(a->dtype) || (a->o_dtype != a->dtype && a->o_dtype != ATTN_F32))
+        return ATTN_EINVAL;
+    const bool dot = a->edge_scores == nullptr;
+    if (dot && !(a->scale == a->scale && a->scale != INFINITY && a->scale != -INFINITY))
+        return ATTN_EINVAL;
+    if ((int64_t)a->n_dst * a->H >= ((int64_t)1 << 40)) return ATTN_EUNSUPPORTED;
+    if (a->n_dst == 0) return ATTN_OK;
+    const bool any_e = a->n_edges > 0;
+    if (!a->row_ptr || (any_e && !a->col_idx) || (reinterpret_cast<uintptr_t>(a->row_ptr) & 7) ||
+        (reinterpret_cast<uintptr_t>(a->col_idx) & 3) ||
+        (!dot && (reinterpret_cast<uintptr_t>(a->edge_scores) & 3)))
+        return ATTN_EINVAL;
+    if (!valid_view(a->o, a->o_dtype, true) || !valid_view(a->v, a->dtype, any_e && a->n_src > 0) ||
+        (dot && (!valid_view(a->q, a->dtype, true) || !valid_view(a->k, a->dtype, any_e && a->n_src > 0))))
+        return ATTN_EINVAL;
+    CsrParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.row_ptr = a->row_ptr;
+    p.col = a->col_idx;
+    p.n_edges = a->n_edges;
+    p.n_dst = a->n_dst;
+    p.n_src = a->n_src;
+    p.H = a->H;
+    p.D = a->D;
+    p.scores = a->edge_scores;
+    p.q = a->q.ptr; p.k = a->k.ptr; p.v = a->v.ptr; p.o = a->o.ptr; p.lse = a->lse;
+    p.q_st = a->q.stride_tok; p.q_sh = a->q.stride_head;
+    p.k_st = a->k.stride_tok; p.k_sh = a->k.stride_head;
+    p.v_st = a->v.stride_tok; p.v_sh = a->v.stride_head;
+    p.o_st = a->o.stride_tok; p.o_sh = a->o.stride_head;
+    p.scale_log2 = a->scale * 1.4426950408889634f;
+    p.dtype = a->dtype;
+    p.o_dtype = a->o_dtype;
+    p.status = status_ptr();
+    if (!p.status) return ATTN_ECUDA;
+    cudaError_t e = launch_csr_fwd(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return set_cuda_error(e);
+    return ATTN_OK;
+}
+
 const char *attn_strerror(int code) {
     switch (code) {
     case ATTN_OK: return "success";

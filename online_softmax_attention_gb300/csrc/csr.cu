@@ -1,0 +1,209 @@
+// Attention over a general CSR relation: for every destination row i and head
+// h, a softmax over the row's edges e = (j -> i) weighs the source rows v_j.
+//
+// TIGA-lang attention examples page: the varlen section writes the relation
+// as an explicit CSR graph holding exactly the admitted edges, and the GAT
+// section's display equation is this operation with a per-edge score
+// (out_i = sum_e exp(s_e) / sum_e' exp(s_e') x_j).  The score of an edge is
+// either a given field s[e, h] (segment softmax) or the dot-product score
+// scale * <q_i, k_j>.  The scan over a row's edges is the online-softmax
+// recurrence of the OCANNL "Module Ir.Online_softmax" page (fourth bullet)
+// with blocks of 32 edges: per block the new max, the rescale factor, the
+// exponentials, the rescaled sum and the value accumulation U += p v.
+//
+// Gather-bound (each edge reads a row of V, and of K for dot-product scores,
+// wherever its source lies), so CUDA cores, not tensor cores: one warp per
+// (row, head).  Lane t owns edge t of the current block of 32 (its column
+// index and score) and columns 4 t + 128 c of the D-wide rows (float4 chunks,
+// c < 2, so D <= 256).  Dot-product scores: every lane forms its columns'
+// partial dot with each of the 32 edges' K rows, then a transposing butterfly
+// (31 shuffles) leaves lane t with edge t's full dot product.
+//
+// Malformed relations never cause an out-of-bounds access: a row whose
+// offsets decrease or run past the edge count is treated as empty and an edge
+// whose source index is out of range is skipped; both set the device status
+// word to ATTN_EINVAL.
+#include "../../include/attn.h"
+#include "common.cuh"
+
+namespace attn {
+
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kChunks = 2;  // float4 column chunks per lane: D <= 256
+
+template <typename T>
+__device__ __forceinline__ float4 ldg4(const T *p) {
+    return load4(p);
+}
+
+template <typename T, typename Tout, bool kDot>
+__global__ void __launch_bounds__(32 * kWarps) csr_fwd_kernel(const CsrParams p) {
+    const int lane = threadIdx.x & 31;
+    const int64_t pairs = (int64_t)p.n_dst * p.H;
+    const int64_t stride = (int64_t)gridDim.x * kWarps;
+    const T *gv = static_cast<const T *>(p.v);
+    const T *gq = static_cast<const T *>(p.q);
+    const T *gk = static_cast<const T *>(p.k);
+    Tout *go = static_cast<Tout *>(p.o);
+    bool live[kChunks];
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) live[c] = 4 * (lane + 32 * c) < p.D;
+
+    for (int64_t r = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); r < pairs; r += stride) {
+        const int i = (int)(r / p.H), h = (int)(r - (int64_t)i * p.H);
+        int64_t e0 = __ldg(p.row_ptr + i), e1 = __ldg(p.row_ptr + i + 1);
+        if (e0 < 0 || e1 < e0 || e1 > p.n_edges) {
+            if (lane == 0) report_status(p.status, ATTN_EINVAL);
+            e0 = e1 = 0;  // treated as a row without edges
+        }
+        float4 qv[kChunks];
+        if (kDot) {
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c)
+                qv[c] = live[c] ? ldg4(gq + (int64_t)i * p.q_st + (int64_t)h * p.q_sh + 4 * (lane + 32 * c))
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float4 acc[kChunks];
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+        float m = -INFINITY, l = 0.f;
+
+        for (int64_t eb = e0; eb < e1; eb += 32) {
+            const int cnt = e1 - eb < 32 ? (int)(e1 - eb) : 32;
+            const int64_t e = eb + lane;
+            int j = -1;
+            if (lane < cnt) {
+                j = __ldg(p.col + e);
+                if (j < 0 || j >= p.n_src) {
+                    report_status(p.status, ATTN_EINVAL);
+                    j = -1;
+                }
+            }
+            float s;  // this lane's edge score, log2 units (-inf: no edge)
+            if (kDot) {
+                // partial dots of my columns with the block's K rows, then a
+                // transposing butterfly: afterwards d[0] of lane t = edge t's dot
+                float d[32];
+#pragma unroll
+                for (int t = 0; t < 32; ++t) {
+                    const int jt = __shfl_sync(0xffffffffu, j, t);
+                    float acc_d = 0.f;
+                    if (jt >= 0) {
+#pragma unroll
+                        for (int c = 0; c < kChunks; ++c) {
+                            if (!live[c]) continue;
+                            const float4 kv = ldg4(gk + (int64_t)jt * p.k_st + (int64_t)h * p.k_sh + 4 * (lane + 32 * c));
+                            acc_d = fmaf(qv[c].x, kv.x, acc_d);
+                            acc_d = fmaf(qv[c].y, kv.y, acc_d);
+                            acc_d = fmaf(qv[c].z, kv.z, acc_d);
+                            acc_d = fmaf(qv[c].w, kv.w, acc_d);
+                        }
+                    }
+                    d[t] = acc_d;
+                }
+#pragma unroll
+                for (int w = 16; w >= 1; w >>= 1) {
+                    const bool upper = (lane & w) != 0;
+#pragma unroll
+                    for (int t = 0; t < w; ++t) {
+                        const float send = upper ? d[t] : d[t + w];
+                        const float keep = upper ? d[t + w] : d[t];
+                        d[t] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+                    }
+                }
+                s = j >= 0 ? d[0] * p.scale_log2 : -INFINITY;
+            } else {
+                s = j >= 0 ? __ldg(p.scores + e * p.H + h) * kLog2e : -INFINITY;
+            }
+
+            // online softmax update over this block of edges
+            float bmax = s;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, o));
+            const float m_new = fmaxf(m, bmax);
+            if (m_new == -INFINITY) continue;  // nothing admitted yet (uniform)
+            const float alpha = exp2_approx(m - m_new);
+            const float pe = exp2_approx(s - m_new);
+            float psum = pe;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
+            l = l * alpha + psum;
+            m = m_new;
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c) {
+                acc[c].x *= alpha;
+                acc[c].y *= alpha;
+                acc[c].z *= alpha;
+                acc[c].w *= alpha;
+            }
+            // U += p v over the block's edges, eight row gathers in flight
+            for (int t0 = 0; t0 < cnt; t0 += 8) {
+                float pt[8];
+                int jt[8];
+                float4 vv[8][kChunks];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    pt[u] = __shfl_sync(0xffffffffu, pe, (t0 + u) & 31);
+                    jt[u] = __shfl_sync(0xffffffffu, j, (t0 + u) & 31);
+                    const bool use = t0 + u < cnt && jt[u] >= 0 && pt[u] != 0.f;
+#pragma unroll
+                    for (int c = 0; c < kChunks; ++c)
+                        vv[u][c] = use && live[c]
+                                       ? ldg4(gv + (int64_t)jt[u] * p.v_st + (int64_t)h * p.v_sh + 4 * (lane + 32 * c))
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (!use) pt[u] = 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+#pragma unroll
+                    for (int c = 0; c < kChunks; ++c) {
+                        acc[c].x = fmaf(pt[u], vv[u][c].x, acc[c].x);
+                        acc[c].y = fmaf(pt[u], vv[u][c].y, acc[c].y);
+                        acc[c].z = fmaf(pt[u], vv[u][c].z, acc[c].z);
+                        acc[c].w = fmaf(pt[u], vv[u][c].w, acc[c].w);
+                    }
+            }
+        }
+
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        Tout *orow = go + (int64_t)i * p.o_st + (int64_t)h * p.o_sh;
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c)
+            if (live[c])
+                store4(orow + 4 * (lane + 32 * c),
+                       make_float4(acc[c].x * inv, acc[c].y * inv, acc[c].z * inv, acc[c].w * inv));
+        if (lane == 0 && p.lse)
+            p.lse[(int64_t)h * p.n_dst + i] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+    }
+}
+
+template <typename T, typename Tout>
+cudaError_t launch_typed(const CsrParams &p, cudaStream_t s) {
+    const int64_t pairs = (int64_t)p.n_dst * p.H;
+    const int64_t want = (pairs + kWarps - 1) / kWarps;
+    const int64_t cap = (int64_t)sm_count() * 16;
+    const int grid = (int)(want < cap ? want : cap);
+    if (p.scores) csr_fwd_kernel<T, Tout, false><<<grid, 32 * kWarps, 0, s>>>(p);
+    else csr_fwd_kernel<T, Tout, true><<<grid, 32 * kWarps, 0, s>>>(p);
+    count_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_csr_fwd(const CsrParams &p, cudaStream_t s) {
+    if ((int64_t)p.n_dst * p.H == 0) return cudaSuccess;
+    if (p.D > 4 * 32 * kChunks) return cudaErrorInvalidValue;
+    switch (p.dtype) {
+    case ATTN_F16:
+        return p.o_dtype == ATTN_F32 ? launch_typed<__half, float>(p, s) : launch_typed<__half, __half>(p, s);
+    case ATTN_BF16:
+        return p.o_dtype == ATTN_F32 ? launch_typed<__nv_bfloat16, float>(p, s)
+                                     : launch_typed<__nv_bfloat16, __nv_bfloat16>(p, s);
+    default: return launch_typed<float, float>(p, s);
+    }
+}
+
+}  // namespace attn

@@ -70,6 +70,24 @@ struct MergeParams {
     int n_parts, n_q, H, D, o_dtype;
 };
 
+// Attention over a CSR relation (row_ptr over destination rows, col = sources).
+struct CsrParams {
+    const int64_t *row_ptr;
+    const int32_t *col;
+    int64_t n_edges;
+    int n_dst, n_src, H, D;
+    const float *scores;  // (n_edges, H) field scores, or null: dot-product scores
+    const void *q, *k, *v;
+    void *o;
+    float *lse;
+    int64_t q_st, q_sh, k_st, k_sh, v_st, v_sh, o_st, o_sh;
+    float scale_log2;
+    int dtype, o_dtype;
+    int *status;
+};
+
+cudaError_t launch_csr_fwd(const CsrParams &p, cudaStream_t s);
+
 struct BwdParams {
     const void *q, *k, *v, *o, *dout;
     const float *lse;

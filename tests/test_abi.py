@@ -217,3 +217,40 @@ def test_pruning_fails_closed_on_varlen_and_backward():
     b.prune_threshold = 0.5
     for fn in (lib.attn_bwd, lib.attn_bwd_preprocess, lib.attn_bwd_dkdv, lib.attn_bwd_dq):
         assert fn(ctypes.byref(b), None) == _abi.ATTN_EUNSUPPORTED
+
+
+def _csr_args(**kw):
+    a = _abi.CsrArgs()
+    H, D = kw.get("H", 2), kw.get("D", 64)
+    a.row_ptr = kw.get("row_ptr", FAKE)
+    a.col_idx = kw.get("col", FAKE)
+    a.n_edges = kw.get("n_edges", 100)
+    a.n_dst, a.n_src, a.H, a.D = kw.get("n_dst", 10), kw.get("n_src", 20), H, D
+    a.edge_scores = kw.get("scores", FAKE)
+    for name in ("q", "k", "v", "o"):
+        setattr(a, name, _abi.AttnTensor(kw.get(name, FAKE), H * D, D))
+    a.lse = FAKE
+    a.scale = kw.get("scale", 0.125)
+    a.dtype = kw.get("dtype", _abi.ATTN_BF16)
+    a.o_dtype = kw.get("o_dtype", a.dtype)
+    return a
+
+
+@pytest.mark.parametrize("kw", [
+    {"D": 6}, {"D": 260}, {"D": 0}, {"H": 0}, {"n_dst": -1}, {"n_src": -1}, {"n_edges": -5},
+    {"dtype": 7}, {"o_dtype": _abi.ATTN_F16}, {"row_ptr": None}, {"row_ptr": FAKE + 4},
+    {"col": None}, {"col": FAKE + 2}, {"scores": FAKE + 1}, {"v": None}, {"o": FAKE + 8},
+    {"scores": None, "q": None}, {"scores": None, "k": None},
+    {"scores": None, "scale": float("inf")},
+])
+def test_csr_argument_validation(kw):
+    lib = _abi.load()
+    assert lib.attn_csr_fwd(ctypes.byref(_csr_args(**kw)), None) == _abi.ATTN_EINVAL
+    assert lib.attn_csr_fwd(None, None) == _abi.ATTN_EINVAL
+
+
+def test_csr_without_rows_launches_nothing():
+    lib = _abi.load()
+    before = lib.attn_launch_count()
+    assert lib.attn_csr_fwd(ctypes.byref(_csr_args(n_dst=0)), None) == _abi.ATTN_OK
+    assert lib.attn_launch_count() == before

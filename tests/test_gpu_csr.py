@@ -1,0 +1,110 @@
+"""Attention over a general CSR relation (TIGA-lang attention examples page:
+varlen section's explicit CSR relation, GAT section's softmax over incoming
+edges), CUDA path through the C ABI vs the f64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import attn_inputs
+import online_softmax_attention_gb300 as attn
+import oracle
+from parity_util import check_lse, check_o, f64
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _gpu(x, *, dot, out_dtype=None, scale=None):
+    rp, col, v = x["row_ptr"].to(DEV), x["col"].to(DEV), x["v"].to(DEV)
+    if dot:
+        o, lse = attn.csr_fwd(rp, col, v, q=x["q"].to(DEV), k=x["k"].to(DEV), scale=scale,
+                              out_dtype=out_dtype)
+    else:
+        o, lse = attn.csr_fwd(rp, col, v, scores=x["scores"].to(DEV), out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+def _ref(x, *, dot, scale=None):
+    if dot:
+        return oracle.csr_fwd(x["row_ptr"], x["col"], x["v"], q=x["q"], k=x["k"], scale=scale)
+    return oracle.csr_fwd(x["row_ptr"], x["col"], x["v"], scores=x["scores"])
+
+
+def _check(o, lse, o_ref, lse_ref, dtype, o_dtype):
+    if dtype == torch.float32:
+        # field scores arrive in f32 and are used as given; f32 arithmetic throughout
+        assert float(np.abs(f64(o) - o_ref).max()) <= 1e-5
+    else:
+        check_o(o, o_ref, dtype, o_dtype)
+    check_lse(lse, lse_ref)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "fp16"])
+@pytest.mark.parametrize("D", [8, 64, 128, 200])
+@pytest.mark.parametrize("dot", [False, True])
+def test_radius_graph(dtype, D, dot):
+    """The GAT example's graph family: points in the unit cube, an edge for
+    every pair closer than the cutoff (2000 points, average degree ~9)."""
+    _, rp, col = attn_inputs.radius_graph(2000, 0.1, seed=600 + D)
+    x = attn_inputs.make_csr(row_ptr=rp, col=col, n_src=2000, H=3, D=D, dtype=dtype, seed=601,
+                             field_scores=not dot, score_std=2.0)
+    out = torch.float32 if dtype == "bf16" else None
+    o, lse = _gpu(x, dot=dot, out_dtype=out)
+    assert attn.device_status() == 0
+    o_ref, lse_ref = _ref(x, dot=dot)
+    _check(o, lse, o_ref, lse_ref, attn_inputs.DTYPES[dtype], o.dtype)
+
+
+@pytest.mark.parametrize("causal,lengths_q,lengths_k", [
+    (True, [384, 1, 96, 640, 57], None),   # the varlen example's relation, as CSR
+    (False, [100, 3, 257], [31, 300, 128]),
+    (True, [0, 5, 0, 70], None),
+])
+def test_segment_relations_as_csr_match_dense_attention(causal, lengths_q, lengths_k):
+    """Rows with hundreds of edges (many blocks of 32), empty rows, and the
+    same result as the cu_seqlens forward's oracle."""
+    lk = lengths_k or lengths_q
+    x = attn_inputs.make(dtype="fp16", H=2, D=64, seed=602, lengths=lengths_q, lengths_k=lk)
+    rp, col = attn_inputs.csr_of_segments(lengths_q, lk, causal)
+    o, lse = attn.csr_fwd(rp.to(DEV), col.to(DEV), x["v"].to(DEV), q=x["q"].to(DEV),
+                          k=x["k"].to(DEV))
+    torch.cuda.synchronize()
+    assert attn.device_status() == 0
+    o_ref, lse_ref = oracle.fwd(x["q"], x["k"], x["v"], causal=causal,
+                                cu_seqlens_q=x["cu_seqlens_q"], cu_seqlens_k=x["cu_seqlens_k"])
+    check_o(o, o_ref, torch.float16, o.dtype)
+    check_lse(lse, lse_ref)
+
+
+def test_repeated_edges_empty_rows_and_large_scores():
+    rng = np.random.default_rng(603)
+    deg = rng.integers(0, 80, 300)
+    deg[::7] = 0
+    rp = torch.tensor(np.concatenate([[0], np.cumsum(deg)]), dtype=torch.int64)
+    col = torch.tensor(rng.integers(0, 40, int(deg.sum())), dtype=torch.int32)  # many repeats
+    x = attn_inputs.make_csr(row_ptr=rp, col=col, n_src=40, H=2, D=128, dtype="bf16", seed=604,
+                             field_scores=True, score_std=30.0)
+    o, lse = _gpu(x, dot=False, out_dtype=torch.float32)
+    assert attn.device_status() == 0
+    o_ref, lse_ref = _ref(x, dot=False)
+    _check(o, lse, o_ref, lse_ref, torch.bfloat16, o.dtype)
+    assert not f64(o)[::7].any() and np.isneginf(f64(lse)[:, ::7]).all()
+
+
+def test_malformed_relation_is_reported_and_skipped():
+    """An out-of-range source and a decreasing offset: the kernel skips them
+    (no out-of-bounds read) and reports ATTN_EINVAL; other rows are exact."""
+    rp = torch.tensor([0, 3, 5, 4, 8], dtype=torch.int64)   # row 2 decreases
+    col = torch.tensor([0, 1, 2, 1, 99, 0, 1, 2], dtype=torch.int32)  # 99 out of range
+    x = attn_inputs.make_csr(row_ptr=rp, col=col, n_src=3, H=1, D=64, dtype="f32", seed=605,
+                             field_scores=True)
+    o, lse = _gpu(x, dot=False)
+    assert attn.device_status() == attn._abi.ATTN_EINVAL
+    assert attn.device_status() == 0  # cleared by the read
+    good = oracle.csr_fwd([0, 3], col[:3], x["v"], scores=x["scores"][:3])
+    assert float(np.abs(f64(o)[0] - good[0][0]).max()) <= 1e-5
+    assert not f64(o)[2].any() and np.isneginf(f64(lse)[0, 2])
+    row1 = oracle.csr_fwd([0, 1], col[3:4], x["v"], scores=x["scores"][3:4])  # edge 99 skipped
+    assert float(np.abs(f64(o)[1] - row1[0][0]).max()) <= 1e-5
