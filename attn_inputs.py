@@ -152,41 +152,41 @@ def radius_graph(n: int, cutoff: float, seed: int):
     every pair with |p_i - p_j| < cutoff, i != j.  Returns (positions (n, 3)
     f32, row_ptr (n + 1) int64 over destinations i, col (E) int32 sources j,
     sorted within each row).  Pairs are found through a grid of cells of side
-    >= cutoff (the 27 neighbouring cells of each point's cell)."""
-    import numpy as np
+    >= cutoff (the 27 neighbouring cells of each point's cell); distances are
+    compared in f64."""
     gen = torch.Generator().manual_seed(seed)
     pos = torch.rand((n, 3), generator=gen, dtype=torch.float32)
-    p = pos.double().numpy()
+    p = pos.double()
     cells = max(1, int(1.0 / cutoff))
-    cid = np.minimum((p * cells).astype(np.int64), cells - 1)
+    cid = torch.clamp((p * cells).long(), max=cells - 1)
     key = (cid[:, 0] * cells + cid[:, 1]) * cells + cid[:, 2]
-    order = np.argsort(key, kind="stable")
-    starts = np.searchsorted(key[order], np.arange(cells ** 3), side="left")
-    counts = np.searchsorted(key[order], np.arange(cells ** 3), side="right") - starts
+    skey, order = torch.sort(key, stable=True)
+    grid = torch.arange(cells ** 3)
+    starts = torch.searchsorted(skey, grid, right=False)
+    counts = torch.searchsorted(skey, grid, right=True) - starts
     dst_all, src_all = [], []
     for a in (-1, 0, 1):
         for b in (-1, 0, 1):
             for c in (-1, 0, 1):
-                nc = cid + np.array([a, b, c])
-                ok = ((nc >= 0) & (nc < cells)).all(axis=1)
-                i_idx = np.nonzero(ok)[0]
+                nc = cid + torch.tensor([a, b, c])
+                ok = ((nc >= 0) & (nc < cells)).all(dim=1)
+                i_idx = torch.nonzero(ok).squeeze(1)
                 kk = (nc[i_idx, 0] * cells + nc[i_idx, 1]) * cells + nc[i_idx, 2]
                 cnt = counts[kk]
-                i_rep = np.repeat(i_idx, cnt)
-                first = np.repeat(starts[kk] - np.concatenate([[0], np.cumsum(cnt)[:-1]]), cnt)
-                j = order[first + np.arange(len(i_rep))]
-                d2 = ((p[i_rep] - p[j]) ** 2).sum(axis=1)
+                i_rep = torch.repeat_interleave(i_idx, cnt)
+                base = starts[kk] - (torch.cumsum(cnt, 0) - cnt)
+                j = order[torch.repeat_interleave(base, cnt) + torch.arange(len(i_rep))]
+                d2 = ((p[i_rep] - p[j]) ** 2).sum(dim=1)
                 keep = (d2 < cutoff * cutoff) & (i_rep != j)
                 dst_all.append(i_rep[keep])
                 src_all.append(j[keep])
-    dst = np.concatenate(dst_all)
-    src = np.concatenate(src_all)
-    srt = np.lexsort((src, dst))
+    dst = torch.cat(dst_all)
+    src = torch.cat(src_all)
+    srt = torch.argsort(dst * n + src)
     dst, src = dst[srt], src[srt]
-    row_ptr = torch.tensor(np.concatenate([[0], np.cumsum(np.bincount(dst, minlength=n))]),
-                           dtype=torch.int64)
-    col = torch.tensor(src.astype(np.int32), dtype=torch.int32)
-    return pos, row_ptr, col
+    row_ptr = torch.cat([torch.zeros(1, dtype=torch.int64),
+                         torch.cumsum(torch.bincount(dst, minlength=n), 0)])
+    return pos, row_ptr, src.to(torch.int32)
 
 
 def csr_of_segments(lengths_q, lengths_k, causal: bool):
@@ -223,3 +223,45 @@ def make_csr(*, row_ptr, col, n_src: int, H: int, D: int, dtype: str, seed: int,
         out["q"] = _randn(gen, (n_dst, H, D), tdt)
         out["k"] = _randn(gen, (n_src, H, D), tdt)
     return out
+
+
+@dataclass(frozen=True)
+class CsrWorkload:
+    name: str
+    n: int            # nodes (destination rows = source rows)
+    degree: float     # target average degree of the radius graph
+    H: int
+    D: int
+    dtype: str
+    field_scores: bool
+    seed: int
+    note: str = field(default="", compare=False)
+
+    @property
+    def cutoff(self) -> float:
+        # expected degree of an interior point: n * (4/3) pi r^3
+        return (self.degree / (self.n * 4.0 / 3.0 * 3.141592653589793)) ** (1.0 / 3.0)
+
+
+CSR_WORKLOADS = {
+    # the GAT example's scale: 512 points, cutoff 0.15 (average degree ~6-7), 8 features
+    "csr_gat_n512": CsrWorkload("csr_gat_n512", 512, 0.0, 1, 8, "f32", True, 0,
+                                note="radius graph n=512, cutoff 0.15, field scores, H=1, D=8, f32"),
+    "csr_radius_field_bf16": CsrWorkload(
+        "csr_radius_field_bf16", 1 << 20, 32.0, 4, 64, "bf16", True, 11,
+        note="radius graph n=2^20, average degree ~32, field scores, H=4, D=64, bf16"),
+    "csr_radius_dot_bf16": CsrWorkload(
+        "csr_radius_dot_bf16", 1 << 20, 32.0, 4, 64, "bf16", False, 12,
+        note="radius graph n=2^20, average degree ~32, dot-product scores, H=4, D=64, bf16"),
+}
+
+
+def make_csr_workload(w: CsrWorkload | str) -> dict:
+    """Graph and tensors of one named CSR workload (graph seed = w.seed,
+    tensors seed = w.seed + 1)."""
+    if isinstance(w, str):
+        w = CSR_WORKLOADS[w]
+    cutoff = 0.15 if w.degree == 0.0 else w.cutoff
+    _, row_ptr, col = radius_graph(w.n, cutoff, w.seed)
+    return make_csr(row_ptr=row_ptr, col=col, n_src=w.n, H=w.H, D=w.D, dtype=w.dtype,
+                    seed=w.seed + 1, field_scores=w.field_scores)

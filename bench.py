@@ -16,7 +16,8 @@ Prints one JSON line.  `--impl reference` times the f64 CPU oracle instead,
 on a bounded sample of the same workload.  `--workload <name>` measures the
 forward alone on one of the smaller workloads (causal_fp16_n256,
 full_fp16_n1024, varlen_causal_bf16, cross_f32_8192x2048, and
-pruned_full_bf16_n8192 for `--prune-threshold`) with the same line.
+pruned_full_bf16_n8192 for `--prune-threshold`) with the same line;
+`--workload csr_*` measures attention over a CSR relation (radius graphs).
 """
 from __future__ import annotations
 
@@ -181,6 +182,7 @@ def time_oracle_sample(x, w, max_seconds=20.0):
 
 FWD_WORKLOADS = ("causal_fp16_n256", "full_fp16_n1024", "varlen_causal_bf16", "cross_f32_8192x2048",
                  "pruned_full_bf16_n8192")
+CSR_WORKLOADS = ("csr_gat_n512", "csr_radius_field_bf16", "csr_radius_dot_bf16")
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -345,6 +347,164 @@ def run_forward_workload(args, rank, world):
         dist.destroy_process_group()
 
 
+def time_oracle_csr_rows(x, w, max_seconds=15.0):
+    """Time the oracle's CSR forward on random destination rows of the
+    workload (their edges, scores and the source rows they read), adding rows
+    until about `max_seconds` of CPU work; report edge-head pairs per second."""
+    import numpy as np
+    import torch
+
+    import oracle
+    rp = x["row_ptr"].numpy()
+    col = x["col"].numpy()
+    n_dst = len(rp) - 1
+    rng = np.random.default_rng(0)
+    spent, edges, rows_done, n = 0.0, 0, 0, 256
+    while spent < max_seconds * 0.5:
+        rows = rng.integers(0, n_dst, n)
+        seg = [np.arange(rp[r], rp[r + 1]) for r in rows]
+        eidx = np.concatenate(seg)
+        srcs, remap = np.unique(col[eidx], return_inverse=True)
+        sub_rp = np.concatenate([[0], np.cumsum([len(a) for a in seg])])
+        kw = {}
+        if x["scores"] is not None:
+            kw["scores"] = x["scores"][torch.from_numpy(eidx)]
+        else:
+            kw["q"] = x["q"][torch.from_numpy(rows)]
+            kw["k"] = x["k"][torch.from_numpy(srcs)]
+        v = x["v"][torch.from_numpy(srcs)]
+        t0 = time.perf_counter()
+        oracle.csr_fwd(sub_rp, remap.astype(np.int32), v, **kw)
+        spent += time.perf_counter() - t0
+        edges += len(eidx) * w.H
+        rows_done += n
+        n = min(4 * n, 1 << 16)
+    return {"value": edges / spent / 1e9, "unit": "Gedge/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"{rows_done} random destination rows of the graph (all their edges, "
+                      f"all heads), forward: {spent:.1f} s"}
+
+
+def run_csr_workload(args, rank, world):
+    """Attention over a CSR relation: edge-head pairs per second, with the
+    gathered bytes against the HBM copy bandwidth."""
+    import torch
+    import torch.distributed as dist
+
+    import attn_inputs
+    import online_softmax_attention_gb300 as attn
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    w = attn_inputs.CSR_WORKLOADS[args.workload]
+    x = attn_inputs.make_csr_workload(w)
+    rp, col, v = x["row_ptr"].to(dev), x["col"].to(dev), x["v"].to(dev)
+    n, E = len(x["row_ptr"]) - 1, x["col"].numel()
+    kw = {"scores": x["scores"].to(dev)} if w.field_scores else \
+        {"q": x["q"].to(dev), "k": x["k"].to(dev)}
+    call = attn.CsrCall(rp, col, v, **kw)
+    es = v.element_size()
+    # bytes of one launch as the algorithm touches them: the relation, the
+    # scores, one row of V (and of K) per edge and head, Q, O and lse
+    gathered = 8 * (n + 1) + 4 * E + E * w.H * w.D * es + n * w.H * w.D * es + 4 * n * w.H
+    gathered += 4 * E * w.H if w.field_scores else (E * w.H * w.D * es + n * w.H * w.D * es)
+    compulsory = 8 * (n + 1) + 4 * E + v.numel() * es + n * w.H * w.D * es + 4 * n * w.H
+    compulsory += 4 * E * w.H if w.field_scores else 2 * v.numel() * es
+    in_bytes = sum(t.numel() * t.element_size() for t in [rp, col, v] + list(kw.values()))
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if in_bytes < L2_BYTES else None
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        call.run(stream)
+    torch.cuda.synchronize()
+    if attn.device_status() != 0:
+        raise RuntimeError("device status set during warm-up")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    n0 = attn.launch_count()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for e0, e1 in evs:
+            if flush is not None:
+                flush.zero_()
+            e0.record(stream)
+            call.run(stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    launches = attn.launch_count() - n0
+    ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in evs), dev)
+
+    # end to end: the relation, scores / q, k and v in from pinned host memory, o and lse out
+    host = {"row_ptr": x["row_ptr"], "col": x["col"], "v": x["v"]}
+    devt = {"row_ptr": rp, "col": col, "v": v}
+    for name, t in kw.items():
+        host[name] = x[name]
+        devt[name] = t
+    pin = {k_: t.contiguous().pin_memory() for k_, t in host.items()}
+    o_h = torch.empty(call.o.shape, dtype=call.o.dtype).pin_memory()
+    l_h = torch.empty(call.lse.shape, dtype=torch.float32).pin_memory()
+
+    def e2e():
+        for k_, t in pin.items():
+            devt[k_].copy_(t, non_blocking=True)
+        call.run(stream)
+        o_h.copy_(call.o, non_blocking=True)
+        l_h.copy_(call.lse, non_blocking=True)
+
+    e2e()
+    torch.cuda.synchronize()
+    e_steps = max(2, min(args.steps, 10))
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(e_steps):
+        e2e()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(t0.elapsed_time(t1) / e_steps, dev)
+    if attn.device_status() != 0:
+        raise RuntimeError("device status set in the timed region")
+
+    peaks = load_peaks()
+    rate = E * w.H * world / (ms * 1e-3) / 1e9
+    achieved = gathered / (ms * 1e-3) / 1e9
+    line = {
+        "metric": f"attention over a CSR relation, Gedge/s ({w.note})", "value": rate,
+        "unit": "Gedge/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": {"fp16": "f16", "bf16": "bf16", "f32": "f32"}[w.dtype], "data": "synthetic",
+        "config": {"workload": w.name, "nodes": n, "edges": E, "avg_degree": E / max(1, n),
+                   "heads": w.H, "head_dim": w.D,
+                   "scores": "field" if w.field_scores else "dot-product",
+                   "bytes_gathered_per_launch": gathered, "bytes_compulsory_per_launch": compulsory,
+                   "l2": "flushed before every launch (inputs fit in L2)" if flush is not None
+                   else "no flush: inputs larger than L2",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": "csr_fwd",
+                     "peak_source": f"HBM copy ({peaks['source']})",
+                     "bytes": "gathered: one V (and K) row per edge and head"},
+        "e2e": {"value": E * w.H * world / (e2e_ms * 1e-3) / 1e9, "unit": "Gedge/s",
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in pin.values()),
+                "d2h_bytes_per_step": o_h.numel() * o_h.element_size() + l_h.numel() * 4,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "cpu_baseline": None,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = time_oracle_csr_rows(x, w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def run_reference(args, rank, world):
     """Reference arm: the f64 CPU oracle on the host cores, bounded samples."""
     if rank != 0:
@@ -383,8 +543,9 @@ def main():
     ap.add_argument("--batch", type=int, default=4,
                     help="sequences of N=8192 (4 = the benchmark workload; fewer for profiling)")
     ap.add_argument("--skip-e2e", action="store_true", help="profiling runs: no host-buffer leg")
-    ap.add_argument("--workload", default=WORKLOAD, choices=(WORKLOAD,) + FWD_WORKLOADS,
-                    help="the training workload (default), or a forward-only workload")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    choices=(WORKLOAD,) + FWD_WORKLOADS + CSR_WORKLOADS,
+                    help="the training workload (default), a forward-only workload, or a CSR one")
     ap.add_argument("--num-splits", type=int, default=0,
                     help="forward-only workloads: key splits (0 = library's choice)")
     ap.add_argument("--prune-threshold", type=float, default=0.0,
@@ -398,6 +559,9 @@ def main():
 
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.workload in CSR_WORKLOADS:
+        run_csr_workload(args, rank, world)
         return
     if args.workload != WORKLOAD:
         run_forward_workload(args, rank, world)
