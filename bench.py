@@ -98,8 +98,9 @@ def recorded_traffic(kernel_key, src_hash):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms; the summary
+    keeps the samples taken between start() and stop() (the timed region)."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -107,26 +108,46 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.file = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.file, stderr=subprocess.DEVNULL)
+            # wait (up to 3 s) for the first sample so that the region is covered
+            deadline = time.time() + 3.0
+            while time.time() < deadline and os.path.getsize(self.file.name) == 0:
+                time.sleep(0.02)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
 
+    def start(self):
+        self.t0 = time.time()
+
+    def stop(self):
+        self.t1 = time.time()
+
     def __exit__(self, *exc):
         if self.proc:
+            time.sleep(0.06)  # one more sample after the region
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
         return False
+
+    @staticmethod
+    def _when(stamp):
+        import datetime
+        try:
+            return datetime.datetime.strptime(stamp.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
 
     def summary(self):
         if not self.proc or not self.file:
@@ -135,23 +156,26 @@ class ClockSampler:
         with open(self.file.name) as f:
             rows = [r.strip().split(", ") for r in f if r.strip()]
         os.unlink(self.file.name)
-        sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        parsed = []
         for r in rows:
-            if len(r) < 9:
+            if len(r) < 10:
                 continue
             try:
-                sm.append(float(r[1]))
-                mx = float(r[2])
+                parsed.append((self._when(r[0]), float(r[2]), float(r[3]), r[6:10]))
             except ValueError:
                 continue
-            for n, val in zip(names, r[5:9]):
-                if val.strip().lower() == "active":
-                    reasons.add(n)
-        if not sm:
+        inside = parsed
+        if self.t0 is not None and self.t1 is not None:
+            # the region plus one sampling period on each side
+            inside = [x for x in parsed if x[0] is not None and self.t0 - 0.05 <= x[0] <= self.t1 + 0.05]
+            if not inside:
+                inside = parsed
+        if not inside:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        reasons = {n for x in inside for n, val in zip(names, x[3]) if val.strip().lower() == "active"}
+        return {"sm_mhz": statistics.median(x[1] for x in inside), "sm_max_mhz": inside[-1][2],
+                "reasons": sorted(reasons), "samples": len(inside)}
 
 
 def time_oracle_sample(x, w, max_seconds=20.0):
@@ -257,6 +281,7 @@ def run_forward_workload(args, rank, world):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        clk.start()
         for e0, e1 in evs:
             if flush is not None:
                 flush.zero_()
@@ -264,6 +289,7 @@ def run_forward_workload(args, rank, world):
             call.run(stream)
             e1.record(stream)
         torch.cuda.synchronize()
+        clk.stop()
     if world > 1:
         dist.barrier()
     launches = attn.launch_count() - n0
@@ -428,6 +454,7 @@ def run_csr_workload(args, rank, world):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        clk.start()
         for e0, e1 in evs:
             if flush is not None:
                 flush.zero_()
@@ -435,6 +462,7 @@ def run_csr_workload(args, rank, world):
             call.run(stream)
             e1.record(stream)
         torch.cuda.synchronize()
+        clk.stop()
     if world > 1:
         dist.barrier()
     launches = attn.launch_count() - n0
@@ -535,7 +563,7 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc"])
@@ -548,6 +576,9 @@ def main():
                     help="the training workload (default), a forward-only workload, or a CSR one")
     ap.add_argument("--num-splits", type=int, default=0,
                     help="forward-only workloads: key splits (0 = library's choice)")
+    ap.add_argument("--dq-mode", default="auto", choices=["auto", "fused", "separate"],
+                    help="training workload: backward dq accumulated in the dK/dV kernel (fused) "
+                         "or by its own deterministic kernel (separate); auto = separate")
     ap.add_argument("--prune-threshold", type=float, default=0.0,
                     help="forward-only workloads, full relation: tile pruning rho (0 = exact)")
     args = ap.parse_args()
@@ -597,7 +628,8 @@ def main():
     fcall = attn.FwdCall(q, k, v, causal=True, cu_seqlens_q=cu, out_dtype=torch.float32,
                          kernel=args.kernel)
     bcall = attn.BwdCall(q, k, v, fcall.o, fcall.lse, dO, causal=True, cu_seqlens_q=cu,
-                         kernel=args.kernel)
+                         kernel=args.kernel, dq_mode=args.dq_mode)
+    dq_mode = bcall.selected_dq_mode()
     stream = torch.cuda.current_stream()
     stages = ["fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq"]
 
@@ -630,11 +662,13 @@ def main():
     with ClockSampler(local) as clk:
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
+        clk.start()
         start.record(stream)
         for i in range(args.steps):
             step(evs[i])
         end.record(stream)
         torch.cuda.synchronize()
+        clk.stop()
     barrier()
     launches = attn.launch_count() - n0
     ms = start.elapsed_time(end) / args.steps
@@ -683,10 +717,15 @@ def main():
 
     peaks = load_peaks()
     # algorithmic FLOPs per launch of each stage: fwd = S and PV contractions;
-    # dkdv = S (recompute), dP, dV, dK; dq = dQ only (its S / dP recomputes are
-    # not algorithmic work); preprocess is HBM-bound (reads O f32 and dO bf16).
-    stage_flops = {"fwd": fwd_flops, "bwd_dkdv": 2.0 * fwd_flops, "bwd_dq": 0.5 * fwd_flops}
-    dominant = max(("fwd", "bwd_dkdv", "bwd_dq"), key=lambda s: stage_ms[s])
+    # separate dq: dkdv = S (recompute), dP, dV, dK and dq = dQ only (its S / dP
+    # recomputes are not algorithmic work); fused dq: dkdv = all five and the dq
+    # stage is an HBM-bound conversion of the partial sums, as is the
+    # preprocess (reads O f32 and dO bf16).
+    if dq_mode == "fused":
+        stage_flops = {"fwd": fwd_flops, "bwd_dkdv": 2.5 * fwd_flops}
+    else:
+        stage_flops = {"fwd": fwd_flops, "bwd_dkdv": 2.0 * fwd_flops, "bwd_dq": 0.5 * fwd_flops}
+    dominant = max(stage_flops, key=lambda s: stage_ms[s])
     family = {"fwd": fcall.selected_kernel(), "bwd_dkdv": bcall.selected_kernel(),
               "bwd_dq": bcall.selected_kernel()}
     csrc = "online_softmax_attention_gb300/csrc/"
@@ -710,7 +749,8 @@ def main():
         bound, punit = "alu", "TFLOP/s"
         peak_note = f"FP32 FFMA: {sms} SMs x 128 lanes x 2 FLOP x {peaks['sm_max_mhz']:.0f} MHz"
     src = [p for p in kernel_files[(dominant, family[dominant])] if os.path.exists(os.path.join(ROOT, p))]
-    traffic = recorded_traffic(dominant, source_hash(src)) if src else None
+    tkey = dominant + ("_fused" if dominant == "bwd_dkdv" and dq_mode == "fused" else "")
+    traffic = recorded_traffic(tkey, source_hash(src)) if src else None
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": punit,
                 "frac": achieved / peak, "traffic": traffic, "kernel": dominant,
                 "peak_source": peak_note}
@@ -725,7 +765,7 @@ def main():
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD if w.batch == 4 else f"{WORKLOAD} (batch {w.batch})", "batch": w.batch, "seq_len": 8192, "heads": 32, "head_dim": 128,
                    "relation": "causal", "o_dtype": "f32", "grad_dtype": "bf16",
-                   "kernels": family,
+                   "kernels": family, "dq_mode": dq_mode,
                    "l2": "no flush: each input tensor is 268 MB, larger than the 129 MB L2",
                    "parallelism": f"replicas x{world}"},
         "breakdown": {"fwd_ms": stage_ms["fwd"], "bwd_ms": bwd_ms,

@@ -27,9 +27,11 @@
  *
  * Backward (same page, third bullet): Dr_i = sum_d dO_id * O_id per row;
  * per pair recompute p and dp = <dO_i, v_j>; ds = p * (dp - Dr_i);
- * dq = scale * ds . k, dk = scale * ds^T . q, dv = p^T . dO.  Each output is
- * written by exactly one kernel that owns it (no atomics), so results are
- * run-to-run deterministic.
+ * dq = scale * ds . k, dk = scale * ds^T . q, dv = p^T . dO.  In the page's
+ * layout each gradient has a nest of its own that owns what it writes
+ * (ATTN_DQ_SEPARATE: no atomics, run-to-run deterministic); ATTN_DQ_FUSED
+ * instead folds the dq nest into the dk/dv nest with f32 reductions (see
+ * attn_dq_mode).
  *
  * Conventions for every entry point:
  *  - Every tensor pointer is a DEVICE pointer on the current CUDA device,
@@ -62,7 +64,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 2
+#define ATTN_ABI_VERSION 3
 
 #if defined(__GNUC__)
 #define ATTN_API __attribute__((visibility("default")))
@@ -87,6 +89,21 @@ typedef enum attn_relation { ATTN_FULL = 0, ATTN_CAUSAL = 1 } attn_relation;
  * the FP32 SIMT kernels for f32.  SIMT forces the CUDA-core kernels (any
  * dtype); TC forces the tensor-core kernels (f16/bf16 only). */
 typedef enum attn_kernel { ATTN_KERNEL_AUTO = 0, ATTN_KERNEL_SIMT = 1, ATTN_KERNEL_TC = 2 } attn_kernel;
+
+/* How the backward computes dq.
+ * SEPARATE: dk/dv by one kernel (per key block, loop over query blocks) and
+ *   dq by another (per query block, loop over key blocks), each writing its
+ *   gradient once: deterministic, but the dq kernel recomputes the scores and
+ *   dp of every pair (7 contractions per pair in all).
+ * FUSED: the dk/dv kernel also forms dq's per-pair contribution ds . k
+ *   (5 contractions per pair) and adds it with f32 reductions to partial sums
+ *   in the workspace; the dq stage scales and converts the sums.  The order of
+ *   the additions varies from run to run, so dq may differ in the last bits
+ *   between runs.  Tensor-core kernels only (ATTN_EUNSUPPORTED with SIMT).
+ * AUTO: SEPARATE (on the causal training shapes the fused kernel's f32
+ *   reduction traffic, 64 KiB per pair of 128-row tiles, costs more than the
+ *   recomputation it saves). */
+typedef enum attn_dq_mode { ATTN_DQ_AUTO = 0, ATTN_DQ_SEPARATE = 1, ATTN_DQ_FUSED = 2 } attn_dq_mode;
 
 /* A (tokens, heads, D) tensor view: element strides of the token and head axes. */
 typedef struct attn_tensor {
@@ -158,6 +175,7 @@ typedef struct attn_bwd_args {
     int32_t num_ctas;
     float prune_threshold; /* must be 0: the backward of a tile-pruned forward is not
                               defined, and a non-zero value returns ATTN_EUNSUPPORTED */
+    int32_t dq_mode;      /* attn_dq_mode */
 } attn_bwd_args;
 
 /* Partial attention results over disjoint key sets, to be merged
@@ -213,7 +231,8 @@ ATTN_API size_t attn_csr_args_size(void);
 
 /* Bytes of device workspace the call needs (depends on n_seq, H, n_q, and
  * for the forward on the number of key splits: n_splits > 1 adds the partial
- * results, n_splits * n_q * H * (D + 1) * 4 bytes). */
+ * results, n_splits * n_q * H * (D + 1) * 4 bytes; for the backward on the dq
+ * mode: ATTN_DQ_FUSED adds the dq partial sums, n_q * H * D * 4 bytes). */
 ATTN_API size_t attn_fwd_workspace_bytes(const attn_fwd_args *a);
 ATTN_API size_t attn_bwd_workspace_bytes(const attn_bwd_args *a);
 
@@ -249,9 +268,12 @@ ATTN_API int attn_merge(const attn_merge_args *a, void *stream);
 ATTN_API int attn_bwd(const attn_bwd_args *a, void *stream);
 
 /* The three stages of attn_bwd, callable one by one (e.g. to time each):
- *  preprocess: Dr = rowsum(dO * O) into the workspace, and the schedules;
- *  dkdv:       per key block, loop over query blocks, write dk and dv;
- *  dq:         per query block, loop over key blocks, write dq.
+ *  preprocess: Dr = rowsum(dO * O) into the workspace, and the schedules
+ *              (FUSED: also zeroes the dq partial sums);
+ *  dkdv:       per key block, loop over query blocks, write dk and dv
+ *              (FUSED: also add each pair's dq contribution to the sums);
+ *  dq:         SEPARATE: per query block, loop over key blocks, write dq;
+ *              FUSED: dq = scale * partial sums, converted to grad_dtype.
  * dkdv and dq read what preprocess wrote into the same workspace. */
 ATTN_API int attn_bwd_preprocess(const attn_bwd_args *a, void *stream);
 ATTN_API int attn_bwd_dkdv(const attn_bwd_args *a, void *stream);
@@ -270,6 +292,10 @@ ATTN_API int attn_fwd_simple(const void *q, const void *k, const void *v, void *
  * would be rejected.  Host-only; launches nothing. */
 ATTN_API int attn_fwd_selected_kernel(const attn_fwd_args *a);
 ATTN_API int attn_bwd_selected_kernel(const attn_bwd_args *a);
+
+/* The dq mode a backward with these arguments runs (ATTN_DQ_SEPARATE or
+ * ATTN_DQ_FUSED, resolving AUTO), or a negative attn_status.  Host-only. */
+ATTN_API int attn_bwd_selected_dq_mode(const attn_bwd_args *a);
 
 /* Attention over the CSR relation of `a` (see attn_csr_args). */
 ATTN_API int attn_csr_fwd(const attn_csr_args *a, void *stream);

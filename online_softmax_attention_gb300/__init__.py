@@ -34,6 +34,9 @@ __all__ = ["fwd", "bwd", "merge", "csr_fwd", "FwdCall", "BwdCall", "MergeCall", 
 
 _DT = {torch.float16: ATTN_F16, torch.bfloat16: ATTN_BF16, torch.float32: ATTN_F32}
 _KERNELS = {"auto": ATTN_KERNEL_AUTO, "simt": ATTN_KERNEL_SIMT, "tc": ATTN_KERNEL_TC}
+# backward dq: "separate" (own kernel, deterministic), "fused" (dK/dV kernel adds
+# f32 partial sums; tensor-core kernels only), "auto" (= separate)
+_DQ_MODES = {"auto": _abi.ATTN_DQ_AUTO, "separate": _abi.ATTN_DQ_SEPARATE, "fused": _abi.ATTN_DQ_FUSED}
 
 
 def library_path() -> str:
@@ -201,7 +204,8 @@ class BwdCall:
     def __init__(self, q, k, v, o, lse, dout, *, causal: bool = False, scale: float | None = None,
                  cu_seqlens_q=None, cu_seqlens_k=None, grad_dtype: torch.dtype | None = None,
                  kernel: str = "auto", num_ctas: int = 0, dq=None, dk=None, dv=None,
-                 workspace: torch.Tensor | None = None, prune_threshold: float = 0.0):
+                 workspace: torch.Tensor | None = None, prune_threshold: float = 0.0,
+                 dq_mode: str = "auto"):
         dev = q.device
         Tq, H, D = q.shape
         Tk = k.shape[0]
@@ -228,6 +232,7 @@ class BwdCall:
         a.kernel = _KERNELS[kernel]
         a.num_ctas = int(num_ctas)
         a.prune_threshold = float(prune_threshold)  # non-zero: the library refuses (fails closed)
+        a.dq_mode = _DQ_MODES[dq_mode]
         lib = _abi.load()
         need = lib.attn_bwd_workspace_bytes(ctypes.byref(a))
         self.workspace = workspace if workspace is not None else _workspace(need, dev)
@@ -257,6 +262,13 @@ class BwdCall:
         """"tc" or "simt": the kernel family these arguments run."""
         return _selected(self._lib.attn_bwd_selected_kernel(ctypes.byref(self.args)),
                          "attn_bwd_selected_kernel")
+
+    def selected_dq_mode(self) -> str:
+        """"fused" or "separate": how these arguments compute dq."""
+        code = self._lib.attn_bwd_selected_dq_mode(ctypes.byref(self.args))
+        if code < 0:
+            check(code, "attn_bwd_selected_dq_mode")
+        return "fused" if code == _abi.ATTN_DQ_FUSED else "separate"
 
 
 class CsrCall:
@@ -340,8 +352,8 @@ def merge(o_parts, lse_parts, *, out_dtype: torch.dtype = torch.float32):
 
 def bwd(q, k, v, o, lse, dout, *, causal: bool = False, scale: float | None = None,
         cu_seqlens_q=None, cu_seqlens_k=None, grad_dtype: torch.dtype | None = None,
-        kernel: str = "auto", num_ctas: int = 0):
+        kernel: str = "auto", num_ctas: int = 0, dq_mode: str = "auto"):
     """Attention backward from the forward's o and lse.  Returns ``(dq, dk, dv)``."""
     return BwdCall(q, k, v, o, lse, dout, causal=causal, scale=scale, cu_seqlens_q=cu_seqlens_q,
                    cu_seqlens_k=cu_seqlens_k, grad_dtype=grad_dtype, kernel=kernel,
-                   num_ctas=num_ctas).run()
+                   num_ctas=num_ctas, dq_mode=dq_mode).run()

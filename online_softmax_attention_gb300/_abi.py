@@ -12,12 +12,13 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_lib", "libattn_gb300.so")
 
-ABI_VERSION = 2
+ABI_VERSION = 3
 
 ATTN_OK, ATTN_EINVAL, ATTN_EUNSUPPORTED, ATTN_ECUDA, ATTN_ETIMEOUT, ATTN_EWORKSPACE = 0, -1, -2, -3, -4, -5
 ATTN_F16, ATTN_BF16, ATTN_F32 = 0, 1, 2
 ATTN_FULL, ATTN_CAUSAL = 0, 1
 ATTN_KERNEL_AUTO, ATTN_KERNEL_SIMT, ATTN_KERNEL_TC = 0, 1, 2
+ATTN_DQ_AUTO, ATTN_DQ_SEPARATE, ATTN_DQ_FUSED = 0, 1, 2
 ATTN_NOALLOC_MAX_SEQ = 16367
 ATTN_MAX_SPLITS = 64
 
@@ -30,6 +31,7 @@ EXPORTS = (
     "attn_fwd_selected_kernel", "attn_bwd_selected_kernel", "attn_fwd_noalloc",
     "attn_selftest_exp2", "attn_set_watchdog_cycles", "attn_merge_args_size",
     "attn_fwd_num_splits", "attn_merge", "attn_csr_args_size", "attn_csr_fwd",
+    "attn_bwd_selected_dq_mode",
 )
 
 
@@ -82,7 +84,7 @@ class BwdArgs(ctypes.Structure):
         ("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_k", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("kernel", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
-        ("prune_threshold", ctypes.c_float),
+        ("prune_threshold", ctypes.c_float), ("dq_mode", ctypes.c_int32),
     ]
 
 
@@ -127,6 +129,7 @@ def load() -> ctypes.CDLL:
         "attn_selftest_exp2": (ctypes.c_int, [vp, vp, i32, vp]),
         "attn_set_watchdog_cycles": (ctypes.c_longlong, [ctypes.c_longlong]),
         "attn_bwd_selected_kernel": (ctypes.c_int, [ba]),
+        "attn_bwd_selected_dq_mode": (ctypes.c_int, [ba]),
         "attn_launch_count": (ctypes.c_uint64, []),
         "attn_strerror": (ctypes.c_char_p, [ctypes.c_int]),
         "attn_last_error_string": (ctypes.c_char_p, []),

@@ -248,18 +248,36 @@ void split_params(const attn_fwd_args *a, const FwdParams &p, FwdParams &part, M
 // ---- backward --------------------------------------------------------------
 
 struct BwdLayout {
-    size_t kv, q, dr, lse2, total;
+    size_t kv, q, dr, lse2, dqa, total;
 };
 
-BwdLayout bwd_layout(int n_seq, int H, int n_q) {
+// fused: room for the dq partial sums (n_q * H * D f32) after the row statistics
+BwdLayout bwd_layout(int n_seq, int H, int n_q, int D, bool fused) {
     BwdLayout L;
     const size_t rows = align256(sizeof(float) * (size_t)H * (size_t)(n_q > 0 ? n_q : 1));
     L.kv = 0;
     L.q = sched_bytes(n_seq);
     L.dr = L.q + sched_bytes(n_seq);
     L.lse2 = L.dr + rows;
-    L.total = L.lse2 + rows;
+    L.dqa = L.lse2 + rows;
+    L.total = L.dqa + (fused ? align256(sizeof(float) * (size_t)H * (size_t)(n_q > 0 ? n_q : 0) * (size_t)D) : 0);
     return L;
+}
+
+// Whether a backward with these arguments accumulates dq inside the dK/dV
+// kernel: the caller asked for it and the tensor-core kernels run (AUTO
+// resolves to the separate dq kernel).
+bool bwd_fused(const attn_bwd_args *a) {
+    if (a->dq_mode != ATTN_DQ_FUSED) return false;
+    BwdParams t;
+    std::memset(&t, 0, sizeof(t));
+    t.dtype = a->dtype;
+    t.D = a->D;
+    t.n_q = a->n_q;
+    t.n_k = a->n_k;
+    bool use_tc = false;
+    if (choose_tc(a->kernel, tc_bwd_supported(t), use_tc) != ATTN_OK) return false;
+    return use_tc;
 }
 
 int build_bwd(const attn_bwd_args *a, BwdParams &p, bool &use_tc) {
@@ -270,6 +288,8 @@ int build_bwd(const attn_bwd_args *a, BwdParams &p, bool &use_tc) {
     if (a->o_dtype != a->dtype && a->o_dtype != ATTN_F32) return ATTN_EINVAL;
     if (a->grad_dtype != a->dtype && a->grad_dtype != ATTN_F32) return ATTN_EINVAL;
     if (a->prune_threshold != 0.f) return ATTN_EUNSUPPORTED;  // fails closed
+    if (a->dq_mode != ATTN_DQ_AUTO && a->dq_mode != ATTN_DQ_SEPARATE && a->dq_mode != ATTN_DQ_FUSED)
+        return ATTN_EINVAL;
     const bool any_q = a->n_q > 0, any_k = a->n_k > 0;
     if (!valid_view(a->q, a->dtype, any_q) || !valid_view(a->o, a->o_dtype, any_q) ||
         !valid_view(a->dout, a->dtype, any_q) || !valid_view(a->dq, a->grad_dtype, any_q) ||
@@ -298,16 +318,21 @@ int build_bwd(const attn_bwd_args *a, BwdParams &p, bool &use_tc) {
     p.dtype = a->dtype; p.o_dtype = a->o_dtype; p.grad_dtype = a->grad_dtype;
     p.n_seq = a->n_seq;
     p.cu_q = a->cu_seqlens_q; p.cu_k = a->cu_seqlens_k;
-    const BwdLayout L = bwd_layout(a->n_seq, a->H, a->n_q);
+    const bool fused = bwd_fused(a);
+    const BwdLayout L = bwd_layout(a->n_seq, a->H, a->n_q, a->D, fused);
     char *ws = static_cast<char *>(a->workspace);
     p.sched_kv = sched_at(ws + L.kv);
     p.sched_q = sched_at(ws + L.q);
     p.dr = reinterpret_cast<float *>(ws + L.dr);
     p.lse2 = reinterpret_cast<float *>(ws + L.lse2);
+    p.dq_accum = fused ? reinterpret_cast<float *>(ws + L.dqa) : nullptr;
     p.status = status_ptr();
     p.watchdog_cycles = watchdog_cycles();
     if (!p.status) return ATTN_ECUDA;
-    return choose_tc(a->kernel, tc_bwd_supported(p), use_tc);
+    rc = choose_tc(a->kernel, tc_bwd_supported(p), use_tc);
+    if (rc) return rc;
+    if (a->dq_mode == ATTN_DQ_FUSED && !use_tc) return ATTN_EUNSUPPORTED;
+    return ATTN_OK;
 }
 
 }  // namespace
@@ -348,8 +373,8 @@ size_t attn_fwd_workspace_bytes(const attn_fwd_args *a) {
 size_t attn_merge_args_size(void) { return sizeof(attn_merge_args); }
 
 size_t attn_bwd_workspace_bytes(const attn_bwd_args *a) {
-    if (!a || a->n_seq < 1 || a->H < 1 || a->n_q < 0) return 0;
-    return bwd_layout(a->n_seq, a->H, a->n_q).total;
+    if (!a || a->n_seq < 1 || a->H < 1 || a->n_q < 0 || a->D < 0) return 0;
+    return bwd_layout(a->n_seq, a->H, a->n_q, a->D, bwd_fused(a)).total;
 }
 
 int attn_fwd(const attn_fwd_args *a, void *stream) {
@@ -422,10 +447,11 @@ int attn_bwd_preprocess(const attn_bwd_args *a, void *stream) {
     const int q_block = use_tc ? tc_bwd_q_block(p) : kSimtBlock;
     cudaError_t e = launch_prep(p.cu_q, p.cu_k, p.n_seq, p.n_q, p.n_k, p.H, kv_block, p.causal, 1,
                                 1, p.sched_kv, p.status, s);
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && !p.dq_accum)  // the fused dq needs no query-block schedule
         e = launch_prep(p.cu_q, p.cu_k, p.n_seq, p.n_q, p.n_k, p.H, q_block, p.causal, 0,
                         1, p.sched_q, p.status, s);
     if (e == cudaSuccess) e = launch_bwd_preprocess(p, s);
+    if (e == cudaSuccess && p.dq_accum) e = launch_dq_accum_zero(p, s);
     if (e != cudaSuccess) return set_cuda_error(e);
     return ATTN_OK;
 }
@@ -450,7 +476,9 @@ int attn_bwd_dq(const attn_bwd_args *a, void *stream) {
     if (rc) return rc;
     if (a->n_q == 0) return ATTN_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = use_tc ? launch_bwd_dq_tc(p, a->num_ctas, s) : launch_bwd_dq_simt(p, a->num_ctas, s);
+    cudaError_t e = p.dq_accum ? launch_dq_accum_convert(p, s)
+                    : use_tc   ? launch_bwd_dq_tc(p, a->num_ctas, s)
+                               : launch_bwd_dq_simt(p, a->num_ctas, s);
     if (e != cudaSuccess) return set_cuda_error(e);
     return ATTN_OK;
 }
@@ -501,6 +529,13 @@ int attn_bwd_selected_kernel(const attn_bwd_args *a) {
     bool use_tc = false;
     const int rc = build_bwd(a, p, use_tc);
     return rc ? rc : (use_tc ? ATTN_KERNEL_TC : ATTN_KERNEL_SIMT);
+}
+
+int attn_bwd_selected_dq_mode(const attn_bwd_args *a) {
+    BwdParams p;
+    bool use_tc = false;
+    const int rc = build_bwd(a, p, use_tc);
+    return rc ? rc : (p.dq_accum ? ATTN_DQ_FUSED : ATTN_DQ_SEPARATE);
 }
 
 long long attn_set_watchdog_cycles(long long cycles) {

@@ -54,13 +54,26 @@ struct BCfg {
     // the K ring is deeper; both prefetch far enough ahead to hide L2 latency
     static constexpr int kDqKStages = D == 128 ? 3 : 5;
     static constexpr int kDqVStages = D == 128 ? 2 : 3;
-    static constexpr int kDkdvSmem = (2 + kDkdvQStages + kDkdvDoStages) * kTileBytes + 1024;
+    // fused dQ: the 16-bit dS tile (128 keys x 128 query rows, 32 KiB) for the
+    // dQ contraction lives in the dO ring slot of its block at D = 128 (same
+    // size; dO is dead once dP^T is done) and in a buffer of its own at D = 64
+    static constexpr int kDsBytes = BT * BT * 2;
+    static constexpr bool kDsInDoSlot = kTileBytes == kDsBytes;
+    static constexpr int kDkdvSmem =
+        (2 + kDkdvQStages + kDkdvDoStages) * kTileBytes + (kDsInDoSlot ? 0 : kDsBytes) + 1024;
+    // fused dQ accumulator columns: at D = 128 TMEM is full (S^T, dP^T, dV, dK),
+    // so dQ of a block reuses the dP^T columns once its dS^T has been consumed
+    static constexpr uint32_t kDqCol = D == 128 ? BT : 256 + 2 * D;
     static constexpr int kDqSmem = (2 + kDqKStages + kDqVStages) * kTileBytes + 1024;
     // dynamic + static (barriers, stats) shared memory within the 227 KiB per block
     static_assert(kDkdvSmem + 3 * 1024 <= 232448 && kDqSmem + 1024 <= 232448, "shared memory budget");
     static constexpr int kRegsProducer = 88;
     static constexpr int kRegsEw = 208;
     static_assert(128 * kRegsProducer + 256 * kRegsEw <= kThreads * 168, "register split");
+    // fused dQ: the MMA issuer keeps more descriptors and counters live
+    static constexpr int kRegsProducerFused = 112;
+    static constexpr int kRegsEwFused = 184;
+    static_assert(128 * kRegsProducerFused + 256 * kRegsEwFused <= kThreads * 168, "register split");
 };
 
 struct TcBwdArgs {
@@ -163,6 +176,8 @@ struct __align__(8) DkdvBars {
     uint64_t st_full, dp_full, p_ready, ds_ready, acc_done, acc_free;
     uint64_t stats_ready[2];  // all elementwise threads staged a query block's lse2 / Dr
     uint64_t mma_drain;       // abort path: completion of the MMAs already issued
+    uint64_t dq_full, dq_free; // fused dQ: a block's dQ partial is in TMEM / has been read out
+    uint64_t dv_done;          // fused dQ: dV of a block has read its dO tile (the slot may take dS)
     SchedRing sched;
 };
 
@@ -338,6 +353,132 @@ __device__ void dkdv_mma(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, uint32
     }
 }
 
+// Fused-dQ variant of the issuer: per query block also dQ_qb = dS K, from the
+// dS tile the elementwise warps wrote into shared memory (A operand, M-major:
+// rows = keys, query rows contiguous) and the resident K tile (B, N-major).
+// Issue order S_0, dP_0, then per block dV_qb, dP_qb (qb > 0), S_{qb+1}, dK_qb,
+// dQ_qb: the score MMA of the next block covers the elementwise dS work, and
+// dV of the next block covers the read-out of dQ_qb.
+template <int D, bool kBF16>
+__device__ void dkdvq_mma(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, uint32_t sV, uint32_t sQ,
+                          uint32_t sDO, uint32_t sDS, uint32_t tmem, const Watchdog &wd) {
+    using C = BCfg<D>;
+    const BwdParams &p = a.p;
+    const int total = p.sched_kv.hdr[1];
+    constexpr uint32_t idSS = idesc_f16(kBF16, BT, BT, 0);
+    const uint32_t idST = idSS | (p.scale_log2 < 0.f ? (1u << 13) : 0u);
+    constexpr uint32_t idTS = idesc_f16(kBF16, BT, D, 1);
+    constexpr uint32_t idDQ = idesc_f16(kBF16, BT, D, 1) | (1u << 15);  // A (dS) M-major
+    constexpr bool kAlias = C::kDqCol == (uint32_t)BT;  // dQ shares the dP^T columns
+    uint32_t kv_cnt = 0, p_cnt = 0, ds_cnt = 0, af_cnt = 0, dqf_cnt = 0, dq_issued = 0;
+    RingPos<C::kDkdvQStages> qr;
+    RingPos<C::kDkdvDoStages> dr;
+
+    const uint64_t kmaj = sdesc_sw128(0, 16, 1024);
+    const uint64_t nmaj = sdesc_sw128(0, C::kBoxBytes, 1024);
+    auto issue_ss = [&](uint32_t col, uint32_t A, uint32_t B, uint32_t id) {
+        const uint64_t ad = kmaj + sdesc_step(A), bd = kmaj + sdesc_step(B);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t off = sdesc_step((kk >> 2) * C::kBoxBytes + (kk & 3) * 32);
+            mma_ss(tmem + col, ad + off, bd + off, id, kk > 0);
+        }
+    };
+    auto issue_ts = [&](uint32_t acc_col, uint32_t a_col, uint32_t Y, bool acc) {
+        const uint64_t yd = nmaj + sdesc_step(Y);
+#pragma unroll
+        for (int kk = 0; kk < BT / 16; ++kk)
+            mma_ts(tmem + acc_col, tmem + a_col + 8 * kk + (kk >= 4 ? 32 : 0), yd + sdesc_step(kk * 2048), idTS,
+                   acc || kk > 0);
+    };
+    // dQ = dS K: both operands M/N-major, 128-row slabs of 16 keys 2048 bytes apart
+    const uint64_t dsd0 = sdesc_sw128(0, C::kDsBytes / 2, 1024);
+    auto issue_dq = [&](uint32_t ds) {
+        const uint64_t ad = dsd0 + sdesc_step(ds), bd = nmaj + sdesc_step(sK);
+#pragma unroll
+        for (int kk = 0; kk < BT / 16; ++kk)
+            mma_ss(tmem + C::kDqCol, ad + sdesc_step(kk * 2048), bd + sdesc_step(kk * 2048), idDQ, kk > 0);
+    };
+    // every dQ issued so far has been read out of TMEM by the elementwise warps
+    auto dq_region_free = [&]() -> bool {
+        while (dqf_cnt < dq_issued) {
+            if (!mbar_wait(smem_u32(&bars.dq_free), dqf_cnt & 1, wd)) return false;
+            ++dqf_cnt;
+        }
+        return true;
+    };
+    auto take = [&](uint64_t *full, uint32_t slot, uint32_t phase) -> bool {
+        return mbar_wait(smem_u32(&full[slot]), phase, wd);
+    };
+
+    for (int i = 0;; ++i) {
+        int w;
+        if (!sched_take(bars.sched, i, w, wd)) return;
+        if (w >= total) return;
+        const DkdvInfo f = dkdv_info(p, w);
+        if (f.nq == 0) continue;
+        if (!mbar_wait(smem_u32(&bars.kv_full), kv_cnt & 1, wd)) return;
+        ++kv_cnt;
+        uint32_t qs = qr.slot(), os = dr.slot();
+        if (!take(bars.q_full, qs, qr.phase())) return;
+        ++qr.i;
+        tc_fence_after();
+        issue_ss(0, sK, sQ + qs * C::kTileBytes, idST);  // S^T_0 = K Q^T
+        tc_commit(smem_u32(&bars.st_full));
+        if (kAlias && !dq_region_free()) return;
+        if (!take(bars.do_full, os, dr.phase())) return;
+        ++dr.i;
+        tc_fence_after();
+        issue_ss(BT, sV, sDO + os * C::kTileBytes, idSS);  // dP^T_0 = V dO^T
+        tc_commit(smem_u32(&bars.dp_full));
+        for (int qb = 0; qb < f.nq; ++qb) {
+            if (qb > 0) {
+                os = dr.slot();
+                if (!take(bars.do_full, os, dr.phase())) return;
+                ++dr.i;
+            }
+            if (!mbar_wait(smem_u32(&bars.p_ready), p_cnt & 1, wd)) return;
+            ++p_cnt;
+            if (qb == 0) {
+                if (!mbar_wait(smem_u32(&bars.acc_free), (af_cnt & 1) ^ 1, wd)) return;
+                ++af_cnt;
+            }
+            tc_fence_after();
+            issue_ts(256, 0, sDO + os * C::kTileBytes, qb > 0);  // dV += P^T dO
+            if (C::kDsInDoSlot) tc_commit(smem_u32(&bars.dv_done));
+            if (qb > 0) {
+                if (kAlias && !dq_region_free()) return;
+                tc_fence_after();
+                issue_ss(BT, sV, sDO + os * C::kTileBytes, idSS);  // dP^T
+                tc_commit(smem_u32(&bars.dp_full));
+            }
+            uint32_t qsn = 0;
+            if (qb + 1 < f.nq) {
+                qsn = qr.slot();
+                if (!take(bars.q_full, qsn, qr.phase())) return;
+                ++qr.i;
+                tc_fence_after();
+                issue_ss(0, sK, sQ + qsn * C::kTileBytes, idST);  // S^T of the next block
+                tc_commit(smem_u32(&bars.st_full));
+            }
+            if (!mbar_wait(smem_u32(&bars.ds_ready), ds_cnt & 1, wd)) return;
+            ++ds_cnt;
+            tc_fence_after();
+            issue_ts(256 + D, BT, sQ + qs * C::kTileBytes, qb > 0);  // dK += dS^T Q
+            tc_commit(smem_u32(&bars.q_empty[qs]));
+            if (!kAlias && !dq_region_free()) return;
+            tc_fence_after();
+            issue_dq(C::kDsInDoSlot ? sDO + os * C::kTileBytes : sDS);  // dQ_qb = dS K
+            ++dq_issued;
+            tc_commit(smem_u32(&bars.dq_full));
+            tc_commit(smem_u32(&bars.do_empty[os]));  // dO, and at D = 128 the dS in its slot
+            qs = qsn;
+        }
+        tc_commit(smem_u32(&bars.acc_done));
+        tc_commit(smem_u32(&bars.kv_empty));
+    }
+}
+
 template <int D, bool kBF16, typename Tg>
 __device__ void dkdv_elementwise(const TcBwdArgs &a, DkdvBars &bars, float *stats, uint32_t tmem,
                                  const Watchdog &wd) {
@@ -459,7 +600,176 @@ __device__ void dkdv_elementwise(const TcBwdArgs &a, DkdvBars &bars, float *stat
     }
 }
 
+// Fused-dQ variant of the elementwise warps.  Per query block: P^T (as in the
+// separate variant); then the read-out of the previous block's dQ partial from
+// TMEM (thread = query row) with f32 reductions into the workspace sums; then
+// dS^T, written 16-bit both to TMEM (A operand of dK) and, 128-byte swizzled,
+// to shared memory (A operand of dQ).
 template <int D, bool kBF16, typename Tg>
+__device__ void dkdvq_elementwise(const TcBwdArgs &a, DkdvBars &bars, float *stats, uint32_t sDO, uint32_t sDS,
+                                  uint32_t tmem, const Watchdog &wd) {
+    using C = BCfg<D>;
+    const BwdParams &p = a.p;
+    const int total = p.sched_kv.hdr[1];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = threadIdx.x - 128;
+    const int wg = (warp - 4) >> 2;
+    const int quarter = warp & 3;
+    const int kl = 32 * quarter + lane;    // TMEM lane: key row of S^T / dP^T, query row of dQ
+    const uint32_t lane_base = tmem_addr(tmem, 32 * quarter, 0);
+    const float sl2 = fabsf(p.scale_log2);
+    uint32_t st_cnt = 0, dp_cnt = 0, ad_cnt = 0, stat_i = 0, dqf_cnt = 0, blk = 0;
+    const int64_t acc_step = (int64_t)p.n_q * 4;  // floats between 4-column groups
+
+    // read dQ of block j of item f out of TMEM and add it to the workspace sums
+    auto drain = [&](const DkdvInfo &f, int j) -> bool {
+        bool ok = mbar_wait(smem_u32(&bars.dq_full), dqf_cnt & 1, wd);
+        ++dqf_cnt;
+        if (!__all_sync(0xffffffffu, ok)) return false;
+        tc_fence_after();
+        const int row = BT * (f.qb0 + j) + kl;
+        float *dst = p.dq_accum + (((int64_t)f.h * (D / 4) + wg * (D / 8)) * p.n_q + f.q_start + row) * 4;
+        // 32 columns at a time (8 groups of 4); TMEM is released after the last load
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+            uint32_t u[32];
+            tmem_ld_x32(lane_base + C::kDqCol + (D / 2) * wg + 32 * c, u);
+            tmem_ld_wait(u);
+            if (c == D / 64 - 1) {
+                tc_fence_before();
+                mbar_arrive(smem_u32(&bars.dq_free));
+            }
+            if (row < f.Lq) {
+#pragma unroll
+                for (int g = 0; g < 8; ++g)
+                    red_add_v4(dst + (8 * c + g) * acc_step, __uint_as_float(u[4 * g]), __uint_as_float(u[4 * g + 1]),
+                               __uint_as_float(u[4 * g + 2]), __uint_as_float(u[4 * g + 3]));
+            }
+        }
+        return true;
+    };
+
+    for (int i = 0;; ++i) {
+        int w;
+        if (!sched_take_warp(bars.sched, i, w, wd)) return;
+        if (w >= total) return;
+        const DkdvInfo f = dkdv_info(p, w);
+        const int key = f.key0 + kl;
+        const bool live = key < f.Lk;
+        Tg *dst = static_cast<Tg *>(wg == 0 ? p.dv : p.dk) +
+                  (int64_t)(f.k_start + key) * (wg == 0 ? p.dv_st : p.dk_st) +
+                  (int64_t)f.h * (wg == 0 ? p.dv_sh : p.dk_sh);
+        if (f.nq == 0) {
+            if (live) zero_cols(dst, D);
+            continue;
+        }
+        const float *stat_src = (e < BT ? p.lse2 : p.dr) + (int64_t)f.h * p.n_q + f.q_start;
+        auto fetch_stat = [&](int qb, bool &valid) -> float {
+            const int qr = BT * (f.qb0 + qb) + (e & (BT - 1));
+            valid = qr < f.Lq;
+            return __ldg(stat_src + min(qr, f.Lq - 1));
+        };
+        bool stat_valid;
+        float stat_next = fetch_stat(0, stat_valid);
+        for (int qb = 0; qb < f.nq; ++qb, ++blk) {
+            float *sb = stats + (stat_i & 1) * 2 * BT;
+            sb[e] = stat_valid ? -stat_next : (e < BT ? -INFINITY : 0.f);
+            mbar_arrive(smem_u32(&bars.stats_ready[stat_i & 1]));
+            bool ok = mbar_wait(smem_u32(&bars.stats_ready[stat_i & 1]), (stat_i >> 1) & 1, wd);
+            if (!__all_sync(0xffffffffu, ok)) return;
+            ++stat_i;
+            if (qb + 1 < f.nq) stat_next = fetch_stat(qb + 1, stat_valid);
+            const float2 *nlse2 = reinterpret_cast<const float2 *>(sb + 64 * wg);
+            const float2 *ndr = reinterpret_cast<const float2 *>(sb + BT + 64 * wg);
+
+            ok = mbar_wait(smem_u32(&bars.st_full), st_cnt & 1, wd);
+            ++st_cnt;
+            if (!__all_sync(0xffffffffu, ok)) return;
+            tc_fence_after();
+            uint32_t r[2][32];
+            tmem_ld_x32(lane_base + 64 * wg, r[0]);
+            tmem_ld_x32(lane_base + 64 * wg + 32, r[1]);
+            tmem_ld_wait(r[0]);
+            tmem_ld_wait(r[1]);
+            float2 pr[32];
+            const bool diag = p.causal && (f.qb0 + qb == f.t);
+            const float2 sc2 = make_float2(sl2, sl2);
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const float2 sv = make_float2(__uint_as_float(r[(2 * c) >> 5][(2 * c) & 31]),
+                                              __uint_as_float(r[(2 * c + 1) >> 5][(2 * c + 1) & 31]));
+                const float2 x = __ffma2_rn(sv, sc2, nlse2[c]);
+                float2 pv = make_float2(exp2_approx(x.x), exp2_approx(x.y));
+                if (!live) {  // key past its sequence (the tile reaches into the next one):
+                    pv = make_float2(0.f, 0.f);  // its dS row must add nothing to dQ
+                } else if (diag) {
+                    if (kl > 64 * wg + 2 * c) pv.x = 0.f;
+                    if (kl > 64 * wg + 2 * c + 1) pv.y = 0.f;
+                }
+                pr[c] = pv;
+                pk[c] = pack2(pv.x, pv.y, kBF16);
+            }
+            tmem_st_x32(lane_base + 64 * wg, pk);
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars.p_ready));
+
+            if (qb > 0 && !drain(f, qb - 1)) return;
+
+            ok = mbar_wait(smem_u32(&bars.dp_full), dp_cnt & 1, wd);
+            ++dp_cnt;
+            if (!__all_sync(0xffffffffu, ok)) return;
+            tc_fence_after();
+            tmem_ld_x32(lane_base + BT + 64 * wg, r[0]);
+            tmem_ld_x32(lane_base + BT + 64 * wg + 32, r[1]);
+            tmem_ld_wait(r[0]);
+            tmem_ld_wait(r[1]);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const float2 dp = make_float2(__uint_as_float(r[(2 * c) >> 5][(2 * c) & 31]),
+                                              __uint_as_float(r[(2 * c + 1) >> 5][(2 * c + 1) & 31]));
+                const float2 d = __fmul2_rn(pr[c], __fadd2_rn(dp, ndr[c]));
+                pk[c] = pack2(d.x, d.y, kBF16);
+            }
+            tmem_st_x32(lane_base + BT + 64 * wg, pk);
+            if (C::kDsInDoSlot) {
+                // dS goes over this block's dO tile: dV must have read it (dP of
+                // the first block of an item is issued before its dV)
+                ok = mbar_wait(smem_u32(&bars.dv_done), blk & 1, wd);
+                if (!__all_sync(0xffffffffu, ok)) return;
+            }
+            // the same dS^T row into the shared dS tile: box wg holds query rows
+            // [64 wg, 64 wg + 64), 128 bytes per key row, 16-byte chunks swizzled
+            const uint32_t ds_row = (C::kDsInDoSlot ? sDO + (blk % C::kDkdvDoStages) * C::kTileBytes : sDS) +
+                                    wg * (C::kDsBytes / 2) + kl * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                st_shared_v4(ds_row + ((j ^ (kl & 7)) << 4), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            fence_proxy_async_smem();
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars.ds_ready));
+        }
+        if (!drain(f, f.nq - 1)) return;
+        bool ok = mbar_wait(smem_u32(&bars.acc_done), ad_cnt & 1, wd);
+        ++ad_cnt;
+        if (!__all_sync(0xffffffffu, ok)) return;
+        tc_fence_after();
+        const float mul = wg == 0 ? 1.f : p.scale;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t u[32];
+            tmem_ld_x32(lane_base + 256 + D * wg + 32 * c, u);
+            tmem_ld_wait(u);
+            if (live) store_row32(dst + 32 * c, u, mul);
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars.acc_free));
+    }
+}
+
+template <int D, bool kBF16, typename Tg, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1) dkdv_tc_kernel(const __grid_constant__ TcBwdArgs a) {
     using C = BCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -470,6 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_tc_kernel(const __grid_const
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const uint32_t sK = base, sV = base + C::kTileBytes, sQ = base + 2 * C::kTileBytes;
     const uint32_t sDO = sQ + C::kDkdvQStages * C::kTileBytes;
+    const uint32_t sDS = sDO + C::kDkdvDoStages * C::kTileBytes;  // used at D = 64 only
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const Watchdog wd{a.p.watchdog_cycles, &abort_flag, a.p.status};
 
@@ -494,6 +805,9 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_tc_kernel(const __grid_const
         mbar_init(smem_u32(&bars.stats_ready[0]), kEw);
         mbar_init(smem_u32(&bars.stats_ready[1]), kEw);
         mbar_init(smem_u32(&bars.mma_drain), 1);
+        mbar_init(smem_u32(&bars.dq_full), 1);
+        mbar_init(smem_u32(&bars.dq_free), kEw);
+        mbar_init(smem_u32(&bars.dv_done), 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&bars.sched.full[s]), 1);
             mbar_init(smem_u32(&bars.sched.empty[s]), kSchedConsumers + 1);  // + the dO producer
@@ -512,18 +826,20 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_tc_kernel(const __grid_const
     tc_fence_after();
     const uint32_t tmem = tmem_base;
     if (warp < 4) {
-        regs_dec<C::kRegsProducer>();
+        regs_dec<kFused ? C::kRegsProducerFused : C::kRegsProducer>();
         if ((warp == 0 || warp == 2) && lane == 0) dkdv_producer<D>(a, bars, sK, sV, sQ, sDO, warp == 2, wd);
         else if (warp == 1 && lane == 0) {
-            dkdv_mma<D, kBF16>(a, bars, sK, sV, sQ, sDO, tmem, wd);
+            if constexpr (kFused) dkdvq_mma<D, kBF16>(a, bars, sK, sV, sQ, sDO, sDS, tmem, wd);
+            else dkdv_mma<D, kBF16>(a, bars, sK, sV, sQ, sDO, tmem, wd);
             if (aborting(wd)) {  // let issued MMAs finish before TMEM is freed
                 tc_commit(smem_u32(&bars.mma_drain));
                 drain_wait(smem_u32(&bars.mma_drain), 0, kDrainCycles);
             }
         }
     } else {
-        regs_inc<C::kRegsEw>();
-        dkdv_elementwise<D, kBF16, Tg>(a, bars, stats, tmem, wd);
+        regs_inc<kFused ? C::kRegsEwFused : C::kRegsEw>();
+        if constexpr (kFused) dkdvq_elementwise<D, kBF16, Tg>(a, bars, stats, sDO, sDS, tmem, wd);
+        else dkdv_elementwise<D, kBF16, Tg>(a, bars, stats, tmem, wd);
     }
     tc_fence_before();
     __syncthreads();
@@ -886,7 +1202,9 @@ cudaError_t launch(K kern, int smem, const TcBwdArgs &a, int num_ctas, cudaStrea
 
 template <int D, bool kBF16, typename Tg>
 cudaError_t launch_typed(const TcBwdArgs &a, int num_ctas, cudaStream_t s, bool dkdv) {
-    if (dkdv) return launch(dkdv_tc_kernel<D, kBF16, Tg>, BCfg<D>::kDkdvSmem, a, num_ctas, s);
+    if (dkdv && a.p.dq_accum)
+        return launch(dkdv_tc_kernel<D, kBF16, Tg, true>, BCfg<D>::kDkdvSmem, a, num_ctas, s);
+    if (dkdv) return launch(dkdv_tc_kernel<D, kBF16, Tg, false>, BCfg<D>::kDkdvSmem, a, num_ctas, s);
     return launch(dq_tc_kernel<D, kBF16, Tg>, BCfg<D>::kDqSmem, a, num_ctas, s);
 }
 

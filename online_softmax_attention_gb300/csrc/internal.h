@@ -102,6 +102,10 @@ struct BwdParams {
     const int32_t *cu_q, *cu_k;
     float *dr;          // (H, n_q) rowsum(dO * O), in the workspace
     float *lse2;        // (H, n_q) lse * log2(e), +inf where lse = -inf, in the workspace
+    // fused dQ (tensor-core dK/dV kernel also accumulates dQ): f32 partial sums
+    // laid out (H, D/4, n_q, 4) in the workspace, so that 32 consecutive query
+    // rows of one 4-column group are 512 contiguous bytes; null = separate dQ kernel
+    float *dq_accum;
     Sched sched_kv;     // items over key blocks (dk, dv)
     Sched sched_q;      // items over query blocks (dq)
     int *status;
@@ -125,6 +129,10 @@ int fwd_simt_ctas_per_sm(const FwdParams &p);  // resident CTAs per SM of the ke
 cudaError_t launch_bwd_preprocess(const BwdParams &p, cudaStream_t s);
 cudaError_t launch_bwd_dkdv_simt(const BwdParams &p, int num_ctas, cudaStream_t s);
 cudaError_t launch_bwd_dq_simt(const BwdParams &p, int num_ctas, cudaStream_t s);
+// fused dQ: zero the partial sums (before the dK/dV kernel); dq = scale * sums
+// converted to grad_dtype with dq's strides (after it)
+cudaError_t launch_dq_accum_zero(const BwdParams &p, cudaStream_t s);
+cudaError_t launch_dq_accum_convert(const BwdParams &p, cudaStream_t s);
 
 // Number of multiprocessors of the current device.
 int sm_count();

@@ -10,22 +10,31 @@ from parity_util import check_grad
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = ["auto", "simt", "tc"]
+# kernel family / dq mode: "auto" resolves to the separate (deterministic)
+# dq kernel; "tc/fused" accumulates dq inside the dK/dV kernel
+KERNELS = ["auto", "simt", "tc", "tc/fused"]
 DEV = "cuda"
 
 
 def _skip_unsupported(kernel, dtype):
-    if kernel == "tc" and dtype == "f32":
+    if kernel.startswith("tc") and dtype == "f32":
         pytest.skip("the tensor-core kernels take f16 / bf16 only")
 
 
+def _split(kernel):
+    fam, _, mode = kernel.partition("/")
+    return fam, mode or "auto"
+
+
 def _fwd_bwd(x, *, causal, kernel, out_dtype=None, grad_dtype=None, num_ctas=0, scale=None):
+    fam, mode = _split(kernel)
     q, k, v, dO = (x[n].to(DEV) for n in ("q", "k", "v", "dO"))
     cq, ck = x["cu_seqlens_q"], x["cu_seqlens_k"]
     o, lse = attn.fwd(q, k, v, causal=causal, scale=scale, cu_seqlens_q=cq, cu_seqlens_k=ck,
-                      out_dtype=out_dtype, kernel=kernel)
+                      out_dtype=out_dtype, kernel=fam)
     dq, dk, dv = attn.bwd(q, k, v, o, lse, dO, causal=causal, scale=scale, cu_seqlens_q=cq,
-                          cu_seqlens_k=ck, grad_dtype=grad_dtype, kernel=kernel, num_ctas=num_ctas)
+                          cu_seqlens_k=ck, grad_dtype=grad_dtype, kernel=fam, num_ctas=num_ctas,
+                          dq_mode=mode)
     torch.cuda.synchronize()
     assert attn.device_status() == 0
     return dq, dk, dv
@@ -74,13 +83,50 @@ def test_f32_gradients_and_custom_scale(kernel):
     _check(got, _ref(x, causal=True, scale=0.2))
 
 
-@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("kernel", ["auto", "simt", "tc"])
 def test_deterministic_and_grid_independent(kernel):
     x = attn_inputs.make(dtype="bf16", H=2, D=128, seed=24, lengths=[300, 70], backward=True)
     runs = [_fwd_bwd(x, causal=True, kernel=kernel, num_ctas=n) for n in (0, 3, 0)]
     for r in runs[1:]:
         for a, b in zip(r, runs[0]):
             assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_fused_dq_grid_independent(D):
+    """Fused dq: dk and dv are written once (bitwise equal across grids); dq is a
+    sum of f32 reductions in varying order (equal up to rounding)."""
+    x = attn_inputs.make(dtype="bf16", H=2, D=D, seed=24, lengths=[300, 70], backward=True)
+    runs = [_fwd_bwd(x, causal=True, kernel="tc/fused", num_ctas=n, grad_dtype=torch.float32)
+            for n in (0, 3, 0)]
+    for r in runs[1:]:
+        assert torch.equal(r[1], runs[0][1]) and torch.equal(r[2], runs[0][2])
+        rel = float((r[0] - runs[0][0]).norm() / runs[0][0].norm())
+        assert rel < 1e-5, rel
+
+
+def test_dq_mode_selection():
+    x = attn_inputs.make(dtype="bf16", H=2, D=64, seed=27, n_q=130, backward=True)
+    q, k, v, dO = (x[n].to(DEV) for n in ("q", "k", "v", "dO"))
+    o, lse = attn.fwd(q, k, v, causal=True)
+    assert attn.BwdCall(q, k, v, o, lse, dO, causal=True).selected_dq_mode() == "separate"
+    assert attn.BwdCall(q, k, v, o, lse, dO, causal=True, dq_mode="fused").selected_dq_mode() == "fused"
+    assert attn.BwdCall(q, k, v, o, lse, dO, causal=True, kernel="simt").selected_dq_mode() == "separate"
+    with pytest.raises(attn.AttnError):
+        attn.BwdCall(q, k, v, o, lse, dO, causal=True, kernel="simt", dq_mode="fused").run()
+    # the fused mode's workspace holds the dq partial sums, n_q * H * D f32
+    fused = attn.BwdCall(q, k, v, o, lse, dO, causal=True, dq_mode="fused")
+    sep = attn.BwdCall(q, k, v, o, lse, dO, causal=True)
+    assert fused.workspace.numel() - sep.workspace.numel() >= 130 * 2 * 64 * 4
+
+
+def test_fused_dq_matches_separate_closely():
+    x = attn_inputs.make(dtype="bf16", H=4, D=128, seed=28, lengths=[1000, 129, 384], backward=True)
+    a = _fwd_bwd(x, causal=True, kernel="tc/fused", out_dtype=torch.float32, grad_dtype=torch.float32)
+    b = _fwd_bwd(x, causal=True, kernel="tc", out_dtype=torch.float32, grad_dtype=torch.float32)
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2]), "dk / dv differ between dq modes"
+    rel = float((a[0] - b[0]).norm() / b[0].norm())
+    assert rel < 1e-3, rel
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
