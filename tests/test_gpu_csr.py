@@ -108,3 +108,24 @@ def test_malformed_relation_is_reported_and_skipped():
     assert not f64(o)[2].any() and np.isneginf(f64(lse)[0, 2])
     row1 = oracle.csr_fwd([0, 1], col[3:4], x["v"], scores=x["scores"][3:4])  # edge 99 skipped
     assert float(np.abs(f64(o)[1] - row1[0][0]).max()) <= 1e-5
+
+
+@pytest.mark.parametrize("dot", [False, True])
+def test_strided_views_match_packed_rows(dot):
+    """Tensors whose heads are not back to back in a row ((H, N, D) storage
+    viewed as (N, H, D)) take the general kernel; packed rows take the
+    row-centric one.  Both equal the oracle on the same relation."""
+    _, rp, col = attn_inputs.radius_graph(1500, 0.1, seed=606)
+    x = attn_inputs.make_csr(row_ptr=rp, col=col, n_src=1500, H=4, D=64, dtype="bf16", seed=607,
+                             field_scores=not dot, score_std=2.0)
+    o_ref, lse_ref = _ref(x, dot=dot)
+    packed = _gpu(x, dot=dot, out_dtype=torch.float32)
+    strided = dict(x)
+    for name in ("v", "q", "k"):
+        if x.get(name) is not None:
+            strided[name] = x[name].permute(1, 0, 2).contiguous().permute(1, 0, 2)
+    assert strided["v"].stride(1) != x["v"].shape[2]
+    o_s, lse_s = _gpu(strided, dot=dot, out_dtype=torch.float32)
+    assert attn.device_status() == 0
+    for o, lse in (packed, (o_s, lse_s)):
+        _check(o, lse, o_ref, lse_ref, torch.bfloat16, o.dtype)
