@@ -499,6 +499,8 @@ def run_csr_workload(args, rank, world):
         raise RuntimeError("device status set in the timed region")
 
     peaks = load_peaks()
+    csrc = "online_softmax_attention_gb300/csrc/"
+    traffic = recorded_traffic(w.name, source_hash([csrc + "csr.cu", csrc + "common.cuh", csrc + "internal.h"]))
     rate = E * w.H * world / (ms * 1e-3) / 1e9
     achieved = gathered / (ms * 1e-3) / 1e9
     line = {
@@ -514,7 +516,7 @@ def run_csr_workload(args, rank, world):
                    else "no flush: inputs larger than L2",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": "csr_fwd",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "kernel": "csr_fwd",
                      "peak_source": f"HBM copy ({peaks['source']})",
                      "bytes": "gathered: one V (and K) row per edge and head"},
         "e2e": {"value": E * w.H * world / (e2e_ms * 1e-3) / 1e9, "unit": "Gedge/s",
