@@ -96,6 +96,13 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
 }
 
 constexpr long long kDrainCycles = 1ll << 31;  // post-abort wait for TMA loads in flight
+
+// The dq kernel's elementwise warps are on its critical path and bound by the
+// SFU (16384 exponentials per 128 x 128 block); computing one pair in four with
+// the FMA-pipe polynomial (exp2_fma2) took the dq stage of the causal training
+// workload from 2.70 to 2.48 ms (one in eight: 2.58, three in eight: 2.52, one
+// in two: 2.56).  The dK/dV kernel got slower with it and keeps the SFU only.
+constexpr int kDqExpFmaEvery = 4;
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long long budget) {
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
@@ -1078,7 +1085,9 @@ __device__ void dq_elementwise(const TcBwdArgs &a, DqBars &bars, uint32_t tmem, 
                 const float2 sv = make_float2(__uint_as_float(rs[(2 * c) >> 5][(2 * c) & 31]),
                                               __uint_as_float(rs[(2 * c + 1) >> 5][(2 * c + 1) & 31]));
                 const float2 x = __ffma2_rn(sv, sc2, nl2);
-                float2 pv = make_float2(exp2_approx(x.x), exp2_approx(x.y));
+                // one pair in kDqExpFmaEvery on the FMA pipe, the rest on the SFU
+                float2 pv = (c % kDqExpFmaEvery) == 0 ? exp2_fma2(x)
+                                                      : make_float2(exp2_approx(x.x), exp2_approx(x.y));
                 if (masked) {
                     if (c0 + 2 * c >= lim) pv.x = 0.f;
                     if (c0 + 2 * c + 1 >= lim) pv.y = 0.f;
