@@ -530,7 +530,7 @@ __device__ void dkdv_elementwise(const TcBwdArgs &a, DkdvBars &bars, float *stat
         for (int qb = 0; qb < f.nq; ++qb) {
             float *sb = stats + (stat_i & 1) * 2 * BT;
             sb[e] = stat_valid ? -stat_next : (e < BT ? -INFINITY : 0.f);
-            mbar_arrive(smem_u32(&bars.stats_ready[stat_i & 1]));
+            mbar_arrive_warp(smem_u32(&bars.stats_ready[stat_i & 1]));
             bool ok = mbar_wait(smem_u32(&bars.stats_ready[stat_i & 1]), (stat_i >> 1) & 1, wd);
             if (!__all_sync(0xffffffffu, ok)) return;
             ++stat_i;
@@ -567,7 +567,7 @@ __device__ void dkdv_elementwise(const TcBwdArgs &a, DkdvBars &bars, float *stat
             tmem_st_x32(lane_base + 64 * wg, pk);
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(smem_u32(&bars.p_ready));
+            mbar_arrive_warp(smem_u32(&bars.p_ready));
 
             ok = mbar_wait(smem_u32(&bars.dp_full), dp_cnt & 1, wd);
             ++dp_cnt;
@@ -587,7 +587,7 @@ __device__ void dkdv_elementwise(const TcBwdArgs &a, DkdvBars &bars, float *stat
             tmem_st_x32(lane_base + BT + 64 * wg, pk);
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(smem_u32(&bars.ds_ready));
+            mbar_arrive_warp(smem_u32(&bars.ds_ready));
         }
         // epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK * scale
         bool ok = mbar_wait(smem_u32(&bars.acc_done), ad_cnt & 1, wd);
@@ -603,7 +603,7 @@ __device__ void dkdv_elementwise(const TcBwdArgs &a, DkdvBars &bars, float *stat
             if (live) store_row32(dst + 32 * c, u, mul);
         }
         tc_fence_before();
-        mbar_arrive(smem_u32(&bars.acc_free));
+        mbar_arrive_warp(smem_u32(&bars.acc_free));
     }
 }
 
@@ -644,7 +644,7 @@ __device__ void dkdvq_elementwise(const TcBwdArgs &a, DkdvBars &bars, float *sta
             tmem_ld_wait(u);
             if (c == D / 64 - 1) {
                 tc_fence_before();
-                mbar_arrive(smem_u32(&bars.dq_free));
+                mbar_arrive_warp(smem_u32(&bars.dq_free));
             }
             if (row < f.Lq) {
 #pragma unroll
@@ -681,7 +681,7 @@ __device__ void dkdvq_elementwise(const TcBwdArgs &a, DkdvBars &bars, float *sta
         for (int qb = 0; qb < f.nq; ++qb, ++blk) {
             float *sb = stats + (stat_i & 1) * 2 * BT;
             sb[e] = stat_valid ? -stat_next : (e < BT ? -INFINITY : 0.f);
-            mbar_arrive(smem_u32(&bars.stats_ready[stat_i & 1]));
+            mbar_arrive_warp(smem_u32(&bars.stats_ready[stat_i & 1]));
             bool ok = mbar_wait(smem_u32(&bars.stats_ready[stat_i & 1]), (stat_i >> 1) & 1, wd);
             if (!__all_sync(0xffffffffu, ok)) return;
             ++stat_i;
@@ -720,7 +720,7 @@ __device__ void dkdvq_elementwise(const TcBwdArgs &a, DkdvBars &bars, float *sta
             tmem_st_x32(lane_base + 64 * wg, pk);
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(smem_u32(&bars.p_ready));
+            mbar_arrive_warp(smem_u32(&bars.p_ready));
 
             if (qb > 0 && !drain(f, qb - 1)) return;
 
@@ -756,7 +756,7 @@ __device__ void dkdvq_elementwise(const TcBwdArgs &a, DkdvBars &bars, float *sta
             fence_proxy_async_smem();
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(smem_u32(&bars.ds_ready));
+            mbar_arrive_warp(smem_u32(&bars.ds_ready));
         }
         if (!drain(f, f.nq - 1)) return;
         bool ok = mbar_wait(smem_u32(&bars.acc_done), ad_cnt & 1, wd);
@@ -772,7 +772,7 @@ __device__ void dkdvq_elementwise(const TcBwdArgs &a, DkdvBars &bars, float *sta
             if (live) store_row32(dst + 32 * c, u, mul);
         }
         tc_fence_before();
-        mbar_arrive(smem_u32(&bars.acc_free));
+        mbar_arrive_warp(smem_u32(&bars.acc_free));
     }
 }
 
@@ -805,15 +805,15 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_tc_kernel(const __grid_const
         }
         mbar_init(smem_u32(&bars.st_full), 1);
         mbar_init(smem_u32(&bars.dp_full), 1);
-        mbar_init(smem_u32(&bars.p_ready), kEw);
-        mbar_init(smem_u32(&bars.ds_ready), kEw);
+        mbar_init(smem_u32(&bars.p_ready), kEw / 32);
+        mbar_init(smem_u32(&bars.ds_ready), kEw / 32);
         mbar_init(smem_u32(&bars.acc_done), 1);
-        mbar_init(smem_u32(&bars.acc_free), kEw);
-        mbar_init(smem_u32(&bars.stats_ready[0]), kEw);
-        mbar_init(smem_u32(&bars.stats_ready[1]), kEw);
+        mbar_init(smem_u32(&bars.acc_free), kEw / 32);
+        mbar_init(smem_u32(&bars.stats_ready[0]), kEw / 32);
+        mbar_init(smem_u32(&bars.stats_ready[1]), kEw / 32);
         mbar_init(smem_u32(&bars.mma_drain), 1);
         mbar_init(smem_u32(&bars.dq_full), 1);
-        mbar_init(smem_u32(&bars.dq_free), kEw);
+        mbar_init(smem_u32(&bars.dq_free), kEw / 32);
         mbar_init(smem_u32(&bars.dv_done), 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&bars.sched.full[s]), 1);
@@ -1069,7 +1069,7 @@ __device__ void dq_elementwise(const TcBwdArgs &a, DqBars &bars, uint32_t tmem, 
             tmem_ld_wait(rp[0]);
             tmem_ld_wait(rp[1]);
             tc_fence_before();
-            mbar_arrive(smem_u32(&bars.sp_free));  // S and dP buffers may be overwritten
+            mbar_arrive_warp(smem_u32(&bars.sp_free));  // S and dP buffers may be overwritten
 
             const int key0 = BT * j;
             int lim = BT;  // keys [0, lim) of the tile are admitted for this row
@@ -1100,7 +1100,7 @@ __device__ void dq_elementwise(const TcBwdArgs &a, DqBars &bars, uint32_t tmem, 
             tmem_st_x32(lane_base + 256 + 64 * (j & 1) + 32 * wg, pk);
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(smem_u32(&bars.ds_ready));
+            mbar_arrive_warp(smem_u32(&bars.ds_ready));
         }
         bool ok = mbar_wait(smem_u32(&bars.acc_done), ad_cnt & 1, wd);
         ++ad_cnt;
@@ -1114,7 +1114,7 @@ __device__ void dq_elementwise(const TcBwdArgs &a, DqBars &bars, uint32_t tmem, 
             if (live) store_row32(dst + 32 * c, u, p.scale);
         }
         tc_fence_before();
-        mbar_arrive(smem_u32(&bars.acc_free));
+        mbar_arrive_warp(smem_u32(&bars.acc_free));
     }
     (void)step;
 }
@@ -1146,10 +1146,10 @@ __global__ void __launch_bounds__(kThreads, 1) dq_tc_kernel(const __grid_constan
         }
         mbar_init(smem_u32(&bars.sp_full), 1);
         mbar_init(smem_u32(&bars.mma_drain), 1);
-        mbar_init(smem_u32(&bars.sp_free), kEw);
-        mbar_init(smem_u32(&bars.ds_ready), kEw);
+        mbar_init(smem_u32(&bars.sp_free), kEw / 32);
+        mbar_init(smem_u32(&bars.ds_ready), kEw / 32);
         mbar_init(smem_u32(&bars.acc_done), 1);
-        mbar_init(smem_u32(&bars.acc_free), kEw);
+        mbar_init(smem_u32(&bars.acc_free), kEw / 32);
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&bars.sched.full[s]), 1);
             mbar_init(smem_u32(&bars.sched.empty[s]), kSchedConsumers);

@@ -446,7 +446,7 @@ __device__ void softmax_wg(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
                     // nothing of this tile enters m, l or U; S_t may be overwritten
                     if (lrow == 0 && p.pruned_tiles) atomicAdd(p.pruned_tiles, 1ull);
                     tc_fence_before();
-                    mbar_arrive(smem_u32(&bars.p_full[t]));
+                    mbar_arrive_warp(smem_u32(&bars.p_full[t]));
                     continue;
                 }
                 m_run = fmaxf(m_run, m_tile);
@@ -499,7 +499,7 @@ __device__ void softmax_wg(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(smem_u32(&bars.p_full[t]));
+            mbar_arrive_warp(smem_u32(&bars.p_full[t]));
         }
 
         // epilogue: O = U / l, lse = (m + log2 l) ln 2
@@ -524,7 +524,7 @@ __device__ void softmax_wg(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
         }
         if (live && lse_at) *lse_at = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
         tc_fence_before();
-        mbar_arrive(smem_u32(&bars.o_free[t]));
+        mbar_arrive_warp(smem_u32(&bars.o_free[t]));
     }
 }
 
@@ -551,9 +551,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             mbar_init(smem_u32(&bars.q_full[t]), 1);
             mbar_init(smem_u32(&bars.q_empty[t]), 1);
             mbar_init(smem_u32(&bars.s_full[t]), 1);
-            mbar_init(smem_u32(&bars.p_full[t]), 128);
+            mbar_init(smem_u32(&bars.p_full[t]), 4);  // one arrival per softmax warp
             mbar_init(smem_u32(&bars.o_done[t]), 1);
-            mbar_init(smem_u32(&bars.o_free[t]), 128);
+            mbar_init(smem_u32(&bars.o_free[t]), 4);
             mbar_init(smem_u32(&bars.tile_max[t]), 4);
         }
         for (int s = 0; s < C::kKStages; ++s) {

@@ -33,6 +33,17 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// One arrival per warp on `bar` (initialised with the number of arriving
+// warps) once all 32 lanes have reached this point.  Writes the lanes made
+// before -- TMEM stores completed by tcgen05.wait::st and followed by
+// tcgen05.fence::before_thread_sync, or shared-memory stores -- are ordered
+// before lane 0's release arrive by the warp barrier.  128 or 256 per-thread
+// arrivals on one mbarrier serialise; 4 or 8 do not.
+__device__ __forceinline__ void mbar_arrive_warp(uint32_t bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
