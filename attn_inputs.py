@@ -49,6 +49,7 @@ class Workload:
     layout: str = "thd"
     backward: bool = False
     key_gain: tuple = ()      # (block, lo, hi): structured keys, see the recipe
+    qk_fp8: bool = False      # q and k rounded to float8_e4m3fn (v stays `dtype`)
     note: str = field(default="", compare=False)
 
 
@@ -69,6 +70,11 @@ WORKLOADS = {
         "causal_train_bf16_b4_n8192", "bf16", H=32, D=128, causal=True, seed=5, n_q=8192,
         n_k=8192, batch=4, backward=True,
         note="causal fwd+bwd, batch 4 x N=8192, H=32, D=128, bf16"),
+    # fp8 queries and keys: the training workload's forward with q, k in e4m3
+    "causal_fp8qk_b4_n8192": Workload(
+        "causal_fp8qk_b4_n8192", "bf16", H=32, D=128, causal=True, seed=5, n_q=8192, n_k=8192,
+        batch=4, qk_fp8=True,
+        note="causal fwd, batch 4 x N=8192, H=32, D=128, q and k e4m3, v bf16"),
     # tile pruning (approximate forward): keys with one gain in [0.2, 3] per
     # 128-key tile and head, so that whole tiles differ in their best score
     "pruned_full_bf16_n8192": Workload(
@@ -85,14 +91,16 @@ def _randn(gen: torch.Generator, shape, dtype: torch.dtype) -> torch.Tensor:
 def make(*, dtype: str, H: int, D: int, seed: int, n_q: int | None = None,
          n_k: int | None = None, batch: int = 1, lengths=None, lengths_k=None,
          varlen: tuple = (), layout: str = "thd", backward: bool = False,
-         key_gain: tuple = ()) -> dict:
+         key_gain: tuple = (), qk_fp8: bool = False) -> dict:
     """Draw one input set.  Returns CPU tensors and host cu_seqlens.
 
     Keys: q, k, v, (dO), cu_seqlens_q, cu_seqlens_k (int32, or None for a
-    single sequence), lengths_q, lengths_k (python lists).
+    single sequence), lengths_q, lengths_k (python lists).  With qk_fp8, q and
+    k are the same N(0, 1) draws rounded to float8_e4m3fn instead of `dtype`.
     """
     gen = torch.Generator().manual_seed(seed)
     tdt = DTYPES[dtype]
+    qkdt = torch.float8_e4m3fn if qk_fp8 else tdt
     if varlen:
         n_seq, lo, hi = varlen
         lq = torch.randint(lo, hi + 1, (n_seq,), generator=gen).tolist()
@@ -105,12 +113,12 @@ def make(*, dtype: str, H: int, D: int, seed: int, n_q: int | None = None,
         lk = [int(n_k if n_k is not None else n_q)] * batch
     Tq, Tk = sum(lq), sum(lk)
 
-    def draw(T):
+    def draw(T, dt=tdt):
         if layout == "hnd":
-            return _randn(gen, (H, T, D), tdt).permute(1, 0, 2)
-        return _randn(gen, (T, H, D), tdt)
+            return _randn(gen, (H, T, D), dt).permute(1, 0, 2)
+        return _randn(gen, (T, H, D), dt)
 
-    out = {"q": draw(Tq), "k": draw(Tk), "v": draw(Tk)}
+    out = {"q": draw(Tq, qkdt), "k": draw(Tk, qkdt), "v": draw(Tk)}
     if backward:
         out["dO"] = draw(Tq)
     if key_gain:
@@ -118,7 +126,7 @@ def make(*, dtype: str, H: int, D: int, seed: int, n_q: int | None = None,
         n_blocks = (Tk + block - 1) // block
         g = lo + (hi - lo) * torch.rand((n_blocks, H), generator=gen, dtype=torch.float32)
         gain = g.repeat_interleave(block, dim=0)[:Tk].unsqueeze(-1)  # (Tk, H, 1)
-        out["k"] = (out["k"].to(torch.float32) * gain).to(tdt)
+        out["k"] = (out["k"].to(torch.float32) * gain).to(qkdt)
     multi = len(lq) > 1 or varlen or lengths is not None
     if multi:
         out["cu_seqlens_q"] = torch.tensor([0] + lq, dtype=torch.int64).cumsum(0).to(torch.int32)
@@ -136,7 +144,7 @@ def make_workload(w: Workload | str) -> dict:
         w = WORKLOADS[w]
     return make(dtype=w.dtype, H=w.H, D=w.D, seed=w.seed, n_q=w.n_q or None,
                 n_k=w.n_k or None, batch=w.batch, varlen=w.varlen, layout=w.layout,
-                backward=w.backward, key_gain=w.key_gain)
+                backward=w.backward, key_gain=w.key_gain, qk_fp8=w.qk_fp8)
 
 
 # ---- CSR relations (general sparse attention / segment softmax) ---------------------

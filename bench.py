@@ -205,7 +205,7 @@ def time_oracle_sample(x, w, max_seconds=20.0):
 
 
 FWD_WORKLOADS = ("causal_fp16_n256", "full_fp16_n1024", "varlen_causal_bf16", "cross_f32_8192x2048",
-                 "pruned_full_bf16_n8192")
+                 "pruned_full_bf16_n8192", "causal_fp8qk_b4_n8192")
 CSR_WORKLOADS = ("csr_gat_n512", "csr_radius_field_bf16", "csr_radius_dot_bf16")
 L2_BYTES = 129 * 1024 * 1024
 
@@ -327,7 +327,13 @@ def run_forward_workload(args, rank, world):
     peaks = load_peaks()
     family = call.selected_kernel()
     achieved = flops / (ms * 1e-3) / 1e12
-    if family == "tc":
+    if family == "tc" and w.qk_fp8:
+        # half the FLOPs (S = Q K^T) at the fp8 rate, 2x the 16-bit rate (nominal
+        # ratio), half (P V) at the 16-bit rate: peak = 2 / (1/(2 P) + 1/P) = 4 P / 3
+        peak, bound = peaks["bf16_tflops"] * 4.0 / 3.0, "tensor"
+        note = (f"mixed: fp8 score contraction at 2x and bf16 value contraction at 1x the "
+                f"bf16 dense burst peak ({peaks['source']}), i.e. 4/3 of it")
+    elif family == "tc":
         peak, bound = peaks["bf16_tflops"], "tensor"
         note = f"bf16/f16 dense, burst ({peaks['source']})"
     else:
@@ -350,7 +356,8 @@ def run_forward_workload(args, rank, world):
         "metric": metric, "value": job_rate(flops, world, ms) / 1e12, "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": {"fp16": "f16", "bf16": "bf16", "f32": "f32"}[w.dtype], "data": "synthetic",
+        "dtype": ("e4m3+" if w.qk_fp8 else "") + {"fp16": "f16", "bf16": "bf16", "f32": "f32"}[w.dtype],
+        "data": "synthetic",
         "config": {"workload": w.name, "kernel": family, "num_splits": call.num_splits(),
                    "tokens_q": int(sum(x["lengths_q"])), "tokens_k": int(sum(x["lengths_k"])),
                    "heads": w.H, "head_dim": w.D, "relation": "causal" if w.causal else "full",
@@ -507,7 +514,8 @@ def run_csr_workload(args, rank, world):
         "metric": f"attention over a CSR relation, Gedge/s ({w.note})", "value": rate,
         "unit": "Gedge/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": {"fp16": "f16", "bf16": "bf16", "f32": "f32"}[w.dtype], "data": "synthetic",
+        "dtype": ("e4m3+" if w.qk_fp8 else "") + {"fp16": "f16", "bf16": "bf16", "f32": "f32"}[w.dtype],
+        "data": "synthetic",
         "config": {"workload": w.name, "nodes": n, "edges": E, "avg_degree": E / max(1, n),
                    "heads": w.H, "head_dim": w.D,
                    "scores": "field" if w.field_scores else "dot-product",

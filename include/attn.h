@@ -64,7 +64,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 3
+#define ATTN_ABI_VERSION 4
 
 #if defined(__GNUC__)
 #define ATTN_API __attribute__((visibility("default")))
@@ -137,7 +137,17 @@ typedef struct attn_fwd_args {
                               the exact forward; 0 < rho <= 1 enables it */
     uint64_t *pruned_tiles; /* optional device counter, or NULL: with pruning on, the
                                forward adds the number of pruned tiles to it */
+    int32_t qk_fp8;       /* 0: q and k are `dtype`; 1: q and k are fp8 e4m3 (see below) */
 } attn_fwd_args;
+
+/* fp8 queries and keys (qk_fp8 = 1; no counterpart on the pages, a use of the
+ * sm_103a tensor cores' 8-bit score contraction): q and k hold e4m3 values,
+ * one byte per element (strides in elements = bytes, rows 16-byte aligned);
+ * v is `dtype` (f16 or bf16), P is rounded to it and o is o_dtype as usual.
+ * The scores are the exact products of the e4m3 values accumulated in f32,
+ * times `scale`; a caller with per-tensor dequantisation factors for q and k
+ * folds them into `scale`.  Tensor-core kernel only: D = 128 and scale > 0,
+ * else ATTN_EUNSUPPORTED (also with ATTN_KERNEL_SIMT).  Backward: none. */
 
 /* Tile pruning (TIGA-lang attention examples page, section
  * "基于 tile 剪枝的稀疏注意力", tile-pruned sparse attention): an explicit,

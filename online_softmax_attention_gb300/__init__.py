@@ -33,6 +33,7 @@ __all__ = ["fwd", "bwd", "merge", "csr_fwd", "FwdCall", "BwdCall", "MergeCall", 
            "device_status", "launch_count", "AttnError", "library_path"]
 
 _DT = {torch.float16: ATTN_F16, torch.bfloat16: ATTN_BF16, torch.float32: ATTN_F32}
+_E4M3 = getattr(torch, "float8_e4m3fn", None)
 _KERNELS = {"auto": ATTN_KERNEL_AUTO, "simt": ATTN_KERNEL_SIMT, "tc": ATTN_KERNEL_TC}
 # backward dq: "separate" (own kernel, deterministic), "fused" (dK/dV kernel adds
 # f32 partial sums; tensor-core kernels only), "auto" (= separate)
@@ -103,12 +104,18 @@ class FwdCall:
                  kernel: str = "auto", num_ctas: int = 0, num_splits: int = 0,
                  prune_threshold: float = 0.0, out: torch.Tensor | None = None,
                  lse: torch.Tensor | None = None, workspace: torch.Tensor | None = None):
-        if q.dtype != k.dtype or q.dtype != v.dtype:
+        # fp8 (e4m3) queries and keys with a 16-bit v: the tensor-core kernel
+        # contracts the scores in fp8 (attn.h, qk_fp8)
+        qk_fp8 = q.dtype == _E4M3 and _E4M3 is not None
+        if qk_fp8:
+            if k.dtype != _E4M3:
+                raise TypeError("fp8 queries need fp8 (float8_e4m3fn) keys")
+        elif q.dtype != k.dtype or q.dtype != v.dtype:
             raise TypeError("q, k, v must share one dtype")
         dev = q.device
         Tq, H, D = q.shape
         Tk = k.shape[0]
-        out_dtype = out_dtype or q.dtype
+        out_dtype = out_dtype or v.dtype
         self.cu_q = _cu(cu_seqlens_q, dev)
         self.cu_k = _cu(cu_seqlens_k if cu_seqlens_k is not None else cu_seqlens_q, dev)
         self.o = out if out is not None else torch.empty((Tq, H, D), dtype=out_dtype, device=dev)
@@ -120,7 +127,8 @@ class FwdCall:
         a.n_q, a.n_k, a.H, a.D = Tq, Tk, H, D
         a.scale = float(scale) if scale is not None else D ** -0.5
         a.relation = ATTN_CAUSAL if causal else ATTN_FULL
-        a.dtype, a.o_dtype = _dtype_code(q.dtype), _dtype_code(self.o.dtype)
+        a.dtype, a.o_dtype = _dtype_code(v.dtype), _dtype_code(self.o.dtype)
+        a.qk_fp8 = 1 if qk_fp8 else 0
         a.n_seq = (self.cu_q.numel() - 1) if self.cu_q is not None else 1
         a.cu_seqlens_q = self.cu_q.data_ptr() if self.cu_q is not None else None
         a.cu_seqlens_k = self.cu_k.data_ptr() if self.cu_k is not None else None

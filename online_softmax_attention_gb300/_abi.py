@@ -12,7 +12,7 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_lib", "libattn_gb300.so")
 
-ABI_VERSION = 3
+ABI_VERSION = 4
 
 ATTN_OK, ATTN_EINVAL, ATTN_EUNSUPPORTED, ATTN_ECUDA, ATTN_ETIMEOUT, ATTN_EWORKSPACE = 0, -1, -2, -3, -4, -5
 ATTN_F16, ATTN_BF16, ATTN_F32 = 0, 1, 2
@@ -51,6 +51,7 @@ class FwdArgs(ctypes.Structure):
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("kernel", ctypes.c_int32), ("num_ctas", ctypes.c_int32), ("num_splits", ctypes.c_int32),
         ("prune_threshold", ctypes.c_float), ("pruned_tiles", ctypes.c_void_p),
+        ("qk_fp8", ctypes.c_int32),
     ]
 
 

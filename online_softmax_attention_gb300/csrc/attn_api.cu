@@ -69,12 +69,15 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 // A tensor view is usable when its pointer and row strides keep every
 // D-element row 16-byte aligned.
-bool valid_view(const attn_tensor &t, int dt, bool required) {
+bool valid_view_bytes(const attn_tensor &t, int64_t es, bool required) {
     if (!t.ptr) return !required;
-    const int64_t es = (int64_t)elem_size(dt);
     if (!aligned16(t.ptr)) return false;
     if (t.stride_tok <= 0 || t.stride_head <= 0) return false;
     return (t.stride_tok * es) % 16 == 0 && (t.stride_head * es) % 16 == 0;
+}
+
+bool valid_view(const attn_tensor &t, int dt, bool required) {
+    return valid_view_bytes(t, (int64_t)elem_size(dt), required);
 }
 
 // Which implementation runs: true = tcgen05 kernels.  `tc_ok` says whether
@@ -171,11 +174,18 @@ int plan_fwd(const attn_fwd_args *a, FwdParams &p, bool &use_tc) {
     // tile pruning is defined for the dense relation over one sequence, unsplit
     if (rho > 0.f && (a->relation != ATTN_FULL || a->cu_seqlens_q || a->num_splits > 1))
         return ATTN_EUNSUPPORTED;
+    if (a->qk_fp8 != 0 && a->qk_fp8 != 1) return ATTN_EINVAL;
+    // fp8 Q / K: tensor-core kernels, V (and P) 16-bit, D = 128, positive scale
+    if (a->qk_fp8 && (a->dtype == ATTN_F32 || a->D != 128 || !(a->scale > 0.f) ||
+                      a->kernel == ATTN_KERNEL_SIMT))
+        return ATTN_EUNSUPPORTED;
     const bool any_q = a->n_q > 0, any_k = a->n_k > 0;
-    if (!valid_view(a->q, a->dtype, any_q) || !valid_view(a->o, a->o_dtype, any_q) ||
-        !valid_view(a->k, a->dtype, any_k) || !valid_view(a->v, a->dtype, any_k))
+    const bool qk_ok = a->qk_fp8 ? valid_view_bytes(a->q, 1, any_q) && valid_view_bytes(a->k, 1, any_k)
+                                 : valid_view(a->q, a->dtype, any_q) && valid_view(a->k, a->dtype, any_k);
+    if (!qk_ok || !valid_view(a->o, a->o_dtype, any_q) || !valid_view(a->v, a->dtype, any_k))
         return ATTN_EINVAL;
     std::memset(&p, 0, sizeof(p));
+    p.qk_fp8 = a->qk_fp8;
     p.q = a->q.ptr; p.k = a->k.ptr; p.v = a->v.ptr; p.o = a->o.ptr; p.lse = a->lse;
     p.q_st = a->q.stride_tok; p.q_sh = a->q.stride_head;
     p.k_st = a->k.stride_tok; p.k_sh = a->k.stride_head;
@@ -191,6 +201,7 @@ int plan_fwd(const attn_fwd_args *a, FwdParams &p, bool &use_tc) {
     p.watchdog_cycles = watchdog_cycles();
     rc = choose_tc(a->kernel, tc_fwd_supported(p), use_tc);
     if (rc) return rc;
+    if (p.qk_fp8 && !use_tc) return ATTN_EUNSUPPORTED;  // no CUDA-core fp8 path
     p.prune = rho > 0.f;
     p.prune_log2 = p.prune ? std::log2(rho) : 0.f;
     p.pruned_tiles = reinterpret_cast<unsigned long long *>(a->pruned_tiles);

@@ -80,14 +80,23 @@ constexpr float kRescaleThreshold = 8.f;  // log2 units
 #define ATTN_FWD_EXP_FMA 0
 #endif
 
-template <int D>
+// kF8: Q and K are fp8 (e4m3), one byte per element (D = 128 only): their
+// tiles are 128 rows x 128 bytes, one 128-byte swizzled box, and the score
+// contraction is tcgen05.mma kind::f8f6f4 (K = 32 per instruction); V, P and U
+// keep the 16-bit / f32 path.
+template <int D, bool kF8 = false>
 struct Cfg {
-    static constexpr int kBoxes = D / 64;
-    static constexpr int kBoxBytes = 128 * 64 * 2;
-    static constexpr int kTileBytes = 128 * D * 2;
-    static constexpr int kKStages = D == 128 ? ATTN_FWD_KSTAGES_D128 : 4;
+    static_assert(!kF8 || D == 128, "fp8 Q/K: D = 128 only");
+    static constexpr int kBoxBytes = 128 * 128;            // one box: 128 rows x 128 bytes
+    static constexpr int kVBoxes = D / 64;                  // V: 64 16-bit columns per box
+    static constexpr int kVTileBytes = 128 * D * 2;
+    static constexpr int kQKBoxes = kF8 ? 1 : D / 64;       // Q / K boxes per tile
+    static constexpr int kQKBoxCols = kF8 ? 128 : 64;       // Q / K elements per box row
+    static constexpr int kQKTileBytes = kF8 ? 128 * D : kVTileBytes;
+    static constexpr int kSSteps = kF8 ? D / 32 : D / 16;   // score MMAs per tile
+    static constexpr int kKStages = kF8 ? 4 : (D == 128 ? ATTN_FWD_KSTAGES_D128 : 4);
     static constexpr int kVStages = D == 128 ? ATTN_FWD_VSTAGES_D128 : 4;
-    static constexpr int kSmemBytes = (NQT + kKStages + kVStages) * kTileBytes + 1024;
+    static constexpr int kSmemBytes = (NQT + kKStages) * kQKTileBytes + kVStages * kVTileBytes + 1024;
     static_assert(kSmemBytes + 1024 <= 232448, "shared memory budget (dynamic + static)");
     static constexpr int kRegsProducer = D == 128 ? 88 : 72;
     static constexpr int kRegsSoftmax = D == 128 ? 208 : 216;
@@ -178,24 +187,25 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long l
 
 // ---- warp 0: TMA producer ------------------------------------------------------
 
-template <int D>
+template <int D, bool kF8>
 __device__ void producer(const TcFwdArgs &a, FwdBars &bars, int *sched_item, uint32_t sQ, uint32_t sK,
                          uint32_t sV, const Watchdog &wd) {
-    using C = Cfg<D>;
+    using C = Cfg<D, kF8>;
     const FwdParams &p = a.p;
     const int total = p.sched.hdr[1];
     RingPos<C::kKStages> kr;
     RingPos<C::kVStages> vr;
     uint32_t q_uses[NQT] = {0, 0};
     bool q_pending[NQT] = {false, false};
+    // one K or V tile (tile_bytes in boxes of box_cols elements) into ring slot `slot`
     auto load_kv = [&](uint64_t *full, uint64_t *empty, uint32_t slot, uint32_t phase, uint32_t base,
-                       const CUtensorMap *tm, int row, int h) -> bool {
+                       const CUtensorMap *tm, int row, int h, int tile_bytes, int boxes,
+                       int box_cols) -> bool {
         if (!mbar_wait(smem_u32(&empty[slot]), phase ^ 1, wd)) return false;
         const uint32_t bar = smem_u32(&full[slot]);
-        mbar_expect_tx(bar, C::kTileBytes);
-#pragma unroll
-        for (int g = 0; g < C::kBoxes; ++g)
-            tma_load_3d(base + slot * C::kTileBytes + g * C::kBoxBytes, tm, 64 * g, row, h, bar);
+        mbar_expect_tx(bar, tile_bytes);
+        for (int g = 0; g < boxes; ++g)
+            tma_load_3d(base + slot * tile_bytes + g * C::kBoxBytes, tm, box_cols * g, row, h, bar);
         return true;
     };
     for (int i = 0;; ++i) {
@@ -214,10 +224,10 @@ __device__ void producer(const TcFwdArgs &a, FwdBars &bars, int *sched_item, uin
             ok = mbar_wait(smem_u32(&bars.q_empty[t]), (q_uses[t] & 1) ^ 1, wd);
             if (!ok) break;
             const uint32_t bar = smem_u32(&bars.q_full[t]);
-            mbar_expect_tx(bar, C::kTileBytes);
+            mbar_expect_tx(bar, C::kQKTileBytes);
 #pragma unroll
-            for (int g = 0; g < C::kBoxes; ++g)
-                tma_load_3d(sQ + t * C::kTileBytes + g * C::kBoxBytes, &a.tq, 64 * g,
+            for (int g = 0; g < C::kQKBoxes; ++g)
+                tma_load_3d(sQ + t * C::kQKTileBytes + g * C::kBoxBytes, &a.tq, C::kQKBoxCols * g,
                             f.q_start + f.row0 + BM * t, f.h, bar);
             ++q_uses[t];
             q_pending[t] = true;
@@ -225,10 +235,12 @@ __device__ void producer(const TcFwdArgs &a, FwdBars &bars, int *sched_item, uin
         if (!ok) break;
         for (int j = 0; j < f.nkv && ok; ++j) {
             const int krow = f.k_start + BN * (f.j0 + j);
-            ok = load_kv(bars.k_full, bars.k_empty, kr.slot(), kr.phase(), sK, &a.tk, krow, f.h);
+            ok = load_kv(bars.k_full, bars.k_empty, kr.slot(), kr.phase(), sK, &a.tk, krow, f.h,
+                         C::kQKTileBytes, C::kQKBoxes, C::kQKBoxCols);
             if (!ok) break;
             ++kr.i;
-            ok = load_kv(bars.v_full, bars.v_empty, vr.slot(), vr.phase(), sV, &a.tv, krow, f.h);
+            ok = load_kv(bars.v_full, bars.v_empty, vr.slot(), vr.phase(), sV, &a.tv, krow, f.h,
+                         C::kVTileBytes, C::kVBoxes, 64);
             if (!ok) break;
             ++vr.i;
         }
@@ -249,16 +261,17 @@ __device__ void producer(const TcFwdArgs &a, FwdBars &bars, int *sched_item, uin
 
 // ---- warp 1: MMA issuer ----------------------------------------------------------
 
-template <int D, bool kBF16>
+template <int D, bool kBF16, bool kF8>
 __device__ void mma_issuer(const TcFwdArgs &a, FwdBars &bars, const int *sched_item,
                            const PruneShared *ps, uint32_t sQ, uint32_t sK, uint32_t sV,
                            uint32_t tmem, const Watchdog &wd) {
-    using C = Cfg<D>;
+    using C = Cfg<D, kF8>;
     const FwdParams &p = a.p;
     const int total = p.sched.hdr[1];
     // a negative scale negates Q in the score MMA (A-negate bit), so the softmax
-    // always scales by |scale|
-    const uint32_t idS = idesc_f16(kBF16, BM, BN, 0) | (p.scale_log2 < 0.f ? (1u << 13) : 0u);
+    // always scales by |scale| (fp8 Q / K take positive scales only)
+    const uint32_t idS = kF8 ? idesc_f8(BM, BN)
+                             : idesc_f16(kBF16, BM, BN, 0) | (p.scale_log2 < 0.f ? (1u << 13) : 0u);
     constexpr uint32_t idO = idesc_f16(kBF16, BM, D, 1);
     uint32_t q_cnt[NQT] = {0, 0}, p_cnt[NQT] = {0, 0}, of_cnt[NQT] = {0, 0};
     RingPos<C::kKStages> kr;
@@ -269,21 +282,23 @@ __device__ void mma_issuer(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
     const uint64_t q_desc = sdesc_sw128(sQ, 16, 1024);
     const uint64_t k_desc = sdesc_sw128(sK, 16, 1024);
     const uint64_t v_desc = sdesc_sw128(sV, C::kBoxBytes, 1024);
-    // S_t = Q_t K^T over D in steps of 16 (32 bytes inside a 128-byte swizzle row)
+    // S_t = Q_t K^T over D in steps of 32 bytes inside a 128-byte swizzle row
+    // (16 elements of a 16-bit type, 32 fp8 elements)
     auto issue_s = [&](int t, uint32_t kslot) {  // K tile in slot `kslot` of the K ring
-        const uint64_t qa = q_desc + sdesc_step(t * C::kTileBytes);
-        const uint64_t ka = k_desc + sdesc_step(kslot * C::kTileBytes);
+        const uint64_t qa = q_desc + sdesc_step(t * C::kQKTileBytes);
+        const uint64_t ka = k_desc + sdesc_step(kslot * C::kQKTileBytes);
         const uint32_t d = tmem + BN * t;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < C::kSSteps; ++kk) {
             const uint64_t off = sdesc_step((kk >> 2) * C::kBoxBytes + (kk & 3) * 32);
-            mma_ss(d, qa + off, ka + off, idS, kk > 0);
+            if (kF8) mma_ss_f8(d, qa + off, ka + off, idS, kk > 0);
+            else mma_ss(d, qa + off, ka + off, idS, kk > 0);
         }
         tc_commit(smem_u32(&bars.s_full[t]));
     };
     // U_t (+)= P_t V over the 128 keys in steps of 16 (8 TMEM columns of P)
     auto issue_pv = [&](int t, uint32_t vslot, bool acc) {  // V tile in slot `vslot` of the V ring
-        const uint64_t va = v_desc + sdesc_step(vslot * C::kTileBytes);
+        const uint64_t va = v_desc + sdesc_step(vslot * C::kVTileBytes);
         const uint32_t d = tmem + 256 + D * t, pa = tmem + BN * t;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
@@ -528,9 +543,9 @@ __device__ void softmax_wg(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
     }
 }
 
-template <int D, bool kBF16, typename Tout>
+template <int D, bool kBF16, typename Tout, bool kF8>
 __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ TcFwdArgs a) {
-    using C = Cfg<D>;
+    using C = Cfg<D, kF8>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ FwdBars bars;
     __shared__ PruneShared prune_shared;
@@ -540,8 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sQ = (raw + 1023u) & ~1023u;
-    const uint32_t sK = sQ + NQT * C::kTileBytes;
-    const uint32_t sV = sK + C::kKStages * C::kTileBytes;
+    const uint32_t sK = sQ + NQT * C::kQKTileBytes;
+    const uint32_t sV = sK + C::kKStages * C::kQKTileBytes;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const Watchdog wd{a.p.watchdog_cycles, &abort_flag, a.p.status};
 
@@ -585,10 +600,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     if (warp < 4) {
         regs_dec<C::kRegsProducer>();
         if (warp == 0) {
-            if (lane == 0) producer<D>(a, bars, sched_item, sQ, sK, sV, wd);
+            if (lane == 0) producer<D, kF8>(a, bars, sched_item, sQ, sK, sV, wd);
         } else if (warp == 1) {
             if (lane == 0) {
-                mma_issuer<D, kBF16>(a, bars, sched_item, &prune_shared, sQ, sK, sV, tmem, wd);
+                mma_issuer<D, kBF16, kF8>(a, bars, sched_item, &prune_shared, sQ, sK, sV, tmem, wd);
                 if (aborting(wd)) {  // let issued MMAs finish before TMEM is freed
                     tc_commit(smem_u32(&bars.mma_drain));
                     drain_wait(smem_u32(&bars.mma_drain), 0, kDrainCycles);
@@ -610,10 +625,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 
 // ---- host side ------------------------------------------------------------------
 
-template <int D, bool kBF16, typename Tout>
+template <int D, bool kBF16, typename Tout, bool kF8>
 cudaError_t launch_typed(const TcFwdArgs &args, int num_ctas, cudaStream_t s) {
-    auto kern = fwd_tc_kernel<D, kBF16, Tout>;
-    const int smem = Cfg<D>::kSmemBytes;
+    auto kern = fwd_tc_kernel<D, kBF16, Tout, kF8>;
+    const int smem = Cfg<D, kF8>::kSmemBytes;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (num_ctas <= 0) num_ctas = sm_count();
@@ -622,15 +637,15 @@ cudaError_t launch_typed(const TcFwdArgs &args, int num_ctas, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool kF8>
 cudaError_t launch_d(const TcFwdArgs &args, int num_ctas, cudaStream_t s) {
     const FwdParams &p = args.p;
     if (p.dtype == ATTN_BF16) {
-        if (p.o_dtype == ATTN_F32) return launch_typed<D, true, float>(args, num_ctas, s);
-        return launch_typed<D, true, __nv_bfloat16>(args, num_ctas, s);
+        if (p.o_dtype == ATTN_F32) return launch_typed<D, true, float, kF8>(args, num_ctas, s);
+        return launch_typed<D, true, __nv_bfloat16, kF8>(args, num_ctas, s);
     }
-    if (p.o_dtype == ATTN_F32) return launch_typed<D, false, float>(args, num_ctas, s);
-    return launch_typed<D, false, __half>(args, num_ctas, s);
+    if (p.o_dtype == ATTN_F32) return launch_typed<D, false, float, kF8>(args, num_ctas, s);
+    return launch_typed<D, false, __half, kF8>(args, num_ctas, s);
 }
 
 }  // namespace
@@ -638,6 +653,7 @@ cudaError_t launch_d(const TcFwdArgs &args, int num_ctas, cudaStream_t s) {
 bool tc_fwd_supported(const FwdParams &p) {
     if (p.dtype != ATTN_F16 && p.dtype != ATTN_BF16) return false;
     if (p.D != 64 && p.D != 128) return false;
+    if (p.qk_fp8 && (p.D != 128 || !(p.scale_log2 > 0.f))) return false;
     if (p.n_q <= 0 || p.n_k <= 0) return false;
     return tc_device_ok();
 }
@@ -647,11 +663,13 @@ int tc_fwd_block_rows(const FwdParams &) { return kItemRows; }
 cudaError_t launch_fwd_tc(const FwdParams &p, int num_ctas, cudaStream_t s) {
     TcFwdArgs args;
     args.p = p;
-    if (!make_tile_map(&args.tq, p.q, p.dtype, p.D, p.n_q, p.H, p.q_st, p.q_sh) ||
-        !make_tile_map(&args.tk, p.k, p.dtype, p.D, p.n_k, p.H, p.k_st, p.k_sh) ||
+    const int qk_dtype = p.qk_fp8 ? kDtypeE4M3 : p.dtype;
+    if (!make_tile_map(&args.tq, p.q, qk_dtype, p.D, p.n_q, p.H, p.q_st, p.q_sh) ||
+        !make_tile_map(&args.tk, p.k, qk_dtype, p.D, p.n_k, p.H, p.k_st, p.k_sh) ||
         !make_tile_map(&args.tv, p.v, p.dtype, p.D, p.n_k, p.H, p.v_st, p.v_sh))
         return cudaErrorInvalidValue;
-    return p.D == 64 ? launch_d<64>(args, num_ctas, s) : launch_d<128>(args, num_ctas, s);
+    if (p.qk_fp8) return p.D == 128 ? launch_d<128, true>(args, num_ctas, s) : cudaErrorInvalidValue;
+    return p.D == 64 ? launch_d<64, false>(args, num_ctas, s) : launch_d<128, false>(args, num_ctas, s);
 }
 
 }  // namespace attn

@@ -28,6 +28,7 @@ struct FwdParams {
     float scale_log2;  // scale * log2(e)
     int causal;
     int dtype, o_dtype;
+    int qk_fp8;        // q and k are e4m3 (one byte per element); v is `dtype`
     int n_seq;
     const int32_t *cu_q, *cu_k;  // null => one sequence
     Sched sched;

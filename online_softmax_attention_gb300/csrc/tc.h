@@ -10,8 +10,12 @@ namespace attn {
 // True on an sm_103 device with the driver's tensor-map encoder available.
 bool tc_device_ok();
 
-// (tokens, heads, D) 16-bit tensor -> 3-D TMA map {D, tokens, heads} with a
-// {64, 128, 1} box and 128-byte swizzle.  False if the encoder rejects it.
+// Internal element-type code of fp8 (e4m3) Q / K tensors for make_tile_map.
+constexpr int kDtypeE4M3 = 16;
+
+// (tokens, heads, D) tensor -> 3-D TMA map {D, tokens, heads} with a box of 128
+// rows x 128 bytes ({64, 128, 1} elements for 16-bit types, {128, 128, 1} for
+// e4m3) and 128-byte swizzle.  False if the encoder rejects it.
 bool make_tile_map(CUtensorMap *m, const void *ptr, int dtype, int D, int tokens, int H,
                    int64_t stride_tok, int64_t stride_head);
 

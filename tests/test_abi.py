@@ -63,6 +63,7 @@ def _fwd_args(**kw):
     a.kernel = kw.get("kernel", _abi.ATTN_KERNEL_AUTO)
     a.num_splits = kw.get("num_splits", 0)
     a.prune_threshold = kw.get("prune", 0.0)
+    a.qk_fp8 = kw.get("qk_fp8", 0)
     lib = _abi.load()
     a.workspace = FAKE
     a.workspace_bytes = kw.get("ws", lib.attn_fwd_workspace_bytes(ctypes.byref(a)))
@@ -87,6 +88,10 @@ def _fwd_args(**kw):
     ({"num_splits": _abi.ATTN_MAX_SPLITS + 1}, _abi.ATTN_EINVAL),
     ({"kernel": 42}, None),
     ({"dtype": _abi.ATTN_F32, "kernel": _abi.ATTN_KERNEL_TC}, None),
+    ({"qk_fp8": 2}, _abi.ATTN_EINVAL),
+    ({"qk_fp8": 1}, _abi.ATTN_EUNSUPPORTED),                   # fp8 Q / K: D = 128 only
+    ({"qk_fp8": 1, "D": 128, "dtype": _abi.ATTN_F32}, _abi.ATTN_EUNSUPPORTED),  # v 16-bit
+    ({"qk_fp8": 1, "D": 128, "kernel": _abi.ATTN_KERNEL_SIMT}, _abi.ATTN_EUNSUPPORTED),
 ])
 def test_forward_argument_validation(kw, code):
     lib = _abi.load()
