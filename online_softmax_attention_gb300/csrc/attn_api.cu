@@ -3,6 +3,7 @@
 // contract of each entry point.
 #include <atomic>
 #include <cmath>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -58,6 +59,19 @@ long long watchdog_cycles() {
     const long long x = e ? std::atoll(e) : 0;
     return x > 0 ? x : kDefaultWatchdog;
 }
+
+// ATTN_LOG=1 in the environment: one line on stderr per forward / backward
+// call naming the schedule the library chose (kernel family, key splits, dq
+// mode).  Off by default.
+bool log_on() {
+    static const bool on = [] {
+        const char *e = std::getenv("ATTN_LOG");
+        return e && std::atoi(e) > 0;
+    }();
+    return on;
+}
+
+const char *dtype_name(int dt) { return dt == ATTN_F16 ? "f16" : dt == ATTN_BF16 ? "bf16" : "f32"; }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -394,6 +408,13 @@ int attn_fwd(const attn_fwd_args *a, void *stream) {
     int rc = build_fwd(a, p, use_tc);
     if (rc) return rc;
     if (a->n_q == 0) return ATTN_OK;
+    if (log_on())
+        std::fprintf(stderr,
+                     "[attn] fwd n_q=%d n_k=%d H=%d D=%d n_seq=%d relation=%s dtype=%s%s o_dtype=%s "
+                     "kernel=%s splits=%d prune=%g\n",
+                     a->n_q, a->n_k, a->H, a->D, a->n_seq, p.causal ? "causal" : "full",
+                     p.qk_fp8 ? "e4m3+" : "", dtype_name(a->dtype), dtype_name(a->o_dtype),
+                     use_tc ? "tc" : "simt", p.n_splits, (double)a->prune_threshold);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int block = use_tc ? tc_fwd_block_rows(p) : kSimtBlock;
     cudaError_t e = launch_prep(p.cu_q, p.cu_k, p.n_seq, p.n_q, p.n_k, p.H, block, p.causal, 0,
@@ -495,6 +516,17 @@ int attn_bwd_dq(const attn_bwd_args *a, void *stream) {
 }
 
 int attn_bwd(const attn_bwd_args *a, void *stream) {
+    if (log_on()) {
+        BwdParams p;
+        bool use_tc = false;
+        if (build_bwd(a, p, use_tc) == ATTN_OK)
+            std::fprintf(stderr,
+                         "[attn] bwd n_q=%d n_k=%d H=%d D=%d n_seq=%d relation=%s dtype=%s "
+                         "grad_dtype=%s kernel=%s dq=%s\n",
+                         a->n_q, a->n_k, a->H, a->D, a->n_seq, p.causal ? "causal" : "full",
+                         dtype_name(a->dtype), dtype_name(a->grad_dtype), use_tc ? "tc" : "simt",
+                         p.dq_accum ? "fused" : "separate");
+    }
     int rc = attn_bwd_preprocess(a, stream);
     if (rc) return rc;
     rc = attn_bwd_dkdv(a, stream);

@@ -88,3 +88,23 @@ def test_unsupported_combinations_fail_closed():
         _run(x, causal=False, kernel="simt")
     with pytest.raises(attn.AttnError):  # negative scale
         _run(x, causal=False, scale=-0.1)
+
+
+@pytest.mark.parametrize("seed,rho", [(501, 0.5), (502, 0.1)])
+def test_tile_pruning(seed, rho):
+    """The approximate tile-pruned forward on fp8 queries and keys: decisions
+    (checked decisive on the oracle, margin > 0.01 in log units) and results
+    equal the oracle's pruned forward with the kernel's 128 x 128 tiles."""
+    x = attn_inputs.make(dtype="bf16", H=2, D=128, seed=seed, lengths=[1000], lengths_k=[1500],
+                         key_gain=(128, 0.2, 3.0), qk_fp8=True)
+    o_ref, lse_ref, n_ref, margin = oracle.fwd_pruned(x["q"], x["k"], x["v"], rho=rho,
+                                                      block_q=128, block_k=128)
+    assert margin > 0.01 and n_ref > 0
+    q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
+    call = attn.FwdCall(q, k, v, causal=False, prune_threshold=rho, out_dtype=torch.float32)
+    o, lse = call.run()
+    torch.cuda.synchronize()
+    assert attn.device_status() == 0
+    assert call.pruned_count() == n_ref
+    check_o(o, o_ref, torch.bfloat16, o.dtype)
+    check_lse(lse, lse_ref)
