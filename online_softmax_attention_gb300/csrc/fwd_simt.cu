@@ -30,9 +30,41 @@ constexpr int BK = 64;          // keys per tile
 constexpr int NT = 256;
 constexpr int LDP = BK + 4;
 
-template <int D>
+// f32 inputs at D = 64 stage K and V with cp.async into two alternating
+// buffers, so the next key tile's loads overlap this tile's arithmetic (two
+// CTAs per SM still fit); other cases stage synchronously through registers.
+template <typename Tin, int D>
+constexpr bool kAsyncKV = sizeof(Tin) == 4 && D == 64;
+
+template <typename Tin, int D>
 constexpr size_t fwd_smem_bytes() {
-    return sizeof(float) * (size_t)(BQ * (D + 4) + 2 * BK * (D + 4) + BQ * LDP);
+    return sizeof(float) * (size_t)(BQ * (D + 4) + (kAsyncKV<Tin, D> ? 4 : 2) * BK * (D + 4) + BQ * LDP);
+}
+
+// Start copying rows [row0, row0 + 64) of an f32 (tokens, heads, D) tensor
+// into shared memory (16-byte cp.async per chunk; rows at or beyond `nrows`
+// are zero-filled without reading global memory).
+template <int D>
+__device__ __forceinline__ void stage_tile_async(float *dst, const float *src, int64_t st, int row0,
+                                                 int nrows) {
+    constexpr int LD = D + 4;
+    constexpr int CPR = D / 4;
+    for (int c = threadIdx.x; c < 64 * CPR; c += NT) {
+        const int r = c / CPR, cc = c - r * CPR;
+        const bool in = row0 + r < nrows;
+        const float *g = in ? src + (int64_t)(row0 + r) * st + cc * 4 : src;
+        const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(dst + r * LD + cc * 4));
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sa), "l"(g), "r"(in ? 16 : 0)
+                     : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Wait until at most `n` (0 or 2: the next tile's K and V groups) of this
+// thread's cp.async groups are still pending.
+__device__ __forceinline__ void cp_async_wait_all_but(int n) {
+    if (n == 0) asm volatile("cp.async.wait_group 0;" ::: "memory");
+    else asm volatile("cp.async.wait_group 2;" ::: "memory");
 }
 
 // Stage rows [row0, row0 + 64) of a (tokens, heads, D) tensor into shared
@@ -54,11 +86,12 @@ template <typename Tin, typename Tout, int D>
 __global__ void __launch_bounds__(NT) fwd_simt_kernel(const FwdParams p) {
     constexpr int LD = D + 4;
     constexpr int NG = D / 64;  // column groups of 64 per thread row
+    constexpr bool kAsync = kAsyncKV<Tin, D>;
     extern __shared__ float4 smem4[];
     float *sQ = reinterpret_cast<float *>(smem4);
-    float *sK = sQ + BQ * LD;
-    float *sV = sK + BK * LD;
-    float *sP = sV + BK * LD;
+    float *sKb = sQ + BQ * LD;                        // K buffer(s), then V buffer(s)
+    float *sVb = sKb + (kAsync ? 2 : 1) * BK * LD;
+    float *sP = sVb + (kAsync ? 2 : 1) * BK * LD;
     __shared__ int s_w;
     __shared__ float s_tile_max[NT / 32];  // tile pruning: per-warp largest score
 
@@ -99,11 +132,32 @@ __global__ void __launch_bounds__(NT) fwd_simt_kernel(const FwdParams p) {
         const Tin *kbase = gk + (int64_t)k_start * p.k_st + (int64_t)h * p.k_sh;
         const Tin *vbase = gv + (int64_t)k_start * p.v_st + (int64_t)h * p.v_sh;
 
+        if constexpr (kAsync) {
+            if (chunk.begin < chunk.end) {
+                __syncthreads();  // the previous item's last tile is no longer read
+                stage_tile_async<D>(sKb, reinterpret_cast<const float *>(kbase), p.k_st, chunk.begin * BK, Lk);
+                stage_tile_async<D>(sVb, reinterpret_cast<const float *>(vbase), p.v_st, chunk.begin * BK, Lk);
+            }
+        }
         for (int kt = chunk.begin; kt < chunk.end; ++kt) {
             const int key0 = kt * BK;
             __syncthreads();  // previous tile's sK / sV / sP no longer read
-            stage_tile<Tin, D>(sK, kbase, p.k_st, key0, Lk);
-            stage_tile<Tin, D>(sV, vbase, p.v_st, key0, Lk);
+            float *sK = sKb, *sV = sVb;
+            if constexpr (kAsync) {
+                const int buf = (kt - chunk.begin) & 1;
+                sK = sKb + buf * BK * LD;
+                sV = sVb + buf * BK * LD;
+                const bool more = kt + 1 < chunk.end;
+                if (more) {  // the next tile into the other buffer, read two iterations ago
+                    float *nK = sKb + (buf ^ 1) * BK * LD, *nV = sVb + (buf ^ 1) * BK * LD;
+                    stage_tile_async<D>(nK, reinterpret_cast<const float *>(kbase), p.k_st, key0 + BK, Lk);
+                    stage_tile_async<D>(nV, reinterpret_cast<const float *>(vbase), p.v_st, key0 + BK, Lk);
+                }
+                cp_async_wait_all_but(more ? 2 : 0);  // this tile's two groups have landed
+            } else {
+                stage_tile<Tin, D>(sK, kbase, p.k_st, key0, Lk);
+                stage_tile<Tin, D>(sV, vbase, p.v_st, key0, Lk);
+            }
             __syncthreads();
 
             // score micro-tile: rows ty + 16 r, keys tx + 16 c
@@ -239,7 +293,7 @@ __global__ void __launch_bounds__(NT) fwd_simt_kernel(const FwdParams p) {
 template <typename Tin, typename Tout, int D>
 cudaError_t launch_typed(const FwdParams &p, int num_ctas, cudaStream_t s, int *per_sm_out) {
     auto kern = fwd_simt_kernel<Tin, Tout, D>;
-    const size_t smem = fwd_smem_bytes<D>();
+    const size_t smem = fwd_smem_bytes<Tin, D>();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (num_ctas <= 0) {
