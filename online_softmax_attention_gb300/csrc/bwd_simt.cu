@@ -87,26 +87,59 @@ __device__ __forceinline__ void tile_nt(float (&acc)[4][4], const float *A, cons
 
 // ---- preprocess: Dr = rowsum(dO * O), and lse in the base-2 domain ----------
 
+constexpr int kRowDotRows = 4;  // rows per warp with loads in flight at once
+
+// One warp per row r = t * H + h (token t, head h); each pass of a warp issues
+// the loads of kRowDotRows rows before reducing any, so that enough bytes are
+// in flight per SM to cover the HBM latency.  Rows are numbered in int64
+// (n_q * H * 32 threads can exceed 2^32); a warp's rows are nwarps apart, so
+// (t, h) advance by a fixed step without a division per row.
 template <typename Tin, typename To, int D>
 __global__ void __launch_bounds__(256) row_dot_kernel(const BwdParams p) {
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    static_assert(D <= 128, "one 4-column chunk per lane");
+    constexpr int U = kRowDotRows;
     const int lane = threadIdx.x & 31;
-    if (warp >= p.n_q * p.H) return;
-    const int t = warp / p.H, h = warp - t * p.H;
-    const Tin *dO = static_cast<const Tin *>(p.dout) + (int64_t)t * p.do_st + (int64_t)h * p.do_sh;
-    const To *O = static_cast<const To *>(p.o) + (int64_t)t * p.o_st + (int64_t)h * p.o_sh;
-    float acc = 0.f;
-    for (int d = lane * 4; d < D; d += 128) {
-        const float4 a = load4(dO + d), b = load4(O + d);
-        acc += a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
-    }
+    const int64_t rows = (int64_t)p.n_q * p.H;
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t r_first = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t step_t = nwarps / p.H;
+    const int step_h = (int)(nwarps - step_t * p.H);
+    int64_t t = r_first / p.H;
+    int h = (int)(r_first - t * p.H);
+    const int d = 4 * lane;  // lanes past D idle
+    for (int64_t r0 = r_first; r0 < rows; r0 += U * nwarps) {
+        // all loads of the pass (lse included) are issued before any store
+        float4 a[U], b[U];
+        float x[U];
+        int64_t at[U];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) {
-        const int64_t at = (int64_t)h * p.n_q + t;
-        p.dr[at] = acc;
-        const float x = p.lse[at];
-        p.lse2[at] = x == -INFINITY ? INFINITY : x * kLog2e;
+        for (int u = 0; u < U; ++u) {
+            const bool live = r0 + u * nwarps < rows;
+            at[u] = (int64_t)h * p.n_q + t;
+            a[u] = b[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            x[u] = 0.f;
+            if (live && d < D) {
+                a[u] = load4(static_cast<const Tin *>(p.dout) + t * p.do_st + (int64_t)h * p.do_sh + d);
+                b[u] = load4(static_cast<const To *>(p.o) + t * p.o_st + (int64_t)h * p.o_sh + d);
+            }
+            if (live && lane == 0) x[u] = __ldg(p.lse + at[u]);
+            t += step_t;
+            h += step_h;
+            if (h >= p.H) {
+                h -= p.H;
+                ++t;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            float acc = a[u].x * b[u].x + a[u].y * b[u].y + a[u].z * b[u].z + a[u].w * b[u].w;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if (lane == 0 && r0 + u * nwarps < rows) {
+                p.dr[at[u]] = acc;
+                p.lse2[at[u]] = x[u] == -INFINITY ? INFINITY : x[u] * kLog2e;
+            }
+        }
     }
 }
 
@@ -399,9 +432,12 @@ cudaError_t bwd_d(const BwdParams &p, int num_ctas, cudaStream_t s, bool dkdv) {
 
 template <typename Tin, typename To, int D>
 cudaError_t row_dot_typed(const BwdParams &p, cudaStream_t s) {
-    const int64_t warps = (int64_t)p.n_q * p.H;
-    const int blocks = (int)((warps * 32 + 255) / 256);
-    row_dot_kernel<Tin, To, D><<<blocks, 256, 0, s>>>(p);
+    const int64_t rows = (int64_t)p.n_q * p.H;
+    if (rows == 0) return cudaSuccess;
+    // 8 warps per block, kRowDotRows rows per warp and pass; at most 8 blocks per SM
+    const int64_t want = (rows + 8 * kRowDotRows - 1) / (8 * kRowDotRows);
+    const int64_t cap = 8LL * sm_count();
+    row_dot_kernel<Tin, To, D><<<(int)(want < cap ? want : cap), 256, 0, s>>>(p);
     count_launch();
     return cudaGetLastError();
 }
