@@ -43,6 +43,8 @@
 // Every mbarrier wait is bounded (sm100::mbar_wait); on expiry the CTA stops
 // issuing work, drains its outstanding TMA loads, frees TMEM and exits, and
 // the status word reads ATTN_ETIMEOUT.
+#include <cfloat>
+
 #include "sm100.cuh"
 #include "tc.h"
 
@@ -384,8 +386,11 @@ __device__ void softmax_wg(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
     const int lrow = 32 * quarter + lane;
     const uint32_t s_addr = tmem_addr(tmem, 32 * quarter, BN * t);
     const uint32_t o_addr = tmem_addr(tmem, 32 * quarter, 256 + D * t);
-    // the score MMA negated S when the scale is negative
-    const float sl2 = fabsf(p.scale_log2);
+    // the score MMA negated S when the scale is negative.  Masked scores are -inf
+    // before the scale multiplies them; a zero scale is raised to the smallest
+    // normal f32 so that they stay -inf (not NaN) while every admitted score
+    // still scales to 0 within f32 rounding
+    const float sl2 = fmaxf(fabsf(p.scale_log2), FLT_MIN);
     uint32_t s_cnt = 0, o_cnt = 0, tm_cnt = 0;
     Tout *go = static_cast<Tout *>(p.o);
 

@@ -1,5 +1,6 @@
 """Backward parity: CUDA dq, dk, dv (through the C ABI) vs the oracle's
 explicit-Jacobian backward, on seeded inputs spanning tiles and ragged tails."""
+import numpy as np
 import pytest
 import torch
 
@@ -147,3 +148,19 @@ def test_tc_backward_matches_simt_closely():
     for u, v in zip(a, b):
         rel = float((u - v).norm() / v.norm())
         assert rel < 5e-3, rel
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_zero_scale(kernel):
+    """scale = 0: P is uniform over the admitted keys, dq = dk = 0."""
+    x = attn_inputs.make(dtype="bf16", H=2, D=128, seed=48, lengths=[300, 1, 129], backward=True)
+    got = _fwd_bwd(x, causal=True, kernel=kernel, scale=0.0)
+    _check(got, _ref(x, causal=True, scale=0.0))
+    assert float(got[0].abs().max()) == 0.0 and float(got[1].abs().max()) == 0.0
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_many_short_sequences(kernel):
+    lengths = np.random.default_rng(49).integers(0, 5, 20000).tolist()
+    x = attn_inputs.make(dtype="fp16", H=2, D=64, seed=49, lengths=lengths, backward=True)
+    _check(_fwd_bwd(x, causal=True, kernel=kernel), _ref(x, causal=True))

@@ -177,3 +177,34 @@ def test_tc_matches_simt_closely(dtype, D):
     o2, l2 = _run(x, causal=True, kernel="simt", out_dtype=torch.float32)
     assert (o1 - o2).abs().max().item() < 1e-2
     assert (l1 - l2).abs().max().item() < 1e-4
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("dtype,D", [("fp16", 64), ("bf16", 128), ("f32", 64)])
+@pytest.mark.parametrize("splits", [1, 3])
+def test_zero_scale_is_uniform_attention(kernel, dtype, D, splits):
+    """scale = 0: every admitted score is 0, so O is the mean of the admitted
+    values and lse = ln(count); masked keys (causal diagonal, ragged tails)
+    must still weigh nothing."""
+    _skip_unsupported(kernel, dtype)
+    x = attn_inputs.make(dtype=dtype, H=2, D=D, seed=23, lengths=[300, 1, 129])
+    q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
+    o, lse = attn.fwd(q, k, v, causal=True, scale=0.0, cu_seqlens_q=x["cu_seqlens_q"],
+                      out_dtype=_out_dtype(dtype), kernel=kernel, num_splits=splits)
+    torch.cuda.synchronize()
+    assert attn.device_status() == 0
+    o_ref, lse_ref = _ref(x, causal=True, scale=0.0)
+    check_o(o, o_ref, x["q"].dtype, o.dtype)
+    check_lse(lse, lse_ref)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_many_short_sequences(kernel):
+    """20000 sequences of 0 to 4 tokens: the schedule's prefix over many
+    sequences, empty ones among them, and one partial tile per sequence."""
+    lengths = np.random.default_rng(24).integers(0, 5, 20000).tolist()
+    x = attn_inputs.make(dtype="fp16", H=2, D=64, seed=24, lengths=lengths)
+    o, lse = _run(x, causal=True, kernel=kernel)
+    o_ref, lse_ref = _ref(x, causal=True)
+    check_o(o, o_ref, x["q"].dtype, o.dtype)
+    check_lse(lse, lse_ref)

@@ -67,6 +67,28 @@ def test_hand_cases_backward(case):
 
 # --- closed forms and invariants -----------------------------------------------
 
+def test_zero_scale_is_the_uniform_average():
+    """scale = 0 makes every admitted score 0: O_i is the plain mean of the
+    admitted values, lse_i = ln |A_i|, dq = dk = 0 and dv_j is the sum of
+    dO_i / |A_i| over the rows that admit key j (causal, two segments)."""
+    lengths = [5, 3]
+    cu = [0, 5, 8]
+    H, D = 2, 3
+    q, k, v, dO = (_rand((8, H, D), s) for s in (61, 62, 63, 64))
+    o, lse = oracle.fwd(q, k, v, causal=True, scale=0.0, cu_seqlens_q=cu)
+    dq, dk, dv = oracle.bwd(q, k, v, dO, causal=True, scale=0.0, cu_seqlens_q=cu)
+    dv_ref = np.zeros_like(v)
+    for b, L in enumerate(lengths):
+        s0 = cu[b]
+        for i in range(L):
+            n = i + 1  # keys 0..i of the segment
+            np.testing.assert_allclose(o[s0 + i], v[s0:s0 + n].mean(axis=0), rtol=0, atol=1e-14)
+            np.testing.assert_allclose(lse[:, s0 + i], math.log(n), rtol=0, atol=1e-14)
+            dv_ref[s0:s0 + n] += dO[s0 + i] / n
+    assert not dq.any() and not dk.any()
+    np.testing.assert_allclose(dv, dv_ref, rtol=0, atol=1e-13)
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_identical_keys_give_mean_of_admitted_values(causal):
     T, H, D = 37, 3, 8
