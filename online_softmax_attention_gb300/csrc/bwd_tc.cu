@@ -83,18 +83,6 @@ struct TcBwdArgs {
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
-__device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
-    uint32_t u;
-    if (bf16) {
-        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-        u = *reinterpret_cast<uint32_t *>(&v);
-    } else {
-        __half2 v = __floats2half2_rn(lo, hi);
-        u = *reinterpret_cast<uint32_t *>(&v);
-    }
-    return u;
-}
-
 constexpr long long kDrainCycles = 1ll << 31;  // post-abort wait for TMA loads in flight
 
 // The dq kernel's elementwise warps are on its critical path and bound by the
@@ -143,14 +131,6 @@ __device__ __forceinline__ bool sched_take_warp(SchedRing &r, int i, int &w, con
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&r.empty[slot]));
     return true;
-}
-
-template <typename T>
-__device__ __forceinline__ void store_row32(T *dst, const uint32_t (&u)[32], float mul) {
-#pragma unroll
-    for (int e = 0; e < 32; e += 4)
-        store4(dst + e, make_float4(__uint_as_float(u[e]) * mul, __uint_as_float(u[e + 1]) * mul,
-                                    __uint_as_float(u[e + 2]) * mul, __uint_as_float(u[e + 3]) * mul));
 }
 
 template <typename T>
@@ -595,12 +575,16 @@ __device__ void dkdv_elementwise(const TcBwdArgs &a, DkdvBars &bars, float *stat
         if (!__all_sync(0xffffffffu, ok)) return;
         tc_fence_after();
         const float mul = wg == 0 ? 1.f : p.scale;
+        // the warp's 32 key rows: the first one's address, and how many exist
+        const int64_t gst = wg == 0 ? p.dv_st : p.dk_st;
+        Tg *wrow0 = dst - (int64_t)lane * gst;
+        const int rows_live = min(32, max(0, f.Lk - (f.key0 + 32 * quarter)));
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
             uint32_t u[32];
             tmem_ld_x32(lane_base + 256 + D * wg + 32 * c, u);
             tmem_ld_wait(u);
-            if (live) store_row32(dst + 32 * c, u, mul);
+            store_rows_chunk(u, mul, wrow0 + 32 * c, gst, rows_live, lane);
         }
         tc_fence_before();
         mbar_arrive_warp(smem_u32(&bars.acc_free));
@@ -764,12 +748,16 @@ __device__ void dkdvq_elementwise(const TcBwdArgs &a, DkdvBars &bars, float *sta
         if (!__all_sync(0xffffffffu, ok)) return;
         tc_fence_after();
         const float mul = wg == 0 ? 1.f : p.scale;
+        // the warp's 32 key rows: the first one's address, and how many exist
+        const int64_t gst = wg == 0 ? p.dv_st : p.dk_st;
+        Tg *wrow0 = dst - (int64_t)lane * gst;
+        const int rows_live = min(32, max(0, f.Lk - (f.key0 + 32 * quarter)));
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
             uint32_t u[32];
             tmem_ld_x32(lane_base + 256 + D * wg + 32 * c, u);
             tmem_ld_wait(u);
-            if (live) store_row32(dst + 32 * c, u, mul);
+            store_rows_chunk(u, mul, wrow0 + 32 * c, gst, rows_live, lane);
         }
         tc_fence_before();
         mbar_arrive_warp(smem_u32(&bars.acc_free));
@@ -1106,12 +1094,15 @@ __device__ void dq_elementwise(const TcBwdArgs &a, DqBars &bars, uint32_t tmem, 
         ++ad_cnt;
         if (!__all_sync(0xffffffffu, ok)) return;
         tc_fence_after();
+        // the warp's 32 query rows: the first one's address, and how many exist
+        Tg *wrow0 = dst - (int64_t)lane * p.dq_st;
+        const int rows_live = min(32, max(0, f.Lq - (f.row0 + 32 * quarter)));
 #pragma unroll 1
         for (int c = 0; c < D / 64; ++c) {
             uint32_t u[32];
             tmem_ld_x32(lane_base + 384 + (D / 2) * wg + 32 * c, u);
             tmem_ld_wait(u);
-            if (live) store_row32(dst + 32 * c, u, p.scale);
+            store_rows_chunk(u, p.scale, wrow0 + 32 * c, p.dq_st, rows_live, lane);
         }
         tc_fence_before();
         mbar_arrive_warp(smem_u32(&bars.acc_free));

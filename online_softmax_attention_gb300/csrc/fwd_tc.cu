@@ -166,18 +166,6 @@ __device__ __forceinline__ ItemInfo item_info(const FwdParams &p, int w) {
     return f;
 }
 
-__device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
-    uint32_t u;
-    if (bf16) {
-        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-        u = *reinterpret_cast<uint32_t *>(&v);
-    } else {
-        __half2 v = __floats2half2_rn(lo, hi);
-        u = *reinterpret_cast<uint32_t *>(&v);
-    }
-    return u;
-}
-
 // Bounded wait for outstanding TMA writes before the CTA exits after an abort.
 constexpr long long kDrainCycles = 1ll << 31;
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long long budget) {
@@ -529,18 +517,16 @@ __device__ void softmax_wg(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
         tc_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
         const bool live = row < f.Lq;
+        // the warp's 32 rows: the first one's address, and how many exist
+        Tout *wrow0 = go + f.c * p.o_split_st + (int64_t)(f.q_start + r0 + 32 * quarter) * p.o_st +
+                      (int64_t)f.h * p.o_sh;
+        const int rows_live = min(32, max(0, f.Lq - (r0 + 32 * quarter)));
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
             uint32_t u[32];
             tmem_ld_x32(o_addr + 32 * c, u);
             tmem_ld_wait(u);
-            if (live) {
-#pragma unroll
-                for (int e = 0; e < 32; e += 4)
-                    store4(orow + 32 * c + e,
-                           make_float4(__uint_as_float(u[e]) * inv, __uint_as_float(u[e + 1]) * inv,
-                                       __uint_as_float(u[e + 2]) * inv, __uint_as_float(u[e + 3]) * inv));
-            }
+            store_rows_chunk(u, inv, wrow0 + 32 * c, p.o_st, rows_live, lane);
         }
         if (live && lse_at) *lse_at = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
         tc_fence_before();

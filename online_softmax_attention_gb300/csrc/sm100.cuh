@@ -1,6 +1,7 @@
 // Inline-PTX wrappers for the sm_100-family (sm_103a) features the
 // tensor-core attention kernels use: mbarriers, TMA tile loads, and the
-// tcgen05 tensor-memory (TMEM) allocator, MMA, commit, loads and stores.
+// tcgen05 tensor-memory (TMEM) allocator, MMA, commit, loads and stores; and
+// the epilogue store of accumulator rows held one row per lane.
 //
 // Every mbarrier wait is bounded: after `budget` clock cycles it raises the
 // CTA's abort flag, records ATTN_ETIMEOUT in the device status word and
@@ -9,6 +10,8 @@
 
 #include <cuda.h>
 #include <stdint.h>
+
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -327,6 +330,96 @@ __device__ __forceinline__ void tmem_st_wait() {
 // TMEM address of (lane, column) relative to an allocation base.
 __device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t lane, uint32_t col) {
     return base + (lane << 16) + col;
+}
+
+// ---- 16-bit packing and row-per-lane stores ---------------------------------------
+
+// Two f32 values rounded to nearest even as one packed 16-bit pair (lo first).
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
+    uint32_t u;
+    if (bf16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        u = *reinterpret_cast<uint32_t *>(&v);
+    } else {
+        __half2 v = __floats2half2_rn(lo, hi);
+        u = *reinterpret_cast<uint32_t *>(&v);
+    }
+    return u;
+}
+
+__device__ __forceinline__ void st_piece(float *p, const uint32_t (&w)[8]) {  // 32-byte aligned
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+template <typename T16>
+__device__ __forceinline__ void st_piece(T16 *p, const uint32_t (&w)[4]) {  // 16-byte aligned
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                 "r"(w[3])
+                 : "memory");
+}
+
+// A warp that read 32 rows of a TMEM accumulator with tcgen05.ld 32x32b holds one
+// row per lane, so plain stores would write a few bytes of 32 different rows per
+// instruction.  This stores one 32-column chunk of those rows (u: the lane's row
+// as f32 bits; each value times `mul`, rounded to T) by cutting it into four
+// 8-column pieces that the lanes of each group of four exchange, a 4 x 4
+// transpose by xor shuffles: afterwards lane 4g + j holds piece j of rows
+// 4g .. 4g + 3, and each store instruction writes eight rows' whole chunks, four
+// lanes per row (128 contiguous bytes for f32, 64 for 16-bit types).
+//   row0: the warp's first row at the chunk's first column; st: row stride in
+//   elements; rows_live: how many of the 32 rows exist (the rest are not
+//   written).  All 32 lanes must call it.  f32 pieces are 32-byte stores, so
+//   f32 rows that are not 32-byte aligned are written one lane per row instead.
+template <typename T>
+__device__ __forceinline__ void store_rows_chunk(uint32_t (&u)[32], float mul, T *row0, int64_t st,
+                                                 int rows_live, int lane) {
+    constexpr int W = sizeof(T) == 4 ? 8 : 4;  // 32-bit words per 8 values
+    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * mul);
+    const bool wide = sizeof(T) < 4 || ((reinterpret_cast<uintptr_t>(row0) & 31) == 0 &&
+                                        ((st * (int64_t)sizeof(T)) & 31) == 0);
+    if (!wide) {  // the same for every lane of the warp
+        if (lane < rows_live) {
+            T *dst = row0 + (int64_t)lane * st;
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+                store4(dst + e, make_float4(__uint_as_float(u[e]), __uint_as_float(u[e + 1]),
+                                            __uint_as_float(u[e + 2]), __uint_as_float(u[e + 3])));
+        }
+        return;
+    }
+    uint32_t w[4][W];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+        for (int i = 0; i < W; ++i)
+            w[k][i] = W == 8 ? u[8 * k + i]
+                             : pack2(__uint_as_float(u[8 * k + 2 * i]), __uint_as_float(u[8 * k + 2 * i + 1]),
+                                     kBf16);
+    const int gl = lane & 3;
+#pragma unroll
+    for (int d = 1; d <= 2; d <<= 1) {
+        const bool upper = (gl & d) != 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (k & d) continue;
+            // the lower lane keeps piece k and sends k | d; the upper keeps k | d and sends k
+#pragma unroll
+            for (int i = 0; i < W; ++i) {
+                const uint32_t send = upper ? w[k][i] : w[k | d][i];
+                const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, d);
+                if (upper) w[k][i] = recv;
+                else w[k | d][i] = recv;
+            }
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int r = (lane & ~3) + k;
+        if (r < rows_live) st_piece(row0 + (int64_t)r * st + 8 * gl, w[k]);
+    }
 }
 
 }  // namespace sm100
