@@ -863,7 +863,7 @@ __device__ __forceinline__ DqInfo dq_info(const BwdParams &p, int w) {
 
 struct __align__(8) DqBars {
     uint64_t q_full, q_empty;
-    uint64_t k_full[8], k_empty[8], v_full[8], v_empty[8];
+    uint64_t k_full[8], k_empty[8], v_empty[8];  // k_full: the K and V tiles of a key block
     uint64_t sp_full, sp_free, ds_ready, acc_done, acc_free;
     uint64_t mma_drain;  // abort path: completion of the MMAs already issued
     SchedRing sched;
@@ -879,15 +879,21 @@ __device__ void dq_producer(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint3
     RingPos<C::kDqKStages> kr;
     RingPos<C::kDqVStages> vr;
     bool q_pending = false;
-    // load one K or V tile of key block j into its ring
-    auto load_kv = [&](uint64_t *full, uint64_t *empty, uint32_t slot, uint32_t phase, uint32_t base,
-                       const CUtensorMap *tm, const DqInfo &f, int j) -> bool {
-        if (!mbar_wait(smem_u32(&empty[slot]), phase ^ 1, wd)) return false;
-        const uint32_t bar = smem_u32(&full[slot]);
-        mbar_expect_tx(bar, C::kTileBytes);
+    // load the K and V tiles of key block j into their rings; both land on the
+    // K slot's full barrier, so the MMA issuer waits once per key block
+    auto load_kv = [&](const DqInfo &f, int j) -> bool {
+        const uint32_t ks = kr.slot(), vs = vr.slot();
+        if (!mbar_wait(smem_u32(&bars.k_empty[ks]), kr.phase() ^ 1, wd)) return false;
+        if (!mbar_wait(smem_u32(&bars.v_empty[vs]), vr.phase() ^ 1, wd)) return false;
+        const uint32_t bar = smem_u32(&bars.k_full[ks]);
+        mbar_expect_tx(bar, 2 * C::kTileBytes);
 #pragma unroll
-        for (int g = 0; g < C::kBoxes; ++g)
-            tma_load_3d(base + slot * C::kTileBytes + g * C::kBoxBytes, tm, 64 * g, f.k_start + BT * j, f.h, bar);
+        for (int g = 0; g < C::kBoxes; ++g) {
+            tma_load_3d(sK + ks * C::kTileBytes + g * C::kBoxBytes, &a.tk, 64 * g, f.k_start + BT * j, f.h, bar);
+            tma_load_3d(sV + vs * C::kTileBytes + g * C::kBoxBytes, &a.tv, 64 * g, f.k_start + BT * j, f.h, bar);
+        }
+        ++kr.i;
+        ++vr.i;
         return true;
     };
     for (int i = 0;; ++i) {
@@ -909,22 +915,13 @@ __device__ void dq_producer(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint3
             q_pending = true;
         }
         bool ok = true;
-        for (int j = 0; j < f.nk && ok; ++j) {
-            ok = load_kv(bars.k_full, bars.k_empty, kr.slot(), kr.phase(), sK, &a.tk, f, j);
-            if (!ok) break;
-            ++kr.i;
-            ok = load_kv(bars.v_full, bars.v_empty, vr.slot(), vr.phase(), sV, &a.tv, f, j);
-            if (!ok) break;
-            ++vr.i;
-        }
+        for (int j = 0; j < f.nk && ok; ++j) ok = load_kv(f, j);
         if (!ok) break;
     }
     if (aborting(wd)) {
         const long long budget = kDrainCycles;  // loads in flight land within microseconds
         for (uint32_t k = kr.i > (uint32_t)C::kDqKStages ? kr.i - C::kDqKStages : 0; k < kr.i; ++k)
             drain_wait(smem_u32(&bars.k_full[k % C::kDqKStages]), (k / C::kDqKStages) & 1, budget);
-        for (uint32_t k = vr.i > (uint32_t)C::kDqVStages ? vr.i - C::kDqVStages : 0; k < vr.i; ++k)
-            drain_wait(smem_u32(&bars.v_full[k % C::kDqVStages]), (k / C::kDqVStages) & 1, budget);
         if (q_pending) drain_wait(smem_u32(&bars.q_full), (q_uses - 1) & 1, budget);
     }
 }
@@ -953,13 +950,12 @@ __device__ void dq_mma(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint32_t s
             mma_ss(tmem + col, ad + off, bd + off, id, kk > 0);
         }
     };
-    // wait for the next K and V tiles; returns their slots
+    // wait for the next K and V tiles (one barrier for both); returns their slots
     auto take_kv = [&](uint32_t &ks, uint32_t &vs) -> bool {
         ks = kr.slot();
+        vs = vr.slot();
         if (!mbar_wait(smem_u32(&bars.k_full[ks]), kr.phase(), wd)) return false;
         ++kr.i;
-        vs = vr.slot();
-        if (!mbar_wait(smem_u32(&bars.v_full[vs]), vr.phase(), wd)) return false;
         ++vr.i;
         return true;
     };
@@ -1131,10 +1127,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_tc_kernel(const __grid_constan
             mbar_init(smem_u32(&bars.k_full[s]), 1);
             mbar_init(smem_u32(&bars.k_empty[s]), 1);
         }
-        for (int s = 0; s < C::kDqVStages; ++s) {
-            mbar_init(smem_u32(&bars.v_full[s]), 1);
-            mbar_init(smem_u32(&bars.v_empty[s]), 1);
-        }
+        for (int s = 0; s < C::kDqVStages; ++s) mbar_init(smem_u32(&bars.v_empty[s]), 1);
         mbar_init(smem_u32(&bars.sp_full), 1);
         mbar_init(smem_u32(&bars.mma_drain), 1);
         mbar_init(smem_u32(&bars.sp_free), kEw / 32);
