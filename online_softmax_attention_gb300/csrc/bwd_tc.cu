@@ -159,7 +159,7 @@ __device__ __forceinline__ DkdvInfo dkdv_info(const BwdParams &p, int w) {
 
 struct __align__(8) DkdvBars {
     uint64_t kv_full, kv_empty;
-    uint64_t q_full[4], q_empty[4], do_full[4], do_empty[4];
+    uint64_t q_full[4], q_empty[4], do_empty[4];  // q_full: the Q and dO tiles of a query block
     uint64_t st_full, dp_full, p_ready, ds_ready, acc_done, acc_free;
     uint64_t stats_ready[2];  // all elementwise threads staged a query block's lse2 / Dr
     uint64_t mma_drain;       // abort path: completion of the MMAs already issued
@@ -205,7 +205,7 @@ __device__ void dkdv_producer(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, u
         bool ok = true;
         if (dout_role) {
             for (int qb = 0; qb < f.nq; ++qb) {
-                ok = load_row(bars.do_full, bars.do_empty, dr.slot(), dr.phase(), sDO, &a.tdo,
+                ok = load_row(bars.q_full, bars.do_empty, dr.slot(), dr.phase(), sDO, &a.tdo,
                               f.q_start + BT * (f.qb0 + qb), f.h);
                 if (!ok) break;
                 ++dr.i;
@@ -238,7 +238,7 @@ __device__ void dkdv_producer(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, u
         for (uint32_t k = qr.i > (uint32_t)C::kDkdvQStages ? qr.i - C::kDkdvQStages : 0; k < qr.i; ++k)
             drain_wait(smem_u32(&bars.q_full[k % C::kDkdvQStages]), (k / C::kDkdvQStages) & 1, budget);
         for (uint32_t k = dr.i > (uint32_t)C::kDkdvDoStages ? dr.i - C::kDkdvDoStages : 0; k < dr.i; ++k)
-            drain_wait(smem_u32(&bars.do_full[k % C::kDkdvDoStages]), (k / C::kDkdvDoStages) & 1, budget);
+            drain_wait(smem_u32(&bars.q_full[k % C::kDkdvDoStages]), (k / C::kDkdvDoStages) & 1, budget);
         if (kv_pending) drain_wait(smem_u32(&bars.kv_full), (kv_uses - 1) & 1, budget);
     }
 }
@@ -291,7 +291,7 @@ __device__ void dkdv_mma(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, uint32
         if (!mbar_wait(smem_u32(&bars.kv_full), kv_cnt & 1, wd)) return;
         ++kv_cnt;
         uint32_t qs = qr.slot(), os = dr.slot();
-        if (!take(bars.q_full, qs, qr.phase()) || !take(bars.do_full, os, dr.phase())) return;
+        if (!take(bars.q_full, qs, qr.phase())) return;  // Q and dO of the block
         ++qr.i;
         ++dr.i;
         tc_fence_after();
@@ -325,10 +325,8 @@ __device__ void dkdv_mma(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, uint32
             issue_ts(256 + D, BT, sQ + qs * C::kTileBytes, qb > 0);  // dK += dS^T Q
             tc_commit(smem_u32(&bars.q_empty[qs]));
             if (next) {
-                osn = dr.slot();
-                if (!take(bars.do_full, osn, dr.phase())) return;
+                osn = dr.slot();  // dO landed with its Q (q_full, waited above)
                 ++dr.i;
-                tc_fence_after();
                 issue_ss(BT, sV, sDO + osn * C::kTileBytes, idSS);  // dP^T of the next block
                 tc_commit(smem_u32(&bars.dp_full));
                 qs = qsn;
@@ -413,15 +411,13 @@ __device__ void dkdvq_mma(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, uint3
         issue_ss(0, sK, sQ + qs * C::kTileBytes, idST);  // S^T_0 = K Q^T
         tc_commit(smem_u32(&bars.st_full));
         if (kAlias && !dq_region_free()) return;
-        if (!take(bars.do_full, os, dr.phase())) return;
-        ++dr.i;
+        ++dr.i;  // dO landed with its Q (q_full)
         tc_fence_after();
         issue_ss(BT, sV, sDO + os * C::kTileBytes, idSS);  // dP^T_0 = V dO^T
         tc_commit(smem_u32(&bars.dp_full));
         for (int qb = 0; qb < f.nq; ++qb) {
             if (qb > 0) {
-                os = dr.slot();
-                if (!take(bars.do_full, os, dr.phase())) return;
+                os = dr.slot();  // dO landed with its Q (q_full, waited before S^T of this block)
                 ++dr.i;
             }
             if (!mbar_wait(smem_u32(&bars.p_ready), p_cnt & 1, wd)) return;
@@ -783,14 +779,12 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_tc_kernel(const __grid_const
         abort_flag = 0;
         mbar_init(smem_u32(&bars.kv_full), 1);
         mbar_init(smem_u32(&bars.kv_empty), 1);
+        // q_full[s]: one arrival from each producer warp (Q and dO of the same block)
         for (int s = 0; s < C::kDkdvQStages; ++s) {
-            mbar_init(smem_u32(&bars.q_full[s]), 1);
+            mbar_init(smem_u32(&bars.q_full[s]), 2);
             mbar_init(smem_u32(&bars.q_empty[s]), 1);
         }
-        for (int s = 0; s < C::kDkdvDoStages; ++s) {
-            mbar_init(smem_u32(&bars.do_full[s]), 1);
-            mbar_init(smem_u32(&bars.do_empty[s]), 1);
-        }
+        for (int s = 0; s < C::kDkdvDoStages; ++s) mbar_init(smem_u32(&bars.do_empty[s]), 1);
         mbar_init(smem_u32(&bars.st_full), 1);
         mbar_init(smem_u32(&bars.dp_full), 1);
         mbar_init(smem_u32(&bars.p_ready), kEw / 32);
