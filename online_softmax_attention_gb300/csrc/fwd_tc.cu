@@ -112,7 +112,7 @@ struct TcFwdArgs {
 
 struct __align__(8) FwdBars {
     uint64_t q_full[NQT], q_empty[NQT];
-    uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+    uint64_t k_full[4], k_empty[4], v_empty[4];  // k_full: the K and V tiles of a key tile
     uint64_t s_full[NQT], p_full[NQT], o_done[NQT], o_free[NQT];
     uint64_t sched_full[2], sched_empty[2];
     uint64_t mma_drain;  // abort path: completion of the MMAs already issued
@@ -187,15 +187,20 @@ __device__ void producer(const TcFwdArgs &a, FwdBars &bars, int *sched_item, uin
     RingPos<C::kVStages> vr;
     uint32_t q_uses[NQT] = {0, 0};
     bool q_pending[NQT] = {false, false};
-    // one K or V tile (tile_bytes in boxes of box_cols elements) into ring slot `slot`
-    auto load_kv = [&](uint64_t *full, uint64_t *empty, uint32_t slot, uint32_t phase, uint32_t base,
-                       const CUtensorMap *tm, int row, int h, int tile_bytes, int boxes,
-                       int box_cols) -> bool {
-        if (!mbar_wait(smem_u32(&empty[slot]), phase ^ 1, wd)) return false;
-        const uint32_t bar = smem_u32(&full[slot]);
-        mbar_expect_tx(bar, tile_bytes);
-        for (int g = 0; g < boxes; ++g)
-            tma_load_3d(base + slot * tile_bytes + g * C::kBoxBytes, tm, box_cols * g, row, h, bar);
+    // the K and V tiles of one key tile into their rings; both land on the K
+    // slot's full barrier, so the MMA issuer waits once per key tile
+    auto load_kv = [&](int row, int h) -> bool {
+        const uint32_t ks = kr.slot(), vs = vr.slot();
+        if (!mbar_wait(smem_u32(&bars.k_empty[ks]), kr.phase() ^ 1, wd)) return false;
+        if (!mbar_wait(smem_u32(&bars.v_empty[vs]), vr.phase() ^ 1, wd)) return false;
+        const uint32_t bar = smem_u32(&bars.k_full[ks]);
+        mbar_expect_tx(bar, C::kQKTileBytes + C::kVTileBytes);
+        for (int g = 0; g < C::kQKBoxes; ++g)
+            tma_load_3d(sK + ks * C::kQKTileBytes + g * C::kBoxBytes, &a.tk, C::kQKBoxCols * g, row, h, bar);
+        for (int g = 0; g < C::kVBoxes; ++g)
+            tma_load_3d(sV + vs * C::kVTileBytes + g * C::kBoxBytes, &a.tv, 64 * g, row, h, bar);
+        ++kr.i;
+        ++vr.i;
         return true;
     };
     for (int i = 0;; ++i) {
@@ -223,17 +228,7 @@ __device__ void producer(const TcFwdArgs &a, FwdBars &bars, int *sched_item, uin
             q_pending[t] = true;
         }
         if (!ok) break;
-        for (int j = 0; j < f.nkv && ok; ++j) {
-            const int krow = f.k_start + BN * (f.j0 + j);
-            ok = load_kv(bars.k_full, bars.k_empty, kr.slot(), kr.phase(), sK, &a.tk, krow, f.h,
-                         C::kQKTileBytes, C::kQKBoxes, C::kQKBoxCols);
-            if (!ok) break;
-            ++kr.i;
-            ok = load_kv(bars.v_full, bars.v_empty, vr.slot(), vr.phase(), sV, &a.tv, krow, f.h,
-                         C::kVTileBytes, C::kVBoxes, 64);
-            if (!ok) break;
-            ++vr.i;
-        }
+        for (int j = 0; j < f.nkv && ok; ++j) ok = load_kv(f.k_start + BN * (f.j0 + j), f.h);
         if (!ok) break;
     }
     if (aborting(wd)) {
@@ -241,8 +236,6 @@ __device__ void producer(const TcFwdArgs &a, FwdBars &bars, int *sched_item, uin
         const long long budget = kDrainCycles;  // loads in flight land within microseconds
         for (uint32_t k = kr.i > (uint32_t)C::kKStages ? kr.i - C::kKStages : 0; k < kr.i; ++k)
             drain_wait(smem_u32(&bars.k_full[k % C::kKStages]), (k / C::kKStages) & 1, budget);
-        for (uint32_t k = vr.i > (uint32_t)C::kVStages ? vr.i - C::kVStages : 0; k < vr.i; ++k)
-            drain_wait(smem_u32(&bars.v_full[k % C::kVStages]), (k / C::kVStages) & 1, budget);
 #pragma unroll
         for (int t = 0; t < NQT; ++t)
             if (q_pending[t]) drain_wait(smem_u32(&bars.q_full[t]), (q_uses[t] - 1) & 1, budget);
@@ -323,8 +316,7 @@ __device__ void mma_issuer(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
         tc_commit(smem_u32(&bars.k_empty[ks]));
 
         for (int j = 0; j < f.nkv; ++j) {
-            const uint32_t vs = vr.slot();
-            if (!mbar_wait(smem_u32(&bars.v_full[vs]), vr.phase(), wd)) return;
+            const uint32_t vs = vr.slot();  // V_j landed with K_j (k_full, waited before S_j)
             ++vr.i;
             bool have_next_k = false;
             uint32_t nks = 0;
@@ -566,10 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             mbar_init(smem_u32(&bars.k_full[s]), 1);
             mbar_init(smem_u32(&bars.k_empty[s]), 1);
         }
-        for (int s = 0; s < C::kVStages; ++s) {
-            mbar_init(smem_u32(&bars.v_full[s]), 1);
-            mbar_init(smem_u32(&bars.v_empty[s]), 1);
-        }
+        for (int s = 0; s < C::kVStages; ++s) mbar_init(smem_u32(&bars.v_empty[s]), 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&bars.sched_full[s]), 1);
             mbar_init(smem_u32(&bars.sched_empty[s]), kSchedConsumers);
