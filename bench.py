@@ -76,6 +76,13 @@ def load_peaks():
             "sm_max_mhz": 2070.0, "source": "fallback"}
 
 
+def dtype_label(w) -> str:
+    """The arithmetic type a workload computes in, for the JSON line ("e4m3+bf16"
+    when fp8 queries and keys feed the score contraction)."""
+    base = {"fp16": "f16", "bf16": "bf16", "f32": "f32"}[w.dtype]
+    return ("e4m3+" if getattr(w, "qk_fp8", False) else "") + base
+
+
 def source_hash(paths):
     h = hashlib.sha256()
     for p in paths:
@@ -356,7 +363,7 @@ def run_forward_workload(args, rank, world):
         "metric": metric, "value": job_rate(flops, world, ms) / 1e12, "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": ("e4m3+" if w.qk_fp8 else "") + {"fp16": "f16", "bf16": "bf16", "f32": "f32"}[w.dtype],
+        "dtype": dtype_label(w),
         "data": "synthetic",
         "config": {"workload": w.name, "kernel": family, "num_splits": call.num_splits(),
                    "tokens_q": int(sum(x["lengths_q"])), "tokens_k": int(sum(x["lengths_k"])),
@@ -514,7 +521,7 @@ def run_csr_workload(args, rank, world):
         "metric": f"attention over a CSR relation, Gedge/s ({w.note})", "value": rate,
         "unit": "Gedge/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": ("e4m3+" if w.qk_fp8 else "") + {"fp16": "f16", "bf16": "bf16", "f32": "f32"}[w.dtype],
+        "dtype": dtype_label(w),
         "data": "synthetic",
         "config": {"workload": w.name, "nodes": n, "edges": E, "avg_degree": E / max(1, n),
                    "heads": w.H, "head_dim": w.D,

@@ -1,0 +1,24 @@
+"""Host-side pieces of bench.py that need no GPU: every workload name it
+accepts resolves to a workload description, the JSON line's dtype label, and
+the FLOP convention."""
+import pytest
+
+import attn_inputs
+import bench
+
+
+def test_every_bench_workload_exists_and_has_a_dtype_label():
+    for name in bench.FWD_WORKLOADS + (bench.WORKLOAD,):
+        w = attn_inputs.WORKLOADS[name]
+        assert bench.dtype_label(w) in ("f16", "bf16", "f32", "e4m3+bf16", "e4m3+f16")
+    for name in bench.CSR_WORKLOADS:
+        w = attn_inputs.CSR_WORKLOADS[name]
+        assert bench.dtype_label(w) in ("f16", "bf16", "f32")
+    assert bench.dtype_label(attn_inputs.WORKLOADS["causal_fp8qk_b4_n8192"]) == "e4m3+bf16"
+
+
+def test_flop_convention():
+    # causal: 4 N^2 D H / 2 per sequence, four sequences of the training workload
+    assert bench.attention_flops([8192] * 4, [8192] * 4, 32, 128, True) == pytest.approx(2.199023255552e12)
+    # full cross attention of the Vx page's shape
+    assert bench.attention_flops([8192], [2048], 1, 64, False) == pytest.approx(4.294967296e9)
