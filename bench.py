@@ -76,6 +76,11 @@ def load_peaks():
             "sm_max_mhz": 2070.0, "source": "fallback"}
 
 
+def spread(ms_list):
+    """Median, minimum and maximum of per-step times (ms)."""
+    return {"median": statistics.median(ms_list), "min": min(ms_list), "max": max(ms_list)}
+
+
 def dtype_label(w) -> str:
     """The arithmetic type a workload computes in, for the JSON line ("e4m3+bf16"
     when fp8 queries and keys feed the score contraction)."""
@@ -301,9 +306,19 @@ def run_forward_workload(args, rank, world):
         dist.barrier()
     launches = attn.launch_count() - n0
     pruned_per_run = call.pruned_count() / (args.warmup + args.steps)
-    ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in evs), dev)
+    per_launch = [a.elapsed_time(b) for a, b in evs]
+    ms = max_over_ranks(statistics.mean(per_launch), dev)
     if attn.device_status() != 0:
         raise RuntimeError("device status set in the timed region")
+    unflushed = None
+    if flush is not None:
+        # the same launches back to back with the inputs left in L2, for reference
+        for e0, e1 in evs:
+            e0.record(stream)
+            call.run(stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        unflushed = spread([a.elapsed_time(b) for a, b in evs])
 
     # end to end: host inputs in, o and lse out, through the same call
     pin = {n: x[n].contiguous().pin_memory() for n in ("q", "k", "v")}
@@ -365,6 +380,7 @@ def run_forward_workload(args, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": dtype_label(w),
         "data": "synthetic",
+        "step_ms": spread(per_launch), "step_ms_unflushed": unflushed,
         "config": {"workload": w.name, "kernel": family, "num_splits": call.num_splits(),
                    "tokens_q": int(sum(x["lengths_q"])), "tokens_k": int(sum(x["lengths_k"])),
                    "heads": w.H, "head_dim": w.D, "relation": "causal" if w.causal else "full",
@@ -690,6 +706,7 @@ def main():
     launches = attn.launch_count() - n0
     ms = start.elapsed_time(end) / args.steps
     stage_ms = {s: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j, s in enumerate(stages)}
+    step_spread = spread([e[0].elapsed_time(e[4]) for e in evs])
     ms = max_over_ranks(ms, dev)
     status = attn.device_status()
     if status != 0:
@@ -832,6 +849,7 @@ def main():
                    "kernels": family, "dq_mode": dq_mode,
                    "l2": "no flush: each input tensor is 268 MB, larger than the 129 MB L2",
                    "parallelism": f"replicas x{world}"},
+        "step_ms": step_spread,
         "breakdown": {"fwd_ms": stage_ms["fwd"], "bwd_ms": bwd_ms,
                       "stage_ms": stage_ms, "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
                       "fwd_frac_of_bf16_peak": fwd_tflops / peaks["bf16_tflops"],

@@ -22,3 +22,7 @@ def test_flop_convention():
     assert bench.attention_flops([8192] * 4, [8192] * 4, 32, 128, True) == pytest.approx(2.199023255552e12)
     # full cross attention of the Vx page's shape
     assert bench.attention_flops([8192], [2048], 1, 64, False) == pytest.approx(4.294967296e9)
+
+
+def test_step_time_spread():
+    assert bench.spread([3.0, 1.0, 2.0, 10.0]) == {"median": 2.5, "min": 1.0, "max": 10.0}
