@@ -244,7 +244,7 @@ __device__ void producer(const TcFwdArgs &a, FwdBars &bars, int *sched_item, uin
 
 // ---- warp 1: MMA issuer ----------------------------------------------------------
 
-template <int D, bool kBF16, bool kF8>
+template <int D, bool kBF16, bool kF8, bool kPrune>
 __device__ void mma_issuer(const TcFwdArgs &a, FwdBars &bars, const int *sched_item,
                            const PruneShared *ps, uint32_t sQ, uint32_t sK, uint32_t sV,
                            uint32_t tmem, const Watchdog &wd) {
@@ -332,7 +332,7 @@ __device__ void mma_issuer(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
                 }
                 tc_fence_after();
                 // a pruned tile adds nothing to U (the first tile is always admitted)
-                const bool pruned = p.prune && *reinterpret_cast<const volatile int *>(&ps->skip[t]);
+                const bool pruned = kPrune && *reinterpret_cast<const volatile int *>(&ps->skip[t]);
                 if (!pruned) issue_pv(t, vs, j > 0);
                 if (j == f.n[t] - 1) tc_commit(smem_u32(&bars.o_done[t]));
                 if (j + 1 < f.n[t]) {
@@ -355,7 +355,7 @@ __device__ void mma_issuer(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
 
 // ---- warps 4-11: softmax and epilogue ------------------------------------------
 
-template <int D, bool kBF16, typename Tout>
+template <int D, bool kBF16, typename Tout, bool kPrune>
 __device__ void softmax_wg(const TcFwdArgs &a, FwdBars &bars, const int *sched_item, PruneShared *ps,
                            uint32_t tmem, const Watchdog &wd) {
     const FwdParams &p = a.p;
@@ -424,7 +424,7 @@ __device__ void softmax_wg(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
                     if (c >= lim) s[c] = -INFINITY;
             }
             const float mx = row_max<BN>(s) * sl2;
-            if (p.prune) {
+            if (kPrune) {
                 // largest score of the whole 128 x 128 tile (rows past the queries excluded),
                 // gathered from the four warps through shared memory and an mbarrier
                 float tm = row < f.Lq ? mx : -INFINITY;
@@ -526,7 +526,8 @@ __device__ void softmax_wg(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
     }
 }
 
-template <int D, bool kBF16, typename Tout, bool kF8>
+// kPrune: the tile-pruned forward (its tile-max exchange is compiled only there)
+template <int D, bool kBF16, typename Tout, bool kF8, bool kPrune>
 __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ TcFwdArgs a) {
     using C = Cfg<D, kF8>;
     extern __shared__ uint8_t smem_raw[];
@@ -583,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             if (lane == 0) producer<D, kF8>(a, bars, sched_item, sQ, sK, sV, wd);
         } else if (warp == 1) {
             if (lane == 0) {
-                mma_issuer<D, kBF16, kF8>(a, bars, sched_item, &prune_shared, sQ, sK, sV, tmem, wd);
+                mma_issuer<D, kBF16, kF8, kPrune>(a, bars, sched_item, &prune_shared, sQ, sK, sV, tmem, wd);
                 if (aborting(wd)) {  // let issued MMAs finish before TMEM is freed
                     tc_commit(smem_u32(&bars.mma_drain));
                     drain_wait(smem_u32(&bars.mma_drain), 0, kDrainCycles);
@@ -592,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         }
     } else {
         regs_inc<C::kRegsSoftmax>();
-        softmax_wg<D, kBF16, Tout>(a, bars, sched_item, &prune_shared, tmem, wd);
+        softmax_wg<D, kBF16, Tout, kPrune>(a, bars, sched_item, &prune_shared, tmem, wd);
     }
 
     tc_fence_before();
@@ -607,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 
 template <int D, bool kBF16, typename Tout, bool kF8>
 cudaError_t launch_typed(const TcFwdArgs &args, int num_ctas, cudaStream_t s) {
-    auto kern = fwd_tc_kernel<D, kBF16, Tout, kF8>;
+    auto kern = args.p.prune ? fwd_tc_kernel<D, kBF16, Tout, kF8, true> : fwd_tc_kernel<D, kBF16, Tout, kF8, false>;
     const int smem = Cfg<D, kF8>::kSmemBytes;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
