@@ -532,13 +532,24 @@ __device__ void dkdv_elementwise(const TcBwdArgs &a, DkdvBars &bars, float *stat
                 const float2 sv = make_float2(__uint_as_float(r[(2 * c) >> 5][(2 * c) & 31]),
                                               __uint_as_float(r[(2 * c + 1) >> 5][(2 * c + 1) & 31]));
                 const float2 x = __ffma2_rn(sv, sc2, nlse2[c]);
-                float2 pv = make_float2(exp2_approx(x.x), exp2_approx(x.y));
-                if (diag) {  // key after query
-                    if (kl > 64 * wg + 2 * c) pv.x = 0.f;
-                    if (kl > 64 * wg + 2 * c + 1) pv.y = 0.f;
-                }
+                const float2 pv = make_float2(exp2_approx(x.x), exp2_approx(x.y));
                 pr[c] = pv;
                 pk[c] = pack2(pv.x, pv.y, kBF16);
+            }
+            if (diag) {
+                // queries before the key: P^T = 0 (whatever their discarded exponentials
+                // gave); kept out of the loop above, which every block runs
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const int q = 64 * wg + 2 * c;
+                    if (kl > q + 1) {
+                        pr[c] = make_float2(0.f, 0.f);
+                        pk[c] = 0u;
+                    } else if (kl > q) {
+                        pr[c].x = 0.f;
+                        pk[c] &= 0xFFFF0000u;  // the pair's first value
+                    }
+                }
             }
             tmem_st_x32(lane_base + 64 * wg, pk);
             tmem_st_wait();
@@ -1064,16 +1075,23 @@ __device__ void dq_elementwise(const TcBwdArgs &a, DqBars &bars, uint32_t tmem, 
                                               __uint_as_float(rs[(2 * c + 1) >> 5][(2 * c + 1) & 31]));
                 const float2 x = __ffma2_rn(sv, sc2, nl2);
                 // one pair in kDqExpFmaEvery on the FMA pipe, the rest on the SFU
-                float2 pv = (c % kDqExpFmaEvery) == 0 ? exp2_fma2(x)
-                                                      : make_float2(exp2_approx(x.x), exp2_approx(x.y));
-                if (masked) {
-                    if (c0 + 2 * c >= lim) pv.x = 0.f;
-                    if (c0 + 2 * c + 1 >= lim) pv.y = 0.f;
-                }
+                const float2 pv = (c % kDqExpFmaEvery) == 0 ? exp2_fma2(x)
+                                                            : make_float2(exp2_approx(x.x), exp2_approx(x.y));
                 const float2 dp = make_float2(__uint_as_float(rp[(2 * c) >> 5][(2 * c) & 31]),
                                               __uint_as_float(rp[(2 * c + 1) >> 5][(2 * c + 1) & 31]));
                 const float2 d = __fmul2_rn(pv, __fadd2_rn(dp, ndr2));
                 pk[c] = pack2(d.x, d.y, kBF16);
+            }
+            if (masked) {
+                // keys at or past lim: dS = 0 (whatever their discarded exponentials
+                // gave, inf or NaN included); kept out of the loop above, which
+                // every tile runs
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const int col = c0 + 2 * c;
+                    if (col >= lim) pk[c] = 0u;
+                    else if (col + 1 >= lim) pk[c] &= 0xFFFFu;  // the pair's second value
+                }
             }
             tmem_st_x32(lane_base + 256 + 64 * (j & 1) + 32 * wg, pk);
             tmem_st_wait();
