@@ -284,8 +284,9 @@ def run_forward_workload(args, rank, world):
     for _ in range(args.warmup):
         call.run(stream)
     torch.cuda.synchronize()
-    if attn.device_status() != 0:
-        raise RuntimeError("device status set during warm-up")
+    status = attn.device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} ({attn.strerror(status)}) set during warm-up")
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
     n0 = attn.launch_count()
@@ -308,8 +309,9 @@ def run_forward_workload(args, rank, world):
     pruned_per_run = call.pruned_count() / (args.warmup + args.steps)
     per_launch = [a.elapsed_time(b) for a, b in evs]
     ms = max_over_ranks(statistics.mean(per_launch), dev)
-    if attn.device_status() != 0:
-        raise RuntimeError("device status set in the timed region")
+    status = attn.device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} ({attn.strerror(status)}) set in the timed region")
     unflushed = None
     if flush is not None:
         # the same launches back to back with the inputs left in L2, for reference
@@ -475,8 +477,9 @@ def run_csr_workload(args, rank, world):
     for _ in range(args.warmup):
         call.run(stream)
     torch.cuda.synchronize()
-    if attn.device_status() != 0:
-        raise RuntimeError("device status set during warm-up")
+    status = attn.device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} ({attn.strerror(status)}) set during warm-up")
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
     n0 = attn.launch_count()
@@ -525,8 +528,9 @@ def run_csr_workload(args, rank, world):
     t1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(t0.elapsed_time(t1) / e_steps, dev)
-    if attn.device_status() != 0:
-        raise RuntimeError("device status set in the timed region")
+    status = attn.device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} ({attn.strerror(status)}) set in the timed region")
 
     peaks = load_peaks()
     csrc = "online_softmax_attention_gb300/csrc/"
@@ -685,8 +689,9 @@ def main():
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    if attn.device_status() != 0:
-        raise RuntimeError("device status set during warm-up")
+    status = attn.device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} ({attn.strerror(status)}) set during warm-up")
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     barrier()
@@ -793,8 +798,9 @@ def main():
     torch.cuda.synchronize()
     barrier()
     e2e_ms = max_over_ranks(t0.elapsed_time(t1) / e_steps, dev)
-    if attn.device_status() != 0:
-        raise RuntimeError("device status set in the end-to-end leg")
+    status = attn.device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} ({attn.strerror(status)}) set in the end-to-end leg")
 
     peaks = load_peaks()
     # algorithmic FLOPs per launch of each stage: fwd = S and PV contractions;

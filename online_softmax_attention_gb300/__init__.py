@@ -55,6 +55,11 @@ def device_status(stream: torch.cuda.Stream | None = None) -> int:
     return int(_abi.load().attn_device_status(ctypes.c_void_p(s.cuda_stream)))
 
 
+def strerror(code: int) -> str:
+    """The library's message for a status code."""
+    return _abi.load().attn_strerror(int(code)).decode()
+
+
 def _dtype_code(dt: torch.dtype) -> int:
     if dt not in _DT:
         raise TypeError(f"unsupported dtype {dt}; use float16, bfloat16 or float32")

@@ -869,7 +869,12 @@ __device__ __forceinline__ DqInfo dq_info(const BwdParams &p, int w) {
 struct __align__(8) DqBars {
     uint64_t q_full, q_empty;
     uint64_t k_full[8], k_empty[8], v_empty[8];  // k_full: the K and V tiles of a key block
-    uint64_t sp_full, sp_free, ds_ready, acc_done, acc_free;
+    uint64_t sp_full, sp_free, acc_done, acc_free;
+    // dS of a key block is in TMEM, alternating by block: the next S / dP pair
+    // waits only for every warp's read of this one (sp_free), so a fast warp can
+    // finish the next block's dS before a slow one has finished this block's; with
+    // one barrier its early arrival would complete the wrong phase
+    uint64_t ds_ready[2];
     uint64_t mma_drain;  // abort path: completion of the MMAs already issued
     SchedRing sched;
 };
@@ -993,7 +998,7 @@ __device__ void dq_mma(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint32_t s
                 tc_commit(smem_u32(&bars.sp_full));
                 tc_commit(smem_u32(&bars.v_empty[vsn]));
             }
-            if (!mbar_wait(smem_u32(&bars.ds_ready), ds_cnt & 1, wd)) return;
+            if (!mbar_wait(smem_u32(&bars.ds_ready[ds_cnt & 1]), (ds_cnt >> 1) & 1, wd)) return;
             ++ds_cnt;
             if (j == 0) {
                 if (!mbar_wait(smem_u32(&bars.acc_free), (af_cnt & 1) ^ 1, wd)) return;
@@ -1096,7 +1101,7 @@ __device__ void dq_elementwise(const TcBwdArgs &a, DqBars &bars, uint32_t tmem, 
             tmem_st_x32(lane_base + 256 + 64 * (j & 1) + 32 * wg, pk);
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive_warp(smem_u32(&bars.ds_ready));
+            mbar_arrive_warp(smem_u32(&bars.ds_ready[step & 1]));
         }
         bool ok = mbar_wait(smem_u32(&bars.acc_done), ad_cnt & 1, wd);
         ++ad_cnt;
@@ -1115,7 +1120,6 @@ __device__ void dq_elementwise(const TcBwdArgs &a, DqBars &bars, uint32_t tmem, 
         tc_fence_before();
         mbar_arrive_warp(smem_u32(&bars.acc_free));
     }
-    (void)step;
 }
 
 template <int D, bool kBF16, typename Tg>
@@ -1143,7 +1147,8 @@ __global__ void __launch_bounds__(kThreads, 1) dq_tc_kernel(const __grid_constan
         mbar_init(smem_u32(&bars.sp_full), 1);
         mbar_init(smem_u32(&bars.mma_drain), 1);
         mbar_init(smem_u32(&bars.sp_free), kEw / 32);
-        mbar_init(smem_u32(&bars.ds_ready), kEw / 32);
+        mbar_init(smem_u32(&bars.ds_ready[0]), kEw / 32);
+        mbar_init(smem_u32(&bars.ds_ready[1]), kEw / 32);
         mbar_init(smem_u32(&bars.acc_done), 1);
         mbar_init(smem_u32(&bars.acc_free), kEw / 32);
         for (int s = 0; s < 2; ++s) {
