@@ -1,0 +1,287 @@
+"""A randomized model of the tensor-core kernels' mbarrier protocols (test
+infrastructure; it models the protocols, it shares no code with the kernels).
+
+Each warp role is a generator that yields the operations it performs on
+mbarriers: wait for a phase (by parity, as mbarrier.try_wait.parity does),
+arrive with a tag naming the block it signals, or issue work to the tensor
+core.  The tensor core is a FIFO: issued MMAs and commits retire in order at
+random times, and a commit arrives on its barrier when it retires (as
+tcgen05.commit does).  A scheduler runs the roles in a random interleaving
+with random per-role speeds (so one warp can fall far behind the others).
+
+Checked per run: every completed phase of a tagged barrier collected arrivals
+that all carry the same tag (a fast warp's arrival for the next block must not
+complete the phase of this one), and the run ends with every role finished
+(no deadlock).
+"""
+from __future__ import annotations
+
+import random
+
+
+class Barrier:
+    def __init__(self, name, count, tagged=True):
+        self.name, self.count, self.tagged = name, count, tagged
+        self.phase = 0
+        self.pending = count
+        self.tags = []
+
+    def arrive(self, tag, violations):
+        self.tags.append(tag)
+        self.pending -= 1
+        if self.pending == 0:
+            if self.tagged and len(set(self.tags)) > 1:
+                violations.append(f"{self.name} phase {self.phase} completed with arrivals for {sorted(set(self.tags))}")
+            self.phase += 1
+            self.pending = self.count
+            self.tags = []
+
+    def done(self, parity):
+        """try_wait.parity(parity): the phase with that parity has completed."""
+        return (self.phase & 1) != parity
+
+
+class TensorCore:
+    """In-order queue of ("mma", None) and ("commit", barrier, tag) items."""
+
+    def __init__(self):
+        self.queue = []
+
+    def retire_one(self, violations):
+        kind, bar, tag = self.queue.pop(0)
+        if kind == "commit":
+            bar.arrive(tag, violations)
+
+
+def run(roles, tc, rng, max_steps=200000):
+    """Interleave the role generators randomly.  Each role yields
+    ("wait", bar, parity), ("arrive", bar, tag), ("mma",), ("commit", bar, tag)
+    or ("work",) (local computation, no synchronisation).  Returns
+    (violations, deadlocked)."""
+    violations = []
+    speed = {name: rng.choice([0.05, 0.3, 1.0, 1.0, 1.0]) for name in roles}
+    pending = {}
+    for name, gen in roles.items():
+        pending[name] = next(gen, None)
+    for _ in range(max_steps):
+        ready = [n for n, op in pending.items()
+                 if op is not None and not (op[0] == "wait" and not op[1].done(op[2]))]
+        choices = ready + (["__tc__"] if tc.queue else [])
+        if not choices:
+            stuck = [n for n, op in pending.items() if op is not None]
+            return violations, bool(stuck)
+        weights = [speed.get(c, 1.0) for c in choices]
+        who = rng.choices(choices, weights)[0]
+        if who == "__tc__":
+            tc.retire_one(violations)
+            continue
+        op = pending[who]
+        if op[0] == "arrive":
+            op[1].arrive(op[2], violations)
+        elif op[0] == "mma":
+            tc.queue.append(("mma", None, None))
+        elif op[0] == "commit":
+            tc.queue.append(("commit", op[1], op[2]))
+        pending[who] = next(roles[who], None)
+    return violations + ["step limit"], True
+
+
+# ---- the kernels' protocols ---------------------------------------------------------
+# Only the synchronisation is modelled; "work" stands for computation and
+# tensor-memory loads / stores.  Tags: the global block (or item) index the
+# arrival belongs to.
+
+def dq_protocol(items, rng, n_warps=8, split_ds=True):
+    """dq kernel: per key block S and dP into TMEM (commit sp_full), the
+    elementwise warps read them (sp_free), form dS (ds_ready), the issuer
+    issues the next block's S / dP after sp_free and dQ after ds_ready.
+    split_ds: dS-ready alternates between two barriers by block (the fix);
+    False models the earlier single barrier."""
+    tc = TensorCore()
+    sp_full, sp_free = Barrier("sp_full", 1), Barrier("sp_free", n_warps)
+    ds = [Barrier("ds_ready[0]", n_warps), Barrier("ds_ready[1]", n_warps)] if split_ds \
+        else [Barrier("ds_ready", n_warps)]
+    acc_done, acc_free = Barrier("acc_done", 1), Barrier("acc_free", n_warps)
+
+    def issuer():
+        spf = dsc = af = 0
+        blk = 0
+        for it, nk in enumerate(items):
+            yield ("mma",)
+            yield ("mma",)
+            yield ("commit", sp_full, blk)
+            for j in range(nk):
+                yield ("wait", sp_free, spf & 1)
+                spf += 1
+                if j + 1 < nk:
+                    yield ("mma",)
+                    yield ("mma",)
+                    yield ("commit", sp_full, blk + j + 1)
+                if split_ds:
+                    yield ("wait", ds[dsc & 1], (dsc >> 1) & 1)
+                else:
+                    yield ("wait", ds[0], dsc & 1)
+                dsc += 1
+                if j == 0:
+                    yield ("wait", acc_free, (af & 1) ^ 1)
+                    af += 1
+                yield ("mma",)  # dQ += dS K
+            yield ("commit", acc_done, it)
+            blk += nk
+
+    def warp():
+        sp = ad = step = 0
+        for it, nk in enumerate(items):
+            for _ in range(nk):
+                yield ("wait", sp_full, sp & 1)
+                sp += 1
+                yield ("work",)
+                yield ("arrive", sp_free, step)
+                for _ in range(rng.randint(1, 6)):
+                    yield ("work",)
+                yield ("arrive", ds[step & 1] if split_ds else ds[0], step)
+                step += 1
+            yield ("wait", acc_done, ad & 1)
+            ad += 1
+            yield ("work",)
+            yield ("arrive", acc_free, it)
+
+    roles = {"issuer": issuer()}
+    roles.update({f"warp{w}": warp() for w in range(n_warps)})
+    return roles, tc
+
+
+def fwd_protocol(items, rng, warps_per_tile=4):
+    """Forward kernel: two query tiles ping-pong; per key tile the issuer waits
+    for P_j(t) (p_full, one arrival per softmax warp), issues PV_j(t) and
+    S_{j+1}(t) (commit s_full); after the last PV it commits o_done, and before
+    the next item's first PV it waits for the epilogue's o_free."""
+    tc = TensorCore()
+    s_full = [Barrier(f"s_full[{t}]", 1) for t in (0, 1)]
+    p_full = [Barrier(f"p_full[{t}]", warps_per_tile) for t in (0, 1)]
+    o_done = [Barrier(f"o_done[{t}]", 1) for t in (0, 1)]
+    o_free = [Barrier(f"o_free[{t}]", warps_per_tile) for t in (0, 1)]
+
+    def issuer():
+        pc = [0, 0]
+        of = [0, 0]
+        blk = 0
+        for it, n in enumerate(items):
+            for t in (0, 1):
+                yield ("mma",)
+                yield ("commit", s_full[t], blk)
+            for j in range(n):
+                for t in (0, 1):
+                    yield ("wait", p_full[t], pc[t] & 1)
+                    pc[t] += 1
+                    if j == 0:
+                        yield ("wait", o_free[t], (of[t] & 1) ^ 1)
+                        of[t] += 1
+                    yield ("mma",)  # PV_j(t)
+                    if j == n - 1:
+                        yield ("commit", o_done[t], it)
+                    else:
+                        yield ("mma",)  # S_{j+1}(t)
+                        yield ("commit", s_full[t], blk + j + 1)
+            blk += n
+
+    def softmax(t):
+        sc = oc = 0
+        blk = 0
+        for it, n in enumerate(items):
+            for j in range(n):
+                yield ("wait", s_full[t], sc & 1)
+                sc += 1
+                for _ in range(rng.randint(1, 6)):
+                    yield ("work",)
+                yield ("arrive", p_full[t], blk + j)
+            blk += n
+            yield ("wait", o_done[t], oc & 1)
+            oc += 1
+            yield ("work",)
+            yield ("arrive", o_free[t], it)
+
+    roles = {"issuer": issuer()}
+    for t in (0, 1):
+        roles.update({f"sm{t}.{w}": softmax(t) for w in range(warps_per_tile)})
+    return roles, tc
+
+
+def dkdv_protocol(items, rng, n_warps=8):
+    """dK/dV kernel: issue order dV_i, S^T_{i+1}, dK_i, dP^T_{i+1}; the
+    elementwise warps stage each query block's statistics (double-buffered
+    stats_ready), write P^T (p_ready) and dS^T (ds_ready)."""
+    tc = TensorCore()
+    st_full, dp_full = Barrier("st_full", 1), Barrier("dp_full", 1)
+    p_ready, ds_ready = Barrier("p_ready", n_warps), Barrier("ds_ready", n_warps)
+    acc_done, acc_free = Barrier("acc_done", 1), Barrier("acc_free", n_warps)
+    stats = [Barrier("stats_ready[0]", n_warps), Barrier("stats_ready[1]", n_warps)]
+
+    def issuer():
+        pr = dsr = af = 0
+        blk = 0
+        for it, nq in enumerate(items):
+            yield ("mma",)
+            yield ("commit", st_full, blk)
+            yield ("mma",)
+            yield ("commit", dp_full, blk)
+            for qb in range(nq):
+                yield ("wait", p_ready, pr & 1)
+                pr += 1
+                if qb == 0:
+                    yield ("wait", acc_free, (af & 1) ^ 1)
+                    af += 1
+                yield ("mma",)  # dV
+                nxt = qb + 1 < nq
+                if nxt:
+                    yield ("mma",)
+                    yield ("commit", st_full, blk + qb + 1)
+                yield ("wait", ds_ready, dsr & 1)
+                dsr += 1
+                yield ("mma",)  # dK
+                if nxt:
+                    yield ("mma",)
+                    yield ("commit", dp_full, blk + qb + 1)
+            yield ("commit", acc_done, it)
+            blk += nq
+
+    def warp():
+        st = dp = ad = si = 0
+        blk = 0
+        for it, nq in enumerate(items):
+            for qb in range(nq):
+                yield ("arrive", stats[si & 1], si)
+                yield ("wait", stats[si & 1], (si >> 1) & 1)
+                si += 1
+                yield ("wait", st_full, st & 1)
+                st += 1
+                for _ in range(rng.randint(1, 6)):
+                    yield ("work",)
+                yield ("arrive", p_ready, blk + qb)
+                yield ("wait", dp_full, dp & 1)
+                dp += 1
+                for _ in range(rng.randint(1, 3)):
+                    yield ("work",)
+                yield ("arrive", ds_ready, blk + qb)
+            blk += nq
+            yield ("wait", acc_done, ad & 1)
+            ad += 1
+            yield ("work",)
+            yield ("arrive", acc_free, it)
+
+    roles = {"issuer": issuer()}
+    roles.update({f"warp{w}": warp() for w in range(n_warps)})
+    return roles, tc
+
+
+def explore(protocol, trials, seed, **kw):
+    """Run `trials` random interleavings of random items; returns the first
+    violation or deadlock found (or None)."""
+    rng = random.Random(seed)
+    for trial in range(trials):
+        items = [rng.choice([1, 1, 2, 3, 5]) for _ in range(rng.randint(1, 4))]
+        roles, tc = protocol(items, rng, **kw)
+        violations, deadlocked = run(roles, tc, rng)
+        if violations or deadlocked:
+            return {"trial": trial, "items": items, "violations": violations, "deadlock": deadlocked}
+    return None
