@@ -20,21 +20,34 @@ import random
 
 
 class Barrier:
+    """Arrival count and transaction bytes (expect-tx / complete-tx, as TMA
+    loads use them): a phase completes when every arrival is in and the
+    outstanding byte count is back to zero."""
+
     def __init__(self, name, count, tagged=True):
         self.name, self.count, self.tagged = name, count, tagged
         self.phase = 0
         self.pending = count
+        self.tx = 0
         self.tags = []
 
-    def arrive(self, tag, violations):
-        self.tags.append(tag)
-        self.pending -= 1
-        if self.pending == 0:
+    def _maybe_complete(self, violations):
+        if self.pending == 0 and self.tx == 0:
             if self.tagged and len(set(self.tags)) > 1:
                 violations.append(f"{self.name} phase {self.phase} completed with arrivals for {sorted(set(self.tags))}")
             self.phase += 1
             self.pending = self.count
             self.tags = []
+
+    def arrive(self, tag, violations, expect_tx=0):
+        self.tags.append(tag)
+        self.tx += expect_tx
+        self.pending -= 1
+        self._maybe_complete(violations)
+
+    def complete_tx(self, nbytes, violations):
+        self.tx -= nbytes
+        self._maybe_complete(violations)
 
     def done(self, parity):
         """try_wait.parity(parity): the phase with that parity has completed."""
@@ -55,10 +68,12 @@ class TensorCore:
 
 def run(roles, tc, rng, max_steps=200000):
     """Interleave the role generators randomly.  Each role yields
-    ("wait", bar, parity), ("arrive", bar, tag), ("mma",), ("commit", bar, tag)
-    or ("work",) (local computation, no synchronisation).  Returns
-    (violations, deadlocked)."""
+    ("wait", bar, parity), ("arrive", bar, tag), ("arrive_tx", bar, tag, loads)
+    (arrive with expect-tx for `loads` one-unit TMA loads, which then land in
+    any order), ("mma",), ("commit", bar, tag) or ("work",) (local
+    computation, no synchronisation).  Returns (violations, deadlocked)."""
     violations = []
+    tma = []  # barriers with one load in flight each
     speed = {name: rng.choice([0.05, 0.3, 1.0, 1.0, 1.0]) for name in roles}
     pending = {}
     for name, gen in roles.items():
@@ -66,7 +81,7 @@ def run(roles, tc, rng, max_steps=200000):
     for _ in range(max_steps):
         ready = [n for n, op in pending.items()
                  if op is not None and not (op[0] == "wait" and not op[1].done(op[2]))]
-        choices = ready + (["__tc__"] if tc.queue else [])
+        choices = ready + (["__tc__"] if tc.queue else []) + (["__tma__"] if tma else [])
         if not choices:
             stuck = [n for n, op in pending.items() if op is not None]
             return violations, bool(stuck)
@@ -75,9 +90,15 @@ def run(roles, tc, rng, max_steps=200000):
         if who == "__tc__":
             tc.retire_one(violations)
             continue
+        if who == "__tma__":
+            tma.pop(rng.randrange(len(tma))).complete_tx(1, violations)
+            continue
         op = pending[who]
         if op[0] == "arrive":
             op[1].arrive(op[2], violations)
+        elif op[0] == "arrive_tx":
+            op[1].arrive(op[2], violations, expect_tx=op[3])
+            tma.extend([op[1]] * op[3])
         elif op[0] == "mma":
             tc.queue.append(("mma", None, None))
         elif op[0] == "commit":
@@ -285,3 +306,287 @@ def explore(protocol, trials, seed, **kw):
         if violations or deadlocked:
             return {"trial": trial, "items": items, "violations": violations, "deadlock": deadlocked}
     return None
+
+
+# ---- protocols with their TMA producers -------------------------------------------
+
+def _dkdv_elementwise(items, rng, st_full, dp_full, p_ready, ds_ready, acc_done, acc_free, stats):
+    st = dp = ad = si = 0
+    blk = 0
+    for it, nq in enumerate(items):
+        for qb in range(nq):
+            yield ("arrive", stats[si & 1], si)
+            yield ("wait", stats[si & 1], (si >> 1) & 1)
+            si += 1
+            yield ("wait", st_full, st & 1)
+            st += 1
+            for _ in range(rng.randint(1, 6)):
+                yield ("work",)
+            yield ("arrive", p_ready, blk + qb)
+            yield ("wait", dp_full, dp & 1)
+            dp += 1
+            yield ("work",)
+            yield ("arrive", ds_ready, blk + qb)
+        blk += nq
+        yield ("wait", acc_done, ad & 1)
+        ad += 1
+        yield ("work",)
+        yield ("arrive", acc_free, it)
+
+
+def dkdv_loads_protocol(items, rng, n_warps=8, stages=2, q_full_arrivals=2):
+    """The dK/dV kernel with its producers: warp 0 loads K, V (kv_full) and
+    the Q ring, warp 2 the dO ring, and a block's Q and dO land on one full
+    barrier (q_full, one arrival with expect-tx from each producer).
+    q_full_arrivals = 1 models forgetting the second producer's arrival."""
+    tc = TensorCore()
+    kv_full, kv_empty = Barrier("kv_full", 1), Barrier("kv_empty", 1)
+    q_full = [Barrier(f"q_full[{s}]", q_full_arrivals) for s in range(stages)]
+    q_empty = [Barrier(f"q_empty[{s}]", 1) for s in range(stages)]
+    do_empty = [Barrier(f"do_empty[{s}]", 1) for s in range(stages)]
+    st_full, dp_full = Barrier("st_full", 1), Barrier("dp_full", 1)
+    p_ready, ds_ready = Barrier("p_ready", n_warps), Barrier("ds_ready", n_warps)
+    acc_done, acc_free = Barrier("acc_done", 1), Barrier("acc_free", n_warps)
+    stats = [Barrier("stats_ready[0]", n_warps), Barrier("stats_ready[1]", n_warps)]
+
+    def q_producer():
+        kvu = n = 0
+        for it, nq in enumerate(items):
+            yield ("wait", kv_empty, (kvu & 1) ^ 1)
+            kvu += 1
+            yield ("arrive_tx", kv_full, it, 2)
+            for _ in range(nq):
+                yield ("wait", q_empty[n % stages], ((n // stages) & 1) ^ 1)
+                yield ("arrive_tx", q_full[n % stages], n, 1)
+                n += 1
+
+    def do_producer():
+        n = 0
+        for it, nq in enumerate(items):
+            for _ in range(nq):
+                yield ("wait", do_empty[n % stages], ((n // stages) & 1) ^ 1)
+                yield ("arrive_tx", q_full[n % stages], n, 1)
+                n += 1
+
+    def issuer():
+        kvc = pr = dsr = af = n = 0
+        for it, nq in enumerate(items):
+            yield ("wait", kv_full, kvc & 1)
+            kvc += 1
+            yield ("wait", q_full[n % stages], (n // stages) & 1)
+            yield ("mma",)
+            yield ("commit", st_full, n)
+            yield ("mma",)
+            yield ("commit", dp_full, n)
+            for qb in range(nq):
+                cur = n + qb
+                yield ("wait", p_ready, pr & 1)
+                pr += 1
+                if qb == 0:
+                    yield ("wait", acc_free, (af & 1) ^ 1)
+                    af += 1
+                yield ("mma",)  # dV reads dO
+                yield ("commit", do_empty[cur % stages], cur)
+                nxt = qb + 1 < nq
+                if nxt:
+                    yield ("wait", q_full[(cur + 1) % stages], ((cur + 1) // stages) & 1)
+                    yield ("mma",)
+                    yield ("commit", st_full, cur + 1)
+                yield ("wait", ds_ready, dsr & 1)
+                dsr += 1
+                yield ("mma",)  # dK reads Q
+                yield ("commit", q_empty[cur % stages], cur)
+                if nxt:
+                    yield ("mma",)
+                    yield ("commit", dp_full, cur + 1)
+            yield ("commit", acc_done, it)
+            yield ("commit", kv_empty, it)
+            n += nq
+
+    roles = {"q_producer": q_producer(), "do_producer": do_producer(), "issuer": issuer()}
+    for w in range(n_warps):
+        roles[f"warp{w}"] = _dkdv_elementwise(items, rng, st_full, dp_full, p_ready, ds_ready, acc_done,
+                                              acc_free, stats)
+    return roles, tc
+
+
+def fwd_loads_protocol(items, rng, warps_per_tile=4, kstages=2, vstages=3):
+    """The forward kernel with its producer: Q per tile (q_full / q_empty),
+    and each key tile's K and V landing on the K slot's full barrier (two
+    loads); the issuer waits once per key tile and releases K after the score
+    MMAs and V after the value MMAs.  items: (key tiles of tile 0, of tile 1)."""
+    tc = TensorCore()
+    q_full = [Barrier(f"q_full[{t}]", 1) for t in (0, 1)]
+    q_empty = [Barrier(f"q_empty[{t}]", 1) for t in (0, 1)]
+    k_full = [Barrier(f"k_full[{s}]", 1) for s in range(kstages)]
+    k_empty = [Barrier(f"k_empty[{s}]", 1) for s in range(kstages)]
+    v_empty = [Barrier(f"v_empty[{s}]", 1) for s in range(vstages)]
+    s_full = [Barrier(f"s_full[{t}]", 1) for t in (0, 1)]
+    p_full = [Barrier(f"p_full[{t}]", warps_per_tile) for t in (0, 1)]
+    o_done = [Barrier(f"o_done[{t}]", 1) for t in (0, 1)]
+    o_free = [Barrier(f"o_free[{t}]", warps_per_tile) for t in (0, 1)]
+
+    def producer():
+        qu = [0, 0]
+        kn = 0
+        for it, ns in enumerate(items):
+            for t in (0, 1):
+                if ns[t] == 0:
+                    continue
+                yield ("wait", q_empty[t], (qu[t] & 1) ^ 1)
+                qu[t] += 1
+                yield ("arrive_tx", q_full[t], it, 1)
+            for _ in range(max(ns)):
+                yield ("wait", k_empty[kn % kstages], ((kn // kstages) & 1) ^ 1)
+                yield ("wait", v_empty[kn % vstages], ((kn // vstages) & 1) ^ 1)
+                yield ("arrive_tx", k_full[kn % kstages], kn, 2)
+                kn += 1
+
+    def issuer():
+        qc, pc, of = [0, 0], [0, 0], [0, 0]
+        kn = 0  # global number of the next key tile to take
+        for it, ns in enumerate(items):
+            nkv = max(ns)
+            if nkv == 0:
+                continue
+            for t in (0, 1):
+                if ns[t]:
+                    yield ("wait", q_full[t], qc[t] & 1)
+                    qc[t] += 1
+            g = kn  # key tile 0 of this item
+            yield ("wait", k_full[g % kstages], (g // kstages) & 1)
+            kn += 1
+            for t in (0, 1):
+                if ns[t]:
+                    yield ("mma",)
+                    yield ("commit", s_full[t], (it, 0))
+                    if ns[t] == 1:
+                        yield ("commit", q_empty[t], it)
+            yield ("commit", k_empty[g % kstages], g)
+            for j in range(nkv):
+                gj = g + j  # V_j landed with K_j
+                have_next = False
+                for t in (0, 1):
+                    if j >= ns[t]:
+                        continue
+                    yield ("wait", p_full[t], pc[t] & 1)
+                    pc[t] += 1
+                    if j == 0:
+                        yield ("wait", o_free[t], (of[t] & 1) ^ 1)
+                        of[t] += 1
+                    yield ("mma",)  # PV_j(t) reads V_j
+                    if j == ns[t] - 1:
+                        yield ("commit", o_done[t], it)
+                    if j + 1 < ns[t]:
+                        if not have_next:
+                            yield ("wait", k_full[(gj + 1) % kstages], ((gj + 1) // kstages) & 1)
+                            kn += 1
+                            have_next = True
+                        yield ("mma",)  # S_{j+1}(t)
+                        yield ("commit", s_full[t], (it, j + 1))
+                        if j + 1 == ns[t] - 1:
+                            yield ("commit", q_empty[t], it)
+                yield ("commit", v_empty[gj % vstages], gj)
+                if have_next:
+                    yield ("commit", k_empty[(gj + 1) % kstages], gj + 1)
+
+    def softmax(t):
+        sc = oc = 0
+        for it, ns in enumerate(items):
+            n = ns[t]
+            if n == 0:
+                continue
+            for j in range(n):
+                yield ("wait", s_full[t], sc & 1)
+                sc += 1
+                for _ in range(rng.randint(1, 6)):
+                    yield ("work",)
+                yield ("arrive", p_full[t], (it, j))
+            yield ("wait", o_done[t], oc & 1)
+            oc += 1
+            yield ("work",)
+            yield ("arrive", o_free[t], it)
+
+    roles = {"producer": producer(), "issuer": issuer()}
+    for t in (0, 1):
+        roles.update({f"sm{t}.{w}": softmax(t) for w in range(warps_per_tile)})
+    return roles, tc
+
+
+def dq_loads_protocol(items, rng, n_warps=8, kstages=3, vstages=2):
+    """The dq kernel with its producer: Q and dO per item (q_full / q_empty),
+    each key block's K and V on the K slot's full barrier; V is released after
+    S / dP, K after dQ; dS-ready alternates between two barriers."""
+    tc = TensorCore()
+    q_full, q_empty = Barrier("q_full", 1), Barrier("q_empty", 1)
+    k_full = [Barrier(f"k_full[{s}]", 1) for s in range(kstages)]
+    k_empty = [Barrier(f"k_empty[{s}]", 1) for s in range(kstages)]
+    v_empty = [Barrier(f"v_empty[{s}]", 1) for s in range(vstages)]
+    sp_full, sp_free = Barrier("sp_full", 1), Barrier("sp_free", n_warps)
+    ds = [Barrier("ds_ready[0]", n_warps), Barrier("ds_ready[1]", n_warps)]
+    acc_done, acc_free = Barrier("acc_done", 1), Barrier("acc_free", n_warps)
+
+    def producer():
+        qu = kn = 0
+        for it, nk in enumerate(items):
+            yield ("wait", q_empty, (qu & 1) ^ 1)
+            qu += 1
+            yield ("arrive_tx", q_full, it, 2)
+            for _ in range(nk):
+                yield ("wait", k_empty[kn % kstages], ((kn // kstages) & 1) ^ 1)
+                yield ("wait", v_empty[kn % vstages], ((kn // vstages) & 1) ^ 1)
+                yield ("arrive_tx", k_full[kn % kstages], kn, 2)
+                kn += 1
+
+    def issuer():
+        qc = spf = dsc = af = kn = 0
+        for it, nk in enumerate(items):
+            yield ("wait", q_full, qc & 1)
+            qc += 1
+            g = kn
+            yield ("wait", k_full[g % kstages], (g // kstages) & 1)
+            kn += 1
+            yield ("mma",)
+            yield ("mma",)
+            yield ("commit", sp_full, g)
+            yield ("commit", v_empty[g % vstages], g)
+            for j in range(nk):
+                yield ("wait", sp_free, spf & 1)
+                spf += 1
+                if j + 1 < nk:
+                    yield ("wait", k_full[(g + j + 1) % kstages], ((g + j + 1) // kstages) & 1)
+                    kn += 1
+                    yield ("mma",)
+                    yield ("mma",)
+                    yield ("commit", sp_full, g + j + 1)
+                    yield ("commit", v_empty[(g + j + 1) % vstages], g + j + 1)
+                yield ("wait", ds[dsc & 1], (dsc >> 1) & 1)
+                dsc += 1
+                if j == 0:
+                    yield ("wait", acc_free, (af & 1) ^ 1)
+                    af += 1
+                yield ("mma",)  # dQ reads K_j
+                yield ("commit", k_empty[(g + j) % kstages], g + j)
+            yield ("commit", acc_done, it)
+            yield ("commit", q_empty, it)
+
+    def warp():
+        sp = ad = step = 0
+        for it, nk in enumerate(items):
+            for _ in range(nk):
+                yield ("wait", sp_full, sp & 1)
+                sp += 1
+                yield ("work",)
+                yield ("arrive", sp_free, step)
+                for _ in range(rng.randint(1, 6)):
+                    yield ("work",)
+                yield ("arrive", ds[step & 1], step)
+                step += 1
+            yield ("wait", acc_done, ad & 1)
+            ad += 1
+            yield ("work",)
+            yield ("arrive", acc_free, it)
+
+    roles = {"producer": producer(), "issuer": issuer()}
+    roles.update({f"warp{w}": warp() for w in range(n_warps)})
+    return roles, tc

@@ -35,3 +35,37 @@ def test_the_model_reports_a_deadlock():
 
     violations, deadlocked = bm.run({"waiter": waiter()}, bm.TensorCore(), random.Random(0))
     assert deadlocked and not violations
+
+
+def _explore_fwd(trials, seed, **kw):
+    rng = random.Random(seed)
+    for _ in range(trials):
+        items = []
+        for _ in range(rng.randint(1, 4)):
+            n0 = rng.choice([0, 1, 1, 2, 3, 5])
+            n1 = n0 + rng.choice([0, 1]) if n0 else rng.choice([0, 1, 2])
+            items.append((n0, n1))  # causal: the second query tile sees one more key tile
+        roles, tc = bm.fwd_loads_protocol(items, rng, **kw)
+        violations, deadlocked = bm.run(roles, tc, rng)
+        if violations or deadlocked:
+            return items, violations, deadlocked
+    return None
+
+
+def test_forward_with_its_producer_shared_kv_barrier():
+    assert _explore_fwd(400, 21) is None                          # bf16: K ring 2, V ring 3
+    assert _explore_fwd(300, 22, kstages=4, vstages=3) is None    # fp8 Q / K: K ring 4
+
+
+def test_dkdv_with_both_producers_shared_q_do_barrier():
+    assert bm.explore(bm.dkdv_loads_protocol, trials=400, seed=23) is None
+    assert bm.explore(bm.dkdv_loads_protocol, trials=300, seed=24, stages=4) is None  # D = 64
+
+
+def test_the_model_notices_a_missing_producer_arrival():
+    assert bm.explore(bm.dkdv_loads_protocol, trials=200, seed=25, q_full_arrivals=1) is not None
+
+
+def test_dq_with_its_producer_shared_kv_barrier():
+    assert bm.explore(bm.dq_loads_protocol, trials=400, seed=26) is None
+    assert bm.explore(bm.dq_loads_protocol, trials=300, seed=27, kstages=5, vstages=3) is None  # D = 64
