@@ -590,3 +590,134 @@ def dq_loads_protocol(items, rng, n_warps=8, kstages=3, vstages=2):
     roles = {"producer": producer(), "issuer": issuer()}
     roles.update({f"warp{w}": warp() for w in range(n_warps)})
     return roles, tc
+
+
+def dkdv_fused_protocol(items, rng, n_warps=8, stages=2, ds_in_do_slot=True):
+    """The dK/dV kernel with dq folded in (opt-in fused mode): per block also
+    dQ_qb = dS K into TMEM (dq_full), read out by the elementwise warps in the
+    next block (dq_free); at D = 128 dS lives in the block's dO slot, so its
+    store waits for dV (dv_done) and the next dP^T waits for the dQ read-out
+    (dq_region_free); at D = 64 (ds_in_do_slot False) dQ has TMEM of its own
+    and only the dQ MMA waits for the previous read-out."""
+    tc = TensorCore()
+    kv_full, kv_empty = Barrier("kv_full", 1), Barrier("kv_empty", 1)
+    q_full = [Barrier(f"q_full[{s}]", 2) for s in range(stages)]
+    q_empty = [Barrier(f"q_empty[{s}]", 1) for s in range(stages)]
+    do_empty = [Barrier(f"do_empty[{s}]", 1) for s in range(stages)]
+    st_full, dp_full = Barrier("st_full", 1), Barrier("dp_full", 1)
+    p_ready, ds_ready = Barrier("p_ready", n_warps), Barrier("ds_ready", n_warps)
+    acc_done, acc_free = Barrier("acc_done", 1), Barrier("acc_free", n_warps)
+    dq_full, dq_free = Barrier("dq_full", 1), Barrier("dq_free", n_warps)
+    dv_done = Barrier("dv_done", 1)
+    stats = [Barrier("stats_ready[0]", n_warps), Barrier("stats_ready[1]", n_warps)]
+
+    def q_producer():
+        kvu = n = 0
+        for it, nq in enumerate(items):
+            yield ("wait", kv_empty, (kvu & 1) ^ 1)
+            kvu += 1
+            yield ("arrive_tx", kv_full, it, 2)
+            for _ in range(nq):
+                yield ("wait", q_empty[n % stages], ((n // stages) & 1) ^ 1)
+                yield ("arrive_tx", q_full[n % stages], n, 1)
+                n += 1
+
+    def do_producer():
+        n = 0
+        for it, nq in enumerate(items):
+            for _ in range(nq):
+                yield ("wait", do_empty[n % stages], ((n // stages) & 1) ^ 1)
+                yield ("arrive_tx", q_full[n % stages], n, 1)
+                n += 1
+
+    def issuer():
+        st = {"kv": 0, "p": 0, "ds": 0, "af": 0, "dqf": 0, "issued": 0}
+
+        def region_free():
+            while st["dqf"] < st["issued"]:
+                yield ("wait", dq_free, st["dqf"] & 1)
+                st["dqf"] += 1
+
+        n = 0
+        for it, nq in enumerate(items):
+            yield ("wait", kv_full, st["kv"] & 1)
+            st["kv"] += 1
+            yield ("wait", q_full[n % stages], (n // stages) & 1)
+            yield ("mma",)
+            yield ("commit", st_full, n)
+            if ds_in_do_slot:
+                yield from region_free()
+            yield ("mma",)
+            yield ("commit", dp_full, n)
+            for qb in range(nq):
+                cur = n + qb
+                yield ("wait", p_ready, st["p"] & 1)
+                st["p"] += 1
+                if qb == 0:
+                    yield ("wait", acc_free, (st["af"] & 1) ^ 1)
+                    st["af"] += 1
+                yield ("mma",)  # dV reads dO
+                if ds_in_do_slot:
+                    yield ("commit", dv_done, cur)
+                if qb > 0:
+                    if ds_in_do_slot:
+                        yield from region_free()
+                    yield ("mma",)  # dP^T of this block
+                    yield ("commit", dp_full, cur)
+                if qb + 1 < nq:
+                    yield ("wait", q_full[(cur + 1) % stages], ((cur + 1) // stages) & 1)
+                    yield ("mma",)
+                    yield ("commit", st_full, cur + 1)
+                yield ("wait", ds_ready, st["ds"] & 1)
+                st["ds"] += 1
+                yield ("mma",)  # dK reads Q
+                yield ("commit", q_empty[cur % stages], cur)
+                if not ds_in_do_slot:
+                    yield from region_free()
+                yield ("mma",)  # dQ reads dS (in the dO slot at D = 128)
+                st["issued"] += 1
+                yield ("commit", dq_full, cur)
+                yield ("commit", do_empty[cur % stages], cur)
+            yield ("commit", acc_done, it)
+            yield ("commit", kv_empty, it)
+            n += nq
+
+    def warp():
+        c = {"st": 0, "dp": 0, "ad": 0, "si": 0, "dqf": 0}
+        blk = 0
+
+        def drain(tag):
+            yield ("wait", dq_full, c["dqf"] & 1)
+            c["dqf"] += 1
+            yield ("work",)
+            yield ("arrive", dq_free, tag)
+
+        for it, nq in enumerate(items):
+            for qb in range(nq):
+                yield ("arrive", stats[c["si"] & 1], c["si"])
+                yield ("wait", stats[c["si"] & 1], (c["si"] >> 1) & 1)
+                c["si"] += 1
+                yield ("wait", st_full, c["st"] & 1)
+                c["st"] += 1
+                for _ in range(rng.randint(1, 6)):
+                    yield ("work",)
+                yield ("arrive", p_ready, blk)
+                if qb > 0:
+                    yield from drain(blk - 1)
+                yield ("wait", dp_full, c["dp"] & 1)
+                c["dp"] += 1
+                yield ("work",)
+                if ds_in_do_slot:
+                    yield ("wait", dv_done, blk & 1)
+                yield ("work",)
+                yield ("arrive", ds_ready, blk)
+                blk += 1
+            yield from drain(blk - 1)
+            yield ("wait", acc_done, c["ad"] & 1)
+            c["ad"] += 1
+            yield ("work",)
+            yield ("arrive", acc_free, it)
+
+    roles = {"q_producer": q_producer(), "do_producer": do_producer(), "issuer": issuer()}
+    roles.update({f"warp{w}": warp() for w in range(n_warps)})
+    return roles, tc

@@ -69,3 +69,8 @@ def test_the_model_notices_a_missing_producer_arrival():
 def test_dq_with_its_producer_shared_kv_barrier():
     assert bm.explore(bm.dq_loads_protocol, trials=400, seed=26) is None
     assert bm.explore(bm.dq_loads_protocol, trials=300, seed=27, kstages=5, vstages=3) is None  # D = 64
+
+
+def test_fused_dq_dkdv_protocol():
+    assert bm.explore(bm.dkdv_fused_protocol, trials=400, seed=31) is None
+    assert bm.explore(bm.dkdv_fused_protocol, trials=300, seed=32, stages=4, ds_in_do_slot=False) is None
