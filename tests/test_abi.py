@@ -55,7 +55,7 @@ def _fwd_args(**kw):
     a.n_q = kw.get("n_q", N)
     a.n_k = kw.get("n_k", N)
     a.H, a.D = H, D
-    a.scale = D ** -0.5
+    a.scale = kw.get("scale", D ** -0.5)
     a.relation = kw.get("relation", _abi.ATTN_CAUSAL)
     a.dtype = kw.get("dtype", _abi.ATTN_F16)
     a.o_dtype = kw.get("o_dtype", a.dtype)
@@ -92,6 +92,10 @@ def _fwd_args(**kw):
     ({"qk_fp8": 1}, _abi.ATTN_EUNSUPPORTED),                   # fp8 Q / K: D = 128 only
     ({"qk_fp8": 1, "D": 128, "dtype": _abi.ATTN_F32}, _abi.ATTN_EUNSUPPORTED),  # v 16-bit
     ({"qk_fp8": 1, "D": 128, "kernel": _abi.ATTN_KERNEL_SIMT}, _abi.ATTN_EUNSUPPORTED),
+    ({"scale": float("nan")}, _abi.ATTN_EINVAL),
+    ({"scale": float("inf")}, _abi.ATTN_EINVAL),
+    ({"scale": float("-inf")}, _abi.ATTN_EINVAL),
+    ({"qk_fp8": 1, "D": 128, "scale": 0.0}, _abi.ATTN_EUNSUPPORTED),  # fp8 Q / K: positive scales
 ])
 def test_forward_argument_validation(kw, code):
     lib = _abi.load()
