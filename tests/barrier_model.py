@@ -721,3 +721,36 @@ def dkdv_fused_protocol(items, rng, n_warps=8, stages=2, ds_in_do_slot=True):
     roles = {"q_producer": q_producer(), "do_producer": do_producer(), "issuer": issuer()}
     roles.update({f"warp{w}": warp() for w in range(n_warps)})
     return roles, tc
+
+
+def sched_ring_protocol(n_items, rng, n_consumers=10, counted_consumers=None, record=None):
+    """The two-slot ring through which a CTA's producer warp hands its work
+    items to the other roles (sched_full: one arrival; sched_empty: one per
+    consumer).  Each consumer must read the items in order: `record` collects
+    what every consumer read.  counted_consumers < n_consumers models a
+    consumer left out of sched_empty's count."""
+    tc = TensorCore()
+    counted = n_consumers if counted_consumers is None else counted_consumers
+    full = [Barrier(f"sched_full[{s}]", 1) for s in (0, 1)]
+    empty = [Barrier(f"sched_empty[{s}]", counted) for s in (0, 1)]
+    slot_value = [None, None]
+    seen = record if record is not None else {}
+
+    def producer():
+        for i in range(n_items + 1):  # the last item is the end marker
+            s = i & 1
+            yield ("wait", empty[s], ((i >> 1) & 1) ^ 1)
+            slot_value[s] = i
+            yield ("arrive", full[s], i)
+
+    def consumer(c):
+        got = seen.setdefault(c, [])
+        for i in range(n_items + 1):
+            s = i & 1
+            yield ("wait", full[s], (i >> 1) & 1)
+            got.append(slot_value[s])
+            yield ("arrive", empty[s], i)
+
+    roles = {"producer": producer()}
+    roles.update({f"c{c}": consumer(c) for c in range(n_consumers)})
+    return roles, tc

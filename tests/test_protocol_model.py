@@ -74,3 +74,24 @@ def test_dq_with_its_producer_shared_kv_barrier():
 def test_fused_dq_dkdv_protocol():
     assert bm.explore(bm.dkdv_fused_protocol, trials=400, seed=31) is None
     assert bm.explore(bm.dkdv_fused_protocol, trials=300, seed=32, stages=4, ds_in_do_slot=False) is None
+
+
+def _ring_runs(trials, seed, **kw):
+    rng = random.Random(seed)
+    for _ in range(trials):
+        n = rng.randint(1, 6)
+        seen = {}
+        roles, tc = bm.sched_ring_protocol(n, rng, record=seen, **kw)
+        violations, deadlocked = bm.run(roles, tc, rng)
+        wrong = any(v != list(range(n + 1)) for v in seen.values())
+        if violations or deadlocked or wrong:
+            return n, seen, violations, deadlocked
+    return None
+
+
+def test_work_item_ring_hands_every_item_to_every_consumer():
+    assert _ring_runs(400, 41, n_consumers=10) is None  # dK/dV: issuer, 8 warps, dO producer
+
+
+def test_the_model_notices_an_uncounted_ring_consumer():
+    assert _ring_runs(400, 42, n_consumers=10, counted_consumers=9) is not None
