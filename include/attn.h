@@ -120,7 +120,9 @@ typedef struct attn_fwd_args {
     float *lse;           /* out: (H, n_q) f32, natural-log row log-sum-exp; may be NULL */
     int32_t n_q, n_k;     /* total query / key tokens */
     int32_t H, D;         /* heads; head dim (64 or 128) */
-    float scale;          /* score scale, usually D^-1/2 */
+    float scale;          /* score scale, usually D^-1/2: any finite value (0 gives the
+                             uniform average of the admitted values, a negative one
+                             is accepted); NaN or +-inf: ATTN_EINVAL */
     int32_t relation;     /* attn_relation */
     int32_t dtype;        /* attn_dtype of q, k, v */
     int32_t o_dtype;      /* attn_dtype of o: dtype or ATTN_F32 */
