@@ -4,7 +4,9 @@ configuration the benchmark uses (AUTO kernel choice, one CTA per SM).
 Small workloads are compared element by element with the oracle; the large
 ones on sampled (token, head) rows that the oracle computes one by one:
 segment ends, tile edges and random rows for O / lse / dq, and sampled key
-rows for dk / dv."""
+rows of six (sequence, head) pairs of the training workload -- the first and
+the last head among them -- for dk / dv, each pair held to the gradient bar
+on its own."""
 import numpy as np
 import pytest
 import torch
@@ -75,15 +77,29 @@ def test_causal_training_workload_sampled():
     check_o(_at(o, toks, heads), o_ref, x["q"].dtype, o.dtype)
     check_lse(_at(lse, heads, toks), lse_ref)
 
-    # gradients: dq on sampled rows; dk, dv on sampled keys of two (sequence, head) pairs
+    # gradients on six (sequence, head) pairs, (b0, h0) and the last head (b3,
+    # h31) among them: dk, dv on sampled keys (tile edges and random keys) of
+    # every pair; dq on the sampled rows above plus tile-edge rows of every pair
+    L = w.n_q
+    pairs = [(0, 0), (0, 31), (1, 11), (2, 22), (3, 0), (3, 31)]
     rng = np.random.default_rng(55)
-    kt = np.concatenate([rng.integers(0, 8192, 24), [0, 8191, 127, 128],
-                         3 * 8192 + rng.integers(0, 8192, 24), [4 * 8192 - 1]]).astype(np.int64)
-    kh = np.array([0] * 28 + [31] * 25, dtype=np.int32)
+    kt, kh, qt, qh = [], [], [], []
+    for b, h in pairs:
+        keys = np.concatenate([rng.integers(0, L, 12), [0, 127, 128, L - 1]])
+        kt += list(b * L + keys)
+        kh += [h] * len(keys)
+        rows = np.concatenate([rng.integers(0, L, 6), [0, 255, 256, L - 1]])
+        qt += list(b * L + rows)
+        qh += [h] * len(rows)
+    kt, kh = np.array(kt, dtype=np.int64), np.array(kh, dtype=np.int32)
+    qt = np.concatenate([np.array(qt, dtype=np.int64), toks[:120]])
+    qh = np.concatenate([np.array(qh, dtype=np.int32), heads[:120]])
     rq, rk, rv = oracle.bwd(x["q"], x["k"], x["v"], x["dO"], causal=True, cu_seqlens_q=cu,
-                            q_rows=(toks[:120], heads[:120]), k_rows=(kt, kh))
-    check_grad(_at(dq, toks[:120], heads[:120]), rq, "dq")
-    check_grad(_at(dk, kt, kh), rk, "dk")
-    check_grad(_at(dv, kt, kh), rv, "dv")
+                            q_rows=(qt, qh), k_rows=(kt, kh))
+    check_grad(_at(dq, qt, qh), rq, "dq")
+    for i, (b, h) in enumerate(pairs):
+        sl = slice(16 * i, 16 * (i + 1))
+        check_grad(_at(dk, kt[sl], kh[sl]), rk[sl], f"dk (b{b}, h{h})")
+        check_grad(_at(dv, kt[sl], kh[sl]), rv[sl], f"dv (b{b}, h{h})")
     for g in (dq, dk, dv):
         assert bool(torch.isfinite(g).all())
