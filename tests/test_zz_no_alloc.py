@@ -5,12 +5,15 @@ that a host framework calls with tensors it owns, with no allocator or
 workspace to hand, or a serving loop that must not call cudaMalloc.  The entry
 point takes its scheduler scratch from a fixed array inside the library.
 
-These tests call it through the C ABI and check that it returns what the
-regular attn_fwd returns (within the forward parity tolerances), on two calls
-in a row with different problems, and that it rejects a sequence count beyond
-its fixed scratch.  The file sorts last so that a run stopping at the first
-failure has already run every other test; it also passes on its own in a
-fresh process (the first call sets up the scratch address).
+These tests call it through the C ABI on two calls in a row with different
+problems (and the first problem once more after the second, since the shared
+array keeps the last call's contents), and check each result against the f64
+oracle element by element at the forward tolerances, and bit for bit against
+the regular attn_fwd run with the same schedule (num_splits = 1, the only one
+the fixed scratch allows).  They also check that a sequence count beyond the
+fixed scratch is rejected.  The file sorts last so that a run stopping at the
+first failure has already run every other test; it also passes on its own in
+a fresh process (the first call sets up the scratch address).
 """
 import ctypes
 
@@ -19,7 +22,9 @@ import torch
 
 import attn_inputs
 import online_softmax_attention_gb300 as attn
+import oracle
 from online_softmax_attention_gb300 import _abi
+from parity_util import check_lse, check_o
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -33,10 +38,10 @@ def _inputs(case):
     return x, False, None
 
 
-def _call(x, causal, out_dtype):
+def _call(x, causal, out_dtype, num_splits=1):
     q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
     return attn.FwdCall(q, k, v, causal=causal, cu_seqlens_q=x["cu_seqlens_q"],
-                        cu_seqlens_k=x["cu_seqlens_k"], out_dtype=out_dtype)
+                        cu_seqlens_k=x["cu_seqlens_k"], out_dtype=out_dtype, num_splits=num_splits)
 
 
 def _noalloc(call):
@@ -45,33 +50,40 @@ def _noalloc(call):
     return lib.attn_fwd_noalloc(ctypes.byref(call.args), ctypes.c_void_p(s.cuda_stream))
 
 
-def _close(o, o_ref, lse, lse_ref):
-    # forward parity bounds: max|err| <= 1e-2 on O, <= 1e-3 on lse
-    assert (o.float() - o_ref.float()).abs().max().item() <= 1e-2
-    assert (lse - lse_ref).abs().max().item() <= 1e-3
+def _check(call, x, causal, o_ref, lse_ref):
+    # against the oracle at the forward bounds, and bit for bit against attn_fwd
+    # with the same (unsplit) schedule
+    ro, rl = oracle.fwd(x["q"], x["k"], x["v"], causal=causal, cu_seqlens_q=x["cu_seqlens_q"],
+                        cu_seqlens_k=x["cu_seqlens_k"])
+    check_o(call.o, ro, x["q"].dtype, call.o.dtype)
+    check_lse(call.lse, rl)
+    assert torch.equal(call.o, o_ref)
+    assert torch.equal(call.lse, lse_ref)
 
 
-def test_noalloc_matches_attn_fwd_on_two_calls_in_a_row():
+def test_noalloc_matches_the_oracle_and_attn_fwd_on_two_calls_in_a_row():
     results = []
     for case in ("varlen", "single"):
         x, causal, odt = _inputs(case)
-        ref = _call(x, causal, odt)
+        ref = _call(x, causal, odt, num_splits=1)
         o_ref, lse_ref = (t.clone() for t in ref.run())
+        torch.cuda.synchronize()
         call = _call(x, causal, odt)
         call.o.fill_(float("nan"))
         call.lse.fill_(float("nan"))
         assert _noalloc(call) == _abi.ATTN_OK
         torch.cuda.synchronize()
         assert attn.device_status() == 0
-        _close(call.o, o_ref, call.lse, lse_ref)
-        results.append((call, o_ref, lse_ref))
+        _check(call, x, causal, o_ref, lse_ref)
+        results.append((call, x, causal, o_ref, lse_ref))
     # the first problem again: the scratch keeps the second call's contents
-    call, o_ref, lse_ref = results[0]
+    call, x, causal, o_ref, lse_ref = results[0]
     call.o.zero_()
+    call.lse.zero_()
     assert _noalloc(call) == _abi.ATTN_OK
     torch.cuda.synchronize()
     assert attn.device_status() == 0
-    _close(call.o, o_ref, call.lse, lse_ref)
+    _check(call, x, causal, o_ref, lse_ref)
 
 
 def test_noalloc_rejects_more_sequences_than_its_scratch_holds():
