@@ -64,7 +64,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 4
+#define ATTN_ABI_VERSION 5
 
 #if defined(__GNUC__)
 #define ATTN_API __attribute__((visibility("default")))
@@ -244,14 +244,20 @@ ATTN_API size_t attn_csr_args_size(void);
 /* Bytes of device workspace the call needs (depends on n_seq, H, n_q, and
  * for the forward on the number of key splits: n_splits > 1 adds the partial
  * results, n_splits * n_q * H * (D + 1) * 4 bytes; for the backward on the dq
- * mode: ATTN_DQ_FUSED adds the dq partial sums, n_q * H * D * 4 bytes). */
+ * mode: ATTN_DQ_FUSED adds the dq partial sums, n_q * H * D * 4 bytes).
+ * Only sizes, dtypes, the relation, the kernel choice, num_splits and whether
+ * cu_seqlens are given are read: the tensor and workspace pointers may still
+ * be unset.  Arguments the call would reject give the unsplit size. */
 ATTN_API size_t attn_fwd_workspace_bytes(const attn_fwd_args *a);
 ATTN_API size_t attn_bwd_workspace_bytes(const attn_bwd_args *a);
 
 /* Forward: writes o and lse.  Launches a schedule-preparation kernel and one
  * persistent attention kernel on `stream`; with key splits (split-K) the
  * attention kernel writes one partial result per split into the workspace
- * and a merge kernel (as attn_merge) combines them into o and lse. */
+ * and a merge kernel (as attn_merge) combines them into o and lse.  One
+ * sequence (no cu_seqlens) whose work items fit in one wave of the default
+ * grid (num_ctas = 0) needs no preparation: the attention kernel then runs
+ * one item per CTA and is the only launch (plus the merge when split). */
 ATTN_API int attn_fwd(const attn_fwd_args *a, void *stream);
 
 /* Key splits a forward with these arguments runs (>= 1), resolving
@@ -292,12 +298,25 @@ ATTN_API int attn_bwd_dkdv(const attn_bwd_args *a, void *stream);
 ATTN_API int attn_bwd_dq(const attn_bwd_args *a, void *stream);
 
 /* Flat form for contiguous (N, H, D) self-attention tensors (token stride
- * H*D, head stride D), o in the input dtype, AUTO kernel choice.
- * cu_seqlens: device, n_seq+1 entries, or NULL for one sequence. */
+ * H*D, head stride D), o in the input dtype, AUTO kernel choice and AUTO key
+ * splits (the same schedule attn_fwd picks for these arguments).
+ * cu_seqlens: device, n_seq+1 entries, or NULL for one sequence (n_seq is
+ * then ignored).  workspace: device, 256-byte aligned, at least
+ * attn_fwd_simple_workspace_bytes(N, H, D, relation, n_seq, dtype) bytes
+ * (ATTN_EWORKSPACE otherwise).  Defined as in attn_fwd (TIGA-lang attention
+ * examples page, section "全量注意力，无掩码", and its causal and varlen
+ * sections). */
 ATTN_API int attn_fwd_simple(const void *q, const void *k, const void *v, void *out, float *lse,
                     int32_t N, int32_t H, int32_t D, float scale, int32_t relation,
                     const int32_t *cu_seqlens, int32_t n_seq, int32_t dtype,
                     void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes attn_fwd_simple needs for these sizes (n_seq: the number of
+ * sequences cu_seqlens will describe, 1 without cu_seqlens); host-only.  Large
+ * enough for any key-split count the library may choose on the current device;
+ * 0 for n_seq < 1. */
+ATTN_API size_t attn_fwd_simple_workspace_bytes(int32_t N, int32_t H, int32_t D, int32_t relation,
+                                                int32_t n_seq, int32_t dtype);
 
 /* The kernel family a call with these arguments runs (ATTN_KERNEL_SIMT or
  * ATTN_KERNEL_TC, resolving AUTO), or a negative attn_status if the call
@@ -323,6 +342,8 @@ ATTN_API int attn_csr_fwd(const attn_csr_args *a, void *stream);
  *    ATTN_EUNSUPPORTED before any launch.
  *  - The first call on a device looks up the array's device address (with
  *    that device current); make that first call before any stream capture.
+ *    The address is kept per device ordinal, so calls must run in the
+ *    device's primary context (the CUDA runtime's default context).
  *  - All calls share the one array and each call rewrites the part it reads,
  *    so calls whose kernels overlap on the GPU (concurrent streams, or
  *    threads on one device) race: serialise them on one stream. */
@@ -346,7 +367,9 @@ ATTN_API int attn_device_status(void *stream);
 /* Diagnostic: y[i] = 2^x[i] computed by the polynomial exp2 that the
  * tensor-core kernels run on the FMA pipe for part of the softmax (Cody-Waite
  * range reduction, degree-4 polynomial; max relative error 2.9e-6 for
- * -126 <= x <= 127).  x, y: device arrays of n floats. */
+ * -126 <= x <= 127; x is clamped to that range first, so larger arguments
+ * give about 2^127 and smaller ones about 2^-126).  x, y: device arrays of n
+ * floats. */
 ATTN_API int attn_selftest_exp2(const float *x, float *y, int32_t n, void *stream);
 
 /* Number of kernels the library has launched in this process (all devices). */

@@ -12,7 +12,7 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_lib", "libattn_gb300.so")
 
-ABI_VERSION = 4
+ABI_VERSION = 5
 
 ATTN_OK, ATTN_EINVAL, ATTN_EUNSUPPORTED, ATTN_ECUDA, ATTN_ETIMEOUT, ATTN_EWORKSPACE = 0, -1, -2, -3, -4, -5
 ATTN_F16, ATTN_BF16, ATTN_F32 = 0, 1, 2
@@ -31,7 +31,7 @@ EXPORTS = (
     "attn_fwd_selected_kernel", "attn_bwd_selected_kernel", "attn_fwd_noalloc",
     "attn_selftest_exp2", "attn_set_watchdog_cycles", "attn_merge_args_size",
     "attn_fwd_num_splits", "attn_merge", "attn_csr_args_size", "attn_csr_fwd",
-    "attn_bwd_selected_dq_mode",
+    "attn_bwd_selected_dq_mode", "attn_fwd_simple_workspace_bytes",
 )
 
 
@@ -124,6 +124,7 @@ def load() -> ctypes.CDLL:
         "attn_bwd_dq": (ctypes.c_int, [ba, vp]),
         "attn_fwd_simple": (ctypes.c_int, [vp, vp, vp, vp, vp, i32, i32, i32, ctypes.c_float, i32,
                                            vp, i32, i32, vp, sz, vp]),
+        "attn_fwd_simple_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32]),
         "attn_device_status": (ctypes.c_int, [vp]),
         "attn_fwd_selected_kernel": (ctypes.c_int, [fa]),
         "attn_fwd_noalloc": (ctypes.c_int, [fa, vp]),

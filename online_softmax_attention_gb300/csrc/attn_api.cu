@@ -175,8 +175,11 @@ FwdLayout fwd_layout(int n_seq, int n_q, int H, int D, int splits) {
 }
 
 // Validates everything but the workspace and fills the kernel parameters that
-// do not depend on it; resolves the kernel family and the key splits.
-int plan_fwd(const attn_fwd_args *a, FwdParams &p, bool &use_tc) {
+// do not depend on it; resolves the kernel family and the key splits.  With
+// `check_views` false the tensor pointers and strides are not looked at (the
+// workspace size depends on sizes only, so a caller may size it before its
+// tensors exist).
+int plan_fwd(const attn_fwd_args *a, FwdParams &p, bool &use_tc, bool check_views = true) {
     if (!a) return ATTN_EINVAL;
     int rc = check_common(a->n_q, a->n_k, a->H, a->D, a->relation, a->dtype, a->n_seq,
                           a->cu_seqlens_q, a->cu_seqlens_k, a->scale);
@@ -196,7 +199,8 @@ int plan_fwd(const attn_fwd_args *a, FwdParams &p, bool &use_tc) {
     const bool any_q = a->n_q > 0, any_k = a->n_k > 0;
     const bool qk_ok = a->qk_fp8 ? valid_view_bytes(a->q, 1, any_q) && valid_view_bytes(a->k, 1, any_k)
                                  : valid_view(a->q, a->dtype, any_q) && valid_view(a->k, a->dtype, any_k);
-    if (!qk_ok || !valid_view(a->o, a->o_dtype, any_q) || !valid_view(a->v, a->dtype, any_k))
+    if (check_views &&
+        (!qk_ok || !valid_view(a->o, a->o_dtype, any_q) || !valid_view(a->v, a->dtype, any_k)))
         return ATTN_EINVAL;
     std::memset(&p, 0, sizeof(p));
     p.qk_fp8 = a->qk_fp8;
@@ -390,7 +394,7 @@ size_t attn_fwd_workspace_bytes(const attn_fwd_args *a) {
     FwdParams p;
     bool use_tc = false;
     // arguments the forward would reject need no split buffers
-    const int splits = plan_fwd(a, p, use_tc) == ATTN_OK ? p.n_splits : 1;
+    const int splits = plan_fwd(a, p, use_tc, false) == ATTN_OK ? p.n_splits : 1;
     return fwd_layout(a->n_seq, a->n_q > 0 ? a->n_q : 0, a->H > 0 ? a->H : 0,
                       a->D > 0 ? a->D : 0, splits).total;
 }
@@ -417,16 +421,25 @@ int attn_fwd(const attn_fwd_args *a, void *stream) {
                      use_tc ? "tc" : "simt", p.n_splits, (double)a->prune_threshold);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int block = use_tc ? tc_fwd_block_rows(p) : kSimtBlock;
-    cudaError_t e = launch_prep(p.cu_q, p.cu_k, p.n_seq, p.n_q, p.n_k, p.H, block, p.causal, 0,
-                                p.n_splits, p.sched, p.status, s);
+    // One sequence whose work items all fit in one wave of the default grid:
+    // static schedule (CTA i runs item i), no preparation launch.
+    const int64_t items = ((int64_t)p.n_q + block - 1) / block * p.H * p.n_splits;
+    if (!p.cu_q && a->num_ctas == 0 &&
+        items <= (int64_t)sm_count() * (use_tc ? 1 : fwd_simt_ctas_per_sm(p)))
+        p.static_items = (int)items;
+    cudaError_t e = cudaSuccess;
+    if (!p.static_items)
+        e = launch_prep(p.cu_q, p.cu_k, p.n_seq, p.n_q, p.n_k, p.H, block, p.causal, 0, p.n_splits,
+                        p.sched, p.status, s);
     if (e != cudaSuccess) return set_cuda_error(e);
+    const int grid = p.static_items ? p.static_items : a->num_ctas;
     if (p.n_splits == 1) {
-        e = use_tc ? launch_fwd_tc(p, a->num_ctas, s) : launch_fwd_simt(p, a->num_ctas, s);
+        e = use_tc ? launch_fwd_tc(p, grid, s) : launch_fwd_simt(p, grid, s);
     } else {
         FwdParams part;
         MergeParams m;
         split_params(a, p, part, m);
-        e = use_tc ? launch_fwd_tc(part, a->num_ctas, s) : launch_fwd_simt(part, a->num_ctas, s);
+        e = use_tc ? launch_fwd_tc(part, grid, s) : launch_fwd_simt(part, grid, s);
         if (e == cudaSuccess) e = launch_merge(m, s);
     }
     if (e != cudaSuccess) return set_cuda_error(e);
@@ -534,10 +547,15 @@ int attn_bwd(const attn_bwd_args *a, void *stream) {
     return attn_bwd_dq(a, stream);
 }
 
-int attn_fwd_simple(const void *q, const void *k, const void *v, void *out, float *lse,
-                    int32_t N, int32_t H, int32_t D, float scale, int32_t relation,
-                    const int32_t *cu_seqlens, int32_t n_seq, int32_t dtype, void *workspace,
-                    size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+namespace {
+
+// The argument struct of the flat form: contiguous (N, H, D) tensors (token
+// stride H * D, head stride D), o in the input dtype, AUTO kernel and splits.
+attn_fwd_args simple_args(const void *q, const void *k, const void *v, void *out, float *lse,
+                          int32_t N, int32_t H, int32_t D, float scale, int32_t relation,
+                          const int32_t *cu_seqlens, int32_t n_seq, int32_t dtype) {
     attn_fwd_args a;
     std::memset(&a, 0, sizeof(a));
     const int64_t st = (int64_t)H * D;
@@ -554,10 +572,33 @@ int attn_fwd_simple(const void *q, const void *k, const void *v, void *out, floa
     a.dtype = a.o_dtype = dtype;
     a.n_seq = cu_seqlens ? n_seq : 1;
     a.cu_seqlens_q = a.cu_seqlens_k = cu_seqlens;
+    a.kernel = ATTN_KERNEL_AUTO;
+    return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd_simple(const void *q, const void *k, const void *v, void *out, float *lse,
+                    int32_t N, int32_t H, int32_t D, float scale, int32_t relation,
+                    const int32_t *cu_seqlens, int32_t n_seq, int32_t dtype, void *workspace,
+                    size_t workspace_bytes, void *stream) {
+    attn_fwd_args a = simple_args(q, k, v, out, lse, N, H, D, scale, relation, cu_seqlens, n_seq, dtype);
     a.workspace = workspace;
     a.workspace_bytes = workspace_bytes;
-    a.kernel = ATTN_KERNEL_AUTO;
     return attn_fwd(&a, stream);
+}
+
+size_t attn_fwd_simple_workspace_bytes(int32_t N, int32_t H, int32_t D, int32_t relation,
+                                       int32_t n_seq, int32_t dtype) {
+    if (n_seq < 1) return 0;
+    // only the presence of cu_seqlens matters for the size (n_seq > 1 needs it);
+    // this placeholder is never dereferenced
+    static const int32_t placeholder[2] = {0, 0};
+    const attn_fwd_args a = simple_args(nullptr, nullptr, nullptr, nullptr, nullptr, N, H, D, 1.f,
+                                        relation, n_seq > 1 ? placeholder : nullptr, n_seq, dtype);
+    return attn_fwd_workspace_bytes(&a);
 }
 
 int attn_fwd_selected_kernel(const attn_fwd_args *a) {

@@ -100,6 +100,30 @@ __device__ __forceinline__ WorkItem map_item(int w, const int *prefix, int n_seq
     return {lo, h, t, ntiles, c};
 }
 
+// The same mapping for one sequence (no cu_seqlens) of `total` items, which
+// needs no prefix from the workspace.
+__device__ __forceinline__ WorkItem map_item_single(int w, int total, int H, bool descending,
+                                                    int splits = 1) {
+    const int per_head = total / H;  // tiles * splits
+    const int h = w / per_head;
+    const int rem = w - h * per_head;
+    int t = splits == 1 ? rem : rem / splits;
+    const int c = rem - t * splits;
+    const int ntiles = per_head / splits;
+    if (descending) t = ntiles - 1 - t;
+    return {0, h, t, ntiles, c};
+}
+
+// Work-item fetch of the persistent kernels.  Dynamic schedule (static_items
+// = 0): items come from the global counter that the preparation kernel reset.
+// Static schedule (static_items > 0: one sequence whose items all fit in one
+// wave, grid = static_items): CTA i runs item i and nothing else, so neither a
+// counter nor a preparation launch is needed.  `k` counts this CTA's fetches.
+__device__ __forceinline__ int fetch_item(int *counter, int static_items, int k) {
+    if (static_items > 0) return k == 0 ? (int)blockIdx.x : static_items;
+    return atomicAdd(counter, 1);
+}
+
 // Offsets of sequence b (one sequence when cu is null).
 __device__ __forceinline__ void seq_bounds(const int32_t *cu, int total, int b, int &start, int &len) {
     if (cu) {

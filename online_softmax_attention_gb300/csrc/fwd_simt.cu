@@ -96,19 +96,20 @@ __global__ void __launch_bounds__(NT) fwd_simt_kernel(const FwdParams p) {
     __shared__ float s_tile_max[NT / 32];  // tile pruning: per-warp largest score
 
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-    const int total = p.sched.hdr[1];
+    const int total = p.static_items > 0 ? p.static_items : p.sched.hdr[1];
     const Tin *gq = static_cast<const Tin *>(p.q);
     const Tin *gk = static_cast<const Tin *>(p.k);
     const Tin *gv = static_cast<const Tin *>(p.v);
     Tout *go = static_cast<Tout *>(p.o);
 
-    for (;;) {
-        if (tid == 0) s_w = atomicAdd(p.sched.hdr, 1);
+    for (int fetch = 0;; ++fetch) {
+        if (tid == 0) s_w = fetch_item(p.sched.hdr, p.static_items, fetch);
         __syncthreads();
         const int w = s_w;
         __syncthreads();
         if (w >= total) break;
-        const WorkItem it = map_item(w, p.sched.prefix, p.n_seq, p.H, true, p.n_splits);
+        const WorkItem it = p.static_items > 0 ? map_item_single(w, p.static_items, p.H, true, p.n_splits)
+                                               : map_item(w, p.sched.prefix, p.n_seq, p.H, true, p.n_splits);
         int q_start, Lq, k_start, Lk;
         seq_bounds(p.cu_q, p.n_q, it.b, q_start, Lq);
         seq_bounds(p.cu_k, p.n_k, it.b, k_start, Lk);

@@ -10,7 +10,9 @@
 // Work item: 256 query rows of one (sequence, head), split in two 128-row
 // tiles (t = 0, 1) that ping-pong between the tensor core and the softmax
 // warps.  Items are taken from a global counter (persistent grid, one CTA per
-// SM) and broadcast to the warp roles through a two-slot shared ring.
+// SM) and broadcast to the warp roles through a two-slot shared ring; a single
+// sequence whose items fit in one wave runs one item per CTA instead (static
+// schedule, no counter, one launch).
 //
 // Warp roles (12 warps):
 //   warp 0      TMA producer: Q tiles, then K_j, V_j tiles into a ring of
@@ -137,8 +139,15 @@ struct ItemInfo {
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
+// Items in the schedule (static: known at launch; dynamic: written by the
+// preparation kernel).
+__device__ __forceinline__ int total_items(const FwdParams &p) {
+    return p.static_items > 0 ? p.static_items : p.sched.hdr[1];
+}
+
 __device__ __forceinline__ ItemInfo item_info(const FwdParams &p, int w) {
-    const WorkItem it = map_item(w, p.sched.prefix, p.n_seq, p.H, true, p.n_splits);
+    const WorkItem it = p.static_items > 0 ? map_item_single(w, p.static_items, p.H, true, p.n_splits)
+                                           : map_item(w, p.sched.prefix, p.n_seq, p.H, true, p.n_splits);
     ItemInfo f;
     seq_bounds(p.cu_q, p.n_q, it.b, f.q_start, f.Lq);
     seq_bounds(p.cu_k, p.n_k, it.b, f.k_start, f.Lk);
@@ -182,7 +191,7 @@ __device__ void producer(const TcFwdArgs &a, FwdBars &bars, int *sched_item, uin
                          uint32_t sV, const Watchdog &wd) {
     using C = Cfg<D, kF8>;
     const FwdParams &p = a.p;
-    const int total = p.sched.hdr[1];
+    const int total = total_items(p);
     RingPos<C::kKStages> kr;
     RingPos<C::kVStages> vr;
     uint32_t q_uses[NQT] = {0, 0};
@@ -206,7 +215,7 @@ __device__ void producer(const TcFwdArgs &a, FwdBars &bars, int *sched_item, uin
     for (int i = 0;; ++i) {
         const int slot = i & 1;
         if (!mbar_wait(smem_u32(&bars.sched_empty[slot]), ((i >> 1) & 1) ^ 1, wd)) break;
-        const int w = atomicAdd(p.sched.hdr, 1);
+        const int w = fetch_item(p.sched.hdr, p.static_items, i);
         sched_item[slot] = w;
         mbar_arrive(smem_u32(&bars.sched_full[slot]));
         if (w >= total) break;
@@ -250,7 +259,7 @@ __device__ void mma_issuer(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
                            uint32_t tmem, const Watchdog &wd) {
     using C = Cfg<D, kF8>;
     const FwdParams &p = a.p;
-    const int total = p.sched.hdr[1];
+    const int total = total_items(p);
     // a negative scale negates Q in the score MMA (A-negate bit), so the softmax
     // always scales by |scale| (fp8 Q / K take positive scales only)
     const uint32_t idS = kF8 ? idesc_f8(BM, BN)
@@ -359,7 +368,7 @@ template <int D, bool kBF16, typename Tout, bool kPrune>
 __device__ void softmax_wg(const TcFwdArgs &a, FwdBars &bars, const int *sched_item, PruneShared *ps,
                            uint32_t tmem, const Watchdog &wd) {
     const FwdParams &p = a.p;
-    const int total = p.sched.hdr[1];
+    const int total = total_items(p);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = (warp - 4) >> 2;    // query tile of this warpgroup
     const int quarter = warp & 3;     // TMEM lane quarter this warp may access

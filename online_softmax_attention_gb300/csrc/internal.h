@@ -32,6 +32,10 @@ struct FwdParams {
     int n_seq;
     const int32_t *cu_q, *cu_k;  // null => one sequence
     Sched sched;
+    // > 0: static schedule of one sequence (cu_q, cu_k null) with this many
+    // work items, one per CTA of a grid of exactly this size; the workspace's
+    // schedule block is neither written nor read.  0: dynamic schedule.
+    int static_items;
     int *status;
     long long watchdog_cycles;
     // split-K: key tiles of every query tile cut into n_splits chunks; chunk c

@@ -263,3 +263,62 @@ def test_csr_without_rows_launches_nothing():
     before = lib.attn_launch_count()
     assert lib.attn_csr_fwd(ctypes.byref(_csr_args(n_dst=0)), None) == _abi.ATTN_OK
     assert lib.attn_launch_count() == before
+
+
+def test_workspace_size_does_not_depend_on_the_pointers():
+    """A caller may size the workspace before its tensors exist: the size
+    depends on sizes, dtypes, relation and splits only."""
+    lib = _abi.load()
+    for splits in (0, 1, 5):
+        a = _fwd_args(H=3, D=128, N=1000, num_splits=splits, relation=_abi.ATTN_FULL)
+        with_ptrs = lib.attn_fwd_workspace_bytes(ctypes.byref(a))
+        for name in ("q", "k", "v", "o"):
+            setattr(a, name, _abi.AttnTensor(None, 0, 0))
+        a.lse = None
+        assert lib.attn_fwd_workspace_bytes(ctypes.byref(a)) == with_ptrs
+
+
+@pytest.mark.parametrize("N,H,D,rel,n_seq,dt", [
+    (256, 2, 64, _abi.ATTN_CAUSAL, 1, _abi.ATTN_F16),
+    (1024, 4, 64, _abi.ATTN_FULL, 1, _abi.ATTN_F16),
+    (1178, 4, 128, _abi.ATTN_CAUSAL, 5, _abi.ATTN_BF16),
+    (8192, 1, 64, _abi.ATTN_FULL, 1, _abi.ATTN_F32),
+])
+def test_simple_form_workspace_matches_the_struct_form(N, H, D, rel, n_seq, dt):
+    """attn_fwd_simple_workspace_bytes sizes exactly what attn_fwd needs for
+    the flat form's arguments (contiguous (N, H, D), AUTO kernel and splits)."""
+    lib = _abi.load()
+    a = _fwd_args(H=H, D=D, N=N, relation=rel, dtype=dt, num_splits=0)
+    if n_seq > 1:
+        a.n_seq = n_seq
+        a.cu_seqlens_q = a.cu_seqlens_k = FAKE
+    want = lib.attn_fwd_workspace_bytes(ctypes.byref(a))
+    got = lib.attn_fwd_simple_workspace_bytes(N, H, D, rel, n_seq, dt)
+    assert got == want and got > 0 and got % 256 == 0
+    assert lib.attn_fwd_simple_workspace_bytes(N, H, D, rel, 0, dt) == 0
+
+
+def test_simple_form_rejects_a_short_workspace_before_launch():
+    lib = _abi.load()
+    need = lib.attn_fwd_simple_workspace_bytes(256, 2, 64, _abi.ATTN_CAUSAL, 1, _abi.ATTN_F16)
+    before = lib.attn_launch_count()
+    rc = lib.attn_fwd_simple(FAKE, FAKE, FAKE, FAKE, FAKE, 256, 2, 64, 0.125, _abi.ATTN_CAUSAL,
+                             None, 1, _abi.ATTN_F16, FAKE, need - 256, None)
+    assert rc == _abi.ATTN_EWORKSPACE
+    assert lib.attn_launch_count() == before
+
+
+def test_library_source_allocates_no_device_memory():
+    """Every entry point works in caller-owned memory (workspace, or the fixed
+    array of the allocation-free forward): no allocation or free call appears
+    in the library's sources."""
+    csrc = os.path.join(ROOT, "online_softmax_attention_gb300", "csrc")
+    banned = re.compile(r"\b(cudaMalloc\w*|cudaFree\w*|cuMemAlloc\w*|cuMemFree\w*|"
+                        r"cudaHostAlloc|cudaMallocHost|cuMemCreate|cuMemMap)\s*\(")
+    seen = []
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name)) as f:
+            for i, line in enumerate(f, 1):
+                if banned.search(line.split("//")[0]):
+                    seen.append(f"{name}:{i}: {line.strip()}")
+    assert not seen, "allocation calls in the library: " + "; ".join(seen)

@@ -208,3 +208,33 @@ def test_many_short_sequences(kernel):
     o_ref, lse_ref = _ref(x, causal=True)
     check_o(o, o_ref, x["q"].dtype, o.dtype)
     check_lse(lse, lse_ref)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("dtype,D,N,causal,splits", [
+    ("fp16", 64, 256, True, 0), ("fp16", 64, 1024, False, 0), ("fp16", 64, 1024, False, 1),
+    ("bf16", 128, 300, True, 1), ("f32", 64, 2048, False, 0)])
+def test_single_launch_schedule_matches_the_dynamic_one(kernel, dtype, D, N, causal, splits):
+    """One sequence whose items fit in one wave runs without the preparation
+    kernel (CTA i runs item i): one launch, plus the merge when split.  Its
+    results equal those of the dynamic schedule (explicit grid) bit for bit
+    and match the oracle."""
+    _skip_unsupported(kernel, dtype)
+    x = attn_inputs.make(dtype=dtype, H=3, D=D, seed=60 + N, n_q=N)
+    q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    odt = _out_dtype(dtype)
+    one = attn.FwdCall(q, k, v, causal=causal, kernel=kernel, num_splits=splits, out_dtype=odt)
+    dyn = attn.FwdCall(q, k, v, causal=causal, kernel=kernel, num_splits=splits, out_dtype=odt,
+                       num_ctas=sms)
+    n0 = attn.launch_count()
+    one.run()
+    launched = attn.launch_count() - n0
+    dyn.run()
+    torch.cuda.synchronize()
+    assert attn.device_status() == 0
+    assert launched == (1 if one.num_splits() == 1 else 2)
+    assert torch.equal(one.o, dyn.o) and torch.equal(one.lse, dyn.lse)
+    o_ref, lse_ref = _ref(x, causal=causal)
+    check_o(one.o, o_ref, x["q"].dtype, one.o.dtype)
+    check_lse(one.lse, lse_ref)
