@@ -130,12 +130,13 @@ __device__ __forceinline__ float row_max(const float *v) {
 // constant, f = x - n in [-1/2, 1/2]; 2^f by a degree-4 polynomial fitted for
 // this library (relative minimax on [-1/2, 1/2] with p(0) = 1; max relative
 // error 2.9e-6 evaluated in f32); the result's exponent field gets n added.
-// x is clamped to >= -126, so the result is >= ~2^-126 (never 0): callers use
-// it only where no -inf mask applies.
+// x is clamped to [-126, 127], so the result is >= ~2^-126 (never 0): callers
+// use it only where no -inf mask applies.  Above 127 it saturates near 2^127
+// (finite) instead of carrying the exponent into the sign bit.
 __device__ __forceinline__ float2 exp2_fma2(float2 x) {
     constexpr float kRound = 12582912.f;  // 1.5 * 2^23
-    x.x = fmaxf(x.x, -126.f);
-    x.y = fmaxf(x.y, -126.f);
+    x.x = fminf(fmaxf(x.x, -126.f), 127.f);
+    x.y = fminf(fmaxf(x.y, -126.f), 127.f);
     const float2 t = __fadd2_rn(x, make_float2(kRound, kRound));
     const float2 n = __fadd2_rn(t, make_float2(-kRound, -kRound));
     const float2 f = __ffma2_rn(n, make_float2(-1.f, -1.f), x);
