@@ -12,6 +12,12 @@ sequence and bwd = 2.5 x fwd, summed over the batch; `value` is the whole-job
 rate over all ranks (each rank runs the full batch: weak scaling, no
 collective on the data path).
 
+The default run also times the forward alone on the four smaller
+configurations (causal N=256 fp16, full N=1024 fp16, varlen causal bf16, cross
+f32 8192 x 2048) and adds them to the same line as a `workloads` record
+(device time per call, TFLOP/s, algorithmic bytes and GB/s, roofline, clocks,
+the oracle's rate); `--no-workloads` skips it.
+
 Prints one JSON line.  `--impl reference` times the f64 CPU oracle instead,
 on a bounded sample of the same workload.  `--workload <name>` measures the
 forward alone on one of the smaller workloads (causal_fp16_n256,
@@ -222,6 +228,57 @@ CSR_WORKLOADS = ("csr_gat_n512", "csr_radius_field_bf16", "csr_radius_dot_bf16")
 L2_BYTES = 129 * 1024 * 1024
 
 
+# the four smaller configurations, timed forward-only inside the default run
+SUB_WORKLOADS = ("causal_fp16_n256", "full_fp16_n1024", "varlen_causal_bf16", "cross_f32_8192x2048")
+
+
+def fwd_algorithmic_bytes(lengths_q, lengths_k, H, D, qk_es, v_es, o_es):
+    """Bytes a forward must move at least: q, k and v read once, o and lse
+    (f32) written once."""
+    tq, tk = sum(lengths_q), sum(lengths_k)
+    return (tq * qk_es + tk * qk_es + tk * v_es) * H * D + tq * H * D * o_es + 4 * tq * H
+
+
+def copy_bandwidth(dev, nbytes=256 << 20, reps=4):
+    """Pinned host <-> device copy bandwidth on this machine, GB/s: host to
+    device alone, device to host alone, and both directions at once (two
+    streams; the total of both)."""
+    import torch
+    h_in = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h_out = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d_out = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    main = torch.cuda.current_stream(dev)
+    sa, sb = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def run(h2d, d2h):
+        ev = torch.cuda.Event()
+        ev.record(main)
+        for st, on, fn in ((sa, h2d, lambda: d_in.copy_(h_in, non_blocking=True)),
+                           (sb, d2h, lambda: h_out.copy_(d_out, non_blocking=True))):
+            if on:
+                st.wait_event(ev)
+                with torch.cuda.stream(st):
+                    fn()
+                done = torch.cuda.Event()
+                done.record(st)
+                main.wait_event(done)
+
+    out = {}
+    for name, h2d, d2h in (("h2d_gbs", True, False), ("d2h_gbs", False, True), ("both_gbs", True, True)):
+        run(h2d, d2h)
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(main)
+        for _ in range(reps):
+            run(h2d, d2h)
+        t1.record(main)
+        torch.cuda.synchronize()
+        moved = nbytes * reps * (int(h2d) + int(d2h))
+        out[name] = moved / (t0.elapsed_time(t1) * 1e-3) / 1e9
+    return out
+
+
 def time_oracle_fwd_rows(x, w, max_seconds=15.0):
     """Time the oracle's forward on randomly drawn query rows of the workload,
     adding rows until about `max_seconds` of CPU work; report the workload's
@@ -253,6 +310,123 @@ def time_oracle_fwd_rows(x, w, max_seconds=15.0):
                       f"{spent:.1f} s"}
 
 
+def time_forward_launches(call, stream, flush, steps, warmup, local, sync_ranks=None):
+    """Device time (ms, CUDA events on `stream`) of each of `steps` forward
+    launches after `warmup` untimed ones, the L2 flushed before each launch when
+    `flush` (a device buffer larger than L2) is given; nvidia-smi clocks are
+    sampled during the timed launches.  Returns (per-launch ms, kernels
+    launched, clock summary)."""
+    import torch
+
+    import online_softmax_attention_gb300 as attn
+    for _ in range(warmup):
+        call.run(stream)
+    torch.cuda.synchronize()
+    status = attn.device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} ({attn.strerror(status)}) set during warm-up")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    n0 = attn.launch_count()
+    if sync_ranks:
+        sync_ranks()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        clk.start()
+        for e0, e1 in evs:
+            if flush is not None:
+                flush.zero_()
+            e0.record(stream)
+            call.run(stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        clk.stop()
+    if sync_ranks:
+        sync_ranks()
+    launches = attn.launch_count() - n0
+    status = attn.device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} ({attn.strerror(status)}) set in the timed region")
+    return [a.elapsed_time(b) for a, b in evs], launches, clk.summary()
+
+
+def fwd_peak(family, w, peaks, dev):
+    """(peak, bound, note) of a forward's roofline: the bf16 / f16 dense
+    tensor peak (burst: a forward launch is timed alone), 4/3 of it with fp8
+    scores, or the FP32 FFMA peak for the CUDA-core kernel."""
+    import torch
+    if family == "tc" and w.qk_fp8:
+        # half the FLOPs (S = Q K^T) at the fp8 rate, 2x the 16-bit rate (nominal
+        # ratio), half (P V) at the 16-bit rate: peak = 2 / (1/(2 P) + 1/P) = 4 P / 3
+        return (peaks["bf16_tflops"] * 4.0 / 3.0, "tensor",
+                f"mixed: fp8 score contraction at 2x and bf16 value contraction at 1x the "
+                f"bf16 dense burst peak ({peaks['source']}), i.e. 4/3 of it")
+    if family == "tc":
+        return peaks["bf16_tflops"], "tensor", f"bf16/f16 dense, burst ({peaks['source']})"
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    return (sms * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12, "alu",
+            f"FP32 FFMA: {sms} SMs x 128 lanes x 2 FLOP x {peaks['sm_max_mhz']:.0f} MHz")
+
+
+def fwd_kernel_sources(family):
+    csrc = "online_softmax_attention_gb300/csrc/"
+    shared = [csrc + "common.cuh", csrc + "internal.h"]
+    if family == "tc":
+        return [csrc + "fwd_tc.cu"] + shared + [csrc + "sm100.cuh"]
+    return [csrc + "fwd_simt.cu"] + shared
+
+
+def forward_record(name, dev, local, steps, warmup, oracle_seconds):
+    """Forward-only measurement of one of the smaller configurations, for the
+    `workloads` record of the default run: device time per forward call (L2
+    flushed before each call when the inputs fit in L2), FLOP rate, algorithmic
+    bytes and their rate, the roofline of the attention kernel, clocks, and the
+    oracle's rate on a bounded sample of the same rows."""
+    import torch
+
+    import attn_inputs
+    import online_softmax_attention_gb300 as attn
+    w = attn_inputs.WORKLOADS[name]
+    x = attn_inputs.make_workload(w)
+    flops = attention_flops(x["lengths_q"], x["lengths_k"], w.H, w.D, w.causal)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    cq = x["cu_seqlens_q"].to(dev) if x["cu_seqlens_q"] is not None else None
+    ck = x["cu_seqlens_k"].to(dev) if x["cu_seqlens_k"] is not None else None
+    call = attn.FwdCall(q, k, v, causal=w.causal, cu_seqlens_q=cq, cu_seqlens_k=ck,
+                        out_dtype=torch.float32 if w.dtype == "bf16" else None)
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v))
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if in_bytes < L2_BYTES else None
+    stream = torch.cuda.current_stream()
+    per_launch, launches, clocks = time_forward_launches(call, stream, flush, steps, warmup, local)
+    ms = statistics.median(per_launch)
+    nbytes = fwd_algorithmic_bytes(x["lengths_q"], x["lengths_k"], w.H, w.D, q.element_size(),
+                                   v.element_size(), call.o.element_size())
+    family = call.selected_kernel()
+    peaks = load_peaks()
+    peak, bound, note = fwd_peak(family, w, peaks, dev)
+    tflops = flops / (ms * 1e-3) / 1e12
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    traffic = recorded_traffic("fwd:" + name, source_hash(fwd_kernel_sources(family)))
+    rec = {
+        "config": w.note, "kernel": family, "num_splits": call.num_splits(),
+        "dtype": dtype_label(w), "o_dtype": str(call.o.dtype).replace("torch.", ""),
+        "ms": ms, "ms_spread": spread(per_launch), "steps": steps, "warmup": warmup,
+        "flops": flops, "tflops": tflops, "bytes": nbytes, "gbs": gbs,
+        "gpu_launches_per_call": launches / steps,
+        "l2": "flushed before every call (inputs fit in L2)" if flush is not None
+              else "no flush: inputs larger than L2",
+        "roofline": {"bound": bound, "achieved": tflops, "peak": peak, "unit": UNIT,
+                     "frac": tflops / peak, "peak_source": note,
+                     "hbm_frac": gbs / peaks["hbm_gbs"], "traffic": traffic},
+        "clocks": clocks,
+    }
+    if oracle_seconds:
+        rec["cpu_baseline"] = time_oracle_fwd_rows(x, w, max_seconds=oracle_seconds)
+    del call, q, k, v, flush
+    torch.cuda.empty_cache()
+    return rec
+
+
 def run_forward_workload(args, rank, world):
     """Forward-only measurement of one of the smaller workloads (a parity
     workload, timed on request): TFLOP/s of the forward, L2 flushed between
@@ -281,40 +455,16 @@ def run_forward_workload(args, rank, world):
     in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v))
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if in_bytes < L2_BYTES else None
     stream = torch.cuda.current_stream()
-    for _ in range(args.warmup):
-        call.run(stream)
-    torch.cuda.synchronize()
-    status = attn.device_status()
-    if status != 0:
-        raise RuntimeError(f"device status {status} ({attn.strerror(status)}) set during warm-up")
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    n0 = attn.launch_count()
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        clk.start()
-        for e0, e1 in evs:
-            if flush is not None:
-                flush.zero_()
-            e0.record(stream)
-            call.run(stream)
-            e1.record(stream)
-        torch.cuda.synchronize()
-        clk.stop()
-    if world > 1:
-        dist.barrier()
-    launches = attn.launch_count() - n0
+    sync = dist.barrier if world > 1 else None
+    per_launch, launches, clocks = time_forward_launches(call, stream, flush, args.steps, args.warmup,
+                                                         local, sync)
     pruned_per_run = call.pruned_count() / (args.warmup + args.steps)
-    per_launch = [a.elapsed_time(b) for a, b in evs]
     ms = max_over_ranks(statistics.mean(per_launch), dev)
-    status = attn.device_status()
-    if status != 0:
-        raise RuntimeError(f"device status {status} ({attn.strerror(status)}) set in the timed region")
     unflushed = None
     if flush is not None:
         # the same launches back to back with the inputs left in L2, for reference
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
         for e0, e1 in evs:
             e0.record(stream)
             call.run(stream)
@@ -351,19 +501,9 @@ def run_forward_workload(args, rank, world):
     peaks = load_peaks()
     family = call.selected_kernel()
     achieved = flops / (ms * 1e-3) / 1e12
-    if family == "tc" and w.qk_fp8:
-        # half the FLOPs (S = Q K^T) at the fp8 rate, 2x the 16-bit rate (nominal
-        # ratio), half (P V) at the 16-bit rate: peak = 2 / (1/(2 P) + 1/P) = 4 P / 3
-        peak, bound = peaks["bf16_tflops"] * 4.0 / 3.0, "tensor"
-        note = (f"mixed: fp8 score contraction at 2x and bf16 value contraction at 1x the "
-                f"bf16 dense burst peak ({peaks['source']}), i.e. 4/3 of it")
-    elif family == "tc":
-        peak, bound = peaks["bf16_tflops"], "tensor"
-        note = f"bf16/f16 dense, burst ({peaks['source']})"
-    else:
-        sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        peak, bound = sms * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12, "alu"
-        note = f"FP32 FFMA: {sms} SMs x 128 lanes x 2 FLOP x {peaks['sm_max_mhz']:.0f} MHz"
+    peak, bound, note = fwd_peak(family, w, peaks, dev)
+    nbytes = fwd_algorithmic_bytes(x["lengths_q"], x["lengths_k"], w.H, w.D, q.element_size(),
+                                   v.element_size(), call.o.element_size())
     metric = f"attention fwd TFLOP/s ({w.note})"
     prune = {}
     if args.prune_threshold:
@@ -376,6 +516,8 @@ def run_forward_workload(args, rank, world):
                  "pruned_fraction": pruned_per_run / tiles,
                  "flops": "of the exact forward (exact-equivalent rate)"}
         metric = f"attention fwd TFLOP/s, tile-pruned rho={args.prune_threshold} ({w.note})"
+    traffic = None if (args.prune_threshold or args.num_splits or args.kernel != "auto") else \
+        recorded_traffic("fwd:" + w.name, source_hash(fwd_kernel_sources(family)))
     line = {
         "metric": metric, "value": job_rate(flops, world, ms) / 1e12, "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -390,11 +532,13 @@ def run_forward_workload(args, rank, world):
                    else "no flush: inputs larger than L2",
                    "parallelism": f"replicas x{world}", **prune},
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": UNIT,
-                     "frac": achieved / peak, "traffic": None, "kernel": "fwd", "peak_source": note},
+                     "frac": achieved / peak, "traffic": traffic, "kernel": "fwd", "peak_source": note,
+                     "bytes_per_launch": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9,
+                     "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]},
         "e2e": {"value": job_rate(flops, world, e2e_ms) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches,
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "cpu_baseline": None,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -608,6 +752,8 @@ def main():
     ap.add_argument("--batch", type=int, default=4,
                     help="sequences of N=8192 (4 = the benchmark workload; fewer for profiling)")
     ap.add_argument("--skip-e2e", action="store_true", help="profiling runs: no host-buffer leg")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="training workload: skip the forward-only records of the smaller configurations")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=(WORKLOAD,) + FWD_WORKLOADS + CSR_WORKLOADS,
                     help="the training workload (default), a forward-only workload, or a CSR one")
@@ -826,9 +972,18 @@ def main():
                     ("bwd_dq", "tc"): [csrc + "bwd_tc.cu"] + tc_shared}
     using_tc = family[dominant] == "tc"
     achieved = stage_flops[dominant] / (stage_ms[dominant] * 1e-3) / 1e12
+    region_s = ms * args.steps * 1e-3
+    extra = {}
     if using_tc:
-        peak, bound, punit = peaks["bf16_tflops_sustained"], "tensor", "TFLOP/s"
-        peak_note = f"bf16 dense, sustained ({peaks['source']})"
+        # the burst peak for a timed region shorter than the seconds-long loop
+        # that measured the sustained one; both fractions are printed
+        sustained = region_s >= 4.0
+        peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+        bound, punit = "tensor", "TFLOP/s"
+        peak_note = (f"bf16 dense, {'sustained' if sustained else 'burst'} ({peaks['source']}); "
+                     f"timed region {region_s:.2f} s")
+        extra = {"frac_of_burst": achieved / peaks["bf16_tflops"],
+                 "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"]}
     else:
         # FP32 FFMA: 152 SMs x 128 lanes x 2 FLOP x max SM clock
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -840,7 +995,10 @@ def main():
     traffic = recorded_traffic(tkey, source_hash(src)) if src else None
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": punit,
                 "frac": achieved / peak, "traffic": traffic, "kernel": dominant,
-                "peak_source": peak_note}
+                "peak_source": peak_note, "flops_per_launch": stage_flops[dominant],
+                "ms_per_launch": stage_ms[dominant],
+                "algorithmic": "dK/dV: S recompute, dP, dV, dK = 2 x forward FLOPs" if dominant == "bwd_dkdv"
+                else "see breakdown", **extra}
 
     fwd_tflops = fwd_flops / (stage_ms["fwd"] * 1e-3) / 1e12
     bwd_ms = stage_ms["bwd_preprocess"] + stage_ms["bwd_dkdv"] + stage_ms["bwd_dq"]
@@ -872,10 +1030,23 @@ def main():
     }
     if args.skip_e2e:
         line["e2e"] = None
+    else:
+        # what the host link allows: the step's bytes at the copy bandwidth
+        # measured now (both directions at once), against the device step
+        bw = copy_bandwidth(dev)
+        line["e2e"]["copy_gbs"] = bw
+        line["e2e"]["copy_floor_ms"] = (h2d + d2h) / (bw["both_gbs"] * 1e9) * 1e3
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = time_oracle_sample(x, w)
     else:
         line["cpu_baseline"] = None
+    if not args.no_workloads:
+        # free the training workload's buffers first
+        del fcall, bcall, seqs, q, k, v, dO, outs_host, pin, dev_in
+        torch.cuda.empty_cache()
+        oracle_s = 6.0 if (rank == 0 and world == 1 and not args.no_cpu_baseline) else 0.0
+        line["workloads"] = {name: forward_record(name, dev, local, 20, 5, oracle_s)
+                             for name in SUB_WORKLOADS}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -26,3 +26,11 @@ def test_flop_convention():
 
 def test_step_time_spread():
     assert bench.spread([3.0, 1.0, 2.0, 10.0]) == {"median": 2.5, "min": 1.0, "max": 10.0}
+
+
+def test_forward_algorithmic_bytes():
+    # causal N=256, H=2, D=64, fp16 q, k, v and o: three inputs read, o and f32 lse written
+    assert bench.fwd_algorithmic_bytes([256], [256], 2, 64, 2, 2, 2) == 3 * 256 * 2 * 64 * 2 + 256 * 2 * 64 * 2 + 4 * 256 * 2
+    # cross f32 8192 x 2048, D=64, H=1
+    assert bench.fwd_algorithmic_bytes([8192], [2048], 1, 64, 4, 4, 4) == (8192 + 2 * 2048 + 8192) * 64 * 4 + 4 * 8192
+    assert set(bench.SUB_WORKLOADS) <= set(bench.FWD_WORKLOADS)
