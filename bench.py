@@ -361,6 +361,12 @@ def fwd_peak(family, w, peaks, dev):
         return (peaks["bf16_tflops"] * 4.0 / 3.0, "tensor",
                 f"mixed: fp8 score contraction at 2x and bf16 value contraction at 1x the "
                 f"bf16 dense burst peak ({peaks['source']}), i.e. 4/3 of it")
+    if family == "tc" and w.dtype == "f32":
+        # f32 inputs on the tensor cores: each contraction is six bf16 products
+        # of the operands' bf16 parts, so the tensor pipe does 6x the algorithmic work
+        return (peaks["bf16_tflops"] / 6.0, "tensor",
+                f"f32 by bf16 operand splitting: six bf16 products per contraction, 1/6 of the "
+                f"bf16 dense burst peak ({peaks['source']})")
     if family == "tc":
         return peaks["bf16_tflops"], "tensor", f"bf16/f16 dense, burst ({peaks['source']})"
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -368,11 +374,11 @@ def fwd_peak(family, w, peaks, dev):
             f"FP32 FFMA: {sms} SMs x 128 lanes x 2 FLOP x {peaks['sm_max_mhz']:.0f} MHz")
 
 
-def fwd_kernel_sources(family):
+def fwd_kernel_sources(family, dtype="bf16"):
     csrc = "online_softmax_attention_gb300/csrc/"
     shared = [csrc + "common.cuh", csrc + "internal.h"]
     if family == "tc":
-        return [csrc + "fwd_tc.cu"] + shared + [csrc + "sm100.cuh"]
+        return [csrc + ("fwd_x3.cu" if dtype == "f32" else "fwd_tc.cu")] + shared + [csrc + "sm100.cuh"]
     return [csrc + "fwd_simt.cu"] + shared
 
 
@@ -406,7 +412,9 @@ def forward_record(name, dev, local, steps, warmup, oracle_seconds):
     peak, bound, note = fwd_peak(family, w, peaks, dev)
     tflops = flops / (ms * 1e-3) / 1e12
     gbs = nbytes / (ms * 1e-3) / 1e9
-    traffic = recorded_traffic("fwd:" + name, source_hash(fwd_kernel_sources(family)))
+    traffic = recorded_traffic("fwd:" + name, source_hash(fwd_kernel_sources(family, w.dtype)))
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    ffma_peak = sms * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
     rec = {
         "config": w.note, "kernel": family, "num_splits": call.num_splits(),
         "dtype": dtype_label(w), "o_dtype": str(call.o.dtype).replace("torch.", ""),
@@ -417,7 +425,8 @@ def forward_record(name, dev, local, steps, warmup, oracle_seconds):
               else "no flush: inputs larger than L2",
         "roofline": {"bound": bound, "achieved": tflops, "peak": peak, "unit": UNIT,
                      "frac": tflops / peak, "peak_source": note,
-                     "hbm_frac": gbs / peaks["hbm_gbs"], "traffic": traffic},
+                     "hbm_frac": gbs / peaks["hbm_gbs"], "frac_of_fp32_ffma": tflops / ffma_peak,
+                     "traffic": traffic},
         "clocks": clocks,
     }
     if oracle_seconds:
@@ -517,7 +526,7 @@ def run_forward_workload(args, rank, world):
                  "flops": "of the exact forward (exact-equivalent rate)"}
         metric = f"attention fwd TFLOP/s, tile-pruned rho={args.prune_threshold} ({w.note})"
     traffic = None if (args.prune_threshold or args.num_splits or args.kernel != "auto") else \
-        recorded_traffic("fwd:" + w.name, source_hash(fwd_kernel_sources(family)))
+        recorded_traffic("fwd:" + w.name, source_hash(fwd_kernel_sources(family, w.dtype)))
     line = {
         "metric": metric, "value": job_rate(flops, world, ms) / 1e12, "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,

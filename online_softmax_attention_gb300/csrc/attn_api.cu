@@ -158,20 +158,33 @@ int auto_splits(const FwdParams &p, bool use_tc) {
 }
 
 struct FwdLayout {
-    size_t o_parts, lse_parts, total;
+    size_t o_parts, lse_parts, split_ops, total;
 };
 
-FwdLayout fwd_layout(int n_seq, int n_q, int H, int D, int splits) {
+// Workspace of a forward: the schedule block; with key splits the f32 partial
+// outputs and lse; for f32 inputs on the tensor cores the bf16 parts of q, k, v.
+FwdLayout fwd_layout(int n_seq, int n_q, int H, int D, int splits, size_t op_bytes) {
     FwdLayout L;
     L.o_parts = sched_bytes(n_seq);
     L.lse_parts = L.o_parts;
-    L.total = L.o_parts;
+    L.split_ops = L.o_parts;
     if (splits > 1) {
         const size_t rows = (size_t)splits * (size_t)n_q * (size_t)H;
         L.lse_parts = L.o_parts + align256(sizeof(float) * rows * (size_t)D);
-        L.total = L.lse_parts + align256(sizeof(float) * rows);
+        L.split_ops = L.lse_parts + align256(sizeof(float) * rows);
     }
+    L.total = L.split_ops + align256(op_bytes);
     return L;
+}
+
+// Bytes of the bf16 operand parts a forward with these parameters keeps in the
+// workspace (f32 inputs on the tensor cores only).
+size_t split_op_bytes(const FwdParams &p, bool use_tc) {
+    return use_tc && p.dtype == ATTN_F32 ? x3_split_bytes(p.n_q, p.n_k, p.H) : 0;
+}
+
+FwdLayout fwd_layout_of(const FwdParams &p, bool use_tc) {
+    return fwd_layout(p.n_seq, p.n_q, p.H, p.D, p.n_splits, split_op_bytes(p, use_tc));
 }
 
 // Validates everything but the workspace and fills the kernel parameters that
@@ -217,12 +230,12 @@ int plan_fwd(const attn_fwd_args *a, FwdParams &p, bool &use_tc, bool check_view
     p.n_seq = a->n_seq;
     p.cu_q = a->cu_seqlens_q; p.cu_k = a->cu_seqlens_k;
     p.watchdog_cycles = watchdog_cycles();
-    rc = choose_tc(a->kernel, tc_fwd_supported(p), use_tc);
-    if (rc) return rc;
-    if (p.qk_fp8 && !use_tc) return ATTN_EUNSUPPORTED;  // no CUDA-core fp8 path
     p.prune = rho > 0.f;
     p.prune_log2 = p.prune ? std::log2(rho) : 0.f;
     p.pruned_tiles = reinterpret_cast<unsigned long long *>(a->pruned_tiles);
+    rc = choose_tc(a->kernel, tc_fwd_supported(p), use_tc);
+    if (rc) return rc;
+    if (p.qk_fp8 && !use_tc) return ATTN_EUNSUPPORTED;  // no CUDA-core fp8 path
     p.n_splits = p.prune ? 1 : (a->num_splits > 0 ? a->num_splits : auto_splits(p, use_tc));
     // work items (tiles x heads x splits) are numbered in int32
     const int64_t tiles = (int64_t)a->H * ((int64_t)a->n_q / kSimtBlock + a->n_seq + 1);
@@ -233,11 +246,12 @@ int plan_fwd(const attn_fwd_args *a, FwdParams &p, bool &use_tc, bool check_view
 int build_fwd(const attn_fwd_args *a, FwdParams &p, bool &use_tc) {
     int rc = plan_fwd(a, p, use_tc);
     if (rc) return rc;
-    const FwdLayout L = fwd_layout(a->n_seq, a->n_q, a->H, a->D, p.n_splits);
+    const FwdLayout L = fwd_layout_of(p, use_tc);
     if (!a->workspace || a->workspace_bytes < L.total ||
         (reinterpret_cast<uintptr_t>(a->workspace) & 255))
         return ATTN_EWORKSPACE;
     p.sched = sched_at(a->workspace);
+    p.split_ws = split_op_bytes(p, use_tc) ? static_cast<char *>(a->workspace) + L.split_ops : nullptr;
     p.status = status_ptr();
     if (!p.status) return ATTN_ECUDA;
     return ATTN_OK;
@@ -246,8 +260,8 @@ int build_fwd(const attn_fwd_args *a, FwdParams &p, bool &use_tc) {
 // Kernel parameters of the split-K partial pass and of its merge: the
 // attention kernel writes chunk c's O_c (f32, token stride H*D, head stride D)
 // and lse_c into the workspace; the merge writes the caller's o and lse.
-void split_params(const attn_fwd_args *a, const FwdParams &p, FwdParams &part, MergeParams &m) {
-    const FwdLayout L = fwd_layout(a->n_seq, a->n_q, a->H, a->D, p.n_splits);
+void split_params(const attn_fwd_args *a, const FwdParams &p, bool use_tc, FwdParams &part, MergeParams &m) {
+    const FwdLayout L = fwd_layout_of(p, use_tc);
     char *ws = static_cast<char *>(a->workspace);
     float *o_parts = reinterpret_cast<float *>(ws + L.o_parts);
     float *lse_parts = reinterpret_cast<float *>(ws + L.lse_parts);
@@ -394,9 +408,9 @@ size_t attn_fwd_workspace_bytes(const attn_fwd_args *a) {
     FwdParams p;
     bool use_tc = false;
     // arguments the forward would reject need no split buffers
-    const int splits = plan_fwd(a, p, use_tc, false) == ATTN_OK ? p.n_splits : 1;
-    return fwd_layout(a->n_seq, a->n_q > 0 ? a->n_q : 0, a->H > 0 ? a->H : 0,
-                      a->D > 0 ? a->D : 0, splits).total;
+    if (plan_fwd(a, p, use_tc, false) == ATTN_OK) return fwd_layout_of(p, use_tc).total;
+    return fwd_layout(a->n_seq, a->n_q > 0 ? a->n_q : 0, a->H > 0 ? a->H : 0, a->D > 0 ? a->D : 0, 1, 0)
+        .total;
 }
 
 size_t attn_merge_args_size(void) { return sizeof(attn_merge_args); }
@@ -438,7 +452,7 @@ int attn_fwd(const attn_fwd_args *a, void *stream) {
     } else {
         FwdParams part;
         MergeParams m;
-        split_params(a, p, part, m);
+        split_params(a, p, use_tc, part, m);
         e = use_tc ? launch_fwd_tc(part, grid, s) : launch_fwd_simt(part, grid, s);
         if (e == cudaSuccess) e = launch_merge(m, s);
     }

@@ -641,6 +641,7 @@ cudaError_t launch_d(const TcFwdArgs &args, int num_ctas, cudaStream_t s) {
 }  // namespace
 
 bool tc_fwd_supported(const FwdParams &p) {
+    if (p.dtype == ATTN_F32) return x3_fwd_supported(p);
     if (p.dtype != ATTN_F16 && p.dtype != ATTN_BF16) return false;
     if (p.D != 64 && p.D != 128) return false;
     if (p.qk_fp8 && (p.D != 128 || !(p.scale_log2 > 0.f))) return false;
@@ -651,6 +652,7 @@ bool tc_fwd_supported(const FwdParams &p) {
 int tc_fwd_block_rows(const FwdParams &) { return kItemRows; }
 
 cudaError_t launch_fwd_tc(const FwdParams &p, int num_ctas, cudaStream_t s) {
+    if (p.dtype == ATTN_F32) return launch_fwd_x3(p, num_ctas, s);
     TcFwdArgs args;
     args.p = p;
     const int qk_dtype = p.qk_fp8 ? kDtypeE4M3 : p.dtype;

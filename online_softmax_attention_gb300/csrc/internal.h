@@ -47,6 +47,9 @@ struct FwdParams {
     int prune;
     float prune_log2;  // log2(rho)
     unsigned long long *pruned_tiles;
+    // f32 inputs on the tensor cores: workspace region for the bf16 parts of
+    // q, k and v (see fwd_x3.cu), else null
+    void *split_ws;
 };
 
 // Key-tile range [begin, end) of chunk c when n_tiles key tiles are cut into

@@ -52,6 +52,9 @@ extern "C" int attn_fwd_noalloc(const attn_fwd_args *a, void *stream) {
     b.workspace = nullptr;
     b.workspace_bytes = 0;
     b.num_splits = 1;  // split-K partials would need more scratch than the fixed array
+    // the tensor-core f32 forward keeps bf16 parts of q, k, v in its workspace:
+    // f32 inputs take the CUDA-core kernel here unless the caller insists
+    if (b.dtype == ATTN_F32 && b.kernel == ATTN_KERNEL_AUTO) b.kernel = ATTN_KERNEL_SIMT;
     if (attn_fwd_workspace_bytes(&b) > kScratchBytes) return ATTN_EUNSUPPORTED;
     void *scratch = scratch_address();
     if (!scratch) return ATTN_ECUDA;

@@ -39,14 +39,14 @@ bool tc_device_ok() {
 }
 
 bool make_tile_map(CUtensorMap *m, const void *ptr, int dtype, int D, int tokens, int H, int64_t st,
-                   int64_t sh) {
+                   int64_t sh, int box_rows) {
     auto enc = encode_fn();
     if (!enc) return false;
     const bool f8 = dtype == kDtypeE4M3;
     const cuuint64_t es_bytes = f8 ? 1 : 2;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)tokens, (cuuint64_t)H};
     cuuint64_t strides[2] = {(cuuint64_t)st * es_bytes, (cuuint64_t)sh * es_bytes};
-    cuuint32_t box[3] = {f8 ? 128u : 64u, 128, 1};
+    cuuint32_t box[3] = {f8 ? 128u : 64u, (cuuint32_t)box_rows, 1};
     cuuint32_t es[3] = {1, 1, 1};
     const CUtensorMapDataType dt = f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                    : dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16

@@ -70,7 +70,7 @@ def test_forward_and_backward(kernel, dtype, D, dq_mode):
         assert torch.equal(view.cpu(), x[n]), f"{n} was written to"
 
 
-@pytest.mark.parametrize("kernel,dtype,D", [("tc", "bf16", 128), ("simt", "f32", 64)])
+@pytest.mark.parametrize("kernel,dtype,D", [("tc", "bf16", 128), ("simt", "f32", 64), ("tc", "f32", 64)])
 def test_split_forward_and_merge(kernel, dtype, D):
     """Key splits write f32 partials to the workspace; the merge writes O
     through the far view."""

@@ -15,9 +15,9 @@ KERNELS = ["auto", "simt", "tc"]
 DEV = "cuda"
 
 
-def _skip_unsupported(kernel, dtype):
-    if kernel == "tc" and dtype in ("f32", torch.float32):
-        pytest.skip("the tensor-core kernels take f16 / bf16 only")
+def _skip_unsupported(kernel, dtype, D=64):
+    if kernel == "tc" and dtype in ("f32", torch.float32) and D != 64:
+        pytest.skip("the tensor-core kernels take f32 inputs at D = 64 only")
 
 
 def _run(x, *, causal, kernel, out_dtype=None, scale=None, num_ctas=0):
@@ -47,7 +47,7 @@ def _out_dtype(dtype):
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N", [1, 127, 129, 300])
 def test_single_sequence(kernel, dtype, D, causal, N):
-    _skip_unsupported(kernel, dtype)
+    _skip_unsupported(kernel, dtype, D)
     x = attn_inputs.make(dtype=dtype, H=3, D=D, seed=100 + N, n_q=N)
     o, lse = _run(x, causal=causal, kernel=kernel, out_dtype=_out_dtype(dtype))
     o_ref, lse_ref = _ref(x, causal=causal)
@@ -165,8 +165,10 @@ def test_auto_selects_tensor_cores_for_16_bit():
     x = attn_inputs.make(dtype="bf16", H=2, D=128, seed=20, n_q=256)
     q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
     assert attn.FwdCall(q, k, v, causal=True).selected_kernel() == "tc"
-    q32 = q.float()
+    q32 = q.float()  # f32 at D = 128: the CUDA-core kernel
     assert attn.FwdCall(q32, q32, q32, causal=True).selected_kernel() == "simt"
+    q64 = q32[..., :64].contiguous()  # f32 at D = 64: the tensor cores (split operands)
+    assert attn.FwdCall(q64, q64, q64, causal=True).selected_kernel() == "tc"
 
 
 @pytest.mark.parametrize("dtype,D", [("bf16", 128), ("fp16", 64)])
@@ -216,7 +218,8 @@ def test_many_short_sequences(kernel):
     ("bf16", 128, 300, True, 1), ("f32", 64, 2048, False, 0)])
 def test_single_launch_schedule_matches_the_dynamic_one(kernel, dtype, D, N, causal, splits):
     """One sequence whose items fit in one wave runs without the preparation
-    kernel (CTA i runs item i): one launch, plus the merge when split.  Its
+    kernel (CTA i runs item i): one attention launch, plus the merge when split
+    (and the operand-splitting prepass for f32 on the tensor cores).  Its
     results equal those of the dynamic schedule (explicit grid) bit for bit
     and match the oracle."""
     _skip_unsupported(kernel, dtype)
@@ -233,7 +236,9 @@ def test_single_launch_schedule_matches_the_dynamic_one(kernel, dtype, D, N, cau
     dyn.run()
     torch.cuda.synchronize()
     assert attn.device_status() == 0
-    assert launched == (1 if one.num_splits() == 1 else 2)
+    # f32 on the tensor cores adds the operand-splitting prepass
+    prepass = 1 if (dtype == "f32" and one.selected_kernel() == "tc") else 0
+    assert launched == (1 if one.num_splits() == 1 else 2) + prepass
     assert torch.equal(one.o, dyn.o) and torch.equal(one.lse, dyn.lse)
     o_ref, lse_ref = _ref(x, causal=causal)
     check_o(one.o, o_ref, x["q"].dtype, one.o.dtype)

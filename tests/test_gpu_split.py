@@ -37,13 +37,15 @@ def _out(dtype):
 
 
 @pytest.mark.parametrize("kernel,dtype", [("simt", "f32"), ("simt", "fp16"), ("tc", "fp16"),
-                                          ("tc", "bf16")])
+                                          ("tc", "bf16"), ("tc", "f32")])
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("splits", [2, 3, 8])
 def test_split_forward_single_sequence(kernel, dtype, D, causal, splits):
     """N = 700: 11 SIMT / 6 tensor-core key tiles, split unevenly, ragged tail;
     at 8 splits some chunks of the short causal rows are empty."""
+    if kernel == "tc" and dtype == "f32" and D != 64:
+        pytest.skip("the tensor-core kernels take f32 inputs at D = 64 only")
     x = attn_inputs.make(dtype=dtype, H=2, D=D, seed=300 + splits, n_q=700)
     o, lse = _run(x, causal=causal, kernel=kernel, splits=splits, out_dtype=_out(dtype))
     o_ref, lse_ref = _ref(x, causal=causal)
@@ -51,7 +53,7 @@ def test_split_forward_single_sequence(kernel, dtype, D, causal, splits):
     check_lse(lse, lse_ref)
 
 
-@pytest.mark.parametrize("kernel,dtype", [("simt", "f32"), ("tc", "bf16")])
+@pytest.mark.parametrize("kernel,dtype", [("simt", "f32"), ("tc", "bf16"), ("tc", "f32")])
 def test_split_forward_varlen_cross_with_empty_sequences(kernel, dtype):
     x = attn_inputs.make(dtype=dtype, H=3, D=64 if dtype == "f32" else 128, seed=310,
                          lengths=[130, 0, 1, 257, 64], lengths_k=[900, 40, 0, 1, 300])
