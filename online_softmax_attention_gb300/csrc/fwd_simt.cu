@@ -36,6 +36,13 @@ constexpr int LDP = BK + 4;
 template <typename Tin, int D>
 constexpr bool kAsyncKV = sizeof(Tin) == 4 && D == 64;
 
+// The score contraction uses packed FP32 FMAs (fma.rn.f32x2: two FMAs per
+// instruction), pairing adjacent d into separate even / odd partial sums, so
+// each operand pair is two adjacent registers of a 16-byte shared-memory load
+// of a Q or K row.  (Pairing keys in the value contraction the same way needs V
+// key-pair interleaved in shared memory; with the extra repacking pass and
+// barrier that was slower, 158 vs 150 us at the cross f32 8192 x 2048 shape.)
+
 template <typename Tin, int D>
 constexpr size_t fwd_smem_bytes() {
     return sizeof(float) * (size_t)(BQ * (D + 4) + (kAsyncKV<Tin, D> ? 4 : 2) * BK * (D + 4) + BQ * LDP);
@@ -161,28 +168,35 @@ __global__ void __launch_bounds__(NT) fwd_simt_kernel(const FwdParams p) {
             }
             __syncthreads();
 
-            // score micro-tile: rows ty + 16 r, keys tx + 16 c
+            // score micro-tile: rows ty + 16 r, keys tx + 16 c; packed FMAs over
+            // (d, d + 1) pairs into even / odd partial sums
             float s[4][4];
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) s[r][c] = 0.f;
-#pragma unroll 4
-            for (int d = 0; d < D; d += 4) {
-                float4 a[4], b[4];
-#pragma unroll
-                for (int r = 0; r < 4; ++r) a[r] = *reinterpret_cast<const float4 *>(sQ + (ty + 16 * r) * LD + d);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) b[c] = *reinterpret_cast<const float4 *>(sK + (tx + 16 * c) * LD + d);
+            {
+                float2 s2[4][4];
 #pragma unroll
                 for (int r = 0; r < 4; ++r)
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        s[r][c] = fmaf(a[r].x, b[c].x, s[r][c]);
-                        s[r][c] = fmaf(a[r].y, b[c].y, s[r][c]);
-                        s[r][c] = fmaf(a[r].z, b[c].z, s[r][c]);
-                        s[r][c] = fmaf(a[r].w, b[c].w, s[r][c]);
+                    for (int c = 0; c < 4; ++c) s2[r][c] = make_float2(0.f, 0.f);
+                // (unrolled by 2: deeper unrolling spills under the 128-register cap)
+#pragma unroll 2
+                for (int d = 0; d < D; d += 4) {
+                    float4 b[4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) b[c] = *reinterpret_cast<const float4 *>(sK + (tx + 16 * c) * LD + d);
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const float4 a = *reinterpret_cast<const float4 *>(sQ + (ty + 16 * r) * LD + d);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            s2[r][c] = __ffma2_rn(make_float2(a.x, a.y), make_float2(b[c].x, b[c].y), s2[r][c]);
+                            s2[r][c] = __ffma2_rn(make_float2(a.z, a.w), make_float2(b[c].z, b[c].w), s2[r][c]);
+                        }
                     }
+                }
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) s[r][c] = s2[r][c].x + s2[r][c].y;
             }
 
             // scale into the base-2 domain, mask
