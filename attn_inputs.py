@@ -197,6 +197,22 @@ def radius_graph(n: int, cutoff: float, seed: int):
     return pos, row_ptr, src.to(torch.int32)
 
 
+def curve_order(pos: torch.Tensor, cell: float) -> torch.Tensor:
+    """A processing order for the rows of a graph over points: the points
+    sorted along a Z-order (Morton) curve through cells of side `cell`, ties
+    by index.  Rows taken in this order have spatially close neighbours in
+    flight together.  Returns an int32 permutation of range(len(pos))."""
+    cells = max(1, int(1.0 / cell))
+    bits = max(1, (cells - 1).bit_length())
+    c = torch.clamp((pos.double() * cells).long(), 0, cells - 1)
+    code = torch.zeros(len(pos), dtype=torch.int64)
+    for b in range(bits):
+        for axis in range(3):
+            code |= ((c[:, axis] >> b) & 1) << (3 * b + axis)
+    key = code * len(pos) + torch.arange(len(pos), dtype=torch.int64)
+    return torch.argsort(key).to(torch.int32)
+
+
 def csr_of_segments(lengths_q, lengths_k, causal: bool):
     """CSR of the block-diagonal relation of cu_seqlens-packed sequences:
     query i of sequence b has edges to keys of sequence b (j <= i if causal)."""
@@ -270,6 +286,8 @@ def make_csr_workload(w: CsrWorkload | str) -> dict:
     if isinstance(w, str):
         w = CSR_WORKLOADS[w]
     cutoff = 0.15 if w.degree == 0.0 else w.cutoff
-    _, row_ptr, col = radius_graph(w.n, cutoff, w.seed)
-    return make_csr(row_ptr=row_ptr, col=col, n_src=w.n, H=w.H, D=w.D, dtype=w.dtype,
-                    seed=w.seed + 1, field_scores=w.field_scores)
+    pos, row_ptr, col = radius_graph(w.n, cutoff, w.seed)
+    x = make_csr(row_ptr=row_ptr, col=col, n_src=w.n, H=w.H, D=w.D, dtype=w.dtype,
+                 seed=w.seed + 1, field_scores=w.field_scores)
+    x["row_order"] = curve_order(pos, cutoff)
+    return x

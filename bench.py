@@ -616,7 +616,10 @@ def run_csr_workload(args, rank, world):
     n, E = len(x["row_ptr"]) - 1, x["col"].numel()
     kw = {"scores": x["scores"].to(dev)} if w.field_scores else \
         {"q": x["q"].to(dev), "k": x["k"].to(dev)}
-    call = attn.CsrCall(rp, col, v, **kw)
+    # rows taken along a Z-order curve through the points (part of the
+    # relation's description, computed with the graph), or in index order
+    order = x["row_order"].to(dev) if args.row_order == "curve" else None
+    call = attn.CsrCall(rp, col, v, row_order=order, **kw)
     es = v.element_size()
     # bytes of one launch as the algorithm touches them: the relation, the
     # scores, one row of V (and of K) per edge and head, Q, O and lse
@@ -657,6 +660,9 @@ def run_csr_workload(args, rank, world):
     # end to end: the relation, scores / q, k and v in from pinned host memory, o and lse out
     host = {"row_ptr": x["row_ptr"], "col": x["col"], "v": x["v"]}
     devt = {"row_ptr": rp, "col": col, "v": v}
+    if order is not None:
+        host["row_order"] = x["row_order"]
+        devt["row_order"] = order
     for name, t in kw.items():
         host[name] = x[name]
         devt[name] = t
@@ -699,6 +705,7 @@ def run_csr_workload(args, rank, world):
         "config": {"workload": w.name, "nodes": n, "edges": E, "avg_degree": E / max(1, n),
                    "heads": w.H, "head_dim": w.D,
                    "scores": "field" if w.field_scores else "dot-product",
+                   "row_order": "Z-order curve through the points" if order is not None else "index order",
                    "bytes_gathered_per_launch": gathered, "bytes_compulsory_per_launch": compulsory,
                    "l2": "flushed before every launch (inputs fit in L2)" if flush is not None
                    else "no flush: inputs larger than L2",
@@ -706,7 +713,9 @@ def run_csr_workload(args, rank, world):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "kernel": "csr_fwd",
                      "peak_source": f"HBM copy ({peaks['source']})",
-                     "bytes": "gathered: one V (and K) row per edge and head"},
+                     "bytes": "gathered: one V (and K) row per edge and head",
+                     "compulsory_gbs": compulsory / (ms * 1e-3) / 1e9,
+                     "frac_compulsory": compulsory / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]},
         "e2e": {"value": E * w.H * world / (e2e_ms * 1e-3) / 1e9, "unit": "Gedge/s",
                 "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in pin.values()),
                 "d2h_bytes_per_step": o_h.numel() * o_h.element_size() + l_h.numel() * 4,
@@ -771,6 +780,9 @@ def main():
     ap.add_argument("--dq-mode", default="auto", choices=["auto", "fused", "separate"],
                     help="training workload: backward dq accumulated in the dK/dV kernel (fused) "
                          "or by its own deterministic kernel (separate); auto = separate")
+    ap.add_argument("--row-order", default="curve", choices=["curve", "none"],
+                    help="CSR workloads: rows taken along a Z-order curve through the points "
+                         "(default) or in index order")
     ap.add_argument("--prune-threshold", type=float, default=0.0,
                     help="forward-only workloads, full relation: tile pruning rho (0 = exact)")
     args = ap.parse_args()
@@ -877,18 +889,31 @@ def main():
     # computed (forward + backward) on one of two compute streams (alternating,
     # so that the last wave of one sequence's kernels overlaps the next
     # sequence's first) and copied out on a fourth, so one sequence's copies
-    # overlap its neighbours' computation.
+    # overlap its neighbours' computation.  Consecutive steps use two sets of
+    # device buffers (slots), so that a step's copies in and its kernels need
+    # not wait for the previous step's copies out: the host link, the
+    # bottleneck here, then never idles between steps.
     pin = {n: x[n].contiguous().pin_memory() for n in ("q", "k", "v", "dO")}
-    dev_in = {"q": q, "k": k, "v": v, "dO": dO}
     n_seq_b, len_b = w.batch, w.n_q
-    seqs = []
-    for b_ in range(n_seq_b):
-        sl = slice(b_ * len_b, (b_ + 1) * len_b)
-        fb = attn.FwdCall(q[sl], k[sl], v[sl], causal=True, out_dtype=torch.float32, kernel=args.kernel)
-        bb = attn.BwdCall(q[sl], k[sl], v[sl], fb.o, fb.lse, dO[sl], causal=True, kernel=args.kernel,
-                          dq_mode=args.dq_mode)
-        seqs.append((sl, fb, bb))
     T_, H_, D_ = q.shape
+
+    def make_slot(dev_in):
+        seqs_ = []
+        for b_ in range(n_seq_b):
+            sl = slice(b_ * len_b, (b_ + 1) * len_b)
+            fb = attn.FwdCall(dev_in["q"][sl], dev_in["k"][sl], dev_in["v"][sl], causal=True,
+                              out_dtype=torch.float32, kernel=args.kernel)
+            bb = attn.BwdCall(dev_in["q"][sl], dev_in["k"][sl], dev_in["v"][sl], fb.o, fb.lse,
+                              dev_in["dO"][sl], causal=True, kernel=args.kernel, dq_mode=args.dq_mode)
+            seqs_.append((sl, fb, bb))
+        evs_ = {k_: [torch.cuda.Event() for _ in seqs_] for k_ in ("in", "done", "out", "used")}
+        for e_ in evs_["out"] + evs_["used"]:
+            e_.record(stream)
+        return {"dev_in": dev_in, "seqs": seqs_, "ev": evs_}
+
+    slots = [make_slot({"q": q, "k": k, "v": v, "dO": dO})]
+    if not args.skip_e2e:
+        slots.append(make_slot({n: torch.empty_like(t) for n, t in (("q", q), ("k", k), ("v", v), ("dO", dO))}))
     outs_host = {"o": torch.empty((T_, H_, D_), dtype=torch.float32).pin_memory(),
                  "lse": torch.empty((n_seq_b, H_, len_b), dtype=torch.float32).pin_memory(),
                  "dq": torch.empty((T_, H_, D_), dtype=bcall.dq.dtype).pin_memory(),
@@ -898,49 +923,50 @@ def main():
     d2h = sum(t.numel() * t.element_size() for t in outs_host.values())
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     s_comp = [stream, torch.cuda.Stream(device=dev)]
-    ev_in = [torch.cuda.Event() for _ in seqs]      # sequence's inputs are on the device
-    ev_done = [torch.cuda.Event() for _ in seqs]    # its outputs are computed
-    ev_out = [torch.cuda.Event() for _ in seqs]     # its outputs have left the device
-    ev_used = [torch.cuda.Event() for _ in seqs]    # its inputs are no longer read
-    for e_ in ev_out + ev_used:
-        e_.record(stream)
+    e2e_count = [0]
 
     def e2e_step():
         if args.skip_e2e:
             return
-        for i_, (sl, fb, bb) in enumerate(seqs):
-            s_in.wait_event(ev_used[i_])  # the previous step's kernels have read this slot
+        slot = slots[e2e_count[0] % len(slots)]
+        e2e_count[0] += 1
+        seqs_, ev, dev_in = slot["seqs"], slot["ev"], slot["dev_in"]
+        for i_, (sl, fb, bb) in enumerate(seqs_):
+            s_in.wait_event(ev["used"][i_])  # this slot's previous kernels have read it
             with torch.cuda.stream(s_in):
                 for n in ("q", "k", "v", "dO"):
                     dev_in[n][sl].copy_(pin[n][sl], non_blocking=True)
-            ev_in[i_].record(s_in)
-        for i_, (sl, fb, bb) in enumerate(seqs):
+            ev["in"][i_].record(s_in)
+        for i_, (sl, fb, bb) in enumerate(seqs_):
             cs = s_comp[i_ % 2]
-            cs.wait_event(ev_in[i_])
-            cs.wait_event(ev_out[i_])  # the previous step's outputs were copied out
+            cs.wait_event(ev["in"][i_])
+            cs.wait_event(ev["out"][i_])  # this slot's previous outputs were copied out
             fb.run(cs)
             bb.run(cs)
-            ev_done[i_].record(cs)
-            ev_used[i_].record(cs)
-        for i_, (sl, fb, bb) in enumerate(seqs):
-            s_out.wait_event(ev_done[i_])
+            ev["done"][i_].record(cs)
+            ev["used"][i_].record(cs)
+        for i_, (sl, fb, bb) in enumerate(seqs_):
+            s_out.wait_event(ev["done"][i_])
             with torch.cuda.stream(s_out):
                 outs_host["o"][sl].copy_(fb.o, non_blocking=True)
                 outs_host["lse"][i_].copy_(fb.lse, non_blocking=True)
                 outs_host["dq"][sl].copy_(bb.dq, non_blocking=True)
                 outs_host["dk"][sl].copy_(bb.dk, non_blocking=True)
                 outs_host["dv"][sl].copy_(bb.dv, non_blocking=True)
-            ev_out[i_].record(s_out)
+            ev["out"][i_].record(s_out)
 
-    e2e_step()
-    torch.cuda.synchronize()
     if not args.skip_e2e:
-        # the per-sequence calls compute what the batched call did, bit for bit
-        same = all(torch.equal(outs_host[n_], t_.cpu()) for n_, t_ in
-                   (("o", fcall.o), ("dq", bcall.dq), ("dk", bcall.dk), ("dv", bcall.dv)))
+        # the per-sequence calls compute what the batched call did, bit for bit, in both slots
         lse_b = fcall.lse.cpu().view(H_, n_seq_b, len_b).permute(1, 0, 2)
-        if not (same and torch.equal(outs_host["lse"], lse_b)):
-            raise RuntimeError("end-to-end leg: per-sequence results differ from the batched call")
+        for _ in slots:
+            for t_ in outs_host.values():
+                t_.zero_()
+            e2e_step()
+            torch.cuda.synchronize()
+            same = all(torch.equal(outs_host[n_], t_.cpu()) for n_, t_ in
+                       (("o", fcall.o), ("dq", bcall.dq), ("dk", bcall.dk), ("dv", bcall.dv)))
+            if not (same and torch.equal(outs_host["lse"], lse_b)):
+                raise RuntimeError("end-to-end leg: per-sequence results differ from the batched call")
     e_steps = max(2, args.steps)  # the same K steps as the device-timed leg
     barrier()
     torch.cuda.synchronize()
@@ -1033,7 +1059,8 @@ def main():
                 "how": "per sequence: pinned host -> device copies, forward + backward, device -> "
                        "pinned host copies of o, lse, dq, dk, dv; copies on their own streams, "
                        "sequences alternating between two compute streams, so that copies and "
-                       "kernel tails overlap the other sequences' computation"},
+                       "kernel tails overlap the other sequences' computation; consecutive steps "
+                       "alternate between two sets of device buffers"},
         "gpu_launches": launches,
         "clocks": clk.summary(),
     }
@@ -1051,7 +1078,7 @@ def main():
         line["cpu_baseline"] = None
     if not args.no_workloads:
         # free the training workload's buffers first
-        del fcall, bcall, seqs, q, k, v, dO, outs_host, pin, dev_in
+        del fcall, bcall, slots, q, k, v, dO, outs_host, pin
         torch.cuda.empty_cache()
         oracle_s = 6.0 if (rank == 0 and world == 1 and not args.no_cpu_baseline) else 0.0
         line["workloads"] = {name: forward_record(name, dev, local, 20, 5, oracle_s)

@@ -64,7 +64,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 5
+#define ATTN_ABI_VERSION 6
 
 #if defined(__GNUC__)
 #define ATTN_API __attribute__((visibility("default")))
@@ -231,6 +231,15 @@ typedef struct attn_csr_args {
     float scale;              /* dot-product scores only */
     int32_t dtype;            /* attn_dtype of q, k, v */
     int32_t o_dtype;          /* dtype or ATTN_F32 */
+    /* device, n_dst entries: the order in which the kernel takes the rows (a
+     * permutation of [0, n_dst)), or NULL for 0, 1, 2, ...  Results do not
+     * depend on it, bit for bit; it only decides which rows are in flight
+     * together, and so how often their sources' rows are found in the L2:
+     * an order that keeps rows with shared sources close (e.g. points sorted
+     * along a space-filling curve) turns most gathers into L2 hits.  An entry
+     * outside [0, n_dst) is skipped and reported as ATTN_EINVAL; a row the
+     * order omits is not written. */
+    const int32_t *row_order;
 } attn_csr_args;
 
 /* Library ABI version (ATTN_ABI_VERSION) and struct sizes, for bindings to

@@ -291,11 +291,15 @@ class CsrCall:
     the relation (row i's edges are ``col[row_ptr[i]:row_ptr[i+1]]``); ``v``
     is (n_src, H, D).  Scores: ``scores`` (E, H) float32 field scores, or
     ``q`` (n_dst, H, D) and ``k`` (n_src, H, D) for scale * <q_i, k_j>.
+    ``row_order`` (n_dst) int32 on the device: the order in which the kernel
+    takes the rows (results are the same bit for bit; an order that keeps
+    rows with shared sources together makes their gathers L2 hits).
     """
 
     def __init__(self, row_ptr, col, v, *, scores=None, q=None, k=None, n_dst: int | None = None,
                  scale: float | None = None, out_dtype: torch.dtype | None = None,
-                 out: torch.Tensor | None = None, lse: torch.Tensor | None = None):
+                 out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                 row_order: torch.Tensor | None = None):
         dev = v.device
         if row_ptr.dtype != torch.int64 or col.dtype != torch.int32:
             raise TypeError("row_ptr must be int64 and col int32")
@@ -327,6 +331,12 @@ class CsrCall:
         a.lse = self.lse.data_ptr() if self.lse.numel() else None
         a.scale = float(scale) if scale is not None else D ** -0.5
         a.dtype, a.o_dtype = _dtype_code(v.dtype), _dtype_code(self.o.dtype)
+        if row_order is not None:
+            if row_order.dtype != torch.int32 or not row_order.is_cuda or row_order.numel() != n_dst \
+                    or not row_order.is_contiguous():
+                raise ValueError("row_order must be a contiguous int32 CUDA tensor of n_dst entries")
+            a.row_order = row_order.data_ptr() if n_dst else None
+            self.inputs = self.inputs + (row_order,)
         self.args = a
         self._fn = _abi.load().attn_csr_fwd
 
@@ -337,10 +347,10 @@ class CsrCall:
 
 
 def csr_fwd(row_ptr, col, v, *, scores=None, q=None, k=None, scale: float | None = None,
-            out_dtype: torch.dtype | None = None):
+            out_dtype: torch.dtype | None = None, row_order=None):
     """Attention over a CSR relation.  Returns ``(o, lse)``."""
     return CsrCall(row_ptr, col, v, scores=scores, q=q, k=k, scale=scale,
-                   out_dtype=out_dtype).run()
+                   out_dtype=out_dtype, row_order=row_order).run()
 
 
 def fwd(q, k, v, *, causal: bool = False, scale: float | None = None, cu_seqlens_q=None,

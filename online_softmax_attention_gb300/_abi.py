@@ -12,7 +12,7 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_lib", "libattn_gb300.so")
 
-ABI_VERSION = 5
+ABI_VERSION = 6
 
 ATTN_OK, ATTN_EINVAL, ATTN_EUNSUPPORTED, ATTN_ECUDA, ATTN_ETIMEOUT, ATTN_EWORKSPACE = 0, -1, -2, -3, -4, -5
 ATTN_F16, ATTN_BF16, ATTN_F32 = 0, 1, 2
@@ -70,7 +70,7 @@ class CsrArgs(ctypes.Structure):
         ("D", ctypes.c_int32), ("edge_scores", ctypes.c_void_p),
         ("q", AttnTensor), ("k", AttnTensor), ("v", AttnTensor), ("o", AttnTensor),
         ("lse", ctypes.c_void_p), ("scale", ctypes.c_float), ("dtype", ctypes.c_int32),
-        ("o_dtype", ctypes.c_int32),
+        ("o_dtype", ctypes.c_int32), ("row_order", ctypes.c_void_p),
     ]
 
 

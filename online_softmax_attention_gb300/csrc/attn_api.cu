@@ -673,7 +673,8 @@ int attn_csr_fwd(const attn_csr_args *a, void *stream) {
     const bool any_e = a->n_edges > 0;
     if (!a->row_ptr || (any_e && !a->col_idx) || (reinterpret_cast<uintptr_t>(a->row_ptr) & 7) ||
         (reinterpret_cast<uintptr_t>(a->col_idx) & 3) ||
-        (!dot && (reinterpret_cast<uintptr_t>(a->edge_scores) & 3)))
+        (!dot && (reinterpret_cast<uintptr_t>(a->edge_scores) & 3)) ||
+        (reinterpret_cast<uintptr_t>(a->row_order) & 3))
         return ATTN_EINVAL;
     if (!valid_view(a->o, a->o_dtype, true) || !valid_view(a->v, a->dtype, any_e && a->n_src > 0) ||
         (dot && (!valid_view(a->q, a->dtype, true) || !valid_view(a->k, a->dtype, any_e && a->n_src > 0))))
@@ -696,6 +697,7 @@ int attn_csr_fwd(const attn_csr_args *a, void *stream) {
     p.scale_log2 = a->scale * 1.4426950408889634f;
     p.dtype = a->dtype;
     p.o_dtype = a->o_dtype;
+    p.row_order = a->row_order;
     p.status = status_ptr();
     if (!p.status) return ATTN_ECUDA;
     cudaError_t e = launch_csr_fwd(p, static_cast<cudaStream_t>(stream));

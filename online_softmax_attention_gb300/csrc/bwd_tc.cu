@@ -85,8 +85,8 @@ __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 constexpr long long kDrainCycles = 1ll << 31;  // post-abort wait for TMA loads in flight
 
-// The dq kernel's elementwise warps are on its critical path and bound by the
-// SFU (16384 exponentials per 128 x 128 block); computing one pair in four with
+// The dq kernel's elementwise warps are on its critical path (16384
+// exponentials per 128 x 128 block); computing one pair in four with
 // the FMA-pipe polynomial (exp2_fma2) took the dq stage of the causal training
 // workload from 2.70 to 2.48 ms (one in eight: 2.58, three in eight: 2.52, one
 // in two: 2.56).  The dK/dV kernel got slower with it and keeps the SFU only.

@@ -17,6 +17,9 @@
 //    back to back: one warp per destination row gathers whole source rows
 //    (all heads, 512 contiguous bytes at H = 4, D = 64 bf16) in 16-byte lane
 //    chunks with several edges in flight -- the one the benchmarks run;
+// Both take the rows in the caller's row order when one is given (the warps
+// in flight at any moment hold consecutive entries of it, so an order that
+// keeps rows with shared sources together lets the L2 serve their gathers).
 //  * general (csr_fwd_kernel), any strides: one warp per (row, head).  Lane t
 //    owns edge t of the current block of 32 (its column index and score) and
 //    columns 4 t + 128 c of the D-wide rows (float4 chunks, c < 2, so
@@ -43,6 +46,19 @@ __device__ __forceinline__ float4 ldg4(const T *p) {
     return load4(p);
 }
 
+// The destination row taken in position `r` of the processing order (the
+// caller's row_order, else r itself); -1, with the status word set, for an
+// entry outside [0, n_dst).  Every lane of a warp asks for the same r.
+__device__ __forceinline__ int row_at(const CsrParams &p, int r) {
+    if (!p.row_order) return r;
+    const int i = __ldg(p.row_order + r);
+    if (i < 0 || i >= p.n_dst) {
+        if ((threadIdx.x & 31) == 0) report_status(p.status, ATTN_EINVAL);
+        return -1;
+    }
+    return i;
+}
+
 template <typename T, typename Tout, bool kDot>
 __global__ void __launch_bounds__(32 * kWarps) csr_fwd_kernel(const CsrParams p) {
     const int lane = threadIdx.x & 31;
@@ -57,7 +73,9 @@ __global__ void __launch_bounds__(32 * kWarps) csr_fwd_kernel(const CsrParams p)
     for (int c = 0; c < kChunks; ++c) live[c] = 4 * (lane + 32 * c) < p.D;
 
     for (int64_t r = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); r < pairs; r += stride) {
-        const int i = (int)(r / p.H), h = (int)(r - (int64_t)i * p.H);
+        const int ri = (int)(r / p.H), h = (int)(r - (int64_t)ri * p.H);
+        const int i = row_at(p, ri);
+        if (i < 0) continue;  // (warp-uniform) entry outside the rows, reported
         int64_t e0 = __ldg(p.row_ptr + i), e1 = __ldg(p.row_ptr + i + 1);
         if (e0 < 0 || e1 < e0 || e1 > p.n_edges) {
             if (lane == 0) report_status(p.status, ATTN_EINVAL);
@@ -267,7 +285,9 @@ __global__ void __launch_bounds__(32 * kWarps) csr_rows_kernel(const CsrParams p
     Tout *go = static_cast<Tout *>(p.o);
     const int64_t stride = (int64_t)gridDim.x * kWarps;
 
-    for (int64_t i = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); i < p.n_dst; i += stride) {
+    for (int64_t ri = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); ri < p.n_dst; ri += stride) {
+        const int64_t i = row_at(p, (int)ri);
+        if (i < 0) continue;  // (warp-uniform) entry outside the rows, reported
         int64_t e0 = __ldg(p.row_ptr + i), e1 = __ldg(p.row_ptr + i + 1);
         if (e0 < 0 || e1 < e0 || e1 > p.n_edges) {
             if (lane == 0) report_status(p.status, ATTN_EINVAL);

@@ -91,6 +91,7 @@ struct CsrParams {
     int64_t q_st, q_sh, k_st, k_sh, v_st, v_sh, o_st, o_sh;
     float scale_log2;
     int dtype, o_dtype;
+    const int32_t *row_order;  // n_dst rows in processing order, or null: identity
     int *status;
 };
 

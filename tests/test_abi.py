@@ -12,6 +12,16 @@ from online_softmax_attention_gb300 import _abi
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
+@pytest.fixture(autouse=True)
+def _no_launch():
+    """The calls here pass fake device pointers: none may reach a launch (on
+    a machine with a GPU it would read and write those addresses)."""
+    lib = _abi.load()
+    before = lib.attn_launch_count()
+    yield
+    assert lib.attn_launch_count() == before, "a validation test launched a kernel"
+
+
 def _declared():
     with open(os.path.join(ROOT, "include", "attn.h")) as f:
         text = f.read()
@@ -86,8 +96,8 @@ def _fwd_args(**kw):
     ({"prune": 0.5}, _abi.ATTN_EUNSUPPORTED),                  # causal: fails closed
     ({"prune": 0.5, "relation": _abi.ATTN_FULL, "num_splits": 2}, _abi.ATTN_EUNSUPPORTED),
     ({"num_splits": _abi.ATTN_MAX_SPLITS + 1}, _abi.ATTN_EINVAL),
-    ({"kernel": 42}, None),
-    ({"dtype": _abi.ATTN_F32, "kernel": _abi.ATTN_KERNEL_TC}, None),
+    ({"kernel": 42}, _abi.ATTN_EINVAL),
+    ({"dtype": _abi.ATTN_F32, "kernel": _abi.ATTN_KERNEL_TC, "D": 128}, _abi.ATTN_EUNSUPPORTED),
     ({"qk_fp8": 2}, _abi.ATTN_EINVAL),
     ({"qk_fp8": 1}, _abi.ATTN_EUNSUPPORTED),                   # fp8 Q / K: D = 128 only
     ({"qk_fp8": 1, "D": 128, "dtype": _abi.ATTN_F32}, _abi.ATTN_EUNSUPPORTED),  # v 16-bit
@@ -98,13 +108,13 @@ def _fwd_args(**kw):
     ({"qk_fp8": 1, "D": 128, "scale": 0.0}, _abi.ATTN_EUNSUPPORTED),  # fp8 Q / K: positive scales
 ])
 def test_forward_argument_validation(kw, code):
+    # every case is rejected on the host, before any launch: these arguments
+    # hold fake pointers, so a launch on a machine with a GPU would fault
     lib = _abi.load()
     a = _fwd_args(**kw)
-    rc = lib.attn_fwd(ctypes.byref(a), None)
-    if code is None:
-        assert rc in (_abi.ATTN_EINVAL, _abi.ATTN_EUNSUPPORTED, _abi.ATTN_ECUDA)
-    else:
-        assert rc == code
+    before = lib.attn_launch_count()
+    assert lib.attn_fwd(ctypes.byref(a), None) == code
+    assert lib.attn_launch_count() == before
 
 
 def test_forward_rejects_misaligned_strides_and_null_pointers():
@@ -242,10 +252,12 @@ def _csr_args(**kw):
     a.scale = kw.get("scale", 0.125)
     a.dtype = kw.get("dtype", _abi.ATTN_BF16)
     a.o_dtype = kw.get("o_dtype", a.dtype)
+    a.row_order = kw.get("row_order", None)
     return a
 
 
 @pytest.mark.parametrize("kw", [
+    {"row_order": FAKE + 2},
     {"D": 6}, {"D": 260}, {"D": 0}, {"H": 0}, {"n_dst": -1}, {"n_src": -1}, {"n_edges": -5},
     {"dtype": 7}, {"o_dtype": _abi.ATTN_F16}, {"row_ptr": None}, {"row_ptr": FAKE + 4},
     {"col": None}, {"col": FAKE + 2}, {"scores": FAKE + 1}, {"v": None}, {"o": FAKE + 8},

@@ -129,3 +129,48 @@ def test_strided_views_match_packed_rows(dot):
     assert attn.device_status() == 0
     for o, lse in (packed, (o_s, lse_s)):
         _check(o, lse, o_ref, lse_ref, torch.bfloat16, o.dtype)
+
+
+@pytest.mark.parametrize("dot", [False, True])
+@pytest.mark.parametrize("layout", ["packed", "strided"])
+def test_row_order_leaves_results_unchanged(dot, layout):
+    """Rows taken along a Z-order curve through the points, or in a random
+    order: the same outputs, bit for bit, as index order, and the oracle's."""
+    pos, rp, col = attn_inputs.radius_graph(3000, 0.08, seed=608)
+    x = attn_inputs.make_csr(row_ptr=rp, col=col, n_src=3000, H=4, D=64, dtype="bf16", seed=609,
+                             field_scores=not dot, score_std=2.0)
+    if layout == "strided":  # the general kernel
+        for name in ("v", "q", "k"):
+            if x.get(name) is not None:
+                x[name] = x[name].permute(1, 0, 2).contiguous().permute(1, 0, 2)
+    args = dict(q=x["q"].to(DEV), k=x["k"].to(DEV)) if dot else dict(scores=x["scores"].to(DEV))
+    rpd, cold, vd = rp.to(DEV), col.to(DEV), x["v"].to(DEV)
+    base = attn.csr_fwd(rpd, cold, vd, out_dtype=torch.float32, **args)
+    orders = [attn_inputs.curve_order(pos, 0.08),
+              torch.randperm(3000, generator=torch.Generator().manual_seed(610)).to(torch.int32)]
+    for order in orders:
+        o, lse = attn.csr_fwd(rpd, cold, vd, out_dtype=torch.float32, row_order=order.to(DEV), **args)
+        torch.cuda.synchronize()
+        assert attn.device_status() == 0
+        assert torch.equal(o, base[0]) and torch.equal(lse, base[1])
+    o_ref, lse_ref = _ref(x, dot=dot)
+    _check(o, lse, o_ref, lse_ref, torch.bfloat16, o.dtype)
+
+
+def test_row_order_entry_outside_the_rows_is_reported_and_skipped():
+    """Entries -1 and n_dst + 93 are skipped (no out-of-bounds access) with
+    ATTN_EINVAL; the rows the order names are exact, the two it omits untouched."""
+    _, rp, col = attn_inputs.radius_graph(6, 0.9, seed=611)
+    x = attn_inputs.make_csr(row_ptr=rp, col=col, n_src=6, H=2, D=64, dtype="f32", seed=612,
+                             field_scores=True)
+    order = torch.tensor([5, 0, -1, 3, 99, 1], dtype=torch.int32, device=DEV)
+    out = torch.full((6, 2, 64), 7.0, device=DEV)
+    lse = torch.full((2, 6), 7.0, device=DEV)
+    attn.CsrCall(rp.to(DEV), col.to(DEV), x["v"].to(DEV), scores=x["scores"].to(DEV), out=out,
+                 lse=lse, row_order=order).run()
+    assert attn.device_status() == attn._abi.ATTN_EINVAL
+    o_ref, lse_ref = _ref(x, dot=False)
+    done = [0, 1, 3, 5]
+    assert float(np.abs(f64(out)[done] - o_ref[done]).max()) <= 1e-5
+    assert float(np.abs(f64(lse)[:, done] - lse_ref[:, done]).max()) <= 1e-5
+    assert (f64(out)[[2, 4]] == 7.0).all() and (f64(lse)[:, [2, 4]] == 7.0).all()
