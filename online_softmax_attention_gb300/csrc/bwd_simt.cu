@@ -96,6 +96,8 @@ constexpr int kRowDotRows = 4;  // rows per warp with loads in flight at once
 // (t, h) advance by a fixed step without a division per row.
 template <typename Tin, typename To, int D>
 __global__ void __launch_bounds__(256) row_dot_kernel(const BwdParams p) {
+    pdl_trigger();
+    pdl_wait();
     static_assert(D <= 128, "one 4-column chunk per lane");
     constexpr int U = kRowDotRows;
     const int lane = threadIdx.x & 31;
@@ -152,6 +154,8 @@ constexpr size_t dkdv_smem_bytes() {
 
 template <typename Tin, typename Tg, int D>
 __global__ void __launch_bounds__(NT) dkdv_simt_kernel(const BwdParams p) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int LD = D + 4;
     constexpr int NG = D / 64;
     extern __shared__ float4 smem4[];
@@ -283,6 +287,8 @@ constexpr size_t dq_smem_bytes() {
 
 template <typename Tin, typename Tg, int D>
 __global__ void __launch_bounds__(NT) dq_simt_kernel(const BwdParams p) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int LD = D + 4;
     constexpr int NG = D / 64;
     extern __shared__ float4 smem4[];
@@ -404,9 +410,9 @@ cudaError_t launch_persistent(K kern, size_t smem, int num_ctas, const BwdParams
         if (e != cudaSuccess) return e;
         num_ctas = sm_count() * (per_sm > 0 ? per_sm : 1);
     }
-    kern<<<num_ctas, NT, smem, s>>>(p);
+    e = launch_pdl(kern, dim3(num_ctas), dim3(NT), smem, s, p);
     count_launch();
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <typename Tin, typename Tg, int D>
@@ -437,9 +443,9 @@ cudaError_t row_dot_typed(const BwdParams &p, cudaStream_t s) {
     // 8 warps per block, kRowDotRows rows per warp and pass; at most 8 blocks per SM
     const int64_t want = (rows + 8 * kRowDotRows - 1) / (8 * kRowDotRows);
     const int64_t cap = 8LL * sm_count();
-    row_dot_kernel<Tin, To, D><<<(int)(want < cap ? want : cap), 256, 0, s>>>(p);
+    const cudaError_t e = launch_pdl(row_dot_kernel<Tin, To, D>, dim3((int)(want < cap ? want : cap)), dim3(256), 0, s, p);
     count_launch();
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <typename Tin, int D>

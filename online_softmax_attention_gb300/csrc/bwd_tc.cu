@@ -825,6 +825,9 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_tc_kernel(const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base;
+    // set-up above overlaps the previous kernel on the stream; inputs are read after this
+    pdl_trigger();
+    pdl_wait();
     if (warp < 4) {
         regs_dec<kFused ? C::kRegsProducerFused : C::kRegsProducer>();
         if ((warp == 0 || warp == 2) && lane == 0) dkdv_producer<D>(a, bars, sK, sV, sQ, sDO, warp == 2, wd);
@@ -1168,6 +1171,9 @@ __global__ void __launch_bounds__(kThreads, 1) dq_tc_kernel(const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base;
+    // set-up above overlaps the previous kernel on the stream; inputs are read after this
+    pdl_trigger();
+    pdl_wait();
     if (warp < 4) {
         regs_dec<C::kRegsProducer>();
         if (warp == 0 && lane == 0) dq_producer<D>(a, bars, sQ, sDO, sK, sV, wd);
@@ -1205,7 +1211,7 @@ cudaError_t launch(K kern, int smem, const TcBwdArgs &a, int num_ctas, cudaStrea
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (num_ctas <= 0) num_ctas = sm_count();
-    kern<<<num_ctas, kThreads, smem, s>>>(a);
+    e = launch_pdl(kern, dim3(num_ctas), dim3(kThreads), smem, s, a);
     count_launch();
     return cudaGetLastError();
 }

@@ -15,6 +15,16 @@ namespace attn {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// ---- programmatic dependent launch ----------------------------------------
+// pdl_trigger: the next kernel on the stream (launched with launch_pdl) may
+// start once every CTA of this grid has executed it.  pdl_wait: returns once
+// the previous grid on the stream has completed and its writes are visible
+// (at once when this kernel was launched the ordinary way); a kernel reads no
+// global memory before it.
+
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- element conversion -------------------------------------------------
 
 __device__ __forceinline__ float to_f32(float x) { return x; }

@@ -40,6 +40,10 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kChunks = 2;  // float4 column chunks per lane: D <= 256
+// Row-centric kernel: edges a warp gathers per step (tunable at compile time).
+#ifndef ATTN_CSR_INFLIGHT
+#define ATTN_CSR_INFLIGHT 4
+#endif
 
 template <typename T>
 __device__ __forceinline__ float4 ldg4(const T *p) {
@@ -263,7 +267,7 @@ template <typename T, typename Tout, bool kDot, int LG, int NCL>
 __global__ void __launch_bounds__(32 * kWarps) csr_rows_kernel(const CsrParams p) {
     constexpr int VEC = Vec<T>::N;
     constexpr int EP = 32 / LG;      // edge slots per warp
-    constexpr int U = 4 / NCL;       // edges per slot in flight
+    constexpr int U = ATTN_CSR_INFLIGHT / NCL;  // edges per slot in flight
     constexpr int BLK = EP * U;      // edges per block of the scan
     using raw = typename Vec<T>::raw;
     const int lane = threadIdx.x & 31;

@@ -91,6 +91,8 @@ __device__ __forceinline__ void stage_tile(float *dst, const T *src, int64_t st,
 
 template <typename Tin, typename Tout, int D>
 __global__ void __launch_bounds__(NT) fwd_simt_kernel(const FwdParams p) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int LD = D + 4;
     constexpr int NG = D / 64;  // column groups of 64 per thread row
     constexpr bool kAsync = kAsyncKV<Tin, D>;
@@ -321,9 +323,9 @@ cudaError_t launch_typed(const FwdParams &p, int num_ctas, cudaStream_t s, int *
         }
         num_ctas = sm_count() * (per_sm > 0 ? per_sm : 1);
     }
-    kern<<<num_ctas, NT, smem, s>>>(p);
+    e = launch_pdl(kern, dim3(num_ctas), dim3(NT), smem, s, p);
     count_launch();
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <typename Tin, int D>

@@ -586,6 +586,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base;
+    // set-up above overlaps the previous kernel on the stream; inputs are read after this
+    pdl_trigger();
+    pdl_wait();
 
     if (warp < 4) {
         regs_dec<C::kRegsProducer>();
@@ -622,9 +625,9 @@ cudaError_t launch_typed(const TcFwdArgs &args, int num_ctas, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (num_ctas <= 0) num_ctas = sm_count();
-    kern<<<num_ctas, kThreads, smem, s>>>(args);
+    e = launch_pdl(kern, dim3(num_ctas), dim3(kThreads), smem, s, args);
     count_launch();
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int D, bool kF8>

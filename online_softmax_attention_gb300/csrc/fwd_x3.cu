@@ -174,6 +174,8 @@ struct SplitParams {
 };
 
 __global__ void __launch_bounds__(256) split_parts_kernel(const SplitParams sp) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int C4 = D / 4;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int j = 0; j < 3; ++j) {
@@ -576,6 +578,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_x3_kernel(const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base;
+    // set-up above overlaps the previous kernel on the stream; inputs are read after this
+    pdl_trigger();
+    pdl_wait();
 
     if (warp < 4) {
         regs_dec<kRegsProducer>();
@@ -627,9 +632,9 @@ cudaError_t launch_fwd_x3(const FwdParams &p, int num_ctas, cudaStream_t s) {
     sp.job[2] = SplitJob{static_cast<const float *>(p.v), p.v_st, p.v_sh, p.n_k, kParts, v_parts};
     const int64_t n4 = (qn + kn) / 4;
     const int blocks = (int)std::min<int64_t>((n4 + 255) / 256, (int64_t)sm_count() * 8);
-    split_parts_kernel<<<blocks, 256, 0, s>>>(sp);
+    cudaError_t e = launch_pdl(split_parts_kernel, dim3(blocks), dim3(256), 0, s, sp);
     count_launch();
-    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
     X3Args args;
@@ -645,9 +650,9 @@ cudaError_t launch_fwd_x3(const FwdParams &p, int num_ctas, cudaStream_t s) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     if (num_ctas <= 0) num_ctas = sm_count();
-    kern<<<num_ctas, kThreads, kSmemBytes, s>>>(args);
+    e = launch_pdl(kern, dim3(num_ctas), dim3(kThreads), kSmemBytes, s, args);
     count_launch();
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace attn

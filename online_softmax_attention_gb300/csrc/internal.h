@@ -146,6 +146,30 @@ cudaError_t launch_dq_accum_convert(const BwdParams &p, cudaStream_t s);
 // Number of multiprocessors of the current device.
 int sm_count();
 
+#ifdef __CUDACC__
+// Launch with programmatic stream serialization: the kernel may start while the
+// kernel before it on the stream is still running (once every CTA of that one
+// has started and executed pdl_trigger).  Every kernel launched this way
+// executes pdl_wait -- which returns once the previous grid has completed and
+// its writes are visible -- before it reads global memory, so it sees that
+// kernel's results; what it overlaps is its launch and set-up.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+#endif
+
 // Kernel-launch accounting (attn_launch_count).
 void count_launch(int n = 1);
 

@@ -29,6 +29,8 @@ constexpr int kMaxD = 256;
 
 template <typename Tout>
 __global__ void __launch_bounds__(32 * kWarps) merge_kernel(const MergeParams p) {
+    pdl_trigger();
+    pdl_wait();  // the partials come from the kernel before this one
     const int lane = threadIdx.x & 31;
     const int64_t rows = (int64_t)p.n_q * p.H;
     const int64_t stride = (int64_t)gridDim.x * kWarps;
@@ -87,13 +89,14 @@ cudaError_t launch_merge(const MergeParams &p, cudaStream_t s) {
     if (rows == 0) return cudaSuccess;
     const int64_t want = (rows + kWarps - 1) / kWarps;
     const int grid = (int)(want < (int64_t)sm_count() * 16 ? want : (int64_t)sm_count() * 16);
+    cudaError_t e;
     switch (p.o_dtype) {
-    case ATTN_F16: merge_kernel<__half><<<grid, 32 * kWarps, 0, s>>>(p); break;
-    case ATTN_BF16: merge_kernel<__nv_bfloat16><<<grid, 32 * kWarps, 0, s>>>(p); break;
-    default: merge_kernel<float><<<grid, 32 * kWarps, 0, s>>>(p); break;
+    case ATTN_F16: e = launch_pdl(merge_kernel<__half>, dim3(grid), dim3(32 * kWarps), 0, s, p); break;
+    case ATTN_BF16: e = launch_pdl(merge_kernel<__nv_bfloat16>, dim3(grid), dim3(32 * kWarps), 0, s, p); break;
+    default: e = launch_pdl(merge_kernel<float>, dim3(grid), dim3(32 * kWarps), 0, s, p); break;
     }
     count_launch();
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace attn

@@ -23,6 +23,8 @@ prep_kernel(const int32_t *__restrict__ cu_q, const int32_t *__restrict__ cu_k, 
     __shared__ int s_warp[kPrepThreads / 32];
     __shared__ long long s_carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_trigger();
+    pdl_wait();  // the previous kernel on the stream may still read this schedule block
     if (tid == 0) {
         s_bad = 0;
         s_carry = 0;
@@ -88,11 +90,11 @@ prep_kernel(const int32_t *__restrict__ cu_q, const int32_t *__restrict__ cu_k, 
 cudaError_t launch_prep(const int32_t *cu_q, const int32_t *cu_k, int n_seq, int n_q, int n_k,
                         int H, int block, int causal, int rows_are_keys, int splits, Sched sched,
                         int *status, cudaStream_t s) {
-    prep_kernel<<<1, kPrepThreads, 0, s>>>(cu_q, cu_k, n_seq, n_q, n_k, H, block, causal,
-                                          rows_are_keys, splits, sched.hdr,
-                                          const_cast<int *>(sched.prefix), status);
+    cudaError_t e = launch_pdl(prep_kernel, dim3(1), dim3(kPrepThreads), 0, s, cu_q, cu_k, n_seq, n_q, n_k, H,
+                               block, causal, rows_are_keys, splits, sched.hdr,
+                               const_cast<int *>(sched.prefix), status);
     count_launch();
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace attn
