@@ -260,6 +260,7 @@ __device__ void dkdv_mma(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, uint32
     // Descriptors built once; per MMA a constant is added to the start address.
     const uint64_t kmaj = sdesc_sw128(0, 16, 1024);            // K-major, base address 0
     const uint64_t nmaj = sdesc_sw128(0, C::kBoxBytes, 1024);  // N-major, base address 0
+    // (the issue_* lambdas are called by the elected lane)
     // X^T = A B^T with A, B (128 x D) K-major tiles -> TMEM columns [col, col + 128)
     auto issue_ss = [&](uint32_t col, uint32_t A, uint32_t B, uint32_t id) {
         const uint64_t ad = kmaj + sdesc_step(A), bd = kmaj + sdesc_step(B);
@@ -278,63 +279,82 @@ __device__ void dkdv_mma(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, uint32
             mma_ts(tmem + acc_col, tmem + a_col + 8 * kk + (kk >= 4 ? 32 : 0), yd + sdesc_step(kk * 2048), idTS,
                    acc || kk > 0);
     };
-    auto take = [&](uint64_t *full, uint32_t slot, uint32_t phase) -> bool {
-        return mbar_wait(smem_u32(&full[slot]), phase, wd);
+    auto wait = [&](uint64_t &bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar), parity, wd));
     };
 
     for (int i = 0;; ++i) {
         int w;
-        if (!sched_take(bars.sched, i, w, wd)) return;
+        if (!sched_take_warp(bars.sched, i, w, wd)) return;
         if (w >= total) return;
         const DkdvInfo f = dkdv_info(p, w);
         if (f.nq == 0) continue;
-        if (!mbar_wait(smem_u32(&bars.kv_full), kv_cnt & 1, wd)) return;
+        if (!wait(bars.kv_full, kv_cnt & 1)) return;
         ++kv_cnt;
         uint32_t qs = qr.slot(), os = dr.slot();
-        if (!take(bars.q_full, qs, qr.phase())) return;  // Q and dO of the block
+        if (!wait(bars.q_full[qs], qr.phase())) return;  // Q and dO of the block
         ++qr.i;
         ++dr.i;
         tc_fence_after();
-        issue_ss(0, sK, sQ + qs * C::kTileBytes, idST);  // S^T = K Q^T
-        tc_commit(smem_u32(&bars.st_full));
-        issue_ss(BT, sV, sDO + os * C::kTileBytes, idSS);  // dP^T = V dO^T
-        tc_commit(smem_u32(&bars.dp_full));
+        if (elect_one()) {
+            issue_ss(0, sK, sQ + qs * C::kTileBytes, idST);  // S^T = K Q^T
+            tc_commit(smem_u32(&bars.st_full));
+            issue_ss(BT, sV, sDO + os * C::kTileBytes, idSS);  // dP^T = V dO^T
+            tc_commit(smem_u32(&bars.dp_full));
+        }
+        __syncwarp();
         for (int qb = 0; qb < f.nq; ++qb) {
-            if (!mbar_wait(smem_u32(&bars.p_ready), p_cnt & 1, wd)) return;
+            if (!wait(bars.p_ready, p_cnt & 1)) return;
             ++p_cnt;
             if (qb == 0) {
-                if (!mbar_wait(smem_u32(&bars.acc_free), (af_cnt & 1) ^ 1, wd)) return;
+                if (!wait(bars.acc_free, (af_cnt & 1) ^ 1)) return;
                 ++af_cnt;
             }
             tc_fence_after();
-            issue_ts(256, 0, sDO + os * C::kTileBytes, qb > 0);  // dV += P^T dO
-            tc_commit(smem_u32(&bars.do_empty[os]));
+            if (elect_one()) {
+                issue_ts(256, 0, sDO + os * C::kTileBytes, qb > 0);  // dV += P^T dO
+                tc_commit(smem_u32(&bars.do_empty[os]));
+            }
+            __syncwarp();
             const bool next = qb + 1 < f.nq;
             uint32_t qsn = 0, osn = 0;
             if (next) {
                 qsn = qr.slot();
-                if (!take(bars.q_full, qsn, qr.phase())) return;
+                if (!wait(bars.q_full[qsn], qr.phase())) return;
                 ++qr.i;
                 tc_fence_after();
-                issue_ss(0, sK, sQ + qsn * C::kTileBytes, idST);  // S^T of the next block
-                tc_commit(smem_u32(&bars.st_full));
+                if (elect_one()) {
+                    issue_ss(0, sK, sQ + qsn * C::kTileBytes, idST);  // S^T of the next block
+                    tc_commit(smem_u32(&bars.st_full));
+                }
+                __syncwarp();
             }
-            if (!mbar_wait(smem_u32(&bars.ds_ready), ds_cnt & 1, wd)) return;
+            if (!wait(bars.ds_ready, ds_cnt & 1)) return;
             ++ds_cnt;
             tc_fence_after();
-            issue_ts(256 + D, BT, sQ + qs * C::kTileBytes, qb > 0);  // dK += dS^T Q
-            tc_commit(smem_u32(&bars.q_empty[qs]));
             if (next) {
                 osn = dr.slot();  // dO landed with its Q (q_full, waited above)
                 ++dr.i;
-                issue_ss(BT, sV, sDO + osn * C::kTileBytes, idSS);  // dP^T of the next block
-                tc_commit(smem_u32(&bars.dp_full));
+            }
+            if (elect_one()) {
+                issue_ts(256 + D, BT, sQ + qs * C::kTileBytes, qb > 0);  // dK += dS^T Q
+                tc_commit(smem_u32(&bars.q_empty[qs]));
+                if (next) {
+                    issue_ss(BT, sV, sDO + osn * C::kTileBytes, idSS);  // dP^T of the next block
+                    tc_commit(smem_u32(&bars.dp_full));
+                }
+            }
+            __syncwarp();
+            if (next) {
                 qs = qsn;
                 os = osn;
             }
         }
-        tc_commit(smem_u32(&bars.acc_done));
-        tc_commit(smem_u32(&bars.kv_empty));
+        if (elect_one()) {
+            tc_commit(smem_u32(&bars.acc_done));
+            tc_commit(smem_u32(&bars.kv_empty));
+        }
+        __syncwarp();
     }
 }
 
@@ -831,10 +851,14 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_tc_kernel(const __grid_const
     if (warp < 4) {
         regs_dec<kFused ? C::kRegsProducerFused : C::kRegsProducer>();
         if ((warp == 0 || warp == 2) && lane == 0) dkdv_producer<D>(a, bars, sK, sV, sQ, sDO, warp == 2, wd);
-        else if (warp == 1 && lane == 0) {
-            if constexpr (kFused) dkdvq_mma<D, kBF16>(a, bars, sK, sV, sQ, sDO, sDS, tmem, wd);
-            else dkdv_mma<D, kBF16>(a, bars, sK, sV, sQ, sDO, tmem, wd);
-            if (aborting(wd)) {  // let issued MMAs finish before TMEM is freed
+        else if (warp == 1) {
+            // the separate issuer runs on the whole warp, the fused one on lane 0
+            if constexpr (kFused) {
+                if (lane == 0) dkdvq_mma<D, kBF16>(a, bars, sK, sV, sQ, sDO, sDS, tmem, wd);
+            } else {
+                dkdv_mma<D, kBF16>(a, bars, sK, sV, sQ, sDO, tmem, wd);
+            }
+            if (lane == 0 && aborting(wd)) {  // let issued MMAs finish before TMEM is freed
                 tc_commit(smem_u32(&bars.mma_drain));
                 drain_wait(smem_u32(&bars.mma_drain), 0, kDrainCycles);
             }
@@ -955,6 +979,7 @@ __device__ void dq_mma(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint32_t s
 
     const uint64_t kmaj = sdesc_sw128(0, 16, 1024);
     const uint64_t nmaj = sdesc_sw128(0, C::kBoxBytes, 1024);
+    // (called by the elected lane)
     auto issue_ss = [&](uint32_t col, uint32_t A, uint32_t B, uint32_t id) {
         const uint64_t ad = kmaj + sdesc_step(A), bd = kmaj + sdesc_step(B);
 #pragma unroll
@@ -963,63 +988,74 @@ __device__ void dq_mma(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint32_t s
             mma_ss(tmem + col, ad + off, bd + off, id, kk > 0);
         }
     };
+    auto wait = [&](uint64_t &bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar), parity, wd));
+    };
     // wait for the next K and V tiles (one barrier for both); returns their slots
     auto take_kv = [&](uint32_t &ks, uint32_t &vs) -> bool {
         ks = kr.slot();
         vs = vr.slot();
-        if (!mbar_wait(smem_u32(&bars.k_full[ks]), kr.phase(), wd)) return false;
+        if (!wait(bars.k_full[ks], kr.phase())) return false;
         ++kr.i;
         ++vr.i;
         return true;
     };
+    // S = Q K^T and dP = dO V^T of one key block, then their commits
+    auto issue_s_dp = [&](uint32_t ks, uint32_t vs) {
+        if (elect_one()) {
+            issue_ss(0, sQ, sK + ks * C::kTileBytes, idS);
+            issue_ss(BT, sDO, sV + vs * C::kTileBytes, idSS);
+            tc_commit(smem_u32(&bars.sp_full));
+            tc_commit(smem_u32(&bars.v_empty[vs]));
+        }
+        __syncwarp();
+    };
 
     for (int i = 0;; ++i) {
         int w;
-        if (!sched_take(bars.sched, i, w, wd)) return;
+        if (!sched_take_warp(bars.sched, i, w, wd)) return;
         if (w >= total) return;
         const DqInfo f = dq_info(p, w);
         if (f.nk == 0) continue;
-        if (!mbar_wait(smem_u32(&bars.q_full), q_cnt & 1, wd)) return;
+        if (!wait(bars.q_full, q_cnt & 1)) return;
         ++q_cnt;
         uint32_t ks, vs;
         if (!take_kv(ks, vs)) return;
         tc_fence_after();
-        issue_ss(0, sQ, sK + ks * C::kTileBytes, idS);     // S = Q K^T
-        issue_ss(BT, sDO, sV + vs * C::kTileBytes, idSS);  // dP = dO V^T
-        tc_commit(smem_u32(&bars.sp_full));
-        tc_commit(smem_u32(&bars.v_empty[vs]));
+        issue_s_dp(ks, vs);
         for (int j = 0; j < f.nk; ++j) {
-            if (!mbar_wait(smem_u32(&bars.sp_free), spf_cnt & 1, wd)) return;
+            if (!wait(bars.sp_free, spf_cnt & 1)) return;
             ++spf_cnt;
             uint32_t ksn = 0;
             if (j + 1 < f.nk) {
                 uint32_t vsn;
                 if (!take_kv(ksn, vsn)) return;
                 tc_fence_after();
-                issue_ss(0, sQ, sK + ksn * C::kTileBytes, idS);
-                issue_ss(BT, sDO, sV + vsn * C::kTileBytes, idSS);
-                tc_commit(smem_u32(&bars.sp_full));
-                tc_commit(smem_u32(&bars.v_empty[vsn]));
+                issue_s_dp(ksn, vsn);
             }
-            if (!mbar_wait(smem_u32(&bars.ds_ready[ds_cnt & 1]), (ds_cnt >> 1) & 1, wd)) return;
+            if (!wait(bars.ds_ready[ds_cnt & 1], (ds_cnt >> 1) & 1)) return;
             ++ds_cnt;
             if (j == 0) {
-                if (!mbar_wait(smem_u32(&bars.acc_free), (af_cnt & 1) ^ 1, wd)) return;
+                if (!wait(bars.acc_free, (af_cnt & 1) ^ 1)) return;
                 ++af_cnt;
             }
             tc_fence_after();
-            {
+            if (elect_one()) {
                 const uint64_t kd = nmaj + sdesc_step(sK + ks * C::kTileBytes);
                 const uint32_t ds_col = tmem + 256 + 64 * (j & 1);
 #pragma unroll
                 for (int kk = 0; kk < BT / 16; ++kk)  // dQ += dS K
                     mma_ts(tmem + 384, ds_col + 8 * kk, kd + sdesc_step(kk * 2048), idTS, j > 0 || kk > 0);
+                tc_commit(smem_u32(&bars.k_empty[ks]));
             }
-            tc_commit(smem_u32(&bars.k_empty[ks]));
+            __syncwarp();
             ks = ksn;
         }
-        tc_commit(smem_u32(&bars.acc_done));
-        tc_commit(smem_u32(&bars.q_empty));
+        if (elect_one()) {
+            tc_commit(smem_u32(&bars.acc_done));
+            tc_commit(smem_u32(&bars.q_empty));
+        }
+        __syncwarp();
     }
 }
 
@@ -1177,9 +1213,9 @@ __global__ void __launch_bounds__(kThreads, 1) dq_tc_kernel(const __grid_constan
     if (warp < 4) {
         regs_dec<C::kRegsProducer>();
         if (warp == 0 && lane == 0) dq_producer<D>(a, bars, sQ, sDO, sK, sV, wd);
-        else if (warp == 1 && lane == 0) {
-            dq_mma<D, kBF16>(a, bars, sQ, sDO, sK, sV, tmem, wd);
-            if (aborting(wd)) {  // let issued MMAs finish before TMEM is freed
+        else if (warp == 1) {
+            dq_mma<D, kBF16>(a, bars, sQ, sDO, sK, sV, tmem, wd);  // the whole warp
+            if (lane == 0 && aborting(wd)) {  // let issued MMAs finish before TMEM is freed
                 tc_commit(smem_u32(&bars.mma_drain));
                 drain_wait(smem_u32(&bars.mma_drain), 0, kDrainCycles);
             }

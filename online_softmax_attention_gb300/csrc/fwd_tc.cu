@@ -252,6 +252,13 @@ __device__ void producer(const TcFwdArgs &a, FwdBars &bars, int *sched_item, uin
 }
 
 // ---- warp 1: MMA issuer ----------------------------------------------------------
+// Run by all 32 lanes of warp 1 in step: every lane does the same waits (their
+// results are the same), and one elected lane issues each group of MMAs and the
+// commits.  With the loop converged the compiler keeps the descriptor and
+// counter arithmetic on the uniform datapath, so the issue keeps pace even while
+// the softmax warps on the same sub-partition fill the FMA and ALU pipes (a
+// single lane running the loop alone fell to ~170 cycles per 64-cycle MMA
+// beside FMA-bound neighbours in a microbenchmark; converged: ~73).
 
 template <int D, bool kBF16, bool kF8, bool kPrune>
 __device__ void mma_issuer(const TcFwdArgs &a, FwdBars &bars, const int *sched_item,
@@ -280,49 +287,66 @@ __device__ void mma_issuer(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
         const uint64_t qa = q_desc + sdesc_step(t * C::kQKTileBytes);
         const uint64_t ka = k_desc + sdesc_step(kslot * C::kQKTileBytes);
         const uint32_t d = tmem + BN * t;
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < C::kSSteps; ++kk) {
-            const uint64_t off = sdesc_step((kk >> 2) * C::kBoxBytes + (kk & 3) * 32);
-            if (kF8) mma_ss_f8(d, qa + off, ka + off, idS, kk > 0);
-            else mma_ss(d, qa + off, ka + off, idS, kk > 0);
+            for (int kk = 0; kk < C::kSSteps; ++kk) {
+                const uint64_t off = sdesc_step((kk >> 2) * C::kBoxBytes + (kk & 3) * 32);
+                if (kF8) mma_ss_f8(d, qa + off, ka + off, idS, kk > 0);
+                else mma_ss(d, qa + off, ka + off, idS, kk > 0);
+            }
+            tc_commit(smem_u32(&bars.s_full[t]));
         }
-        tc_commit(smem_u32(&bars.s_full[t]));
+        __syncwarp();
     };
     // U_t (+)= P_t V over the 128 keys in steps of 16 (8 TMEM columns of P)
     auto issue_pv = [&](int t, uint32_t vslot, bool acc) {  // V tile in slot `vslot` of the V ring
         const uint64_t va = v_desc + sdesc_step(vslot * C::kVTileBytes);
         const uint32_t d = tmem + 256 + D * t, pa = tmem + BN * t;
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts(d, pa + 8 * kk, va + sdesc_step(kk * 2048), idO, acc || kk > 0);
+            for (int kk = 0; kk < BN / 16; ++kk)
+                mma_ts(d, pa + 8 * kk, va + sdesc_step(kk * 2048), idO, acc || kk > 0);
+        }
+        __syncwarp();
+    };
+    // the warp's wait: every lane polls (the same observations), and the result
+    // is made warp-uniform so that an abort takes all lanes out together
+    auto wait = [&](uint64_t &bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar), parity, wd));
+    };
+    // a commit by the lane that issued the MMAs
+    auto commit = [&](uint64_t &bar) {
+        if (elect_one()) tc_commit(smem_u32(&bar));
+        __syncwarp();
     };
 
     for (int i = 0;; ++i) {
         const int slot = i & 1;
-        if (!mbar_wait(smem_u32(&bars.sched_full[slot]), (i >> 1) & 1, wd)) return;
+        if (!wait(bars.sched_full[slot], (i >> 1) & 1)) return;
         const int w = sched_item[slot];
-        mbar_arrive(smem_u32(&bars.sched_empty[slot]));
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&bars.sched_empty[slot]));
         if (w >= total) return;
         const ItemInfo f = item_info(p, w);
         if (f.nkv == 0) continue;
 #pragma unroll
         for (int t = 0; t < NQT; ++t) {
             if (f.n[t] == 0) continue;
-            if (!mbar_wait(smem_u32(&bars.q_full[t]), q_cnt[t] & 1, wd)) return;
+            if (!wait(bars.q_full[t], q_cnt[t] & 1)) return;
             ++q_cnt[t];
         }
         // K_0
         const uint32_t ks = kr.slot();
-        if (!mbar_wait(smem_u32(&bars.k_full[ks]), kr.phase(), wd)) return;
+        if (!wait(bars.k_full[ks], kr.phase())) return;
         ++kr.i;
         tc_fence_after();
 #pragma unroll
         for (int t = 0; t < NQT; ++t) {
             if (f.n[t] == 0) continue;
             issue_s(t, ks);
-            if (f.n[t] == 1) tc_commit(smem_u32(&bars.q_empty[t]));
+            if (f.n[t] == 1) commit(bars.q_empty[t]);
         }
-        tc_commit(smem_u32(&bars.k_empty[ks]));
+        commit(bars.k_empty[ks]);
 
         for (int j = 0; j < f.nkv; ++j) {
             const uint32_t vs = vr.slot();  // V_j landed with K_j (k_full, waited before S_j)
@@ -332,32 +356,32 @@ __device__ void mma_issuer(const TcFwdArgs &a, FwdBars &bars, const int *sched_i
 #pragma unroll
             for (int t = 0; t < NQT; ++t) {
                 if (j >= f.n[t]) continue;
-                if (!mbar_wait(smem_u32(&bars.p_full[t]), p_cnt[t] & 1, wd)) return;
+                if (!wait(bars.p_full[t], p_cnt[t] & 1)) return;
                 ++p_cnt[t];
                 if (j == 0) {
                     // the previous item's epilogue of this tile has read U_t
-                    if (!mbar_wait(smem_u32(&bars.o_free[t]), (of_cnt[t] & 1) ^ 1, wd)) return;
+                    if (!wait(bars.o_free[t], (of_cnt[t] & 1) ^ 1)) return;
                     ++of_cnt[t];
                 }
                 tc_fence_after();
                 // a pruned tile adds nothing to U (the first tile is always admitted)
                 const bool pruned = kPrune && *reinterpret_cast<const volatile int *>(&ps->skip[t]);
                 if (!pruned) issue_pv(t, vs, j > 0);
-                if (j == f.n[t] - 1) tc_commit(smem_u32(&bars.o_done[t]));
+                if (j == f.n[t] - 1) commit(bars.o_done[t]);
                 if (j + 1 < f.n[t]) {
                     if (!have_next_k) {
                         nks = kr.slot();
-                        if (!mbar_wait(smem_u32(&bars.k_full[nks]), kr.phase(), wd)) return;
+                        if (!wait(bars.k_full[nks], kr.phase())) return;
                         ++kr.i;
                         have_next_k = true;
                         tc_fence_after();
                     }
                     issue_s(t, nks);
-                    if (j + 1 == f.n[t] - 1) tc_commit(smem_u32(&bars.q_empty[t]));
+                    if (j + 1 == f.n[t] - 1) commit(bars.q_empty[t]);
                 }
             }
-            tc_commit(smem_u32(&bars.v_empty[vs]));
-            if (have_next_k) tc_commit(smem_u32(&bars.k_empty[nks]));
+            commit(bars.v_empty[vs]);
+            if (have_next_k) commit(bars.k_empty[nks]);
         }
     }
 }
@@ -595,12 +619,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         if (warp == 0) {
             if (lane == 0) producer<D, kF8>(a, bars, sched_item, sQ, sK, sV, wd);
         } else if (warp == 1) {
-            if (lane == 0) {
-                mma_issuer<D, kBF16, kF8, kPrune>(a, bars, sched_item, &prune_shared, sQ, sK, sV, tmem, wd);
-                if (aborting(wd)) {  // let issued MMAs finish before TMEM is freed
-                    tc_commit(smem_u32(&bars.mma_drain));
-                    drain_wait(smem_u32(&bars.mma_drain), 0, kDrainCycles);
-                }
+            mma_issuer<D, kBF16, kF8, kPrune>(a, bars, sched_item, &prune_shared, sQ, sK, sV, tmem, wd);
+            if (lane == 0 && aborting(wd)) {  // let issued MMAs finish before TMEM is freed
+                tc_commit(smem_u32(&bars.mma_drain));
+                drain_wait(smem_u32(&bars.mma_drain), 0, kDrainCycles);
             }
         }
     } else {

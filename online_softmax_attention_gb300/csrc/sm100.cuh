@@ -88,6 +88,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
     }
 }
 
+// One lane of a converged warp is elected (the lowest active one: lane 0 when
+// the whole warp runs).
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n"
+        " .reg .pred P;\n"
+        " elect.sync _|P, 0xffffffff;\n"
+        " selp.u32 %0, 1, 0, P;\n"
+        "}\n"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // Position in a ring of N shared-memory slots guarded by full / empty
 // mbarriers; `i` counts the uses of the ring.
 template <int N>
