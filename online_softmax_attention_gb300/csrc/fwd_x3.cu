@@ -264,6 +264,8 @@ __device__ void producer(const X3Args &a, X3Bars &bars, int *sched_item, uint32_
 }
 
 // ---- warp 1: MMA issuer ------------------------------------------------------------
+// Run by all 32 lanes of warp 1 in step (uniform waits; one elected lane issues
+// each group of MMAs and the commits), as in the 16-bit forward.
 
 __device__ void mma_issuer(const X3Args &a, X3Bars &bars, const int *sched_item, uint32_t sQ, uint32_t sK,
                            uint32_t sV, uint32_t tmem, const Watchdog &wd) {
@@ -281,6 +283,7 @@ __device__ void mma_issuer(const X3Args &a, X3Bars &bars, const int *sched_item,
     // S_t = sum over the six part products Q_a K_b^T, 4 steps of 16 over D each
     auto issue_s = [&](int t, uint32_t kslot) {
         const uint32_t d = tmem + kTmemTile * t;
+        if (elect_one()) {
 #pragma unroll
         for (int ch = 0; ch < 6; ++ch) {
             const uint64_t qa = q_desc + sdesc_step(t * kQBytes + prod_a(ch) * kQPart);
@@ -292,11 +295,14 @@ __device__ void mma_issuer(const X3Args &a, X3Bars &bars, const int *sched_item,
             }
         }
         tc_commit(smem_u32(&bars.s_full[t]));
+        }
+        __syncwarp();
     };
     // this key tile's partial U_t = sum over the six part products P_a V_b, from
     // zero; 4 steps of 16 keys (P_a from TMEM, V_b N-major from shared memory)
     auto issue_pv = [&](int t, uint32_t vslot) {
         const uint32_t d = tmem + kTmemTile * t + kColU;
+        if (elect_one()) {
 #pragma unroll
         for (int ch = 0; ch < 6; ++ch) {
             const uint64_t va = v_desc + sdesc_step(vslot * kVBytes + prod_b(ch) * kKVPart);
@@ -307,33 +313,44 @@ __device__ void mma_issuer(const X3Args &a, X3Bars &bars, const int *sched_item,
                 mma_ts(d, tmem + kTmemTile * t + col, va + sdesc_step(kk * 2048), idO, ch > 0 || kk > 0);
             }
         }
+        }
+        __syncwarp();
+    };
+    auto wait = [&](uint64_t &bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar), parity, wd));
+    };
+    // a commit by the lane that issued the MMAs
+    auto commit = [&](uint64_t &bar) {
+        if (elect_one()) tc_commit(smem_u32(&bar));
+        __syncwarp();
     };
 
     for (int i = 0;; ++i) {
         const int slot = i & 1;
-        if (!mbar_wait(smem_u32(&bars.sched_full[slot]), (i >> 1) & 1, wd)) return;
+        if (!wait(bars.sched_full[slot], (i >> 1) & 1)) return;
         const int w = sched_item[slot];
-        mbar_arrive(smem_u32(&bars.sched_empty[slot]));
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&bars.sched_empty[slot]));
         if (w >= total) return;
         const ItemInfo f = item_info(p, w);
         if (f.nkv == 0) continue;
 #pragma unroll
         for (int t = 0; t < NQT; ++t) {
             if (f.n[t] == 0) continue;
-            if (!mbar_wait(smem_u32(&bars.q_full[t]), q_cnt[t] & 1, wd)) return;
+            if (!wait(bars.q_full[t], q_cnt[t] & 1)) return;
             ++q_cnt[t];
         }
         const uint32_t ks = kr.slot();
-        if (!mbar_wait(smem_u32(&bars.k_full[ks]), kr.phase(), wd)) return;
+        if (!wait(bars.k_full[ks], kr.phase())) return;
         ++kr.i;
         tc_fence_after();
 #pragma unroll
         for (int t = 0; t < NQT; ++t) {
             if (f.n[t] == 0) continue;
             issue_s(t, ks);
-            if (f.n[t] == 1) tc_commit(smem_u32(&bars.q_empty[t]));
+            if (f.n[t] == 1) commit(bars.q_empty[t]);
         }
-        tc_commit(smem_u32(&bars.k_empty[ks]));
+        commit(bars.k_empty[ks]);
 
         for (int j = 0; j < f.nkv; ++j) {
             const uint32_t vs = vr.slot();  // V_j landed with K_j
@@ -343,30 +360,30 @@ __device__ void mma_issuer(const X3Args &a, X3Bars &bars, const int *sched_item,
 #pragma unroll
             for (int t = 0; t < NQT; ++t) {
                 if (j >= f.n[t]) continue;
-                if (!mbar_wait(smem_u32(&bars.p_full[t]), p_cnt[t] & 1, wd)) return;
+                if (!wait(bars.p_full[t], p_cnt[t] & 1)) return;
                 ++p_cnt[t];
                 if (j == 0) {
                     // the previous item's epilogue of this tile has read its last partial
-                    if (!mbar_wait(smem_u32(&bars.o_free[t]), (of_cnt[t] & 1) ^ 1, wd)) return;
+                    if (!wait(bars.o_free[t], (of_cnt[t] & 1) ^ 1)) return;
                     ++of_cnt[t];
                 }
                 tc_fence_after();
                 issue_pv(t, vs);
-                if (j == f.n[t] - 1) tc_commit(smem_u32(&bars.o_done[t]));
+                if (j == f.n[t] - 1) commit(bars.o_done[t]);
                 if (j + 1 < f.n[t]) {
                     if (!have_next_k) {
                         nks = kr.slot();
-                        if (!mbar_wait(smem_u32(&bars.k_full[nks]), kr.phase(), wd)) return;
+                        if (!wait(bars.k_full[nks], kr.phase())) return;
                         ++kr.i;
                         have_next_k = true;
                         tc_fence_after();
                     }
                     issue_s(t, nks);
-                    if (j + 1 == f.n[t] - 1) tc_commit(smem_u32(&bars.q_empty[t]));
+                    if (j + 1 == f.n[t] - 1) commit(bars.q_empty[t]);
                 }
             }
-            tc_commit(smem_u32(&bars.v_empty[vs]));
-            if (have_next_k) tc_commit(smem_u32(&bars.k_empty[nks]));
+            commit(bars.v_empty[vs]);
+            if (have_next_k) commit(bars.k_empty[nks]);
         }
     }
 }
@@ -587,12 +604,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_x3_kernel(const __grid_consta
         if (warp == 0) {
             if (lane == 0) producer(a, bars, sched_item, sQ, sK, sV, wd);
         } else if (warp == 1) {
-            if (lane == 0) {
-                mma_issuer(a, bars, sched_item, sQ, sK, sV, tmem, wd);
-                if (aborting(wd)) {  // let issued MMAs finish before TMEM is freed
-                    tc_commit(smem_u32(&bars.mma_drain));
-                    drain_wait(smem_u32(&bars.mma_drain), 0, kDrainCycles);
-                }
+            mma_issuer(a, bars, sched_item, sQ, sK, sV, tmem, wd);  // the whole warp
+            if (lane == 0 && aborting(wd)) {  // let issued MMAs finish before TMEM is freed
+                tc_commit(smem_u32(&bars.mma_drain));
+                drain_wait(smem_u32(&bars.mma_drain), 0, kDrainCycles);
             }
         }
     } else {
