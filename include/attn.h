@@ -364,7 +364,9 @@ ATTN_API int attn_fwd_noalloc(const attn_fwd_args *a, void *stream);
  * ATTN_WATCHDOG_CYCLES environment variable; cycles <= 0 restores that).  When
  * a wait runs out the kernel stops, drains its loads in flight, frees its
  * tensor memory and exits; attn_device_status() then returns ATTN_ETIMEOUT.
- * Returns the previous budget. */
+ * Budgets below 2^20 cycles (meant for failure-detection tests) make every
+ * wait poll without suspending, so that they run out reliably; larger ones let
+ * a wait suspend in hardware first.  Returns the previous budget. */
 ATTN_API long long attn_set_watchdog_cycles(long long cycles);
 
 /* Synchronises `stream`, then returns and clears the device-side status word

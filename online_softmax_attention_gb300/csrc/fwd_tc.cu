@@ -185,6 +185,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long l
 }
 
 // ---- warp 0: TMA producer ------------------------------------------------------
+// Run by all 32 lanes of warp 0 in step: uniform waits, one elected lane takes
+// the work item and issues the loads (as the MMA issuer, so that the loop's
+// arithmetic stays on the uniform datapath beside the busy softmax warps).
 
 template <int D, bool kF8>
 __device__ void producer(const TcFwdArgs &a, FwdBars &bars, int *sched_item, uint32_t sQ, uint32_t sK,
@@ -196,28 +199,38 @@ __device__ void producer(const TcFwdArgs &a, FwdBars &bars, int *sched_item, uin
     RingPos<C::kVStages> vr;
     uint32_t q_uses[NQT] = {0, 0};
     bool q_pending[NQT] = {false, false};
+    auto wait = [&](uint64_t &bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar), parity, wd));
+    };
     // the K and V tiles of one key tile into their rings; both land on the K
     // slot's full barrier, so the MMA issuer waits once per key tile
     auto load_kv = [&](int row, int h) -> bool {
         const uint32_t ks = kr.slot(), vs = vr.slot();
-        if (!mbar_wait(smem_u32(&bars.k_empty[ks]), kr.phase() ^ 1, wd)) return false;
-        if (!mbar_wait(smem_u32(&bars.v_empty[vs]), vr.phase() ^ 1, wd)) return false;
-        const uint32_t bar = smem_u32(&bars.k_full[ks]);
-        mbar_expect_tx(bar, C::kQKTileBytes + C::kVTileBytes);
-        for (int g = 0; g < C::kQKBoxes; ++g)
-            tma_load_3d(sK + ks * C::kQKTileBytes + g * C::kBoxBytes, &a.tk, C::kQKBoxCols * g, row, h, bar);
-        for (int g = 0; g < C::kVBoxes; ++g)
-            tma_load_3d(sV + vs * C::kVTileBytes + g * C::kBoxBytes, &a.tv, 64 * g, row, h, bar);
+        if (!wait(bars.k_empty[ks], kr.phase() ^ 1)) return false;
+        if (!wait(bars.v_empty[vs], vr.phase() ^ 1)) return false;
+        if (elect_one()) {
+            const uint32_t bar = smem_u32(&bars.k_full[ks]);
+            mbar_expect_tx(bar, C::kQKTileBytes + C::kVTileBytes);
+            for (int g = 0; g < C::kQKBoxes; ++g)
+                tma_load_3d(sK + ks * C::kQKTileBytes + g * C::kBoxBytes, &a.tk, C::kQKBoxCols * g, row, h, bar);
+            for (int g = 0; g < C::kVBoxes; ++g)
+                tma_load_3d(sV + vs * C::kVTileBytes + g * C::kBoxBytes, &a.tv, 64 * g, row, h, bar);
+        }
+        __syncwarp();
         ++kr.i;
         ++vr.i;
         return true;
     };
     for (int i = 0;; ++i) {
         const int slot = i & 1;
-        if (!mbar_wait(smem_u32(&bars.sched_empty[slot]), ((i >> 1) & 1) ^ 1, wd)) break;
-        const int w = fetch_item(p.sched.hdr, p.static_items, i);
-        sched_item[slot] = w;
-        mbar_arrive(smem_u32(&bars.sched_full[slot]));
+        if (!wait(bars.sched_empty[slot], ((i >> 1) & 1) ^ 1)) break;
+        int w = 0;
+        if (elect_one()) {
+            w = fetch_item(p.sched.hdr, p.static_items, i);
+            sched_item[slot] = w;
+            mbar_arrive(smem_u32(&bars.sched_full[slot]));
+        }
+        w = __shfl_sync(0xffffffffu, w, 0);
         if (w >= total) break;
         const ItemInfo f = item_info(p, w);
         bool ok = true;
@@ -225,14 +238,17 @@ __device__ void producer(const TcFwdArgs &a, FwdBars &bars, int *sched_item, uin
         for (int t = 0; t < NQT; ++t) {
             if (!ok) break;
             if (f.n[t] == 0) continue;
-            ok = mbar_wait(smem_u32(&bars.q_empty[t]), (q_uses[t] & 1) ^ 1, wd);
+            ok = wait(bars.q_empty[t], (q_uses[t] & 1) ^ 1);
             if (!ok) break;
-            const uint32_t bar = smem_u32(&bars.q_full[t]);
-            mbar_expect_tx(bar, C::kQKTileBytes);
+            if (elect_one()) {
+                const uint32_t bar = smem_u32(&bars.q_full[t]);
+                mbar_expect_tx(bar, C::kQKTileBytes);
 #pragma unroll
-            for (int g = 0; g < C::kQKBoxes; ++g)
-                tma_load_3d(sQ + t * C::kQKTileBytes + g * C::kBoxBytes, &a.tq, C::kQKBoxCols * g,
-                            f.q_start + f.row0 + BM * t, f.h, bar);
+                for (int g = 0; g < C::kQKBoxes; ++g)
+                    tma_load_3d(sQ + t * C::kQKTileBytes + g * C::kBoxBytes, &a.tq, C::kQKBoxCols * g,
+                                f.q_start + f.row0 + BM * t, f.h, bar);
+            }
+            __syncwarp();
             ++q_uses[t];
             q_pending[t] = true;
         }
@@ -240,7 +256,7 @@ __device__ void producer(const TcFwdArgs &a, FwdBars &bars, int *sched_item, uin
         for (int j = 0; j < f.nkv && ok; ++j) ok = load_kv(f.k_start + BN * (f.j0 + j), f.h);
         if (!ok) break;
     }
-    if (aborting(wd)) {
+    if (aborting(wd) && (threadIdx.x & 31) == 0) {
         // the newest load of every slot may still be landing in shared memory
         const long long budget = kDrainCycles;  // loads in flight land within microseconds
         for (uint32_t k = kr.i > (uint32_t)C::kKStages ? kr.i - C::kKStages : 0; k < kr.i; ++k)
@@ -617,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     if (warp < 4) {
         regs_dec<C::kRegsProducer>();
         if (warp == 0) {
-            if (lane == 0) producer<D, kF8>(a, bars, sched_item, sQ, sK, sV, wd);
+            producer<D, kF8>(a, bars, sched_item, sQ, sK, sV, wd);  // the whole warp
         } else if (warp == 1) {
             mma_issuer<D, kBF16, kF8, kPrune>(a, bars, sched_item, &prune_shared, sQ, sK, sV, tmem, wd);
             if (lane == 0 && aborting(wd)) {  // let issued MMAs finish before TMEM is freed

@@ -66,15 +66,48 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-suspending test of the phase (mbarrier.test_wait).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        " .reg .pred p;\n"
+        " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 struct Watchdog {
     long long budget;   // clock cycles per wait
     int *abort_flag;    // shared: set once any wait of the CTA gave up
     int *status;        // global device status word
 };
 
+// Budgets below this many cycles (failure-detection tests) are polled with
+// test_wait: try_wait may suspend the thread until the phase completes, up to a
+// hardware time limit, so a wait that ends within that limit would never see a
+// short budget run out.
+constexpr long long kPolledBudget = 1ll << 20;
+
 // Wait for the phase of parity `parity` to complete.  Returns false if the
 // CTA is aborting (this wait timed out, or another one did).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Watchdog &wd) {
+    if (wd.budget < kPolledBudget) {
+        const long long t0 = clock64();
+        for (;;) {
+            if (mbar_test_wait(bar, parity)) return true;
+            if (*reinterpret_cast<volatile int *>(wd.abort_flag)) return false;
+            if (clock64() - t0 > wd.budget) {
+                *reinterpret_cast<volatile int *>(wd.abort_flag) = 1;
+                report_status(wd.status, ATTN_ETIMEOUT);
+                return false;
+            }
+        }
+    }
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     for (;;) {
