@@ -122,7 +122,22 @@ __device__ __forceinline__ bool sched_take(SchedRing &r, int i, int &w, const Wa
     return true;
 }
 
-// warp-wide version for the elementwise warps (lane 0 arrives)
+// warp-wide versions: every lane waits (the same observations), one lane
+// fetches / arrives, every lane gets the item
+__device__ __forceinline__ bool sched_publish_warp(SchedRing &r, int i, int *counter, int &w, const Watchdog &wd) {
+    const int slot = i & 1;
+    const bool ok = mbar_wait(smem_u32(&r.empty[slot]), ((i >> 1) & 1) ^ 1, wd);
+    if (!__all_sync(0xffffffffu, ok)) return false;
+    int v = 0;
+    if (elect_one()) {
+        v = atomicAdd(counter, 1);
+        r.item[slot] = v;
+        mbar_arrive(smem_u32(&r.full[slot]));
+    }
+    w = __shfl_sync(0xffffffffu, v, 0);
+    return true;
+}
+
 __device__ __forceinline__ bool sched_take_warp(SchedRing &r, int i, int &w, const Watchdog &wd) {
     const int slot = i & 1;
     const bool ok = mbar_wait(smem_u32(&r.full[slot]), (i >> 1) & 1, wd);
@@ -168,8 +183,9 @@ struct __align__(8) DkdvBars {
     SchedRing sched;
 };
 
-// Two producer warps: warp 0 publishes the work items and loads K, V and the Q
-// ring; warp 2 loads the dO ring.  Splitting them keeps a dO load from waiting
+// Two producer warps, each run by all its 32 lanes in step (uniform waits, one
+// elected lane issues the loads): warp 0 publishes the work items and loads K,
+// V and the Q ring; warp 2 loads the dO ring.  Splitting them keeps a dO load from waiting
 // behind a Q slot (Q tiles are released only after dK, dO tiles after dV).
 template <int D>
 __device__ void dkdv_producer(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, uint32_t sV, uint32_t sQ,
@@ -182,22 +198,28 @@ __device__ void dkdv_producer(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, u
     RingPos<C::kDkdvDoStages> dr;
     bool kv_pending = false;
     // load the Q or dO tile of query block `row` into its ring
+    auto wait = [&](uint64_t &bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar), parity, wd));
+    };
     auto load_row = [&](uint64_t *full, uint64_t *empty, uint32_t slot, uint32_t phase, uint32_t base,
                         const CUtensorMap *tm, int row, int h) -> bool {
-        if (!mbar_wait(smem_u32(&empty[slot]), phase ^ 1, wd)) return false;
-        const uint32_t bar = smem_u32(&full[slot]);
-        mbar_expect_tx(bar, C::kTileBytes);
+        if (!wait(empty[slot], phase ^ 1)) return false;
+        if (elect_one()) {
+            const uint32_t bar = smem_u32(&full[slot]);
+            mbar_expect_tx(bar, C::kTileBytes);
 #pragma unroll
-        for (int g = 0; g < C::kBoxes; ++g)
-            tma_load_3d(base + slot * C::kTileBytes + g * C::kBoxBytes, tm, 64 * g, row, h, bar);
+            for (int g = 0; g < C::kBoxes; ++g)
+                tma_load_3d(base + slot * C::kTileBytes + g * C::kBoxBytes, tm, 64 * g, row, h, bar);
+        }
+        __syncwarp();
         return true;
     };
     for (int i = 0;; ++i) {
         int w;
         if (dout_role) {
-            if (!sched_take(bars.sched, i, w, wd)) break;
+            if (!sched_take_warp(bars.sched, i, w, wd)) break;
         } else {
-            if (!sched_publish(bars.sched, i, p.sched_kv.hdr, w, wd)) break;
+            if (!sched_publish_warp(bars.sched, i, p.sched_kv.hdr, w, wd)) break;
         }
         if (w >= total) break;
         const DkdvInfo f = dkdv_info(p, w);
@@ -213,8 +235,8 @@ __device__ void dkdv_producer(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, u
             if (!ok) break;
             continue;
         }
-        if (!mbar_wait(smem_u32(&bars.kv_empty), (kv_uses & 1) ^ 1, wd)) break;
-        {
+        if (!wait(bars.kv_empty, (kv_uses & 1) ^ 1)) break;
+        if (elect_one()) {
             const uint32_t bar = smem_u32(&bars.kv_full);
             mbar_expect_tx(bar, 2 * C::kTileBytes);
 #pragma unroll
@@ -222,9 +244,10 @@ __device__ void dkdv_producer(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, u
                 tma_load_3d(sK + g * C::kBoxBytes, &a.tk, 64 * g, f.k_start + f.key0, f.h, bar);
                 tma_load_3d(sV + g * C::kBoxBytes, &a.tv, 64 * g, f.k_start + f.key0, f.h, bar);
             }
-            ++kv_uses;
-            kv_pending = true;
         }
+        __syncwarp();
+        ++kv_uses;
+        kv_pending = true;
         for (int qb = 0; qb < f.nq; ++qb) {
             ok = load_row(bars.q_full, bars.q_empty, qr.slot(), qr.phase(), sQ, &a.tq,
                           f.q_start + BT * (f.qb0 + qb), f.h);
@@ -233,7 +256,7 @@ __device__ void dkdv_producer(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, u
         }
         if (!ok) break;
     }
-    if (aborting(wd)) {
+    if (aborting(wd) && (threadIdx.x & 31) == 0) {
         const long long budget = kDrainCycles;  // loads in flight land within microseconds
         for (uint32_t k = qr.i > (uint32_t)C::kDkdvQStages ? qr.i - C::kDkdvQStages : 0; k < qr.i; ++k)
             drain_wait(smem_u32(&bars.q_full[k % C::kDkdvQStages]), (k / C::kDkdvQStages) & 1, budget);
@@ -850,7 +873,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_tc_kernel(const __grid_const
     pdl_wait();
     if (warp < 4) {
         regs_dec<kFused ? C::kRegsProducerFused : C::kRegsProducer>();
-        if ((warp == 0 || warp == 2) && lane == 0) dkdv_producer<D>(a, bars, sK, sV, sQ, sDO, warp == 2, wd);
+        if (warp == 0 || warp == 2) dkdv_producer<D>(a, bars, sK, sV, sQ, sDO, warp == 2, wd);  // whole warps
         else if (warp == 1) {
             // the separate issuer runs on the whole warp, the fused one on lane 0
             if constexpr (kFused) {
@@ -979,7 +1002,6 @@ __device__ void dq_mma(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint32_t s
 
     const uint64_t kmaj = sdesc_sw128(0, 16, 1024);
     const uint64_t nmaj = sdesc_sw128(0, C::kBoxBytes, 1024);
-    // (called by the elected lane)
     auto issue_ss = [&](uint32_t col, uint32_t A, uint32_t B, uint32_t id) {
         const uint64_t ad = kmaj + sdesc_step(A), bd = kmaj + sdesc_step(B);
 #pragma unroll
@@ -988,74 +1010,63 @@ __device__ void dq_mma(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint32_t s
             mma_ss(tmem + col, ad + off, bd + off, id, kk > 0);
         }
     };
-    auto wait = [&](uint64_t &bar, uint32_t parity) -> bool {
-        return __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar), parity, wd));
-    };
     // wait for the next K and V tiles (one barrier for both); returns their slots
     auto take_kv = [&](uint32_t &ks, uint32_t &vs) -> bool {
         ks = kr.slot();
         vs = vr.slot();
-        if (!wait(bars.k_full[ks], kr.phase())) return false;
+        if (!mbar_wait(smem_u32(&bars.k_full[ks]), kr.phase(), wd)) return false;
         ++kr.i;
         ++vr.i;
         return true;
     };
-    // S = Q K^T and dP = dO V^T of one key block, then their commits
-    auto issue_s_dp = [&](uint32_t ks, uint32_t vs) {
-        if (elect_one()) {
-            issue_ss(0, sQ, sK + ks * C::kTileBytes, idS);
-            issue_ss(BT, sDO, sV + vs * C::kTileBytes, idSS);
-            tc_commit(smem_u32(&bars.sp_full));
-            tc_commit(smem_u32(&bars.v_empty[vs]));
-        }
-        __syncwarp();
-    };
 
     for (int i = 0;; ++i) {
         int w;
-        if (!sched_take_warp(bars.sched, i, w, wd)) return;
+        if (!sched_take(bars.sched, i, w, wd)) return;
         if (w >= total) return;
         const DqInfo f = dq_info(p, w);
         if (f.nk == 0) continue;
-        if (!wait(bars.q_full, q_cnt & 1)) return;
+        if (!mbar_wait(smem_u32(&bars.q_full), q_cnt & 1, wd)) return;
         ++q_cnt;
         uint32_t ks, vs;
         if (!take_kv(ks, vs)) return;
         tc_fence_after();
-        issue_s_dp(ks, vs);
+        issue_ss(0, sQ, sK + ks * C::kTileBytes, idS);     // S = Q K^T
+        issue_ss(BT, sDO, sV + vs * C::kTileBytes, idSS);  // dP = dO V^T
+        tc_commit(smem_u32(&bars.sp_full));
+        tc_commit(smem_u32(&bars.v_empty[vs]));
         for (int j = 0; j < f.nk; ++j) {
-            if (!wait(bars.sp_free, spf_cnt & 1)) return;
+            if (!mbar_wait(smem_u32(&bars.sp_free), spf_cnt & 1, wd)) return;
             ++spf_cnt;
             uint32_t ksn = 0;
             if (j + 1 < f.nk) {
                 uint32_t vsn;
                 if (!take_kv(ksn, vsn)) return;
                 tc_fence_after();
-                issue_s_dp(ksn, vsn);
+                issue_ss(0, sQ, sK + ksn * C::kTileBytes, idS);
+                issue_ss(BT, sDO, sV + vsn * C::kTileBytes, idSS);
+                tc_commit(smem_u32(&bars.sp_full));
+                tc_commit(smem_u32(&bars.v_empty[vsn]));
             }
-            if (!wait(bars.ds_ready[ds_cnt & 1], (ds_cnt >> 1) & 1)) return;
+            if (!mbar_wait(smem_u32(&bars.ds_ready[ds_cnt & 1]), (ds_cnt >> 1) & 1, wd)) return;
             ++ds_cnt;
             if (j == 0) {
-                if (!wait(bars.acc_free, (af_cnt & 1) ^ 1)) return;
+                if (!mbar_wait(smem_u32(&bars.acc_free), (af_cnt & 1) ^ 1, wd)) return;
                 ++af_cnt;
             }
             tc_fence_after();
-            if (elect_one()) {
+            {
                 const uint64_t kd = nmaj + sdesc_step(sK + ks * C::kTileBytes);
                 const uint32_t ds_col = tmem + 256 + 64 * (j & 1);
 #pragma unroll
                 for (int kk = 0; kk < BT / 16; ++kk)  // dQ += dS K
                     mma_ts(tmem + 384, ds_col + 8 * kk, kd + sdesc_step(kk * 2048), idTS, j > 0 || kk > 0);
-                tc_commit(smem_u32(&bars.k_empty[ks]));
             }
-            __syncwarp();
+            tc_commit(smem_u32(&bars.k_empty[ks]));
             ks = ksn;
         }
-        if (elect_one()) {
-            tc_commit(smem_u32(&bars.acc_done));
-            tc_commit(smem_u32(&bars.q_empty));
-        }
-        __syncwarp();
+        tc_commit(smem_u32(&bars.acc_done));
+        tc_commit(smem_u32(&bars.q_empty));
     }
 }
 
@@ -1214,7 +1225,9 @@ __global__ void __launch_bounds__(kThreads, 1) dq_tc_kernel(const __grid_constan
         regs_dec<C::kRegsProducer>();
         if (warp == 0 && lane == 0) dq_producer<D>(a, bars, sQ, sDO, sK, sV, wd);
         else if (warp == 1) {
-            dq_mma<D, kBF16>(a, bars, sQ, sDO, sK, sV, tmem, wd);  // the whole warp
+            // one lane: the converged form (as in the dK/dV issuer) measured
+            // +-3 % on the dq stage depending on the GPU, no clear gain
+            if (lane == 0) dq_mma<D, kBF16>(a, bars, sQ, sDO, sK, sV, tmem, wd);
             if (lane == 0 && aborting(wd)) {  // let issued MMAs finish before TMEM is freed
                 tc_commit(smem_u32(&bars.mma_drain));
                 drain_wait(smem_u32(&bars.mma_drain), 0, kDrainCycles);
