@@ -967,18 +967,25 @@ def main():
                        (("o", fcall.o), ("dq", bcall.dq), ("dk", bcall.dk), ("dv", bcall.dv)))
             if not (same and torch.equal(outs_host["lse"], lse_b)):
                 raise RuntimeError("end-to-end leg: per-sequence results differ from the batched call")
-    e_steps = max(2, args.steps)  # the same K steps as the device-timed leg
-    barrier()
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(s_in)  # before the first copy in
-    for _ in range(e_steps):
-        e2e_step()
-    t1.record(s_out)  # after the last copy out
-    torch.cuda.synchronize()
-    barrier()
-    e2e_ms = max_over_ranks(t0.elapsed_time(t1) / e_steps, dev)
+    # The same K steps as the device-timed leg, timed three times; the line
+    # reports the median repetition (every repetition is listed beside it).  The
+    # host link is shared with the machine's other GPUs, and one repetition can
+    # catch a burst of someone else's traffic.
+    e_steps = max(2, args.steps)
+    e2e_reps = []
+    for _ in range(3 if not args.skip_e2e else 1):
+        barrier()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(s_in)  # before the first copy in
+        for _ in range(e_steps):
+            e2e_step()
+        t1.record(s_out)  # after the last copy out
+        torch.cuda.synchronize()
+        barrier()
+        e2e_reps.append(max_over_ranks(t0.elapsed_time(t1) / e_steps, dev))
+    e2e_ms = statistics.median(e2e_reps)
     status = attn.device_status()
     if status != 0:
         raise RuntimeError(f"device status {status} ({attn.strerror(status)}) set in the end-to-end leg")
@@ -1056,6 +1063,7 @@ def main():
         "roofline": roofline,
         "e2e": {"value": job_rate(step_flops, world, e2e_ms) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "ms_per_step_repetitions": e2e_reps, "steps_per_repetition": e_steps,
                 "how": "per sequence: pinned host -> device copies, forward + backward, device -> "
                        "pinned host copies of o, lse, dq, dk, dv; copies on their own streams, "
                        "sequences alternating between two compute streams, so that copies and "
