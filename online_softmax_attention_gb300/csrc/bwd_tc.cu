@@ -20,13 +20,15 @@
 // of one block with the contractions of the next.
 //
 // dq kernel -- work item = 128 query rows; loop over key blocks:
-//   S = Q K^T, dP = dO V^T into TMEM; the elementwise warps read both into
-//   registers at once (freeing the buffers for the next block's MMAs), form
+//   S = Q K^T, dP = dO V^T into TMEM, each with its own commit; the
+//   elementwise warps read S into registers (freeing its buffer for the next
+//   block's S), exponentiate it, then read dP (freeing that buffer), form
 //   dS = P (dP - Dr) and write it, 16-bit, into one of two TMEM buffers;
-//   dQ += dS K (TMEM x smem, K N-major).
+//   dQ += dS K (TMEM x smem, K N-major).  Issue order S_{j+1}, dP_{j+1}, dQ_j.
 //
-// Warp roles (12 warps): 0 TMA producer, 1 MMA issuer (one thread), 4-11 two
-// elementwise warpgroups that split each row's 128 columns in halves.  lse2 =
+// Warp roles (12 warps): 0 TMA producer, 1 MMA issuer (the whole warp runs
+// the loop, one elected lane issues), 4-11 two elementwise warpgroups that
+// split each row's 128 columns in halves.  lse2 =
 // lse * log2(e) and Dr come from the preprocess kernel.  All waits bounded.
 #include "sm100.cuh"
 #include "tc.h"
@@ -919,9 +921,12 @@ __device__ __forceinline__ DqInfo dq_info(const BwdParams &p, int w) {
 struct __align__(8) DqBars {
     uint64_t q_full, q_empty;
     uint64_t k_full[8], k_empty[8], v_empty[8];  // k_full: the K and V tiles of a key block
-    uint64_t sp_full, sp_free, acc_done, acc_free;
+    // S and dP of a key block are committed, and read out of TMEM, separately:
+    // the next block's S starts once every warp has read this block's S, while
+    // they still wait for (or read) its dP
+    uint64_t s_full, s_free, dp_full, dp_free, acc_done, acc_free;
     // dS of a key block is in TMEM, alternating by block: the next S / dP pair
-    // waits only for every warp's read of this one (sp_free), so a fast warp can
+    // waits only for every warp's read of this one (s_free, dp_free), so a fast warp can
     // finish the next block's dS before a slow one has finished this block's; with
     // one barrier its early arrival would complete the wrong phase
     uint64_t ds_ready[2];
@@ -990,83 +995,144 @@ template <int D, bool kBF16>
 __device__ void dq_mma(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint32_t sDO, uint32_t sK, uint32_t sV,
                        uint32_t tmem, const Watchdog &wd) {
     using C = BCfg<D>;
+    constexpr uint32_t KS = C::kDqKStages, VS = C::kDqVStages;
     const BwdParams &p = a.p;
     const int total = p.sched_q.hdr[1];
     constexpr uint32_t idSS = idesc_f16(kBF16, BT, BT, 0);
     // S with a negative scale: negate Q (the A operand) so P uses |scale|
     const uint32_t idS = idSS | (p.scale_log2 < 0.f ? (1u << 13) : 0u);
     constexpr uint32_t idTS = idesc_f16(kBF16, BT, D, 1);
-    uint32_t q_cnt = 0, spf_cnt = 0, ds_cnt = 0, af_cnt = 0;
-    RingPos<C::kDqKStages> kr;
-    RingPos<C::kDqVStages> vr;
+    uint32_t q_cnt = 0, sf_cnt = 0, df_cnt = 0, ds_cnt = 0, af_cnt = 0;
+    uint32_t g0 = 0;  // key blocks (K and V tiles) taken before this item; block g uses slots g % KS, g % VS
 
     const uint64_t kmaj = sdesc_sw128(0, 16, 1024);
     const uint64_t nmaj = sdesc_sw128(0, C::kBoxBytes, 1024);
-    auto issue_ss = [&](uint32_t col, uint32_t A, uint32_t B, uint32_t id) {
-        const uint64_t ad = kmaj + sdesc_step(A), bd = kmaj + sdesc_step(B);
+    const uint64_t dq_desc = kmaj + sdesc_step(sQ), ddo_desc = kmaj + sdesc_step(sDO);
+    // one smem x smem contraction over D (the elected lane)
+    auto issue_ss = [&](uint32_t col, uint64_t ad, uint32_t B, uint32_t id) {
+        const uint64_t bd = kmaj + sdesc_step(B);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t off = sdesc_step((kk >> 2) * C::kBoxBytes + (kk & 3) * 32);
-            mma_ss(tmem + col, ad + off, bd + off, id, kk > 0);
+            const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+            mma_ss(tmem + col, sdesc_add(ad, off), sdesc_add(bd, off), id, kk > 0);
         }
     };
-    // wait for the next K and V tiles (one barrier for both); returns their slots
-    auto take_kv = [&](uint32_t &ks, uint32_t &vs) -> bool {
-        ks = kr.slot();
-        vs = vr.slot();
-        if (!mbar_wait(smem_u32(&bars.k_full[ks]), kr.phase(), wd)) return false;
-        ++kr.i;
-        ++vr.i;
-        return true;
+    // S = Q K^T and dP = dO V^T of global key block g, each with its commit
+    auto issue_s = [&](uint32_t g) {
+        if (elect_one()) {
+            issue_ss(0, dq_desc, sK + (g % KS) * C::kTileBytes, idS);
+            tc_commit(smem_u32(&bars.s_full));
+        }
+        __syncwarp();
+    };
+    auto issue_dp = [&](uint32_t g) {
+        if (elect_one()) {
+            issue_ss(BT, ddo_desc, sV + (g % VS) * C::kTileBytes, idSS);
+            tc_commit(smem_u32(&bars.dp_full));
+            tc_commit(smem_u32(&bars.v_empty[g % VS]));
+        }
+        __syncwarp();
+    };
+    // the whole warp waits (or polls: mbarrier.test_wait, no suspension); a
+    // barrier's phase that a poll saw complete stays complete until the issuer
+    // itself lets the next phase start, so a successful poll replaces the wait
+    auto wait = [&](uint64_t &bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar), parity, wd));
+    };
+    auto poll = [&](uint64_t &bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, mbar_test_wait(smem_u32(&bar), parity));
     };
 
     for (int i = 0;; ++i) {
         int w;
-        if (!sched_take(bars.sched, i, w, wd)) return;
+        if (!sched_take_warp(bars.sched, i, w, wd)) return;
         if (w >= total) return;
         const DqInfo f = dq_info(p, w);
         if (f.nk == 0) continue;
-        if (!mbar_wait(smem_u32(&bars.q_full), q_cnt & 1, wd)) return;
+        if (!wait(bars.q_full, q_cnt & 1)) return;
         ++q_cnt;
-        uint32_t ks, vs;
-        if (!take_kv(ks, vs)) return;
+        if (!wait(bars.k_full[g0 % KS], (g0 / KS) & 1)) return;
         tc_fence_after();
-        issue_ss(0, sQ, sK + ks * C::kTileBytes, idS);     // S = Q K^T
-        issue_ss(BT, sDO, sV + vs * C::kTileBytes, idSS);  // dP = dO V^T
-        tc_commit(smem_u32(&bars.sp_full));
-        tc_commit(smem_u32(&bars.v_empty[vs]));
+        issue_s(g0);
+        issue_dp(g0);
+        // Issue order S_{j+1}, dP_{j+1}, dQ_j.  Every warp has read S_{j+1}
+        // (and usually dP_{j+1} too) well before dQ_j is issued, so the elected
+        // lane tests those barriers between dQ_j's MMAs and, when they hold,
+        // issues S_{j+2} and dP_{j+2} in the same straight run: the tensor pipe
+        // then meets one issuer turnaround per block instead of three.  When a
+        // test fails, the warp waits at the top of the next iteration.
+        bool pre_s = false, pre_dp = false;  // S_{j+1} / dP_{j+1} already issued
         for (int j = 0; j < f.nk; ++j) {
-            if (!mbar_wait(smem_u32(&bars.sp_free), spf_cnt & 1, wd)) return;
-            ++spf_cnt;
-            uint32_t ksn = 0;
-            if (j + 1 < f.nk) {
-                uint32_t vsn;
-                if (!take_kv(ksn, vsn)) return;
-                tc_fence_after();
-                issue_ss(0, sQ, sK + ksn * C::kTileBytes, idS);
-                issue_ss(BT, sDO, sV + vsn * C::kTileBytes, idSS);
-                tc_commit(smem_u32(&bars.sp_full));
-                tc_commit(smem_u32(&bars.v_empty[vsn]));
+            const uint32_t g = g0 + j;
+            const bool more = j + 1 < f.nk;
+            if (!pre_s) {
+                if (!wait(bars.s_free, sf_cnt & 1)) return;  // every warp has read S_j
+                ++sf_cnt;
+                if (more) {
+                    if (!wait(bars.k_full[(g + 1) % KS], ((g + 1) / KS) & 1)) return;
+                    tc_fence_after();
+                    issue_s(g + 1);
+                }
             }
-            if (!mbar_wait(smem_u32(&bars.ds_ready[ds_cnt & 1]), (ds_cnt >> 1) & 1, wd)) return;
+            if (!pre_dp) {
+                if (!poll(bars.dp_free, df_cnt & 1) && !wait(bars.dp_free, df_cnt & 1)) return;  // dP_j read
+                ++df_cnt;
+                if (more) {
+                    tc_fence_after();
+                    issue_dp(g + 1);
+                }
+            }
+            if (!poll(bars.ds_ready[ds_cnt & 1], (ds_cnt >> 1) & 1) &&
+                !wait(bars.ds_ready[ds_cnt & 1], (ds_cnt >> 1) & 1))
+                return;
             ++ds_cnt;
             if (j == 0) {
-                if (!mbar_wait(smem_u32(&bars.acc_free), (af_cnt & 1) ^ 1, wd)) return;
+                if (!wait(bars.acc_free, (af_cnt & 1) ^ 1)) return;
                 ++af_cnt;
             }
+            const bool ahead = j + 2 < f.nk;
+            const uint32_t gn = g + 2;
+            uint32_t issued = 0;  // 1: S_{j+2}; 3: S_{j+2} and dP_{j+2}
             tc_fence_after();
-            {
-                const uint64_t kd = nmaj + sdesc_step(sK + ks * C::kTileBytes);
+            if (elect_one()) {
+                const uint64_t kd = nmaj + sdesc_step(sK + (g % KS) * C::kTileBytes);
                 const uint32_t ds_col = tmem + 256 + 64 * (j & 1);
+                // dQ += dS K: five MMAs, the tests for block j + 2, three more
 #pragma unroll
-                for (int kk = 0; kk < BT / 16; ++kk)  // dQ += dS K
-                    mma_ts(tmem + 384, ds_col + 8 * kk, kd + sdesc_step(kk * 2048), idTS, j > 0 || kk > 0);
+                for (int kk = 0; kk < 5; ++kk)
+                    mma_ts(tmem + 384, ds_col + 8 * kk, sdesc_add(kd, kk * 2048), idTS, j > 0 || kk > 0);
+                const bool go_s = ahead && mbar_test_wait(smem_u32(&bars.s_free), sf_cnt & 1) &&
+                                  mbar_test_wait(smem_u32(&bars.k_full[gn % KS]), (gn / KS) & 1);
+#pragma unroll
+                for (int kk = 5; kk < BT / 16; ++kk)
+                    mma_ts(tmem + 384, ds_col + 8 * kk, sdesc_add(kd, kk * 2048), idTS, 1);
+                tc_commit(smem_u32(&bars.k_empty[g % KS]));
+                if (go_s) {
+                    tc_fence_after();
+                    issue_ss(0, dq_desc, sK + (gn % KS) * C::kTileBytes, idS);
+                    tc_commit(smem_u32(&bars.s_full));
+                    issued = 1;
+                    if (mbar_test_wait(smem_u32(&bars.dp_free), df_cnt & 1)) {
+                        tc_fence_after();
+                        issue_ss(BT, ddo_desc, sV + (gn % VS) * C::kTileBytes, idSS);
+                        tc_commit(smem_u32(&bars.dp_full));
+                        tc_commit(smem_u32(&bars.v_empty[gn % VS]));
+                        issued = 3;
+                    }
+                }
             }
-            tc_commit(smem_u32(&bars.k_empty[ks]));
-            ks = ksn;
+            issued = __reduce_or_sync(0xffffffffu, issued);
+            pre_s = issued & 1;
+            pre_dp = issued & 2;
+            sf_cnt += pre_s;
+            df_cnt += pre_dp;
         }
-        tc_commit(smem_u32(&bars.acc_done));
-        tc_commit(smem_u32(&bars.q_empty));
+        g0 += f.nk;
+        if (elect_one()) {
+            tc_commit(smem_u32(&bars.acc_done));
+            tc_commit(smem_u32(&bars.q_empty));
+        }
+        __syncwarp();
     }
 }
 
@@ -1080,7 +1146,7 @@ __device__ void dq_elementwise(const TcBwdArgs &a, DqBars &bars, uint32_t tmem, 
     const int rl = 32 * quarter + lane;
     const uint32_t lane_base = tmem_addr(tmem, 32 * quarter, 0);
     const float sl2 = fabsf(p.scale_log2);  // the score MMA negated S for a negative scale
-    uint32_t sp_cnt = 0, ad_cnt = 0, step = 0;
+    uint32_t s_cnt = 0, dp_cnt = 0, ad_cnt = 0, step = 0;
 
     for (int i = 0;; ++i) {
         int w;
@@ -1099,39 +1165,54 @@ __device__ void dq_elementwise(const TcBwdArgs &a, DqBars &bars, uint32_t tmem, 
             continue;
         }
         for (int j = 0; j < f.nk; ++j, ++step) {
-            bool ok = mbar_wait(smem_u32(&bars.sp_full), sp_cnt & 1, wd);
-            ++sp_cnt;
+            bool ok = mbar_wait(smem_u32(&bars.s_full), s_cnt & 1, wd);
+            ++s_cnt;
             if (!__all_sync(0xffffffffu, ok)) return;
             tc_fence_after();
             uint32_t rs[2][32], rp[2][32];
             tmem_ld_x32(lane_base + 64 * wg, rs[0]);
             tmem_ld_x32(lane_base + 64 * wg + 32, rs[1]);
-            tmem_ld_x32(lane_base + BT + 64 * wg, rp[0]);
-            tmem_ld_x32(lane_base + BT + 64 * wg + 32, rp[1]);
             tmem_ld_wait(rs[0]);
             tmem_ld_wait(rs[1]);
+            tc_fence_before();
+            mbar_arrive_warp(smem_u32(&bars.s_free));  // the S buffer may be overwritten
+
+            // P = 2^(S scale log2e - lse2), in place of S, while dP may still be in flight
+            const float2 sc2 = make_float2(sl2, sl2), nl2 = make_float2(-lse2, -lse2);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                uint32_t &s0 = rs[(2 * c) >> 5][(2 * c) & 31], &s1 = rs[(2 * c + 1) >> 5][(2 * c + 1) & 31];
+                const float2 x = __ffma2_rn(make_float2(__uint_as_float(s0), __uint_as_float(s1)), sc2, nl2);
+                // one pair in kDqExpFmaEvery on the FMA pipe, the rest on the SFU
+                const float2 pv = (c % kDqExpFmaEvery) == 0 ? exp2_fma2(x)
+                                                            : make_float2(exp2_approx(x.x), exp2_approx(x.y));
+                s0 = __float_as_uint(pv.x);
+                s1 = __float_as_uint(pv.y);
+            }
+
+            ok = mbar_wait(smem_u32(&bars.dp_full), dp_cnt & 1, wd);
+            ++dp_cnt;
+            if (!__all_sync(0xffffffffu, ok)) return;
+            tc_fence_after();
+            tmem_ld_x32(lane_base + BT + 64 * wg, rp[0]);
+            tmem_ld_x32(lane_base + BT + 64 * wg + 32, rp[1]);
             tmem_ld_wait(rp[0]);
             tmem_ld_wait(rp[1]);
             tc_fence_before();
-            mbar_arrive_warp(smem_u32(&bars.sp_free));  // S and dP buffers may be overwritten
+            mbar_arrive_warp(smem_u32(&bars.dp_free));  // the dP buffer may be overwritten
 
             const int key0 = BT * j;
             int lim = BT;  // keys [0, lim) of the tile are admitted for this row
             if ((p.causal && key0 + BT - 1 > f.row0) || key0 + BT > f.Lk)
                 lim = min(f.Lk - key0, p.causal ? row - key0 + 1 : BT);
             const int c0 = 64 * wg;
-            const float2 sc2 = make_float2(sl2, sl2), nl2 = make_float2(-lse2, -lse2);
             const float2 ndr2 = make_float2(-drr, -drr);
             const bool masked = lim < BT;
             uint32_t pk[32];
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
-                const float2 sv = make_float2(__uint_as_float(rs[(2 * c) >> 5][(2 * c) & 31]),
+                const float2 pv = make_float2(__uint_as_float(rs[(2 * c) >> 5][(2 * c) & 31]),
                                               __uint_as_float(rs[(2 * c + 1) >> 5][(2 * c + 1) & 31]));
-                const float2 x = __ffma2_rn(sv, sc2, nl2);
-                // one pair in kDqExpFmaEvery on the FMA pipe, the rest on the SFU
-                const float2 pv = (c % kDqExpFmaEvery) == 0 ? exp2_fma2(x)
-                                                            : make_float2(exp2_approx(x.x), exp2_approx(x.y));
                 const float2 dp = make_float2(__uint_as_float(rp[(2 * c) >> 5][(2 * c) & 31]),
                                               __uint_as_float(rp[(2 * c + 1) >> 5][(2 * c + 1) & 31]));
                 const float2 d = __fmul2_rn(pv, __fadd2_rn(dp, ndr2));
@@ -1194,9 +1275,11 @@ __global__ void __launch_bounds__(kThreads, 1) dq_tc_kernel(const __grid_constan
             mbar_init(smem_u32(&bars.k_empty[s]), 1);
         }
         for (int s = 0; s < C::kDqVStages; ++s) mbar_init(smem_u32(&bars.v_empty[s]), 1);
-        mbar_init(smem_u32(&bars.sp_full), 1);
+        mbar_init(smem_u32(&bars.s_full), 1);
+        mbar_init(smem_u32(&bars.dp_full), 1);
         mbar_init(smem_u32(&bars.mma_drain), 1);
-        mbar_init(smem_u32(&bars.sp_free), kEw / 32);
+        mbar_init(smem_u32(&bars.s_free), kEw / 32);
+        mbar_init(smem_u32(&bars.dp_free), kEw / 32);
         mbar_init(smem_u32(&bars.ds_ready[0]), kEw / 32);
         mbar_init(smem_u32(&bars.ds_ready[1]), kEw / 32);
         mbar_init(smem_u32(&bars.acc_done), 1);
@@ -1225,9 +1308,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_tc_kernel(const __grid_constan
         regs_dec<C::kRegsProducer>();
         if (warp == 0 && lane == 0) dq_producer<D>(a, bars, sQ, sDO, sK, sV, wd);
         else if (warp == 1) {
-            // one lane: the converged form (as in the dK/dV issuer) measured
-            // +-3 % on the dq stage depending on the GPU, no clear gain
-            if (lane == 0) dq_mma<D, kBF16>(a, bars, sQ, sDO, sK, sV, tmem, wd);
+            dq_mma<D, kBF16>(a, bars, sQ, sDO, sK, sV, tmem, wd);  // the whole warp
             if (lane == 0 && aborting(wd)) {  // let issued MMAs finish before TMEM is freed
                 tc_commit(smem_u32(&bars.mma_drain));
                 drain_wait(smem_u32(&bars.mma_drain), 0, kDrainCycles);

@@ -337,6 +337,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
 // 256 KiB shared window) only adds to its start-address field.
 __host__ __device__ constexpr uint64_t sdesc_step(uint32_t bytes) { return static_cast<uint64_t>(bytes >> 4); }
 
+// The same advance as a 32-bit add on the descriptor's low word (the
+// start-address field cannot carry out of it inside the 256 KiB window).
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t d, uint32_t bytes) {
+    const uint32_t lo = static_cast<uint32_t>(d) + (bytes >> 4);
+    return (d & 0xFFFFFFFF00000000ull) | lo;
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16 with an f32 accumulator.
 // is_bf16: A and B are bf16 (else f16); b_mn_major: B is N-contiguous.
 __host__ __device__ constexpr uint32_t idesc_f16(int is_bf16, int M, int N, int b_mn_major) {

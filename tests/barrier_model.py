@@ -12,7 +12,12 @@ with random per-role speeds (so one warp can fall far behind the others).
 Checked per run: every completed phase of a tagged barrier collected arrivals
 that all carry the same tag (a fast warp's arrival for the next block must not
 complete the phase of this one), and the run ends with every role finished
-(no deadlock).
+(no deadlock).  Where a protocol names the tensor-memory buffers its MMAs and
+warps use, the model also tracks which block each buffer holds: an MMA writes
+its result when it retires and checks the operands it reads then, a warp checks
+the buffer it reads (or sets the one it writes) at that step, so a buffer
+overwritten before every reader is done, or read before it is written, is
+reported.
 """
 from __future__ import annotations
 
@@ -55,23 +60,37 @@ class Barrier:
 
 
 class TensorCore:
-    """In-order queue of ("mma", None) and ("commit", barrier, tag) items."""
+    """In-order queue of ("mma", reads, writes) and ("commit", barrier, tag)
+    items; `mem` maps a tensor-memory buffer to the block it holds."""
 
     def __init__(self):
         self.queue = []
+        self.mem = {}
+
+    def check(self, who, buf, tag, violations):
+        if self.mem.get(buf) != tag:
+            violations.append(f"{who} read {buf} holding {self.mem.get(buf)}, expected {tag}")
 
     def retire_one(self, violations):
-        kind, bar, tag = self.queue.pop(0)
+        kind, x, y = self.queue.pop(0)
         if kind == "commit":
-            bar.arrive(tag, violations)
+            x.arrive(y, violations)
+            return
+        for buf, tag in x or ():
+            self.check("mma", buf, tag, violations)
+        for buf, tag in y or ():
+            self.mem[buf] = tag
 
 
 def run(roles, tc, rng, max_steps=200000):
     """Interleave the role generators randomly.  Each role yields
     ("wait", bar, parity), ("arrive", bar, tag), ("arrive_tx", bar, tag, loads)
     (arrive with expect-tx for `loads` one-unit TMA loads, which then land in
-    any order), ("mma",), ("commit", bar, tag) or ("work",) (local
-    computation, no synchronisation).  Returns (violations, deadlocked)."""
+    any order), ("mma",) or ("mma", reads, writes) (lists of (buffer, tag)),
+    ("commit", bar, tag), ("read", buffer, tag), ("write", buffer, tag),
+    ("poll", bar, parity) (mbarrier.test_wait: never blocks; the generator
+    receives whether the phase has completed) or ("work",) (local computation,
+    no synchronisation).  Returns (violations, deadlocked)."""
     violations = []
     tma = []  # barriers with one load in flight each
     speed = {name: rng.choice([0.05, 0.3, 1.0, 1.0, 1.0]) for name in roles}
@@ -100,9 +119,19 @@ def run(roles, tc, rng, max_steps=200000):
             op[1].arrive(op[2], violations, expect_tx=op[3])
             tma.extend([op[1]] * op[3])
         elif op[0] == "mma":
-            tc.queue.append(("mma", None, None))
+            tc.queue.append(("mma", op[1], op[2]) if len(op) > 1 else ("mma", None, None))
+        elif op[0] == "read":
+            tc.check(who, op[1], op[2], violations)
+        elif op[0] == "write":
+            tc.mem[op[1]] = op[2]
         elif op[0] == "commit":
             tc.queue.append(("commit", op[1], op[2]))
+        elif op[0] == "poll":
+            try:
+                pending[who] = roles[who].send(op[1].done(op[2]))
+            except StopIteration:
+                pending[who] = None
+            continue
         pending[who] = next(roles[who], None)
     return violations + ["step limit"], True
 
@@ -112,63 +141,140 @@ def run(roles, tc, rng, max_steps=200000):
 # tensor-memory loads / stores.  Tags: the global block (or item) index the
 # arrival belongs to.
 
-def dq_protocol(items, rng, n_warps=8, split_ds=True):
-    """dq kernel: per key block S and dP into TMEM (commit sp_full), the
-    elementwise warps read them (sp_free), form dS (ds_ready), the issuer
-    issues the next block's S / dP after sp_free and dQ after ds_ready.
-    split_ds: dS-ready alternates between two barriers by block (the fix);
-    False models the earlier single barrier."""
+def _dq_issue_s(g, bars):
+    yield ("mma", [], [("S", g)])
+    yield ("commit", bars["s_full"], g)
+
+
+def _dq_issue_dp(g, bars, vstages):
+    yield ("mma", [], [("dP", g)])
+    yield ("commit", bars["dp_full"], g)
+    if bars["v_empty"] is not None:
+        yield ("commit", bars["v_empty"][g % vstages], g)
+
+
+def _dq_wait_or_poll(bar, parity):
+    ok = yield ("poll", bar, parity)
+    if not ok:
+        yield ("wait", bar, parity)
+
+
+def _dq_issuer_item(it, g0, nk, st, bars, kstages, vstages, ds_buffers=2, test_s_free=True):
+    """The dq issuer's work item: S_0 and dP_0, then per key block j (global
+    index g) S_{j+1}, dP_{j+1}, dQ_j.  Between dQ_j's MMAs the issuing lane
+    tests (polls) whether every warp has read S_{j+1} and block j + 2's K / V
+    tiles have landed, and if so issues S_{j+2} at once, then dP_{j+2} if dP_{j+1}
+    has been read too; the next iteration waits only for what was not issued.
+    ds_buffers, test_s_free: planted mistakes for the model's own tests."""
+    k_full = bars["k_full"]
+    if k_full is not None:
+        yield ("wait", k_full[g0 % kstages], (g0 // kstages) & 1)
+    yield from _dq_issue_s(g0, bars)
+    yield from _dq_issue_dp(g0, bars, vstages)
+    pre_s = pre_dp = False
+    ds = bars["ds"]
+    for j in range(nk):
+        g, more = g0 + j, j + 1 < nk
+        if not pre_s:
+            yield ("wait", bars["s_free"], st["sf"] & 1)
+            st["sf"] += 1
+            if more:
+                if k_full is not None:
+                    yield ("wait", k_full[(g + 1) % kstages], ((g + 1) // kstages) & 1)
+                yield from _dq_issue_s(g + 1, bars)
+        if not pre_dp:
+            yield from _dq_wait_or_poll(bars["dp_free"], st["df"] & 1)
+            st["df"] += 1
+            if more:
+                yield from _dq_issue_dp(g + 1, bars, vstages)
+        if len(ds) == 2:
+            yield from _dq_wait_or_poll(ds[st["ds"] & 1], (st["ds"] >> 1) & 1)
+        else:
+            yield from _dq_wait_or_poll(ds[0], st["ds"] & 1)
+        st["ds"] += 1
+        if j == 0:
+            yield ("wait", bars["acc_free"], (st["af"] & 1) ^ 1)
+            st["af"] += 1
+        dq = ("mma", [(("dS", j % ds_buffers), g)], [])  # dQ += dS_j K_j, in two parts
+        yield dq
+        go_s = False
+        if j + 2 < nk:
+            go_s = (yield ("poll", bars["s_free"], st["sf"] & 1)) if test_s_free else True
+            if go_s and k_full is not None:
+                gn = g + 2
+                go_s = yield ("poll", k_full[gn % kstages], (gn // kstages) & 1)
+        yield dq
+        if bars["k_empty"] is not None:
+            yield ("commit", bars["k_empty"][g % kstages], g)
+        pre_s = pre_dp = False
+        if go_s:
+            yield from _dq_issue_s(g + 2, bars)
+            pre_s = True
+            if (yield ("poll", bars["dp_free"], st["df"] & 1)):
+                yield from _dq_issue_dp(g + 2, bars, vstages)
+                pre_dp = True
+        st["sf"] += pre_s
+        st["df"] += pre_dp
+    yield ("commit", bars["acc_done"], it)
+
+
+def _dq_warp(items, rng, bars, ds_buffers=2):
+    c = {"s": 0, "dp": 0, "ad": 0}
+    ds = bars["ds"]
+    step = 0
+    for it, nk in enumerate(items):
+        for j in range(nk):
+            yield ("wait", bars["s_full"], c["s"] & 1)
+            c["s"] += 1
+            yield ("read", "S", step)
+            yield ("arrive", bars["s_free"], step)
+            yield ("work",)  # the exponentials
+            yield ("wait", bars["dp_full"], c["dp"] & 1)
+            c["dp"] += 1
+            yield ("read", "dP", step)
+            yield ("arrive", bars["dp_free"], step)
+            for _ in range(rng.randint(1, 6)):
+                yield ("work",)
+            yield ("write", ("dS", j % ds_buffers), step)
+            yield ("arrive", ds[step & 1] if len(ds) == 2 else ds[0], step)
+            step += 1
+        yield ("wait", bars["acc_done"], c["ad"] & 1)
+        c["ad"] += 1
+        yield ("work",)
+        yield ("arrive", bars["acc_free"], it)
+
+
+def _dq_bars(n_warps, split_ds=True):
+    return {
+        "s_full": Barrier("s_full", 1), "s_free": Barrier("s_free", n_warps),
+        "dp_full": Barrier("dp_full", 1), "dp_free": Barrier("dp_free", n_warps),
+        "ds": [Barrier("ds_ready[0]", n_warps), Barrier("ds_ready[1]", n_warps)] if split_ds
+        else [Barrier("ds_ready", n_warps)],
+        "acc_done": Barrier("acc_done", 1), "acc_free": Barrier("acc_free", n_warps),
+        "k_full": None, "k_empty": None, "v_empty": None,
+    }
+
+
+def dq_protocol(items, rng, n_warps=8, split_ds=True, ds_buffers=2, test_s_free=True):
+    """dq kernel: per key block S and dP into TMEM, each committed on its own
+    barrier (s_full, dp_full); the elementwise warps read S (s_free), then dP
+    (dp_free), form dS into one of two TMEM buffers (ds_ready); the issuer's
+    order is S_{j+1}, dP_{j+1}, dQ_j, with S_{j+2} / dP_{j+2} issued early when
+    polls find them free (see _dq_issuer_item).  split_ds False models the
+    earlier single dS-ready barrier, whose lapping race the model must find;
+    ds_buffers=1 and test_s_free=False plant mistakes the TMEM checks must catch."""
     tc = TensorCore()
-    sp_full, sp_free = Barrier("sp_full", 1), Barrier("sp_free", n_warps)
-    ds = [Barrier("ds_ready[0]", n_warps), Barrier("ds_ready[1]", n_warps)] if split_ds \
-        else [Barrier("ds_ready", n_warps)]
-    acc_done, acc_free = Barrier("acc_done", 1), Barrier("acc_free", n_warps)
+    bars = _dq_bars(n_warps, split_ds)
+    st = {"sf": 0, "df": 0, "ds": 0, "af": 0}
 
     def issuer():
-        spf = dsc = af = 0
-        blk = 0
+        g = 0
         for it, nk in enumerate(items):
-            yield ("mma",)
-            yield ("mma",)
-            yield ("commit", sp_full, blk)
-            for j in range(nk):
-                yield ("wait", sp_free, spf & 1)
-                spf += 1
-                if j + 1 < nk:
-                    yield ("mma",)
-                    yield ("mma",)
-                    yield ("commit", sp_full, blk + j + 1)
-                if split_ds:
-                    yield ("wait", ds[dsc & 1], (dsc >> 1) & 1)
-                else:
-                    yield ("wait", ds[0], dsc & 1)
-                dsc += 1
-                if j == 0:
-                    yield ("wait", acc_free, (af & 1) ^ 1)
-                    af += 1
-                yield ("mma",)  # dQ += dS K
-            yield ("commit", acc_done, it)
-            blk += nk
-
-    def warp():
-        sp = ad = step = 0
-        for it, nk in enumerate(items):
-            for _ in range(nk):
-                yield ("wait", sp_full, sp & 1)
-                sp += 1
-                yield ("work",)
-                yield ("arrive", sp_free, step)
-                for _ in range(rng.randint(1, 6)):
-                    yield ("work",)
-                yield ("arrive", ds[step & 1] if split_ds else ds[0], step)
-                step += 1
-            yield ("wait", acc_done, ad & 1)
-            ad += 1
-            yield ("work",)
-            yield ("arrive", acc_free, it)
+            yield from _dq_issuer_item(it, g, nk, st, bars, 1, 1, ds_buffers, test_s_free)
+            g += nk
 
     roles = {"issuer": issuer()}
-    roles.update({f"warp{w}": warp() for w in range(n_warps)})
+    roles.update({f"warp{w}": _dq_warp(items, rng, bars, ds_buffers) for w in range(n_warps)})
     return roles, tc
 
 
@@ -516,15 +622,15 @@ def fwd_loads_protocol(items, rng, warps_per_tile=4, kstages=2, vstages=3):
 def dq_loads_protocol(items, rng, n_warps=8, kstages=3, vstages=2):
     """The dq kernel with its producer: Q and dO per item (q_full / q_empty),
     each key block's K and V on the K slot's full barrier; V is released after
-    S / dP, K after dQ; dS-ready alternates between two barriers."""
+    dP, K after dQ; the issuer as in dq_protocol, its early S / dP issue also
+    conditional on the K / V tiles having landed."""
     tc = TensorCore()
     q_full, q_empty = Barrier("q_full", 1), Barrier("q_empty", 1)
-    k_full = [Barrier(f"k_full[{s}]", 1) for s in range(kstages)]
-    k_empty = [Barrier(f"k_empty[{s}]", 1) for s in range(kstages)]
-    v_empty = [Barrier(f"v_empty[{s}]", 1) for s in range(vstages)]
-    sp_full, sp_free = Barrier("sp_full", 1), Barrier("sp_free", n_warps)
-    ds = [Barrier("ds_ready[0]", n_warps), Barrier("ds_ready[1]", n_warps)]
-    acc_done, acc_free = Barrier("acc_done", 1), Barrier("acc_free", n_warps)
+    bars = _dq_bars(n_warps)
+    bars["k_full"] = [Barrier(f"k_full[{s}]", 1) for s in range(kstages)]
+    bars["k_empty"] = [Barrier(f"k_empty[{s}]", 1) for s in range(kstages)]
+    bars["v_empty"] = [Barrier(f"v_empty[{s}]", 1) for s in range(vstages)]
+    st = {"sf": 0, "df": 0, "ds": 0, "af": 0}
 
     def producer():
         qu = kn = 0
@@ -533,62 +639,22 @@ def dq_loads_protocol(items, rng, n_warps=8, kstages=3, vstages=2):
             qu += 1
             yield ("arrive_tx", q_full, it, 2)
             for _ in range(nk):
-                yield ("wait", k_empty[kn % kstages], ((kn // kstages) & 1) ^ 1)
-                yield ("wait", v_empty[kn % vstages], ((kn // vstages) & 1) ^ 1)
-                yield ("arrive_tx", k_full[kn % kstages], kn, 2)
+                yield ("wait", bars["k_empty"][kn % kstages], ((kn // kstages) & 1) ^ 1)
+                yield ("wait", bars["v_empty"][kn % vstages], ((kn // vstages) & 1) ^ 1)
+                yield ("arrive_tx", bars["k_full"][kn % kstages], kn, 2)
                 kn += 1
 
     def issuer():
-        qc = spf = dsc = af = kn = 0
+        qc = g = 0
         for it, nk in enumerate(items):
             yield ("wait", q_full, qc & 1)
             qc += 1
-            g = kn
-            yield ("wait", k_full[g % kstages], (g // kstages) & 1)
-            kn += 1
-            yield ("mma",)
-            yield ("mma",)
-            yield ("commit", sp_full, g)
-            yield ("commit", v_empty[g % vstages], g)
-            for j in range(nk):
-                yield ("wait", sp_free, spf & 1)
-                spf += 1
-                if j + 1 < nk:
-                    yield ("wait", k_full[(g + j + 1) % kstages], ((g + j + 1) // kstages) & 1)
-                    kn += 1
-                    yield ("mma",)
-                    yield ("mma",)
-                    yield ("commit", sp_full, g + j + 1)
-                    yield ("commit", v_empty[(g + j + 1) % vstages], g + j + 1)
-                yield ("wait", ds[dsc & 1], (dsc >> 1) & 1)
-                dsc += 1
-                if j == 0:
-                    yield ("wait", acc_free, (af & 1) ^ 1)
-                    af += 1
-                yield ("mma",)  # dQ reads K_j
-                yield ("commit", k_empty[(g + j) % kstages], g + j)
-            yield ("commit", acc_done, it)
+            yield from _dq_issuer_item(it, g, nk, st, bars, kstages, vstages)
             yield ("commit", q_empty, it)
-
-    def warp():
-        sp = ad = step = 0
-        for it, nk in enumerate(items):
-            for _ in range(nk):
-                yield ("wait", sp_full, sp & 1)
-                sp += 1
-                yield ("work",)
-                yield ("arrive", sp_free, step)
-                for _ in range(rng.randint(1, 6)):
-                    yield ("work",)
-                yield ("arrive", ds[step & 1], step)
-                step += 1
-            yield ("wait", acc_done, ad & 1)
-            ad += 1
-            yield ("work",)
-            yield ("arrive", acc_free, it)
+            g += nk
 
     roles = {"producer": producer(), "issuer": issuer()}
-    roles.update({f"warp{w}": warp() for w in range(n_warps)})
+    roles.update({f"warp{w}": _dq_warp(items, rng, bars) for w in range(n_warps)})
     return roles, tc
 
 

@@ -1,7 +1,8 @@
 """The tensor-core kernels' mbarrier protocols, checked on the CPU with a
 randomized model (tests/barrier_model.py): random interleavings and random
 per-warp speeds, asserting that no barrier phase completes with arrivals for
-two different blocks and that no run deadlocks.  The model also has to find
+two different blocks, that no tensor-memory buffer is overwritten before it is
+read (where a protocol names its buffers) and that no run deadlocks.  The model also has to find
 the lapping race of the dq kernel's earlier single dS-ready barrier, which
 shows that it can see this class of bug."""
 import random
@@ -17,6 +18,16 @@ def test_the_model_finds_the_single_ds_barrier_race():
     found = bm.explore(bm.dq_protocol, trials=500, seed=12, split_ds=False)
     assert found is not None
     assert any(v.startswith("ds_ready phase") for v in found["violations"])
+
+
+def test_the_model_finds_tmem_buffers_overwritten_before_they_are_read():
+    """Planted in the model: S_{j+2} issued early without testing that every
+    warp has read S_{j+1}, and one dS buffer where dQ_j runs after dS_{j+1} is
+    written."""
+    found = bm.explore(bm.dq_protocol, trials=500, seed=16, test_s_free=False)
+    assert found is not None and any(" read S holding " in v for v in found["violations"])
+    found = bm.explore(bm.dq_protocol, trials=500, seed=17, ds_buffers=1)
+    assert found is not None and any("mma read ('dS', 0) holding" in v for v in found["violations"])
 
 
 def test_forward_protocol():
