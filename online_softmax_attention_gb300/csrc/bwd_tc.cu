@@ -93,6 +93,8 @@ constexpr long long kDrainCycles = 1ll << 31;  // post-abort wait for TMA loads 
 // workload from 2.70 to 2.48 ms (one in eight: 2.58, three in eight: 2.52, one
 // in two: 2.56).  The dK/dV kernel got slower with it and keeps the SFU only.
 constexpr int kDqExpFmaEvery = 4;
+// test_wait polls of the issuing lane on a barrier due within a few hundred cycles
+constexpr int kIssuerSpin = 32;
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long long budget) {
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
@@ -278,9 +280,10 @@ __device__ void dkdv_mma(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, uint32
     // S^T with a negative scale: negate K (the A operand) so P uses |scale|
     const uint32_t idST = idSS | (p.scale_log2 < 0.f ? (1u << 13) : 0u);
     constexpr uint32_t idTS = idesc_f16(kBF16, BT, D, 1);
-    uint32_t kv_cnt = 0, p_cnt = 0, ds_cnt = 0, af_cnt = 0;
-    RingPos<C::kDkdvQStages> qr;
-    RingPos<C::kDkdvDoStages> dr;
+    // Q and dO of a query block share a ring position (one full barrier)
+    static_assert(C::kDkdvQStages == C::kDkdvDoStages, "Q and dO rings advance together");
+    constexpr uint32_t QS = C::kDkdvQStages;
+    uint32_t kv_cnt = 0, af_cnt = 0;
 
     // Descriptors built once; per MMA a constant is added to the start address.
     const uint64_t kmaj = sdesc_sw128(0, 16, 1024);            // K-major, base address 0
@@ -308,6 +311,22 @@ __device__ void dkdv_mma(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, uint32
         return __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar), parity, wd));
     };
 
+    // the leader's copy of a value, for the whole warp
+    auto from_leader = [](uint32_t v, bool lead) {
+        return __shfl_sync(0xffffffffu, v, __ffs(__ballot_sync(0xffffffffu, lead)) - 1);
+    };
+    // a short bounded spin of the issuing lane on a phase that is due any moment
+    auto due = [](uint64_t &bar, uint32_t parity) -> bool {
+        for (int k = 0; k < kIssuerSpin; ++k)
+            if (mbar_test_wait(smem_u32(&bar), parity)) return true;
+        return false;
+    };
+    // query blocks taken before this item: block b of the item uses Q / dO ring
+    // position q0 + b and is phase q0 + b of p_ready and ds_ready
+    uint32_t q0 = 0;
+    auto qslot = [&](int b) { return (q0 + b) % QS; };
+    auto qphase = [&](int b) { return ((q0 + b) / QS) & 1; };
+
     for (int i = 0;; ++i) {
         int w;
         if (!sched_take_warp(bars.sched, i, w, wd)) return;
@@ -316,65 +335,71 @@ __device__ void dkdv_mma(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, uint32
         if (f.nq == 0) continue;
         if (!wait(bars.kv_full, kv_cnt & 1)) return;
         ++kv_cnt;
-        uint32_t qs = qr.slot(), os = dr.slot();
-        if (!wait(bars.q_full[qs], qr.phase())) return;  // Q and dO of the block
-        ++qr.i;
-        ++dr.i;
+        if (!wait(bars.q_full[qslot(0)], qphase(0))) return;  // Q and dO of the block
         tc_fence_after();
         if (elect_one()) {
-            issue_ss(0, sK, sQ + qs * C::kTileBytes, idST);  // S^T = K Q^T
+            issue_ss(0, sK, sQ + qslot(0) * C::kTileBytes, idST);  // S^T = K Q^T
             tc_commit(smem_u32(&bars.st_full));
-            issue_ss(BT, sV, sDO + os * C::kTileBytes, idSS);  // dP^T = V dO^T
+            issue_ss(BT, sV, sDO + qslot(0) * C::kTileBytes, idSS);  // dP^T = V dO^T
             tc_commit(smem_u32(&bars.dp_full));
         }
         __syncwarp();
-        for (int qb = 0; qb < f.nq; ++qb) {
-            if (!wait(bars.p_ready, p_cnt & 1)) return;
-            ++p_cnt;
-            if (qb == 0) {
-                if (!wait(bars.acc_free, (af_cnt & 1) ^ 1)) return;
-                ++af_cnt;
+        // Per query block qb three issue steps, each behind one barrier:
+        //   0: dV += P^T dO           after P^T_qb is in TMEM (p_ready)
+        //   1: S^T of block qb + 1    after its Q / dO tiles landed (q_full)
+        //   2: dK += dS^T Q, then dP^T of block qb + 1   after dS^T_qb is in TMEM (ds_ready)
+        // The elected lane runs the steps back to back, testing each step's
+        // barrier (a short spin) while the MMAs before it are still queued, so
+        // the tensor pipe does not wait for the warp's own turnaround; only
+        // when a barrier is not yet complete does the whole warp wait for it
+        // (bounded) and the lane resume from there.
+        int qb = 0, step = 0;
+        while (qb < f.nq) {
+            bool ok;
+            if (step == 0) {
+                ok = wait(bars.p_ready, (q0 + qb) & 1);
+                if (ok && qb == 0) ok = wait(bars.acc_free, (af_cnt & 1) ^ 1);
+            } else if (step == 1) {
+                ok = wait(bars.q_full[qslot(qb + 1)], qphase(qb + 1));
+            } else {
+                ok = wait(bars.ds_ready, (q0 + qb) & 1);
             }
-            tc_fence_after();
-            if (elect_one()) {
-                issue_ts(256, 0, sDO + os * C::kTileBytes, qb > 0);  // dV += P^T dO
-                tc_commit(smem_u32(&bars.do_empty[os]));
-            }
-            __syncwarp();
-            const bool next = qb + 1 < f.nq;
-            uint32_t qsn = 0, osn = 0;
-            if (next) {
-                qsn = qr.slot();
-                if (!wait(bars.q_full[qsn], qr.phase())) return;
-                ++qr.i;
-                tc_fence_after();
-                if (elect_one()) {
-                    issue_ss(0, sK, sQ + qsn * C::kTileBytes, idST);  // S^T of the next block
-                    tc_commit(smem_u32(&bars.st_full));
+            if (!ok) return;
+            const bool lead = elect_one();
+            if (lead) {
+                for (;;) {
+                    tc_fence_after();
+                    if (step == 0) {
+                        issue_ts(256, 0, sDO + qslot(qb) * C::kTileBytes, qb > 0);  // dV += P^T dO
+                        tc_commit(smem_u32(&bars.do_empty[qslot(qb)]));
+                        step = qb + 1 < f.nq ? 1 : 2;
+                    } else if (step == 1) {
+                        issue_ss(0, sK, sQ + qslot(qb + 1) * C::kTileBytes, idST);  // S^T of the next block
+                        tc_commit(smem_u32(&bars.st_full));
+                        step = 2;
+                    } else {
+                        issue_ts(256 + D, BT, sQ + qslot(qb) * C::kTileBytes, qb > 0);  // dK += dS^T Q
+                        tc_commit(smem_u32(&bars.q_empty[qslot(qb)]));
+                        if (qb + 1 < f.nq) {
+                            issue_ss(BT, sV, sDO + qslot(qb + 1) * C::kTileBytes, idSS);  // dP^T of the next block
+                            tc_commit(smem_u32(&bars.dp_full));
+                        }
+                        ++qb;
+                        step = 0;
+                    }
+                    if (qb == f.nq) break;
+                    const bool ready = step == 0   ? due(bars.p_ready, (q0 + qb) & 1)
+                                       : step == 1 ? due(bars.q_full[qslot(qb + 1)], qphase(qb + 1))
+                                                   : due(bars.ds_ready, (q0 + qb) & 1);
+                    if (!ready) break;
                 }
-                __syncwarp();
             }
-            if (!wait(bars.ds_ready, ds_cnt & 1)) return;
-            ++ds_cnt;
-            tc_fence_after();
-            if (next) {
-                osn = dr.slot();  // dO landed with its Q (q_full, waited above)
-                ++dr.i;
-            }
-            if (elect_one()) {
-                issue_ts(256 + D, BT, sQ + qs * C::kTileBytes, qb > 0);  // dK += dS^T Q
-                tc_commit(smem_u32(&bars.q_empty[qs]));
-                if (next) {
-                    issue_ss(BT, sV, sDO + osn * C::kTileBytes, idSS);  // dP^T of the next block
-                    tc_commit(smem_u32(&bars.dp_full));
-                }
-            }
-            __syncwarp();
-            if (next) {
-                qs = qsn;
-                os = osn;
-            }
+            const uint32_t st = from_leader((uint32_t)qb | ((uint32_t)step << 16), lead);
+            qb = (int)(st & 0xFFFFu);
+            step = (int)(st >> 16);
         }
+        ++af_cnt;
+        q0 += f.nq;
         if (elect_one()) {
             tc_commit(smem_u32(&bars.acc_done));
             tc_commit(smem_u32(&bars.kv_empty));
@@ -1002,8 +1027,10 @@ __device__ void dq_mma(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint32_t s
     // S with a negative scale: negate Q (the A operand) so P uses |scale|
     const uint32_t idS = idSS | (p.scale_log2 < 0.f ? (1u << 13) : 0u);
     constexpr uint32_t idTS = idesc_f16(kBF16, BT, D, 1);
-    uint32_t q_cnt = 0, sf_cnt = 0, df_cnt = 0, ds_cnt = 0, af_cnt = 0;
-    uint32_t g0 = 0;  // key blocks (K and V tiles) taken before this item; block g uses slots g % KS, g % VS
+    uint32_t q_cnt = 0, af_cnt = 0;
+    // key blocks taken before this item: block g uses K / V slots g % KS, g % VS,
+    // and is the g-th phase of s_free, dp_free and (alternating) ds_ready
+    uint32_t g0 = 0;
 
     const uint64_t kmaj = sdesc_sw128(0, 16, 1024);
     const uint64_t nmaj = sdesc_sw128(0, C::kBoxBytes, 1024);
@@ -1017,30 +1044,17 @@ __device__ void dq_mma(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint32_t s
             mma_ss(tmem + col, sdesc_add(ad, off), sdesc_add(bd, off), id, kk > 0);
         }
     };
-    // S = Q K^T and dP = dO V^T of global key block g, each with its commit
-    auto issue_s = [&](uint32_t g) {
-        if (elect_one()) {
-            issue_ss(0, dq_desc, sK + (g % KS) * C::kTileBytes, idS);
-            tc_commit(smem_u32(&bars.s_full));
-        }
-        __syncwarp();
-    };
-    auto issue_dp = [&](uint32_t g) {
-        if (elect_one()) {
-            issue_ss(BT, ddo_desc, sV + (g % VS) * C::kTileBytes, idSS);
-            tc_commit(smem_u32(&bars.dp_full));
-            tc_commit(smem_u32(&bars.v_empty[g % VS]));
-        }
-        __syncwarp();
-    };
-    // the whole warp waits (or polls: mbarrier.test_wait, no suspension); a
-    // barrier's phase that a poll saw complete stays complete until the issuer
-    // itself lets the next phase start, so a successful poll replaces the wait
     auto wait = [&](uint64_t &bar, uint32_t parity) -> bool {
         return __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar), parity, wd));
     };
-    auto poll = [&](uint64_t &bar, uint32_t parity) -> bool {
-        return __all_sync(0xffffffffu, mbar_test_wait(smem_u32(&bar), parity));
+    auto from_leader = [](uint32_t v, bool lead) {
+        return __shfl_sync(0xffffffffu, v, __ffs(__ballot_sync(0xffffffffu, lead)) - 1);
+    };
+    // a short bounded spin of the issuing lane on a phase that is due any moment
+    auto due = [](uint64_t &bar, uint32_t parity) -> bool {
+        for (int k = 0; k < kIssuerSpin; ++k)
+            if (mbar_test_wait(smem_u32(&bar), parity)) return true;
+        return false;
     };
 
     for (int i = 0;; ++i) {
@@ -1053,80 +1067,73 @@ __device__ void dq_mma(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint32_t s
         ++q_cnt;
         if (!wait(bars.k_full[g0 % KS], (g0 / KS) & 1)) return;
         tc_fence_after();
-        issue_s(g0);
-        issue_dp(g0);
-        // Issue order S_{j+1}, dP_{j+1}, dQ_j.  Every warp has read S_{j+1}
-        // (and usually dP_{j+1} too) well before dQ_j is issued, so the elected
-        // lane tests those barriers between dQ_j's MMAs and, when they hold,
-        // issues S_{j+2} and dP_{j+2} in the same straight run: the tensor pipe
-        // then meets one issuer turnaround per block instead of three.  When a
-        // test fails, the warp waits at the top of the next iteration.
-        bool pre_s = false, pre_dp = false;  // S_{j+1} / dP_{j+1} already issued
-        for (int j = 0; j < f.nk; ++j) {
-            const uint32_t g = g0 + j;
-            const bool more = j + 1 < f.nk;
-            if (!pre_s) {
-                if (!wait(bars.s_free, sf_cnt & 1)) return;  // every warp has read S_j
-                ++sf_cnt;
-                if (more) {
-                    if (!wait(bars.k_full[(g + 1) % KS], ((g + 1) / KS) & 1)) return;
-                    tc_fence_after();
-                    issue_s(g + 1);
-                }
-            }
-            if (!pre_dp) {
-                if (!poll(bars.dp_free, df_cnt & 1) && !wait(bars.dp_free, df_cnt & 1)) return;  // dP_j read
-                ++df_cnt;
-                if (more) {
-                    tc_fence_after();
-                    issue_dp(g + 1);
-                }
-            }
-            if (!poll(bars.ds_ready[ds_cnt & 1], (ds_cnt >> 1) & 1) &&
-                !wait(bars.ds_ready[ds_cnt & 1], (ds_cnt >> 1) & 1))
-                return;
-            ++ds_cnt;
-            if (j == 0) {
-                if (!wait(bars.acc_free, (af_cnt & 1) ^ 1)) return;
-                ++af_cnt;
-            }
-            const bool ahead = j + 2 < f.nk;
-            const uint32_t gn = g + 2;
-            uint32_t issued = 0;  // 1: S_{j+2}; 3: S_{j+2} and dP_{j+2}
-            tc_fence_after();
-            if (elect_one()) {
-                const uint64_t kd = nmaj + sdesc_step(sK + (g % KS) * C::kTileBytes);
-                const uint32_t ds_col = tmem + 256 + 64 * (j & 1);
-                // dQ += dS K: five MMAs, the tests for block j + 2, three more
-#pragma unroll
-                for (int kk = 0; kk < 5; ++kk)
-                    mma_ts(tmem + 384, ds_col + 8 * kk, sdesc_add(kd, kk * 2048), idTS, j > 0 || kk > 0);
-                const bool go_s = ahead && mbar_test_wait(smem_u32(&bars.s_free), sf_cnt & 1) &&
-                                  mbar_test_wait(smem_u32(&bars.k_full[gn % KS]), (gn / KS) & 1);
-#pragma unroll
-                for (int kk = 5; kk < BT / 16; ++kk)
-                    mma_ts(tmem + 384, ds_col + 8 * kk, sdesc_add(kd, kk * 2048), idTS, 1);
-                tc_commit(smem_u32(&bars.k_empty[g % KS]));
-                if (go_s) {
-                    tc_fence_after();
-                    issue_ss(0, dq_desc, sK + (gn % KS) * C::kTileBytes, idS);
-                    tc_commit(smem_u32(&bars.s_full));
-                    issued = 1;
-                    if (mbar_test_wait(smem_u32(&bars.dp_free), df_cnt & 1)) {
-                        tc_fence_after();
-                        issue_ss(BT, ddo_desc, sV + (gn % VS) * C::kTileBytes, idSS);
-                        tc_commit(smem_u32(&bars.dp_full));
-                        tc_commit(smem_u32(&bars.v_empty[gn % VS]));
-                        issued = 3;
-                    }
-                }
-            }
-            issued = __reduce_or_sync(0xffffffffu, issued);
-            pre_s = issued & 1;
-            pre_dp = issued & 2;
-            sf_cnt += pre_s;
-            df_cnt += pre_dp;
+        if (elect_one()) {
+            issue_ss(0, dq_desc, sK + (g0 % KS) * C::kTileBytes, idS);  // S = Q K^T
+            tc_commit(smem_u32(&bars.s_full));
+            issue_ss(BT, ddo_desc, sV + (g0 % VS) * C::kTileBytes, idSS);  // dP = dO V^T
+            tc_commit(smem_u32(&bars.dp_full));
+            tc_commit(smem_u32(&bars.v_empty[g0 % VS]));
         }
+        __syncwarp();
+        // Per key block j (global g = g0 + j) three issue steps, each behind its barriers:
+        //   0: S of block j + 1     after every warp has read S_j (s_free) and K / V of j + 1 landed
+        //   1: dP of block j + 1    after every warp has read dP_j (dp_free)
+        //   2: dQ += dS_j K_j       after dS_j is in TMEM (ds_ready; at j = 0 also acc_free)
+        // (steps 0 and 1 of the last block issue nothing but still take their
+        // barrier, so that the next item's S and dP overwrite only what was read).
+        // The elected lane runs the steps back to back, testing each step's
+        // barriers (a short spin) while the MMAs before it are still queued;
+        // only when one is not yet complete does the whole warp wait for it
+        // (bounded) and the lane resume from there.
+        auto ready = [&](int j, int step, bool spin) -> bool {
+            const uint32_t g = g0 + j;
+            auto chk = [&](uint64_t &bar, uint32_t parity) { return spin ? due(bar, parity) : wait(bar, parity); };
+            if (step == 0)
+                return chk(bars.s_free, g & 1) &&
+                       (j + 1 >= f.nk || chk(bars.k_full[(g + 1) % KS], ((g + 1) / KS) & 1));
+            if (step == 1) return chk(bars.dp_free, g & 1);
+            return chk(bars.ds_ready[g & 1], (g >> 1) & 1) && (j != 0 || chk(bars.acc_free, (af_cnt & 1) ^ 1));
+        };
+        int j = 0, step = 0;
+        while (j < f.nk) {
+            if (!ready(j, step, false)) return;
+            const bool lead = elect_one();
+            if (lead) {
+                for (;;) {
+                    const uint32_t g = g0 + j;
+                    const bool more = j + 1 < f.nk;
+                    tc_fence_after();
+                    if (step == 0) {
+                        if (more) {
+                            issue_ss(0, dq_desc, sK + ((g + 1) % KS) * C::kTileBytes, idS);
+                            tc_commit(smem_u32(&bars.s_full));
+                        }
+                        step = 1;
+                    } else if (step == 1) {
+                        if (more) {
+                            issue_ss(BT, ddo_desc, sV + ((g + 1) % VS) * C::kTileBytes, idSS);
+                            tc_commit(smem_u32(&bars.dp_full));
+                            tc_commit(smem_u32(&bars.v_empty[(g + 1) % VS]));
+                        }
+                        step = 2;
+                    } else {
+                        const uint64_t kd = nmaj + sdesc_step(sK + (g % KS) * C::kTileBytes);
+                        const uint32_t ds_col = tmem + 256 + 64 * (j & 1);
+#pragma unroll
+                        for (int kk = 0; kk < BT / 16; ++kk)  // dQ += dS K
+                            mma_ts(tmem + 384, ds_col + 8 * kk, sdesc_add(kd, kk * 2048), idTS, j > 0 || kk > 0);
+                        tc_commit(smem_u32(&bars.k_empty[g % KS]));
+                        ++j;
+                        step = 0;
+                    }
+                    if (j == f.nk || !ready(j, step, true)) break;
+                }
+            }
+            const uint32_t st = from_leader((uint32_t)j | ((uint32_t)step << 16), lead);
+            j = (int)(st & 0xFFFFu);
+            step = (int)(st >> 16);
+        }
+        ++af_cnt;
         g0 += f.nk;
         if (elect_one()) {
             tc_commit(smem_u32(&bars.acc_done));

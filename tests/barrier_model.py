@@ -153,68 +153,43 @@ def _dq_issue_dp(g, bars, vstages):
         yield ("commit", bars["v_empty"][g % vstages], g)
 
 
-def _dq_wait_or_poll(bar, parity):
-    ok = yield ("poll", bar, parity)
-    if not ok:
-        yield ("wait", bar, parity)
-
-
 def _dq_issuer_item(it, g0, nk, st, bars, kstages, vstages, ds_buffers=2, test_s_free=True):
     """The dq issuer's work item: S_0 and dP_0, then per key block j (global
-    index g) S_{j+1}, dP_{j+1}, dQ_j.  Between dQ_j's MMAs the issuing lane
-    tests (polls) whether every warp has read S_{j+1} and block j + 2's K / V
-    tiles have landed, and if so issues S_{j+2} at once, then dP_{j+2} if dP_{j+1}
-    has been read too; the next iteration waits only for what was not issued.
+    index g) three steps, each behind its barriers: S_{j+1} once every warp has
+    read S_j (and block j + 1's K / V landed), dP_{j+1} once dP_j has been read,
+    dQ_j once dS_j is in TMEM (and, at j = 0, the previous item's dQ was read
+    out).  The kernel's issuing lane tests these barriers with short polls and
+    the warp falls back to a bounded wait; either way a step starts only once
+    its barriers are complete, which is what is modelled.
     ds_buffers, test_s_free: planted mistakes for the model's own tests."""
     k_full = bars["k_full"]
     if k_full is not None:
         yield ("wait", k_full[g0 % kstages], (g0 // kstages) & 1)
     yield from _dq_issue_s(g0, bars)
     yield from _dq_issue_dp(g0, bars, vstages)
-    pre_s = pre_dp = False
     ds = bars["ds"]
     for j in range(nk):
         g, more = g0 + j, j + 1 < nk
-        if not pre_s:
-            yield ("wait", bars["s_free"], st["sf"] & 1)
-            st["sf"] += 1
-            if more:
-                if k_full is not None:
-                    yield ("wait", k_full[(g + 1) % kstages], ((g + 1) // kstages) & 1)
-                yield from _dq_issue_s(g + 1, bars)
-        if not pre_dp:
-            yield from _dq_wait_or_poll(bars["dp_free"], st["df"] & 1)
-            st["df"] += 1
-            if more:
-                yield from _dq_issue_dp(g + 1, bars, vstages)
+        if test_s_free:
+            yield ("wait", bars["s_free"], g & 1)
+        if more:
+            if k_full is not None:
+                yield ("wait", k_full[(g + 1) % kstages], ((g + 1) // kstages) & 1)
+            yield from _dq_issue_s(g + 1, bars)
+        yield ("wait", bars["dp_free"], g & 1)
+        if more:
+            yield from _dq_issue_dp(g + 1, bars, vstages)
         if len(ds) == 2:
-            yield from _dq_wait_or_poll(ds[st["ds"] & 1], (st["ds"] >> 1) & 1)
+            yield ("wait", ds[g & 1], (g >> 1) & 1)
         else:
-            yield from _dq_wait_or_poll(ds[0], st["ds"] & 1)
+            yield ("wait", ds[0], st["ds"] & 1)
         st["ds"] += 1
         if j == 0:
             yield ("wait", bars["acc_free"], (st["af"] & 1) ^ 1)
             st["af"] += 1
-        dq = ("mma", [(("dS", j % ds_buffers), g)], [])  # dQ += dS_j K_j, in two parts
-        yield dq
-        go_s = False
-        if j + 2 < nk:
-            go_s = (yield ("poll", bars["s_free"], st["sf"] & 1)) if test_s_free else True
-            if go_s and k_full is not None:
-                gn = g + 2
-                go_s = yield ("poll", k_full[gn % kstages], (gn // kstages) & 1)
-        yield dq
+        yield ("mma", [(("dS", j % ds_buffers), g)], [])  # dQ += dS_j K_j
         if bars["k_empty"] is not None:
             yield ("commit", bars["k_empty"][g % kstages], g)
-        pre_s = pre_dp = False
-        if go_s:
-            yield from _dq_issue_s(g + 2, bars)
-            pre_s = True
-            if (yield ("poll", bars["dp_free"], st["df"] & 1)):
-                yield from _dq_issue_dp(g + 2, bars, vstages)
-                pre_dp = True
-        st["sf"] += pre_s
-        st["df"] += pre_dp
     yield ("commit", bars["acc_done"], it)
 
 
@@ -259,13 +234,14 @@ def dq_protocol(items, rng, n_warps=8, split_ds=True, ds_buffers=2, test_s_free=
     """dq kernel: per key block S and dP into TMEM, each committed on its own
     barrier (s_full, dp_full); the elementwise warps read S (s_free), then dP
     (dp_free), form dS into one of two TMEM buffers (ds_ready); the issuer's
-    order is S_{j+1}, dP_{j+1}, dQ_j, with S_{j+2} / dP_{j+2} issued early when
-    polls find them free (see _dq_issuer_item).  split_ds False models the
-    earlier single dS-ready barrier, whose lapping race the model must find;
-    ds_buffers=1 and test_s_free=False plant mistakes the TMEM checks must catch."""
+    order is S_{j+1}, dP_{j+1}, dQ_j (see _dq_issuer_item).  split_ds False
+    models the earlier single dS-ready barrier, whose lapping race the model
+    must find; ds_buffers=1 and test_s_free=False (S_{j+1} issued without
+    waiting for every warp's read of S_j) plant mistakes the TMEM checks must
+    catch."""
     tc = TensorCore()
     bars = _dq_bars(n_warps, split_ds)
-    st = {"sf": 0, "df": 0, "ds": 0, "af": 0}
+    st = {"ds": 0, "af": 0}
 
     def issuer():
         g = 0
@@ -334,70 +310,115 @@ def fwd_protocol(items, rng, warps_per_tile=4):
     return roles, tc
 
 
-def dkdv_protocol(items, rng, n_warps=8):
+def _dkdv_regions(n_warps, what, blk):
+    """Each elementwise warp's part of the S^T (or dP^T) TMEM columns, holding
+    `what` of block blk."""
+    region = "S" if what in ("S", "P") else "D"
+    return [((region, w), (what, blk)) for w in range(n_warps)]
+
+
+def _dkdv_issuer_item(it, n, nq, st, bars, n_warps, stages=None, s_before_dv=False):
+    """The dK/dV issuer's work item (query blocks n .. n + nq - 1 in ring
+    order): S^T_0, dP^T_0, then per block qb the steps dV_qb (after P^T_qb is
+    in TMEM), S^T_{qb+1} (after its Q / dO tiles landed), dK_qb and dP^T_{qb+1}
+    (after dS^T_qb is in TMEM).  S^T_{qb+1} overwrites the P^T that dV_qb reads
+    and dP^T_{qb+1} the dS^T that dK_qb reads, so they follow those MMAs on the
+    in-order tensor pipe.  s_before_dv plants the mistake of issuing S^T_{qb+1}
+    ahead of dV_qb (once P^T_qb is complete)."""
+    q_full = bars["q_full"]
+    if q_full is not None:
+        yield ("wait", q_full[n % stages], (n // stages) & 1)
+    yield ("mma", [], _dkdv_regions(n_warps, "S", n))
+    yield ("commit", bars["st_full"], n)
+    yield ("mma", [], _dkdv_regions(n_warps, "dP", n))
+    yield ("commit", bars["dp_full"], n)
+    for qb in range(nq):
+        cur, nxt = n + qb, qb + 1 < nq
+
+        def next_s():
+            if q_full is not None:
+                yield ("wait", q_full[(cur + 1) % stages], ((cur + 1) // stages) & 1)
+            yield ("mma", [], _dkdv_regions(n_warps, "S", cur + 1))
+            yield ("commit", bars["st_full"], cur + 1)
+
+        yield ("wait", bars["p_ready"], st["pr"] & 1)
+        st["pr"] += 1
+        if qb == 0:
+            yield ("wait", bars["acc_free"], (st["af"] & 1) ^ 1)
+            st["af"] += 1
+        if s_before_dv and nxt:
+            yield from next_s()
+        yield ("mma", _dkdv_regions(n_warps, "P", cur), [])  # dV += P^T dO
+        if bars["do_empty"] is not None:
+            yield ("commit", bars["do_empty"][cur % stages], cur)
+        if nxt and not s_before_dv:
+            yield from next_s()
+        yield ("wait", bars["ds_ready"], st["dsr"] & 1)
+        st["dsr"] += 1
+        yield ("mma", _dkdv_regions(n_warps, "dS", cur), [])  # dK += dS^T Q
+        if bars["q_empty"] is not None:
+            yield ("commit", bars["q_empty"][cur % stages], cur)
+        if nxt:
+            yield ("mma", [], _dkdv_regions(n_warps, "dP", cur + 1))
+            yield ("commit", bars["dp_full"], cur + 1)
+    yield ("commit", bars["acc_done"], it)
+
+
+def _dkdv_elementwise(items, rng, w, bars, stats):
+    st = dp = ad = si = 0
+    blk = 0
+    for it, nq in enumerate(items):
+        for qb in range(nq):
+            yield ("arrive", stats[si & 1], si)
+            yield ("wait", stats[si & 1], (si >> 1) & 1)
+            si += 1
+            yield ("wait", bars["st_full"], st & 1)
+            st += 1
+            yield ("read", ("S", w), ("S", blk + qb))
+            for _ in range(rng.randint(1, 6)):
+                yield ("work",)
+            yield ("write", ("S", w), ("P", blk + qb))  # P^T over S^T
+            yield ("arrive", bars["p_ready"], blk + qb)
+            yield ("wait", bars["dp_full"], dp & 1)
+            dp += 1
+            yield ("read", ("D", w), ("dP", blk + qb))
+            for _ in range(rng.randint(1, 3)):
+                yield ("work",)
+            yield ("write", ("D", w), ("dS", blk + qb))  # dS^T over dP^T
+            yield ("arrive", bars["ds_ready"], blk + qb)
+        blk += nq
+        yield ("wait", bars["acc_done"], ad & 1)
+        ad += 1
+        yield ("work",)
+        yield ("arrive", bars["acc_free"], it)
+
+
+def _dkdv_bars(n_warps):
+    return {
+        "st_full": Barrier("st_full", 1), "dp_full": Barrier("dp_full", 1),
+        "p_ready": Barrier("p_ready", n_warps), "ds_ready": Barrier("ds_ready", n_warps),
+        "acc_done": Barrier("acc_done", 1), "acc_free": Barrier("acc_free", n_warps),
+        "q_full": None, "q_empty": None, "do_empty": None,
+    }
+
+
+def dkdv_protocol(items, rng, n_warps=8, s_before_dv=False):
     """dK/dV kernel: issue order dV_i, S^T_{i+1}, dK_i, dP^T_{i+1}; the
     elementwise warps stage each query block's statistics (double-buffered
-    stats_ready), write P^T (p_ready) and dS^T (ds_ready)."""
+    stats_ready), write P^T over S^T (p_ready) and dS^T over dP^T (ds_ready)."""
     tc = TensorCore()
-    st_full, dp_full = Barrier("st_full", 1), Barrier("dp_full", 1)
-    p_ready, ds_ready = Barrier("p_ready", n_warps), Barrier("ds_ready", n_warps)
-    acc_done, acc_free = Barrier("acc_done", 1), Barrier("acc_free", n_warps)
+    bars = _dkdv_bars(n_warps)
     stats = [Barrier("stats_ready[0]", n_warps), Barrier("stats_ready[1]", n_warps)]
+    st = {"pr": 0, "dsr": 0, "af": 0}
 
     def issuer():
-        pr = dsr = af = 0
         blk = 0
         for it, nq in enumerate(items):
-            yield ("mma",)
-            yield ("commit", st_full, blk)
-            yield ("mma",)
-            yield ("commit", dp_full, blk)
-            for qb in range(nq):
-                yield ("wait", p_ready, pr & 1)
-                pr += 1
-                if qb == 0:
-                    yield ("wait", acc_free, (af & 1) ^ 1)
-                    af += 1
-                yield ("mma",)  # dV
-                nxt = qb + 1 < nq
-                if nxt:
-                    yield ("mma",)
-                    yield ("commit", st_full, blk + qb + 1)
-                yield ("wait", ds_ready, dsr & 1)
-                dsr += 1
-                yield ("mma",)  # dK
-                if nxt:
-                    yield ("mma",)
-                    yield ("commit", dp_full, blk + qb + 1)
-            yield ("commit", acc_done, it)
+            yield from _dkdv_issuer_item(it, blk, nq, st, bars, n_warps, s_before_dv=s_before_dv)
             blk += nq
-
-    def warp():
-        st = dp = ad = si = 0
-        blk = 0
-        for it, nq in enumerate(items):
-            for qb in range(nq):
-                yield ("arrive", stats[si & 1], si)
-                yield ("wait", stats[si & 1], (si >> 1) & 1)
-                si += 1
-                yield ("wait", st_full, st & 1)
-                st += 1
-                for _ in range(rng.randint(1, 6)):
-                    yield ("work",)
-                yield ("arrive", p_ready, blk + qb)
-                yield ("wait", dp_full, dp & 1)
-                dp += 1
-                for _ in range(rng.randint(1, 3)):
-                    yield ("work",)
-                yield ("arrive", ds_ready, blk + qb)
-            blk += nq
-            yield ("wait", acc_done, ad & 1)
-            ad += 1
-            yield ("work",)
-            yield ("arrive", acc_free, it)
 
     roles = {"issuer": issuer()}
-    roles.update({f"warp{w}": warp() for w in range(n_warps)})
+    roles.update({f"warp{w}": _dkdv_elementwise(items, rng, w, bars, stats) for w in range(n_warps)})
     return roles, tc
 
 
@@ -416,30 +437,6 @@ def explore(protocol, trials, seed, **kw):
 
 # ---- protocols with their TMA producers -------------------------------------------
 
-def _dkdv_elementwise(items, rng, st_full, dp_full, p_ready, ds_ready, acc_done, acc_free, stats):
-    st = dp = ad = si = 0
-    blk = 0
-    for it, nq in enumerate(items):
-        for qb in range(nq):
-            yield ("arrive", stats[si & 1], si)
-            yield ("wait", stats[si & 1], (si >> 1) & 1)
-            si += 1
-            yield ("wait", st_full, st & 1)
-            st += 1
-            for _ in range(rng.randint(1, 6)):
-                yield ("work",)
-            yield ("arrive", p_ready, blk + qb)
-            yield ("wait", dp_full, dp & 1)
-            dp += 1
-            yield ("work",)
-            yield ("arrive", ds_ready, blk + qb)
-        blk += nq
-        yield ("wait", acc_done, ad & 1)
-        ad += 1
-        yield ("work",)
-        yield ("arrive", acc_free, it)
-
-
 def dkdv_loads_protocol(items, rng, n_warps=8, stages=2, q_full_arrivals=2):
     """The dK/dV kernel with its producers: warp 0 loads K, V (kv_full) and
     the Q ring, warp 2 the dO ring, and a block's Q and dO land on one full
@@ -447,13 +444,12 @@ def dkdv_loads_protocol(items, rng, n_warps=8, stages=2, q_full_arrivals=2):
     q_full_arrivals = 1 models forgetting the second producer's arrival."""
     tc = TensorCore()
     kv_full, kv_empty = Barrier("kv_full", 1), Barrier("kv_empty", 1)
-    q_full = [Barrier(f"q_full[{s}]", q_full_arrivals) for s in range(stages)]
-    q_empty = [Barrier(f"q_empty[{s}]", 1) for s in range(stages)]
-    do_empty = [Barrier(f"do_empty[{s}]", 1) for s in range(stages)]
-    st_full, dp_full = Barrier("st_full", 1), Barrier("dp_full", 1)
-    p_ready, ds_ready = Barrier("p_ready", n_warps), Barrier("ds_ready", n_warps)
-    acc_done, acc_free = Barrier("acc_done", 1), Barrier("acc_free", n_warps)
+    bars = _dkdv_bars(n_warps)
+    bars["q_full"] = [Barrier(f"q_full[{s}]", q_full_arrivals) for s in range(stages)]
+    bars["q_empty"] = [Barrier(f"q_empty[{s}]", 1) for s in range(stages)]
+    bars["do_empty"] = [Barrier(f"do_empty[{s}]", 1) for s in range(stages)]
     stats = [Barrier("stats_ready[0]", n_warps), Barrier("stats_ready[1]", n_warps)]
+    st = {"pr": 0, "dsr": 0, "af": 0}
 
     def q_producer():
         kvu = n = 0
@@ -462,57 +458,29 @@ def dkdv_loads_protocol(items, rng, n_warps=8, stages=2, q_full_arrivals=2):
             kvu += 1
             yield ("arrive_tx", kv_full, it, 2)
             for _ in range(nq):
-                yield ("wait", q_empty[n % stages], ((n // stages) & 1) ^ 1)
-                yield ("arrive_tx", q_full[n % stages], n, 1)
+                yield ("wait", bars["q_empty"][n % stages], ((n // stages) & 1) ^ 1)
+                yield ("arrive_tx", bars["q_full"][n % stages], n, 1)
                 n += 1
 
     def do_producer():
         n = 0
         for it, nq in enumerate(items):
             for _ in range(nq):
-                yield ("wait", do_empty[n % stages], ((n // stages) & 1) ^ 1)
-                yield ("arrive_tx", q_full[n % stages], n, 1)
+                yield ("wait", bars["do_empty"][n % stages], ((n // stages) & 1) ^ 1)
+                yield ("arrive_tx", bars["q_full"][n % stages], n, 1)
                 n += 1
 
     def issuer():
-        kvc = pr = dsr = af = n = 0
+        kvc = n = 0
         for it, nq in enumerate(items):
             yield ("wait", kv_full, kvc & 1)
             kvc += 1
-            yield ("wait", q_full[n % stages], (n // stages) & 1)
-            yield ("mma",)
-            yield ("commit", st_full, n)
-            yield ("mma",)
-            yield ("commit", dp_full, n)
-            for qb in range(nq):
-                cur = n + qb
-                yield ("wait", p_ready, pr & 1)
-                pr += 1
-                if qb == 0:
-                    yield ("wait", acc_free, (af & 1) ^ 1)
-                    af += 1
-                yield ("mma",)  # dV reads dO
-                yield ("commit", do_empty[cur % stages], cur)
-                nxt = qb + 1 < nq
-                if nxt:
-                    yield ("wait", q_full[(cur + 1) % stages], ((cur + 1) // stages) & 1)
-                    yield ("mma",)
-                    yield ("commit", st_full, cur + 1)
-                yield ("wait", ds_ready, dsr & 1)
-                dsr += 1
-                yield ("mma",)  # dK reads Q
-                yield ("commit", q_empty[cur % stages], cur)
-                if nxt:
-                    yield ("mma",)
-                    yield ("commit", dp_full, cur + 1)
-            yield ("commit", acc_done, it)
+            yield from _dkdv_issuer_item(it, n, nq, st, bars, n_warps, stages)
             yield ("commit", kv_empty, it)
             n += nq
 
     roles = {"q_producer": q_producer(), "do_producer": do_producer(), "issuer": issuer()}
-    for w in range(n_warps):
-        roles[f"warp{w}"] = _dkdv_elementwise(items, rng, st_full, dp_full, p_ready, ds_ready, acc_done,
-                                              acc_free, stats)
+    roles.update({f"warp{w}": _dkdv_elementwise(items, rng, w, bars, stats) for w in range(n_warps)})
     return roles, tc
 
 
@@ -622,15 +590,14 @@ def fwd_loads_protocol(items, rng, warps_per_tile=4, kstages=2, vstages=3):
 def dq_loads_protocol(items, rng, n_warps=8, kstages=3, vstages=2):
     """The dq kernel with its producer: Q and dO per item (q_full / q_empty),
     each key block's K and V on the K slot's full barrier; V is released after
-    dP, K after dQ; the issuer as in dq_protocol, its early S / dP issue also
-    conditional on the K / V tiles having landed."""
+    dP, K after dQ; the issuer as in dq_protocol."""
     tc = TensorCore()
     q_full, q_empty = Barrier("q_full", 1), Barrier("q_empty", 1)
     bars = _dq_bars(n_warps)
     bars["k_full"] = [Barrier(f"k_full[{s}]", 1) for s in range(kstages)]
     bars["k_empty"] = [Barrier(f"k_empty[{s}]", 1) for s in range(kstages)]
     bars["v_empty"] = [Barrier(f"v_empty[{s}]", 1) for s in range(vstages)]
-    st = {"sf": 0, "df": 0, "ds": 0, "af": 0}
+    st = {"ds": 0, "af": 0}
 
     def producer():
         qu = kn = 0

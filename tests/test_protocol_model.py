@@ -21,9 +21,8 @@ def test_the_model_finds_the_single_ds_barrier_race():
 
 
 def test_the_model_finds_tmem_buffers_overwritten_before_they_are_read():
-    """Planted in the model: S_{j+2} issued early without testing that every
-    warp has read S_{j+1}, and one dS buffer where dQ_j runs after dS_{j+1} is
-    written."""
+    """Planted in the model: S_{j+1} issued without waiting for every warp's
+    read of S_j, and one dS buffer where dQ_j runs after dS_{j+1} is written."""
     found = bm.explore(bm.dq_protocol, trials=500, seed=16, test_s_free=False)
     assert found is not None and any(" read S holding " in v for v in found["violations"])
     found = bm.explore(bm.dq_protocol, trials=500, seed=17, ds_buffers=1)
@@ -36,6 +35,13 @@ def test_forward_protocol():
 
 def test_dkdv_protocol():
     assert bm.explore(bm.dkdv_protocol, trials=500, seed=14) is None
+
+
+def test_the_model_finds_p_overwritten_before_dv_reads_it():
+    """Planted in the model: S^T of the next block issued ahead of dV, which
+    still has to read P^T from the same TMEM columns."""
+    found = bm.explore(bm.dkdv_protocol, trials=300, seed=18, s_before_dv=True)
+    assert found is not None and any(v.startswith("mma read ('S', ") for v in found["violations"])
 
 
 def test_the_model_reports_a_deadlock():
