@@ -93,8 +93,6 @@ constexpr long long kDrainCycles = 1ll << 31;  // post-abort wait for TMA loads 
 // workload from 2.70 to 2.48 ms (one in eight: 2.58, three in eight: 2.52, one
 // in two: 2.56).  The dK/dV kernel got slower with it and keeps the SFU only.
 constexpr int kDqExpFmaEvery = 4;
-// test_wait polls of the issuing lane on a barrier due within a few hundred cycles
-constexpr int kIssuerSpin = 32;
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long long budget) {
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
@@ -133,12 +131,13 @@ __device__ __forceinline__ bool sched_publish_warp(SchedRing &r, int i, int *cou
     const bool ok = mbar_wait(smem_u32(&r.empty[slot]), ((i >> 1) & 1) ^ 1, wd);
     if (!__all_sync(0xffffffffu, ok)) return false;
     int v = 0;
-    if (elect_one()) {
+    const bool lead = elect_one();
+    if (lead) {
         v = atomicAdd(counter, 1);
         r.item[slot] = v;
         mbar_arrive(smem_u32(&r.full[slot]));
     }
-    w = __shfl_sync(0xffffffffu, v, 0);
+    w = (int)from_leader((uint32_t)v, lead);
     return true;
 }
 
@@ -311,16 +310,7 @@ __device__ void dkdv_mma(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, uint32
         return __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar), parity, wd));
     };
 
-    // the leader's copy of a value, for the whole warp
-    auto from_leader = [](uint32_t v, bool lead) {
-        return __shfl_sync(0xffffffffu, v, __ffs(__ballot_sync(0xffffffffu, lead)) - 1);
-    };
-    // a short bounded spin of the issuing lane on a phase that is due any moment
-    auto due = [](uint64_t &bar, uint32_t parity) -> bool {
-        for (int k = 0; k < kIssuerSpin; ++k)
-            if (mbar_test_wait(smem_u32(&bar), parity)) return true;
-        return false;
-    };
+    auto due = [](uint64_t &bar, uint32_t parity) { return mbar_due(smem_u32(&bar), parity); };
     // query blocks taken before this item: block b of the item uses Q / dO ring
     // position q0 + b and is phase q0 + b of p_ready and ds_ready
     uint32_t q0 = 0;
@@ -1047,15 +1037,7 @@ __device__ void dq_mma(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint32_t s
     auto wait = [&](uint64_t &bar, uint32_t parity) -> bool {
         return __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar), parity, wd));
     };
-    auto from_leader = [](uint32_t v, bool lead) {
-        return __shfl_sync(0xffffffffu, v, __ffs(__ballot_sync(0xffffffffu, lead)) - 1);
-    };
-    // a short bounded spin of the issuing lane on a phase that is due any moment
-    auto due = [](uint64_t &bar, uint32_t parity) -> bool {
-        for (int k = 0; k < kIssuerSpin; ++k)
-            if (mbar_test_wait(smem_u32(&bar), parity)) return true;
-        return false;
-    };
+    auto due = [](uint64_t &bar, uint32_t parity) { return mbar_due(smem_u32(&bar), parity); };
 
     for (int i = 0;; ++i) {
         int w;

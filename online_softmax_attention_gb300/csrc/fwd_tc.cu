@@ -225,12 +225,13 @@ __device__ void producer(const TcFwdArgs &a, FwdBars &bars, int *sched_item, uin
         const int slot = i & 1;
         if (!wait(bars.sched_empty[slot], ((i >> 1) & 1) ^ 1)) break;
         int w = 0;
-        if (elect_one()) {
+        const bool lead = elect_one();
+        if (lead) {
             w = fetch_item(p.sched.hdr, p.static_items, i);
             sched_item[slot] = w;
             mbar_arrive(smem_u32(&bars.sched_full[slot]));
         }
-        w = __shfl_sync(0xffffffffu, w, 0);
+        w = (int)from_leader((uint32_t)w, lead);
         if (w >= total) break;
         const ItemInfo f = item_info(p, w);
         bool ok = true;

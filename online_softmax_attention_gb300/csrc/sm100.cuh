@@ -121,8 +121,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
     }
 }
 
-// One lane of a converged warp is elected (the lowest active one: lane 0 when
-// the whole warp runs).
+// One lane of a converged warp is elected; from_leader() gives its values to
+// the other lanes.
 __device__ __forceinline__ bool elect_one() {
     uint32_t pred = 0;
     asm volatile(
@@ -133,6 +133,22 @@ __device__ __forceinline__ bool elect_one() {
         "}\n"
         : "=r"(pred));
     return pred != 0;
+}
+
+// The value `v` of the lane for which `lead` is set, for the whole warp.
+__device__ __forceinline__ uint32_t from_leader(uint32_t v, bool lead) {
+    return __shfl_sync(0xffffffffu, v, __ffs(__ballot_sync(0xffffffffu, lead)) - 1);
+}
+
+// An MMA-issuing lane's short, bounded spin (mbarrier.test_wait, which never
+// suspends) on a phase that is due within a few hundred cycles; false if it has
+// not completed after kIssuerSpin tests, and the warp then waits for it with
+// the watchdog.
+constexpr int kIssuerSpin = 32;
+__device__ __forceinline__ bool mbar_due(uint32_t bar, uint32_t parity) {
+    for (int k = 0; k < kIssuerSpin; ++k)
+        if (mbar_test_wait(bar, parity)) return true;
+    return false;
 }
 
 // Position in a ring of N shared-memory slots guarded by full / empty
