@@ -87,12 +87,6 @@ __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 constexpr long long kDrainCycles = 1ll << 31;  // post-abort wait for TMA loads in flight
 
-// The dq kernel's elementwise warps are on its critical path (16384
-// exponentials per 128 x 128 block); computing one pair in four with
-// the FMA-pipe polynomial (exp2_fma2) took the dq stage of the causal training
-// workload from 2.70 to 2.48 ms (one in eight: 2.58, three in eight: 2.52, one
-// in two: 2.56).  The dK/dV kernel got slower with it and keeps the SFU only.
-constexpr int kDqExpFmaEvery = 4;
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long long budget) {
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
@@ -1172,9 +1166,12 @@ __device__ void dq_elementwise(const TcBwdArgs &a, DqBars &bars, uint32_t tmem, 
             for (int c = 0; c < 32; ++c) {
                 uint32_t &s0 = rs[(2 * c) >> 5][(2 * c) & 31], &s1 = rs[(2 * c + 1) >> 5][(2 * c + 1) & 31];
                 const float2 x = __ffma2_rn(make_float2(__uint_as_float(s0), __uint_as_float(s1)), sc2, nl2);
-                // one pair in kDqExpFmaEvery on the FMA pipe, the rest on the SFU
-                const float2 pv = (c % kDqExpFmaEvery) == 0 ? exp2_fma2(x)
-                                                            : make_float2(exp2_approx(x.x), exp2_approx(x.y));
+                // all on the SFU: a share of the pairs on the FMA pipe (exp2_fma2)
+                // helped while these warps bounded the kernel, but their extra
+                // instructions now cost the MMA-issuing warp of the same
+                // sub-partition more issue slots than they save (one pair in
+                // four: 2.047 ms, one in eight: 2.035, none: 2.007 on the training shape)
+                const float2 pv = make_float2(exp2_approx(x.x), exp2_approx(x.y));
                 s0 = __float_as_uint(pv.x);
                 s1 = __float_as_uint(pv.y);
             }
