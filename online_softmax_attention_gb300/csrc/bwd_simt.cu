@@ -440,9 +440,14 @@ template <typename Tin, typename To, int D>
 cudaError_t row_dot_typed(const BwdParams &p, cudaStream_t s) {
     const int64_t rows = (int64_t)p.n_q * p.H;
     if (rows == 0) return cudaSuccess;
-    // 8 warps per block, kRowDotRows rows per warp and pass; at most 8 blocks per SM
+    // 8 warps per block, kRowDotRows rows per warp and pass; at most one wave of
+    // resident blocks (a second wave would leave the first one's SMs idle at its tail)
+    static int per_sm = 0;  // resident blocks per SM of this instantiation
+    if (per_sm == 0 &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, row_dot_kernel<Tin, To, D>, 256, 0) != cudaSuccess)
+        per_sm = 1;
     const int64_t want = (rows + 8 * kRowDotRows - 1) / (8 * kRowDotRows);
-    const int64_t cap = 8LL * sm_count();
+    const int64_t cap = (int64_t)(per_sm > 0 ? per_sm : 1) * sm_count();
     const cudaError_t e = launch_pdl(row_dot_kernel<Tin, To, D>, dim3((int)(want < cap ? want : cap)), dim3(256), 0, s, p);
     count_launch();
     return e != cudaSuccess ? e : cudaGetLastError();
