@@ -378,9 +378,11 @@ __device__ void dkdv_mma(const TcBwdArgs &a, DkdvBars &bars, uint32_t sK, uint32
                     if (!ready) break;
                 }
             }
-            const uint32_t st = from_leader((uint32_t)qb | ((uint32_t)step << 16), lead);
-            qb = (int)(st & 0xFFFFu);
-            step = (int)(st >> 16);
+            // (block, step) in one word: step < 4 in the low bits, the block
+            // index (< 2^24 for 2^31 rows) above them
+            const uint32_t st = from_leader(((uint32_t)qb << 2) | (uint32_t)step, lead);
+            qb = (int)(st >> 2);
+            step = (int)(st & 3u);
         }
         ++af_cnt;
         q0 += f.nq;
@@ -1105,9 +1107,11 @@ __device__ void dq_mma(const TcBwdArgs &a, DqBars &bars, uint32_t sQ, uint32_t s
                     if (j == f.nk || !ready(j, step, true)) break;
                 }
             }
-            const uint32_t st = from_leader((uint32_t)j | ((uint32_t)step << 16), lead);
-            j = (int)(st & 0xFFFFu);
-            step = (int)(st >> 16);
+            // (block, step) in one word: step < 4 in the low bits, the block
+            // index (< 2^24 for 2^31 keys) above them
+            const uint32_t st = from_leader(((uint32_t)j << 2) | (uint32_t)step, lead);
+            j = (int)(st >> 2);
+            step = (int)(st & 3u);
         }
         ++af_cnt;
         g0 += f.nk;

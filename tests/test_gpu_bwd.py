@@ -7,7 +7,7 @@ import torch
 import attn_inputs
 import online_softmax_attention_gb300 as attn
 import oracle
-from parity_util import check_grad
+from parity_util import check_grad, check_lse, check_o
 
 pytestmark = pytest.mark.gpu
 
@@ -164,3 +164,68 @@ def test_many_short_sequences(kernel):
     lengths = np.random.default_rng(49).integers(0, 5, 20000).tolist()
     x = attn_inputs.make(dtype="fp16", H=2, D=64, seed=49, lengths=lengths, backward=True)
     _check(_fwd_bwd(x, causal=True, kernel=kernel), _ref(x, causal=True))
+
+
+
+def _rel_rms_tiled(g, ref, copies, factor=1.0):
+    """Relative RMS of g (copies x block rows) against `ref` (one block, f64)
+    times `factor`, repeated over the copies; summed on the device in chunks."""
+    r = torch.as_tensor(np.asarray(ref) * factor, dtype=torch.float32, device=DEV)
+    gv = g.reshape(copies, *r.shape)
+    num = den = 0.0
+    for c in gv.split(4096):
+        assert bool(torch.isfinite(c).all())
+        d = c.float() - r
+        num += float(torch.sum(d * d, dtype=torch.float64))
+        den += float(torch.sum(r * r, dtype=torch.float64)) * c.shape[0]
+    return (num / den) ** 0.5
+
+
+@pytest.mark.parametrize("long_side", ["keys", "queries"])
+def test_more_than_65536_blocks_in_one_item(long_side):
+    """One work item spanning more than 2^16 blocks of 128 rows: the forward's
+    and the dq kernel's key loops (long keys) or the dK/dV kernel's query loop
+    (long queries) run 65540 blocks.  One block carries the problem, the other
+    65539 contribute exactly nothing, so the answer is the single-block
+    problem's: filler keys score -100 against every query after scaling (q's
+    first component is 4, the fillers' -200, scale 1/8), so their softmax
+    weights, e^-100 below the smallest normal float, flush to 0; filler query
+    rows repeat the query block
+    with dO = 0 (their dS is 0, their O and lse repeat the block's).  Adding
+    zeros keeps the tensor core's f32 accumulators exact, so the ordinary bars
+    apply however many blocks an accumulator spans."""
+    m = 65540
+    x = attn_inputs.make(dtype="bf16", H=1, D=64, seed=91, n_q=256 if long_side == "keys" else 128,
+                         n_k=128, backward=True)
+    if long_side == "keys":
+        x["q"][:, :, 0] = 4.0
+    o_ref, lse_ref = oracle.fwd(x["q"], x["k"], x["v"], causal=False)
+    rq, rk, rv = oracle.bwd(x["q"], x["k"], x["v"], x["dO"], causal=False)
+    q, k, v, dO = (x[n].to(DEV) for n in ("q", "k", "v", "dO"))
+    if long_side == "keys":
+        filler = torch.zeros(((m - 1) * 128, 1, 64), dtype=k.dtype, device=DEV)
+        kf = filler.clone()
+        kf[:, :, 0] = -200.0
+        k, v = torch.cat([k, kf]), torch.cat([v, filler])
+    else:
+        q = q.repeat(m, 1, 1)
+        dO = torch.cat([dO, torch.zeros(((m - 1) * 128, 1, 64), dtype=dO.dtype, device=DEV)])
+    o, lse = attn.fwd(q, k, v, causal=False, out_dtype=torch.float32)
+    dq, dk, dv = attn.bwd(q, k, v, o, lse, dO, causal=False, grad_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert attn.device_status() == 0
+    if long_side == "keys":
+        check_o(o, o_ref, torch.bfloat16, o.dtype)
+        check_lse(lse, lse_ref)
+        check_grad(dq, rq, "dq")
+        check_grad(dk[:128], rk, "dk")
+        check_grad(dv[:128], rv, "dv")
+        assert float(dk[128:].abs().max()) == 0.0 and float(dv[128:].abs().max()) == 0.0
+    else:
+        assert _rel_rms_tiled(o, o_ref, m) <= 2e-3
+        lse_d = lse.reshape(1, m, 128) - torch.as_tensor(lse_ref, dtype=torch.float32, device=DEV)[:, None, :]
+        assert float(lse_d.abs().max()) <= 1e-3
+        check_grad(dq[:128], rq, "dq")
+        assert float(dq[128:].abs().max()) == 0.0
+        check_grad(dk, rk, "dk")
+        check_grad(dv, rv, "dv")
