@@ -17,7 +17,8 @@
 // Warp roles (12 warps):
 //   warp 0      TMA producer: Q tiles, then K_j, V_j tiles into a ring of
 //               shared-memory slots (128-byte swizzle, 64-column boxes).
-//   warp 1      MMA issuer (one thread): S_t = Q_t K_j^T into TMEM, and
+//   warp 1      MMA issuer (the whole warp, one elected lane issuing):
+//               S_t = Q_t K_j^T into TMEM, and
 //               U_t += P_t V_j with P_t read from TMEM (it overwrites S_t).
 //               Issue order PV_j(0), S_{j+1}(0), PV_j(1), S_{j+1}(1) keeps the
 //               tensor core busy while the other tile's softmax runs.
