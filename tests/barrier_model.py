@@ -484,11 +484,19 @@ def dkdv_loads_protocol(items, rng, n_warps=8, stages=2, q_full_arrivals=2):
     return roles, tc
 
 
-def fwd_loads_protocol(items, rng, warps_per_tile=4, kstages=2, vstages=3):
+def fwd_loads_protocol(items, rng, warps_per_tile=4, kstages=2, vstages=3, s_before_pv=False,
+                       wait_o_free=True):
     """The forward kernel with its producer: Q per tile (q_full / q_empty),
     and each key tile's K and V landing on the K slot's full barrier (two
     loads); the issuer waits once per key tile and releases K after the score
-    MMAs and V after the value MMAs.  items: (key tiles of tile 0, of tile 1)."""
+    MMAs and V after the value MMAs.  items: (key tiles of tile 0, of tile 1).
+    TMEM per softmax warp w of tile t: ("S", t, w) holds S_j, then the P_j the
+    warp writes over it, which PV_j reads; ("U", t, w) holds the value
+    accumulator after PV_j (tag j), which the warp may rescale after seeing
+    S_{j+1} and reads out after o_done.  s_before_pv and wait_o_free=False
+    plant mistakes (S_{j+1} issued ahead of the PV_j that reads P_j; the next
+    item's first PV issued before the epilogue has read U)."""
+    W = range(warps_per_tile)
     tc = TensorCore()
     q_full = [Barrier(f"q_full[{t}]", 1) for t in (0, 1)]
     q_empty = [Barrier(f"q_empty[{t}]", 1) for t in (0, 1)]
@@ -532,7 +540,7 @@ def fwd_loads_protocol(items, rng, warps_per_tile=4, kstages=2, vstages=3):
             kn += 1
             for t in (0, 1):
                 if ns[t]:
-                    yield ("mma",)
+                    yield ("mma", [], [(("S", t, w), ("S", it, 0)) for w in W])
                     yield ("commit", s_full[t], (it, 0))
                     if ns[t] == 1:
                         yield ("commit", q_empty[t], it)
@@ -546,25 +554,36 @@ def fwd_loads_protocol(items, rng, warps_per_tile=4, kstages=2, vstages=3):
                     yield ("wait", p_full[t], pc[t] & 1)
                     pc[t] += 1
                     if j == 0:
-                        yield ("wait", o_free[t], (of[t] & 1) ^ 1)
+                        if wait_o_free:
+                            yield ("wait", o_free[t], (of[t] & 1) ^ 1)
                         of[t] += 1
-                    yield ("mma",)  # PV_j(t) reads V_j
-                    if j == ns[t] - 1:
-                        yield ("commit", o_done[t], it)
-                    if j + 1 < ns[t]:
+
+                    def next_s():
+                        nonlocal have_next, kn
                         if not have_next:
                             yield ("wait", k_full[(gj + 1) % kstages], ((gj + 1) // kstages) & 1)
                             kn += 1
                             have_next = True
-                        yield ("mma",)  # S_{j+1}(t)
+                        yield ("mma", [], [(("S", t, w), ("S", it, j + 1)) for w in W])  # S_{j+1}(t)
                         yield ("commit", s_full[t], (it, j + 1))
                         if j + 1 == ns[t] - 1:
                             yield ("commit", q_empty[t], it)
+
+                    if s_before_pv and j + 1 < ns[t]:
+                        yield from next_s()
+                    # PV_j(t) reads V_j and P_j, and adds to U (which must hold j - 1)
+                    yield ("mma", [(("S", t, w), ("P", it, j)) for w in W] +
+                           ([(("U", t, w), ("U", it, j - 1)) for w in W] if j else []),
+                           [(("U", t, w), ("U", it, j)) for w in W])
+                    if j == ns[t] - 1:
+                        yield ("commit", o_done[t], it)
+                    if j + 1 < ns[t] and not s_before_pv:
+                        yield from next_s()
                 yield ("commit", v_empty[gj % vstages], gj)
                 if have_next:
                     yield ("commit", k_empty[(gj + 1) % kstages], gj + 1)
 
-    def softmax(t):
+    def softmax(t, w):
         sc = oc = 0
         for it, ns in enumerate(items):
             n = ns[t]
@@ -573,17 +592,23 @@ def fwd_loads_protocol(items, rng, warps_per_tile=4, kstages=2, vstages=3):
             for j in range(n):
                 yield ("wait", s_full[t], sc & 1)
                 sc += 1
+                yield ("read", ("S", t, w), ("S", it, j))
+                if j and rng.random() < 0.3:  # the row max grew: rescale U (PV_{j-1} is done)
+                    yield ("read", ("U", t, w), ("U", it, j - 1))
+                    yield ("write", ("U", t, w), ("U", it, j - 1))
                 for _ in range(rng.randint(1, 6)):
                     yield ("work",)
+                yield ("write", ("S", t, w), ("P", it, j))
                 yield ("arrive", p_full[t], (it, j))
             yield ("wait", o_done[t], oc & 1)
             oc += 1
+            yield ("read", ("U", t, w), ("U", it, n - 1))  # the epilogue reads U
             yield ("work",)
             yield ("arrive", o_free[t], it)
 
     roles = {"producer": producer(), "issuer": issuer()}
     for t in (0, 1):
-        roles.update({f"sm{t}.{w}": softmax(t) for w in range(warps_per_tile)})
+        roles.update({f"sm{t}.{w}": softmax(t, w) for w in W})
     return roles, tc
 
 

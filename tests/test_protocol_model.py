@@ -74,6 +74,16 @@ def test_forward_with_its_producer_shared_kv_barrier():
     assert _explore_fwd(300, 22, kstages=4, vstages=3) is None    # fp8 Q / K: K ring 4
 
 
+def test_the_model_finds_forward_tmem_overwrites():
+    """Planted: S_{j+1} issued ahead of the PV_j that reads P_j from the same
+    columns; the next item's first PV issued without waiting for the epilogue's
+    read of U."""
+    found = _explore_fwd(300, 34, s_before_pv=True)
+    assert found is not None and any(v.startswith("mma read ('S', ") for v in found[1])
+    found = _explore_fwd(300, 35, wait_o_free=False)
+    assert found is not None and any(" read ('U', " in v for v in found[1])
+
+
 def test_dkdv_with_both_producers_shared_q_do_barrier():
     assert bm.explore(bm.dkdv_loads_protocol, trials=400, seed=23) is None
     assert bm.explore(bm.dkdv_loads_protocol, trials=300, seed=24, stages=4) is None  # D = 64
