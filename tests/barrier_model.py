@@ -484,8 +484,7 @@ def dkdv_loads_protocol(items, rng, n_warps=8, stages=2, q_full_arrivals=2):
     return roles, tc
 
 
-def fwd_loads_protocol(items, rng, warps_per_tile=4, kstages=2, vstages=3, s_before_pv=False,
-                       wait_o_free=True):
+def fwd_loads_protocol(items, rng, warps_per_tile=4, kstages=2, vstages=3, s_before_pv=False):
     """The forward kernel with its producer: Q per tile (q_full / q_empty),
     and each key tile's K and V landing on the K slot's full barrier (two
     loads); the issuer waits once per key tile and releases K after the score
@@ -493,9 +492,10 @@ def fwd_loads_protocol(items, rng, warps_per_tile=4, kstages=2, vstages=3, s_bef
     TMEM per softmax warp w of tile t: ("S", t, w) holds S_j, then the P_j the
     warp writes over it, which PV_j reads; ("U", t, w) holds the value
     accumulator after PV_j (tag j), which the warp may rescale after seeing
-    S_{j+1} and reads out after o_done.  s_before_pv and wait_o_free=False
-    plant mistakes (S_{j+1} issued ahead of the PV_j that reads P_j; the next
-    item's first PV issued before the epilogue has read U)."""
+    S_{j+1} and reads out after o_done.  (The issuer's o_free wait before an
+    item's first PV is implied by that PV's p_full: each softmax warp writes the
+    item's first P only after its epilogue has read U.)  s_before_pv plants the
+    mistake of issuing S_{j+1} ahead of the PV_j that reads P_j."""
     W = range(warps_per_tile)
     tc = TensorCore()
     q_full = [Barrier(f"q_full[{t}]", 1) for t in (0, 1)]
@@ -554,8 +554,7 @@ def fwd_loads_protocol(items, rng, warps_per_tile=4, kstages=2, vstages=3, s_bef
                     yield ("wait", p_full[t], pc[t] & 1)
                     pc[t] += 1
                     if j == 0:
-                        if wait_o_free:
-                            yield ("wait", o_free[t], (of[t] & 1) ^ 1)
+                        yield ("wait", o_free[t], (of[t] & 1) ^ 1)
                         of[t] += 1
 
                     def next_s():
